@@ -1,0 +1,38 @@
+"""CPU oracle for paged single-token decode attention -- TEST INFRASTRUCTURE ONLY.
+
+This package is a plain, slow, fp64 restatement of what the paged-KV decode path
+computes. It exists so that the CUDA library can be checked against something
+obviously correct. Only the test-suite, the smoke check in ``__graft_entry__`` and
+the CPU-baseline leg of ``bench.py`` may import it; the product path (the C-ABI
+library and its Python binding) never does, and it shares no code with it.
+
+Sources (the pages the method is taken from):
+
+* "大模型工程（五）：推理优化核心技法" (chenk.top, LLM engineering part 5), sections
+  "两个特性截然不同的阶段" (decode reads the whole KV cache every step),
+  "分页注意力" (fixed 16-token blocks, per-request block table, the 47/200-token
+  worked example, at most 15 tokens wasted, prefix sharing), "块管理器：分页如何运作"
+  (free list, refcounted copy-on-write blocks), "INT8 仅权重量化" (``w_q = round(w/s)``)
+  and "KV 缓存量化" (per-token-per-head scales).
+* The gsyq.cn inference-optimisation page, section 2.1 (the KV-cache size formula and
+  its 7B example), 2.2 (block sizes 16 or 32, shared blocks) and 2.3 (per-token or
+  per-channel KV scales, softmax stability after quantisation).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against the pages'
+worked examples, closed forms, invariants and brute force; none is marked
+"parity unpinned".
+"""
+
+from .paged_attention import (  # noqa: F401
+    num_blocks_for,
+    kv_cache_bytes,
+    append_scatter,
+    quantize_rows_int8,
+    dequantize_rows_int8,
+    append_scatter_int8,
+    gather_sequence,
+    gather_sequence_int8,
+    attend_one_head,
+    decode_attention,
+    decode_attention_int8,
+)

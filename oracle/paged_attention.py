@@ -1,0 +1,230 @@
+"""fp64 CPU oracle for paged-KV append and single-token decode attention.
+
+TEST INFRASTRUCTURE: imported only by tests, the smoke check and the CPU-baseline leg
+of the benchmark. Nothing in the product library calls it.
+
+Readings of the pages that this file fixes (the pages leave them open):
+
+* Cache layout: K and V are separate arrays shaped ``[num_blocks, num_kv_heads,
+  block_size, head_dim]``. Only the addressing matters for the result, so any layout
+  read through the same indexing gives the same output.
+* Slot encoding: ``slot = physical_block * block_size + offset``; a negative slot
+  means "no token" and is skipped.
+* Grouped-query attention: query head ``h`` reads KV head ``h // g`` with
+  ``g = num_q_heads // num_kv_heads`` (consecutive grouping).
+* ``context_lens[s]`` counts every cached token the new query attends to, the token
+  appended in this step included; a sequence with 0 tokens yields a zero output.
+* INT8 KV: symmetric, one fp32 scale per (token, KV head), separately for K and V;
+  ``s = absmax / 127`` and ``q = clamp(round_half_even(x / s), -127, 127)``, both in
+  IEEE fp32; ``absmax = 0`` gives ``s = 0`` and ``q = 0``.
+
+Arithmetic is float64 throughout (inputs are converted exactly), except the INT8
+quantiser, which the pages define on the stored fp32 values.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# Paging arithmetic -- "分页注意力" section of "大模型工程（五）：推理优化核心技法"
+# (chenk.top): KV is allocated in fixed-size blocks (16 tokens by default); a
+# request of n tokens holds ceil(n / block_size) blocks and only its last block is
+# partly filled.
+# ---------------------------------------------------------------------------
+
+def num_blocks_for(num_tokens: int, block_size: int) -> int:
+    """Blocks a request of ``num_tokens`` tokens occupies (the page's 47 -> 3, 200 -> 13)."""
+    if num_tokens < 0 or block_size <= 0:
+        raise ValueError("num_tokens must be >= 0 and block_size > 0")
+    return -(-num_tokens // block_size)
+
+
+def kv_cache_bytes(batch: int, seq_len: int, num_layers: int, num_heads: int,
+                   head_dim: int, dtype_bytes: int) -> int:
+    """KV-cache size from section 2.1 of the gsyq.cn page:
+    2 (K and V) x batch x seq_len x layers x heads x head_dim x bytes per element."""
+    return 2 * batch * seq_len * num_layers * num_heads * head_dim * dtype_bytes
+
+
+# ---------------------------------------------------------------------------
+# Append -- "块管理器：分页如何运作" (block manager) of the chenk.top page: a growing
+# request writes its new token into the slot its block table maps it to.
+# ---------------------------------------------------------------------------
+
+def append_scatter(k, v, k_cache, v_cache, slot_mapping, block_size):
+    """Literal scatter of new tokens into the paged caches; returns new arrays.
+
+    ``k``, ``v``: [T, Hkv, D]; caches: [NB, Hkv, bs, D]; ``slot_mapping``: [T] ints.
+    Token ``t`` with ``slot >= 0`` lands at ``cache[slot // bs, :, slot % bs, :]``.
+    """
+    k_out = np.array(k_cache, copy=True)
+    v_out = np.array(v_cache, copy=True)
+    for t in range(len(slot_mapping)):
+        slot = int(slot_mapping[t])
+        if slot < 0:
+            continue
+        blk, off = slot // block_size, slot % block_size
+        for h in range(k.shape[1]):
+            k_out[blk, h, off, :] = k[t, h, :]
+            v_out[blk, h, off, :] = v[t, h, :]
+    return k_out, v_out
+
+
+# ---------------------------------------------------------------------------
+# INT8 KV quantiser -- "INT8 仅权重量化" of the chenk.top page gives the form
+# w_q = round(w / s); "KV 缓存量化" of the same page and section 2.3 of the gsyq.cn
+# page put one scale on each token (and head), never one global scale.
+# ---------------------------------------------------------------------------
+
+def quantize_rows_int8(x):
+    """Symmetric per-row INT8 quantisation in IEEE fp32.
+
+    ``x``: [..., D] values (converted to float32; bf16 inputs convert exactly).
+    Returns ``(q int8 [..., D], s float32 [...])`` with ``s = absmax / 127`` and
+    ``q = clamp(rint(x / s), -127, 127)`` (numpy's rint rounds half to even).
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    s = (amax / np.float32(127.0)).astype(np.float32)
+    q = np.zeros(x32.shape, dtype=np.int8)
+    nz = s > 0
+    if np.any(nz):
+        ratio = (x32[nz] / s[nz][..., None]).astype(np.float32)
+        q[nz] = np.clip(np.rint(ratio), -127, 127).astype(np.int8)
+    return q, s
+
+
+def dequantize_rows_int8(q, s):
+    """Real value of stored INT8 codes: ``q * s`` evaluated in float64."""
+    return np.asarray(q, dtype=np.float64) * np.asarray(s, dtype=np.float64)[..., None]
+
+
+def append_scatter_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, block_size):
+    """Quantise each new token's K and V rows per KV head, then scatter codes and scales.
+
+    Caches: int8 [NB, Hkv, bs, D]; scales: float32 [NB, Hkv, bs]. Returns new arrays.
+    """
+    kq, ks = quantize_rows_int8(k)
+    vq, vs = quantize_rows_int8(v)
+    outs = [np.array(a, copy=True) for a in (k_cache, v_cache, k_scale, v_scale)]
+    kc, vc, ksc, vsc = outs
+    for t in range(len(slot_mapping)):
+        slot = int(slot_mapping[t])
+        if slot < 0:
+            continue
+        blk, off = slot // block_size, slot % block_size
+        for h in range(k.shape[1]):
+            kc[blk, h, off, :] = kq[t, h, :]
+            vc[blk, h, off, :] = vq[t, h, :]
+            ksc[blk, h, off] = ks[t, h]
+            vsc[blk, h, off] = vs[t, h]
+    return kc, vc, ksc, vsc
+
+
+# ---------------------------------------------------------------------------
+# Decode attention -- "两个特性截然不同的阶段" of the chenk.top page: one new query
+# per request attends over that request's whole cached K/V; "分页注意力" of the same
+# page: the cached tokens are reached through the request's block table.
+# ---------------------------------------------------------------------------
+
+def gather_sequence(cache, block_table_row, context_len, kv_head, block_size):
+    """Contiguous [L, D] float64 copy of one sequence's cached rows for one KV head.
+
+    Logical token ``t`` lives in physical block ``block_table_row[t // bs]`` at offset
+    ``t % bs``; table entries past ``ceil(L / bs)`` are never read.
+    """
+    L = int(context_len)
+    rows = []
+    for t in range(L):
+        phys = int(block_table_row[t // block_size])
+        rows.append(np.asarray(cache[phys, kv_head, t % block_size, :], dtype=np.float64))
+    if not rows:
+        return np.zeros((0, cache.shape[-1]), dtype=np.float64)
+    return np.stack(rows)
+
+
+def attend_one_head(q, K, V, scale):
+    """softmax(scale * K q) V for one head, float64, max-subtracted for stability.
+
+    ``q``: [D]; ``K``, ``V``: [L, D]. Returns ([D] output, [L] weights). L = 0 gives a
+    zero output and no weights. The dot products are elementwise sums (no BLAS), so
+    the oracle runs on one core.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    if K.shape[0] == 0:
+        return np.zeros(V.shape[-1], dtype=np.float64), np.zeros(0, dtype=np.float64)
+    z = float(scale) * np.sum(K * q[None, :], axis=1)
+    e = np.exp(z - np.max(z))
+    w = e / np.sum(e)
+    out = np.sum(w[:, None] * V, axis=0)
+    return out, w
+
+
+def _kv_head_of(h, group):
+    return h // group
+
+
+def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, block_size=None):
+    """Reference paged decode attention (MHA and GQA), float64.
+
+    ``q``: [B, Hq, D]; caches: [NB, Hkv, bs, D] (real values, any float dtype);
+    ``block_tables``: [B, MBS] ints; ``context_lens``: [B] ints. Returns [B, Hq, D]
+    float64.
+    """
+    q = np.asarray(q)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    bs = int(block_size) if block_size is not None else k_cache.shape[2]
+    if Hq % Hkv != 0:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    g = Hq // Hkv
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    for s in range(B):
+        L = int(context_lens[s])
+        for kvh in range(Hkv):
+            K = gather_sequence(k_cache, block_tables[s], L, kvh, bs)
+            V = gather_sequence(v_cache, block_tables[s], L, kvh, bs)
+            for h in range(Hq):
+                if _kv_head_of(h, g) != kvh:
+                    continue
+                out[s, h], _ = attend_one_head(q[s, h], K, V, scale)
+    return out
+
+
+def gather_sequence_int8(codes, scales, block_table_row, context_len, kv_head, block_size):
+    """Real [L, D] float64 values of one sequence's INT8 rows: code times its scale."""
+    q = gather_sequence(codes, block_table_row, context_len, kv_head, block_size)
+    L = int(context_len)
+    s = np.array([float(scales[int(block_table_row[t // block_size]), kv_head, t % block_size])
+                  for t in range(L)], dtype=np.float64)
+    return q * s[:, None]
+
+
+def decode_attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                          context_lens, scale, block_size=None):
+    """Paged decode attention over an INT8 cache: the stored codes times their fp32
+    per-(token, head) scales are the cached K/V values (exact in float64), then the
+    same attention as :func:`decode_attention`.
+    """
+    q = np.asarray(q)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    bs = int(block_size) if block_size is not None else k_cache.shape[2]
+    if Hq % Hkv != 0:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    g = Hq // Hkv
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    for s in range(B):
+        L = int(context_lens[s])
+        for kvh in range(Hkv):
+            K = gather_sequence_int8(k_cache, k_scale, block_tables[s], L, kvh, bs)
+            V = gather_sequence_int8(v_cache, v_scale, block_tables[s], L, kvh, bs)
+            for h in range(Hq):
+                if _kv_head_of(h, g) != kvh:
+                    continue
+                out[s, h], _ = attend_one_head(q[s, h], K, V, scale)
+    return out

@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of one paged-KV decode step: append the new token of every request
+(paged_kv_append) and attend over the whole paged cache (paged_decode_attention,
+split-KV merge included), on seeded synthetic inputs shaped like the pages' workloads.
+
+Prints ONE JSON line (rank 0). ``value`` is achieved HBM throughput in GB/s of
+algorithmic bytes (valid KV rows + scales + q + out + used table entries + context
+lengths + the appended rows) over the measured step time, summed over ranks; the line
+also carries KV tokens/s, the roofline of the decode kernel, an end-to-end figure with
+host buffers, clocks, and the CPU oracle timed on a bounded sample.
+
+    python bench.py [--config 7b] [--steps K] [--warmup W] [--gpus N]
+    python bench.py --impl reference ...     # the CPU oracle as the reference arm
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD_TEXT = {
+    "tiny": "tiny: batch 4, 8 q = 8 kv heads, head_dim 64, block 16, context U[1,64], 64-block "
+            "permuted pool",
+    "7b": "7B-like layer: batch 32, 32 q = 32 kv heads, head_dim 128, context 2048, block 16, "
+          "shuffled pool 1.2x demand",
+    "70b-gqa": "70B-like GQA: batch 64, 64 q / 8 kv heads, head_dim 128, block 16, context "
+               "log-normal (median 1024, sigma 1) clipped [128, 32768]",
+    "prefix": "prefix sharing: batch 256, 32 q / 8 kv heads, head_dim 128, block 16, shared "
+              "2048-token prefix (128 refcounted blocks) + suffix U[16,512]",
+    "int8": "INT8 KV: batch 128, 32 q / 8 kv heads, head_dim 128, context 8192, block 32, "
+            "per-token per-head fp32 scales",
+    "int8-bs16": "INT8 KV: batch 128, 32 q / 8 kv heads, head_dim 128, context 8192, block 16, "
+                 "per-token per-head fp32 scales",
+}
+L2_BYTES = 129e6
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="7b", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Byte accounting (algorithmic: what the method must move at least once)
+# ---------------------------------------------------------------------------
+
+def decode_bytes(w):
+    import numpy as np
+    L = w.context_lens.cpu().numpy().astype(np.int64)
+    elt = 1 if w.kv_dtype == "int8" else 2
+    tokens = int(L.sum())
+    kv = tokens * 2 * w.num_kv_heads * w.head_dim * elt
+    scales = tokens * 2 * w.num_kv_heads * 4 if w.kv_dtype == "int8" else 0
+    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * 2
+    tables = int(sum(-(-int(x) // w.block_size) for x in L)) * 4
+    return {"kv": kv, "scales": scales, "q_out": qo, "tables": tables + 4 * w.num_seqs,
+            "total": kv + scales + qo + tables + 4 * w.num_seqs, "tokens": tokens}
+
+
+def append_bytes(w):
+    T = int((w.slot_mapping >= 0).sum().item())
+    elt = 1 if w.kv_dtype == "int8" else 2
+    rows = T * 2 * w.num_kv_heads * w.head_dim
+    scales = T * 2 * w.num_kv_heads * 4 if w.kv_dtype == "int8" else 0
+    return rows * 2 + rows * elt + scales + 8 * w.num_seqs
+
+
+def unique_kv_bytes(w):
+    """Bytes of distinct physical KV rows the step touches (prefix blocks counted once)."""
+    import numpy as np
+    L = w.context_lens.cpu().numpy()
+    bt = w.block_tables.cpu().numpy()
+    seen = {}
+    for s, Ls in enumerate(L):
+        n = -(-int(Ls) // w.block_size)
+        for j in range(n):
+            fill = min(w.block_size, int(Ls) - j * w.block_size)
+            seen[int(bt[s, j])] = max(seen.get(int(bt[s, j]), 0), fill)
+    elt = 1 if w.kv_dtype == "int8" else 2
+    return sum(seen.values()) * 2 * w.num_kv_heads * w.head_dim * elt
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(", ") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (the reported baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _host_units(w, count, seed=0):
+    """Copy `count` (sequence, KV head) units of the workload to host arrays."""
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(seed)
+    units = []
+    g = w.num_q_heads // w.num_kv_heads
+    for _ in range(count):
+        s = int(rng.integers(w.num_seqs))
+        kvh = int(rng.integers(w.num_kv_heads))
+        L = int(w.context_lens[s].item())
+        n = -(-L // w.block_size)
+        blocks = w.block_tables[s, :n].to(torch.int64)
+        unit = {"L": L, "q": w.q[s, kvh * g:(kvh + 1) * g].double().cpu().numpy(),
+                "table": np.arange(n)}
+        if w.kv_dtype == "int8":
+            unit["k"] = w.k_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
+            unit["v"] = w.v_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
+            unit["ks"] = w.k_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
+            unit["vs"] = w.v_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
+        else:
+            unit["k"] = w.k_cache[blocks][:, kvh:kvh + 1].double().cpu().numpy()
+            unit["v"] = w.v_cache[blocks][:, kvh:kvh + 1].double().cpu().numpy()
+        units.append(unit)
+    return units
+
+
+def _oracle_unit(w, u):
+    import oracle
+    if w.kv_dtype == "int8":
+        K = oracle.gather_sequence_int8(u["k"], u["ks"], u["table"], u["L"], 0, w.block_size)
+        V = oracle.gather_sequence_int8(u["v"], u["vs"], u["table"], u["L"], 0, w.block_size)
+    else:
+        K = oracle.gather_sequence(u["k"], u["table"], u["L"], 0, w.block_size)
+        V = oracle.gather_sequence(u["v"], u["table"], u["L"], 0, w.block_size)
+    for qh in u["q"]:
+        oracle.attend_one_head(qh, K, V, w.scale)
+
+
+def _unit_bytes(w, u):
+    elt = 1 if w.kv_dtype == "int8" else 2
+    g = w.num_q_heads // w.num_kv_heads
+    b = u["L"] * 2 * w.head_dim * elt + 2 * g * w.head_dim * 2 + 4 * len(u["table"])
+    if w.kv_dtype == "int8":
+        b += u["L"] * 2 * 4
+    return b
+
+
+def cpu_baseline(w, seconds):
+    units = _host_units(w, 64)
+    t0 = time.perf_counter()
+    done_bytes = done_tokens = n = 0
+    while True:
+        u = units[n % len(units)]
+        _oracle_unit(w, u)
+        done_bytes += _unit_bytes(w, u)
+        done_tokens += u["L"]
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": done_bytes / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "kv_tokens_per_s": done_tokens / el,
+            "sample": f"{n} (sequence, kv-head) units of the {w.name} workload "
+                      f"({done_tokens} KV tokens, {el:.1f} s, fp64 numpy, one thread)"}
+
+
+# ---------------------------------------------------------------------------
+# The GPU step
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world):
+    import torch
+
+    import paged_kv_decode_02_gb300 as pk
+    from paged_kv_decode_02_gb300 import build_lib
+    from paged_kv_decode_02_gb300.workloads import make_workload
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pk.load_library()
+    w = make_workload(args.config, device=dev)
+    int8 = w.kv_dtype == "int8"
+    need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                     w.block_size, w.num_blocks, w.max_blocks_per_seq,
+                                     pk.pagedkv.KV_INT8 if int8 else pk.pagedkv.KV_BF16)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(w.q)
+    stream = torch.cuda.current_stream(dev)
+
+    def append():
+        if int8:
+            pk.paged_kv_append_int8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                    w.slot_mapping)
+        else:
+            pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
+
+    def decode():
+        if int8:
+            pk.paged_decode_attention_int8(w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                           w.block_tables, w.context_lens, w.scale, out=out,
+                                           workspace=ws)
+        else:
+            pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                                      w.scale, out=out, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        append()
+        decode()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index) if (rank == 0 and not args.no_clocks) else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)  # let the sampler start before the timed region
+    t_start.record(stream)
+    for i in range(K):
+        append()
+        dec_ev[i][0].record(stream)
+        decode()
+        dec_ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop() if clocks else None
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    dec_ms = sum(a.elapsed_time(b) for a, b in dec_ev) / K
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / K
+
+    db = decode_bytes(w)
+    step_bytes = db["total"] + append_bytes(w)
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    tokens_per_s = world * db["tokens"] / (ms_step * 1e-3)
+    peak, peak_kind = measured_peak()
+    achieved = db["total"] / (dec_ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, pk, dev, append, out, ws, step_bytes, world)
+
+    result = {
+        "metric": "paged decode attention: achieved HBM GB/s (% of GB300 peak) and KV tokens/s",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype,
+        "data": "synthetic (seeded)",
+        "kv_tokens_per_s": round(tokens_per_s, 1),
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                   "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "num_blocks": w.num_blocks,
+                   "kv_tokens": db["tokens"], "step_bytes": step_bytes,
+                   "unique_kv_bytes": unique_kv_bytes(w) if args.config == "prefix" else None,
+                   "l2": f"inputs larger than L2: {db['kv'] / 1e6:.0f} MB of KV per step vs "
+                         f"{L2_BYTES / 1e6:.0f} MB L2, no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "kernel": "paged_decode_kernel + merge (one decode call)",
+                     "bytes_per_launch": db["total"], "avg_launch_ms": round(dec_ms, 5),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    return result, w
+
+
+def run_e2e(args, w, pk, dev, append_dev, out, ws, step_bytes, world):
+    """Same step through the public API from pinned HOST buffers: per step, copy the
+    step's inputs host->device, append + decode, copy the output device->host."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    int8 = w.kv_dtype == "int8"
+    host_in = {n: getattr(w, n).cpu().pin_memory()
+               for n in ("q", "new_k", "new_v", "slot_mapping", "block_tables", "context_lens")}
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def step():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        if int8:
+            pk.paged_kv_append_int8(dev_in["new_k"], dev_in["new_v"], w.k_cache, w.v_cache,
+                                    w.k_scale, w.v_scale, dev_in["slot_mapping"])
+            pk.paged_decode_attention_int8(dev_in["q"], w.k_cache, w.v_cache, w.k_scale,
+                                           w.v_scale, dev_in["block_tables"],
+                                           dev_in["context_lens"], w.scale, out=out,
+                                           workspace=ws)
+        else:
+            pk.paged_kv_append(dev_in["new_k"], dev_in["new_v"], w.k_cache, w.v_cache,
+                               dev_in["slot_mapping"])
+            pk.paged_decode_attention(dev_in["q"], w.k_cache, w.v_cache, dev_in["block_tables"],
+                                      dev_in["context_lens"], w.scale, out=out, workspace=ws)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    K = max(1, min(args.steps, 500))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / K
+    return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "steps": K,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_reference(args, rank):
+    """The CPU oracle as the reference arm: each step runs it, as it stands, on a
+    bounded sample of the same workload on the host cores."""
+    import torch
+    from paged_kv_decode_02_gb300.workloads import make_workload
+    if rank != 0:
+        return None
+    w = make_workload(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
+    units = _host_units(w, 16, seed=1)
+    budget_s = 150.0
+    per_step = max(1e-3, budget_s / max(1, args.steps + args.warmup))
+    done_bytes = 0
+    done_tokens = 0
+    for _ in range(args.warmup):
+        _oracle_unit(w, units[0])
+    t0 = time.perf_counter()
+    n = 0
+    for _ in range(args.steps):
+        ts = time.perf_counter()
+        while True:
+            u = units[n % len(units)]
+            _oracle_unit(w, u)
+            done_bytes += _unit_bytes(w, u)
+            done_tokens += u["L"]
+            n += 1
+            if time.perf_counter() - ts >= per_step:
+                break
+    el = time.perf_counter() - t0
+    value = done_bytes / el / 1e9
+    sample = (f"{n} (sequence, kv-head) units of the {args.config} workload per run "
+              f"({done_tokens} KV tokens), fp64 numpy oracle, one thread")
+    return {
+        "impl": "reference",
+        "metric": "paged decode attention: achieved HBM GB/s (% of GB300 peak) and KV tokens/s",
+        "value": round(value, 6), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * el / max(1, args.steps), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "kv_tokens_per_s": round(done_tokens / el, 1),
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    res, w = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

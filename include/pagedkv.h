@@ -1,0 +1,160 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: single-token decode attention over a paged
+ * KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation: every request (sequence) keeps its keys and values in fixed-size
+ * physical blocks of `block_size` tokens; a per-request block table maps logical
+ * block j to a physical block id ("分页注意力" section of "大模型工程（五）：推理优化
+ * 核心技法", chenk.top; section 2.2 of the gsyq.cn inference-optimisation page, which
+ * recommends 16- or 32-token blocks). Each decode step appends the new token's K/V
+ * into its slot and then attends one query per head over the whole cached context
+ * ("两个特性截然不同的阶段" of the chenk.top page: decode reads the entire KV cache
+ * every step and is memory-bound).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers on the current CUDA device, owned by
+ *     the caller. The library never allocates, frees or synchronises; every call is
+ *     asynchronous on `stream` (NULL = the legacy default stream).
+ *   - Host-side validation happens before any launch; a failed check returns a
+ *     negative pkv_status and launches nothing.
+ *   - Layouts (row-major, contiguous):
+ *       q, out          [num_seqs, num_q_heads, head_dim]            bf16
+ *       k, v (new)      [num_tokens, num_kv_heads, head_dim]         bf16
+ *       k_cache,v_cache [num_blocks, num_kv_heads, block_size, head_dim]  bf16 or int8
+ *       k_scale,v_scale [num_blocks, num_kv_heads, block_size]       fp32 (int8 only)
+ *       block_tables    [num_seqs, max_blocks_per_seq]               int32
+ *       context_lens    [num_seqs]                                   int32
+ *       slot_mapping    [num_tokens]                                 int64
+ *     A slot is physical_block * block_size + offset; a negative slot is skipped.
+ *     Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *     context_lens[s] counts every token sequence s attends to (the one appended
+ *     this step included); entries of block_tables past ceil(context_len /
+ *     block_size) are never read. A sequence with context_len 0 gets a zero output.
+ *   - Every cache/q/out pointer must be 16-byte aligned.
+ *   - Supported sizes: head_dim 64 or 128; block_size 16 or 32; any
+ *     num_q_heads / num_kv_heads group size (groups of 4 and more run on the tensor
+ *     cores, smaller ones on the CUDA cores).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_NULL = -1,         /* a required pointer is NULL */
+  PKV_ERR_DTYPE = -2,        /* unknown KV dtype code */
+  PKV_ERR_SHAPE = -3,        /* a size is non-positive or sizes disagree */
+  PKV_ERR_UNSUPPORTED = -4,  /* head_dim / block_size / batch outside what is built */
+  PKV_ERR_WORKSPACE = -5,    /* workspace NULL, too small or misaligned */
+  PKV_ERR_CUDA = -6,         /* a CUDA runtime or driver call failed */
+  PKV_ERR_ALIGNMENT = -7     /* a device pointer is not 16-byte aligned */
+} pkv_status;
+
+typedef enum pkv_kv_dtype {
+  PKV_KV_BF16 = 0,
+  PKV_KV_INT8 = 1            /* int8 codes + one fp32 scale per (token, KV head) */
+} pkv_kv_dtype;
+
+typedef struct pkv_dims {
+  int32_t num_seqs;            /* B: requests in the batch                      */
+  int32_t num_q_heads;         /* Hq                                            */
+  int32_t num_kv_heads;        /* Hkv; Hq must be a multiple of Hkv             */
+  int32_t head_dim;            /* D: 64 or 128                                  */
+  int32_t block_size;          /* tokens per physical block: 16 or 32           */
+  int32_t num_blocks;          /* physical blocks in the pool (cache dim 0)     */
+  int32_t max_blocks_per_seq;  /* row length of block_tables                    */
+} pkv_dims;
+
+/* Bits of the optional device status word (see pkv_decode_*). */
+#define PKV_DEV_BAD_CONTEXT_LEN 0x1  /* context_len < 0 or > max_blocks_per_seq*block_size */
+#define PKV_DEV_BAD_BLOCK_ID    0x2  /* a block id the context needs is outside [0, num_blocks) */
+#define PKV_DEV_TIMEOUT         0x4  /* a shared-memory copy did not complete in time */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* pkv_status_string(pkv_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int pkv_version(void);
+
+/*
+ * pkv_append_bf16 -- write each new token's K and V rows into its cache slot.
+ * Block manager of the chenk.top page ("块管理器：分页如何运作"): a growing request
+ * writes into the block its table appends.
+ *   k, v          [num_tokens, Hkv, D] bf16, read.
+ *   k_cache/v_cache  [num_blocks, Hkv, block_size, D] bf16, written at the slots.
+ *   slot_mapping  [num_tokens] int64; slot < 0 skips the token; a slot at or past
+ *                 num_blocks*block_size is also skipped (nothing is written).
+ * num_tokens == 0 is a no-op returning PKV_OK. Bit-exact copy.
+ */
+pkv_status pkv_append_bf16(const void* k, const void* v, void* k_cache, void* v_cache,
+                           const int64_t* slot_mapping, int32_t num_tokens,
+                           const pkv_dims* dims, pkv_stream_t stream);
+
+/*
+ * pkv_append_int8 -- quantise each new token's K and V rows per KV head and write
+ * codes and scales into the slot. INT8 KV of section 2.3 of the gsyq.cn page and
+ * "KV 缓存量化" of the chenk.top page (per-token, per-head scales), with the
+ * round(w / s) form of "INT8 仅权重量化" on the same page:
+ *   s = absmax(row) / 127 (fp32, IEEE division); q = clamp(rint(x / s), -127, 127)
+ *   (IEEE division, round half to even); absmax == 0 gives s = 0 and q = 0.
+ *   k, v       [num_tokens, Hkv, D] bf16, read.
+ *   k_cache, v_cache  int8 [num_blocks, Hkv, block_size, D], written.
+ *   k_scale, v_scale  fp32 [num_blocks, Hkv, block_size], written.
+ */
+pkv_status pkv_append_int8(const void* k, const void* v, int8_t* k_cache, int8_t* v_cache,
+                           float* k_scale, float* v_scale, const int64_t* slot_mapping,
+                           int32_t num_tokens, const pkv_dims* dims, pkv_stream_t stream);
+
+/*
+ * pkv_decode_workspace_bytes -- size of the device workspace that pkv_decode_bf16 /
+ * pkv_decode_int8 need for these dims and KV dtype on the CURRENT device (it
+ * depends on the device's SM count). Host-only query; writes *bytes.
+ */
+pkv_status pkv_decode_workspace_bytes(const pkv_dims* dims, pkv_kv_dtype kv_dtype,
+                                      size_t* bytes);
+
+/*
+ * pkv_decode_bf16 -- out[s, h, :] = softmax(scale * K_s q[s, h]) V_s, where K_s, V_s
+ * are sequence s's first context_lens[s] cached rows of KV head h / g, gathered
+ * through block_tables[s]. fp32 accumulation, bf16 output (round to nearest even).
+ *   workspace  device scratch of at least pkv_decode_workspace_bytes() bytes,
+ *              256-byte aligned, caller-owned; contents need no initialisation and
+ *              are overwritten. Calls that share a workspace must not overlap.
+ *   status     optional device int32 (NULL to skip the checks). When given, the
+ *              call validates context_lens and the used block ids, ORs the
+ *              PKV_DEV_* bits of what it finds into *status and writes a zero
+ *              output for every sequence that failed. Without it, invalid ids are
+ *              clamped into the pool (no fault) and those outputs are unspecified.
+ * Long contexts are split over several workers and merged with an online-softmax
+ * (max/sum) reduction inside the same call.
+ */
+pkv_status pkv_decode_bf16(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens,
+                           float scale, const pkv_dims* dims, void* workspace,
+                           size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
+
+/*
+ * pkv_decode_int8 -- as pkv_decode_bf16 over an INT8 cache: the cached value of a
+ * row is code * scale with the row's fp32 scale (k_scale for K, v_scale for V).
+ * V scales must stay below 65504 (they are folded into fp16 softmax weights).
+ */
+pkv_status pkv_decode_int8(void* out, const void* q, const int8_t* k_cache,
+                           const int8_t* v_cache, const float* k_scale, const float* v_scale,
+                           const int32_t* block_tables, const int32_t* context_lens,
+                           float scale, const pkv_dims* dims, void* workspace,
+                           size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,312 @@
+// api.cu -- the C ABI of libpagedkv.so: argument checks, launch planning, TMA
+// descriptors and kernel launches. Declared (with semantics) in include/pagedkv.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "pagedkv.h"
+
+namespace pkv {
+namespace {
+
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per shared-memory copy wait
+constexpr int kMaxSmemPerCta = 227 * 1024;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a cache viewed as [num_blocks*Hkv*block_size rows, D elements]; one
+// box is block_size rows by one 128-byte (64-byte for 64-byte rows) swizzle span.
+bool make_cache_map(CUtensorMap* map, const void* base, bool int8, int D, long long rows,
+                    int BS) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const int elt = int8 ? 1 : 2;
+  const int row_bytes = D * elt;
+  const int seg = row_bytes >= 128 ? 128 : 64;
+  cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+  cuuint32_t box[2] = {cuuint32_t(seg / elt), cuuint32_t(BS)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      enc(map, int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          seg == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Launch plan
+// ---------------------------------------------------------------------------
+struct Plan {
+  DecodeKernelInfo k;
+  int g, gs, nsg, HU;
+  int grid, W;
+  size_t smem;
+  size_t off_prefix, off_ml, off_o, ws_bytes;
+};
+
+pkv_status check_dims(const pkv_dims* d) {
+  if (!d) return PKV_ERR_NULL;
+  if (d->num_seqs < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 ||
+      d->block_size <= 0 || d->num_blocks <= 0 || d->max_blocks_per_seq <= 0)
+    return PKV_ERR_SHAPE;
+  if (d->num_q_heads % d->num_kv_heads != 0) return PKV_ERR_SHAPE;
+  if (d->head_dim != 64 && d->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (d->block_size != 16 && d->block_size != 32) return PKV_ERR_UNSUPPORTED;
+  const long long rows = (long long)d->num_blocks * d->num_kv_heads * d->block_size;
+  if (rows >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+  if ((long long)d->max_blocks_per_seq * d->block_size >= (1ll << 31)) return PKV_ERR_SHAPE;
+  return PKV_OK;
+}
+
+std::mutex g_attr_mu;
+
+pkv_status make_plan(const pkv_dims* d, bool int8, Plan* pl) {
+  pkv_status st = check_dims(d);
+  if (st != PKV_OK) return st;
+  Plan P{};
+  P.g = d->num_q_heads / d->num_kv_heads;
+  const bool mma = P.g >= 4;
+  if (mma) {
+    int nsg = 1;
+    while (P.g % nsg != 0 || P.g / nsg > 16) ++nsg;
+    P.nsg = nsg;
+    P.gs = P.g / nsg;
+  } else {
+    P.nsg = 1;
+    P.gs = P.g;
+  }
+  P.HU = d->num_kv_heads * P.nsg;
+  const int simt = mma ? 0 : P.g;
+  const bool found = int8 ? select_decode_int8(d->head_dim, d->block_size, simt, &P.k)
+                          : select_decode_bf16(d->head_dim, d->block_size, simt, &P.k);
+  if (!found) return PKV_ERR_UNSUPPORTED;
+  P.smem = size_t(P.k.warps) * P.k.warp_smem + 1024 + align_up(size_t(d->num_seqs + 1) * 4, 16);
+  if (P.smem > size_t(kMaxSmemPerCta)) return PKV_ERR_UNSUPPORTED;  // batch too large
+
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    if (cudaFuncSetAttribute(P.k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(P.smem)) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, P.k.fn, P.k.warps * 32, P.smem) !=
+          cudaSuccess ||
+      per_sm <= 0)
+    return PKV_ERR_CUDA;
+  P.grid = sms * per_sm;
+  P.W = P.grid * P.k.warps;
+
+  // workspace: [prefix (B+1) int32][partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
+  P.off_prefix = 0;
+  P.off_ml = align_up(size_t(d->num_seqs + 1) * 4, 256);
+  P.off_o = align_up(P.off_ml + size_t(2) * P.W * P.gs * 8, 256);
+  P.ws_bytes = align_up(P.off_o + size_t(2) * P.W * P.gs * d->head_dim * 4, 256);
+  *pl = P;
+  return PKV_OK;
+}
+
+pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
+                      const void* v_cache, const float* k_scale, const float* v_scale,
+                      const int32_t* block_tables, const int32_t* context_lens, float scale,
+                      const pkv_dims* d, void* workspace, size_t workspace_bytes,
+                      int32_t* status, cudaStream_t stream) {
+  pkv_status st = check_dims(d);
+  if (st != PKV_OK) return st;
+  if (d->num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PKV_ERR_NULL;
+  if (int8 && (!k_scale || !v_scale)) return PKV_ERR_NULL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (int8 && (!aligned16(k_scale) || !aligned16(v_scale))))
+    return PKV_ERR_ALIGNMENT;
+  Plan P;
+  st = make_plan(d, int8, &P);
+  if (st != PKV_OK) return st;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < P.ws_bytes)
+    return PKV_ERR_WORKSPACE;
+
+  const long long rows = (long long)d->num_blocks * d->num_kv_heads * d->block_size;
+  CUtensorMap tmk, tmv;
+  if (!make_cache_map(&tmk, k_cache, int8, d->head_dim, rows, d->block_size) ||
+      !make_cache_map(&tmv, v_cache, int8, d->head_dim, rows, d->block_size))
+    return PKV_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeParams p{};
+  p.q = q;
+  p.out = out;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.part_o = reinterpret_cast<float*>(ws + P.off_o);
+  p.part_ml = reinterpret_cast<float*>(ws + P.off_ml);
+  p.prefix_out = reinterpret_cast<int32_t*>(ws + P.off_prefix);
+  p.status = status;
+  p.B = d->num_seqs;
+  p.Hq = d->num_q_heads;
+  p.Hkv = d->num_kv_heads;
+  p.MBS = d->max_blocks_per_seq;
+  p.NB = d->num_blocks;
+  p.g = P.g;
+  p.gs = P.gs;
+  p.nsg = P.nsg;
+  p.HU = P.HU;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = kTimeoutNs;
+
+  void* args[] = {&tmk, &tmv, &p};
+  if (cudaLaunchKernel(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), args, P.smem, stream) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+
+  MergeParams m{};
+  m.out = out;
+  m.part_o = p.part_o;
+  m.part_ml = p.part_ml;
+  m.prefix = p.prefix_out;
+  m.block_tables = block_tables;
+  m.context_lens = context_lens;
+  m.status = status;
+  m.B = p.B;
+  m.Hq = p.Hq;
+  m.MBS = p.MBS;
+  m.NB = p.NB;
+  m.BS = d->block_size;
+  m.D = d->head_dim;
+  m.g = P.g;
+  m.gs = P.gs;
+  m.nsg = P.nsg;
+  m.HU = P.HU;
+  m.W = P.W;
+  launch_merge(m, stream);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+pkv_status check_append(const void* k, const void* v, const void* kc, const void* vc,
+                        const int64_t* slots, int T, const pkv_dims* d) {
+  pkv_status st = check_dims(d);
+  if (st != PKV_OK) return st;
+  if (T < 0) return PKV_ERR_SHAPE;
+  if (T == 0) return PKV_OK;
+  if (!k || !v || !kc || !vc || !slots) return PKV_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(kc) || !aligned16(vc)) return PKV_ERR_ALIGNMENT;
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_NULL: return "PKV_ERR_NULL: a required pointer is NULL";
+    case PKV_ERR_DTYPE: return "PKV_ERR_DTYPE: unknown KV dtype";
+    case PKV_ERR_SHAPE: return "PKV_ERR_SHAPE: sizes are invalid or inconsistent";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: head_dim/block_size/batch not built";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA call failed";
+    case PKV_ERR_ALIGNMENT: return "PKV_ERR_ALIGNMENT: a device pointer is not 16-byte aligned";
+  }
+  return "unknown pkv_status";
+}
+
+int pkv_version(void) { return 100; }
+
+pkv_status pkv_append_bf16(const void* k, const void* v, void* k_cache, void* v_cache,
+                           const int64_t* slot_mapping, int32_t num_tokens,
+                           const pkv_dims* dims, pkv_stream_t stream) {
+  pkv_status st = check_append(k, v, k_cache, v_cache, slot_mapping, num_tokens, dims);
+  if (st != PKV_OK || num_tokens == 0) return st;
+  if (launch_append_bf16(k, v, k_cache, v_cache, slot_mapping, num_tokens, dims->num_kv_heads,
+                         dims->head_dim, dims->block_size, dims->num_blocks,
+                         reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+pkv_status pkv_append_int8(const void* k, const void* v, int8_t* k_cache, int8_t* v_cache,
+                           float* k_scale, float* v_scale, const int64_t* slot_mapping,
+                           int32_t num_tokens, const pkv_dims* dims, pkv_stream_t stream) {
+  pkv_status st = check_append(k, v, k_cache, v_cache, slot_mapping, num_tokens, dims);
+  if (st != PKV_OK || num_tokens == 0) return st;
+  if (!k_scale || !v_scale) return PKV_ERR_NULL;
+  if (launch_append_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
+                         dims->num_kv_heads, dims->head_dim, dims->block_size, dims->num_blocks,
+                         reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_workspace_bytes(const pkv_dims* dims, pkv_kv_dtype kv_dtype,
+                                      size_t* bytes) {
+  if (!bytes) return PKV_ERR_NULL;
+  if (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_INT8) return PKV_ERR_DTYPE;
+  Plan P;
+  pkv_status st = make_plan(dims, kv_dtype == PKV_KV_INT8, &P);
+  if (st != PKV_OK) return st;
+  *bytes = P.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_bf16(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens,
+                           float scale, const pkv_dims* dims, void* workspace,
+                           size_t workspace_bytes, int32_t* status, pkv_stream_t stream) {
+  return run_decode(false, out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
+                    context_lens, scale, dims, workspace, workspace_bytes, status,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_decode_int8(void* out, const void* q, const int8_t* k_cache,
+                           const int8_t* v_cache, const float* k_scale, const float* v_scale,
+                           const int32_t* block_tables, const int32_t* context_lens,
+                           float scale, const pkv_dims* dims, void* workspace,
+                           size_t workspace_bytes, int32_t* status, pkv_stream_t stream) {
+  return run_decode(true, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                    scale, dims, workspace, workspace_bytes, status,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,846 @@
+// decode.cuh -- paged-KV single-token decode attention kernels for sm_103a.
+//
+// What is computed: for every sequence s and query head h,
+//   out[s,h,:] = softmax(scale * K_s q[s,h]) V_s
+// over the first context_lens[s] cached tokens of KV head h/g, reached through the
+// block table ("分页注意力" of "大模型工程（五）：推理优化核心技法", chenk.top). Decode
+// reads every cached byte once per step and is bound by HBM bandwidth ("两个特性截然
+// 不同的阶段", same page), so the design is built around streaming KV blocks:
+//
+// * Work split (stream-K over blocks): the (sequence, work-unit, logical block)
+//   triples are laid out in one flat order and cut into W equal contiguous ranges,
+//   one per warp of a persistent grid (W = warps per CTA x CTAs that fit x SMs).
+//   Ragged lengths therefore cost nothing in balance. A warp whose range covers a
+//   whole (sequence, unit) writes the final output; a cut unit leaves an unnormalised
+//   partial (o, running max, sum) that the merge kernel folds with the usual
+//   online-softmax rescaling.
+// * Data movement: each warp owns a private ring of shared-memory stages. One lane
+//   reads the block id from the table and issues TMA tensor copies of the block's K
+//   and V tiles (128-byte swizzled, so that the tensor-core fragment loads below are
+//   bank-conflict free) plus, for INT8, 1-D bulk copies of the per-token scales, all
+//   completing on that stage's mbarrier. Copies run `stages` blocks ahead of the math.
+// * Math: groups of 4 or more query heads per KV head make q.K^T a small dense
+//   contraction, done with m16n8k16 tensor-core MMAs (query heads on M, padded to 16;
+//   tokens on N; fp32 accumulate); P.V reuses the score fragments as the A operand.
+//   Smaller groups run on the CUDA cores with 16-byte shared loads and warp-shuffle
+//   reductions. Online softmax in base 2 with a max subtraction keeps the weights
+//   in [0, 1] ("softmax 数值稳定性" note of section 2.3 of the gsyq.cn page).
+// * INT8 KV (section 2.3 of the gsyq.cn page; "KV 缓存量化" of the chenk.top page):
+//   codes are widened exactly to fp16 in registers; the K scale multiplies the fp32
+//   score and the V scale is folded into the softmax weight before the P.V MMA.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// Tile geometry: a K (or V) tile holds one physical block of one KV head,
+// block_size rows of head_dim elements, landed by TMA as `halves` boxes of
+// [BS rows x kSeg bytes], each swizzled in 128- (or 64-) byte rows.
+// ---------------------------------------------------------------------------
+template <bool INT8, int D, int BS>
+struct TileGeom {
+  static constexpr int kElt = INT8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElt;
+  static constexpr int kSeg = kRowBytes >= 128 ? 128 : 64;
+  static constexpr int kHalves = kRowBytes / kSeg;
+  static constexpr int kChunksPerSeg = kSeg / 16;
+  static constexpr int kChunksPerRow = kRowBytes / 16;
+  static constexpr int kTileBytes = BS * kRowBytes;
+  static constexpr int kScaleBytes = INT8 ? BS * 4 : 0;
+  static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
+
+  // Swizzled byte offset of 16-byte chunk `cc` of token row `t`.
+  __device__ static __forceinline__ uint32_t off(int t, int cc) {
+    const int half = cc / kChunksPerSeg, ci = cc % kChunksPerSeg;
+    return swz<kSeg>(uint32_t((half * BS + t) * kSeg + ci * 16));
+  }
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128_zero(uint32_t addr) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// First query head of work unit u (KV head u / nsg, subgroup u % nsg).
+__device__ __forceinline__ int unit_head0(const DecodeParams& p, int u) {
+  return (u / p.nsg) * p.g + (u % p.nsg) * p.gs;
+}
+
+// Where a warp leaves a cut unit: slot 2w for the unit its range starts in, 2w+1
+// for the unit its range ends in.
+__device__ __forceinline__ size_t partial_slot(int w, bool first_segment) {
+  return size_t(2 * w + (first_segment ? 0 : 1));
+}
+
+// ===========================================================================
+// CUDA-core path (groups of 1..3 query heads per KV head)
+// ===========================================================================
+template <bool INT8, int D, int BS, int G>
+struct SimtPath {
+  using Geo = TileGeom<INT8, D, BS>;
+  static constexpr int kLPR = Geo::kRowBytes / 16;  // lanes per token row
+  static constexpr int kRPR = 32 / kLPR;            // token rows per round
+  static constexpr int kRounds = BS / kRPR;
+  static constexpr int kEPL = 16 / Geo::kElt;       // elements per lane
+  static_assert(kLPR <= 32 && kRounds >= 1, "row geometry");
+
+  int lane, c, r0, head0, s;
+  float qf[G][kEPL];
+  float m[G], l[G], o[G][kEPL];
+
+  __device__ __forceinline__ void init(int lane_) {
+    lane = lane_;
+    c = lane % kLPR;
+    r0 = lane / kLPR;
+  }
+
+  __device__ __forceinline__ void begin(const DecodeParams& p, int s_, int u) {
+    s = s_;
+    head0 = unit_head0(p, u);
+    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(p.q);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const uint4* src =
+          reinterpret_cast<const uint4*>(qb + (size_t(s) * p.Hq + head0 + h) * D + c * kEPL);
+#pragma unroll
+      for (int v = 0; v < kEPL / 8; ++v) {
+        const uint4 raw = __ldg(src + v);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = unpack_bf16x2(w[k]);
+          qf[h][v * 8 + 2 * k] = f.x * p.scale_log2;
+          qf[h][v * 8 + 2 * k + 1] = f.y * p.scale_log2;
+        }
+      }
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int e = 0; e < kEPL; ++e) o[h][e] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void load_row(uint32_t tile, int row, float (&f)[kEPL]) const {
+    const uint4 raw = lds128(tile + Geo::off(row, c));
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    if constexpr (INT8) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t b = w[k] ^ 0x80808080u;
+        const float2 lo = unpack_f16x2(biased_bytes_to_f16x2(b, 0x4140u));
+        const float2 hi = unpack_f16x2(biased_bytes_to_f16x2(b, 0x4342u));
+        f[4 * k + 0] = lo.x;
+        f[4 * k + 1] = lo.y;
+        f[4 * k + 2] = hi.x;
+        f[4 * k + 3] = hi.y;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 v = unpack_bf16x2(w[k]);
+        f[2 * k] = v.x;
+        f[2 * k + 1] = v.y;
+      }
+    }
+  }
+
+  __device__ __forceinline__ void block(const DecodeParams&, uint32_t sK, uint32_t sV,
+                                        uint32_t sKs, uint32_t sVs, int nvalid) {
+    float sc[G][kRounds];
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int row = r * kRPR + r0;
+      float kf[kEPL];
+      load_row(sK, row, kf);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < kEPL; ++e) acc = fmaf(qf[h][e], kf[e], acc);
+#pragma unroll
+        for (int off = kLPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if constexpr (INT8) acc *= lds_f32(sKs + 4 * row);
+        sc[h][r] = (row < nvalid) ? acc : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float mx = sc[h][0];
+#pragma unroll
+      for (int r = 1; r < kRounds; ++r) mx = fmaxf(mx, sc[h][r]);
+#pragma unroll
+      for (int off = kLPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m[h], mx);
+      const float alpha = fast_exp2(m[h] - mn);
+      m[h] = mn;
+      l[h] *= alpha;
+#pragma unroll
+      for (int e = 0; e < kEPL; ++e) o[h][e] *= alpha;
+#pragma unroll
+      for (int r = 0; r < kRounds; ++r) sc[h][r] = fast_exp2(sc[h][r] - mn);
+    }
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int row = r * kRPR + r0;
+      if (row < nvalid) {
+        float vf[kEPL];
+        load_row(sV, row, vf);
+        float vsc = 1.f;
+        if constexpr (INT8) vsc = lds_f32(sVs + 4 * row);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          l[h] += sc[h][r];
+          const float pw = sc[h][r] * vsc;
+#pragma unroll
+          for (int e = 0; e < kEPL; ++e) o[h][e] = fmaf(pw, vf[e], o[h][e]);
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+      for (int off = kLPR; off < 32; off <<= 1) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+#pragma unroll
+        for (int e = 0; e < kEPL; ++e) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], off);
+      }
+    }
+    if (r0 != 0) return;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      if (complete) {
+        const float inv = 1.f / l[h];
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                             (size_t(s) * p.Hq + head0 + h) * D + c * kEPL;
+#pragma unroll
+        for (int v = 0; v < kEPL / 8; ++v) {
+          uint4 pk;
+          pk.x = pack_bf16x2(o[h][v * 8 + 0] * inv, o[h][v * 8 + 1] * inv);
+          pk.y = pack_bf16x2(o[h][v * 8 + 2] * inv, o[h][v * 8 + 3] * inv);
+          pk.z = pack_bf16x2(o[h][v * 8 + 4] * inv, o[h][v * 8 + 5] * inv);
+          pk.w = pack_bf16x2(o[h][v * 8 + 6] * inv, o[h][v * 8 + 7] * inv);
+          reinterpret_cast<uint4*>(dst)[v] = pk;
+        }
+      } else {
+        float* dst = p.part_o + (slot * p.gs + h) * D + c * kEPL;
+#pragma unroll
+        for (int v = 0; v < kEPL / 4; ++v)
+          reinterpret_cast<float4*>(dst)[v] =
+              make_float4(o[h][4 * v], o[h][4 * v + 1], o[h][4 * v + 2], o[h][4 * v + 3]);
+        if (c == 0)
+          reinterpret_cast<float2*>(p.part_ml)[slot * p.gs + h] = make_float2(m[h], l[h]);
+      }
+    }
+  }
+};
+
+// ===========================================================================
+// Tensor-core path, bf16 cache (groups of 4..16 query heads per work unit)
+// ===========================================================================
+template <int D, int BS>
+struct MmaPathBf16 {
+  using Geo = TileGeom<false, D, BS>;
+  static constexpr int kKS = D / 16;  // k-steps of q.K^T
+  static constexpr int kNT = BS / 8;  // token n-tiles
+  static constexpr int kND = D / 8;   // head_dim n-tiles of P.V
+  static constexpr int kKK = BS / 16; // token k-steps of P.V
+
+  int lane, gid, cq, head0, s, gs;
+  uint32_t qa[kKS][4];
+  float o[kND][4];
+  float m0, m1, l0, l1;
+
+  __device__ __forceinline__ void init(int lane_) {
+    lane = lane_;
+    gid = lane >> 2;
+    cq = lane & 3;
+  }
+
+  __device__ __forceinline__ void begin(const DecodeParams& p, int s_, int u) {
+    s = s_;
+    gs = p.gs;
+    head0 = unit_head0(p, u);
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
+    const bool v0 = gid < gs, v1 = gid + 8 < gs;
+    const size_t row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 2);
+    const size_t row1 = row0 + 8 * (D / 2);
+#pragma unroll
+    for (int ks = 0; ks < kKS; ++ks) {
+      const int w = 8 * ks + cq;  // 32-bit word index of elements 16ks + 2cq
+      qa[ks][0] = v0 ? __ldg(qw + row0 + w) : 0u;
+      qa[ks][1] = v1 ? __ldg(qw + row1 + w) : 0u;
+      qa[ks][2] = v0 ? __ldg(qw + row0 + w + 4) : 0u;
+      qa[ks][3] = v1 ? __ldg(qw + row1 + w + 4) : 0u;
+    }
+#pragma unroll
+    for (int nd = 0; nd < kND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+  }
+
+  __device__ __forceinline__ void block(const DecodeParams& p, uint32_t sK, uint32_t sV, uint32_t,
+                                        uint32_t, int nvalid) {
+    const int r8 = lane & 7, mi = lane >> 3;
+    float sacc[kNT][4];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+    for (int np = 0; np < kNT / 2; ++np) {
+#pragma unroll
+      for (int ks = 0; ks < kKS; ++ks) {
+        uint32_t b[4];
+        ldmatrix_x4(b, sK + Geo::off(np * 16 + ((mi >> 1) << 3) + r8, 2 * ks + (mi & 1)));
+        mma_bf16_16816(sacc[2 * np], qa[ks], b[0], b[1]);
+        mma_bf16_16816(sacc[2 * np + 1], qa[ks], b[2], b[3]);
+      }
+    }
+    // scale, mask the tokens past the context, row maxima
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = nt * 8 + 2 * cq + (e & 1);
+        const float x = tok < nvalid ? sacc[nt][e] * p.scale_log2 : -INFINITY;
+        sacc[nt][e] = x;
+      }
+      mx0 = fmaxf(mx0, fmaxf(sacc[nt][0], sacc[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(sacc[nt][2], sacc[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    l0 *= a0;
+    l1 *= a1;
+#pragma unroll
+    for (int nd = 0; nd < kND; ++nd) {
+      o[nd][0] *= a0;
+      o[nd][1] *= a0;
+      o[nd][2] *= a1;
+      o[nd][3] *= a1;
+    }
+    // weights -> bf16 A fragments; the sums use the rounded weights
+    uint32_t pa[kKK][4];
+#pragma unroll
+    for (int kk = 0; kk < kKK; ++kk) {
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int nt = 2 * kk + hlf;
+        const uint32_t w0 =
+            pack_bf16x2(fast_exp2(sacc[nt][0] - mn0), fast_exp2(sacc[nt][1] - mn0));
+        const uint32_t w1 =
+            pack_bf16x2(fast_exp2(sacc[nt][2] - mn1), fast_exp2(sacc[nt][3] - mn1));
+        pa[kk][2 * hlf] = w0;
+        pa[kk][2 * hlf + 1] = w1;
+        const float2 f0 = unpack_bf16x2(w0), f1 = unpack_bf16x2(w1);
+        l0 += f0.x + f0.y;
+        l1 += f1.x + f1.y;
+      }
+    }
+    // rows past the context may hold anything (even NaN): zero them before P.V
+    if (nvalid < BS) {
+      for (int idx = lane; idx < (BS - nvalid) * Geo::kChunksPerRow; idx += 32)
+        sts128_zero(sV + Geo::off(nvalid + idx / Geo::kChunksPerRow, idx % Geo::kChunksPerRow));
+      __syncwarp();
+    }
+#pragma unroll
+    for (int kk = 0; kk < kKK; ++kk) {
+#pragma unroll
+      for (int nd2 = 0; nd2 < kND / 2; ++nd2) {
+        uint32_t b[4];
+        ldmatrix_x4_trans(b, sV + Geo::off(16 * kk + ((mi & 1) << 3) + r8, 2 * nd2 + (mi >> 1)));
+        mma_bf16_16816(o[2 * nd2], pa[kk], b[0], b[1]);
+        mma_bf16_16816(o[2 * nd2 + 1], pa[kk], b[2], b[3]);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const bool v0 = gid < gs, v1 = gid + 8 < gs;
+    if (complete) {
+      const float i0 = 1.f / l0, i1 = 1.f / l1;
+      uint32_t* out = reinterpret_cast<uint32_t*>(p.out);
+      const size_t row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 2);
+      const size_t row1 = row0 + 8 * (D / 2);
+#pragma unroll
+      for (int nd = 0; nd < kND; ++nd) {
+        if (v0) out[row0 + 4 * nd + cq] = pack_bf16x2(o[nd][0] * i0, o[nd][1] * i0);
+        if (v1) out[row1 + 4 * nd + cq] = pack_bf16x2(o[nd][2] * i1, o[nd][3] * i1);
+      }
+    } else {
+      float2* po = reinterpret_cast<float2*>(p.part_o);
+      const size_t row0 = (slot * p.gs + gid) * (D / 2);
+      const size_t row1 = row0 + 8 * (D / 2);
+#pragma unroll
+      for (int nd = 0; nd < kND; ++nd) {
+        if (v0) po[row0 + 4 * nd + cq] = make_float2(o[nd][0], o[nd][1]);
+        if (v1) po[row1 + 4 * nd + cq] = make_float2(o[nd][2], o[nd][3]);
+      }
+      if (cq == 0) {
+        float2* ml = reinterpret_cast<float2*>(p.part_ml);
+        if (v0) ml[slot * p.gs + gid] = make_float2(m0, l0);
+        if (v1) ml[slot * p.gs + gid + 8] = make_float2(m1, l1);
+      }
+    }
+  }
+};
+
+// ===========================================================================
+// Tensor-core path, INT8 cache (fp16 MMAs on exactly widened codes)
+// ===========================================================================
+template <int D, int BS>
+struct MmaPathInt8 {
+  using Geo = TileGeom<true, D, BS>;
+  static constexpr int kKS = D / 16;
+  static constexpr int kNT = BS / 8;
+  static constexpr int kND = D / 8;
+  static constexpr int kKK = BS / 16;
+  static constexpr int kQB = D / 4;       // bytes of a K row each lane reads
+  static constexpr int kQC = kQB / 16;    // ... as 16-byte chunks
+
+  int lane, gid, cq, head0, s, gs;
+  uint32_t qa[kKS][4];
+  float o[kND][4];
+  float m0, m1, l0, l1, rs0, rs1;
+
+  __device__ __forceinline__ void init(int lane_) {
+    lane = lane_;
+    gid = lane >> 2;
+    cq = lane & 3;
+  }
+
+  // Query rows are scaled by a power of two so that their largest entry sits near
+  // 2^14 before the (then exact) narrowing from bf16 to fp16; the score scale undoes it.
+  __device__ __forceinline__ void begin(const DecodeParams& p, int s_, int u) {
+    s = s_;
+    gs = p.gs;
+    head0 = unit_head0(p, u);
+    const bool v0 = gid < gs, v1 = gid + 8 < gs;
+    const uint2* qd = reinterpret_cast<const uint2*>(p.q);  // 4 bf16 per uint2
+    const size_t row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 4);
+    const size_t row1 = row0 + 8 * (D / 4);
+    float f0[kKS][4], f1[kKS][4];
+    float mx0 = 0.f, mx1 = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kKS; ++ks) {
+      const int w = (kQB / 4) * cq + ks;  // elements kQB*cq + 4ks .. +3
+      const uint2 a = v0 ? __ldg(qd + row0 + w) : make_uint2(0u, 0u);
+      const uint2 b = v1 ? __ldg(qd + row1 + w) : make_uint2(0u, 0u);
+      const float2 a01 = unpack_bf16x2(a.x), a23 = unpack_bf16x2(a.y);
+      const float2 b01 = unpack_bf16x2(b.x), b23 = unpack_bf16x2(b.y);
+      f0[ks][0] = a01.x; f0[ks][1] = a01.y; f0[ks][2] = a23.x; f0[ks][3] = a23.y;
+      f1[ks][0] = b01.x; f1[ks][1] = b01.y; f1[ks][2] = b23.x; f1[ks][3] = b23.y;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        mx0 = fmaxf(mx0, fabsf(f0[ks][e]));
+        mx1 = fmaxf(mx1, fabsf(f1[ks][e]));
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    int e0 = 0, e1 = 0;
+    if (mx0 > 0.f) { frexpf(mx0, &e0); e0 = 14 - e0; }
+    if (mx1 > 0.f) { frexpf(mx1, &e1); e1 = 14 - e1; }
+    const float sc0 = ldexpf(1.f, e0), sc1 = ldexpf(1.f, e1);
+    rs0 = p.scale_log2 * ldexpf(1.f, -e0);
+    rs1 = p.scale_log2 * ldexpf(1.f, -e1);
+#pragma unroll
+    for (int ks = 0; ks < kKS; ++ks) {
+      qa[ks][0] = pack_f16x2(f0[ks][0] * sc0, f0[ks][1] * sc0);
+      qa[ks][1] = pack_f16x2(f1[ks][0] * sc1, f1[ks][1] * sc1);
+      qa[ks][2] = pack_f16x2(f0[ks][2] * sc0, f0[ks][3] * sc0);
+      qa[ks][3] = pack_f16x2(f1[ks][2] * sc1, f1[ks][3] * sc1);
+    }
+#pragma unroll
+    for (int nd = 0; nd < kND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+  }
+
+  __device__ __forceinline__ void block(const DecodeParams& p, uint32_t sK, uint32_t sV,
+                                        uint32_t sKs, uint32_t sVs, int nvalid) {
+    float sacc[kNT][4];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+      const int row = nt * 8 + gid;
+#pragma unroll
+      for (int ch = 0; ch < kQC; ++ch) {
+        const uint4 raw = lds128(sK + Geo::off(row, kQC * cq + ch));
+        const uint32_t w[4] = {raw.x ^ 0x80808080u, raw.y ^ 0x80808080u, raw.z ^ 0x80808080u,
+                               raw.w ^ 0x80808080u};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ks = 4 * ch + k;
+          mma_f16_16816(sacc[nt], qa[ks], biased_bytes_to_f16x2(w[k], 0x4140u),
+                        biased_bytes_to_f16x2(w[k], 0x4342u));
+        }
+      }
+    }
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+    float kscl[kNT][2];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = nt * 8 + 2 * cq + e;
+        kscl[nt][e] = lds_f32(sKs + 4 * tok);
+        const bool ok = tok < nvalid;
+        sacc[nt][e] = ok ? sacc[nt][e] * kscl[nt][e] * rs0 : -INFINITY;
+        sacc[nt][e + 2] = ok ? sacc[nt][e + 2] * kscl[nt][e] * rs1 : -INFINITY;
+      }
+      mx0 = fmaxf(mx0, fmaxf(sacc[nt][0], sacc[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(sacc[nt][2], sacc[nt][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    l0 *= a0;
+    l1 *= a1;
+#pragma unroll
+    for (int nd = 0; nd < kND; ++nd) {
+      o[nd][0] *= a0;
+      o[nd][1] *= a0;
+      o[nd][2] *= a1;
+      o[nd][3] *= a1;
+    }
+    // weights times the V scale -> fp16 A fragments (a token past the context gets 0)
+    uint32_t pa[kKK][4];
+#pragma unroll
+    for (int kk = 0; kk < kKK; ++kk) {
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int nt = 2 * kk + hlf;
+        float w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = fast_exp2(sacc[nt][e] - ((e < 2) ? mn0 : mn1));
+        l0 += w[0] + w[1];
+        l1 += w[2] + w[3];
+        float vs[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tok = nt * 8 + 2 * cq + e;
+          vs[e] = tok < nvalid ? lds_f32(sVs + 4 * tok) : 0.f;
+        }
+        pa[kk][2 * hlf] = pack_f16x2(w[0] * vs[0], w[1] * vs[1]);
+        pa[kk][2 * hlf + 1] = pack_f16x2(w[2] * vs[0], w[3] * vs[1]);
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < kKK; ++kk) {
+      const int ta = 16 * kk + 2 * cq;
+#pragma unroll
+      for (int qg = 0; qg < D / 32; ++qg) {
+        const int bo = 32 * qg + 4 * gid;
+        const int ch = bo >> 4, wi = bo & 15;
+        const uint32_t w0 = lds32(sV + Geo::off(ta, ch) + wi) ^ 0x80808080u;
+        const uint32_t w1 = lds32(sV + Geo::off(ta + 1, ch) + wi) ^ 0x80808080u;
+        const uint32_t w2 = lds32(sV + Geo::off(ta + 8, ch) + wi) ^ 0x80808080u;
+        const uint32_t w3 = lds32(sV + Geo::off(ta + 9, ch) + wi) ^ 0x80808080u;
+        const uint32_t x01 = prmt(w0, w1, 0x5140u), x23 = prmt(w0, w1, 0x7362u);
+        const uint32_t y01 = prmt(w2, w3, 0x5140u), y23 = prmt(w2, w3, 0x7362u);
+        mma_f16_16816(o[4 * qg + 0], pa[kk], biased_bytes_to_f16x2(x01, 0x4140u),
+                      biased_bytes_to_f16x2(y01, 0x4140u));
+        mma_f16_16816(o[4 * qg + 1], pa[kk], biased_bytes_to_f16x2(x01, 0x4342u),
+                      biased_bytes_to_f16x2(y01, 0x4342u));
+        mma_f16_16816(o[4 * qg + 2], pa[kk], biased_bytes_to_f16x2(x23, 0x4140u),
+                      biased_bytes_to_f16x2(y23, 0x4140u));
+        mma_f16_16816(o[4 * qg + 3], pa[kk], biased_bytes_to_f16x2(x23, 0x4342u),
+                      biased_bytes_to_f16x2(y23, 0x4342u));
+      }
+    }
+  }
+
+  // n-tile 4qg+i, column n holds head_dim index 32qg + 4n + i, so a lane's c0 values
+  // over i = 0..3 are the 4 consecutive elements 32qg + 8cq + i and its c1 values
+  // the next 4.
+  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const bool v0 = gid < gs, v1 = gid + 8 < gs;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      if (!(rr == 0 ? v0 : v1)) continue;
+      const int e0 = 2 * rr;
+      const float lsum = rr == 0 ? l0 : l1;
+      const int hrow = gid + 8 * rr;
+#pragma unroll
+      for (int qg = 0; qg < D / 32; ++qg) {
+        float vals[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          vals[i] = o[4 * qg + i][e0];
+          vals[4 + i] = o[4 * qg + i][e0 + 1];
+        }
+        const int d0 = 32 * qg + 8 * cq;
+        if (complete) {
+          const float inv = 1.f / lsum;
+          uint4 pk;
+          pk.x = pack_bf16x2(vals[0] * inv, vals[1] * inv);
+          pk.y = pack_bf16x2(vals[2] * inv, vals[3] * inv);
+          pk.z = pack_bf16x2(vals[4] * inv, vals[5] * inv);
+          pk.w = pack_bf16x2(vals[6] * inv, vals[7] * inv);
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                               (size_t(s) * p.Hq + head0 + hrow) * D + d0;
+          *reinterpret_cast<uint4*>(dst) = pk;
+        } else {
+          float* dst = p.part_o + (slot * p.gs + hrow) * D + d0;
+          reinterpret_cast<float4*>(dst)[0] = make_float4(vals[0], vals[1], vals[2], vals[3]);
+          reinterpret_cast<float4*>(dst)[1] = make_float4(vals[4], vals[5], vals[6], vals[7]);
+        }
+      }
+      if (!complete && cq == 0)
+        reinterpret_cast<float2*>(p.part_ml)[slot * p.gs + hrow] =
+            make_float2(rr == 0 ? m0 : m1, lsum);
+    }
+  }
+};
+
+// ===========================================================================
+// Work cursor over the flat (sequence, unit, block) order.
+// ===========================================================================
+struct Cursor {
+  int s, u, j, n;
+};
+
+__device__ __forceinline__ void cursor_locate(Cursor& c, long long f, const int* prefix, int B,
+                                              int HU) {
+  int lo = 0, hi = B;  // HU*prefix[lo] <= f < HU*prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((long long)HU * prefix[mid] <= f) lo = mid; else hi = mid;
+  }
+  c.s = lo;
+  c.n = prefix[lo + 1] - prefix[lo];
+  const long long rem = f - (long long)HU * prefix[lo];
+  c.u = int(rem / c.n);
+  c.j = int(rem % c.n);
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B, int HU) {
+  if (++c.j < c.n) return;
+  c.j = 0;
+  if (++c.u < HU) return;
+  c.u = 0;
+  do { ++c.s; } while (c.s < B && prefix[c.s + 1] == prefix[c.s]);
+  c.n = c.s < B ? prefix[c.s + 1] - prefix[c.s] : 0;
+}
+
+// ===========================================================================
+// The kernel
+// ===========================================================================
+template <bool INT8, int D, int BS, class Path, int kWarps, int kStages>
+struct DecodeKernel {
+  using Geo = TileGeom<INT8, D, BS>;
+  static constexpr int kTile = Geo::kTileBytes;
+  static constexpr int kScaleBytes = Geo::kScaleBytes;
+  // per-warp shared memory: K tiles, V tiles, K/V scales, mbarriers
+  static constexpr int kOffV = kStages * kTile;
+  static constexpr int kOffScale = 2 * kStages * kTile;
+  static constexpr int kOffBar = kOffScale + kStages * 2 * kScaleBytes;
+  static constexpr int kWarpBytes = ((kOffBar + kStages * 8) + 1023) / 1024 * 1024;
+  static constexpr uint32_t kTxBytes = 2 * kTile + 2 * kScaleBytes;
+};
+
+template <bool INT8, int D, int BS, class Path, int kWarps, int kStages>
+__global__ void __launch_bounds__(kWarps * 32)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+  using K = DecodeKernel<INT8, D, BS, Path, kWarps, kStages>;
+  using Geo = typename K::Geo;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
+  int* s_prefix = reinterpret_cast<int*>(smem_gen + kWarps * K::kWarpBytes);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = p.B;
+
+  // ---- blocks per sequence and their exclusive prefix (every CTA computes it) ----
+  {
+    const int nthr = kWarps * 32;
+    const int per = (B + nthr - 1) / nthr;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int sum = 0;
+    for (int i = b0; i < b1; ++i) {
+      const int L = __ldg(p.context_lens + i);
+      sum += L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS);
+    }
+    // inclusive warp scan, then across warps
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    __shared__ int warp_tot[kWarps];
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w2 = 0; w2 < warp; ++w2) base += warp_tot[w2];
+    int run = base + incl - sum;
+    for (int i = b0; i < b1; ++i) {
+      const int L = __ldg(p.context_lens + i);
+      run += L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS);
+      s_prefix[i + 1] = run;
+    }
+    if (tid == 0) s_prefix[0] = 0;
+    __syncthreads();
+    if (blockIdx.x == 0)
+      for (int i = tid; i <= B; i += nthr) p.prefix_out[i] = s_prefix[i];
+  }
+
+  const int HU = p.HU;
+  const long long T = (long long)HU * s_prefix[B];
+  const int W = gridDim.x * kWarps;
+  const int w = blockIdx.x * kWarps + warp;
+  const long long a = T * w / W, b = T * (w + 1) / W;
+  if (a >= b) return;
+  const int nblk = int(b - a);
+
+  const uint32_t wbase = smem_base + warp * K::kWarpBytes;
+  auto sK = [&](int st) { return wbase + st * K::kTile; };
+  auto sV = [&](int st) { return wbase + K::kOffV + st * K::kTile; };
+  auto sKs = [&](int st) { return wbase + K::kOffScale + st * 2 * K::kScaleBytes; };
+  auto sVs = [&](int st) { return sKs(st) + K::kScaleBytes; };
+  auto bar = [&](int st) { return wbase + K::kOffBar + st * 8; };
+
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) mbar_init(bar(st), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  __syncwarp();
+
+  Cursor pc, cc;
+  cursor_locate(pc, a, s_prefix, B, HU);
+  cc = pc;
+
+  // lane 0 issues the copies of the block at the producer cursor into stage st
+  auto issue = [&](int st) {
+    if (lane == 0) {
+      int phys = __ldg(p.block_tables + size_t(pc.s) * p.MBS + pc.j);
+      phys = (phys < 0 || phys >= p.NB) ? 0 : phys;  // never copy outside the pool
+      const int kvh = pc.u / p.nsg;
+      const int row = (phys * p.Hkv + kvh) * BS;
+      mbar_arrive_expect_tx(bar(st), K::kTxBytes);
+#pragma unroll
+      for (int hf = 0; hf < Geo::kHalves; ++hf) {
+        const int x = hf * (Geo::kSeg / Geo::kElt);
+        tma_load_2d(sK(st) + hf * BS * Geo::kSeg, &tmk, bar(st), x, row);
+        tma_load_2d(sV(st) + hf * BS * Geo::kSeg, &tmv, bar(st), x, row);
+      }
+      if constexpr (INT8) {
+        bulk_load(sKs(st), p.k_scale + size_t(row), K::kScaleBytes, bar(st));
+        bulk_load(sVs(st), p.v_scale + size_t(row), K::kScaleBytes, bar(st));
+      }
+    }
+  };
+
+  const int npro = min(kStages, nblk);
+  for (int i = 0; i < npro; ++i) {
+    issue(i);
+    cursor_next(pc, s_prefix, B, HU);
+  }
+
+  Path path;
+  path.init(lane);
+  path.begin(p, cc.s, cc.u);
+  int seg_j0 = cc.j;
+  bool first_seg = true;
+  int Lc = min(__ldg(p.context_lens + cc.s), p.MBS * BS);
+
+  for (int i = 0; i < nblk; ++i) {
+    const int st = i % kStages;
+    const uint32_t par = uint32_t(i / kStages) & 1u;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(st), par, p.timeout_ns));
+    if (!ok) {
+      if (lane == 0 && p.status) atomicOr(p.status, 0x4);
+      // let the copies already in flight land before the warp leaves
+      const int issued = min(nblk, i + kStages);
+      for (int k2 = i + 1; k2 < issued; ++k2)
+        mbar_wait_bounded(bar(k2 % kStages), uint32_t(k2 / kStages) & 1u, p.timeout_ns);
+      return;
+    }
+    path.block(p, sK(st), sV(st), sKs(st), sVs(st), Lc - cc.j * BS);
+    __syncwarp();
+    if (i + kStages < nblk) {
+      fence_proxy_async_smem();
+      issue(st);
+      cursor_next(pc, s_prefix, B, HU);
+    }
+    const bool seg_end = (cc.j == cc.n - 1) || (i == nblk - 1);
+    if (seg_end) {
+      const bool complete = (seg_j0 == 0) && (cc.j == cc.n - 1);
+      path.finish(p, complete, partial_slot(w, first_seg));
+      first_seg = false;
+    }
+    cursor_next(cc, s_prefix, B, HU);
+    if (seg_end && i + 1 < nblk) {
+      seg_j0 = cc.j;
+      Lc = min(__ldg(p.context_lens + cc.s), p.MBS * BS);
+      path.begin(p, cc.s, cc.u);
+    }
+  }
+}
+
+// Shared-memory bytes of one CTA for a batch of B sequences.
+template <bool INT8, int D, int BS, class Path, int kWarps, int kStages>
+constexpr int decode_smem_bytes_fixed() {
+  return kWarps * DecodeKernel<INT8, D, BS, Path, kWarps, kStages>::kWarpBytes + 1024;
+}
+
+template <bool INT8, int D, int BS, class Path, int kWarps, int kStages>
+DecodeKernelInfo make_decode_info(int mma, int simt_heads) {
+  DecodeKernelInfo info;
+  info.fn = reinterpret_cast<const void*>(&paged_decode_kernel<INT8, D, BS, Path, kWarps, kStages>);
+  info.warps = kWarps;
+  info.stages = kStages;
+  info.warp_smem = DecodeKernel<INT8, D, BS, Path, kWarps, kStages>::kWarpBytes;
+  info.mma = mma;
+  info.simt_heads = simt_heads;
+  return info;
+}
+
+}  // namespace pkv

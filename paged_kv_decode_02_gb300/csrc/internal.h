@@ -1,0 +1,68 @@
+// internal.h -- declarations shared by the library's translation units (not public).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Parameters of one decode launch (device pointers; sizes as in pkv_dims).
+struct DecodeParams {
+  const void* q;               // [B, Hq, D] bf16
+  void* out;                   // [B, Hq, D] bf16
+  const float* k_scale;        // [NB, Hkv, BS] fp32 (int8 caches only)
+  const float* v_scale;
+  const int32_t* block_tables; // [B, MBS]
+  const int32_t* context_lens; // [B]
+  float* part_o;               // [2W, GS, D] fp32 partial outputs (unnormalised)
+  float* part_ml;              // [2W, GS, 2] fp32 (running max in log2 units, sum)
+  int32_t* prefix_out;         // [B+1] blocks-per-sequence exclusive prefix (CTA 0 writes)
+  int32_t* status;             // optional device status word
+  int B, Hq, Hkv, MBS, NB;
+  int g;                       // Hq / Hkv
+  int gs;                      // query heads handled per work unit
+  int nsg;                     // work units per KV head (g / gs)
+  int HU;                      // work units per sequence (Hkv * nsg)
+  float scale_log2;            // softmax scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+// Parameters of the split-KV merge / finalize launch.
+struct MergeParams {
+  void* out;
+  const float* part_o;
+  const float* part_ml;
+  const int32_t* prefix;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t* status;
+  int B, Hq, MBS, NB, BS, D;
+  int g, gs, nsg, HU;
+  int W;                       // number of decode workers (warps)
+};
+
+// A compiled decode kernel and its static shape.
+struct DecodeKernelInfo {
+  const void* fn;
+  int warps;         // warps per CTA (each warp is one independent worker)
+  int stages;        // shared-memory pipeline depth per warp
+  int warp_smem;     // shared-memory bytes per warp (1024-aligned)
+  int mma;           // 1 = tensor-core path (groups >= 4), 0 = CUDA-core path
+  int simt_heads;    // query heads per unit on the CUDA-core path
+};
+
+// Kernel tables, one per translation unit. Return false if the shape is not built.
+bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info);
+bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info);
+
+void launch_merge(const MergeParams& p, cudaStream_t stream);
+
+cudaError_t launch_append_bf16(const void* k, const void* v, void* k_cache, void* v_cache,
+                               const int64_t* slots, int T, int Hkv, int D, int BS, int NB,
+                               cudaStream_t stream);
+cudaError_t launch_append_int8(const void* k, const void* v, int8_t* k_cache, int8_t* v_cache,
+                               float* k_scale, float* v_scale, const int64_t* slots, int T,
+                               int Hkv, int D, int BS, int NB, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,242 @@
+"""ctypes binding over libpagedkv.so (see include/pagedkv.h for the C ABI).
+
+Argument marshalling only: every step of append and decode runs in the library's CUDA
+kernels. PyTorch supplies device memory (outputs and the workspace come from its
+caching allocator) and the current CUDA stream. There is no fallback: if the library
+is missing or a tensor is not on a CUDA device, the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.environ.get("PAGEDKV_LIB", os.path.join(_HERE, "libpagedkv.so"))
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_NULL = -1
+    ERR_DTYPE = -2
+    ERR_SHAPE = -3
+    ERR_UNSUPPORTED = -4
+    ERR_WORKSPACE = -5
+    ERR_CUDA = -6
+    ERR_ALIGNMENT = -7
+
+
+DEV_BAD_CONTEXT_LEN = 0x1
+DEV_BAD_BLOCK_ID = 0x2
+DEV_TIMEOUT = 0x4
+
+KV_BF16 = 0
+KV_INT8 = 1
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib().pkv_status_string(status).decode()}")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32)]
+
+
+EXPORTS = {
+    "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pkv_version": (ctypes.c_int, []),
+    "pkv_append_bf16": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int32, ctypes.c_void_p,
+                                                                ctypes.c_void_p]),
+    "pkv_append_int8": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int32, ctypes.c_void_p,
+                                                                ctypes.c_void_p]),
+    "pkv_decode_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int,
+                                                  ctypes.POINTER(ctypes.c_size_t)]),
+    "pkv_decode_bf16": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float, ctypes.c_void_p,
+                                                                ctypes.c_void_p, ctypes.c_size_t,
+                                                                ctypes.c_void_p, ctypes.c_void_p]),
+    "pkv_decode_int8": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_float, ctypes.c_void_p,
+                                                                ctypes.c_void_p, ctypes.c_size_t,
+                                                                ctypes.c_void_p, ctypes.c_void_p]),
+}
+
+_LIB = None
+_LOCK = threading.Lock()
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libpagedkv.so (raises if it has not been built)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None and path is None:
+            return _LIB
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise ImportError(f"{p} not found: build it with `python -m "
+                              f"paged_kv_decode_02_gb300.build_lib` (there is no CPU fallback)")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _LIB = lib
+        return lib
+
+
+def _lib():
+    return _LIB if _LIB is not None else load_library()
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(status, what):
+    if status != 0:
+        raise PagedKVError(status, what)
+
+
+def _require(t, name, dtype, ndim, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _dims(num_seqs, num_q_heads, k_cache, max_blocks_per_seq):
+    nb, hkv, bs, d = k_cache.shape
+    return Dims(num_seqs, num_q_heads, hkv, d, bs, nb, max_blocks_per_seq)
+
+
+def paged_kv_append(k, v, k_cache, v_cache, slot_mapping):
+    """Write new tokens' K/V rows ([T, Hkv, D] bf16) into the bf16 paged caches
+    ([NB, Hkv, bs, D]) at ``slot_mapping`` ([T] int64, -1 = skip). In place."""
+    dev = k_cache.device
+    for t, n, dt, nd in ((k, "k", torch.bfloat16, 3), (v, "v", torch.bfloat16, 3),
+                         (k_cache, "k_cache", torch.bfloat16, 4),
+                         (v_cache, "v_cache", torch.bfloat16, 4),
+                         (slot_mapping, "slot_mapping", torch.int64, 1)):
+        _require(t, n, dt, nd, dev)
+    dims = _dims(0, k_cache.shape[1], k_cache, 1)
+    with torch.cuda.device(dev):
+        st = _lib().pkv_append_bf16(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(slot_mapping), k.shape[0], ctypes.byref(dims),
+                                    _stream(dev))
+    _check(st, "pkv_append_bf16")
+
+
+def paged_kv_append_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping):
+    """Quantise new tokens' K/V rows per (token, KV head) and write INT8 codes into
+    ``k_cache``/``v_cache`` ([NB, Hkv, bs, D] int8) and fp32 scales into
+    ``k_scale``/``v_scale`` ([NB, Hkv, bs]). In place."""
+    dev = k_cache.device
+    for t, n, dt, nd in ((k, "k", torch.bfloat16, 3), (v, "v", torch.bfloat16, 3),
+                         (k_cache, "k_cache", torch.int8, 4), (v_cache, "v_cache", torch.int8, 4),
+                         (k_scale, "k_scale", torch.float32, 3),
+                         (v_scale, "v_scale", torch.float32, 3),
+                         (slot_mapping, "slot_mapping", torch.int64, 1)):
+        _require(t, n, dt, nd, dev)
+    dims = _dims(0, k_cache.shape[1], k_cache, 1)
+    with torch.cuda.device(dev):
+        st = _lib().pkv_append_int8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), k.shape[0],
+                                    ctypes.byref(dims), _stream(dev))
+    _check(st, "pkv_append_int8")
+
+
+def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           num_blocks, max_blocks_per_seq, kv_dtype=KV_BF16, device=None):
+    dims = Dims(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq)
+    out = ctypes.c_size_t(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = _lib().pkv_decode_workspace_bytes(ctypes.byref(dims), kv_dtype, ctypes.byref(out))
+    _check(st, "pkv_decode_workspace_bytes")
+    return int(out.value)
+
+
+def _decode(int8, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+            out, workspace, status):
+    dev = q.device
+    _require(q, "q", torch.bfloat16, 3, dev)
+    kvt = torch.int8 if int8 else torch.bfloat16
+    _require(k_cache, "k_cache", kvt, 4, dev)
+    _require(v_cache, "v_cache", kvt, 4, dev)
+    if int8:
+        _require(k_scale, "k_scale", torch.float32, 3, dev)
+        _require(v_scale, "v_scale", torch.float32, 3, dev)
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    if k_cache.shape != v_cache.shape or k_cache.shape[3] != D:
+        raise ValueError("cache shapes disagree with q")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    dims = _dims(B, Hq, k_cache, block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _require(out, "out", torch.bfloat16, 3, dev)
+    with torch.cuda.device(dev):
+        need = ctypes.c_size_t(0)
+        _check(_lib().pkv_decode_workspace_bytes(ctypes.byref(dims), KV_INT8 if int8 else KV_BF16,
+                                                 ctypes.byref(need)), "pkv_decode_workspace_bytes")
+        if workspace is None or workspace.numel() < need.value:
+            workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=dev)
+        if int8:
+            st = _lib().pkv_decode_int8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                                        _ptr(context_lens), float(scale), ctypes.byref(dims),
+                                        _ptr(workspace), workspace.numel(), _ptr(status),
+                                        _stream(dev))
+        else:
+            st = _lib().pkv_decode_bf16(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(block_tables), _ptr(context_lens), float(scale),
+                                        ctypes.byref(dims), _ptr(workspace), workspace.numel(),
+                                        _ptr(status), _stream(dev))
+    _check(st, "pkv_decode_int8" if int8 else "pkv_decode_bf16")
+    return out
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                           workspace=None, status=None):
+    """Single-token decode attention over a bf16 paged KV cache (MHA and GQA).
+
+    q [B, Hq, D] bf16; caches [NB, Hkv, bs, D] bf16; block_tables [B, MBS] int32;
+    context_lens [B] int32. Returns out [B, Hq, D] bf16. ``workspace`` (uint8, at
+    least :func:`decode_workspace_bytes`) and ``status`` (int32 [1]) are optional.
+    """
+    return _decode(False, q, k_cache, v_cache, None, None, block_tables, context_lens, scale,
+                   out, workspace, status)
+
+
+def paged_decode_attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                context_lens, scale, out=None, workspace=None, status=None):
+    """As :func:`paged_decode_attention` over an INT8 cache with per-(token, KV head)
+    fp32 scales ``k_scale``/``v_scale`` [NB, Hkv, bs]."""
+    return _decode(True, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                   scale, out, workspace, status)

@@ -1,0 +1,80 @@
+"""Helpers shared by the GPU parity tests: run the CPU oracle on (parts of) a
+workload whose tensors live on the GPU. Nothing here touches the CUDA library."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+# Bound on |GPU - oracle| for bf16 outputs of decode attention (bf16 and INT8 caches).
+DECODE_ATOL = 1e-2
+
+
+def to_f64(t):
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def sequence_blocks(w, s):
+    L = int(w.context_lens[s].item())
+    n = -(-L // w.block_size)
+    return L, w.block_tables[s, :n].to(torch.int64)
+
+
+def oracle_outputs(w, pairs=None):
+    """Oracle outputs [B, Hq, D] (float64; NaN where not computed) for the (s, h)
+    pairs given (all when None). Only each sequence's own blocks are copied to the
+    host, then re-indexed 0..n-1 for the oracle's gather."""
+    B, Hq, D = w.q.shape
+    g = w.group
+    out = np.full((B, Hq, D), np.nan)
+    want = {}
+    for (s, h) in (pairs if pairs is not None else [(s, h) for s in range(B) for h in range(Hq)]):
+        want.setdefault(s, set()).add(h)
+    q = to_f64(w.q)
+    for s, heads in want.items():
+        L, blocks = sequence_blocks(w, s)
+        if L == 0:
+            for h in heads:
+                out[s, h] = 0.0
+            continue
+        table = np.arange(len(blocks))
+        kvhs = sorted({h // g for h in heads})
+        for kvh in kvhs:
+            if w.kv_dtype == "int8":
+                kc = w.k_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
+                vc = w.v_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
+                ks = w.k_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
+                vs = w.v_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
+                K = oracle.gather_sequence_int8(kc, ks, table, L, 0, w.block_size)
+                V = oracle.gather_sequence_int8(vc, vs, table, L, 0, w.block_size)
+            else:
+                kc = to_f64(w.k_cache[blocks][:, kvh:kvh + 1])
+                vc = to_f64(w.v_cache[blocks][:, kvh:kvh + 1])
+                K = oracle.gather_sequence(kc, table, L, 0, w.block_size)
+                V = oracle.gather_sequence(vc, table, L, 0, w.block_size)
+            for h in heads:
+                if h // g == kvh:
+                    out[s, h], _ = oracle.attend_one_head(q[s, h], K, V, w.scale)
+    return out
+
+
+def max_err(gpu_out, ref, pairs=None):
+    got = to_f64(gpu_out)
+    if pairs is None:
+        assert np.all(np.isfinite(got))
+        return float(np.max(np.abs(got - ref)))
+    errs = [np.max(np.abs(got[s, h] - ref[s, h])) for (s, h) in pairs]
+    assert all(np.all(np.isfinite(got[s, h])) for (s, h) in pairs)
+    return float(max(errs))
+
+
+def sample_pairs(w, n, seed=0):
+    rng = np.random.default_rng(seed)
+    B, Hq = w.num_seqs, w.num_q_heads
+    L = w.context_lens.cpu().numpy()
+    picks = {(int(np.argmax(L)), 0), (int(np.argmin(L)), Hq - 1), (0, 0), (B - 1, Hq - 1)}
+    while len(picks) < n:
+        picks.add((int(rng.integers(B)), int(rng.integers(Hq))))
+    return sorted(picks)

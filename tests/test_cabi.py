@@ -1,0 +1,94 @@
+"""The C-ABI library builds, loads, and exports every entry point the public header
+declares; host-side argument checks answer without touching a GPU."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from paged_kv_decode_02_gb300 import build_lib
+    try:
+        return build_lib.build()
+    except RuntimeError as e:  # no nvcc on this machine
+        pytest.skip(str(e))
+
+
+def test_header_declares_the_api():
+    names = _declared_functions()
+    for must in ("pkv_append_bf16", "pkv_append_int8", "pkv_decode_bf16", "pkv_decode_int8",
+                 "pkv_decode_workspace_bytes", "pkv_status_string", "pkv_version"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True)
+    if out.returncode == 0:
+        exported = set(re.findall(r"\bT (pkv_\w+)", out.stdout))
+        assert set(_declared_functions()) <= exported
+
+
+def test_binding_signatures_cover_the_header(lib_path):
+    from paged_kv_decode_02_gb300 import pagedkv
+    assert set(pagedkv.EXPORTS) == set(_declared_functions())
+    lib = pagedkv.load_library(lib_path)
+    assert lib.pkv_version() == 100
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert b"NULL" in lib.pkv_status_string(-1)
+    assert lib.pkv_status_string(12345) == b"unknown pkv_status"
+
+
+def test_host_validation_without_gpu(lib_path):
+    """Each failing check returns before any CUDA call, so these run on a CPU machine."""
+    from paged_kv_decode_02_gb300 import pagedkv
+    lib = pagedkv.load_library(lib_path)
+    good = pagedkv.Dims(4, 8, 8, 64, 16, 64, 4)
+    p = ctypes.c_void_p(0x1000)
+    st = lib.pkv_decode_bf16(None, p, p, p, p, p, 0.1, ctypes.byref(good), p, 1 << 20, None, None)
+    assert st == pagedkv.Status.ERR_NULL
+    bad_bs = pagedkv.Dims(4, 8, 8, 64, 24, 64, 4)
+    st = lib.pkv_decode_bf16(p, p, p, p, p, p, 0.1, ctypes.byref(bad_bs), p, 1 << 20, None, None)
+    assert st == pagedkv.Status.ERR_UNSUPPORTED
+    bad_d = pagedkv.Dims(4, 8, 8, 96, 16, 64, 4)
+    st = lib.pkv_decode_bf16(p, p, p, p, p, p, 0.1, ctypes.byref(bad_d), p, 1 << 20, None, None)
+    assert st == pagedkv.Status.ERR_UNSUPPORTED
+    bad_group = pagedkv.Dims(4, 6, 4, 64, 16, 64, 4)
+    st = lib.pkv_decode_bf16(p, p, p, p, p, p, 0.1, ctypes.byref(bad_group), p, 1 << 20, None,
+                             None)
+    assert st == pagedkv.Status.ERR_SHAPE
+    st = lib.pkv_decode_bf16(p, p, p, p, p, p, 0.1, None, p, 1 << 20, None, None)
+    assert st == pagedkv.Status.ERR_NULL
+    mis = ctypes.c_void_p(0x1008)
+    st = lib.pkv_decode_bf16(mis, p, p, p, p, p, 0.1, ctypes.byref(good), p, 1 << 20, None, None)
+    assert st == pagedkv.Status.ERR_ALIGNMENT
+    st = lib.pkv_decode_int8(p, p, p, p, None, p, p, p, 0.1, ctypes.byref(good), p, 1 << 20, None,
+                             None)
+    assert st == pagedkv.Status.ERR_NULL
+    st = lib.pkv_append_bf16(p, None, p, p, p, 3, ctypes.byref(good), None)
+    assert st == pagedkv.Status.ERR_NULL
+    st = lib.pkv_append_bf16(p, p, p, p, p, -1, ctypes.byref(good), None)
+    assert st == pagedkv.Status.ERR_SHAPE
+    st = lib.pkv_append_bf16(None, None, None, None, None, 0, ctypes.byref(good), None)
+    assert st == pagedkv.Status.OK          # zero tokens: no-op
+    st = lib.pkv_append_int8(p, p, p, p, None, p, p, 3, ctypes.byref(good), None)
+    assert st == pagedkv.Status.ERR_NULL
+    n = ctypes.c_size_t(0)
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 7, ctypes.byref(n)) == \
+        pagedkv.Status.ERR_DTYPE
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 0, None) == pagedkv.Status.ERR_NULL

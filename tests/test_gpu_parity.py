@@ -1,0 +1,215 @@
+"""GPU parity: the CUDA library against the fp64 CPU oracle on seeded inputs.
+
+* append (bf16 scatter, INT8 quantise + scatter): bit-exact;
+* decode (bf16 and INT8 caches): max |gpu - oracle| <= 1e-2 on the bf16 output, on
+  whole outputs at sizes the oracle finishes in seconds (several tiles, ragged tails,
+  every group-size path) and on sampled outputs at the full workload sizes, in the
+  launch configuration the benchmark uses.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_02_gb300.workloads import make_workload
+from parity_helpers import DECODE_ATOL, max_err, oracle_outputs, sample_pairs, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_decode_02_gb300 import build_lib
+    build_lib.build()
+    import paged_kv_decode_02_gb300 as pk
+    pk.load_library()
+    return pk
+
+
+def _decode(pk, w, **kw):
+    if w.kv_dtype == "int8":
+        return pk.paged_decode_attention_int8(w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                              w.block_tables, w.context_lens, w.scale, **kw)
+    return pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                                     w.scale, **kw)
+
+
+# ---------------------------------------------------------------------------
+# append
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,kw", [("tiny", {}), ("70b-gqa", dict(num_seqs=5, head_dim=128)),
+                                     ("7b", dict(num_seqs=3, lengths=[1, 17, 2048]))])
+def test_append_bf16_bit_exact(pk, name, kw):
+    w = make_workload(name, device=DEV, **kw)
+    slots = w.slot_mapping.clone()
+    slots[0] = -1                                   # a skipped token
+    kc0, vc0 = w.k_cache.clone(), w.v_cache.clone()
+    pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, slots)
+    torch.cuda.synchronize()
+    ref_k, ref_v = oracle.append_scatter(
+        w.new_k.view(torch.int16).cpu().numpy(), w.new_v.view(torch.int16).cpu().numpy(),
+        kc0.view(torch.int16).cpu().numpy(), vc0.view(torch.int16).cpu().numpy(),
+        slots.cpu().numpy(), w.block_size)
+    assert np.array_equal(w.k_cache.view(torch.int16).cpu().numpy(), ref_k)
+    assert np.array_equal(w.v_cache.view(torch.int16).cpu().numpy(), ref_v)
+
+
+@pytest.mark.parametrize("D,bs", [(128, 32), (128, 16), (64, 16)])
+def test_append_int8_bit_exact(pk, D, bs):
+    w = make_workload("int8", device=DEV, num_seqs=6, lengths=[1, 31, 32, 33, 100, 64],
+                      head_dim=D, block_size=bs)
+    gen = torch.Generator(device=DEV).manual_seed(7)
+    k = (torch.randn(w.new_k.shape, generator=gen, device=DEV) *
+         torch.logspace(-3, 3, w.new_k.shape[0], device=DEV)[:, None, None]).to(torch.bfloat16)
+    v = torch.randn(w.new_v.shape, generator=gen, device=DEV).to(torch.bfloat16)
+    v[1] = 0                                         # an all-zero row -> scale 0, codes 0
+    k[2, 0, :4] = torch.tensor([127.0, 2.5, -2.5, 3.5])  # exact halves at unit scale
+    k[2, 0, 4:] = 0
+    slots = w.slot_mapping.clone()
+    slots[3] = -1
+    before = [t.clone() for t in (w.k_cache, w.v_cache, w.k_scale, w.v_scale)]
+    pk.paged_kv_append_int8(k, v, w.k_cache, w.v_cache, w.k_scale, w.v_scale, slots)
+    torch.cuda.synchronize()
+    ref = oracle.append_scatter_int8(k.float().cpu().numpy(), v.float().cpu().numpy(),
+                                     *[t.cpu().numpy() for t in before], slots.cpu().numpy(), bs)
+    got = [t.cpu().numpy() for t in (w.k_cache, w.v_cache, w.k_scale, w.v_scale)]
+    for a, b in zip(got, ref):
+        assert np.array_equal(a.view(np.uint8) if a.dtype == np.int8 else a.view(np.uint32),
+                              b.view(np.uint8) if b.dtype == np.int8 else b.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# decode, whole outputs at small sizes
+# ---------------------------------------------------------------------------
+
+def test_decode_tiny_with_poisoned_unused_slots(pk):
+    w = make_workload("tiny", device=DEV, poison_unused=True)
+    out = _decode(pk, w)
+    torch.cuda.synchronize()
+    ref = oracle_outputs(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+
+
+SHAPES = [
+    # (name, Hq, Hkv, D, bs, lengths)
+    ("mha-d128-bs16", 8, 8, 128, 16, [1, 15, 16, 17, 100, 333]),
+    ("mha-d64-bs32", 4, 4, 64, 32, [64, 3, 95, 200]),
+    ("g2-d128-bs32", 8, 4, 128, 32, [33, 7, 250]),
+    ("g3-d64-bs16", 6, 2, 64, 16, [48, 49, 1, 130]),
+    ("g4-d128-bs16", 16, 4, 128, 16, [1, 16, 47, 200, 513]),
+    ("g8-d128-bs16", 16, 2, 128, 16, [40, 700, 9, 64]),
+    ("g8-d64-bs32", 16, 2, 64, 32, [31, 32, 33, 300]),
+    ("g5-d128-bs32", 10, 2, 128, 32, [100, 5]),
+    ("g16-d128-bs16", 32, 2, 128, 16, [77, 260]),
+    ("g32-d64-bs16", 64, 2, 64, 16, [90, 17]),
+]
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
+def test_decode_small_shapes(pk, shape, kv):
+    _, Hq, Hkv, D, bs, lengths = shape
+    name = "int8" if kv == "int8" else "70b-gqa"
+    w = make_workload(name, device=DEV, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                      block_size=bs, lengths=lengths, seed=11, poison_unused=True)
+    out = _decode(pk, w)
+    torch.cuda.synchronize()
+    ref = oracle_outputs(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+
+
+def test_decode_empty_and_single_token_sequences(pk):
+    w = make_workload("70b-gqa", device=DEV, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                      lengths=[0, 1, 0, 16, 1], seed=3)
+    out = _decode(pk, w)
+    torch.cuda.synchronize()
+    got = to_f64(out)
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    ref = oracle_outputs(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+    # one token: the output is that token's V row (rounded to bf16)
+    blk = w.block_tables[1, 0].item()
+    for h in range(16):
+        np.testing.assert_array_equal(got[1, h], to_f64(w.v_cache[blk, h // 4, 0]))
+
+
+def test_decode_single_long_sequence_split_many_ways(pk):
+    """B = 1: one long context is cut across many workers and merged."""
+    w = make_workload("70b-gqa", device=DEV, lengths=[20000], num_q_heads=8, num_kv_heads=1,
+                      seed=5)
+    out = _decode(pk, w)
+    torch.cuda.synchronize()
+    ref = oracle_outputs(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+
+
+def test_decode_permuted_placement_is_bit_identical(pk):
+    w = make_workload("70b-gqa", device=DEV, num_seqs=6, seed=9)
+    out1 = _decode(pk, w).clone()
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(1)).to(DEV)
+    k2 = torch.empty_like(w.k_cache)
+    v2 = torch.empty_like(w.v_cache)
+    k2[perm] = w.k_cache
+    v2[perm] = w.v_cache
+    bt = w.block_tables.clone().long()
+    valid = bt < w.num_blocks
+    bt[valid] = perm[bt[valid]]
+    w.k_cache, w.v_cache, w.block_tables = k2, v2, bt.to(torch.int32)
+    out2 = _decode(pk, w)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+
+
+def test_decode_status_flags_bad_tables(pk):
+    w = make_workload("70b-gqa", device=DEV, num_seqs=4, num_q_heads=16, num_kv_heads=4, seed=4)
+    w.block_tables[1, 0] = w.num_blocks + 100        # out-of-range block id
+    w.context_lens[2] = w.block_tables.shape[1] * w.block_size + 5  # longer than its table
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _decode(pk, w, status=status)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st & 0x2 and st & 0x1 and not st & 0x4
+    got = to_f64(out)
+    assert np.all(got[1] == 0) and np.all(got[2] == 0)
+    good = [(s, h) for s in (0, 3) for h in range(16)]
+    w.context_lens[2] = 1   # keep the oracle away from the invalid rows
+    ref = oracle_outputs(w, good)
+    assert max_err(out, ref, good) <= DECODE_ATOL
+
+
+def test_decode_reuses_caller_workspace_and_output(pk):
+    w = make_workload("70b-gqa", device=DEV, num_seqs=8, seed=6)
+    need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                     w.block_size, w.num_blocks, w.max_blocks_per_seq)
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device=DEV)
+    out = torch.full_like(w.q, float("nan"))
+    r1 = _decode(pk, w, out=out, workspace=ws).clone()
+    r2 = _decode(pk, w, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(r1, r2)
+    ref = oracle_outputs(w)
+    assert max_err(r2, ref) <= DECODE_ATOL
+
+
+# ---------------------------------------------------------------------------
+# decode at the full workload sizes, sampled outputs
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["7b", "70b-gqa", "prefix", "int8", "int8-bs16"])
+def test_decode_full_size_sampled(pk, name):
+    w = make_workload(name, device=DEV)
+    if w.kv_dtype == "bf16":
+        pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
+    else:
+        pk.paged_kv_append_int8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                w.slot_mapping)
+    out = _decode(pk, w)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    pairs = sample_pairs(w, 24)
+    ref = oracle_outputs(w, pairs)
+    assert max_err(out, ref, pairs) <= DECODE_ATOL

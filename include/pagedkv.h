@@ -153,6 +153,31 @@ pkv_status pkv_decode_int8(void* out, const void* q, const int8_t* k_cache,
                            float scale, const pkv_dims* dims, void* workspace,
                            size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
 
+/*
+ * pkv_decode_bf16_noalloc -- pkv_decode_bf16 for callers that cannot allocate device
+ * memory (code running inside another runtime's memory pool, plugins not allowed to
+ * call cudaMalloc, or latency-critical paths where no allocation may happen). The pages
+ * have no counterpart: this is a library convenience, not part of the method.
+ *   Same arguments and result as pkv_decode_bf16, without workspace: the call uses a
+ *   fixed scratch array of PKV_NOALLOC_SCRATCH_BYTES that the library keeps in device
+ *   memory on every GPU that loads it, until the process exits. It allocates nothing
+ *   (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   Returns PKV_ERR_WORKSPACE, launching nothing, when these dims need more scratch
+ *   than PKV_NOALLOC_SCRATCH_BYTES (see pkv_decode_workspace_bytes with PKV_KV_BF16).
+ *   The first call on a device looks up the scratch's device address with
+ *   cudaGetSymbolAddress (once per device, with that device current); make that first
+ *   call before any stream capture.
+ *   Every call on a device shares the one scratch array, which keeps the last call's
+ *   contents (nothing in it needs to start at zero). Calls whose executions overlap
+ *   on the GPU (different streams, or other threads) race on it: serialise them.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+pkv_status pkv_decode_bf16_noalloc(void* out, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables,
+                                   const int32_t* context_lens, float scale,
+                                   const pkv_dims* dims, int32_t* status, pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

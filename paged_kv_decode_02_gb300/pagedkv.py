@@ -69,6 +69,10 @@ EXPORTS = {
     "pkv_decode_int8": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_float, ctypes.c_void_p,
                                                                 ctypes.c_void_p, ctypes.c_size_t,
                                                                 ctypes.c_void_p, ctypes.c_void_p]),
+    "pkv_decode_bf16_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float,
+                                                                        ctypes.c_void_p,
+                                                                        ctypes.c_void_p,
+                                                                        ctypes.c_void_p]),
 }
 
 _LIB = None

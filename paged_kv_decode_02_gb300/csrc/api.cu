@@ -64,6 +64,38 @@ bool make_cache_map(CUtensorMap* map, const void* base, bool int8, int D, long l
   return r == CUDA_SUCCESS;
 }
 
+// Encoded descriptors of recently used caches (the descriptor only depends on the
+// base address and the shape, so a decode loop over the same cache re-uses it).
+struct MapKey {
+  const void* base;
+  long long rows;
+  int D, BS, int8;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && rows == o.rows && D == o.D && BS == o.BS && int8 == o.int8;
+  }
+};
+constexpr int kMapCache = 16;
+std::mutex g_map_mu;
+MapKey g_map_keys[kMapCache];
+CUtensorMap g_maps[kMapCache];
+int g_map_count = 0, g_map_next = 0;
+
+bool cache_map(CUtensorMap* map, const void* base, bool int8, int D, long long rows, int BS) {
+  const MapKey key{base, rows, D, BS, int8 ? 1 : 0};
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (int i = 0; i < g_map_count; ++i)
+    if (g_map_keys[i] == key) {
+      *map = g_maps[i];
+      return true;
+    }
+  if (!make_cache_map(map, base, int8, D, rows, BS)) return false;
+  g_map_keys[g_map_next] = key;
+  g_maps[g_map_next] = *map;
+  g_map_next = (g_map_next + 1) % kMapCache;
+  if (g_map_count < kMapCache) ++g_map_count;
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // Launch plan
 // ---------------------------------------------------------------------------
@@ -89,11 +121,49 @@ pkv_status check_dims(const pkv_dims* d) {
   return PKV_OK;
 }
 
-std::mutex g_attr_mu;
+// Plans depend only on (dims, KV dtype, device); computing one queries occupancy and
+// sets a kernel attribute, which costs tens of microseconds, so recent plans are kept.
+struct PlanKey {
+  pkv_dims d;
+  int int8, device;
+  bool operator==(const PlanKey& o) const {
+    return std::memcmp(&d, &o.d, sizeof(d)) == 0 && int8 == o.int8 && device == o.device;
+  }
+};
+constexpr int kPlanCache = 16;
+std::mutex g_plan_mu;
+PlanKey g_plan_keys[kPlanCache];
+Plan g_plans[kPlanCache];
+int g_plan_count = 0, g_plan_next = 0;
+
+pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl);
 
 pkv_status make_plan(const pkv_dims* d, bool int8, Plan* pl) {
   pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  PlanKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.d = *d;
+  key.int8 = int8 ? 1 : 0;
+  key.device = dev;
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  for (int i = 0; i < g_plan_count; ++i)
+    if (g_plan_keys[i] == key) {
+      *pl = g_plans[i];
+      return PKV_OK;
+    }
+  st = make_plan_uncached(d, int8, pl);
+  if (st != PKV_OK) return st;
+  g_plan_keys[g_plan_next] = key;
+  g_plans[g_plan_next] = *pl;
+  g_plan_next = (g_plan_next + 1) % kPlanCache;
+  if (g_plan_count < kPlanCache) ++g_plan_count;
+  return PKV_OK;
+}
+
+pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl) {
   Plan P{};
   P.g = d->num_q_heads / d->num_kv_heads;
   const bool mma = P.g >= 4;
@@ -118,12 +188,11 @@ pkv_status make_plan(const pkv_dims* d, bool int8, Plan* pl) {
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PKV_ERR_CUDA;
-  {
-    std::lock_guard<std::mutex> lock(g_attr_mu);
-    if (cudaFuncSetAttribute(P.k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(P.smem)) != cudaSuccess)
-      return PKV_ERR_CUDA;
-  }
+  // the attribute is an upper bound only: set it to the most any batch size may need,
+  // so that cached plans of other batch sizes stay launchable
+  if (cudaFuncSetAttribute(P.k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmemPerCta) != cudaSuccess)
+    return PKV_ERR_CUDA;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, P.k.fn, P.k.warps * 32, P.smem) !=
           cudaSuccess ||
       per_sm <= 0)
@@ -163,8 +232,8 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
 
   const long long rows = (long long)d->num_blocks * d->num_kv_heads * d->block_size;
   CUtensorMap tmk, tmv;
-  if (!make_cache_map(&tmk, k_cache, int8, d->head_dim, rows, d->block_size) ||
-      !make_cache_map(&tmv, v_cache, int8, d->head_dim, rows, d->block_size))
+  if (!cache_map(&tmk, k_cache, int8, d->head_dim, rows, d->block_size) ||
+      !cache_map(&tmv, v_cache, int8, d->head_dim, rows, d->block_size))
     return PKV_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -192,7 +261,7 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
   p.timeout_ns = kTimeoutNs;
 
   void* args[] = {&tmk, &tmv, &p};
-  if (cudaLaunchKernel(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), args, P.smem, stream) !=
+  if (launch_pdl(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), args, P.smem, stream) !=
       cudaSuccess)
     return PKV_ERR_CUDA;
 

@@ -3,7 +3,7 @@
 // The block manager of "大模型工程（五）：推理优化核心技法" (chenk.top, section "块管理器：
 // 分页如何运作") grows a request by appending physical blocks to its table; each new
 // token then lands at slot = block * block_size + offset. The bf16 kernel is a pure
-// scatter with 16-byte vector copies (one warp per token). The INT8 kernel applies the
+// scatter with 16-byte vector copies (one thread per 16-byte chunk). The INT8 kernel applies the
 // per-(token, KV head) symmetric quantiser of section 2.3 of the gsyq.cn page with the
 // round(w / s) form of "INT8 仅权重量化" (chenk.top): s = absmax / 127 and
 // q = clamp(rint(x / s), -127, 127), both divisions IEEE round-to-nearest.
@@ -12,26 +12,26 @@
 
 namespace pkv {
 
-__global__ void __launch_bounds__(128)
+// One thread copies one 16-byte chunk of one (token, KV head) row of K and of V.
+__global__ void __launch_bounds__(256)
     paged_kv_append_bf16_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                                 uint4* __restrict__ kc, uint4* __restrict__ vc,
                                 const int64_t* __restrict__ slots, int T, int Hkv, int D, int BS,
                                 int NB) {
-  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
+  const int cpr = D / 8;  // 16-byte chunks per head row
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)T * Hkv * cpr) return;
+  const int t = int(i / (Hkv * cpr));
+  const int rem = int(i % (Hkv * cpr));
+  const int h = rem / cpr, dc = rem % cpr;
   const long long slot = slots[t];
   if (slot < 0 || slot >= (long long)NB * BS) return;
   const long long blk = slot / BS, off = slot % BS;
-  const int cpr = D / 8;  // 16-byte chunks per head row
-  const int total = Hkv * cpr;
-  for (int c = lane; c < total; c += 32) {
-    const int h = c / cpr, dc = c % cpr;
-    const size_t src = (size_t(t) * Hkv + h) * cpr + dc;
-    const size_t dst = ((size_t(blk) * Hkv + h) * BS + off) * cpr + dc;
-    kc[dst] = k[src];
-    vc[dst] = v[src];
-  }
+  const size_t dst = ((size_t(blk) * Hkv + h) * BS + off) * cpr + dc;
+  kc[dst] = k[i];
+  vc[dst] = v[i];
 }
 
 // One warp quantises one (token, KV head) row of K or V (blockIdx.y selects which).
@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(128)
                                 float* __restrict__ vs, const int64_t* __restrict__ slots, int T,
                                 int Hkv, int BS, int NB) {
   constexpr int E = D / 32;  // elements per lane
+  pdl_wait_prior_grid();
+  pdl_allow_next_grid();
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= T * Hkv) return;
@@ -84,10 +86,14 @@ cudaError_t launch_append_bf16(const void* k, const void* v, void* k_cache, void
                                const int64_t* slots, int T, int Hkv, int D, int BS, int NB,
                                cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  paged_kv_append_bf16_kernel<<<(T + 3) / 4, 128, 0, stream>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), slots, T, Hkv, D, BS, NB);
-  return cudaGetLastError();
+  const long long chunks = (long long)T * Hkv * (D / 8);
+  const uint4* kk = static_cast<const uint4*>(k);
+  const uint4* vv = static_cast<const uint4*>(v);
+  uint4* kc = static_cast<uint4*>(k_cache);
+  uint4* vc = static_cast<uint4*>(v_cache);
+  void* args[] = {&kk, &vv, &kc, &vc, &slots, &T, &Hkv, &D, &BS, &NB};
+  return launch_pdl(reinterpret_cast<const void*>(&paged_kv_append_bf16_kernel),
+                    dim3(unsigned((chunks + 255) / 256)), dim3(256), args, 0, stream);
 }
 
 cudaError_t launch_append_int8(const void* k, const void* v, int8_t* k_cache, int8_t* v_cache,
@@ -97,15 +103,12 @@ cudaError_t launch_append_int8(const void* k, const void* v, int8_t* k_cache, in
   const dim3 grid((T * Hkv + 3) / 4, 2);
   const auto* kb = static_cast<const __nv_bfloat16*>(k);
   const auto* vb = static_cast<const __nv_bfloat16*>(v);
-  if (D == 128)
-    paged_kv_append_int8_kernel<128><<<grid, 128, 0, stream>>>(kb, vb, k_cache, v_cache, k_scale,
-                                                               v_scale, slots, T, Hkv, BS, NB);
-  else if (D == 64)
-    paged_kv_append_int8_kernel<64><<<grid, 128, 0, stream>>>(kb, vb, k_cache, v_cache, k_scale,
-                                                              v_scale, slots, T, Hkv, BS, NB);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  void* args[] = {&kb, &vb, &k_cache, &v_cache, &k_scale, &v_scale, &slots, &T, &Hkv, &BS, &NB};
+  const void* fn = D == 128 ? reinterpret_cast<const void*>(&paged_kv_append_int8_kernel<128>)
+                 : D == 64  ? reinterpret_cast<const void*>(&paged_kv_append_int8_kernel<64>)
+                            : nullptr;
+  if (!fn) return cudaErrorInvalidValue;
+  return launch_pdl(fn, grid, dim3(128), args, 0, stream);
 }
 
 }  // namespace pkv

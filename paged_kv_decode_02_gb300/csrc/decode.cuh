@@ -695,6 +695,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.B;
+  pdl_wait_prior_grid();
 
   // ---- blocks per sequence and their exclusive prefix (every CTA computes it) ----
   {

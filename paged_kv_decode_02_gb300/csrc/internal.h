@@ -58,6 +58,25 @@ bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info);
 
 void launch_merge(const MergeParams& p, cudaStream_t stream);
 
+// Launches with programmatic stream serialisation: the kernel may be scheduled while
+// the previous kernel on the stream drains; every kernel of this library waits for its
+// predecessor (griddepcontrol.wait) before touching global memory, so results are
+// the same as with plain stream ordering.
+inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, size_t smem,
+                              cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 cudaError_t launch_append_bf16(const void* k, const void* v, void* k_cache, void* v_cache,
                                const int64_t* slots, int T, int Hkv, int D, int BS, int NB,
                                cudaStream_t stream);

@@ -23,6 +23,7 @@ __device__ __forceinline__ int worker_of(long long x, long long T, int W) {
 }
 
 __global__ void __launch_bounds__(128) paged_decode_merge_kernel(const MergeParams p) {
+  pdl_wait_prior_grid();
   const int s = blockIdx.x / p.HU, u = blockIdx.x % p.HU;
   const int head0 = (u / p.nsg) * p.g + (u % p.nsg) * p.gs;
   const int n = p.prefix[s + 1] - p.prefix[s];
@@ -86,7 +87,11 @@ __global__ void __launch_bounds__(128) paged_decode_merge_kernel(const MergePara
 
 void launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int grid = p.B * p.HU;
-  if (grid > 0) paged_decode_merge_kernel<<<grid, 128, 0, stream>>>(p);
+  if (grid <= 0) return;
+  MergeParams copy = p;
+  void* args[] = {&copy};
+  launch_pdl(reinterpret_cast<const void*>(&paged_decode_merge_kernel), dim3(grid), dim3(128),
+             args, 0, stream);
 }
 
 }  // namespace pkv

@@ -111,6 +111,27 @@ def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+class _OnDevice:
+    """Make `device` current for the library call (a no-op when it already is)."""
+
+    __slots__ = ("dev", "prev")
+
+    def __init__(self, device):
+        self.dev = device.index if device.index is not None else torch.cuda.current_device()
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.dev:
+            self.prev = cur
+            torch.cuda.set_device(self.dev)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
+
+
 def _check(status, what):
     if status != 0:
         raise PagedKVError(status, what)
@@ -146,7 +167,7 @@ def paged_kv_append(k, v, k_cache, v_cache, slot_mapping):
                          (slot_mapping, "slot_mapping", torch.int64, 1)):
         _require(t, n, dt, nd, dev)
     dims = _dims(0, k_cache.shape[1], k_cache, 1)
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         st = _lib().pkv_append_bf16(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(slot_mapping), k.shape[0], ctypes.byref(dims),
                                     _stream(dev))
@@ -165,7 +186,7 @@ def paged_kv_append_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping)
                          (slot_mapping, "slot_mapping", torch.int64, 1)):
         _require(t, n, dt, nd, dev)
     dims = _dims(0, k_cache.shape[1], k_cache, 1)
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         st = _lib().pkv_append_int8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), k.shape[0],
                                     ctypes.byref(dims), _stream(dev))
@@ -205,7 +226,7 @@ def _decode(int8, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_l
         out = torch.empty_like(q)
     else:
         _require(out, "out", torch.bfloat16, 3, dev)
-    with torch.cuda.device(dev):
+    with _OnDevice(dev):
         need = ctypes.c_size_t(0)
         _check(_lib().pkv_decode_workspace_bytes(ctypes.byref(dims), KV_INT8 if int8 else KV_BF16,
                                                  ctypes.byref(need)), "pkv_decode_workspace_bytes")

@@ -15,7 +15,6 @@ namespace pkv {
 namespace {
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per shared-memory copy wait
-constexpr int kMaxSmemPerCta = 227 * 1024;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -182,16 +181,20 @@ pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl) {
                           : select_decode_bf16(d->head_dim, d->block_size, simt, &P.k);
   if (!found) return PKV_ERR_UNSUPPORTED;
   P.smem = size_t(P.k.warps) * P.k.warp_smem + 1024 + align_up(size_t(d->num_seqs + 1) * 4, 16);
-  if (P.smem > size_t(kMaxSmemPerCta)) return PKV_ERR_UNSUPPORTED;  // batch too large
 
-  int dev = 0, sms = 0, per_sm = 0;
+  int dev = 0, sms = 0, per_sm = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return PKV_ERR_CUDA;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, P.k.fn) != cudaSuccess) return PKV_ERR_CUDA;
+  const size_t max_dyn = size_t(optin) - fa.sharedSizeBytes;
+  if (P.smem > max_dyn) return PKV_ERR_UNSUPPORTED;  // batch too large for one CTA's table
   // the attribute is an upper bound only: set it to the most any batch size may need,
   // so that cached plans of other batch sizes stay launchable
-  if (cudaFuncSetAttribute(P.k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kMaxSmemPerCta) != cudaSuccess)
+  if (cudaFuncSetAttribute(P.k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(max_dyn)) !=
+      cudaSuccess)
     return PKV_ERR_CUDA;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, P.k.fn, P.k.warps * 32, P.smem) !=
           cudaSuccess ||

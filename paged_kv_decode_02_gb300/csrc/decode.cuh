@@ -93,19 +93,32 @@ __device__ __forceinline__ size_t partial_slot(int w, bool first_segment) {
 
 // ===========================================================================
 // CUDA-core path (groups of 1..3 query heads per KV head)
+//
+// Eight lanes share a token row (four rows per round); a lane owns one or two
+// 16-byte chunks of head_dim and keeps q for them in registers. Dot products use
+// packed fp32x2 FMAs and a 3-step shuffle reduction over the row's lanes; P.V
+// accumulates each lane's chunks in fp32x2 registers, combined across the four row
+// groups once per work unit.
 // ===========================================================================
 template <bool INT8, int D, int BS, int G>
 struct SimtPath {
   using Geo = TileGeom<INT8, D, BS>;
-  static constexpr int kLPR = Geo::kRowBytes / 16;  // lanes per token row
-  static constexpr int kRPR = 32 / kLPR;            // token rows per round
+  static constexpr int kChunks = Geo::kChunksPerRow;          // 16-byte chunks per row
+  static constexpr int kLPR = kChunks < 8 ? kChunks : 8;      // lanes per token row
+  static constexpr int kCPL = kChunks / kLPR;                 // chunks per lane
+  static constexpr int kRPR = 32 / kLPR;                      // token rows per round
   static constexpr int kRounds = BS / kRPR;
-  static constexpr int kEPL = 16 / Geo::kElt;       // elements per lane
-  static_assert(kLPR <= 32 && kRounds >= 1, "row geometry");
+  static constexpr int kEPC = 16 / Geo::kElt;                 // elements per chunk
+  static constexpr int kEPL = kCPL * kEPC;                    // elements per lane
+  static_assert(kRounds >= 1 && kEPL % 2 == 0, "row geometry");
 
   int lane, c, r0, head0, s;
-  float qf[G][kEPL];
-  float m[G], l[G], o[G][kEPL];
+  float2 q2[G][kEPL / 2];
+  float2 o2[G][kEPL / 2];
+  float m[G], l[G];
+
+  // lane chunk k covers elements [(c + k*kLPR) * kEPC, +kEPC)
+  __device__ __forceinline__ int chunk_of(int k) const { return c + k * kLPR; }
 
   __device__ __forceinline__ void init(int lane_) {
     lane = lane_;
@@ -119,46 +132,45 @@ struct SimtPath {
     const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(p.q);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(qb + (size_t(s) * p.Hq + head0 + h) * D + c * kEPL);
+      const __nv_bfloat16* row = qb + (size_t(s) * p.Hq + head0 + h) * D;
 #pragma unroll
-      for (int v = 0; v < kEPL / 8; ++v) {
-        const uint4 raw = __ldg(src + v);
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      for (int k = 0; k < kCPL; ++k) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = unpack_bf16x2(w[k]);
-          qf[h][v * 8 + 2 * k] = f.x * p.scale_log2;
-          qf[h][v * 8 + 2 * k + 1] = f.y * p.scale_log2;
+        for (int v = 0; v < kEPC / 8; ++v) {
+          const uint4 raw =
+              __ldg(reinterpret_cast<const uint4*>(row + chunk_of(k) * kEPC) + v);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(w[e]);
+            q2[h][(k * kEPC + v * 8) / 2 + e] =
+                make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+          }
         }
       }
       m[h] = -INFINITY;
       l[h] = 0.f;
 #pragma unroll
-      for (int e = 0; e < kEPL; ++e) o[h][e] = 0.f;
+      for (int e = 0; e < kEPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
     }
   }
 
-  __device__ __forceinline__ void load_row(uint32_t tile, int row, float (&f)[kEPL]) const {
-    const uint4 raw = lds128(tile + Geo::off(row, c));
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    if constexpr (INT8) {
+  // kEPL/2 fp32 pairs of one token row (bf16 exactly widened; int8 codes exactly).
+  __device__ __forceinline__ void load_row(uint32_t tile, int row, float2 (&f)[kEPL / 2]) const {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t b = w[k] ^ 0x80808080u;
-        const float2 lo = unpack_f16x2(biased_bytes_to_f16x2(b, 0x4140u));
-        const float2 hi = unpack_f16x2(biased_bytes_to_f16x2(b, 0x4342u));
-        f[4 * k + 0] = lo.x;
-        f[4 * k + 1] = lo.y;
-        f[4 * k + 2] = hi.x;
-        f[4 * k + 3] = hi.y;
-      }
-    } else {
+    for (int k = 0; k < kCPL; ++k) {
+      const uint4 raw = lds128(tile + Geo::off(row, chunk_of(k)));
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      if constexpr (INT8) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 v = unpack_bf16x2(w[k]);
-        f[2 * k] = v.x;
-        f[2 * k + 1] = v.y;
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t b = w[e] ^ 0x80808080u;
+          f[k * 8 + 2 * e] = unpack_f16x2(biased_bytes_to_f16x2(b, 0x4140u));
+          f[k * 8 + 2 * e + 1] = unpack_f16x2(biased_bytes_to_f16x2(b, 0x4342u));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[k * 4 + e] = unpack_bf16x2(w[e]);
       }
     }
   }
@@ -169,17 +181,18 @@ struct SimtPath {
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
       const int row = r * kRPR + r0;
-      float kf[kEPL];
+      float2 kf[kEPL / 2];
       load_row(sK, row, kf);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        float acc = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < kEPL; ++e) acc = fmaf(qf[h][e], kf[e], acc);
+        for (int e = 0; e < kEPL / 2; ++e) acc = __ffma2_rn(q2[h][e], kf[e], acc);
+        float a = acc.x + acc.y;
 #pragma unroll
-        for (int off = kLPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if constexpr (INT8) acc *= lds_f32(sKs + 4 * row);
-        sc[h][r] = (row < nvalid) ? acc : -INFINITY;
+        for (int off = kLPR / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+        if constexpr (INT8) a *= lds_f32(sKs + 4 * row);
+        sc[h][r] = (row < nvalid) ? a : -INFINITY;
       }
     }
 #pragma unroll
@@ -193,8 +206,9 @@ struct SimtPath {
       const float alpha = fast_exp2(m[h] - mn);
       m[h] = mn;
       l[h] *= alpha;
+      const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-      for (int e = 0; e < kEPL; ++e) o[h][e] *= alpha;
+      for (int e = 0; e < kEPL / 2; ++e) o2[h][e] = __fmul2_rn(o2[h][e], a2);
 #pragma unroll
       for (int r = 0; r < kRounds; ++r) sc[h][r] = fast_exp2(sc[h][r] - mn);
     }
@@ -202,7 +216,7 @@ struct SimtPath {
     for (int r = 0; r < kRounds; ++r) {
       const int row = r * kRPR + r0;
       if (row < nvalid) {
-        float vf[kEPL];
+        float2 vf[kEPL / 2];
         load_row(sV, row, vf);
         float vsc = 1.f;
         if constexpr (INT8) vsc = lds_f32(sVs + 4 * row);
@@ -210,8 +224,9 @@ struct SimtPath {
         for (int h = 0; h < G; ++h) {
           l[h] += sc[h][r];
           const float pw = sc[h][r] * vsc;
+          const float2 p2 = make_float2(pw, pw);
 #pragma unroll
-          for (int e = 0; e < kEPL; ++e) o[h][e] = fmaf(pw, vf[e], o[h][e]);
+          for (int e = 0; e < kEPL / 2; ++e) o2[h][e] = __ffma2_rn(p2, vf[e], o2[h][e]);
         }
       }
     }
@@ -224,7 +239,10 @@ struct SimtPath {
       for (int off = kLPR; off < 32; off <<= 1) {
         l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
 #pragma unroll
-        for (int e = 0; e < kEPL; ++e) o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], off);
+        for (int e = 0; e < kEPL / 2; ++e) {
+          o2[h][e].x += __shfl_xor_sync(0xffffffffu, o2[h][e].x, off);
+          o2[h][e].y += __shfl_xor_sync(0xffffffffu, o2[h][e].y, off);
+        }
       }
     }
     if (r0 != 0) return;
@@ -232,23 +250,32 @@ struct SimtPath {
     for (int h = 0; h < G; ++h) {
       if (complete) {
         const float inv = 1.f / l[h];
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                             (size_t(s) * p.Hq + head0 + h) * D + c * kEPL;
+        __nv_bfloat16* row =
+            reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t(s) * p.Hq + head0 + h) * D;
 #pragma unroll
-        for (int v = 0; v < kEPL / 8; ++v) {
-          uint4 pk;
-          pk.x = pack_bf16x2(o[h][v * 8 + 0] * inv, o[h][v * 8 + 1] * inv);
-          pk.y = pack_bf16x2(o[h][v * 8 + 2] * inv, o[h][v * 8 + 3] * inv);
-          pk.z = pack_bf16x2(o[h][v * 8 + 4] * inv, o[h][v * 8 + 5] * inv);
-          pk.w = pack_bf16x2(o[h][v * 8 + 6] * inv, o[h][v * 8 + 7] * inv);
-          reinterpret_cast<uint4*>(dst)[v] = pk;
+        for (int k = 0; k < kCPL; ++k) {
+#pragma unroll
+          for (int v = 0; v < kEPC / 8; ++v) {
+            const float2* f = &o2[h][(k * kEPC + v * 8) / 2];
+            uint4 pk;
+            pk.x = pack_bf16x2(f[0].x * inv, f[0].y * inv);
+            pk.y = pack_bf16x2(f[1].x * inv, f[1].y * inv);
+            pk.z = pack_bf16x2(f[2].x * inv, f[2].y * inv);
+            pk.w = pack_bf16x2(f[3].x * inv, f[3].y * inv);
+            reinterpret_cast<uint4*>(row + chunk_of(k) * kEPC)[v] = pk;
+          }
         }
       } else {
-        float* dst = p.part_o + (slot * p.gs + h) * D + c * kEPL;
+        float* row = p.part_o + (slot * p.gs + h) * D;
 #pragma unroll
-        for (int v = 0; v < kEPL / 4; ++v)
-          reinterpret_cast<float4*>(dst)[v] =
-              make_float4(o[h][4 * v], o[h][4 * v + 1], o[h][4 * v + 2], o[h][4 * v + 3]);
+        for (int k = 0; k < kCPL; ++k) {
+#pragma unroll
+          for (int v = 0; v < kEPC / 4; ++v) {
+            const float2* f = &o2[h][(k * kEPC + v * 4) / 2];
+            reinterpret_cast<float4*>(row + chunk_of(k) * kEPC)[v] =
+                make_float4(f[0].x, f[0].y, f[1].x, f[1].y);
+          }
+        }
         if (c == 0)
           reinterpret_cast<float2*>(p.part_ml)[slot * p.gs + h] = make_float2(m[h], l[h]);
       }

@@ -22,12 +22,16 @@ __device__ __forceinline__ int worker_of(long long x, long long T, int W) {
   return int(((x + 1) * W + T - 1) / T) - 1;
 }
 
-__global__ void __launch_bounds__(128) paged_decode_merge_kernel(const MergeParams p) {
+constexpr int kMergeThreads = 256;
+constexpr int kMergeSlots = 1024;  // partial slots staged in shared memory per pass
+
+__global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const MergeParams p) {
   pdl_wait_prior_grid();
   const int s = blockIdx.x / p.HU, u = blockIdx.x % p.HU;
   const int head0 = (u / p.nsg) * p.g + (u % p.nsg) * p.gs;
   const int n = p.prefix[s + 1] - p.prefix[s];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kMergeThreads / 32;
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t(s) * p.Hq + head0) * p.D;
   const int total = p.gs * p.D;
 
@@ -61,27 +65,88 @@ __global__ void __launch_bounds__(128) paged_decode_merge_kernel(const MergePara
   const int w0 = worker_of(A, T, p.W), w1 = worker_of(E - 1, T, p.W);
   if (w0 == w1) return;  // one worker covered the whole unit and wrote the output
 
+  __shared__ int s_slot[kMergeSlots];
+  __shared__ float s_max[16];
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  for (int i = tid; i < total; i += blockDim.x) {
-    const int row = i / p.D, d = i % p.D;
-    float M = -INFINITY;
-    for (int w = w0; w <= w1; ++w) {
+  const int gs = p.gs, D = p.D;
+  const int nq = total / 4;  // float4 outputs of this unit
+  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  float lsum[2] = {0.f, 0.f};
+
+  // pass 1: the partial slots and each row's maximum over them
+  const int P = w1 - w0 + 1;
+  float rowmax = -INFINITY;  // lane-local, for row `warp` (+ kWarps)
+  float rowmax2 = -INFINITY;
+  for (int base = 0; base < P; base += kMergeSlots) {
+    const int cnt = min(kMergeSlots, P - base);
+    __syncthreads();
+    for (int i = tid; i < cnt; i += blockDim.x) {
+      const int w = w0 + base + i;
       const long long aw = worker_start(T, w, p.W);
-      if (aw == worker_start(T, w + 1, p.W)) continue;
-      const size_t slot = size_t(2 * w + ((w == w0 && aw != A) ? 1 : 0));
-      M = fmaxf(M, ml[slot * p.gs + row].x);
+      const bool empty = aw == worker_start(T, w + 1, p.W);
+      s_slot[i] = empty ? -1 : 2 * w + ((w == w0 && aw != A) ? 1 : 0);
     }
-    float lsum = 0.f, acc = 0.f;
-    for (int w = w0; w <= w1; ++w) {
-      const long long aw = worker_start(T, w, p.W);
-      if (aw == worker_start(T, w + 1, p.W)) continue;
-      const size_t slot = size_t(2 * w + ((w == w0 && aw != A) ? 1 : 0));
-      const float2 mlw = ml[slot * p.gs + row];
-      const float f = fast_exp2(mlw.x - M);
-      lsum += f * mlw.y;
-      acc += f * p.part_o[(slot * p.gs + row) * p.D + d];
+    __syncthreads();
+    for (int i = lane; i < cnt; i += 32) {
+      const int slot = s_slot[i];
+      if (slot < 0) continue;
+      if (warp < gs) rowmax = fmaxf(rowmax, ml[size_t(slot) * gs + warp].x);
+      if (warp + kWarps < gs) rowmax2 = fmaxf(rowmax2, ml[size_t(slot) * gs + warp + kWarps].x);
     }
-    out[i] = __float2bfloat16_rn(acc / lsum);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    rowmax = fmaxf(rowmax, __shfl_xor_sync(0xffffffffu, rowmax, o));
+    rowmax2 = fmaxf(rowmax2, __shfl_xor_sync(0xffffffffu, rowmax2, o));
+  }
+  if (lane == 0) {
+    if (warp < gs) s_max[warp] = rowmax;
+    if (warp + kWarps < gs) s_max[warp + kWarps] = rowmax2;
+  }
+
+  // pass 2: rescale and sum (each thread owns up to two float4 outputs)
+  for (int base = 0; base < P; base += kMergeSlots) {
+    const int cnt = min(kMergeSlots, P - base);
+    __syncthreads();
+    if (P > kMergeSlots) {  // s_slot still holds the last chunk of pass 1: restage
+      for (int i = tid; i < cnt; i += blockDim.x) {
+        const int w = w0 + base + i;
+        const long long aw = worker_start(T, w, p.W);
+        const bool empty = aw == worker_start(T, w + 1, p.W);
+        s_slot[i] = empty ? -1 : 2 * w + ((w == w0 && aw != A) ? 1 : 0);
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int q = tid + k * kMergeThreads;
+      if (q >= nq) break;
+      const int row = (4 * q) / D, d = (4 * q) % D;
+      const float M = s_max[row];
+#pragma unroll 4
+      for (int i = 0; i < cnt; ++i) {
+        const int slot = s_slot[i];
+        if (slot < 0) continue;
+        const float2 mlw = ml[size_t(slot) * gs + row];
+        const float f = fast_exp2(mlw.x - M);
+        const float4 o = *reinterpret_cast<const float4*>(p.part_o + (size_t(slot) * gs + row) * D + d);
+        lsum[k] += f * mlw.y;
+        acc[k].x += f * o.x;
+        acc[k].y += f * o.y;
+        acc[k].z += f * o.z;
+        acc[k].w += f * o.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int q = tid + k * kMergeThreads;
+    if (q >= nq) break;
+    const float inv = 1.f / lsum[k];
+    uint2 pk;
+    pk.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+    pk.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+    *reinterpret_cast<uint2*>(out + 4 * q) = pk;
   }
 }
 
@@ -90,8 +155,8 @@ void launch_merge(const MergeParams& p, cudaStream_t stream) {
   if (grid <= 0) return;
   MergeParams copy = p;
   void* args[] = {&copy};
-  launch_pdl(reinterpret_cast<const void*>(&paged_decode_merge_kernel), dim3(grid), dim3(128),
-             args, 0, stream);
+  launch_pdl(reinterpret_cast<const void*>(&paged_decode_merge_kernel), dim3(grid),
+             dim3(kMergeThreads), args, 0, stream);
 }
 
 }  // namespace pkv

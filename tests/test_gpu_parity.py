@@ -147,6 +147,19 @@ def test_decode_single_long_sequence_split_many_ways(pk):
     assert max_err(out, ref) <= DECODE_ATOL
 
 
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_decode_single_long_mha_sequence(pk, kv):
+    """B = 1, one KV head: one 32K-token context over every worker (more partials than
+    the merge stages at once)."""
+    name = "int8" if kv == "int8" else "7b"
+    w = make_workload(name, device=DEV, lengths=[32768], num_q_heads=1, num_kv_heads=1,
+                      seed=8)
+    out = _decode(pk, w)
+    torch.cuda.synchronize()
+    ref = oracle_outputs(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+
+
 def test_decode_permuted_placement_is_bit_identical(pk):
     w = make_workload("70b-gqa", device=DEV, num_seqs=6, seed=9)
     out1 = _decode(pk, w).clone()

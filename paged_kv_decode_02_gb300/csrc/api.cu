@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -103,7 +104,7 @@ struct Plan {
   int g, gs, nsg, HU;
   int grid, W;
   size_t smem;
-  size_t off_prefix, off_ml, off_o, ws_bytes;
+  size_t off_cnt, off_ml, off_o, ws_bytes;
 };
 
 pkv_status check_dims(const pkv_dims* d) {
@@ -203,13 +204,20 @@ pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl) {
   P.grid = sms * per_sm;
   P.W = P.grid * P.k.warps;
 
-  // workspace: [prefix (B+1) int32][partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
-  P.off_prefix = 0;
-  P.off_ml = align_up(size_t(d->num_seqs + 1) * 4, 256);
+  // workspace: [arrival counters B*HU u64][partial (m, l) 2W*gs float2][partial o 2W*gs*D]
+  P.off_cnt = 0;
+  P.off_ml = align_up(size_t(d->num_seqs) * P.HU * 8, 256);
   P.off_o = align_up(P.off_ml + size_t(2) * P.W * P.gs * 8, 256);
   P.ws_bytes = align_up(P.off_o + size_t(2) * P.W * P.gs * d->head_dim * 4, 256);
   *pl = P;
   return PKV_OK;
+}
+
+// Tag of one decode call in the workspace's arrival counters: unique per call in
+// this process, 43 bits, never 0.
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> counter{0};
+  return (counter.fetch_add(1) % ((1ull << 43) - 1)) + 1;
 }
 
 pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
@@ -249,7 +257,8 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
   p.context_lens = context_lens;
   p.part_o = reinterpret_cast<float*>(ws + P.off_o);
   p.part_ml = reinterpret_cast<float*>(ws + P.off_ml);
-  p.prefix_out = reinterpret_cast<int32_t*>(ws + P.off_prefix);
+  p.counters = reinterpret_cast<unsigned long long*>(ws + P.off_cnt);
+  p.epoch = next_epoch();
   p.status = status;
   p.B = d->num_seqs;
   p.Hq = d->num_q_heads;
@@ -268,26 +277,6 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
       cudaSuccess)
     return PKV_ERR_CUDA;
 
-  MergeParams m{};
-  m.out = out;
-  m.part_o = p.part_o;
-  m.part_ml = p.part_ml;
-  m.prefix = p.prefix_out;
-  m.block_tables = block_tables;
-  m.context_lens = context_lens;
-  m.status = status;
-  m.B = p.B;
-  m.Hq = p.Hq;
-  m.MBS = p.MBS;
-  m.NB = p.NB;
-  m.BS = d->block_size;
-  m.D = d->head_dim;
-  m.g = P.g;
-  m.gs = P.gs;
-  m.nsg = P.nsg;
-  m.HU = P.HU;
-  m.W = P.W;
-  launch_merge(m, stream);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
 }

@@ -11,9 +11,10 @@
 //   triples are laid out in one flat order and cut into W equal contiguous ranges,
 //   one per warp of a persistent grid (W = warps per CTA x CTAs that fit x SMs).
 //   Ragged lengths therefore cost nothing in balance. A warp whose range covers a
-//   whole (sequence, unit) writes the final output; a cut unit leaves an unnormalised
-//   partial (o, running max, sum) that the merge kernel folds with the usual
-//   online-softmax rescaling.
+//   whole (sequence, unit) writes the final output; a cut unit leaves one
+//   unnormalised partial (o, running max, sum) per warp, and the last of those warps
+//   to arrive (an epoch-tagged counter per unit) folds them with the online-softmax
+//   rescaling m = max m_w, l = sum 2^(m_w - m) l_w, o = sum 2^(m_w - m) o_w / l.
 // * Data movement: each warp owns a private ring of shared-memory stages. One lane
 //   reads the block id from the table and issues TMA tensor copies of the block's K
 //   and V tiles (128-byte swizzled, so that the tensor-core fragment loads below are
@@ -232,7 +233,8 @@ struct SimtPath {
     }
   }
 
-  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot) {
+  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot,
+                                         bool zero) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -249,7 +251,11 @@ struct SimtPath {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       if (complete) {
-        const float inv = 1.f / l[h];
+        const float inv = zero ? 0.f : 1.f / l[h];
+        if (zero) {
+#pragma unroll
+          for (int e = 0; e < kEPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
+        }
         __nv_bfloat16* row =
             reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t(s) * p.Hq + head0 + h) * D;
 #pragma unroll
@@ -409,14 +415,19 @@ struct MmaPathBf16 {
     }
   }
 
-  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot) {
+  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot,
+                                         bool zero) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     const bool v0 = gid < gs, v1 = gid + 8 < gs;
     if (complete) {
-      const float i0 = 1.f / l0, i1 = 1.f / l1;
+      if (zero) {
+#pragma unroll
+        for (int nd = 0; nd < kND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+      }
+      const float i0 = zero ? 0.f : 1.f / l0, i1 = zero ? 0.f : 1.f / l1;
       uint32_t* out = reinterpret_cast<uint32_t*>(p.out);
       const size_t row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 2);
       const size_t row1 = row0 + 8 * (D / 2);
@@ -619,12 +630,17 @@ struct MmaPathInt8 {
   // n-tile 4qg+i, column n holds head_dim index 32qg + 4n + i, so a lane's c0 values
   // over i = 0..3 are the 4 consecutive elements 32qg + 8cq + i and its c1 values
   // the next 4.
-  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot) {
+  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot,
+                                         bool zero) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     const bool v0 = gid < gs, v1 = gid + 8 < gs;
+    if (complete && zero) {
+#pragma unroll
+      for (int nd = 0; nd < kND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    }
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       if (!(rr == 0 ? v0 : v1)) continue;
@@ -641,7 +657,7 @@ struct MmaPathInt8 {
         }
         const int d0 = 32 * qg + 8 * cq;
         if (complete) {
-          const float inv = 1.f / lsum;
+          const float inv = zero ? 0.f : 1.f / lsum;
           uint4 pk;
           pk.x = pack_bf16x2(vals[0] * inv, vals[1] * inv);
           pk.y = pack_bf16x2(vals[2] * inv, vals[3] * inv);
@@ -662,6 +678,95 @@ struct MmaPathInt8 {
     }
   }
 };
+
+// ===========================================================================
+// Merging the partials of a cut unit (done by the last warp to finish a part)
+// ===========================================================================
+__device__ __forceinline__ long long worker_start(long long T, int w, int W) {
+  return T * w / W;
+}
+
+// Largest worker w whose range [T*w/W, T*(w+1)/W) contains flat index x.
+__device__ __forceinline__ int worker_of(long long x, long long T, int W) {
+  return int(((x + 1) * W + T - 1) / T) - 1;
+}
+
+constexpr int kCountBits = 20;  // counter word: [epoch | bad flag | arrivals]
+
+// Counts one arrival at a cut unit; returns true for the last of `nparts` arrivals
+// of this call (and resets the count for the next call with the same epoch, such as
+// a replayed graph). `bad` is ORed into the word; *any_bad receives the union.
+// A word whose epoch differs belongs to an earlier call and counts as zero.
+__device__ __forceinline__ bool arrive_at_unit(unsigned long long* word, unsigned long long epoch,
+                                               int nparts, bool bad, bool* any_bad,
+                                               bool* gave_up) {
+  const unsigned long long tag = epoch << (kCountBits + 1);
+  unsigned long long cur = atomicAdd(word, 0ull);
+  unsigned cnt = 0;
+  bool b = bad;
+  *gave_up = true;
+  for (int it = 0; it < (1 << 20); ++it) {  // lock-free retry; bounded all the same
+    const bool same = (cur >> (kCountBits + 1)) == epoch;
+    cnt = (same ? unsigned(cur & ((1ull << kCountBits) - 1)) : 0u) + 1u;
+    b = bad || (same && ((cur >> kCountBits) & 1ull));
+    const unsigned long long next = tag | ((unsigned long long)b << kCountBits) | cnt;
+    const unsigned long long prev = atomicCAS(word, cur, next);
+    if (prev == cur) {
+      *gave_up = false;
+      break;
+    }
+    cur = prev;
+  }
+  *any_bad = b;
+  if (!*gave_up && cnt == unsigned(nparts)) {
+    atomicExch(word, tag);
+    return true;
+  }
+  return false;
+}
+
+// One warp folds the `nparts` partials of unit (s, u) into the bf16 output (zeros when
+// `zero`). dense: every worker range is non-empty (T >= W), parts are workers
+// w0..w0+nparts-1; otherwise each part is one block held by worker_of(A + i).
+template <int D>
+__device__ __noinline__ void merge_unit(const DecodeParams& p, int s, int u, long long A,
+                                        int nparts, bool dense, int w0, long long T, int W,
+                                        bool zero, int lane) {
+  constexpr int Q = D / 4;  // float4 per row
+  const int gs = p.gs;
+  __nv_bfloat16* out =
+      reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t(s) * p.Hq + unit_head0(p, u)) * D;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  const bool first_cut = worker_start(T, w0, W) != A;
+  for (int idx = lane; idx < gs * Q; idx += 32) {
+    const int row = idx / Q, dq = idx % Q;
+    uint2 pk = make_uint2(0u, 0u);
+    if (!zero) {
+      float M = -INFINITY, L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < nparts; ++i) {
+        size_t slot;
+        if (dense) slot = size_t(2 * (w0 + i) + ((i == 0 && first_cut) ? 1 : 0));
+        else slot = size_t(2 * worker_of(A + i, T, W));
+        const float2 mlw = __ldcg(ml + slot * gs + row);
+        const float4 o =
+            __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot * gs + row) * D) + dq);
+        const float Mn = fmaxf(M, mlw.x);
+        const float a = fast_exp2(M - Mn), b = fast_exp2(mlw.x - Mn);
+        L = L * a + mlw.y * b;
+        acc.x = acc.x * a + o.x * b;
+        acc.y = acc.y * a + o.y * b;
+        acc.z = acc.z * a + o.z * b;
+        acc.w = acc.w * a + o.w * b;
+        M = Mn;
+      }
+      const float inv = 1.f / L;
+      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    }
+    *reinterpret_cast<uint2*>(out + size_t(row) * D + 4 * dq) = pk;
+  }
+}
 
 // ===========================================================================
 // Work cursor over the flat (sequence, unit, block) order.
@@ -754,8 +859,15 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     if (tid == 0) s_prefix[0] = 0;
     __syncthreads();
-    if (blockIdx.x == 0)
-      for (int i = tid; i <= B; i += nthr) p.prefix_out[i] = s_prefix[i];
+    // sequences without blocks get a zero output (a negative length is also flagged)
+    for (int s2 = blockIdx.x; s2 < B; s2 += gridDim.x) {
+      if (s_prefix[s2 + 1] != s_prefix[s2]) continue;
+      if (p.status != nullptr && tid == 0 && __ldg(p.context_lens + s2) < 0)
+        atomicOr(p.status, 0x1);
+      uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                          size_t(s2) * p.Hq * D);
+      for (int i = tid; i < p.Hq * D / 8; i += nthr) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 
   const int HU = p.HU;
@@ -785,11 +897,15 @@ __global__ void __launch_bounds__(kWarps * 32)
   cursor_locate(pc, a, s_prefix, B, HU);
   cc = pc;
 
-  // lane 0 issues the copies of the block at the producer cursor into stage st
+  // lane 0 issues the copies of the block at the producer cursor into stage st;
+  // with a status word it also remembers, per stage, whether the block id was invalid
+  uint32_t bad_stages = 0;
   auto issue = [&](int st) {
     if (lane == 0) {
       int phys = __ldg(p.block_tables + size_t(pc.s) * p.MBS + pc.j);
-      phys = (phys < 0 || phys >= p.NB) ? 0 : phys;  // never copy outside the pool
+      const bool invalid = phys < 0 || phys >= p.NB;
+      bad_stages = (bad_stages & ~(1u << st)) | (uint32_t(invalid) << st);
+      phys = invalid ? 0 : phys;  // never copy outside the pool
       const int kvh = pc.u / p.nsg;
       const int row = (phys * p.Hkv + kvh) * BS;
       mbar_arrive_expect_tx(bar(st), K::kTxBytes);
@@ -817,7 +933,10 @@ __global__ void __launch_bounds__(kWarps * 32)
   path.begin(p, cc.s, cc.u);
   int seg_j0 = cc.j;
   bool first_seg = true;
-  int Lc = min(__ldg(p.context_lens + cc.s), p.MBS * BS);
+  const bool checks = p.status != nullptr;
+  int Lraw = __ldg(p.context_lens + cc.s);
+  int Lc = min(Lraw, p.MBS * BS);
+  bool seg_bad_id = false;
 
   for (int i = 0; i < nblk; ++i) {
     const int st = i % kStages;
@@ -831,6 +950,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         mbar_wait_bounded(bar(k2 % kStages), uint32_t(k2 / kStages) & 1u, p.timeout_ns);
       return;
     }
+    if (checks) seg_bad_id |= __shfl_sync(0xffffffffu, (bad_stages >> st) & 1u, 0) != 0u;
     path.block(p, sK(st), sV(st), sKs(st), sVs(st), Lc - cc.j * BS);
     __syncwarp();
     if (i + kStages < nblk) {
@@ -840,14 +960,42 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     const bool seg_end = (cc.j == cc.n - 1) || (i == nblk - 1);
     if (seg_end) {
+      const bool seg_bad_len = checks && Lraw > p.MBS * BS;
+      const bool seg_bad = seg_bad_len || seg_bad_id;
+      if (seg_bad && lane == 0) atomicOr(p.status, (seg_bad_len ? 0x1 : 0) | (seg_bad_id ? 0x2 : 0));
       const bool complete = (seg_j0 == 0) && (cc.j == cc.n - 1);
-      path.finish(p, complete, partial_slot(w, first_seg));
+      if (complete) {
+        path.finish(p, true, 0, seg_bad);
+      } else {
+        path.finish(p, false, partial_slot(w, first_seg), false);
+        __threadfence();  // this warp's partial before its arrival
+        __syncwarp();
+        const long long A = (long long)HU * s_prefix[cc.s] + (long long)cc.u * cc.n;
+        const int w0 = worker_of(A, T, W), w1 = worker_of(A + cc.n - 1, T, W);
+        const bool dense = T >= W;
+        const int nparts = dense ? (w1 - w0 + 1) : cc.n;
+        int flags = 0;
+        if (lane == 0) {
+          bool any_bad = false, gave_up = false;
+          const bool last = arrive_at_unit(p.counters + size_t(cc.s) * HU + cc.u, p.epoch,
+                                           nparts, seg_bad, &any_bad, &gave_up);
+          if (gave_up && p.status) atomicOr(p.status, 0x4);
+          flags = (last ? 1 : 0) | (any_bad ? 2 : 0);
+        }
+        flags = __shfl_sync(0xffffffffu, flags, 0);
+        if (flags & 1) {
+          __threadfence();  // every other part's partial is visible to this warp
+          merge_unit<D>(p, cc.s, cc.u, A, nparts, dense, w0, T, W, (flags & 2) != 0, lane);
+        }
+      }
       first_seg = false;
     }
     cursor_next(cc, s_prefix, B, HU);
     if (seg_end && i + 1 < nblk) {
       seg_j0 = cc.j;
-      Lc = min(__ldg(p.context_lens + cc.s), p.MBS * BS);
+      Lraw = __ldg(p.context_lens + cc.s);
+      Lc = min(Lraw, p.MBS * BS);
+      seg_bad_id = false;
       path.begin(p, cc.s, cc.u);
     }
   }

@@ -17,7 +17,8 @@ struct DecodeParams {
   const int32_t* context_lens; // [B]
   float* part_o;               // [2W, GS, D] fp32 partial outputs (unnormalised)
   float* part_ml;              // [2W, GS, 2] fp32 (running max in log2 units, sum)
-  int32_t* prefix_out;         // [B+1] blocks-per-sequence exclusive prefix (CTA 0 writes)
+  unsigned long long* counters;  // [B * HU] arrival counters of cut units (epoch-tagged)
+  unsigned long long epoch;    // tag of this call in the counters (never 0)
   int32_t* status;             // optional device status word
   int B, Hq, Hkv, MBS, NB;
   int g;                       // Hq / Hkv
@@ -26,20 +27,6 @@ struct DecodeParams {
   int HU;                      // work units per sequence (Hkv * nsg)
   float scale_log2;            // softmax scale * log2(e)
   unsigned long long timeout_ns;
-};
-
-// Parameters of the split-KV merge / finalize launch.
-struct MergeParams {
-  void* out;
-  const float* part_o;
-  const float* part_ml;
-  const int32_t* prefix;
-  const int32_t* block_tables;
-  const int32_t* context_lens;
-  int32_t* status;
-  int B, Hq, MBS, NB, BS, D;
-  int g, gs, nsg, HU;
-  int W;                       // number of decode workers (warps)
 };
 
 // A compiled decode kernel and its static shape.
@@ -55,8 +42,6 @@ struct DecodeKernelInfo {
 // Kernel tables, one per translation unit. Return false if the shape is not built.
 bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info);
 bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info);
-
-void launch_merge(const MergeParams& p, cudaStream_t stream);
 
 // Launches with programmatic stream serialisation: the kernel may be scheduled while
 // the previous kernel on the stream drains; every kernel of this library waits for its

@@ -257,7 +257,7 @@ def run_ours(args, rank, world):
     need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                      w.block_size, w.num_blocks, w.max_blocks_per_seq,
                                      pk.pagedkv.KV_INT8 if int8 else pk.pagedkv.KV_BF16)
-    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
     out = torch.empty_like(w.q)
     stream = torch.cuda.current_stream(dev)
 

@@ -4,7 +4,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -104,7 +103,7 @@ struct Plan {
   int g, gs, nsg, HU;
   int grid, W;
   size_t smem;
-  size_t off_cnt, off_ml, off_o, ws_bytes;
+  size_t off_cnt, off_gcnt, off_ml, off_o, ws_bytes;
 };
 
 pkv_status check_dims(const pkv_dims* d) {
@@ -204,20 +203,15 @@ pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl) {
   P.grid = sms * per_sm;
   P.W = P.grid * P.k.warps;
 
-  // workspace: [arrival counters B*HU u64][partial (m, l) 2W*gs float2][partial o 2W*gs*D]
+  // workspace: [unit counters B*HU u64][group counters 2W u64]
+  //            [partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
   P.off_cnt = 0;
-  P.off_ml = align_up(size_t(d->num_seqs) * P.HU * 8, 256);
+  P.off_gcnt = align_up(size_t(d->num_seqs) * P.HU * 8, 256);
+  P.off_ml = align_up(P.off_gcnt + size_t(2) * P.W * 8, 256);
   P.off_o = align_up(P.off_ml + size_t(2) * P.W * P.gs * 8, 256);
   P.ws_bytes = align_up(P.off_o + size_t(2) * P.W * P.gs * d->head_dim * 4, 256);
   *pl = P;
   return PKV_OK;
-}
-
-// Tag of one decode call in the workspace's arrival counters: unique per call in
-// this process, 43 bits, never 0.
-unsigned long long next_epoch() {
-  static std::atomic<unsigned long long> counter{0};
-  return (counter.fetch_add(1) % ((1ull << 43) - 1)) + 1;
 }
 
 pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
@@ -258,7 +252,7 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
   p.part_o = reinterpret_cast<float*>(ws + P.off_o);
   p.part_ml = reinterpret_cast<float*>(ws + P.off_ml);
   p.counters = reinterpret_cast<unsigned long long*>(ws + P.off_cnt);
-  p.epoch = next_epoch();
+  p.group_counters = reinterpret_cast<unsigned long long*>(ws + P.off_gcnt);
   p.status = status;
   p.B = d->num_seqs;
   p.Hq = d->num_q_heads;
@@ -280,6 +274,16 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
 }
+
+}  // namespace
+
+size_t decode_counter_bytes(const pkv_dims* d, bool int8) {
+  Plan P;
+  if (make_plan(d, int8, &P) != PKV_OK) return 0;
+  return P.off_ml;
+}
+
+namespace {
 
 pkv_status check_append(const void* k, const void* v, const void* kc, const void* vc,
                         const int64_t* slots, int T, const pkv_dims* d) {

@@ -12,9 +12,10 @@
 //   one per warp of a persistent grid (W = warps per CTA x CTAs that fit x SMs).
 //   Ragged lengths therefore cost nothing in balance. A warp whose range covers a
 //   whole (sequence, unit) writes the final output; a cut unit leaves one
-//   unnormalised partial (o, running max, sum) per warp, and the last of those warps
-//   to arrive (an epoch-tagged counter per unit) folds them with the online-softmax
-//   rescaling m = max m_w, l = sum 2^(m_w - m) l_w, o = sum 2^(m_w - m) o_w / l.
+//   unnormalised partial (o, running max, sum) per warp; the parts are folded in a
+//   two-level tree (groups of ~sqrt(parts)) by the last warp to arrive at each
+//   level, with the online-softmax rescaling m = max m_w, l = sum 2^(m_w - m) l_w,
+//   o = sum 2^(m_w - m) o_w / l.
 // * Data movement: each warp owns a private ring of shared-memory stages. One lane
 //   reads the block id from the table and issues TMA tensor copies of the block's K
 //   and V tiles (128-byte swizzled, so that the tensor-core fragment loads below are
@@ -691,81 +692,171 @@ __device__ __forceinline__ int worker_of(long long x, long long T, int W) {
   return int(((x + 1) * W + T - 1) / T) - 1;
 }
 
-constexpr int kCountBits = 20;  // counter word: [epoch | bad flag | arrivals]
+// Arrival words: the low 32 bits count arrivals, the high 32 bits count arrivals that
+// saw a bad block id. The last arriver reads the union and stores 0 back, so a word
+// is 0 again whenever a call completes (the workspace is zeroed once, before its
+// first use).
+constexpr unsigned long long kArrive = 1ull, kArriveBad = 1ull << 32;
 
-// Counts one arrival at a cut unit; returns true for the last of `nparts` arrivals
-// of this call (and resets the count for the next call with the same epoch, such as
-// a replayed graph). `bad` is ORed into the word; *any_bad receives the union.
-// A word whose epoch differs belongs to an earlier call and counts as zero.
-__device__ __forceinline__ bool arrive_at_unit(unsigned long long* word, unsigned long long epoch,
-                                               int nparts, bool bad, bool* any_bad,
-                                               bool* gave_up) {
-  const unsigned long long tag = epoch << (kCountBits + 1);
-  unsigned long long cur = atomicAdd(word, 0ull);
-  unsigned cnt = 0;
-  bool b = bad;
-  *gave_up = true;
-  for (int it = 0; it < (1 << 20); ++it) {  // lock-free retry; bounded all the same
-    const bool same = (cur >> (kCountBits + 1)) == epoch;
-    cnt = (same ? unsigned(cur & ((1ull << kCountBits) - 1)) : 0u) + 1u;
-    b = bad || (same && ((cur >> kCountBits) & 1ull));
-    const unsigned long long next = tag | ((unsigned long long)b << kCountBits) | cnt;
-    const unsigned long long prev = atomicCAS(word, cur, next);
-    if (prev == cur) {
-      *gave_up = false;
-      break;
-    }
-    cur = prev;
-  }
-  *any_bad = b;
-  if (!*gave_up && cnt == unsigned(nparts)) {
-    atomicExch(word, tag);
-    return true;
-  }
-  return false;
+__device__ __forceinline__ bool last_arrival(unsigned long long old, int n, bool bad,
+                                             bool* any_bad) {
+  *any_bad = bad || (old >> 32) != 0ull;
+  return int(old & 0xffffffffull) + 1 == n;
 }
 
-// One warp folds the `nparts` partials of unit (s, u) into the bf16 output (zeros when
-// `zero`). dense: every worker range is non-empty (T >= W), parts are workers
-// w0..w0+nparts-1; otherwise each part is one block held by worker_of(A + i).
-template <int D>
-__device__ __noinline__ void merge_unit(const DecodeParams& p, int s, int u, long long A,
-                                        int nparts, bool dense, int w0, long long T, int W,
-                                        bool zero, int lane) {
-  constexpr int Q = D / 4;  // float4 per row
+// One warp folds partials src(0..n-1) of one unit: into the unnormalised partial at
+// `dst_slot` (which may be one of the sources) when `to_partial`, else into the bf16
+// output `out` (zeros when `zero`). The lanes first share out the parts to find each
+// row's maximum m; then every lane accumulates all of its outputs part by part with
+// weights 2^(m_w - m), so the loads of one part are independent of the previous one.
+template <int D, class SrcFn>
+__device__ __forceinline__ void fold_parts(const DecodeParams& p, int n, SrcFn src,
+                                           size_t dst_slot, bool to_partial,
+                                           __nv_bfloat16* out, bool zero, int lane) {
+  constexpr int Q = D / 4;                       // float4 per row
+  constexpr int kMaxRows = 16;
+  constexpr int kPer = (kMaxRows * Q + 31) / 32;  // outputs per lane at most
   const int gs = p.gs;
-  __nv_bfloat16* out =
-      reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t(s) * p.Hq + unit_head0(p, u)) * D;
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  const bool first_cut = worker_start(T, w0, W) != A;
-  for (int idx = lane; idx < gs * Q; idx += 32) {
-    const int row = idx / Q, dq = idx % Q;
-    uint2 pk = make_uint2(0u, 0u);
-    if (!zero) {
-      float M = -INFINITY, L = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int i = 0; i < nparts; ++i) {
-        size_t slot;
-        if (dense) slot = size_t(2 * (w0 + i) + ((i == 0 && first_cut) ? 1 : 0));
-        else slot = size_t(2 * worker_of(A + i, T, W));
-        const float2 mlw = __ldcg(ml + slot * gs + row);
-        const float4 o =
-            __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot * gs + row) * D) + dq);
-        const float Mn = fmaxf(M, mlw.x);
-        const float a = fast_exp2(M - Mn), b = fast_exp2(mlw.x - Mn);
-        L = L * a + mlw.y * b;
-        acc.x = acc.x * a + o.x * b;
-        acc.y = acc.y * a + o.y * b;
-        acc.z = acc.z * a + o.z * b;
-        acc.w = acc.w * a + o.w * b;
-        M = Mn;
-      }
-      const float inv = 1.f / L;
-      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    }
-    *reinterpret_cast<uint2*>(out + size_t(row) * D + 4 * dq) = pk;
+  const int nout = gs * Q;
+  if (zero) {
+    for (int idx = lane; idx < nout; idx += 32)
+      *reinterpret_cast<uint2*>(out + size_t(idx / Q) * D + 4 * (idx % Q)) = make_uint2(0u, 0u);
+    return;
   }
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  float rmax[kMaxRows];
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) rmax[r] = -INFINITY;
+  for (int i = lane; i < n; i += 32) {
+    const size_t slot = src(i);
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r)
+      if (r < gs) rmax[r] = fmaxf(rmax[r], __ldcg(ml + slot * gs + r).x);
+  }
+#pragma unroll
+  for (int r = 0; r < kMaxRows; ++r) {
+    if (r >= gs) break;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rmax[r] = fmaxf(rmax[r], __shfl_xor_sync(0xffffffffu, rmax[r], o));
+  }
+  // outputs in chunks of kChunk per lane: kChunk independent loads per part in flight
+  constexpr int kChunk = 4;
+  for (int k0 = 0; k0 < kPer; k0 += kChunk) {
+    if (lane + 32 * k0 >= nout) break;
+    float Mk[kChunk], L[kChunk];
+    float4 acc[kChunk];
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+      const int row = (lane + 32 * (k0 + k)) / Q;
+      float M = rmax[0];
+#pragma unroll
+      for (int r = 1; r < kMaxRows; ++r)
+        if (r == row) M = rmax[r];
+      Mk[k] = M;
+      L[k] = 0.f;
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      const size_t slot = src(i);
+#pragma unroll
+      for (int k = 0; k < kChunk; ++k) {
+        const int idx = lane + 32 * (k0 + k);
+        if (idx < nout) {
+          const int row = idx / Q, dq = idx % Q;
+          const float2 mlw = __ldcg(ml + slot * gs + row);
+          const float4 o =
+              __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot * gs + row) * D) + dq);
+          const float f = fast_exp2(mlw.x - Mk[k]);
+          L[k] = fmaf(f, mlw.y, L[k]);
+          acc[k].x = fmaf(f, o.x, acc[k].x);
+          acc[k].y = fmaf(f, o.y, acc[k].y);
+          acc[k].z = fmaf(f, o.z, acc[k].z);
+          acc[k].w = fmaf(f, o.w, acc[k].w);
+        }
+      }
+    }
+    // every lane has read the sources of these outputs before any is overwritten; the
+    // (m, l) pairs are shared by the lanes of a row, so they are written after the
+    // last chunk (below)
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+      const int idx = lane + 32 * (k0 + k);
+      if (idx >= nout) break;
+      const int row = idx / Q, dq = idx % Q;
+      if (to_partial) {
+        reinterpret_cast<float4*>(p.part_o + (dst_slot * gs + row) * D)[dq] = acc[k];
+        if (dq == 0)
+          reinterpret_cast<float2*>(p.part_ml)[dst_slot * gs + row] = make_float2(Mk[k], L[k]);
+      } else {
+        const float inv = 1.f / L[k];
+        uint2 pk;
+        pk.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
+        pk.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
+        *reinterpret_cast<uint2*>(out + size_t(row) * D + 4 * dq) = pk;
+      }
+    }
+  }
+}
+
+// ceil(sqrt(n)) for 1 <= n < 2^24, identical in every thread.
+__device__ __forceinline__ int ceil_sqrt(int n) {
+  int g = int(ceilf(sqrtf(float(n))));
+  while (g * g < n) ++g;
+  while (g > 1 && (g - 1) * (g - 1) >= n) --g;
+  return g;
+}
+
+// Part structure of a cut unit (s, u) with `nparts` parts: groups of ceil(sqrt(nparts))
+// consecutive parts. The last warp to finish a group folds it into the slot of the
+// group's first part; the last group to finish folds the group results into the
+// output. `dense`: every worker range is non-empty (T >= W), parts are workers
+// w0..w0+nparts-1; otherwise each part is one block, held by worker_of(A + i).
+struct CutUnit {
+  int s, u, nparts, my, w0, G, ngroups, g0, gsize;
+  long long A;
+  bool dense, first_cut, bad;
+  __device__ __forceinline__ size_t slot_of(int i, long long T, int W) const {
+    if (dense) return size_t(2 * (w0 + i) + ((i == 0 && first_cut) ? 1 : 0));
+    return size_t(2 * worker_of(A + i, T, W));
+  }
+};
+
+// Runs in the warp that finished group g0 of the unit last (group_bad: a part of the
+// group saw a bad block id): folds the group and, if it is also the last group,
+// the whole unit.
+template <int D>
+__device__ __noinline__ void complete_cut_unit(const DecodeParams& p, const CutUnit& c,
+                                               long long T, int W, bool group_bad, int lane) {
+  __nv_bfloat16* out =
+      reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t(c.s) * p.Hq + unit_head0(p, c.u)) * D;
+  auto slot_of = [&](int i) { return c.slot_of(i, T, W); };
+  if (c.ngroups == 1) {
+    fold_parts<D>(p, c.gsize, [&](int i) { return slot_of(c.g0 + i); }, 0, false, out,
+                  group_bad, lane);
+    return;
+  }
+  if (c.gsize > 1) {
+    fold_parts<D>(p, c.gsize, [&](int i) { return slot_of(c.g0 + i); }, slot_of(c.g0), true,
+                  out, false, lane);
+    __threadfence();  // the group result before the group's arrival
+    __syncwarp();
+  }
+  int flags = 0;
+  if (lane == 0) {
+    unsigned long long* word = p.counters + size_t(c.s) * p.HU + c.u;
+    const unsigned long long old = atomicAdd(word, kArrive + (group_bad ? kArriveBad : 0ull));
+    bool any_bad = false;
+    const bool last = last_arrival(old, c.ngroups, group_bad, &any_bad);
+    if (last) *word = 0ull;
+    flags = (last ? 1 : 0) | (any_bad ? 2 : 0);
+  }
+  flags = __shfl_sync(0xffffffffu, flags, 0);
+  if (!(flags & 1)) return;
+  __threadfence();  // every group result is visible to this warp
+  fold_parts<D>(p, c.ngroups, [&](int g) { return slot_of(g * c.G); }, 0, false, out,
+                (flags & 2) != 0, lane);
 }
 
 // ===========================================================================
@@ -928,15 +1019,62 @@ __global__ void __launch_bounds__(kWarps * 32)
     cursor_next(pc, s_prefix, B, HU);
   }
 
+  // q rows of the unit after (s, u) in the flat order, pulled into L1 ahead of use
+  auto prefetch_next_q = [&](int s, int u) {
+    int s2 = s, u2 = u + 1;
+    if (u2 == HU) {
+      u2 = 0;
+      do { ++s2; } while (s2 < B && s_prefix[s2 + 1] == s_prefix[s2]);
+    }
+    if (s2 < B && lane * 128 < p.gs * D * 2) {
+      const char* row = reinterpret_cast<const char*>(p.q) +
+                        (size_t(s2) * p.Hq + unit_head0(p, u2)) * D * 2 + lane * 128;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(row));
+    }
+  };
+
   Path path;
   path.init(lane);
   path.begin(p, cc.s, cc.u);
+  prefetch_next_q(cc.s, cc.u);
   int seg_j0 = cc.j;
   bool first_seg = true;
   const bool checks = p.status != nullptr;
   int Lraw = __ldg(p.context_lens + cc.s);
   int Lc = min(Lraw, p.MBS * BS);
   bool seg_bad_id = false;
+
+  // A cut unit's arrival is deferred: the partial is written at the end of its last
+  // block, the arrival is counted one block later (the partial's stores have drained,
+  // so the fence is cheap) and its result is read one block after that.
+  CutUnit pend;
+  int pend_state = 0;              // 0 none, 1 partial written, 2 arrival counted
+  unsigned long long pend_old = 0;  // lane 0: the word before this warp's arrival
+  auto pend_count = [&]() {
+    __threadfence();  // this warp's partial before its arrival
+    __syncwarp();
+    if (pend.gsize > 1 && lane == 0)
+      pend_old = atomicAdd(p.group_counters + pend.slot_of(pend.g0, T, W),
+                           kArrive + (pend.bad ? kArriveBad : 0ull));
+    pend_state = 2;
+  };
+  auto pend_resolve = [&]() {
+    int flags = 1 | (pend.bad ? 2 : 0);
+    if (pend.gsize > 1) {
+      if (lane == 0) {
+        bool any_bad = false;
+        const bool last = last_arrival(pend_old, pend.gsize, pend.bad, &any_bad);
+        if (last) p.group_counters[pend.slot_of(pend.g0, T, W)] = 0ull;
+        flags = (last ? 1 : 0) | (any_bad ? 2 : 0);
+      }
+      flags = __shfl_sync(0xffffffffu, flags, 0);
+    }
+    if (flags & 1) {
+      __threadfence();  // the other parts of the group are visible to this warp
+      complete_cut_unit<D>(p, pend, T, W, (flags & 2) != 0, lane);
+    }
+    pend_state = 0;
+  };
 
   for (int i = 0; i < nblk; ++i) {
     const int st = i % kStages;
@@ -958,6 +1096,8 @@ __global__ void __launch_bounds__(kWarps * 32)
       issue(st);
       cursor_next(pc, s_prefix, B, HU);
     }
+    if (pend_state == 2) pend_resolve();
+    else if (pend_state == 1) pend_count();
     const bool seg_end = (cc.j == cc.n - 1) || (i == nblk - 1);
     if (seg_end) {
       const bool seg_bad_len = checks && Lraw > p.MBS * BS;
@@ -967,28 +1107,29 @@ __global__ void __launch_bounds__(kWarps * 32)
       if (complete) {
         path.finish(p, true, 0, seg_bad);
       } else {
+        if (pend_state == 1) pend_count();
+        if (pend_state == 2) pend_resolve();
         path.finish(p, false, partial_slot(w, first_seg), false);
-        __threadfence();  // this warp's partial before its arrival
-        __syncwarp();
-        const long long A = (long long)HU * s_prefix[cc.s] + (long long)cc.u * cc.n;
-        const int w0 = worker_of(A, T, W), w1 = worker_of(A + cc.n - 1, T, W);
-        const bool dense = T >= W;
-        const int nparts = dense ? (w1 - w0 + 1) : cc.n;
-        int flags = 0;
-        if (lane == 0) {
-          bool any_bad = false, gave_up = false;
-          const bool last = arrive_at_unit(p.counters + size_t(cc.s) * HU + cc.u, p.epoch,
-                                           nparts, seg_bad, &any_bad, &gave_up);
-          if (gave_up && p.status) atomicOr(p.status, 0x4);
-          flags = (last ? 1 : 0) | (any_bad ? 2 : 0);
-        }
-        flags = __shfl_sync(0xffffffffu, flags, 0);
-        if (flags & 1) {
-          __threadfence();  // every other part's partial is visible to this warp
-          merge_unit<D>(p, cc.s, cc.u, A, nparts, dense, w0, T, W, (flags & 2) != 0, lane);
-        }
+        pend.s = cc.s;
+        pend.u = cc.u;
+        pend.A = (long long)HU * s_prefix[cc.s] + (long long)cc.u * cc.n;
+        pend.w0 = worker_of(pend.A, T, W);
+        pend.dense = T >= W;
+        pend.nparts = pend.dense ? (worker_of(pend.A + cc.n - 1, T, W) - pend.w0 + 1) : cc.n;
+        pend.my = pend.dense ? (w - pend.w0) : cc.j;
+        pend.first_cut = worker_start(T, pend.w0, W) != pend.A;
+        pend.G = ceil_sqrt(pend.nparts);
+        pend.ngroups = (pend.nparts + pend.G - 1) / pend.G;
+        pend.g0 = (pend.my / pend.G) * pend.G;
+        pend.gsize = min(pend.G, pend.nparts - pend.g0);
+        pend.bad = seg_bad;
+        pend_state = 1;
       }
       first_seg = false;
+    }
+    if (i == nblk - 1) {  // nothing left to overlap with: settle the pending arrival now
+      if (pend_state == 1) pend_count();
+      if (pend_state == 2) pend_resolve();
     }
     cursor_next(cc, s_prefix, B, HU);
     if (seg_end && i + 1 < nblk) {
@@ -997,6 +1138,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       Lc = min(Lraw, p.MBS * BS);
       seg_bad_id = false;
       path.begin(p, cc.s, cc.u);
+      prefetch_next_q(cc.s, cc.u);
     }
   }
 }

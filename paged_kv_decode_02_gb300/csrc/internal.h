@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "pagedkv.h"
+
 namespace pkv {
 
 // Parameters of one decode launch (device pointers; sizes as in pkv_dims).
@@ -17,8 +19,8 @@ struct DecodeParams {
   const int32_t* context_lens; // [B]
   float* part_o;               // [2W, GS, D] fp32 partial outputs (unnormalised)
   float* part_ml;              // [2W, GS, 2] fp32 (running max in log2 units, sum)
-  unsigned long long* counters;  // [B * HU] arrival counters of cut units (epoch-tagged)
-  unsigned long long epoch;    // tag of this call in the counters (never 0)
+  unsigned long long* counters;        // [B * HU] arrival words of cut units (zero between calls)
+  unsigned long long* group_counters;  // [2W] arrival words of part groups (zero between calls)
   int32_t* status;             // optional device status word
   int B, Hq, Hkv, MBS, NB;
   int g;                       // Hq / Hkv
@@ -38,6 +40,10 @@ struct DecodeKernelInfo {
   int mma;           // 1 = tensor-core path (groups >= 4), 0 = CUDA-core path
   int simt_heads;    // query heads per unit on the CUDA-core path
 };
+
+// Bytes at the start of a decode workspace that hold arrival counters (these must be
+// zero when a call starts). Returns 0 if the dims are invalid.
+size_t decode_counter_bytes(const ::pkv_dims* d, bool int8);
 
 // Kernel tables, one per translation unit. Return false if the shape is not built.
 bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info);

@@ -22,9 +22,10 @@ def _declared_functions():
 def lib_path():
     from paged_kv_decode_02_gb300 import build_lib
     try:
-        return build_lib.build()
-    except RuntimeError as e:  # no nvcc on this machine
+        build_lib._nvcc()
+    except RuntimeError as e:  # no CUDA toolkit on this machine
         pytest.skip(str(e))
+    return build_lib.build()   # a compile error fails the test
 
 
 def test_header_declares_the_api():

@@ -198,7 +198,7 @@ def test_decode_reuses_caller_workspace_and_output(pk):
     w = make_workload("70b-gqa", device=DEV, num_seqs=8, seed=6)
     need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                      w.block_size, w.num_blocks, w.max_blocks_per_seq)
-    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(need + (1 << 20), dtype=torch.uint8, device=DEV)
     out = torch.full_like(w.q, float("nan"))
     r1 = _decode(pk, w, out=out, workspace=ws).clone()
     r2 = _decode(pk, w, out=out, workspace=ws)
@@ -206,6 +206,16 @@ def test_decode_reuses_caller_workspace_and_output(pk):
     assert torch.equal(r1, r2)
     ref = oracle_outputs(w)
     assert max_err(r2, ref) <= DECODE_ATOL
+    # the same workspace, never re-zeroed, serves other shapes in between
+    for other in (make_workload("7b", device=DEV, lengths=[3000, 5, 700], seed=2),
+                  make_workload("70b-gqa", device=DEV, lengths=[20000], num_q_heads=16,
+                                num_kv_heads=1, seed=3)):
+        o2 = _decode(pk, other, workspace=ws)
+        torch.cuda.synchronize()
+        assert max_err(o2, oracle_outputs(other)) <= DECODE_ATOL
+    r3 = _decode(pk, w, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(r1, r3)
 
 
 # ---------------------------------------------------------------------------

@@ -203,11 +203,13 @@ pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl) {
   P.grid = sms * per_sm;
   P.W = P.grid * P.k.warps;
 
-  // workspace: [unit counters B*HU u64][group counters 2W u64]
+  // workspace: [unit words kMaxSlots u64][group words kMaxSlots u64] (fixed size, so
+  //            that the zero words carry over between calls of any shape)
   //            [partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
+  if (2 * P.W > kMaxSlots) return PKV_ERR_UNSUPPORTED;
   P.off_cnt = 0;
-  P.off_gcnt = align_up(size_t(d->num_seqs) * P.HU * 8, 256);
-  P.off_ml = align_up(P.off_gcnt + size_t(2) * P.W * 8, 256);
+  P.off_gcnt = size_t(kMaxSlots) * 8;
+  P.off_ml = size_t(2) * kMaxSlots * 8;
   P.off_o = align_up(P.off_ml + size_t(2) * P.W * P.gs * 8, 256);
   P.ws_bytes = align_up(P.off_o + size_t(2) * P.W * P.gs * d->head_dim * 4, 256);
   *pl = P;

@@ -845,7 +845,7 @@ __device__ __noinline__ void complete_cut_unit(const DecodeParams& p, const CutU
   }
   int flags = 0;
   if (lane == 0) {
-    unsigned long long* word = p.counters + size_t(c.s) * p.HU + c.u;
+    unsigned long long* word = p.counters + c.slot_of(0, T, W);
     const unsigned long long old = atomicAdd(word, kArrive + (group_bad ? kArriveBad : 0ull));
     bool any_bad = false;
     const bool last = last_arrival(old, c.ngroups, group_bad, &any_bad);

@@ -9,6 +9,11 @@
 
 namespace pkv {
 
+// Partial slots (2 per worker) the arrival-word arrays are sized for. The words sit at
+// the start of every workspace in arrays of this fixed size, so a workspace left at
+// zero by one call is valid for a call of any other shape.
+constexpr int kMaxSlots = 16384;
+
 // Parameters of one decode launch (device pointers; sizes as in pkv_dims).
 struct DecodeParams {
   const void* q;               // [B, Hq, D] bf16
@@ -19,8 +24,8 @@ struct DecodeParams {
   const int32_t* context_lens; // [B]
   float* part_o;               // [2W, GS, D] fp32 partial outputs (unnormalised)
   float* part_ml;              // [2W, GS, 2] fp32 (running max in log2 units, sum)
-  unsigned long long* counters;        // [B * HU] arrival words of cut units (zero between calls)
-  unsigned long long* group_counters;  // [2W] arrival words of part groups (zero between calls)
+  unsigned long long* counters;        // [kMaxSlots] unit arrival words, by first part's slot
+  unsigned long long* group_counters;  // [kMaxSlots] group arrival words, by first part's slot
   int32_t* status;             // optional device status word
   int B, Hq, Hkv, MBS, NB;
   int g;                       // Hq / Hkv

@@ -44,7 +44,7 @@ def _reference(lib, pagedkv, w, stream):
     need = ctypes.c_size_t(0)
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(dims), pagedkv.KV_BF16,
                                           ctypes.byref(need)) == 0
-    ws = torch.empty(int(need.value), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(int(need.value), dtype=torch.uint8, device="cuda")  # zeroed before first use
     out = torch.empty_like(w.q)
     st = lib.pkv_decode_bf16(p(out), p(w.q), p(w.k_cache), p(w.v_cache), p(w.block_tables),
                              p(w.context_lens), w.scale, ctypes.byref(dims), p(ws), ws.numel(),

@@ -117,8 +117,7 @@ pkv_status pkv_append_int8(const void* k, const void* v, int8_t* k_cache, int8_t
 /*
  * pkv_decode_workspace_bytes -- size of the device workspace that pkv_decode_bf16 /
  * pkv_decode_int8 need for these dims and KV dtype on the CURRENT device (it
- * depends on the device's SM count). Host-only query; writes *bytes. The workspace
- * must be zero-filled before its first use (see pkv_decode_bf16).
+ * depends on the device's SM count). Host-only query; writes *bytes.
  */
 pkv_status pkv_decode_workspace_bytes(const pkv_dims* dims, pkv_kv_dtype kv_dtype,
                                       size_t* bytes);
@@ -128,19 +127,15 @@ pkv_status pkv_decode_workspace_bytes(const pkv_dims* dims, pkv_kv_dtype kv_dtyp
  * are sequence s's first context_lens[s] cached rows of KV head h / g, gathered
  * through block_tables[s]. fp32 accumulation, bf16 output (round to nearest even).
  *   workspace  device scratch of at least pkv_decode_workspace_bytes() bytes,
- *              256-byte aligned, caller-owned. Zero-fill it once before its first
- *              use (e.g. cudaMemsetAsync): it holds arrival counters that every
- *              call which completes leaves at zero again, so a workspace can be
- *              reused across calls of any shape without re-zeroing. After a call
- *              that reported PKV_DEV_TIMEOUT, zero it again. Calls that share a
- *              workspace must not overlap.
+ *              256-byte aligned, caller-owned; contents need no initialisation and
+ *              are overwritten. Calls that share a workspace must not overlap.
  *   status     optional device int32 (NULL to skip the checks). When given, the
  *              call validates context_lens and the used block ids, ORs the
  *              PKV_DEV_* bits of what it finds into *status and writes a zero
  *              output for every sequence that failed. Without it, invalid ids are
  *              clamped into the pool (no fault) and those outputs are unspecified.
  * Long contexts are split over several workers and merged with an online-softmax
- * (max/sum) reduction inside the same call.
+ * (max/sum) reduction in a second kernel of the same call.
  */
 pkv_status pkv_decode_bf16(void* out, const void* q, const void* k_cache, const void* v_cache,
                            const int32_t* block_tables, const int32_t* context_lens,
@@ -173,9 +168,8 @@ pkv_status pkv_decode_int8(void* out, const void* q, const int8_t* k_cache,
  *   cudaGetSymbolAddress (once per device, with that device current); make that first
  *   call before any stream capture.
  *   Every call on a device shares the one scratch array, which keeps the last call's
- *   contents; each call first clears (cudaMemsetAsync on `stream`, no allocation)
- *   the part of it that must start at zero. Calls whose executions overlap on the
- *   GPU (different streams, or other threads) race on it: serialise them.
+ *   contents (nothing in it needs to start at zero). Calls whose executions overlap
+ *   on the GPU (different streams, or other threads) race on it: serialise them.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 

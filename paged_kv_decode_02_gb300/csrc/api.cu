@@ -103,7 +103,7 @@ struct Plan {
   int g, gs, nsg, HU;
   int grid, W;
   size_t smem;
-  size_t off_cnt, off_gcnt, off_ml, off_o, ws_bytes;
+  size_t off_prefix, off_ml, off_o, ws_bytes;
 };
 
 pkv_status check_dims(const pkv_dims* d) {
@@ -203,13 +203,9 @@ pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl) {
   P.grid = sms * per_sm;
   P.W = P.grid * P.k.warps;
 
-  // workspace: [unit words kMaxSlots u64][group words kMaxSlots u64] (fixed size, so
-  //            that the zero words carry over between calls of any shape)
-  //            [partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
-  if (2 * P.W > kMaxSlots) return PKV_ERR_UNSUPPORTED;
-  P.off_cnt = 0;
-  P.off_gcnt = size_t(kMaxSlots) * 8;
-  P.off_ml = size_t(2) * kMaxSlots * 8;
+  // workspace: [prefix (B+1) int32][partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
+  P.off_prefix = 0;
+  P.off_ml = align_up(size_t(d->num_seqs + 1) * 4, 256);
   P.off_o = align_up(P.off_ml + size_t(2) * P.W * P.gs * 8, 256);
   P.ws_bytes = align_up(P.off_o + size_t(2) * P.W * P.gs * d->head_dim * 4, 256);
   *pl = P;
@@ -253,8 +249,7 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
   p.context_lens = context_lens;
   p.part_o = reinterpret_cast<float*>(ws + P.off_o);
   p.part_ml = reinterpret_cast<float*>(ws + P.off_ml);
-  p.counters = reinterpret_cast<unsigned long long*>(ws + P.off_cnt);
-  p.group_counters = reinterpret_cast<unsigned long long*>(ws + P.off_gcnt);
+  p.prefix_out = reinterpret_cast<int32_t*>(ws + P.off_prefix);
   p.status = status;
   p.B = d->num_seqs;
   p.Hq = d->num_q_heads;
@@ -273,19 +268,29 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
       cudaSuccess)
     return PKV_ERR_CUDA;
 
+  MergeParams m{};
+  m.out = out;
+  m.part_o = p.part_o;
+  m.part_ml = p.part_ml;
+  m.prefix = p.prefix_out;
+  m.block_tables = block_tables;
+  m.context_lens = context_lens;
+  m.status = status;
+  m.MBS = p.MBS;
+  m.NB = p.NB;
+  m.BS = d->block_size;
+  m.B = p.B;
+  m.Hq = p.Hq;
+  m.D = d->head_dim;
+  m.g = P.g;
+  m.gs = P.gs;
+  m.nsg = P.nsg;
+  m.HU = P.HU;
+  m.W = P.W;
+  launch_merge(m, stream);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
 }
-
-}  // namespace
-
-size_t decode_counter_bytes(const pkv_dims* d, bool int8) {
-  Plan P;
-  if (make_plan(d, int8, &P) != PKV_OK) return 0;
-  return P.off_ml;
-}
-
-namespace {
 
 pkv_status check_append(const void* k, const void* v, const void* kc, const void* vc,
                         const int64_t* slots, int T, const pkv_dims* d) {

@@ -12,10 +12,10 @@
 //   one per warp of a persistent grid (W = warps per CTA x CTAs that fit x SMs).
 //   Ragged lengths therefore cost nothing in balance. A warp whose range covers a
 //   whole (sequence, unit) writes the final output; a cut unit leaves one
-//   unnormalised partial (o, running max, sum) per warp; the parts are folded in a
-//   two-level tree (groups of ~sqrt(parts)) by the last warp to arrive at each
-//   level, with the online-softmax rescaling m = max m_w, l = sum 2^(m_w - m) l_w,
-//   o = sum 2^(m_w - m) o_w / l.
+//   unnormalised partial (o, running max, sum) per warp, which the merge kernel
+//   (merge.cu) folds with the online-softmax rescaling m = max m_w,
+//   l = sum 2^(m_w - m) l_w, o = sum 2^(m_w - m) o_w / l. The merge kernel also
+//   zero-fills empty sequences and, when asked, validates the tables.
 // * Data movement: each warp owns a private ring of shared-memory stages. One lane
 //   reads the block id from the table and issues TMA tensor copies of the block's K
 //   and V tiles (128-byte swizzled, so that the tensor-core fragment loads below are
@@ -234,8 +234,7 @@ struct SimtPath {
     }
   }
 
-  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot,
-                                         bool zero) {
+  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -252,11 +251,7 @@ struct SimtPath {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       if (complete) {
-        const float inv = zero ? 0.f : 1.f / l[h];
-        if (zero) {
-#pragma unroll
-          for (int e = 0; e < kEPL / 2; ++e) o2[h][e] = make_float2(0.f, 0.f);
-        }
+        const float inv = 1.f / l[h];
         __nv_bfloat16* row =
             reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t(s) * p.Hq + head0 + h) * D;
 #pragma unroll
@@ -416,19 +411,14 @@ struct MmaPathBf16 {
     }
   }
 
-  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot,
-                                         bool zero) {
+  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     const bool v0 = gid < gs, v1 = gid + 8 < gs;
     if (complete) {
-      if (zero) {
-#pragma unroll
-        for (int nd = 0; nd < kND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-      }
-      const float i0 = zero ? 0.f : 1.f / l0, i1 = zero ? 0.f : 1.f / l1;
+      const float i0 = 1.f / l0, i1 = 1.f / l1;
       uint32_t* out = reinterpret_cast<uint32_t*>(p.out);
       const size_t row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 2);
       const size_t row1 = row0 + 8 * (D / 2);
@@ -631,17 +621,12 @@ struct MmaPathInt8 {
   // n-tile 4qg+i, column n holds head_dim index 32qg + 4n + i, so a lane's c0 values
   // over i = 0..3 are the 4 consecutive elements 32qg + 8cq + i and its c1 values
   // the next 4.
-  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot,
-                                         bool zero) {
+  __device__ __forceinline__ void finish(const DecodeParams& p, bool complete, size_t slot) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     const bool v0 = gid < gs, v1 = gid + 8 < gs;
-    if (complete && zero) {
-#pragma unroll
-      for (int nd = 0; nd < kND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-    }
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       if (!(rr == 0 ? v0 : v1)) continue;
@@ -658,7 +643,7 @@ struct MmaPathInt8 {
         }
         const int d0 = 32 * qg + 8 * cq;
         if (complete) {
-          const float inv = zero ? 0.f : 1.f / lsum;
+          const float inv = 1.f / lsum;
           uint4 pk;
           pk.x = pack_bf16x2(vals[0] * inv, vals[1] * inv);
           pk.y = pack_bf16x2(vals[2] * inv, vals[3] * inv);
@@ -679,185 +664,6 @@ struct MmaPathInt8 {
     }
   }
 };
-
-// ===========================================================================
-// Merging the partials of a cut unit (done by the last warp to finish a part)
-// ===========================================================================
-__device__ __forceinline__ long long worker_start(long long T, int w, int W) {
-  return T * w / W;
-}
-
-// Largest worker w whose range [T*w/W, T*(w+1)/W) contains flat index x.
-__device__ __forceinline__ int worker_of(long long x, long long T, int W) {
-  return int(((x + 1) * W + T - 1) / T) - 1;
-}
-
-// Arrival words: the low 32 bits count arrivals, the high 32 bits count arrivals that
-// saw a bad block id. The last arriver reads the union and stores 0 back, so a word
-// is 0 again whenever a call completes (the workspace is zeroed once, before its
-// first use).
-constexpr unsigned long long kArrive = 1ull, kArriveBad = 1ull << 32;
-
-__device__ __forceinline__ bool last_arrival(unsigned long long old, int n, bool bad,
-                                             bool* any_bad) {
-  *any_bad = bad || (old >> 32) != 0ull;
-  return int(old & 0xffffffffull) + 1 == n;
-}
-
-// One warp folds partials src(0..n-1) of one unit: into the unnormalised partial at
-// `dst_slot` (which may be one of the sources) when `to_partial`, else into the bf16
-// output `out` (zeros when `zero`). The lanes first share out the parts to find each
-// row's maximum m; then every lane accumulates all of its outputs part by part with
-// weights 2^(m_w - m), so the loads of one part are independent of the previous one.
-template <int D, class SrcFn>
-__device__ __forceinline__ void fold_parts(const DecodeParams& p, int n, SrcFn src,
-                                           size_t dst_slot, bool to_partial,
-                                           __nv_bfloat16* out, bool zero, int lane) {
-  constexpr int Q = D / 4;                       // float4 per row
-  constexpr int kMaxRows = 16;
-  constexpr int kPer = (kMaxRows * Q + 31) / 32;  // outputs per lane at most
-  const int gs = p.gs;
-  const int nout = gs * Q;
-  if (zero) {
-    for (int idx = lane; idx < nout; idx += 32)
-      *reinterpret_cast<uint2*>(out + size_t(idx / Q) * D + 4 * (idx % Q)) = make_uint2(0u, 0u);
-    return;
-  }
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  float rmax[kMaxRows];
-#pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) rmax[r] = -INFINITY;
-  for (int i = lane; i < n; i += 32) {
-    const size_t slot = src(i);
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r)
-      if (r < gs) rmax[r] = fmaxf(rmax[r], __ldcg(ml + slot * gs + r).x);
-  }
-#pragma unroll
-  for (int r = 0; r < kMaxRows; ++r) {
-    if (r >= gs) break;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) rmax[r] = fmaxf(rmax[r], __shfl_xor_sync(0xffffffffu, rmax[r], o));
-  }
-  // outputs in chunks of kChunk per lane: kChunk independent loads per part in flight
-  constexpr int kChunk = 4;
-  for (int k0 = 0; k0 < kPer; k0 += kChunk) {
-    if (lane + 32 * k0 >= nout) break;
-    float Mk[kChunk], L[kChunk];
-    float4 acc[kChunk];
-#pragma unroll
-    for (int k = 0; k < kChunk; ++k) {
-      const int row = (lane + 32 * (k0 + k)) / Q;
-      float M = rmax[0];
-#pragma unroll
-      for (int r = 1; r < kMaxRows; ++r)
-        if (r == row) M = rmax[r];
-      Mk[k] = M;
-      L[k] = 0.f;
-      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll 4
-    for (int i = 0; i < n; ++i) {
-      const size_t slot = src(i);
-#pragma unroll
-      for (int k = 0; k < kChunk; ++k) {
-        const int idx = lane + 32 * (k0 + k);
-        if (idx < nout) {
-          const int row = idx / Q, dq = idx % Q;
-          const float2 mlw = __ldcg(ml + slot * gs + row);
-          const float4 o =
-              __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot * gs + row) * D) + dq);
-          const float f = fast_exp2(mlw.x - Mk[k]);
-          L[k] = fmaf(f, mlw.y, L[k]);
-          acc[k].x = fmaf(f, o.x, acc[k].x);
-          acc[k].y = fmaf(f, o.y, acc[k].y);
-          acc[k].z = fmaf(f, o.z, acc[k].z);
-          acc[k].w = fmaf(f, o.w, acc[k].w);
-        }
-      }
-    }
-    // every lane has read the sources of these outputs before any is overwritten; the
-    // (m, l) pairs are shared by the lanes of a row, so they are written after the
-    // last chunk (below)
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < kChunk; ++k) {
-      const int idx = lane + 32 * (k0 + k);
-      if (idx >= nout) break;
-      const int row = idx / Q, dq = idx % Q;
-      if (to_partial) {
-        reinterpret_cast<float4*>(p.part_o + (dst_slot * gs + row) * D)[dq] = acc[k];
-        if (dq == 0)
-          reinterpret_cast<float2*>(p.part_ml)[dst_slot * gs + row] = make_float2(Mk[k], L[k]);
-      } else {
-        const float inv = 1.f / L[k];
-        uint2 pk;
-        pk.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
-        pk.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
-        *reinterpret_cast<uint2*>(out + size_t(row) * D + 4 * dq) = pk;
-      }
-    }
-  }
-}
-
-// ceil(sqrt(n)) for 1 <= n < 2^24, identical in every thread.
-__device__ __forceinline__ int ceil_sqrt(int n) {
-  int g = int(ceilf(sqrtf(float(n))));
-  while (g * g < n) ++g;
-  while (g > 1 && (g - 1) * (g - 1) >= n) --g;
-  return g;
-}
-
-// Part structure of a cut unit (s, u) with `nparts` parts: groups of ceil(sqrt(nparts))
-// consecutive parts. The last warp to finish a group folds it into the slot of the
-// group's first part; the last group to finish folds the group results into the
-// output. `dense`: every worker range is non-empty (T >= W), parts are workers
-// w0..w0+nparts-1; otherwise each part is one block, held by worker_of(A + i).
-struct CutUnit {
-  int s, u, nparts, my, w0, G, ngroups, g0, gsize;
-  long long A;
-  bool dense, first_cut, bad;
-  __device__ __forceinline__ size_t slot_of(int i, long long T, int W) const {
-    if (dense) return size_t(2 * (w0 + i) + ((i == 0 && first_cut) ? 1 : 0));
-    return size_t(2 * worker_of(A + i, T, W));
-  }
-};
-
-// Runs in the warp that finished group g0 of the unit last (group_bad: a part of the
-// group saw a bad block id): folds the group and, if it is also the last group,
-// the whole unit.
-template <int D>
-__device__ __noinline__ void complete_cut_unit(const DecodeParams& p, const CutUnit& c,
-                                               long long T, int W, bool group_bad, int lane) {
-  __nv_bfloat16* out =
-      reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t(c.s) * p.Hq + unit_head0(p, c.u)) * D;
-  auto slot_of = [&](int i) { return c.slot_of(i, T, W); };
-  if (c.ngroups == 1) {
-    fold_parts<D>(p, c.gsize, [&](int i) { return slot_of(c.g0 + i); }, 0, false, out,
-                  group_bad, lane);
-    return;
-  }
-  if (c.gsize > 1) {
-    fold_parts<D>(p, c.gsize, [&](int i) { return slot_of(c.g0 + i); }, slot_of(c.g0), true,
-                  out, false, lane);
-    __threadfence();  // the group result before the group's arrival
-    __syncwarp();
-  }
-  int flags = 0;
-  if (lane == 0) {
-    unsigned long long* word = p.counters + c.slot_of(0, T, W);
-    const unsigned long long old = atomicAdd(word, kArrive + (group_bad ? kArriveBad : 0ull));
-    bool any_bad = false;
-    const bool last = last_arrival(old, c.ngroups, group_bad, &any_bad);
-    if (last) *word = 0ull;
-    flags = (last ? 1 : 0) | (any_bad ? 2 : 0);
-  }
-  flags = __shfl_sync(0xffffffffu, flags, 0);
-  if (!(flags & 1)) return;
-  __threadfence();  // every group result is visible to this warp
-  fold_parts<D>(p, c.ngroups, [&](int g) { return slot_of(g * c.G); }, 0, false, out,
-                (flags & 2) != 0, lane);
-}
 
 // ===========================================================================
 // Work cursor over the flat (sequence, unit, block) order.
@@ -950,15 +756,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     if (tid == 0) s_prefix[0] = 0;
     __syncthreads();
-    // sequences without blocks get a zero output (a negative length is also flagged)
-    for (int s2 = blockIdx.x; s2 < B; s2 += gridDim.x) {
-      if (s_prefix[s2 + 1] != s_prefix[s2]) continue;
-      if (p.status != nullptr && tid == 0 && __ldg(p.context_lens + s2) < 0)
-        atomicOr(p.status, 0x1);
-      uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                          size_t(s2) * p.Hq * D);
-      for (int i = tid; i < p.Hq * D / 8; i += nthr) o[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
+    if (blockIdx.x == 0)
+      for (int i = tid; i <= B; i += nthr) p.prefix_out[i] = s_prefix[i];
   }
 
   const int HU = p.HU;
@@ -988,15 +787,11 @@ __global__ void __launch_bounds__(kWarps * 32)
   cursor_locate(pc, a, s_prefix, B, HU);
   cc = pc;
 
-  // lane 0 issues the copies of the block at the producer cursor into stage st;
-  // with a status word it also remembers, per stage, whether the block id was invalid
-  uint32_t bad_stages = 0;
+  // lane 0 issues the copies of the block at the producer cursor into stage st
   auto issue = [&](int st) {
     if (lane == 0) {
       int phys = __ldg(p.block_tables + size_t(pc.s) * p.MBS + pc.j);
-      const bool invalid = phys < 0 || phys >= p.NB;
-      bad_stages = (bad_stages & ~(1u << st)) | (uint32_t(invalid) << st);
-      phys = invalid ? 0 : phys;  // never copy outside the pool
+      phys = (phys < 0 || phys >= p.NB) ? 0 : phys;  // never copy outside the pool
       const int kvh = pc.u / p.nsg;
       const int row = (phys * p.Hkv + kvh) * BS;
       mbar_arrive_expect_tx(bar(st), K::kTxBytes);
@@ -1019,62 +814,12 @@ __global__ void __launch_bounds__(kWarps * 32)
     cursor_next(pc, s_prefix, B, HU);
   }
 
-  // q rows of the unit after (s, u) in the flat order, pulled into L1 ahead of use
-  auto prefetch_next_q = [&](int s, int u) {
-    int s2 = s, u2 = u + 1;
-    if (u2 == HU) {
-      u2 = 0;
-      do { ++s2; } while (s2 < B && s_prefix[s2 + 1] == s_prefix[s2]);
-    }
-    if (s2 < B && lane * 128 < p.gs * D * 2) {
-      const char* row = reinterpret_cast<const char*>(p.q) +
-                        (size_t(s2) * p.Hq + unit_head0(p, u2)) * D * 2 + lane * 128;
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(row));
-    }
-  };
-
   Path path;
   path.init(lane);
   path.begin(p, cc.s, cc.u);
-  prefetch_next_q(cc.s, cc.u);
   int seg_j0 = cc.j;
   bool first_seg = true;
-  const bool checks = p.status != nullptr;
-  int Lraw = __ldg(p.context_lens + cc.s);
-  int Lc = min(Lraw, p.MBS * BS);
-  bool seg_bad_id = false;
-
-  // A cut unit's arrival is deferred: the partial is written at the end of its last
-  // block, the arrival is counted one block later (the partial's stores have drained,
-  // so the fence is cheap) and its result is read one block after that.
-  CutUnit pend;
-  int pend_state = 0;              // 0 none, 1 partial written, 2 arrival counted
-  unsigned long long pend_old = 0;  // lane 0: the word before this warp's arrival
-  auto pend_count = [&]() {
-    __threadfence();  // this warp's partial before its arrival
-    __syncwarp();
-    if (pend.gsize > 1 && lane == 0)
-      pend_old = atomicAdd(p.group_counters + pend.slot_of(pend.g0, T, W),
-                           kArrive + (pend.bad ? kArriveBad : 0ull));
-    pend_state = 2;
-  };
-  auto pend_resolve = [&]() {
-    int flags = 1 | (pend.bad ? 2 : 0);
-    if (pend.gsize > 1) {
-      if (lane == 0) {
-        bool any_bad = false;
-        const bool last = last_arrival(pend_old, pend.gsize, pend.bad, &any_bad);
-        if (last) p.group_counters[pend.slot_of(pend.g0, T, W)] = 0ull;
-        flags = (last ? 1 : 0) | (any_bad ? 2 : 0);
-      }
-      flags = __shfl_sync(0xffffffffu, flags, 0);
-    }
-    if (flags & 1) {
-      __threadfence();  // the other parts of the group are visible to this warp
-      complete_cut_unit<D>(p, pend, T, W, (flags & 2) != 0, lane);
-    }
-    pend_state = 0;
-  };
+  int Lc = min(__ldg(p.context_lens + cc.s), p.MBS * BS);
 
   for (int i = 0; i < nblk; ++i) {
     const int st = i % kStages;
@@ -1088,7 +833,6 @@ __global__ void __launch_bounds__(kWarps * 32)
         mbar_wait_bounded(bar(k2 % kStages), uint32_t(k2 / kStages) & 1u, p.timeout_ns);
       return;
     }
-    if (checks) seg_bad_id |= __shfl_sync(0xffffffffu, (bad_stages >> st) & 1u, 0) != 0u;
     path.block(p, sK(st), sV(st), sKs(st), sVs(st), Lc - cc.j * BS);
     __syncwarp();
     if (i + kStages < nblk) {
@@ -1096,49 +840,17 @@ __global__ void __launch_bounds__(kWarps * 32)
       issue(st);
       cursor_next(pc, s_prefix, B, HU);
     }
-    if (pend_state == 2) pend_resolve();
-    else if (pend_state == 1) pend_count();
     const bool seg_end = (cc.j == cc.n - 1) || (i == nblk - 1);
     if (seg_end) {
-      const bool seg_bad_len = checks && Lraw > p.MBS * BS;
-      const bool seg_bad = seg_bad_len || seg_bad_id;
-      if (seg_bad && lane == 0) atomicOr(p.status, (seg_bad_len ? 0x1 : 0) | (seg_bad_id ? 0x2 : 0));
       const bool complete = (seg_j0 == 0) && (cc.j == cc.n - 1);
-      if (complete) {
-        path.finish(p, true, 0, seg_bad);
-      } else {
-        if (pend_state == 1) pend_count();
-        if (pend_state == 2) pend_resolve();
-        path.finish(p, false, partial_slot(w, first_seg), false);
-        pend.s = cc.s;
-        pend.u = cc.u;
-        pend.A = (long long)HU * s_prefix[cc.s] + (long long)cc.u * cc.n;
-        pend.w0 = worker_of(pend.A, T, W);
-        pend.dense = T >= W;
-        pend.nparts = pend.dense ? (worker_of(pend.A + cc.n - 1, T, W) - pend.w0 + 1) : cc.n;
-        pend.my = pend.dense ? (w - pend.w0) : cc.j;
-        pend.first_cut = worker_start(T, pend.w0, W) != pend.A;
-        pend.G = ceil_sqrt(pend.nparts);
-        pend.ngroups = (pend.nparts + pend.G - 1) / pend.G;
-        pend.g0 = (pend.my / pend.G) * pend.G;
-        pend.gsize = min(pend.G, pend.nparts - pend.g0);
-        pend.bad = seg_bad;
-        pend_state = 1;
-      }
+      path.finish(p, complete, partial_slot(w, first_seg));
       first_seg = false;
-    }
-    if (i == nblk - 1) {  // nothing left to overlap with: settle the pending arrival now
-      if (pend_state == 1) pend_count();
-      if (pend_state == 2) pend_resolve();
     }
     cursor_next(cc, s_prefix, B, HU);
     if (seg_end && i + 1 < nblk) {
       seg_j0 = cc.j;
-      Lraw = __ldg(p.context_lens + cc.s);
-      Lc = min(Lraw, p.MBS * BS);
-      seg_bad_id = false;
+      Lc = min(__ldg(p.context_lens + cc.s), p.MBS * BS);
       path.begin(p, cc.s, cc.u);
-      prefetch_next_q(cc.s, cc.u);
     }
   }
 }

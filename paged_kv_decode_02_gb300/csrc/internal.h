@@ -9,11 +9,6 @@
 
 namespace pkv {
 
-// Partial slots (2 per worker) the arrival-word arrays are sized for. The words sit at
-// the start of every workspace in arrays of this fixed size, so a workspace left at
-// zero by one call is valid for a call of any other shape.
-constexpr int kMaxSlots = 16384;
-
 // Parameters of one decode launch (device pointers; sizes as in pkv_dims).
 struct DecodeParams {
   const void* q;               // [B, Hq, D] bf16
@@ -24,8 +19,7 @@ struct DecodeParams {
   const int32_t* context_lens; // [B]
   float* part_o;               // [2W, GS, D] fp32 partial outputs (unnormalised)
   float* part_ml;              // [2W, GS, 2] fp32 (running max in log2 units, sum)
-  unsigned long long* counters;        // [kMaxSlots] unit arrival words, by first part's slot
-  unsigned long long* group_counters;  // [kMaxSlots] group arrival words, by first part's slot
+  int32_t* prefix_out;         // [B+1] blocks-per-sequence exclusive prefix (CTA 0 writes)
   int32_t* status;             // optional device status word
   int B, Hq, Hkv, MBS, NB;
   int g;                       // Hq / Hkv
@@ -36,6 +30,22 @@ struct DecodeParams {
   unsigned long long timeout_ns;
 };
 
+// Parameters of the split-KV merge launch (units cut between decode workers).
+struct MergeParams {
+  void* out;
+  const float* part_o;
+  const float* part_ml;
+  const int32_t* prefix;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t* status;
+  int B, Hq, D, MBS, NB, BS;
+  int g, gs, nsg, HU;
+  int W;                       // number of decode workers (warps)
+};
+
+void launch_merge(const MergeParams& p, cudaStream_t stream);
+
 // A compiled decode kernel and its static shape.
 struct DecodeKernelInfo {
   const void* fn;
@@ -45,10 +55,6 @@ struct DecodeKernelInfo {
   int mma;           // 1 = tensor-core path (groups >= 4), 0 = CUDA-core path
   int simt_heads;    // query heads per unit on the CUDA-core path
 };
-
-// Bytes at the start of a decode workspace that hold arrival counters (these must be
-// zero when a call starts). Returns 0 if the dims are invalid.
-size_t decode_counter_bytes(const ::pkv_dims* d, bool int8);
 
 // Kernel tables, one per translation unit. Return false if the shape is not built.
 bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info);

@@ -10,7 +10,6 @@
 
 #include <mutex>
 
-#include "internal.h"
 #include "pagedkv.h"
 
 // The scratch itself: PKV_NOALLOC_SCRATCH_BYTES of device memory on every GPU that
@@ -56,12 +55,8 @@ extern "C" pkv_status pkv_decode_bf16_noalloc(void* out, const void* q, const vo
   void* scratch = nullptr;
   st = scratch_on_current_device(&scratch);
   if (st != PKV_OK) return st;
-  // The scratch keeps the previous call's contents; its arrival counters must start at
-  // zero, so clear them on this stream first (a memset, not an allocation).
-  const size_t counters = pkv::decode_counter_bytes(dims, false);
-  if (counters > 0 && cudaMemsetAsync(scratch, 0, counters, reinterpret_cast<cudaStream_t>(stream)) !=
-                          cudaSuccess)
-    return PKV_ERR_CUDA;
+  // Nothing in the scratch has to start at zero: the decode writes the block prefix
+  // and every partial before anything reads them.
   return pkv_decode_bf16(out, q, k_cache, v_cache, block_tables, context_lens, scale, dims,
                          scratch, size_t(PKV_NOALLOC_SCRATCH_BYTES), status, stream);
 }

@@ -231,8 +231,7 @@ def _decode(int8, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_l
         _check(_lib().pkv_decode_workspace_bytes(ctypes.byref(dims), KV_INT8 if int8 else KV_BF16,
                                                  ctypes.byref(need)), "pkv_decode_workspace_bytes")
         if workspace is None or workspace.numel() < need.value:
-            # zero-filled once: the library leaves it zeroed after every completed call
-            workspace = torch.zeros(max(int(need.value), 256), dtype=torch.uint8, device=dev)
+            workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=dev)
         if int8:
             st = _lib().pkv_decode_int8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                         _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
@@ -254,7 +253,7 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
 
     q [B, Hq, D] bf16; caches [NB, Hkv, bs, D] bf16; block_tables [B, MBS] int32;
     context_lens [B] int32. Returns out [B, Hq, D] bf16. ``workspace`` (uint8, at
-    least :func:`decode_workspace_bytes`, zero-filled before its first use) and
+    least :func:`decode_workspace_bytes`) and
     ``status`` (int32 [1]) are optional.
     """
     return _decode(False, q, k_cache, v_cache, None, None, block_tables, context_lens, scale,

@@ -4,30 +4,36 @@
 namespace pkv {
 
 namespace {
-// Pipeline depth per warp keeps ~24 KiB of K+V tiles in flight per warp.
+// CTA shape per path, from sweeps on GB300 (the path is bound by per-warp latency, so
+// more warps with shallow pipelines win): the CUDA-core path runs 8 warps per CTA with
+// one ~8 KiB stage each (24 warps per SM at 16-token blocks); the tensor-core path 4
+// warps with one stage. Larger tiles keep the per-warp bytes in flight near 8-16 KiB.
 template <int D, int BS>
 struct Bf16Shape {
-  static constexpr int kTile = BS * D * 2;
-  static constexpr int kWarps = (2 * kTile >= 16384) ? 3 : 4;
-  static constexpr int kStagesRaw = 24576 / (2 * kTile);
-  static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+  static constexpr int kStage = 2 * BS * D * 2;  // K + V bytes of one block
+  static constexpr int kStages = kStage >= 8192 ? 1 : 8192 / kStage;
+};
+template <int D, int BS, bool MMA>
+struct Bf16Warps {
+  static constexpr int kWarps = MMA ? 4 : (Bf16Shape<D, BS>::kStage > 8192 ? 4 : 8);
 };
 
 template <int D, int BS>
 bool select_shape(int simt_heads, DecodeKernelInfo* info) {
-  using S = Bf16Shape<D, BS>;
+  constexpr int kS = Bf16Shape<D, BS>::kStages;
+  constexpr int kWm = Bf16Warps<D, BS, true>::kWarps, kWs = Bf16Warps<D, BS, false>::kWarps;
   switch (simt_heads) {
     case 0:
-      *info = make_decode_info<false, D, BS, MmaPathBf16<D, BS>, S::kWarps, S::kStages>(1, 0);
+      *info = make_decode_info<false, D, BS, MmaPathBf16<D, BS>, kWm, kS>(1, 0);
       return true;
     case 1:
-      *info = make_decode_info<false, D, BS, SimtPath<false, D, BS, 1>, S::kWarps, S::kStages>(0, 1);
+      *info = make_decode_info<false, D, BS, SimtPath<false, D, BS, 1>, kWs, kS>(0, 1);
       return true;
     case 2:
-      *info = make_decode_info<false, D, BS, SimtPath<false, D, BS, 2>, S::kWarps, S::kStages>(0, 2);
+      *info = make_decode_info<false, D, BS, SimtPath<false, D, BS, 2>, kWs, kS>(0, 2);
       return true;
     case 3:
-      *info = make_decode_info<false, D, BS, SimtPath<false, D, BS, 3>, S::kWarps, S::kStages>(0, 3);
+      *info = make_decode_info<false, D, BS, SimtPath<false, D, BS, 3>, kWs, kS>(0, 3);
       return true;
     default:
       return false;

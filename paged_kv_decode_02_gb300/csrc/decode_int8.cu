@@ -4,13 +4,14 @@
 namespace pkv {
 
 namespace {
-// Pipeline depth per warp keeps ~24 KiB of K+V tiles in flight per warp.
+// CTA shape per path, from sweeps on GB300: the INT8 tensor-core path (more
+// arithmetic per byte) runs one warp per CTA with 12-16 KiB of stages; the CUDA-core
+// path 8 warps with one ~8 KiB stage each.
 template <int D, int BS>
 struct Int8Shape {
-  static constexpr int kTile = BS * D;
-  static constexpr int kWarps = (2 * kTile >= 16384) ? 3 : 4;
-  static constexpr int kStagesRaw = 24576 / (2 * kTile);
-  static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+  static constexpr int kStage = 2 * BS * D;  // K + V bytes of one block (scales aside)
+  static constexpr int kMmaStages = kStage >= 8192 ? 2 : 12288 / kStage;
+  static constexpr int kSimtStages = kStage >= 8192 ? 1 : 8192 / kStage;
 };
 
 template <int D, int BS>
@@ -18,16 +19,16 @@ bool select_shape(int simt_heads, DecodeKernelInfo* info) {
   using S = Int8Shape<D, BS>;
   switch (simt_heads) {
     case 0:
-      *info = make_decode_info<true, D, BS, MmaPathInt8<D, BS>, S::kWarps, S::kStages>(1, 0);
+      *info = make_decode_info<true, D, BS, MmaPathInt8<D, BS>, 1, S::kMmaStages>(1, 0);
       return true;
     case 1:
-      *info = make_decode_info<true, D, BS, SimtPath<true, D, BS, 1>, S::kWarps, S::kStages>(0, 1);
+      *info = make_decode_info<true, D, BS, SimtPath<true, D, BS, 1>, 8, S::kSimtStages>(0, 1);
       return true;
     case 2:
-      *info = make_decode_info<true, D, BS, SimtPath<true, D, BS, 2>, S::kWarps, S::kStages>(0, 2);
+      *info = make_decode_info<true, D, BS, SimtPath<true, D, BS, 2>, 8, S::kSimtStages>(0, 2);
       return true;
     case 3:
-      *info = make_decode_info<true, D, BS, SimtPath<true, D, BS, 3>, S::kWarps, S::kStages>(0, 3);
+      *info = make_decode_info<true, D, BS, SimtPath<true, D, BS, 3>, 8, S::kSimtStages>(0, 3);
       return true;
     default:
       return false;

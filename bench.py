@@ -352,15 +352,12 @@ def run_ours(args, rank, world):
     dec_ms = d_start.elapsed_time(d_end) / K
     dec_how = ("CUDA events around K back-to-back decode calls (decode + merge kernels, "
                "graph replay) after the K timed steps")
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = job_time_ms(ms_total, world, dev)
     ms_step = ms_total / K
 
     db = decode_bytes(w)
     step_bytes = db["total"] + append_bytes(w)
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_throughput(step_bytes, ms_step, world)
     tokens_per_s = world * db["tokens"] / (ms_step * 1e-3)
     peak, peak_kind = measured_peak()
     achieved = db["total"] / (dec_ms * 1e-3) / 1e9
@@ -402,6 +399,22 @@ def run_ours(args, rank, world):
     if e2e is not None:
         result["e2e"] = e2e
     return result, w
+
+
+def job_time_ms(ms_local, world, device):
+    """Whole-job time of the timed region: the maximum over ranks (replicas finish
+    when the slowest does). With one rank, the local time."""
+    if world <= 1:
+        return float(ms_local)
+    import torch
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank, ms_job, world):
+    """Units all ranks processed (bytes) over the whole-job time, in GB/s."""
+    return world * bytes_per_rank / (ms_job * 1e-3) / 1e9
 
 
 def capture(K, fn, dev):

@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cascade", action="store_true",
+                    help="prefix workload: decode through the shared-prefix (cascade) entry point")
     return ap.parse_args()
 
 
@@ -287,9 +289,17 @@ def run_ours(args, rank, world):
     pk.load_library()
     w = make_workload(args.config, device=dev)
     int8 = w.kv_dtype == "int8"
-    need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                     w.block_size, w.num_blocks, w.max_blocks_per_seq,
-                                     pk.pagedkv.KV_INT8 if int8 else pk.pagedkv.KV_BF16)
+    cascade_blocks = w.extra.get("prefix_tokens", 0) // w.block_size if args.cascade else 0
+    if args.cascade and (int8 or cascade_blocks == 0):
+        raise SystemExit("--cascade needs a bf16 workload with a shared prefix (prefix)")
+    if cascade_blocks:
+        need = pk.cascade_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                          w.block_size, w.num_blocks, w.max_blocks_per_seq,
+                                          cascade_blocks)
+    else:
+        need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                         w.block_size, w.num_blocks, w.max_blocks_per_seq,
+                                         pk.pagedkv.KV_INT8 if int8 else pk.pagedkv.KV_BF16)
     ws = torch.zeros(need, dtype=torch.uint8, device=dev)
     out = torch.empty_like(w.q)
     stream = torch.cuda.current_stream(dev)
@@ -306,6 +316,10 @@ def run_ours(args, rank, world):
             pk.paged_decode_attention_int8(w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
                                            w.block_tables, w.context_lens, w.scale, out=out,
                                            workspace=ws)
+        elif cascade_blocks:
+            pk.paged_decode_attention_cascade(w.q, w.k_cache, w.v_cache, w.block_tables,
+                                              w.context_lens, cascade_blocks, w.scale, out=out,
+                                              workspace=ws)
         else:
             pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
                                       w.scale, out=out, workspace=ws)
@@ -364,7 +378,7 @@ def run_ours(args, rank, world):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, pk, dev, append, out, ws, step_bytes, world)
+        e2e = run_e2e(args, w, pk, dev, append, out, ws, step_bytes, world, cascade_blocks)
 
     result = {
         "metric": "paged decode attention: achieved HBM GB/s (% of GB300 peak) and KV tokens/s",
@@ -374,7 +388,9 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded)",
         "kv_tokens_per_s": round(tokens_per_s, 1),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
-        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+        "config": {"workload": WORKLOAD_TEXT[args.config] + (" (cascade decode)" if cascade_blocks
+                                                             else ""),
+                   "name": args.config + ("+cascade" if cascade_blocks else ""),
                    "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                    "block_size": w.block_size, "num_blocks": w.num_blocks,
@@ -393,7 +409,7 @@ def run_ours(args, rank, world):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "timing": dec_how},
-        "gpu_launches": 3 * K,
+        "gpu_launches": (4 if cascade_blocks else 3) * K,
         "clocks": clk,
     }
     if e2e is not None:
@@ -431,7 +447,7 @@ def capture(K, fn, dev):
     return g
 
 
-def run_e2e(args, w, pk, dev, append_dev, out, ws, step_bytes, world):
+def run_e2e(args, w, pk, dev, append_dev, out, ws, step_bytes, world, cascade_blocks=0):
     """Same step through the public API from pinned HOST buffers: per step, copy the
     step's inputs host->device, append + decode, copy the output device->host."""
     import torch
@@ -457,8 +473,14 @@ def run_e2e(args, w, pk, dev, append_dev, out, ws, step_bytes, world):
         else:
             pk.paged_kv_append(dev_in["new_k"], dev_in["new_v"], w.k_cache, w.v_cache,
                                dev_in["slot_mapping"])
-            pk.paged_decode_attention(dev_in["q"], w.k_cache, w.v_cache, dev_in["block_tables"],
-                                      dev_in["context_lens"], w.scale, out=out, workspace=ws)
+            if cascade_blocks:
+                pk.paged_decode_attention_cascade(dev_in["q"], w.k_cache, w.v_cache,
+                                                  dev_in["block_tables"], dev_in["context_lens"],
+                                                  cascade_blocks, w.scale, out=out, workspace=ws)
+            else:
+                pk.paged_decode_attention(dev_in["q"], w.k_cache, w.v_cache,
+                                          dev_in["block_tables"], dev_in["context_lens"], w.scale,
+                                          out=out, workspace=ws)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):

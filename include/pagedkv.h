@@ -78,6 +78,7 @@ typedef struct pkv_dims {
 #define PKV_DEV_BAD_CONTEXT_LEN 0x1  /* context_len < 0 or > max_blocks_per_seq*block_size */
 #define PKV_DEV_BAD_BLOCK_ID    0x2  /* a block id the context needs is outside [0, num_blocks) */
 #define PKV_DEV_TIMEOUT         0x4  /* a shared-memory copy did not complete in time */
+#define PKV_DEV_BAD_PREFIX      0x8  /* cascade: a table does not start with the shared prefix */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* pkv_status_string(pkv_status status);
@@ -152,6 +153,30 @@ pkv_status pkv_decode_int8(void* out, const void* q, const int8_t* k_cache,
                            const int32_t* block_tables, const int32_t* context_lens,
                            float scale, const pkv_dims* dims, void* workspace,
                            size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
+
+/*
+ * pkv_decode_cascade_bf16 -- pkv_decode_bf16 for a batch whose sequences all start
+ * with the same `prefix_blocks` physical blocks (a shared system prompt or few-shot
+ * prefix: the shared blocks of "分页注意力", chenk.top, and section 2.2 of the gsyq.cn
+ * page). Precondition: block_tables[s, 0..prefix_blocks-1] equals row 0's entries and
+ * context_lens[s] >= prefix_blocks * block_size for every s. The result is the same
+ * attention as pkv_decode_bf16 over the whole table; the prefix part is computed once
+ * per KV head for all sequences as one dense tensor-core contraction (query rows of
+ * the batch x prefix tokens), the suffixes by the ordinary decode, then merged.
+ *   workspace  at least pkv_decode_cascade_workspace_bytes() bytes, 256-byte
+ *              aligned, no initialisation needed.
+ *   status     optional; additionally flags PKV_DEV_BAD_PREFIX (and zeroes the
+ *              output) for a sequence that breaks the precondition. Without it,
+ *              such a sequence's output is unspecified.
+ */
+pkv_status pkv_decode_cascade_workspace_bytes(const pkv_dims* dims, int32_t prefix_blocks,
+                                              size_t* bytes);
+
+pkv_status pkv_decode_cascade_bf16(void* out, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables,
+                                   const int32_t* context_lens, int32_t prefix_blocks,
+                                   float scale, const pkv_dims* dims, void* workspace,
+                                   size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
 
 /*
  * pkv_decode_bf16_noalloc -- pkv_decode_bf16 for callers that cannot allocate device

@@ -262,6 +262,8 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
   p.HU = P.HU;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = kTimeoutNs;
+  p.skip = 0;
+  p.unit_slot0 = -1;
 
   void* args[] = {&tmk, &tmv, &p};
   if (launch_pdl(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), args, P.smem, stream) !=
@@ -288,6 +290,156 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
   m.HU = P.HU;
   m.W = P.W;
   launch_merge(m, stream);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Cascade (shared prefix) decode
+// ---------------------------------------------------------------------------
+struct CascadePlan {
+  Plan dec;                    // suffix decode (its partial arrays get 2W + B*HU slots)
+  int R, nsplit, per_split, psmem;
+  const void* pfn;
+  size_t off_prefix, off_ml, off_o, off_pre_o, off_pre_ml, ws_bytes;
+};
+
+pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* cp) {
+  pkv_status st = make_plan(d, false, &cp->dec);
+  if (st != PKV_OK) return st;
+  if (prefix_blocks < 1 || prefix_blocks > d->max_blocks_per_seq) return PKV_ERR_SHAPE;
+  if (!select_prefix_kernel(d->head_dim, d->block_size, &cp->pfn, &cp->psmem))
+    return PKV_ERR_UNSUPPORTED;
+  const Plan& P = cp->dec;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  cp->R = d->num_seqs * P.g;
+  const int ctas = ((cp->R + 63) / 64) * d->num_kv_heads;
+  int nsplit = std::max(1, std::min(prefix_blocks, (3 * sms + ctas - 1) / ctas));
+  cp->per_split = (prefix_blocks + nsplit - 1) / nsplit;
+  cp->nsplit = (prefix_blocks + cp->per_split - 1) / cp->per_split;
+  const size_t nslots = size_t(2) * P.W + size_t(d->num_seqs) * P.HU;
+  cp->off_prefix = 0;
+  cp->off_ml = align_up(size_t(d->num_seqs + 1) * 4, 256);
+  cp->off_o = align_up(cp->off_ml + nslots * P.gs * 8, 256);
+  cp->off_pre_o = align_up(cp->off_o + nslots * P.gs * d->head_dim * 4, 256);
+  const size_t recs = size_t(cp->nsplit) * d->num_kv_heads * cp->R;
+  cp->off_pre_ml = align_up(cp->off_pre_o + recs * d->head_dim * 4, 256);
+  cp->ws_bytes = align_up(cp->off_pre_ml + recs * 8, 256);
+  if (cudaFuncSetAttribute(cp->pfn, cudaFuncAttributeMaxDynamicSharedMemorySize, cp->psmem) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens,
+                       int prefix_blocks, float scale, const pkv_dims* d, void* workspace,
+                       size_t workspace_bytes, int32_t* status, cudaStream_t stream) {
+  pkv_status st = check_dims(d);
+  if (st != PKV_OK) return st;
+  if (d->num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_NULL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ALIGNMENT;
+  CascadePlan C;
+  st = make_cascade_plan(d, prefix_blocks, &C);
+  if (st != PKV_OK) return st;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < C.ws_bytes)
+    return PKV_ERR_WORKSPACE;
+  const Plan& P = C.dec;
+  const long long rows = (long long)d->num_blocks * d->num_kv_heads * d->block_size;
+  CUtensorMap tmk, tmv;
+  if (!cache_map(&tmk, k_cache, false, d->head_dim, rows, d->block_size) ||
+      !cache_map(&tmv, v_cache, false, d->head_dim, rows, d->block_size))
+    return PKV_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const float scale_log2 = scale * 1.4426950408889634f;
+
+  // 1. the shared prefix, once per KV head for all B*g query rows
+  PrefixParams pp{};
+  pp.q = q;
+  pp.prefix_ids = block_tables;  // row 0 holds the shared prefix
+  pp.pre_o = reinterpret_cast<float*>(ws + C.off_pre_o);
+  pp.pre_ml = reinterpret_cast<float*>(ws + C.off_pre_ml);
+  pp.P = prefix_blocks;
+  pp.B = d->num_seqs;
+  pp.Hq = d->num_q_heads;
+  pp.Hkv = d->num_kv_heads;
+  pp.g = P.g;
+  pp.R = C.R;
+  pp.NB = d->num_blocks;
+  pp.nsplit = C.nsplit;
+  pp.per_split = C.per_split;
+  pp.scale_log2 = scale_log2;
+  pp.timeout_ns = kTimeoutNs;
+  pp.status = status;
+  {
+    void* args[] = {&tmk, &tmv, &pp};
+    if (launch_pdl(C.pfn, dim3((C.R + 63) / 64, d->num_kv_heads, C.nsplit), dim3(160), args,
+                   C.psmem, stream) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  // 2. the private suffixes: the ordinary decode over the tables past the prefix; a
+  //    complete unit leaves its partial in slot 2W + s*HU + u
+  DecodeParams p{};
+  p.q = q;
+  p.out = out;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.part_o = reinterpret_cast<float*>(ws + C.off_o);
+  p.part_ml = reinterpret_cast<float*>(ws + C.off_ml);
+  p.prefix_out = reinterpret_cast<int32_t*>(ws + C.off_prefix);
+  p.status = status;
+  p.B = d->num_seqs;
+  p.Hq = d->num_q_heads;
+  p.Hkv = d->num_kv_heads;
+  p.MBS = d->max_blocks_per_seq;
+  p.NB = d->num_blocks;
+  p.g = P.g;
+  p.gs = P.gs;
+  p.nsg = P.nsg;
+  p.HU = P.HU;
+  p.scale_log2 = scale_log2;
+  p.timeout_ns = kTimeoutNs;
+  p.skip = prefix_blocks;
+  p.unit_slot0 = 2 * P.W;
+  {
+    void* args[] = {&tmk, &tmv, &p};
+    if (launch_pdl(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), args, P.smem, stream) !=
+        cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  // 3. fold prefix and suffix partials
+  CascadeMergeParams m{};
+  m.out = out;
+  m.part_o = p.part_o;
+  m.part_ml = p.part_ml;
+  m.pre_o = pp.pre_o;
+  m.pre_ml = pp.pre_ml;
+  m.prefix = p.prefix_out;
+  m.block_tables = block_tables;
+  m.context_lens = context_lens;
+  m.status = status;
+  m.B = p.B;
+  m.Hq = p.Hq;
+  m.Hkv = p.Hkv;
+  m.D = d->head_dim;
+  m.MBS = p.MBS;
+  m.NB = p.NB;
+  m.BS = d->block_size;
+  m.P = prefix_blocks;
+  m.g = P.g;
+  m.gs = P.gs;
+  m.nsg = P.nsg;
+  m.HU = P.HU;
+  m.W = P.W;
+  m.R = C.R;
+  m.nsplit = C.nsplit;
+  launch_cascade_merge(m, stream);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
 }
@@ -369,6 +521,26 @@ pkv_status pkv_decode_bf16(void* out, const void* q, const void* k_cache, const 
   return run_decode(false, out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
                     context_lens, scale, dims, workspace, workspace_bytes, status,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_decode_cascade_workspace_bytes(const pkv_dims* dims, int32_t prefix_blocks,
+                                              size_t* bytes) {
+  if (!bytes) return PKV_ERR_NULL;
+  CascadePlan C;
+  pkv_status st = make_cascade_plan(dims, prefix_blocks, &C);
+  if (st != PKV_OK) return st;
+  *bytes = C.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_cascade_bf16(void* out, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables,
+                                   const int32_t* context_lens, int32_t prefix_blocks,
+                                   float scale, const pkv_dims* dims, void* workspace,
+                                   size_t workspace_bytes, int32_t* status, pkv_stream_t stream) {
+  return run_cascade(out, q, k_cache, v_cache, block_tables, context_lens, prefix_blocks, scale,
+                     dims, workspace, workspace_bytes, status,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 pkv_status pkv_decode_int8(void* out, const void* q, const int8_t* k_cache,

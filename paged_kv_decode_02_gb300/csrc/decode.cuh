@@ -312,21 +312,44 @@ struct MmaPathBf16 {
     gs = p.gs;
     head0 = unit_head0(p, u);
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
-    const bool v0 = gid < gs, v1 = gid + 8 < gs;
     const size_t row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 2);
-    const size_t row1 = row0 + 8 * (D / 2);
+    load_q(qw + row0, qw + row0 + 8 * (D / 2), gid < gs, gid + 8 < gs);
+  }
+
+  // Q fragments from the rows of this lane's two M rows (gid, gid + 8; absent rows are
+  // zero), and a fresh softmax state.
+  __device__ __forceinline__ void load_q(const uint32_t* r0, const uint32_t* r1, bool v0,
+                                         bool v1) {
 #pragma unroll
     for (int ks = 0; ks < kKS; ++ks) {
       const int w = 8 * ks + cq;  // 32-bit word index of elements 16ks + 2cq
-      qa[ks][0] = v0 ? __ldg(qw + row0 + w) : 0u;
-      qa[ks][1] = v1 ? __ldg(qw + row1 + w) : 0u;
-      qa[ks][2] = v0 ? __ldg(qw + row0 + w + 4) : 0u;
-      qa[ks][3] = v1 ? __ldg(qw + row1 + w + 4) : 0u;
+      qa[ks][0] = v0 ? __ldg(r0 + w) : 0u;
+      qa[ks][1] = v1 ? __ldg(r1 + w) : 0u;
+      qa[ks][2] = v0 ? __ldg(r0 + w + 4) : 0u;
+      qa[ks][3] = v1 ? __ldg(r1 + w + 4) : 0u;
     }
 #pragma unroll
     for (int nd = 0; nd < kND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
     m0 = m1 = -INFINITY;
     l0 = l1 = 0.f;
+  }
+
+  // Unnormalised (o, m, l) of the lane's two rows to explicit row addresses.
+  __device__ __forceinline__ void store_rows(float* o_r0, float* o_r1, float2* ml_r0,
+                                             float2* ml_r1, bool v0, bool v1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+#pragma unroll
+    for (int nd = 0; nd < kND; ++nd) {
+      if (v0) reinterpret_cast<float2*>(o_r0)[4 * nd + cq] = make_float2(o[nd][0], o[nd][1]);
+      if (v1) reinterpret_cast<float2*>(o_r1)[4 * nd + cq] = make_float2(o[nd][2], o[nd][3]);
+    }
+    if (cq == 0) {
+      if (v0) *ml_r0 = make_float2(m0, l0);
+      if (v1) *ml_r1 = make_float2(m1, l1);
+    }
   }
 
   __device__ __forceinline__ void block(const DecodeParams& p, uint32_t sK, uint32_t sV, uint32_t,
@@ -734,7 +757,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     int sum = 0;
     for (int i = b0; i < b1; ++i) {
       const int L = __ldg(p.context_lens + i);
-      sum += L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS);
+      sum += max(0, (L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS)) - p.skip);
     }
     // inclusive warp scan, then across warps
     int incl = sum;
@@ -751,7 +774,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     int run = base + incl - sum;
     for (int i = b0; i < b1; ++i) {
       const int L = __ldg(p.context_lens + i);
-      run += L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS);
+      run += max(0, (L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS)) - p.skip);
       s_prefix[i + 1] = run;
     }
     if (tid == 0) s_prefix[0] = 0;
@@ -790,7 +813,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   // lane 0 issues the copies of the block at the producer cursor into stage st
   auto issue = [&](int st) {
     if (lane == 0) {
-      int phys = __ldg(p.block_tables + size_t(pc.s) * p.MBS + pc.j);
+      int phys = __ldg(p.block_tables + size_t(pc.s) * p.MBS + p.skip + pc.j);
       phys = (phys < 0 || phys >= p.NB) ? 0 : phys;  // never copy outside the pool
       const int kvh = pc.u / p.nsg;
       const int row = (phys * p.Hkv + kvh) * BS;
@@ -833,7 +856,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         mbar_wait_bounded(bar(k2 % kStages), uint32_t(k2 / kStages) & 1u, p.timeout_ns);
       return;
     }
-    path.block(p, sK(st), sV(st), sKs(st), sVs(st), Lc - cc.j * BS);
+    path.block(p, sK(st), sV(st), sKs(st), sVs(st), Lc - (p.skip + cc.j) * BS);
     __syncwarp();
     if (i + kStages < nblk) {
       fence_proxy_async_smem();
@@ -843,7 +866,10 @@ __global__ void __launch_bounds__(kWarps * 32)
     const bool seg_end = (cc.j == cc.n - 1) || (i == nblk - 1);
     if (seg_end) {
       const bool complete = (seg_j0 == 0) && (cc.j == cc.n - 1);
-      path.finish(p, complete, partial_slot(w, first_seg));
+      if (complete && p.unit_slot0 >= 0)  // cascade: the suffix result is one more part
+        path.finish(p, false, size_t(p.unit_slot0) + size_t(cc.s) * HU + cc.u);
+      else
+        path.finish(p, complete, partial_slot(w, first_seg));
       first_seg = false;
     }
     cursor_next(cc, s_prefix, B, HU);

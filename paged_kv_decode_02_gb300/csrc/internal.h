@@ -20,6 +20,9 @@ struct DecodeParams {
   float* part_o;               // [2W, GS, D] fp32 partial outputs (unnormalised)
   float* part_ml;              // [2W, GS, 2] fp32 (running max in log2 units, sum)
   int32_t* prefix_out;         // [B+1] blocks-per-sequence exclusive prefix (CTA 0 writes)
+  int skip;                    // table entries skipped at the head of every sequence (cascade)
+  int unit_slot0;              // >= 0: complete units write a partial to slot unit_slot0 + s*HU + u
+                               //       instead of the output (cascade); -1: normal
   int32_t* status;             // optional device status word
   int B, Hq, Hkv, MBS, NB;
   int g;                       // Hq / Hkv
@@ -29,6 +32,38 @@ struct DecodeParams {
   float scale_log2;            // softmax scale * log2(e)
   unsigned long long timeout_ns;
 };
+
+// Parameters of the shared-prefix (cascade) kernel: for KV head h, the B*g query rows
+// (sequence s, group member i) attend the prefix blocks block_tables[0, 0..P-1].
+struct PrefixParams {
+  const void* q;               // [B, Hq, D] bf16
+  const int32_t* prefix_ids;   // [P] physical ids of the shared prefix (row 0 of the tables)
+  float* pre_o;                // [nsplit, Hkv, R, D] unnormalised partial outputs
+  float* pre_ml;               // [nsplit, Hkv, R, 2] (running max in log2 units, sum)
+  int P, B, Hq, Hkv, g, R, NB;  // R = B * g query rows per KV head
+  int nsplit, per_split;       // prefix blocks [z*per_split, min(P, (z+1)*per_split)) for split z
+  float scale_log2;
+  unsigned long long timeout_ns;
+  int32_t* status;
+};
+
+// Parameters of the cascade merge: prefix records plus suffix parts.
+struct CascadeMergeParams {
+  void* out;
+  const float* part_o;         // decode partials: [2W + B*HU, gs, D]
+  const float* part_ml;
+  const float* pre_o;
+  const float* pre_ml;
+  const int32_t* prefix;       // suffix blocks-per-sequence prefix from the decode kernel
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int32_t* status;
+  int B, Hq, Hkv, D, MBS, NB, BS, P;
+  int g, gs, nsg, HU, W, R, nsplit;
+};
+
+bool select_prefix_kernel(int D, int BS, const void** fn, int* smem_bytes);
+void launch_cascade_merge(const CascadeMergeParams& p, cudaStream_t stream);
 
 // Parameters of the split-KV merge launch (units cut between decode workers).
 struct MergeParams {

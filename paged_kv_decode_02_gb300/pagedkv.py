@@ -36,6 +36,7 @@ class Status(enum.IntEnum):
 DEV_BAD_CONTEXT_LEN = 0x1
 DEV_BAD_BLOCK_ID = 0x2
 DEV_TIMEOUT = 0x4
+DEV_BAD_PREFIX = 0x8
 
 KV_BF16 = 0
 KV_INT8 = 1
@@ -69,6 +70,15 @@ EXPORTS = {
     "pkv_decode_int8": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_float, ctypes.c_void_p,
                                                                 ctypes.c_void_p, ctypes.c_size_t,
                                                                 ctypes.c_void_p, ctypes.c_void_p]),
+    "pkv_decode_cascade_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
+                                                          ctypes.POINTER(ctypes.c_size_t)]),
+    "pkv_decode_cascade_bf16": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int32,
+                                                                        ctypes.c_float,
+                                                                        ctypes.c_void_p,
+                                                                        ctypes.c_void_p,
+                                                                        ctypes.c_size_t,
+                                                                        ctypes.c_void_p,
+                                                                        ctypes.c_void_p]),
     "pkv_decode_bf16_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_float,
                                                                         ctypes.c_void_p,
                                                                         ctypes.c_void_p,
@@ -266,3 +276,53 @@ def paged_decode_attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_tab
     fp32 scales ``k_scale``/``v_scale`` [NB, Hkv, bs]."""
     return _decode(True, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                    scale, out, workspace, status)
+
+
+def cascade_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                            num_blocks, max_blocks_per_seq, prefix_blocks, device=None):
+    dims = Dims(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq)
+    out = ctypes.c_size_t(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = _lib().pkv_decode_cascade_workspace_bytes(ctypes.byref(dims), int(prefix_blocks),
+                                                       ctypes.byref(out))
+    _check(st, "pkv_decode_cascade_workspace_bytes")
+    return int(out.value)
+
+
+def paged_decode_attention_cascade(q, k_cache, v_cache, block_tables, context_lens,
+                                   prefix_blocks, scale, out=None, workspace=None, status=None):
+    """Decode attention for a batch whose tables all start with the same
+    ``prefix_blocks`` physical blocks (row 0's): the shared prefix is attended once
+    per KV head for every query row as a dense tensor-core contraction, the suffixes by
+    the ordinary decode. Same result as :func:`paged_decode_attention` (bf16 caches)."""
+    dev = q.device
+    _require(q, "q", torch.bfloat16, 3, dev)
+    _require(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _require(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    if k_cache.shape != v_cache.shape or k_cache.shape[3] != D:
+        raise ValueError("cache shapes disagree with q")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    dims = _dims(B, Hq, k_cache, block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _require(out, "out", torch.bfloat16, 3, dev)
+    with _OnDevice(dev):
+        need = ctypes.c_size_t(0)
+        _check(_lib().pkv_decode_cascade_workspace_bytes(ctypes.byref(dims), int(prefix_blocks),
+                                                         ctypes.byref(need)),
+               "pkv_decode_cascade_workspace_bytes")
+        if workspace is None or workspace.numel() < need.value:
+            workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=dev)
+        st = _lib().pkv_decode_cascade_bf16(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                            _ptr(block_tables), _ptr(context_lens),
+                                            int(prefix_blocks), float(scale), ctypes.byref(dims),
+                                            _ptr(workspace), workspace.numel(), _ptr(status),
+                                            _stream(dev))
+    _check(st, "pkv_decode_cascade_bf16")
+    return out

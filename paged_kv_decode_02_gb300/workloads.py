@@ -233,11 +233,13 @@ def _randn_bf16(shape, gen, device):
 def make_workload(name: str, device="cpu", seed: Optional[int] = None,
                   lengths=None, num_seqs=None, num_q_heads=None, num_kv_heads=None,
                   head_dim=None, block_size=None, num_blocks=None,
-                  poison_unused=False, kv_dtype=None) -> Workload:
+                  poison_unused=False, kv_dtype=None, prefix_tokens=None) -> Workload:
     """Build a named workload (optionally overriding its sizes) on ``device``.
 
     ``poison_unused`` fills every cache row that no request's context covers with NaN
     (bf16) or, for INT8, NaN scales, so that a kernel reading one shows up.
+    ``prefix_tokens`` (a multiple of the block size) puts that many leading tokens of
+    every request in one set of shared, refcounted blocks (2048 for ``prefix``).
     """
     spec = dict(SPECS[name])
     seed = spec["seed"] if seed is None else seed
@@ -254,7 +256,7 @@ def make_workload(name: str, device="cpu", seed: Optional[int] = None,
     B = len(lengths)
     if name == "tiny" and num_blocks is None:
         num_blocks = 64
-    prefix = 2048 if name == "prefix" else 0
+    prefix = (2048 if name == "prefix" else 0) if prefix_tokens is None else int(prefix_tokens)
     tables, last_slots, NB, alloc = build_tables(lengths, bs, rng, num_blocks=num_blocks,
                                                  shared_prefix_tokens=prefix)
     dev = torch.device(device)

@@ -236,3 +236,65 @@ def test_decode_full_size_sampled(pk, name):
     pairs = sample_pairs(w, 24)
     ref = oracle_outputs(w, pairs)
     assert max_err(out, ref, pairs) <= DECODE_ATOL
+
+
+# ---------------------------------------------------------------------------
+# cascade decode for a prefix shared by the whole batch
+# ---------------------------------------------------------------------------
+
+def _cascade(pk, w, prefix_blocks, **kw):
+    return pk.paged_decode_attention_cascade(w.q, w.k_cache, w.v_cache, w.block_tables,
+                                             w.context_lens, prefix_blocks, w.scale, **kw)
+
+
+CASCADE_SHAPES = [
+    # (Hq, Hkv, D, bs, prefix tokens, suffix lengths)
+    (32, 8, 128, 16, 160, [16, 1, 33, 0, 200, 7]),
+    (16, 16, 128, 16, 64, [5, 100, 0]),
+    (8, 2, 64, 32, 96, [40, 3, 64, 1, 500]),
+    (64, 4, 128, 32, 32, [10, 70]),
+    (12, 4, 64, 16, 48, [0, 0, 9]),
+]
+
+
+@pytest.mark.parametrize("shape", CASCADE_SHAPES, ids=[f"c{i}" for i in range(len(CASCADE_SHAPES))])
+def test_cascade_small_shapes(pk, shape):
+    Hq, Hkv, D, bs, pre, suf = shape
+    lengths = [pre + x for x in suf]
+    w = make_workload("prefix", device=DEV, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                      block_size=bs, lengths=lengths, prefix_tokens=pre, seed=13,
+                      poison_unused=True)
+    out = _cascade(pk, w, pre // bs)
+    torch.cuda.synchronize()
+    ref = oracle_outputs(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+    plain = _decode(pk, w)
+    torch.cuda.synchronize()
+    assert float((out.float() - plain.float()).abs().max()) <= DECODE_ATOL
+
+
+def test_cascade_full_prefix_workload(pk):
+    w = make_workload("prefix", device=DEV)
+    out = _cascade(pk, w, 2048 // w.block_size)
+    torch.cuda.synchronize()
+    pairs = sample_pairs(w, 24)
+    ref = oracle_outputs(w, pairs)
+    assert max_err(out, ref, pairs) <= DECODE_ATOL
+
+
+def test_cascade_flags_a_table_without_the_prefix(pk):
+    pre, bs = 64, 16
+    w = make_workload("prefix", device=DEV, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                      lengths=[pre + 20, pre + 5, pre + 40], prefix_tokens=pre, seed=14)
+    bt = w.block_tables.clone()
+    bt[1, 2] = (w.block_tables[1, 2] + 1) % w.num_blocks     # no longer the shared block
+    w.block_tables = bt
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = _cascade(pk, w, pre // bs, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x8
+    got = to_f64(out)
+    assert np.all(got[1] == 0)
+    good = [(s, h) for s in (0, 2) for h in range(16)]
+    ref = oracle_outputs(w, good)
+    assert max_err(out, ref, good) <= DECODE_ATOL

@@ -35,4 +35,12 @@ from .paged_attention import (  # noqa: F401
     attend_one_head,
     decode_attention,
     decode_attention_int8,
+    FP8_MAX,
+    fp8_decode,
+    fp8_round,
+    quantize_rows_fp8,
+    dequantize_rows_fp8,
+    append_scatter_fp8,
+    gather_sequence_fp8,
+    decode_attention_fp8,
 )

@@ -124,6 +124,103 @@ def append_scatter_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, 
 
 
 # ---------------------------------------------------------------------------
+# FP8 KV -- "FP8（及 H100/H200 硬件路径）" and "KV 缓存量化" of the chenk.top page:
+# E4M3 (4 exponent, 3 mantissa bits) and E5M2 (5 exponent, 2 mantissa bits), the
+# latter named for KV caches, with per-token scales computed online. The formats are
+# taken as their usual definitions: E4M3 has exponent bias 7, no infinities, one NaN
+# mantissa pattern (S.1111.111) and largest finite value 448; E5M2 has bias 15 and
+# IEEE-style infinities/NaN, largest finite value 57344.
+# ---------------------------------------------------------------------------
+
+FP8_FORMATS = {"e4m3": (4, 3, 7), "e5m2": (5, 2, 15)}
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
+
+
+def fp8_decode(codes, fmt):
+    """Exact value (float64) of each FP8 byte code; NaN for NaN codes, +-inf for the
+    E5M2 infinities."""
+    e_bits, m_bits, bias = FP8_FORMATS[fmt]
+    c = np.asarray(codes, dtype=np.int64) & 0xFF
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> m_bits) & ((1 << e_bits) - 1)
+    m = c & ((1 << m_bits) - 1)
+    frac = m / float(1 << m_bits)
+    normal = (1.0 + frac) * np.power(2.0, e - bias)
+    sub = frac * 2.0 ** (1 - bias)
+    val = np.where(e == 0, sub, normal)
+    if fmt == "e4m3":
+        val = np.where((e == 15) & (m == 7), np.nan, val)
+    else:
+        val = np.where(e == 31, np.where(m == 0, np.inf, np.nan), val)
+    return sign * val
+
+
+def _fp8_finite_table(fmt):
+    """(values ascending, codes) of every finite non-negative FP8 value."""
+    codes = np.arange(0, 128)
+    vals = fp8_decode(codes, fmt)
+    keep = np.isfinite(vals)
+    return vals[keep], codes[keep]
+
+
+def fp8_round(x, fmt):
+    """Round float32 values to the nearest FP8 code (ties to the even mantissa, i.e.
+    the even code), saturating to the largest finite value; returns uint8 codes."""
+    vals, codes = _fp8_finite_table(fmt)
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    out = np.zeros(x.shape, dtype=np.uint8)
+    flat_a, flat_out = a.reshape(-1), out.reshape(-1)
+    neg = (x.reshape(-1) < 0)
+    for i, v in enumerate(flat_a):
+        if v >= vals[-1]:
+            c = codes[-1]
+        else:
+            d = np.abs(vals - v)
+            best = np.flatnonzero(d == d.min())
+            c = codes[best[0]] if len(best) == 1 else codes[best[np.argmin(codes[best] % 2)]]
+        flat_out[i] = (int(c) | (0x80 if neg[i] else 0)) if not (c == 0 and neg[i]) else 0x80
+    return out
+
+
+def quantize_rows_fp8(x, fmt):
+    """Per-row FP8 quantisation in IEEE fp32: s = absmax / FP8_MAX, code =
+    round_fp8(x / s); absmax = 0 gives s = 0 and zero codes. Returns (uint8 codes, s)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    s = (amax / np.float32(FP8_MAX[fmt])).astype(np.float32)
+    codes = np.zeros(x32.shape, dtype=np.uint8)
+    nz = s > 0
+    if np.any(nz):
+        ratio = (x32[nz] / s[nz][..., None]).astype(np.float32)
+        codes[nz] = fp8_round(ratio, fmt)
+    return codes, s
+
+
+def dequantize_rows_fp8(codes, s, fmt):
+    return fp8_decode(codes, fmt) * np.asarray(s, dtype=np.float64)[..., None]
+
+
+def append_scatter_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, block_size, fmt):
+    """Quantise each new token's K and V rows per KV head to FP8, then scatter codes
+    (uint8) and scales. Returns new arrays."""
+    kq, ks = quantize_rows_fp8(k, fmt)
+    vq, vs = quantize_rows_fp8(v, fmt)
+    kc, vc, ksc, vsc = [np.array(a, copy=True) for a in (k_cache, v_cache, k_scale, v_scale)]
+    for t in range(len(slot_mapping)):
+        slot = int(slot_mapping[t])
+        if slot < 0:
+            continue
+        blk, off = slot // block_size, slot % block_size
+        for h in range(k.shape[1]):
+            kc[blk, h, off, :] = kq[t, h, :]
+            vc[blk, h, off, :] = vq[t, h, :]
+            ksc[blk, h, off] = ks[t, h]
+            vsc[blk, h, off] = vs[t, h]
+    return kc, vc, ksc, vsc
+
+
+# ---------------------------------------------------------------------------
 # Decode attention -- "两个特性截然不同的阶段" of the chenk.top page: one new query
 # per request attends over that request's whole cached K/V; "分页注意力" of the same
 # page: the cached tokens are reached through the request's block table.
@@ -227,4 +324,35 @@ def decode_attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
                 if _kv_head_of(h, g) != kvh:
                     continue
                 out[s, h], _ = attend_one_head(q[s, h], K, V, scale)
+    return out
+
+
+def gather_sequence_fp8(codes, scales, block_table_row, context_len, kv_head, block_size, fmt):
+    """Real [L, D] float64 values of one sequence's FP8 rows: decoded code times scale."""
+    c = gather_sequence(codes, block_table_row, context_len, kv_head, block_size)
+    L = int(context_len)
+    val = fp8_decode(c.astype(np.int64), fmt) if L else c
+    s = np.array([float(scales[int(block_table_row[t // block_size]), kv_head, t % block_size])
+                  for t in range(L)], dtype=np.float64)
+    return val * s[:, None] if L else val
+
+
+def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                         scale, fmt, block_size=None):
+    """Paged decode attention over an FP8 cache (codes decoded exactly, times their
+    fp32 per-(token, head) scales), then the same attention as decode_attention."""
+    q = np.asarray(q)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    bs = int(block_size) if block_size is not None else k_cache.shape[2]
+    g = Hq // Hkv
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    for s in range(B):
+        L = int(context_lens[s])
+        for kvh in range(Hkv):
+            K = gather_sequence_fp8(k_cache, k_scale, block_tables[s], L, kvh, bs, fmt)
+            V = gather_sequence_fp8(v_cache, v_scale, block_tables[s], L, kvh, bs, fmt)
+            for h in range(Hq):
+                if _kv_head_of(h, g) == kvh:
+                    out[s, h], _ = attend_one_head(q[s, h], K, V, scale)
     return out

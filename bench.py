@@ -41,6 +41,10 @@ WORKLOAD_TEXT = {
             "per-token per-head fp32 scales",
     "int8-bs16": "INT8 KV: batch 128, 32 q / 8 kv heads, head_dim 128, context 8192, block 16, "
                  "per-token per-head fp32 scales",
+    "fp8-e5m2": "FP8 E5M2 KV: batch 128, 32 q / 8 kv heads, head_dim 128, context 8192, "
+                "block 32, per-token per-head fp32 scales",
+    "fp8-e4m3": "FP8 E4M3 KV: batch 128, 32 q / 8 kv heads, head_dim 128, context 8192, "
+                "block 32, per-token per-head fp32 scales",
 }
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
@@ -66,13 +70,18 @@ def parse_args():
 # Byte accounting (algorithmic: what the method must move at least once)
 # ---------------------------------------------------------------------------
 
+def _one_byte(w):
+    """INT8 and FP8 caches: one-byte codes plus one fp32 scale per (token, KV head)."""
+    return w.kv_dtype != "bf16"
+
+
 def decode_bytes(w):
     import numpy as np
     L = w.context_lens.cpu().numpy().astype(np.int64)
-    elt = 1 if w.kv_dtype == "int8" else 2
+    elt = 1 if _one_byte(w) else 2
     tokens = int(L.sum())
     kv = tokens * 2 * w.num_kv_heads * w.head_dim * elt
-    scales = tokens * 2 * w.num_kv_heads * 4 if w.kv_dtype == "int8" else 0
+    scales = tokens * 2 * w.num_kv_heads * 4 if _one_byte(w) else 0
     qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * 2
     tables = int(sum(-(-int(x) // w.block_size) for x in L)) * 4
     return {"kv": kv, "scales": scales, "q_out": qo, "tables": tables + 4 * w.num_seqs,
@@ -81,9 +90,9 @@ def decode_bytes(w):
 
 def append_bytes(w):
     T = int((w.slot_mapping >= 0).sum().item())
-    elt = 1 if w.kv_dtype == "int8" else 2
+    elt = 1 if _one_byte(w) else 2
     rows = T * 2 * w.num_kv_heads * w.head_dim
-    scales = T * 2 * w.num_kv_heads * 4 if w.kv_dtype == "int8" else 0
+    scales = T * 2 * w.num_kv_heads * 4 if _one_byte(w) else 0
     return rows * 2 + rows * elt + scales + 8 * w.num_seqs
 
 
@@ -98,7 +107,7 @@ def unique_kv_bytes(w):
         for j in range(n):
             fill = min(w.block_size, int(Ls) - j * w.block_size)
             seen[int(bt[s, j])] = max(seen.get(int(bt[s, j]), 0), fill)
-    elt = 1 if w.kv_dtype == "int8" else 2
+    elt = 1 if _one_byte(w) else 2
     return sum(seen.values()) * 2 * w.num_kv_heads * w.head_dim * elt
 
 
@@ -217,7 +226,7 @@ def _host_units(w, count, seed=0):
         blocks = w.block_tables[s, :n].to(torch.int64)
         unit = {"L": L, "q": w.q[s, kvh * g:(kvh + 1) * g].double().cpu().numpy(),
                 "table": np.arange(n)}
-        if w.kv_dtype == "int8":
+        if _one_byte(w):
             unit["k"] = w.k_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
             unit["v"] = w.v_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
             unit["ks"] = w.k_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
@@ -234,6 +243,10 @@ def _oracle_unit(w, u):
     if w.kv_dtype == "int8":
         K = oracle.gather_sequence_int8(u["k"], u["ks"], u["table"], u["L"], 0, w.block_size)
         V = oracle.gather_sequence_int8(u["v"], u["vs"], u["table"], u["L"], 0, w.block_size)
+    elif w.kv_dtype.startswith("fp8_"):
+        f = w.kv_dtype[4:]
+        K = oracle.gather_sequence_fp8(u["k"], u["ks"], u["table"], u["L"], 0, w.block_size, f)
+        V = oracle.gather_sequence_fp8(u["v"], u["vs"], u["table"], u["L"], 0, w.block_size, f)
     else:
         K = oracle.gather_sequence(u["k"], u["table"], u["L"], 0, w.block_size)
         V = oracle.gather_sequence(u["v"], u["table"], u["L"], 0, w.block_size)
@@ -242,10 +255,10 @@ def _oracle_unit(w, u):
 
 
 def _unit_bytes(w, u):
-    elt = 1 if w.kv_dtype == "int8" else 2
+    elt = 1 if _one_byte(w) else 2
     g = w.num_q_heads // w.num_kv_heads
     b = u["L"] * 2 * w.head_dim * elt + 2 * g * w.head_dim * 2 + 4 * len(u["table"])
-    if w.kv_dtype == "int8":
+    if _one_byte(w):
         b += u["L"] * 2 * 4
     return b
 
@@ -273,6 +286,38 @@ def cpu_baseline(w, seconds):
 # The GPU step
 # ---------------------------------------------------------------------------
 
+def _kv_code(pk, w):
+    return {"bf16": pk.pagedkv.KV_BF16, "int8": pk.pagedkv.KV_INT8,
+            "fp8_e4m3": pk.pagedkv.KV_FP8_E4M3, "fp8_e5m2": pk.pagedkv.KV_FP8_E5M2}[w.kv_dtype]
+
+
+def api_append(pk, w, k, v, slots):
+    """The append call for the workload's cache dtype."""
+    if w.kv_dtype == "int8":
+        pk.paged_kv_append_int8(k, v, w.k_cache, w.v_cache, w.k_scale, w.v_scale, slots)
+    elif w.kv_dtype.startswith("fp8_"):
+        pk.paged_kv_append_fp8(k, v, w.k_cache, w.v_cache, w.k_scale, w.v_scale, slots,
+                               fmt=w.kv_dtype[4:])
+    else:
+        pk.paged_kv_append(k, v, w.k_cache, w.v_cache, slots)
+
+
+def api_decode(pk, w, q, tables, lens, out, ws, cascade_blocks=0):
+    """The decode call for the workload's cache dtype (cascade when asked)."""
+    if w.kv_dtype == "int8":
+        pk.paged_decode_attention_int8(q, w.k_cache, w.v_cache, w.k_scale, w.v_scale, tables,
+                                       lens, w.scale, out=out, workspace=ws)
+    elif w.kv_dtype.startswith("fp8_"):
+        pk.paged_decode_attention_fp8(q, w.k_cache, w.v_cache, w.k_scale, w.v_scale, tables,
+                                      lens, w.scale, fmt=w.kv_dtype[4:], out=out, workspace=ws)
+    elif cascade_blocks:
+        pk.paged_decode_attention_cascade(q, w.k_cache, w.v_cache, tables, lens, cascade_blocks,
+                                          w.scale, out=out, workspace=ws)
+    else:
+        pk.paged_decode_attention(q, w.k_cache, w.v_cache, tables, lens, w.scale, out=out,
+                                  workspace=ws)
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -288,9 +333,8 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     pk.load_library()
     w = make_workload(args.config, device=dev)
-    int8 = w.kv_dtype == "int8"
     cascade_blocks = w.extra.get("prefix_tokens", 0) // w.block_size if args.cascade else 0
-    if args.cascade and (int8 or cascade_blocks == 0):
+    if args.cascade and (_one_byte(w) or cascade_blocks == 0):
         raise SystemExit("--cascade needs a bf16 workload with a shared prefix (prefix)")
     if cascade_blocks:
         need = pk.cascade_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
@@ -299,30 +343,16 @@ def run_ours(args, rank, world):
     else:
         need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                          w.block_size, w.num_blocks, w.max_blocks_per_seq,
-                                         pk.pagedkv.KV_INT8 if int8 else pk.pagedkv.KV_BF16)
+                                         _kv_code(pk, w))
     ws = torch.zeros(need, dtype=torch.uint8, device=dev)
     out = torch.empty_like(w.q)
     stream = torch.cuda.current_stream(dev)
 
     def append():
-        if int8:
-            pk.paged_kv_append_int8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
-                                    w.slot_mapping)
-        else:
-            pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
+        api_append(pk, w, w.new_k, w.new_v, w.slot_mapping)
 
     def decode():
-        if int8:
-            pk.paged_decode_attention_int8(w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
-                                           w.block_tables, w.context_lens, w.scale, out=out,
-                                           workspace=ws)
-        elif cascade_blocks:
-            pk.paged_decode_attention_cascade(w.q, w.k_cache, w.v_cache, w.block_tables,
-                                              w.context_lens, cascade_blocks, w.scale, out=out,
-                                              workspace=ws)
-        else:
-            pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
-                                      w.scale, out=out, workspace=ws)
+        api_decode(pk, w, w.q, w.block_tables, w.context_lens, out, ws, cascade_blocks)
 
     for _ in range(max(args.warmup, 3)):
         append()
@@ -452,7 +482,6 @@ def run_e2e(args, w, pk, dev, append_dev, out, ws, step_bytes, world, cascade_bl
     step's inputs host->device, append + decode, copy the output device->host."""
     import torch
     stream = torch.cuda.current_stream(dev)
-    int8 = w.kv_dtype == "int8"
     host_in = {n: getattr(w, n).cpu().pin_memory()
                for n in ("q", "new_k", "new_v", "slot_mapping", "block_tables", "context_lens")}
     dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
@@ -463,24 +492,9 @@ def run_e2e(args, w, pk, dev, append_dev, out, ws, step_bytes, world, cascade_bl
     def step():
         for n, t in host_in.items():
             dev_in[n].copy_(t, non_blocking=True)
-        if int8:
-            pk.paged_kv_append_int8(dev_in["new_k"], dev_in["new_v"], w.k_cache, w.v_cache,
-                                    w.k_scale, w.v_scale, dev_in["slot_mapping"])
-            pk.paged_decode_attention_int8(dev_in["q"], w.k_cache, w.v_cache, w.k_scale,
-                                           w.v_scale, dev_in["block_tables"],
-                                           dev_in["context_lens"], w.scale, out=out,
-                                           workspace=ws)
-        else:
-            pk.paged_kv_append(dev_in["new_k"], dev_in["new_v"], w.k_cache, w.v_cache,
-                               dev_in["slot_mapping"])
-            if cascade_blocks:
-                pk.paged_decode_attention_cascade(dev_in["q"], w.k_cache, w.v_cache,
-                                                  dev_in["block_tables"], dev_in["context_lens"],
-                                                  cascade_blocks, w.scale, out=out, workspace=ws)
-            else:
-                pk.paged_decode_attention(dev_in["q"], w.k_cache, w.v_cache,
-                                          dev_in["block_tables"], dev_in["context_lens"], w.scale,
-                                          out=out, workspace=ws)
+        api_append(pk, w, dev_in["new_k"], dev_in["new_v"], dev_in["slot_mapping"])
+        api_decode(pk, w, dev_in["q"], dev_in["block_tables"], dev_in["context_lens"], out, ws,
+                   cascade_blocks)
         host_out.copy_(out, non_blocking=True)
 
     for _ in range(3):

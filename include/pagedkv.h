@@ -20,8 +20,9 @@
  *   - Layouts (row-major, contiguous):
  *       q, out          [num_seqs, num_q_heads, head_dim]            bf16
  *       k, v (new)      [num_tokens, num_kv_heads, head_dim]         bf16
- *       k_cache,v_cache [num_blocks, num_kv_heads, block_size, head_dim]  bf16 or int8
- *       k_scale,v_scale [num_blocks, num_kv_heads, block_size]       fp32 (int8 only)
+ *       k_cache,v_cache [num_blocks, num_kv_heads, block_size, head_dim]  bf16, int8
+ *                       or FP8 (E4M3 / E5M2) byte codes
+ *       k_scale,v_scale [num_blocks, num_kv_heads, block_size]       fp32 (one-byte caches)
  *       block_tables    [num_seqs, max_blocks_per_seq]               int32
  *       context_lens    [num_seqs]                                   int32
  *       slot_mapping    [num_tokens]                                 int64
@@ -61,7 +62,9 @@ typedef enum pkv_status {
 
 typedef enum pkv_kv_dtype {
   PKV_KV_BF16 = 0,
-  PKV_KV_INT8 = 1            /* int8 codes + one fp32 scale per (token, KV head) */
+  PKV_KV_INT8 = 1,           /* int8 codes + one fp32 scale per (token, KV head) */
+  PKV_KV_FP8_E4M3 = 2,       /* FP8 E4M3 codes (bias 7, max 448) + fp32 scales */
+  PKV_KV_FP8_E5M2 = 3        /* FP8 E5M2 codes (bias 15, max 57344) + fp32 scales */
 } pkv_kv_dtype;
 
 typedef struct pkv_dims {
@@ -117,7 +120,7 @@ pkv_status pkv_append_int8(const void* k, const void* v, int8_t* k_cache, int8_t
 
 /*
  * pkv_decode_workspace_bytes -- size of the device workspace that pkv_decode_bf16 /
- * pkv_decode_int8 need for these dims and KV dtype on the CURRENT device (it
+ * pkv_decode_int8 / pkv_decode_fp8 need for these dims and KV dtype on the CURRENT device (it
  * depends on the device's SM count). Host-only query; writes *bytes.
  */
 pkv_status pkv_decode_workspace_bytes(const pkv_dims* dims, pkv_kv_dtype kv_dtype,
@@ -153,6 +156,38 @@ pkv_status pkv_decode_int8(void* out, const void* q, const int8_t* k_cache,
                            const int32_t* block_tables, const int32_t* context_lens,
                            float scale, const pkv_dims* dims, void* workspace,
                            size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
+
+/*
+ * pkv_append_fp8 -- as pkv_append_int8 with FP8 codes: the E4M3 or E5M2 KV cache of
+ * "FP8（及 H100/H200 硬件路径）" (chenk.top page; E5M2 is the format it names for KV
+ * caches) with the per-token, per-head scales of "KV 缓存量化" (same page), computed
+ * from the row itself at append time:
+ *   s = absmax(row) / FP8_MAX (FP8_MAX = 448 for E4M3, 57344 for E5M2; IEEE fp32
+ *   division); code = x / s (IEEE division) rounded to the nearest FP8 value, ties to
+ *   the even code, saturating at +-FP8_MAX; absmax == 0 gives s = 0 and zero codes.
+ *   A value that rounds to zero from below keeps its sign bit (code 0x80).
+ *   fp8_format  PKV_KV_FP8_E4M3 or PKV_KV_FP8_E5M2 (else PKV_ERR_DTYPE).
+ *   k_cache, v_cache  uint8 codes [num_blocks, Hkv, block_size, D], written.
+ *   k_scale, v_scale  fp32 [num_blocks, Hkv, block_size], written.
+ */
+pkv_status pkv_append_fp8(const void* k, const void* v, uint8_t* k_cache, uint8_t* v_cache,
+                          float* k_scale, float* v_scale, const int64_t* slot_mapping,
+                          int32_t num_tokens, pkv_kv_dtype fp8_format, const pkv_dims* dims,
+                          pkv_stream_t stream);
+
+/*
+ * pkv_decode_fp8 -- as pkv_decode_bf16 over an FP8 cache: the cached value of a row
+ * element is decode(code) * scale with the row's fp32 scale (k_scale for K, v_scale
+ * for V); codes are widened exactly. The V side folds scale * 2^15 (E5M2) or
+ * scale * 2^8 (E4M3) into fp16 softmax weights, so rows written by pkv_append_fp8
+ * must have absmax below about 1e5. NaN codes are not expected (the append never
+ * writes them). Workspace as pkv_decode_workspace_bytes(dims, fp8_format).
+ */
+pkv_status pkv_decode_fp8(void* out, const void* q, const uint8_t* k_cache,
+                          const uint8_t* v_cache, const float* k_scale, const float* v_scale,
+                          const int32_t* block_tables, const int32_t* context_lens, float scale,
+                          pkv_kv_dtype fp8_format, const pkv_dims* dims, void* workspace,
+                          size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
 
 /*
  * pkv_decode_cascade_bf16 -- pkv_decode_bf16 for a batch whose sequences all start

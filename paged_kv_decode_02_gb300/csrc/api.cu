@@ -68,9 +68,9 @@ bool make_cache_map(CUtensorMap* map, const void* base, bool int8, int D, long l
 struct MapKey {
   const void* base;
   long long rows;
-  int D, BS, int8;
+  int D, BS, q8;
   bool operator==(const MapKey& o) const {
-    return base == o.base && rows == o.rows && D == o.D && BS == o.BS && int8 == o.int8;
+    return base == o.base && rows == o.rows && D == o.D && BS == o.BS && q8 == o.q8;
   }
 };
 constexpr int kMapCache = 16;
@@ -79,15 +79,15 @@ MapKey g_map_keys[kMapCache];
 CUtensorMap g_maps[kMapCache];
 int g_map_count = 0, g_map_next = 0;
 
-bool cache_map(CUtensorMap* map, const void* base, bool int8, int D, long long rows, int BS) {
-  const MapKey key{base, rows, D, BS, int8 ? 1 : 0};
+bool cache_map(CUtensorMap* map, const void* base, bool q8, int D, long long rows, int BS) {
+  const MapKey key{base, rows, D, BS, q8 ? 1 : 0};
   std::lock_guard<std::mutex> lock(g_map_mu);
   for (int i = 0; i < g_map_count; ++i)
     if (g_map_keys[i] == key) {
       *map = g_maps[i];
       return true;
     }
-  if (!make_cache_map(map, base, int8, D, rows, BS)) return false;
+  if (!make_cache_map(map, base, q8, D, rows, BS)) return false;
   g_map_keys[g_map_next] = key;
   g_maps[g_map_next] = *map;
   g_map_next = (g_map_next + 1) % kMapCache;
@@ -124,9 +124,9 @@ pkv_status check_dims(const pkv_dims* d) {
 // sets a kernel attribute, which costs tens of microseconds, so recent plans are kept.
 struct PlanKey {
   pkv_dims d;
-  int int8, device;
+  int kvt, device;
   bool operator==(const PlanKey& o) const {
-    return std::memcmp(&d, &o.d, sizeof(d)) == 0 && int8 == o.int8 && device == o.device;
+    return std::memcmp(&d, &o.d, sizeof(d)) == 0 && kvt == o.kvt && device == o.device;
   }
 };
 constexpr int kPlanCache = 16;
@@ -135,9 +135,9 @@ PlanKey g_plan_keys[kPlanCache];
 Plan g_plans[kPlanCache];
 int g_plan_count = 0, g_plan_next = 0;
 
-pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl);
+pkv_status make_plan_uncached(const pkv_dims* d, int kvt, Plan* pl);
 
-pkv_status make_plan(const pkv_dims* d, bool int8, Plan* pl) {
+pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl) {
   pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
   int dev = 0;
@@ -145,7 +145,7 @@ pkv_status make_plan(const pkv_dims* d, bool int8, Plan* pl) {
   PlanKey key;
   std::memset(&key, 0, sizeof(key));
   key.d = *d;
-  key.int8 = int8 ? 1 : 0;
+  key.kvt = kvt;
   key.device = dev;
   std::lock_guard<std::mutex> lock(g_plan_mu);
   for (int i = 0; i < g_plan_count; ++i)
@@ -153,7 +153,7 @@ pkv_status make_plan(const pkv_dims* d, bool int8, Plan* pl) {
       *pl = g_plans[i];
       return PKV_OK;
     }
-  st = make_plan_uncached(d, int8, pl);
+  st = make_plan_uncached(d, kvt, pl);
   if (st != PKV_OK) return st;
   g_plan_keys[g_plan_next] = key;
   g_plans[g_plan_next] = *pl;
@@ -162,7 +162,7 @@ pkv_status make_plan(const pkv_dims* d, bool int8, Plan* pl) {
   return PKV_OK;
 }
 
-pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl) {
+pkv_status make_plan_uncached(const pkv_dims* d, int kvt, Plan* pl) {
   Plan P{};
   P.g = d->num_q_heads / d->num_kv_heads;
   const bool mma = P.g >= 4;
@@ -177,8 +177,18 @@ pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl) {
   }
   P.HU = d->num_kv_heads * P.nsg;
   const int simt = mma ? 0 : P.g;
-  const bool found = int8 ? select_decode_int8(d->head_dim, d->block_size, simt, &P.k)
-                          : select_decode_bf16(d->head_dim, d->block_size, simt, &P.k);
+  bool found = false;
+  switch (kvt) {
+    case PKV_KV_BF16: found = select_decode_bf16(d->head_dim, d->block_size, simt, &P.k); break;
+    case PKV_KV_INT8: found = select_decode_int8(d->head_dim, d->block_size, simt, &P.k); break;
+    case PKV_KV_FP8_E4M3:
+      found = select_decode_e4m3(d->head_dim, d->block_size, simt, &P.k);
+      break;
+    case PKV_KV_FP8_E5M2:
+      found = select_decode_e5m2(d->head_dim, d->block_size, simt, &P.k);
+      break;
+    default: return PKV_ERR_DTYPE;
+  }
   if (!found) return PKV_ERR_UNSUPPORTED;
   P.smem = size_t(P.k.warps) * P.k.warp_smem + 1024 + align_up(size_t(d->num_seqs + 1) * 4, 16);
 
@@ -212,7 +222,7 @@ pkv_status make_plan_uncached(const pkv_dims* d, bool int8, Plan* pl) {
   return PKV_OK;
 }
 
-pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
+pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
                       const void* v_cache, const float* k_scale, const float* v_scale,
                       const int32_t* block_tables, const int32_t* context_lens, float scale,
                       const pkv_dims* d, void* workspace, size_t workspace_bytes,
@@ -222,12 +232,13 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
   if (d->num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PKV_ERR_NULL;
-  if (int8 && (!k_scale || !v_scale)) return PKV_ERR_NULL;
+  const bool q8 = kvt != PKV_KV_BF16;
+  if (q8 && (!k_scale || !v_scale)) return PKV_ERR_NULL;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      (int8 && (!aligned16(k_scale) || !aligned16(v_scale))))
+      (q8 && (!aligned16(k_scale) || !aligned16(v_scale))))
     return PKV_ERR_ALIGNMENT;
   Plan P;
-  st = make_plan(d, int8, &P);
+  st = make_plan(d, kvt, &P);
   if (st != PKV_OK) return st;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < P.ws_bytes)
@@ -235,8 +246,8 @@ pkv_status run_decode(bool int8, void* out, const void* q, const void* k_cache,
 
   const long long rows = (long long)d->num_blocks * d->num_kv_heads * d->block_size;
   CUtensorMap tmk, tmv;
-  if (!cache_map(&tmk, k_cache, int8, d->head_dim, rows, d->block_size) ||
-      !cache_map(&tmv, v_cache, int8, d->head_dim, rows, d->block_size))
+  if (!cache_map(&tmk, k_cache, q8, d->head_dim, rows, d->block_size) ||
+      !cache_map(&tmv, v_cache, q8, d->head_dim, rows, d->block_size))
     return PKV_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -305,7 +316,7 @@ struct CascadePlan {
 };
 
 pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* cp) {
-  pkv_status st = make_plan(d, false, &cp->dec);
+  pkv_status st = make_plan(d, PKV_KV_BF16, &cp->dec);
   if (st != PKV_OK) return st;
   if (prefix_blocks < 1 || prefix_blocks > d->max_blocks_per_seq) return PKV_ERR_SHAPE;
   if (!select_prefix_kernel(d->head_dim, d->block_size, &cp->pfn, &cp->psmem))
@@ -496,7 +507,7 @@ pkv_status pkv_append_int8(const void* k, const void* v, int8_t* k_cache, int8_t
   pkv_status st = check_append(k, v, k_cache, v_cache, slot_mapping, num_tokens, dims);
   if (st != PKV_OK || num_tokens == 0) return st;
   if (!k_scale || !v_scale) return PKV_ERR_NULL;
-  if (launch_append_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
+  if (launch_append_q8(CODE_I8, k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
                          dims->num_kv_heads, dims->head_dim, dims->block_size, dims->num_blocks,
                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PKV_ERR_CUDA;
@@ -506,9 +517,9 @@ pkv_status pkv_append_int8(const void* k, const void* v, int8_t* k_cache, int8_t
 pkv_status pkv_decode_workspace_bytes(const pkv_dims* dims, pkv_kv_dtype kv_dtype,
                                       size_t* bytes) {
   if (!bytes) return PKV_ERR_NULL;
-  if (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_INT8) return PKV_ERR_DTYPE;
+  if (kv_dtype < PKV_KV_BF16 || kv_dtype > PKV_KV_FP8_E5M2) return PKV_ERR_DTYPE;
   Plan P;
-  pkv_status st = make_plan(dims, kv_dtype == PKV_KV_INT8, &P);
+  pkv_status st = make_plan(dims, kv_dtype, &P);
   if (st != PKV_OK) return st;
   *bytes = P.ws_bytes;
   return PKV_OK;
@@ -518,7 +529,7 @@ pkv_status pkv_decode_bf16(void* out, const void* q, const void* k_cache, const 
                            const int32_t* block_tables, const int32_t* context_lens,
                            float scale, const pkv_dims* dims, void* workspace,
                            size_t workspace_bytes, int32_t* status, pkv_stream_t stream) {
-  return run_decode(false, out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
+  return run_decode(PKV_KV_BF16, out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
                     context_lens, scale, dims, workspace, workspace_bytes, status,
                     reinterpret_cast<cudaStream_t>(stream));
 }
@@ -548,8 +559,36 @@ pkv_status pkv_decode_int8(void* out, const void* q, const int8_t* k_cache,
                            const int32_t* block_tables, const int32_t* context_lens,
                            float scale, const pkv_dims* dims, void* workspace,
                            size_t workspace_bytes, int32_t* status, pkv_stream_t stream) {
-  return run_decode(true, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+  return run_decode(PKV_KV_INT8, out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                    context_lens,
                     scale, dims, workspace, workspace_bytes, status,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_append_fp8(const void* k, const void* v, uint8_t* k_cache, uint8_t* v_cache,
+                          float* k_scale, float* v_scale, const int64_t* slot_mapping,
+                          int32_t num_tokens, pkv_kv_dtype fp8_format, const pkv_dims* dims,
+                          pkv_stream_t stream) {
+  if (fp8_format != PKV_KV_FP8_E4M3 && fp8_format != PKV_KV_FP8_E5M2) return PKV_ERR_DTYPE;
+  pkv_status st = check_append(k, v, k_cache, v_cache, slot_mapping, num_tokens, dims);
+  if (st != PKV_OK || num_tokens == 0) return st;
+  if (!k_scale || !v_scale) return PKV_ERR_NULL;
+  const int code = fp8_format == PKV_KV_FP8_E4M3 ? CODE_E4M3 : CODE_E5M2;
+  if (launch_append_q8(code, k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
+                       dims->num_kv_heads, dims->head_dim, dims->block_size, dims->num_blocks,
+                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_fp8(void* out, const void* q, const uint8_t* k_cache,
+                          const uint8_t* v_cache, const float* k_scale, const float* v_scale,
+                          const int32_t* block_tables, const int32_t* context_lens, float scale,
+                          pkv_kv_dtype fp8_format, const pkv_dims* dims, void* workspace,
+                          size_t workspace_bytes, int32_t* status, pkv_stream_t stream) {
+  if (fp8_format != PKV_KV_FP8_E4M3 && fp8_format != PKV_KV_FP8_E5M2) return PKV_ERR_DTYPE;
+  return run_decode(fp8_format, out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                    context_lens, scale, dims, workspace, workspace_bytes, status,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 

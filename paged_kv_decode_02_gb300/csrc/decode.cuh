@@ -19,7 +19,7 @@
 // * Data movement: each warp owns a private ring of shared-memory stages. One lane
 //   reads the block id from the table and issues TMA tensor copies of the block's K
 //   and V tiles (128-byte swizzled, so that the tensor-core fragment loads below are
-//   bank-conflict free) plus, for INT8, 1-D bulk copies of the per-token scales, all
+//   bank-conflict free) plus, for one-byte caches, 1-D bulk copies of the per-token scales, all
 //   completing on that stage's mbarrier. Copies run `stages` blocks ahead of the math.
 // * Math: groups of 4 or more query heads per KV head make q.K^T a small dense
 //   contraction, done with m16n8k16 tensor-core MMAs (query heads on M, padded to 16;
@@ -27,8 +27,9 @@
 //   Smaller groups run on the CUDA cores with 16-byte shared loads and warp-shuffle
 //   reductions. Online softmax in base 2 with a max subtraction keeps the weights
 //   in [0, 1] ("softmax 数值稳定性" note of section 2.3 of the gsyq.cn page).
-// * INT8 KV (section 2.3 of the gsyq.cn page; "KV 缓存量化" of the chenk.top page):
-//   codes are widened exactly to fp16 in registers; the K scale multiplies the fp32
+// * INT8 KV (section 2.3 of the gsyq.cn page; "KV 缓存量化" of the chenk.top page) and
+//   FP8 KV, E4M3 or E5M2 ("FP8（及 H100/H200 硬件路径）", chenk.top): codes are widened
+//   exactly to fp16 in registers (Code8 below); the K scale multiplies the fp32
 //   score and the V scale is folded into the softmax weight before the P.V MMA.
 #pragma once
 
@@ -38,20 +39,72 @@
 namespace pkv {
 
 // ---------------------------------------------------------------------------
+// One-byte KV codes widened exactly to fp16 pairs in registers. pre() is applied
+// once to each loaded 32-bit word of four codes; lo() then yields codes 0 and 1 of
+// the word as an f16x2, hi() codes 2 and 3. The fp16 values times kScale are the
+// codes' values.
+//   INT8: the byte is placed under the fp16 exponent pattern of 1024 and 1152 is
+//         subtracted (after the sign bit of the code is flipped) -- exact.
+//   E5M2: an E5M2 code is the upper byte of the binary16 of the same value, so a
+//         byte permute that puts it there with a zero lower byte is the conversion.
+//   E4M3: S.EEEE.MMM moved to binary16 bits S.0EEEE.MMM0000000 is the code's value
+//         times 2^-8 (exponent biases 7 and 15), normal and subnormal codes alike;
+//         kScale = 2^8 undoes it. (The one NaN pattern maps to a finite value; a
+//         quantiser with saturation never writes it.)
+// ---------------------------------------------------------------------------
+template <int CODE>
+struct Code8;
+
+template <>
+struct Code8<CODE_I8> {
+  static constexpr float kScale = 1.f;
+  __device__ static __forceinline__ uint32_t pre(uint32_t w) { return w ^ 0x80808080u; }
+  __device__ static __forceinline__ uint32_t lo(uint32_t w) {
+    return biased_bytes_to_f16x2(w, 0x4140u);
+  }
+  __device__ static __forceinline__ uint32_t hi(uint32_t w) {
+    return biased_bytes_to_f16x2(w, 0x4342u);
+  }
+};
+
+template <>
+struct Code8<CODE_E5M2> {
+  static constexpr float kScale = 1.f;
+  __device__ static __forceinline__ uint32_t pre(uint32_t w) { return w; }
+  __device__ static __forceinline__ uint32_t lo(uint32_t w) { return prmt(w, 0u, 0x1404u); }
+  __device__ static __forceinline__ uint32_t hi(uint32_t w) { return prmt(w, 0u, 0x3424u); }
+};
+
+template <>
+struct Code8<CODE_E4M3> {
+  static constexpr float kScale = 256.f;
+  __device__ static __forceinline__ uint32_t pre(uint32_t w) { return w; }
+  __device__ static __forceinline__ uint32_t rebias(uint32_t y) {
+    return (y & 0x80008000u) | ((y >> 1) & 0x3F803F80u);
+  }
+  __device__ static __forceinline__ uint32_t lo(uint32_t w) {
+    return rebias(prmt(w, 0u, 0x1404u));
+  }
+  __device__ static __forceinline__ uint32_t hi(uint32_t w) {
+    return rebias(prmt(w, 0u, 0x3424u));
+  }
+};
+
+// ---------------------------------------------------------------------------
 // Tile geometry: a K (or V) tile holds one physical block of one KV head,
 // block_size rows of head_dim elements, landed by TMA as `halves` boxes of
 // [BS rows x kSeg bytes], each swizzled in 128- (or 64-) byte rows.
 // ---------------------------------------------------------------------------
-template <bool INT8, int D, int BS>
+template <bool Q8, int D, int BS>
 struct TileGeom {
-  static constexpr int kElt = INT8 ? 1 : 2;
+  static constexpr int kElt = Q8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElt;
   static constexpr int kSeg = kRowBytes >= 128 ? 128 : 64;
   static constexpr int kHalves = kRowBytes / kSeg;
   static constexpr int kChunksPerSeg = kSeg / 16;
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kTileBytes = BS * kRowBytes;
-  static constexpr int kScaleBytes = INT8 ? BS * 4 : 0;
+  static constexpr int kScaleBytes = Q8 ? BS * 4 : 0;
   static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
 
   // Swizzled byte offset of 16-byte chunk `cc` of token row `t`.
@@ -102,9 +155,10 @@ __device__ __forceinline__ size_t partial_slot(int w, bool first_segment) {
 // accumulates each lane's chunks in fp32x2 registers, combined across the four row
 // groups once per work unit.
 // ===========================================================================
-template <bool INT8, int D, int BS, int G>
+template <bool Q8, int D, int BS, int G, int CODE = CODE_I8>
 struct SimtPath {
-  using Geo = TileGeom<INT8, D, BS>;
+  using Geo = TileGeom<Q8, D, BS>;
+  using Codec = Code8<CODE>;
   static constexpr int kChunks = Geo::kChunksPerRow;          // 16-byte chunks per row
   static constexpr int kLPR = kChunks < 8 ? kChunks : 8;      // lanes per token row
   static constexpr int kCPL = kChunks / kLPR;                 // chunks per lane
@@ -157,18 +211,19 @@ struct SimtPath {
     }
   }
 
-  // kEPL/2 fp32 pairs of one token row (bf16 exactly widened; int8 codes exactly).
+  // kEPL/2 fp32 pairs of one token row (bf16 exactly widened; one-byte codes exactly,
+  // to their value / Codec::kScale).
   __device__ __forceinline__ void load_row(uint32_t tile, int row, float2 (&f)[kEPL / 2]) const {
 #pragma unroll
     for (int k = 0; k < kCPL; ++k) {
       const uint4 raw = lds128(tile + Geo::off(row, chunk_of(k)));
       const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-      if constexpr (INT8) {
+      if constexpr (Q8) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const uint32_t b = w[e] ^ 0x80808080u;
-          f[k * 8 + 2 * e] = unpack_f16x2(biased_bytes_to_f16x2(b, 0x4140u));
-          f[k * 8 + 2 * e + 1] = unpack_f16x2(biased_bytes_to_f16x2(b, 0x4342u));
+          const uint32_t b = Codec::pre(w[e]);
+          f[k * 8 + 2 * e] = unpack_f16x2(Codec::lo(b));
+          f[k * 8 + 2 * e + 1] = unpack_f16x2(Codec::hi(b));
         }
       } else {
 #pragma unroll
@@ -193,7 +248,7 @@ struct SimtPath {
         float a = acc.x + acc.y;
 #pragma unroll
         for (int off = kLPR / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-        if constexpr (INT8) a *= lds_f32(sKs + 4 * row);
+        if constexpr (Q8) a *= lds_f32(sKs + 4 * row) * Codec::kScale;
         sc[h][r] = (row < nvalid) ? a : -INFINITY;
       }
     }
@@ -221,7 +276,7 @@ struct SimtPath {
         float2 vf[kEPL / 2];
         load_row(sV, row, vf);
         float vsc = 1.f;
-        if constexpr (INT8) vsc = lds_f32(sVs + 4 * row);
+        if constexpr (Q8) vsc = lds_f32(sVs + 4 * row) * Codec::kScale;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           l[h] += sc[h][r];
@@ -469,11 +524,26 @@ struct MmaPathBf16 {
 };
 
 // ===========================================================================
-// Tensor-core path, INT8 cache (fp16 MMAs on exactly widened codes)
+// Tensor-core path, one-byte caches (fp16 MMAs on exactly widened codes)
+//
+// The softmax weight times the V scale becomes the fp16 A operand of P.V. Its size
+// is about w * absmax(v) * kPFold / FP8_MAX-or-127; kPFold (Codec::kScale times a
+// power of two kVUp, undone on the output) keeps it near w * absmax(v) for E5M2,
+// whose scale absmax/57344 would otherwise put every weight in fp16's subnormal
+// range. Rows whose absmax exceeds about 1e5 would overflow fp16 here.
 // ===========================================================================
-template <int D, int BS>
+template <int CODE>
+struct VFold {
+  static constexpr float kVUp = CODE == CODE_E5M2 ? 32768.f : 1.f;
+  static constexpr float kPFold = Code8<CODE>::kScale * kVUp;
+};
+
+template <int D, int BS, int CODE = CODE_I8>
 struct MmaPathInt8 {
   using Geo = TileGeom<true, D, BS>;
+  using Codec = Code8<CODE>;
+  static constexpr float kPFold = VFold<CODE>::kPFold;
+  static constexpr float kOutScale = 1.f / VFold<CODE>::kVUp;
   static constexpr int kKS = D / 16;
   static constexpr int kNT = BS / 8;
   static constexpr int kND = D / 8;
@@ -552,13 +622,12 @@ struct MmaPathInt8 {
 #pragma unroll
       for (int ch = 0; ch < kQC; ++ch) {
         const uint4 raw = lds128(sK + Geo::off(row, kQC * cq + ch));
-        const uint32_t w[4] = {raw.x ^ 0x80808080u, raw.y ^ 0x80808080u, raw.z ^ 0x80808080u,
-                               raw.w ^ 0x80808080u};
+        const uint32_t w[4] = {Codec::pre(raw.x), Codec::pre(raw.y), Codec::pre(raw.z),
+                               Codec::pre(raw.w)};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int ks = 4 * ch + k;
-          mma_f16_16816(sacc[nt], qa[ks], biased_bytes_to_f16x2(w[k], 0x4140u),
-                        biased_bytes_to_f16x2(w[k], 0x4342u));
+          mma_f16_16816(sacc[nt], qa[ks], Codec::lo(w[k]), Codec::hi(w[k]));
         }
       }
     }
@@ -569,7 +638,7 @@ struct MmaPathInt8 {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int tok = nt * 8 + 2 * cq + e;
-        kscl[nt][e] = lds_f32(sKs + 4 * tok);
+        kscl[nt][e] = lds_f32(sKs + 4 * tok) * Codec::kScale;
         const bool ok = tok < nvalid;
         sacc[nt][e] = ok ? sacc[nt][e] * kscl[nt][e] * rs0 : -INFINITY;
         sacc[nt][e + 2] = ok ? sacc[nt][e + 2] * kscl[nt][e] * rs1 : -INFINITY;
@@ -610,7 +679,7 @@ struct MmaPathInt8 {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int tok = nt * 8 + 2 * cq + e;
-          vs[e] = tok < nvalid ? lds_f32(sVs + 4 * tok) : 0.f;
+          vs[e] = tok < nvalid ? lds_f32(sVs + 4 * tok) * kPFold : 0.f;
         }
         pa[kk][2 * hlf] = pack_f16x2(w[0] * vs[0], w[1] * vs[1]);
         pa[kk][2 * hlf + 1] = pack_f16x2(w[2] * vs[0], w[3] * vs[1]);
@@ -623,20 +692,16 @@ struct MmaPathInt8 {
       for (int qg = 0; qg < D / 32; ++qg) {
         const int bo = 32 * qg + 4 * gid;
         const int ch = bo >> 4, wi = bo & 15;
-        const uint32_t w0 = lds32(sV + Geo::off(ta, ch) + wi) ^ 0x80808080u;
-        const uint32_t w1 = lds32(sV + Geo::off(ta + 1, ch) + wi) ^ 0x80808080u;
-        const uint32_t w2 = lds32(sV + Geo::off(ta + 8, ch) + wi) ^ 0x80808080u;
-        const uint32_t w3 = lds32(sV + Geo::off(ta + 9, ch) + wi) ^ 0x80808080u;
+        const uint32_t w0 = Codec::pre(lds32(sV + Geo::off(ta, ch) + wi));
+        const uint32_t w1 = Codec::pre(lds32(sV + Geo::off(ta + 1, ch) + wi));
+        const uint32_t w2 = Codec::pre(lds32(sV + Geo::off(ta + 8, ch) + wi));
+        const uint32_t w3 = Codec::pre(lds32(sV + Geo::off(ta + 9, ch) + wi));
         const uint32_t x01 = prmt(w0, w1, 0x5140u), x23 = prmt(w0, w1, 0x7362u);
         const uint32_t y01 = prmt(w2, w3, 0x5140u), y23 = prmt(w2, w3, 0x7362u);
-        mma_f16_16816(o[4 * qg + 0], pa[kk], biased_bytes_to_f16x2(x01, 0x4140u),
-                      biased_bytes_to_f16x2(y01, 0x4140u));
-        mma_f16_16816(o[4 * qg + 1], pa[kk], biased_bytes_to_f16x2(x01, 0x4342u),
-                      biased_bytes_to_f16x2(y01, 0x4342u));
-        mma_f16_16816(o[4 * qg + 2], pa[kk], biased_bytes_to_f16x2(x23, 0x4140u),
-                      biased_bytes_to_f16x2(y23, 0x4140u));
-        mma_f16_16816(o[4 * qg + 3], pa[kk], biased_bytes_to_f16x2(x23, 0x4342u),
-                      biased_bytes_to_f16x2(y23, 0x4342u));
+        mma_f16_16816(o[4 * qg + 0], pa[kk], Codec::lo(x01), Codec::lo(y01));
+        mma_f16_16816(o[4 * qg + 1], pa[kk], Codec::hi(x01), Codec::hi(y01));
+        mma_f16_16816(o[4 * qg + 2], pa[kk], Codec::lo(x23), Codec::lo(y23));
+        mma_f16_16816(o[4 * qg + 3], pa[kk], Codec::hi(x23), Codec::hi(y23));
       }
     }
   }
@@ -663,6 +728,10 @@ struct MmaPathInt8 {
         for (int i = 0; i < 4; ++i) {
           vals[i] = o[4 * qg + i][e0];
           vals[4 + i] = o[4 * qg + i][e0 + 1];
+        }
+        if constexpr (kOutScale != 1.f) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) vals[i] *= kOutScale;
         }
         const int d0 = 32 * qg + 8 * cq;
         if (complete) {
@@ -721,9 +790,9 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B,
 // ===========================================================================
 // The kernel
 // ===========================================================================
-template <bool INT8, int D, int BS, class Path, int kWarps, int kStages>
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages>
 struct DecodeKernel {
-  using Geo = TileGeom<INT8, D, BS>;
+  using Geo = TileGeom<Q8, D, BS>;
   static constexpr int kTile = Geo::kTileBytes;
   static constexpr int kScaleBytes = Geo::kScaleBytes;
   // per-warp shared memory: K tiles, V tiles, K/V scales, mbarriers
@@ -734,11 +803,11 @@ struct DecodeKernel {
   static constexpr uint32_t kTxBytes = 2 * kTile + 2 * kScaleBytes;
 };
 
-template <bool INT8, int D, int BS, class Path, int kWarps, int kStages>
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages>
 __global__ void __launch_bounds__(kWarps * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
-  using K = DecodeKernel<INT8, D, BS, Path, kWarps, kStages>;
+  using K = DecodeKernel<Q8, D, BS, Path, kWarps, kStages>;
   using Geo = typename K::Geo;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -824,7 +893,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         tma_load_2d(sK(st) + hf * BS * Geo::kSeg, &tmk, bar(st), x, row);
         tma_load_2d(sV(st) + hf * BS * Geo::kSeg, &tmv, bar(st), x, row);
       }
-      if constexpr (INT8) {
+      if constexpr (Q8) {
         bulk_load(sKs(st), p.k_scale + size_t(row), K::kScaleBytes, bar(st));
         bulk_load(sVs(st), p.v_scale + size_t(row), K::kScaleBytes, bar(st));
       }
@@ -882,18 +951,18 @@ __global__ void __launch_bounds__(kWarps * 32)
 }
 
 // Shared-memory bytes of one CTA for a batch of B sequences.
-template <bool INT8, int D, int BS, class Path, int kWarps, int kStages>
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages>
 constexpr int decode_smem_bytes_fixed() {
-  return kWarps * DecodeKernel<INT8, D, BS, Path, kWarps, kStages>::kWarpBytes + 1024;
+  return kWarps * DecodeKernel<Q8, D, BS, Path, kWarps, kStages>::kWarpBytes + 1024;
 }
 
-template <bool INT8, int D, int BS, class Path, int kWarps, int kStages>
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages>
 DecodeKernelInfo make_decode_info(int mma, int simt_heads) {
   DecodeKernelInfo info;
-  info.fn = reinterpret_cast<const void*>(&paged_decode_kernel<INT8, D, BS, Path, kWarps, kStages>);
+  info.fn = reinterpret_cast<const void*>(&paged_decode_kernel<Q8, D, BS, Path, kWarps, kStages>);
   info.warps = kWarps;
   info.stages = kStages;
-  info.warp_smem = DecodeKernel<INT8, D, BS, Path, kWarps, kStages>::kWarpBytes;
+  info.warp_smem = DecodeKernel<Q8, D, BS, Path, kWarps, kStages>::kWarpBytes;
   info.mma = mma;
   info.simt_heads = simt_heads;
   return info;

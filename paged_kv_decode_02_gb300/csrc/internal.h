@@ -13,7 +13,7 @@ namespace pkv {
 struct DecodeParams {
   const void* q;               // [B, Hq, D] bf16
   void* out;                   // [B, Hq, D] bf16
-  const float* k_scale;        // [NB, Hkv, BS] fp32 (int8 caches only)
+  const float* k_scale;        // [NB, Hkv, BS] fp32 (one-byte caches only)
   const float* v_scale;
   const int32_t* block_tables; // [B, MBS]
   const int32_t* context_lens; // [B]
@@ -93,7 +93,12 @@ struct DecodeKernelInfo {
 
 // Kernel tables, one per translation unit. Return false if the shape is not built.
 bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info);
+// One-byte KV code formats.
+enum : int { CODE_I8 = 0, CODE_E4M3 = 1, CODE_E5M2 = 2 };
+
 bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info);
+bool select_decode_e4m3(int D, int BS, int simt_heads, DecodeKernelInfo* info);
+bool select_decode_e5m2(int D, int BS, int simt_heads, DecodeKernelInfo* info);
 
 // Launches with programmatic stream serialisation: the kernel may be scheduled while
 // the previous kernel on the stream drains; every kernel of this library waits for its
@@ -117,8 +122,9 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args
 cudaError_t launch_append_bf16(const void* k, const void* v, void* k_cache, void* v_cache,
                                const int64_t* slots, int T, int Hkv, int D, int BS, int NB,
                                cudaStream_t stream);
-cudaError_t launch_append_int8(const void* k, const void* v, int8_t* k_cache, int8_t* v_cache,
-                               float* k_scale, float* v_scale, const int64_t* slots, int T,
-                               int Hkv, int D, int BS, int NB, cudaStream_t stream);
+// code: CODE_I8, CODE_E4M3 or CODE_E5M2
+cudaError_t launch_append_q8(int code, const void* k, const void* v, void* k_cache,
+                             void* v_cache, float* k_scale, float* v_scale, const int64_t* slots,
+                             int T, int Hkv, int D, int BS, int NB, cudaStream_t stream);
 
 }  // namespace pkv

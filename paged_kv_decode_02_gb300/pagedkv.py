@@ -40,6 +40,9 @@ DEV_BAD_PREFIX = 0x8
 
 KV_BF16 = 0
 KV_INT8 = 1
+KV_FP8_E4M3 = 2
+KV_FP8_E5M2 = 3
+FP8_FORMATS = {"e4m3": KV_FP8_E4M3, "e5m2": KV_FP8_E5M2}
 
 
 class PagedKVError(RuntimeError):
@@ -70,6 +73,12 @@ EXPORTS = {
     "pkv_decode_int8": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_float, ctypes.c_void_p,
                                                                 ctypes.c_void_p, ctypes.c_size_t,
                                                                 ctypes.c_void_p, ctypes.c_void_p]),
+    "pkv_append_fp8": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int32, ctypes.c_int,
+                                                               ctypes.c_void_p, ctypes.c_void_p]),
+    "pkv_decode_fp8": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_float, ctypes.c_int,
+                                                               ctypes.c_void_p, ctypes.c_void_p,
+                                                               ctypes.c_size_t, ctypes.c_void_p,
+                                                               ctypes.c_void_p]),
     "pkv_decode_cascade_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
                                                           ctypes.POINTER(ctypes.c_size_t)]),
     "pkv_decode_cascade_bf16": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int32,
@@ -203,6 +212,28 @@ def paged_kv_append_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping)
     _check(st, "pkv_append_int8")
 
 
+def paged_kv_append_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, fmt="e5m2"):
+    """Quantise new tokens' K/V rows per (token, KV head) to FP8 (``fmt`` "e4m3" or
+    "e5m2") and write the codes into ``k_cache``/``v_cache`` ([NB, Hkv, bs, D] uint8 or
+    the matching torch float8 dtype) and fp32 scales into ``k_scale``/``v_scale``
+    ([NB, Hkv, bs]). In place."""
+    kv = _fp8_format(fmt)
+    dev = k_cache.device
+    for t, n, dt, nd in ((k, "k", torch.bfloat16, 3), (v, "v", torch.bfloat16, 3),
+                         (k_scale, "k_scale", torch.float32, 3),
+                         (v_scale, "v_scale", torch.float32, 3),
+                         (slot_mapping, "slot_mapping", torch.int64, 1)):
+        _require(t, n, dt, nd, dev)
+    _require_any(k_cache, "k_cache", _code_dtypes(kv), 4, dev)
+    _require_any(v_cache, "v_cache", _code_dtypes(kv), 4, dev)
+    dims = _dims(0, k_cache.shape[1], k_cache, 1)
+    with _OnDevice(dev):
+        st = _lib().pkv_append_fp8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), k.shape[0],
+                                   kv, ctypes.byref(dims), _stream(dev))
+    _check(st, "pkv_append_fp8")
+
+
 def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                            num_blocks, max_blocks_per_seq, kv_dtype=KV_BF16, device=None):
     dims = Dims(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
@@ -214,14 +245,34 @@ def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_
     return int(out.value)
 
 
-def _decode(int8, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+def _fp8_format(fmt):
+    if fmt not in FP8_FORMATS:
+        raise ValueError(f"fp8 format must be one of {sorted(FP8_FORMATS)}, got {fmt!r}")
+    return FP8_FORMATS[fmt]
+
+
+def _code_dtypes(kv):
+    """Cache tensor dtypes accepted for a KV dtype code."""
+    if kv == KV_BF16:
+        return (torch.bfloat16,)
+    if kv == KV_INT8:
+        return (torch.int8,)
+    return (torch.uint8, torch.float8_e4m3fn if kv == KV_FP8_E4M3 else torch.float8_e5m2)
+
+
+def _require_any(t, name, dtypes, ndim, device):
+    if isinstance(t, torch.Tensor) and t.dtype in dtypes[1:]:
+        dtypes = (t.dtype,)
+    _require(t, name, dtypes[0], ndim, device)
+
+
+def _decode(kv, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
             out, workspace, status):
     dev = q.device
     _require(q, "q", torch.bfloat16, 3, dev)
-    kvt = torch.int8 if int8 else torch.bfloat16
-    _require(k_cache, "k_cache", kvt, 4, dev)
-    _require(v_cache, "v_cache", kvt, 4, dev)
-    if int8:
+    _require_any(k_cache, "k_cache", _code_dtypes(kv), 4, dev)
+    _require_any(v_cache, "v_cache", _code_dtypes(kv), 4, dev)
+    if kv != KV_BF16:
         _require(k_scale, "k_scale", torch.float32, 3, dev)
         _require(v_scale, "v_scale", torch.float32, 3, dev)
     _require(block_tables, "block_tables", torch.int32, 2, dev)
@@ -238,22 +289,31 @@ def _decode(int8, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_l
         _require(out, "out", torch.bfloat16, 3, dev)
     with _OnDevice(dev):
         need = ctypes.c_size_t(0)
-        _check(_lib().pkv_decode_workspace_bytes(ctypes.byref(dims), KV_INT8 if int8 else KV_BF16,
-                                                 ctypes.byref(need)), "pkv_decode_workspace_bytes")
+        _check(_lib().pkv_decode_workspace_bytes(ctypes.byref(dims), kv, ctypes.byref(need)),
+               "pkv_decode_workspace_bytes")
         if workspace is None or workspace.numel() < need.value:
             workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=dev)
-        if int8:
+        if kv == KV_INT8:
+            name = "pkv_decode_int8"
             st = _lib().pkv_decode_int8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                         _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
                                         _ptr(context_lens), float(scale), ctypes.byref(dims),
                                         _ptr(workspace), workspace.numel(), _ptr(status),
                                         _stream(dev))
-        else:
+        elif kv == KV_BF16:
+            name = "pkv_decode_bf16"
             st = _lib().pkv_decode_bf16(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                         _ptr(block_tables), _ptr(context_lens), float(scale),
                                         ctypes.byref(dims), _ptr(workspace), workspace.numel(),
                                         _ptr(status), _stream(dev))
-    _check(st, "pkv_decode_int8" if int8 else "pkv_decode_bf16")
+        else:
+            name = "pkv_decode_fp8"
+            st = _lib().pkv_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                                       _ptr(context_lens), float(scale), kv, ctypes.byref(dims),
+                                       _ptr(workspace), workspace.numel(), _ptr(status),
+                                       _stream(dev))
+    _check(st, name)
     return out
 
 
@@ -266,7 +326,7 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
     least :func:`decode_workspace_bytes`) and
     ``status`` (int32 [1]) are optional.
     """
-    return _decode(False, q, k_cache, v_cache, None, None, block_tables, context_lens, scale,
+    return _decode(KV_BF16, q, k_cache, v_cache, None, None, block_tables, context_lens, scale,
                    out, workspace, status)
 
 
@@ -274,8 +334,18 @@ def paged_decode_attention_int8(q, k_cache, v_cache, k_scale, v_scale, block_tab
                                 context_lens, scale, out=None, workspace=None, status=None):
     """As :func:`paged_decode_attention` over an INT8 cache with per-(token, KV head)
     fp32 scales ``k_scale``/``v_scale`` [NB, Hkv, bs]."""
-    return _decode(True, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+    return _decode(KV_INT8, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                    scale, out, workspace, status)
+
+
+def paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                               context_lens, scale, fmt="e5m2", out=None, workspace=None,
+                               status=None):
+    """As :func:`paged_decode_attention` over an FP8 cache (``fmt`` "e4m3" or "e5m2";
+    codes as uint8 or the matching torch float8 dtype) with per-(token, KV head) fp32
+    scales ``k_scale``/``v_scale`` [NB, Hkv, bs]."""
+    return _decode(_fp8_format(fmt), q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                   context_lens, scale, out, workspace, status)
 
 
 def cascade_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,

@@ -30,6 +30,11 @@ Workload recipes (names are the shapes they model):
   q bf16, seed 4. The codes are drawn directly as rounded N(0, 42.3^2) values clipped
   to [-127, 127] and the scales uniformly from [2.5, 3.5] / 127, the shape that
   symmetric absmax quantisation of N(0, 1) rows with 128 channels produces.
+* ``fp8-e5m2`` / ``fp8-e4m3``: the ``int8`` shape with an FP8 cache (the formats of
+  "FP8（及 H100/H200 硬件路径）", chenk.top page; E5M2 is the one it names for KV
+  caches): codes are N(0, (FP8_MAX/3)^2) values clipped to +-FP8_MAX and rounded to
+  the format by PyTorch's float8 cast (FP8_MAX = 57344 or 448), scales uniformly from
+  [2.5, 3.5] / FP8_MAX -- again the shape absmax scaling of N(0, 1) rows produces.
 
 The token appended in the step is the last one of each request: ``new_k``/``new_v``
 hold it and ``slot_mapping`` points at its slot (``-1`` for an empty request).
@@ -130,17 +135,17 @@ class Workload:
     block_size: int
     num_blocks: int
     max_blocks_per_seq: int
-    kv_dtype: str                      # "bf16" or "int8"
+    kv_dtype: str                      # "bf16", "int8", "fp8_e4m3" or "fp8_e5m2"
     scale: float
     q: torch.Tensor                    # [B, Hq, D] bf16
-    k_cache: torch.Tensor              # [NB, Hkv, bs, D] bf16 or int8
+    k_cache: torch.Tensor              # [NB, Hkv, bs, D] bf16, int8 or uint8 (FP8 codes)
     v_cache: torch.Tensor
     block_tables: torch.Tensor         # [B, MBS] int32 (entries past a request's blocks are poison)
     context_lens: torch.Tensor         # [B] int32
     new_k: torch.Tensor                # [B, Hkv, D] bf16: the token appended this step
     new_v: torch.Tensor
     slot_mapping: torch.Tensor         # [B] int64
-    k_scale: Optional[torch.Tensor] = None   # [NB, Hkv, bs] fp32 (int8 only)
+    k_scale: Optional[torch.Tensor] = None   # [NB, Hkv, bs] fp32 (one-byte caches only)
     v_scale: Optional[torch.Tensor] = None
     refcount: Optional[np.ndarray] = None
     extra: dict = field(default_factory=dict)
@@ -165,7 +170,11 @@ SPECS = {
     "prefix":    dict(B=256, Hq=32, Hkv=8,  D=128, bs=16, seed=3),
     "int8":      dict(B=128, Hq=32, Hkv=8,  D=128, bs=32, seed=4),
     "int8-bs16": dict(B=128, Hq=32, Hkv=8,  D=128, bs=16, seed=4),
+    "fp8-e5m2":  dict(B=128, Hq=32, Hkv=8,  D=128, bs=32, seed=4),
+    "fp8-e4m3":  dict(B=128, Hq=32, Hkv=8,  D=128, bs=32, seed=4),
 }
+
+FP8_KV = {"fp8_e4m3": (torch.float8_e4m3fn, 448.0), "fp8_e5m2": (torch.float8_e5m2, 57344.0)}
 
 
 def _draw_lengths(name, rng, B):
@@ -177,7 +186,7 @@ def _draw_lengths(name, rng, B):
         return _lognormal_lengths(rng, B, 1024, 1.0, 128, 32768)
     if name == "prefix":
         return 2048 + rng.integers(16, 513, size=B).astype(np.int64)
-    if name.startswith("int8"):
+    if name.startswith("int8") or name.startswith("fp8"):
         return np.full(B, 8192, dtype=np.int64)
     raise KeyError(name)
 
@@ -248,7 +257,8 @@ def make_workload(name: str, device="cpu", seed: Optional[int] = None,
     Hkv = num_kv_heads or spec["Hkv"]
     D = head_dim or spec["D"]
     bs = block_size or spec["bs"]
-    kvt = kv_dtype or ("int8" if name.startswith("int8") else "bf16")
+    kvt = kv_dtype or ("int8" if name.startswith("int8") else
+                       "fp8_" + name[4:] if name.startswith("fp8-") else "bf16")
     rng = np.random.default_rng(seed)
     if lengths is None:
         lengths = _draw_lengths(name, rng, B)
@@ -276,6 +286,15 @@ def make_workload(name: str, device="cpu", seed: Optional[int] = None,
         k_cache, v_cache = codes(), codes()
         k_scale = ((2.5 + torch.rand((NB, Hkv, bs), generator=gen, device=dev)) / 127.0).float()
         v_scale = ((2.5 + torch.rand((NB, Hkv, bs), generator=gen, device=dev)) / 127.0).float()
+    elif kvt in FP8_KV:
+        f8, fmax = FP8_KV[kvt]
+
+        def codes():
+            x = torch.randn((NB, Hkv, bs, D), generator=gen, device=dev) * (fmax / 3.0)
+            return torch.clamp(x, -fmax, fmax).to(f8).view(torch.uint8)
+        k_cache, v_cache = codes(), codes()
+        k_scale = ((2.5 + torch.rand((NB, Hkv, bs), generator=gen, device=dev)) / fmax).float()
+        v_scale = ((2.5 + torch.rand((NB, Hkv, bs), generator=gen, device=dev)) / fmax).float()
     else:
         raise ValueError(f"unknown kv dtype {kvt}")
     if poison_unused:

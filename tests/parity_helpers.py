@@ -8,7 +8,8 @@ import torch
 
 import oracle
 
-# Bound on |GPU - oracle| for bf16 outputs of decode attention (bf16 and INT8 caches).
+# Bound on |GPU - oracle| for bf16 outputs of decode attention (bf16, INT8 and FP8
+# caches).
 DECODE_ATOL = 1e-2
 
 
@@ -49,6 +50,14 @@ def oracle_outputs(w, pairs=None):
                 vs = w.v_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
                 K = oracle.gather_sequence_int8(kc, ks, table, L, 0, w.block_size)
                 V = oracle.gather_sequence_int8(vc, vs, table, L, 0, w.block_size)
+            elif w.kv_dtype.startswith("fp8_"):
+                fmt = w.kv_dtype[4:]
+                kc = w.k_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
+                vc = w.v_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
+                ks = w.k_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
+                vs = w.v_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
+                K = oracle.gather_sequence_fp8(kc, ks, table, L, 0, w.block_size, fmt)
+                V = oracle.gather_sequence_fp8(vc, vs, table, L, 0, w.block_size, fmt)
             else:
                 kc = to_f64(w.k_cache[blocks][:, kvh:kvh + 1])
                 vc = to_f64(w.v_cache[blocks][:, kvh:kvh + 1])

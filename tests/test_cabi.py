@@ -89,7 +89,21 @@ def test_host_validation_without_gpu(lib_path):
     assert st == pagedkv.Status.OK          # zero tokens: no-op
     st = lib.pkv_append_int8(p, p, p, p, None, p, p, 3, ctypes.byref(good), None)
     assert st == pagedkv.Status.ERR_NULL
+    # FP8 entry points take only the two FP8 format codes
+    st = lib.pkv_decode_fp8(p, p, p, p, p, p, p, p, 0.1, pagedkv.KV_INT8, ctypes.byref(good), p,
+                            1 << 20, None, None)
+    assert st == pagedkv.Status.ERR_DTYPE
+    st = lib.pkv_decode_fp8(p, p, p, p, None, p, p, p, 0.1, pagedkv.KV_FP8_E5M2,
+                            ctypes.byref(good), p, 1 << 20, None, None)
+    assert st == pagedkv.Status.ERR_NULL
+    st = lib.pkv_append_fp8(p, p, p, p, p, p, p, 3, pagedkv.KV_BF16, ctypes.byref(good), None)
+    assert st == pagedkv.Status.ERR_DTYPE
+    st = lib.pkv_append_fp8(p, p, p, p, None, p, p, 3, pagedkv.KV_FP8_E4M3, ctypes.byref(good),
+                            None)
+    assert st == pagedkv.Status.ERR_NULL
     n = ctypes.c_size_t(0)
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 4, ctypes.byref(n)) == \
+        pagedkv.Status.ERR_DTYPE
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 7, ctypes.byref(n)) == \
         pagedkv.Status.ERR_DTYPE
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 0, None) == pagedkv.Status.ERR_NULL

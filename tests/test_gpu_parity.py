@@ -1,7 +1,7 @@
 """GPU parity: the CUDA library against the fp64 CPU oracle on seeded inputs.
 
-* append (bf16 scatter, INT8 quantise + scatter): bit-exact;
-* decode (bf16 and INT8 caches): max |gpu - oracle| <= 1e-2 on the bf16 output, on
+* append (bf16 scatter, INT8 and FP8 quantise + scatter): bit-exact;
+* decode (bf16, INT8 and FP8 caches): max |gpu - oracle| <= 1e-2 on the bf16 output, on
   whole outputs at sizes the oracle finishes in seconds (several tiles, ragged tails,
   every group-size path) and on sampled outputs at the full workload sizes, in the
   launch configuration the benchmark uses.
@@ -30,6 +30,10 @@ def pk():
 
 
 def _decode(pk, w, **kw):
+    if w.kv_dtype.startswith("fp8_"):
+        return pk.paged_decode_attention_fp8(w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                             w.block_tables, w.context_lens, w.scale,
+                                             fmt=w.kv_dtype[4:], **kw)
     if w.kv_dtype == "int8":
         return pk.paged_decode_attention_int8(w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
                                               w.block_tables, w.context_lens, w.scale, **kw)
@@ -82,6 +86,33 @@ def test_append_int8_bit_exact(pk, D, bs):
                               b.view(np.uint8) if b.dtype == np.int8 else b.view(np.uint32))
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("D,bs", [(128, 32), (64, 16)])
+def test_append_fp8_bit_exact(pk, fmt, D, bs):
+    w = make_workload("fp8-" + fmt, device=DEV, num_seqs=6, lengths=[1, 31, 32, 33, 100, 64],
+                      head_dim=D, block_size=bs)
+    gen = torch.Generator(device=DEV).manual_seed(9)
+    # magnitudes over six decades, so that small entries of a row land on subnormal
+    # codes or round to (signed) zero
+    k = (torch.randn(w.new_k.shape, generator=gen, device=DEV) *
+         torch.logspace(-3, 3, w.new_k.shape[0], device=DEV)[:, None, None]).to(torch.bfloat16)
+    v = (torch.randn(w.new_v.shape, generator=gen, device=DEV) *
+         torch.logspace(-4, 0, D, device=DEV)).to(torch.bfloat16)
+    v[1] = 0                                         # an all-zero row -> scale 0, codes 0
+    slots = w.slot_mapping.clone()
+    slots[3] = -1
+    before = [t.clone() for t in (w.k_cache, w.v_cache, w.k_scale, w.v_scale)]
+    pk.paged_kv_append_fp8(k, v, w.k_cache, w.v_cache, w.k_scale, w.v_scale, slots, fmt=fmt)
+    torch.cuda.synchronize()
+    ref = oracle.append_scatter_fp8(k.float().cpu().numpy(), v.float().cpu().numpy(),
+                                    *[t.cpu().numpy() for t in before], slots.cpu().numpy(), bs,
+                                    fmt)
+    got = [t.cpu().numpy() for t in (w.k_cache, w.v_cache, w.k_scale, w.v_scale)]
+    for a, b in zip(got, ref):
+        assert np.array_equal(a.view(np.uint8) if a.dtype == np.uint8 else a.view(np.uint32),
+                              b.view(np.uint8) if b.dtype == np.uint8 else b.view(np.uint32))
+
+
 # ---------------------------------------------------------------------------
 # decode, whole outputs at small sizes
 # ---------------------------------------------------------------------------
@@ -109,13 +140,16 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("kv", ["bf16", "int8"])
+KV_WORKLOAD = {"bf16": "70b-gqa", "int8": "int8", "fp8_e4m3": "fp8-e4m3",
+               "fp8_e5m2": "fp8-e5m2"}
+
+
+@pytest.mark.parametrize("kv", list(KV_WORKLOAD))
 @pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
 def test_decode_small_shapes(pk, shape, kv):
     _, Hq, Hkv, D, bs, lengths = shape
-    name = "int8" if kv == "int8" else "70b-gqa"
-    w = make_workload(name, device=DEV, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
-                      block_size=bs, lengths=lengths, seed=11, poison_unused=True)
+    w = make_workload(KV_WORKLOAD[kv], device=DEV, num_q_heads=Hq, num_kv_heads=Hkv,
+                      head_dim=D, block_size=bs, lengths=lengths, seed=11, poison_unused=True)
     out = _decode(pk, w)
     torch.cuda.synchronize()
     ref = oracle_outputs(w)
@@ -147,11 +181,11 @@ def test_decode_single_long_sequence_split_many_ways(pk):
     assert max_err(out, ref) <= DECODE_ATOL
 
 
-@pytest.mark.parametrize("kv", ["bf16", "int8"])
+@pytest.mark.parametrize("kv", ["bf16", "int8", "fp8_e5m2"])
 def test_decode_single_long_mha_sequence(pk, kv):
     """B = 1, one KV head: one 32K-token context over every worker (more partials than
     the merge stages at once)."""
-    name = "int8" if kv == "int8" else "7b"
+    name = "7b" if kv == "bf16" else KV_WORKLOAD[kv]
     w = make_workload(name, device=DEV, lengths=[32768], num_q_heads=1, num_kv_heads=1,
                       seed=8)
     out = _decode(pk, w)
@@ -222,11 +256,15 @@ def test_decode_reuses_caller_workspace_and_output(pk):
 # decode at the full workload sizes, sampled outputs
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["7b", "70b-gqa", "prefix", "int8", "int8-bs16"])
+@pytest.mark.parametrize("name", ["7b", "70b-gqa", "prefix", "int8", "int8-bs16", "fp8-e5m2",
+                                  "fp8-e4m3"])
 def test_decode_full_size_sampled(pk, name):
     w = make_workload(name, device=DEV)
     if w.kv_dtype == "bf16":
         pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
+    elif w.kv_dtype.startswith("fp8_"):
+        pk.paged_kv_append_fp8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                               w.slot_mapping, fmt=w.kv_dtype[4:])
     else:
         pk.paged_kv_append_int8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
                                 w.slot_mapping)

@@ -179,8 +179,8 @@ pkv_status pkv_append_fp8(const void* k, const void* v, uint8_t* k_cache, uint8_
  * pkv_decode_fp8 -- as pkv_decode_bf16 over an FP8 cache: the cached value of a row
  * element is decode(code) * scale with the row's fp32 scale (k_scale for K, v_scale
  * for V); codes are widened exactly. The V side folds scale * 2^15 (E5M2) or
- * scale * 2^8 (E4M3) into fp16 softmax weights, so rows written by pkv_append_fp8
- * must have absmax below about 1e5. NaN codes are not expected (the append never
+ * scale * 2^8 (E4M3) into fp16 softmax weights (undone on the output), so rows
+ * written by pkv_append_fp8 must have absmax below about 1e5. NaN codes are not expected (the append never
  * writes them). Workspace as pkv_decode_workspace_bytes(dims, fp8_format).
  */
 pkv_status pkv_decode_fp8(void* out, const void* q, const uint8_t* k_cache,

@@ -41,23 +41,21 @@ namespace pkv {
 // ---------------------------------------------------------------------------
 // One-byte KV codes widened exactly to fp16 pairs in registers. pre() is applied
 // once to each loaded 32-bit word of four codes; lo() then yields codes 0 and 1 of
-// the word as an f16x2, hi() codes 2 and 3. The fp16 values times kScale are the
-// codes' values.
+// the word as an f16x2, hi() codes 2 and 3, equal to the codes' values.
 //   INT8: the byte is placed under the fp16 exponent pattern of 1024 and 1152 is
 //         subtracted (after the sign bit of the code is flipped) -- exact.
 //   E5M2: an E5M2 code is the upper byte of the binary16 of the same value, so a
 //         byte permute that puts it there with a zero lower byte is the conversion.
-//   E4M3: S.EEEE.MMM moved to binary16 bits S.0EEEE.MMM0000000 is the code's value
-//         times 2^-8 (exponent biases 7 and 15), normal and subnormal codes alike;
-//         kScale = 2^8 undoes it. (The one NaN pattern maps to a finite value; a
-//         quantiser with saturation never writes it.)
+//   E4M3: the conversion instruction for packed E4M3 pairs (every E4M3 value is a
+//         binary16 value, so it is exact). Measured on GB300 it costs the same as
+//         the E5M2 permute, where moving the 7 magnitude bits under the sign with
+//         integer operations (4 per pair) made the decode 44 % slower.
 // ---------------------------------------------------------------------------
 template <int CODE>
 struct Code8;
 
 template <>
 struct Code8<CODE_I8> {
-  static constexpr float kScale = 1.f;
   __device__ static __forceinline__ uint32_t pre(uint32_t w) { return w ^ 0x80808080u; }
   __device__ static __forceinline__ uint32_t lo(uint32_t w) {
     return biased_bytes_to_f16x2(w, 0x4140u);
@@ -69,7 +67,6 @@ struct Code8<CODE_I8> {
 
 template <>
 struct Code8<CODE_E5M2> {
-  static constexpr float kScale = 1.f;
   __device__ static __forceinline__ uint32_t pre(uint32_t w) { return w; }
   __device__ static __forceinline__ uint32_t lo(uint32_t w) { return prmt(w, 0u, 0x1404u); }
   __device__ static __forceinline__ uint32_t hi(uint32_t w) { return prmt(w, 0u, 0x3424u); }
@@ -77,16 +74,16 @@ struct Code8<CODE_E5M2> {
 
 template <>
 struct Code8<CODE_E4M3> {
-  static constexpr float kScale = 256.f;
   __device__ static __forceinline__ uint32_t pre(uint32_t w) { return w; }
-  __device__ static __forceinline__ uint32_t rebias(uint32_t y) {
-    return (y & 0x80008000u) | ((y >> 1) & 0x3F803F80u);
-  }
   __device__ static __forceinline__ uint32_t lo(uint32_t w) {
-    return rebias(prmt(w, 0u, 0x1404u));
+    uint32_t r;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e4m3x2 %0, l; }" : "=r"(r) : "r"(w));
+    return r;
   }
   __device__ static __forceinline__ uint32_t hi(uint32_t w) {
-    return rebias(prmt(w, 0u, 0x3424u));
+    uint32_t r;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e4m3x2 %0, h; }" : "=r"(r) : "r"(w));
+    return r;
   }
 };
 
@@ -211,8 +208,7 @@ struct SimtPath {
     }
   }
 
-  // kEPL/2 fp32 pairs of one token row (bf16 exactly widened; one-byte codes exactly,
-  // to their value / Codec::kScale).
+  // kEPL/2 fp32 pairs of one token row (bf16 and one-byte codes exactly widened).
   __device__ __forceinline__ void load_row(uint32_t tile, int row, float2 (&f)[kEPL / 2]) const {
 #pragma unroll
     for (int k = 0; k < kCPL; ++k) {
@@ -248,7 +244,7 @@ struct SimtPath {
         float a = acc.x + acc.y;
 #pragma unroll
         for (int off = kLPR / 2; off > 0; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-        if constexpr (Q8) a *= lds_f32(sKs + 4 * row) * Codec::kScale;
+        if constexpr (Q8) a *= lds_f32(sKs + 4 * row);
         sc[h][r] = (row < nvalid) ? a : -INFINITY;
       }
     }
@@ -276,7 +272,7 @@ struct SimtPath {
         float2 vf[kEPL / 2];
         load_row(sV, row, vf);
         float vsc = 1.f;
-        if constexpr (Q8) vsc = lds_f32(sVs + 4 * row) * Codec::kScale;
+        if constexpr (Q8) vsc = lds_f32(sVs + 4 * row);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           l[h] += sc[h][r];
@@ -526,24 +522,18 @@ struct MmaPathBf16 {
 // ===========================================================================
 // Tensor-core path, one-byte caches (fp16 MMAs on exactly widened codes)
 //
-// The softmax weight times the V scale becomes the fp16 A operand of P.V. Its size
-// is about w * absmax(v) * kPFold / FP8_MAX-or-127; kPFold (Codec::kScale times a
-// power of two kVUp, undone on the output) keeps it near w * absmax(v) for E5M2,
-// whose scale absmax/57344 would otherwise put every weight in fp16's subnormal
-// range. Rows whose absmax exceeds about 1e5 would overflow fp16 here.
+// The softmax weight w in [0, 1] times the V scale becomes the fp16 A operand of
+// P.V. FP8 scales are absmax/448 or absmax/57344, which would leave most weights
+// in fp16's subnormal range, so the weight also carries a power of two kVUp (2^8
+// for E4M3, 2^15 for E5M2: about w * absmax(v) * 0.57), undone on the output. Rows
+// whose absmax exceeds about 1e5 would overflow fp16 here. INT8 keeps w * scale.
 // ===========================================================================
-template <int CODE>
-struct VFold {
-  static constexpr float kVUp = CODE == CODE_E5M2 ? 32768.f : 1.f;
-  static constexpr float kPFold = Code8<CODE>::kScale * kVUp;
-};
-
 template <int D, int BS, int CODE = CODE_I8>
 struct MmaPathInt8 {
   using Geo = TileGeom<true, D, BS>;
   using Codec = Code8<CODE>;
-  static constexpr float kPFold = VFold<CODE>::kPFold;
-  static constexpr float kOutScale = 1.f / VFold<CODE>::kVUp;
+  static constexpr float kVUp = CODE == CODE_E5M2 ? 32768.f : CODE == CODE_E4M3 ? 256.f : 1.f;
+  static constexpr float kOutScale = 1.f / kVUp;
   static constexpr int kKS = D / 16;
   static constexpr int kNT = BS / 8;
   static constexpr int kND = D / 8;
@@ -554,7 +544,7 @@ struct MmaPathInt8 {
   int lane, gid, cq, head0, s, gs;
   uint32_t qa[kKS][4];
   float o[kND][4];
-  float m0, m1, l0, l1, rs0, rs1;
+  float m0, m1, l0, l1, rs0, rs1, qb0, qb1;
 
   __device__ __forceinline__ void init(int lane_) {
     lane = lane_;
@@ -606,6 +596,26 @@ struct MmaPathInt8 {
       qa[ks][2] = pack_f16x2(f0[ks][2] * sc0, f0[ks][3] * sc0);
       qa[ks][3] = pack_f16x2(f1[ks][2] * sc1, f1[ks][3] * sc1);
     }
+    // INT8 K codes enter the score MMA as c + 1152 (the biased fp16 pattern without
+    // its subtraction); 1152 * sum(q row), of the fp16 q the MMA sees, comes off the
+    // fp32 score instead.
+    qb0 = qb1 = 0.f;
+    if constexpr (CODE == CODE_I8) {
+      float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < kKS; ++ks) {
+        const float2 a = unpack_f16x2(qa[ks][0]), b = unpack_f16x2(qa[ks][2]);
+        const float2 c = unpack_f16x2(qa[ks][1]), d = unpack_f16x2(qa[ks][3]);
+        t0 += (a.x + a.y) + (b.x + b.y);
+        t1 += (c.x + c.y) + (d.x + d.y);
+      }
+      t0 += __shfl_xor_sync(0xffffffffu, t0, 1);
+      t0 += __shfl_xor_sync(0xffffffffu, t0, 2);
+      t1 += __shfl_xor_sync(0xffffffffu, t1, 1);
+      t1 += __shfl_xor_sync(0xffffffffu, t1, 2);
+      qb0 = 1152.f * t0;
+      qb1 = 1152.f * t1;
+    }
 #pragma unroll
     for (int nd = 0; nd < kND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
     m0 = m1 = -INFINITY;
@@ -627,7 +637,11 @@ struct MmaPathInt8 {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int ks = 4 * ch + k;
-          mma_f16_16816(sacc[nt], qa[ks], Codec::lo(w[k]), Codec::hi(w[k]));
+          if constexpr (CODE == CODE_I8)
+            mma_f16_16816(sacc[nt], qa[ks], prmt(w[k], 0x64646464u, 0x4140u),
+                          prmt(w[k], 0x64646464u, 0x4342u));
+          else
+            mma_f16_16816(sacc[nt], qa[ks], Codec::lo(w[k]), Codec::hi(w[k]));
         }
       }
     }
@@ -638,10 +652,10 @@ struct MmaPathInt8 {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int tok = nt * 8 + 2 * cq + e;
-        kscl[nt][e] = lds_f32(sKs + 4 * tok) * Codec::kScale;
+        kscl[nt][e] = lds_f32(sKs + 4 * tok);
         const bool ok = tok < nvalid;
-        sacc[nt][e] = ok ? sacc[nt][e] * kscl[nt][e] * rs0 : -INFINITY;
-        sacc[nt][e + 2] = ok ? sacc[nt][e + 2] * kscl[nt][e] * rs1 : -INFINITY;
+        sacc[nt][e] = ok ? (sacc[nt][e] - qb0) * kscl[nt][e] * rs0 : -INFINITY;
+        sacc[nt][e + 2] = ok ? (sacc[nt][e + 2] - qb1) * kscl[nt][e] * rs1 : -INFINITY;
       }
       mx0 = fmaxf(mx0, fmaxf(sacc[nt][0], sacc[nt][1]));
       mx1 = fmaxf(mx1, fmaxf(sacc[nt][2], sacc[nt][3]));
@@ -679,7 +693,7 @@ struct MmaPathInt8 {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int tok = nt * 8 + 2 * cq + e;
-          vs[e] = tok < nvalid ? lds_f32(sVs + 4 * tok) * kPFold : 0.f;
+          vs[e] = tok < nvalid ? lds_f32(sVs + 4 * tok) * kVUp : 0.f;
         }
         pa[kk][2 * hlf] = pack_f16x2(w[0] * vs[0], w[1] * vs[1]);
         pa[kk][2 * hlf + 1] = pack_f16x2(w[2] * vs[0], w[3] * vs[1]);

@@ -35,6 +35,7 @@ from .paged_attention import (  # noqa: F401
     attend_one_head,
     decode_attention,
     decode_attention_int8,
+    decode_attention_multi,
     FP8_MAX,
     fp8_decode,
     fp8_round,

@@ -292,6 +292,44 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, blo
     return out
 
 
+def decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens, scale,
+                           block_size=None):
+    """Paged attention for q_len new tokens per sequence at once (the verification pass
+    of "推测解码" on the chenk.top page: the target model scores the k drafted tokens
+    and the position after them, q_len = k + 1, in one pass), float64.
+
+    ``q``: [B, q_len, Hq, D]. Every sequence's q_len newest tokens are already in the
+    cache, so ``context_lens[s]`` counts them; new token i sits at position
+    context_lens[s] - q_len + i and attends causally to positions 0 .. itself.
+    Returns [B, q_len, Hq, D]. A sequence with context length 0 gets zeros.
+    """
+    q = np.asarray(q)
+    B, n, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    bs = int(block_size) if block_size is not None else k_cache.shape[2]
+    if Hq % Hkv != 0:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    g = Hq // Hkv
+    out = np.zeros((B, n, Hq, D), dtype=np.float64)
+    for s in range(B):
+        L = int(context_lens[s])
+        if L == 0:
+            continue
+        if L < n:
+            raise ValueError("a sequence holds fewer tokens than its queries")
+        for kvh in range(Hkv):
+            K = gather_sequence(k_cache, block_tables[s], L, kvh, bs)
+            V = gather_sequence(v_cache, block_tables[s], L, kvh, bs)
+            for i in range(n):
+                visible = L - n + i + 1            # positions 0 .. L - n + i
+                for h in range(Hq):
+                    if _kv_head_of(h, g) != kvh:
+                        continue
+                    out[s, i, h], _ = attend_one_head(q[s, i, h], K[:visible], V[:visible],
+                                                      scale)
+    return out
+
+
 def gather_sequence_int8(codes, scales, block_table_row, context_len, kv_head, block_size):
     """Real [L, D] float64 values of one sequence's INT8 rows: code times its scale."""
     q = gather_sequence(codes, block_table_row, context_len, kv_head, block_size)

@@ -45,6 +45,9 @@ WORKLOAD_TEXT = {
                 "block 32, per-token per-head fp32 scales",
     "fp8-e4m3": "FP8 E4M3 KV: batch 128, 32 q / 8 kv heads, head_dim 128, context 8192, "
                 "block 32, per-token per-head fp32 scales",
+    "spec-70b": "speculative verification on the 70B-like GQA shape: batch 64, 64 q / 8 kv "
+                "heads, head_dim 128, block 16, context log-normal (median 1024, sigma 1) "
+                "clipped [128, 32768], q_len 6 new tokens per request (k = 5), causal",
 }
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
@@ -82,7 +85,7 @@ def decode_bytes(w):
     tokens = int(L.sum())
     kv = tokens * 2 * w.num_kv_heads * w.head_dim * elt
     scales = tokens * 2 * w.num_kv_heads * 4 if _one_byte(w) else 0
-    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * 2
+    qo = 2 * w.num_seqs * w.q_len * w.num_q_heads * w.head_dim * 2
     tables = int(sum(-(-int(x) // w.block_size) for x in L)) * 4
     return {"kv": kv, "scales": scales, "q_out": qo, "tables": tables + 4 * w.num_seqs,
             "total": kv + scales + qo + tables + 4 * w.num_seqs, "tokens": tokens}
@@ -93,7 +96,7 @@ def append_bytes(w):
     elt = 1 if _one_byte(w) else 2
     rows = T * 2 * w.num_kv_heads * w.head_dim
     scales = T * 2 * w.num_kv_heads * 4 if _one_byte(w) else 0
-    return rows * 2 + rows * elt + scales + 8 * w.num_seqs
+    return rows * 2 + rows * elt + scales + 8 * w.slot_mapping.numel()
 
 
 def unique_kv_bytes(w):
@@ -224,7 +227,8 @@ def _host_units(w, count, seed=0):
         L = int(w.context_lens[s].item())
         n = -(-L // w.block_size)
         blocks = w.block_tables[s, :n].to(torch.int64)
-        unit = {"L": L, "q": w.q[s, kvh * g:(kvh + 1) * g].double().cpu().numpy(),
+        qs = w.q[s] if w.q_len > 1 else w.q[s][None]        # [q_len, Hq, D]
+        unit = {"L": L, "q": qs[:, kvh * g:(kvh + 1) * g].double().cpu().numpy(),
                 "table": np.arange(n)}
         if _one_byte(w):
             unit["k"] = w.k_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
@@ -250,14 +254,18 @@ def _oracle_unit(w, u):
     else:
         K = oracle.gather_sequence(u["k"], u["table"], u["L"], 0, w.block_size)
         V = oracle.gather_sequence(u["v"], u["table"], u["L"], 0, w.block_size)
-    for qh in u["q"]:
-        oracle.attend_one_head(qh, K, V, w.scale)
+    n = u["q"].shape[0]
+    for i in range(n):                       # causal window of new token i
+        visible = max(u["L"] - n + i + 1, 0)
+        for qh in u["q"][i]:
+            oracle.attend_one_head(qh, K[:visible], V[:visible], w.scale)
 
 
 def _unit_bytes(w, u):
     elt = 1 if _one_byte(w) else 2
     g = w.num_q_heads // w.num_kv_heads
-    b = u["L"] * 2 * w.head_dim * elt + 2 * g * w.head_dim * 2 + 4 * len(u["table"])
+    b = (u["L"] * 2 * w.head_dim * elt + 2 * w.q_len * g * w.head_dim * 2 +
+         4 * len(u["table"]))
     if _one_byte(w):
         b += u["L"] * 2 * 4
     return b
@@ -313,6 +321,9 @@ def api_decode(pk, w, q, tables, lens, out, ws, cascade_blocks=0):
     elif cascade_blocks:
         pk.paged_decode_attention_cascade(q, w.k_cache, w.v_cache, tables, lens, cascade_blocks,
                                           w.scale, out=out, workspace=ws)
+    elif w.q_len > 1:
+        pk.paged_decode_attention_multi(q, w.k_cache, w.v_cache, tables, lens, w.scale, out=out,
+                                        workspace=ws)
     else:
         pk.paged_decode_attention(q, w.k_cache, w.v_cache, tables, lens, w.scale, out=out,
                                   workspace=ws)
@@ -340,6 +351,10 @@ def run_ours(args, rank, world):
         need = pk.cascade_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                           w.block_size, w.num_blocks, w.max_blocks_per_seq,
                                           cascade_blocks)
+    elif w.q_len > 1:
+        need = pk.multi_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                        w.block_size, w.num_blocks, w.max_blocks_per_seq,
+                                        w.q_len)
     else:
         need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                          w.block_size, w.num_blocks, w.max_blocks_per_seq,

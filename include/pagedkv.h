@@ -189,6 +189,41 @@ pkv_status pkv_decode_fp8(void* out, const void* q, const uint8_t* k_cache,
                           pkv_kv_dtype fp8_format, const pkv_dims* dims, void* workspace,
                           size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
 
+/* Largest q_len of pkv_decode_multi_bf16. */
+#define PKV_MAX_QUERY_LEN 16
+
+/*
+ * pkv_decode_multi_workspace_bytes -- workspace that pkv_decode_multi_bf16 needs for
+ * these dims and q_len on the CURRENT device. Host-only query; writes *bytes.
+ */
+pkv_status pkv_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len,
+                                            size_t* bytes);
+
+/*
+ * pkv_decode_multi_bf16 -- paged attention for q_len new tokens per sequence in one
+ * call: the verification pass of speculative decoding ("推测解码", chenk.top page: the
+ * target model scores the k drafted tokens and the next position, q_len = k + 1, in
+ * one forward pass); also a short chunk of chunked prefill ("Orca 的迭代级调度", same
+ * page). Every sequence's q_len newest tokens are already in the cache (appended
+ * with pkv_append_bf16), so context_lens[s] counts them; new token i of sequence s
+ * sits at position context_lens[s] - q_len + i and attends causally:
+ *   out[s, i, h, :] = softmax(scale * K q[s, i, h]) V over positions 0 .. that position.
+ *   q, out     [num_seqs, q_len, num_q_heads, head_dim] bf16.
+ *   q_len      1 .. PKV_MAX_QUERY_LEN (else PKV_ERR_SHAPE); 1 is pkv_decode_bf16.
+ *   workspace  at least pkv_decode_multi_workspace_bytes(dims, q_len) bytes, as for
+ *              pkv_decode_bf16.
+ *   status     as for pkv_decode_bf16; a sequence with 0 < context_len < q_len is
+ *              also flagged PKV_DEV_BAD_CONTEXT_LEN (and zeroed). Without status,
+ *              query tokens that see no position get zeros.
+ * Rows are (token, head) pairs on the tensor cores for every group size. Each KV
+ * block is read ceil(q_len * g / 16) times per KV head.
+ */
+pkv_status pkv_decode_multi_bf16(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_tables,
+                                 const int32_t* context_lens, int32_t q_len, float scale,
+                                 const pkv_dims* dims, void* workspace, size_t workspace_bytes,
+                                 int32_t* status, pkv_stream_t stream);
+
 /*
  * pkv_decode_cascade_bf16 -- pkv_decode_bf16 for a batch whose sequences all start
  * with the same `prefix_blocks` physical blocks (a shared system prompt or few-shot

@@ -9,8 +9,8 @@ generator) can be imported without the library.
 _API = (
     "paged_kv_append", "paged_kv_append_int8", "paged_kv_append_fp8",
     "paged_decode_attention", "paged_decode_attention_int8", "paged_decode_attention_fp8",
-    "paged_decode_attention_cascade",
-    "cascade_workspace_bytes",
+    "paged_decode_attention_cascade", "paged_decode_attention_multi",
+    "cascade_workspace_bytes", "multi_workspace_bytes",
     "decode_workspace_bytes", "library_path", "load_library", "PagedKVError",
     "Status", "Dims",
 )

@@ -15,6 +15,7 @@ namespace pkv {
 namespace {
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per shared-memory copy wait
+constexpr int kMaxQueryLen = PKV_MAX_QUERY_LEN;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -124,9 +125,10 @@ pkv_status check_dims(const pkv_dims* d) {
 // sets a kernel attribute, which costs tens of microseconds, so recent plans are kept.
 struct PlanKey {
   pkv_dims d;
-  int kvt, device;
+  int kvt, q_len, device;
   bool operator==(const PlanKey& o) const {
-    return std::memcmp(&d, &o.d, sizeof(d)) == 0 && kvt == o.kvt && device == o.device;
+    return std::memcmp(&d, &o.d, sizeof(d)) == 0 && kvt == o.kvt && q_len == o.q_len &&
+           device == o.device;
   }
 };
 constexpr int kPlanCache = 16;
@@ -135,9 +137,10 @@ PlanKey g_plan_keys[kPlanCache];
 Plan g_plans[kPlanCache];
 int g_plan_count = 0, g_plan_next = 0;
 
-pkv_status make_plan_uncached(const pkv_dims* d, int kvt, Plan* pl);
+pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl);
 
-pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl) {
+// q_len > 1: the causal multi-query decode (bf16 caches).
+pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1) {
   pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
   int dev = 0;
@@ -146,6 +149,7 @@ pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl) {
   std::memset(&key, 0, sizeof(key));
   key.d = *d;
   key.kvt = kvt;
+  key.q_len = q_len;
   key.device = dev;
   std::lock_guard<std::mutex> lock(g_plan_mu);
   for (int i = 0; i < g_plan_count; ++i)
@@ -153,7 +157,7 @@ pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl) {
       *pl = g_plans[i];
       return PKV_OK;
     }
-  st = make_plan_uncached(d, kvt, pl);
+  st = make_plan_uncached(d, kvt, q_len, pl);
   if (st != PKV_OK) return st;
   g_plan_keys[g_plan_next] = key;
   g_plans[g_plan_next] = *pl;
@@ -162,15 +166,18 @@ pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl) {
   return PKV_OK;
 }
 
-pkv_status make_plan_uncached(const pkv_dims* d, int kvt, Plan* pl) {
+pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
   Plan P{};
   P.g = d->num_q_heads / d->num_kv_heads;
-  const bool mma = P.g >= 4;
+  // query rows per KV head: (new token, group member) pairs, split into work units of
+  // at most 16 rows (the MMA's M) on the tensor-core path
+  const int rows = q_len * P.g;
+  const bool mma = P.g >= 4 || q_len > 1;
   if (mma) {
     int nsg = 1;
-    while (P.g % nsg != 0 || P.g / nsg > 16) ++nsg;
+    while (rows % nsg != 0 || rows / nsg > 16) ++nsg;
     P.nsg = nsg;
-    P.gs = P.g / nsg;
+    P.gs = rows / nsg;
   } else {
     P.nsg = 1;
     P.gs = P.g;
@@ -178,16 +185,21 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, Plan* pl) {
   P.HU = d->num_kv_heads * P.nsg;
   const int simt = mma ? 0 : P.g;
   bool found = false;
-  switch (kvt) {
-    case PKV_KV_BF16: found = select_decode_bf16(d->head_dim, d->block_size, simt, &P.k); break;
-    case PKV_KV_INT8: found = select_decode_int8(d->head_dim, d->block_size, simt, &P.k); break;
-    case PKV_KV_FP8_E4M3:
-      found = select_decode_e4m3(d->head_dim, d->block_size, simt, &P.k);
-      break;
-    case PKV_KV_FP8_E5M2:
-      found = select_decode_e5m2(d->head_dim, d->block_size, simt, &P.k);
-      break;
-    default: return PKV_ERR_DTYPE;
+  if (q_len > 1) {
+    if (kvt != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
+    found = select_decode_bf16_multi(d->head_dim, d->block_size, &P.k);
+  } else {
+    switch (kvt) {
+      case PKV_KV_BF16: found = select_decode_bf16(d->head_dim, d->block_size, simt, &P.k); break;
+      case PKV_KV_INT8: found = select_decode_int8(d->head_dim, d->block_size, simt, &P.k); break;
+      case PKV_KV_FP8_E4M3:
+        found = select_decode_e4m3(d->head_dim, d->block_size, simt, &P.k);
+        break;
+      case PKV_KV_FP8_E5M2:
+        found = select_decode_e5m2(d->head_dim, d->block_size, simt, &P.k);
+        break;
+      default: return PKV_ERR_DTYPE;
+    }
   }
   if (!found) return PKV_ERR_UNSUPPORTED;
   P.smem = size_t(P.k.warps) * P.k.warp_smem + 1024 + align_up(size_t(d->num_seqs + 1) * 4, 16);
@@ -226,9 +238,10 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
                       const void* v_cache, const float* k_scale, const float* v_scale,
                       const int32_t* block_tables, const int32_t* context_lens, float scale,
                       const pkv_dims* d, void* workspace, size_t workspace_bytes,
-                      int32_t* status, cudaStream_t stream) {
+                      int32_t* status, cudaStream_t stream, int q_len = 1) {
   pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
+  if (q_len < 1 || q_len > kMaxQueryLen) return PKV_ERR_SHAPE;
   if (d->num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PKV_ERR_NULL;
@@ -238,7 +251,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
       (q8 && (!aligned16(k_scale) || !aligned16(v_scale))))
     return PKV_ERR_ALIGNMENT;
   Plan P;
-  st = make_plan(d, kvt, &P);
+  st = make_plan(d, kvt, &P, q_len);
   if (st != PKV_OK) return st;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < P.ws_bytes)
@@ -275,6 +288,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   p.timeout_ns = kTimeoutNs;
   p.skip = 0;
   p.unit_slot0 = -1;
+  p.q_len = q_len;
 
   void* args[] = {&tmk, &tmv, &p};
   if (launch_pdl(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), args, P.smem, stream) !=
@@ -295,6 +309,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   m.B = p.B;
   m.Hq = p.Hq;
   m.D = d->head_dim;
+  m.q_len = q_len;
   m.g = P.g;
   m.gs = P.gs;
   m.nsg = P.nsg;
@@ -418,6 +433,7 @@ pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void
   p.timeout_ns = kTimeoutNs;
   p.skip = prefix_blocks;
   p.unit_slot0 = 2 * P.W;
+  p.q_len = 1;
   {
     void* args[] = {&tmk, &tmv, &p};
     if (launch_pdl(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), args, P.smem, stream) !=
@@ -590,6 +606,27 @@ pkv_status pkv_decode_fp8(void* out, const void* q, const uint8_t* k_cache,
   return run_decode(fp8_format, out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
                     context_lens, scale, dims, workspace, workspace_bytes, status,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len,
+                                            size_t* bytes) {
+  if (!bytes) return PKV_ERR_NULL;
+  if (q_len < 1 || q_len > kMaxQueryLen) return PKV_ERR_SHAPE;
+  Plan P;
+  pkv_status st = make_plan(dims, PKV_KV_BF16, &P, q_len);
+  if (st != PKV_OK) return st;
+  *bytes = P.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_multi_bf16(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_tables,
+                                 const int32_t* context_lens, int32_t q_len, float scale,
+                                 const pkv_dims* dims, void* workspace, size_t workspace_bytes,
+                                 int32_t* status, pkv_stream_t stream) {
+  return run_decode(PKV_KV_BF16, out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
+                    context_lens, scale, dims, workspace, workspace_bytes, status,
+                    reinterpret_cast<cudaStream_t>(stream), q_len);
 }
 
 }  // extern "C"

@@ -137,6 +137,21 @@ __device__ __forceinline__ int unit_head0(const DecodeParams& p, int u) {
   return (u / p.nsg) * p.g + (u % p.nsg) * p.gs;
 }
 
+// Query rows of a KV head are the q_len * g pairs (new token i, group member j),
+// numbered R = i * g + j; work unit u takes rows (u % nsg) * gs .. + gs - 1. Row r of
+// unit u of sequence s reads q / writes out row (s * q_len + i) * Hq + kvh * g + j.
+// With q_len = 1 this is head unit_head0 + r of sequence s.
+__device__ __forceinline__ size_t query_row(const DecodeParams& p, int s, int u, int r) {
+  const int R = (u % p.nsg) * p.gs + r;
+  return (size_t(s) * p.q_len + R / p.g) * p.Hq + (u / p.nsg) * p.g + R % p.g;
+}
+
+// Tokens of a unit's visible range that row r may not see: new token i sits at
+// position L - q_len + i, so it sees all but the last q_len - 1 - i positions.
+__device__ __forceinline__ int causal_hidden(const DecodeParams& p, int u, int r) {
+  return p.q_len - 1 - ((u % p.nsg) * p.gs + r) / p.g;
+}
+
 // Where a warp leaves a cut unit: slot 2w for the unit its range starts in, 2w+1
 // for the unit its range ends in.
 __device__ __forceinline__ size_t partial_slot(int w, bool first_segment) {
@@ -338,8 +353,13 @@ struct SimtPath {
 
 // ===========================================================================
 // Tensor-core path, bf16 cache (groups of 4..16 query heads per work unit)
+//
+// kCausal: the multi-query variant (q_len new tokens per sequence; rows are (token,
+// head) pairs, see query_row). Each row hides the positions after its own token, a
+// row may then see no token of a block (its softmax state stays empty: m = -inf,
+// l = 0, handled without NaNs), and a row that sees nothing at all outputs zeros.
 // ===========================================================================
-template <int D, int BS>
+template <int D, int BS, bool kCausal = false>
 struct MmaPathBf16 {
   using Geo = TileGeom<false, D, BS>;
   static constexpr int kKS = D / 16;  // k-steps of q.K^T
@@ -348,6 +368,7 @@ struct MmaPathBf16 {
   static constexpr int kKK = BS / 16; // token k-steps of P.V
 
   int lane, gid, cq, head0, s, gs;
+  int u, hide0, hide1;                // kCausal: unit, hidden trailing tokens of both rows
   uint32_t qa[kKS][4];
   float o[kND][4];
   float m0, m1, l0, l1;
@@ -358,13 +379,22 @@ struct MmaPathBf16 {
     cq = lane & 3;
   }
 
-  __device__ __forceinline__ void begin(const DecodeParams& p, int s_, int u) {
+  __device__ __forceinline__ void begin(const DecodeParams& p, int s_, int u_) {
     s = s_;
     gs = p.gs;
-    head0 = unit_head0(p, u);
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
-    const size_t row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 2);
-    load_q(qw + row0, qw + row0 + 8 * (D / 2), gid < gs, gid + 8 < gs);
+    if constexpr (kCausal) {
+      u = u_;
+      const bool v0 = gid < gs, v1 = gid + 8 < gs;
+      hide0 = v0 ? causal_hidden(p, u, gid) : 0;
+      hide1 = v1 ? causal_hidden(p, u, gid + 8) : 0;
+      load_q(qw + (v0 ? query_row(p, s, u, gid) : 0) * (D / 2),
+             qw + (v1 ? query_row(p, s, u, gid + 8) : 0) * (D / 2), v0, v1);
+    } else {
+      head0 = unit_head0(p, u_);
+      const size_t row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 2);
+      load_q(qw + row0, qw + row0 + 8 * (D / 2), gid < gs, gid + 8 < gs);
+    }
   }
 
   // Q fragments from the rows of this lane's two M rows (gid, gid + 8; absent rows are
@@ -426,7 +456,9 @@ struct MmaPathBf16 {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = nt * 8 + 2 * cq + (e & 1);
-        const float x = tok < nvalid ? sacc[nt][e] * p.scale_log2 : -INFINITY;
+        int lim = nvalid;
+        if constexpr (kCausal) lim -= (e < 2) ? hide0 : hide1;
+        const float x = tok < lim ? sacc[nt][e] * p.scale_log2 : -INFINITY;
         sacc[nt][e] = x;
       }
       mx0 = fmaxf(mx0, fmaxf(sacc[nt][0], sacc[nt][1]));
@@ -436,10 +468,15 @@ struct MmaPathBf16 {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
+    float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float mp0 = m0, mp1 = m1;
     m0 = mn0;
     m1 = mn1;
+    if constexpr (kCausal) {  // a row with nothing visible yet: subtract 0, not -inf
+      mn0 = mn0 == -INFINITY ? 0.f : mn0;
+      mn1 = mn1 == -INFINITY ? 0.f : mn1;
+    }
+    const float a0 = fast_exp2(mp0 - mn0), a1 = fast_exp2(mp1 - mn1);
     l0 *= a0;
     l1 *= a1;
 #pragma unroll
@@ -492,10 +529,18 @@ struct MmaPathBf16 {
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     const bool v0 = gid < gs, v1 = gid + 8 < gs;
     if (complete) {
-      const float i0 = 1.f / l0, i1 = 1.f / l1;
+      float i0 = 1.f / l0, i1 = 1.f / l1;
       uint32_t* out = reinterpret_cast<uint32_t*>(p.out);
-      const size_t row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 2);
-      const size_t row1 = row0 + 8 * (D / 2);
+      size_t row0, row1;
+      if constexpr (kCausal) {
+        i0 = l0 > 0.f ? i0 : 0.f;
+        i1 = l1 > 0.f ? i1 : 0.f;
+        row0 = (v0 ? query_row(p, s, u, gid) : 0) * (D / 2);
+        row1 = (v1 ? query_row(p, s, u, gid + 8) : 0) * (D / 2);
+      } else {
+        row0 = (size_t(s) * p.Hq + head0 + gid) * (D / 2);
+        row1 = row0 + 8 * (D / 2);
+      }
 #pragma unroll
       for (int nd = 0; nd < kND; ++nd) {
         if (v0) out[row0 + 4 * nd + cq] = pack_bf16x2(o[nd][0] * i0, o[nd][1] * i0);

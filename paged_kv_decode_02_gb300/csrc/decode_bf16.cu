@@ -1,4 +1,5 @@
-// decode_bf16.cu -- bf16-cache instantiations of the paged decode kernel.
+// decode_bf16.cu -- bf16-cache instantiations of the paged decode kernel (single-token
+// and the causal multi-query variant).
 #include "decode.cuh"
 
 namespace pkv {
@@ -39,7 +40,21 @@ bool select_shape(int simt_heads, DecodeKernelInfo* info) {
       return false;
   }
 }
+template <int D, int BS>
+DecodeKernelInfo multi_shape() {
+  return make_decode_info<false, D, BS, MmaPathBf16<D, BS, true>, Bf16Warps<D, BS, true>::kWarps,
+                          Bf16Shape<D, BS>::kStages>(1, 0);
+}
 }  // namespace
+
+bool select_decode_bf16_multi(int D, int BS, DecodeKernelInfo* info) {
+  if (D == 128 && BS == 16) *info = multi_shape<128, 16>();
+  else if (D == 128 && BS == 32) *info = multi_shape<128, 32>();
+  else if (D == 64 && BS == 16) *info = multi_shape<64, 16>();
+  else if (D == 64 && BS == 32) *info = multi_shape<64, 32>();
+  else return false;
+  return true;
+}
 
 bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info) {
   if (D == 128 && BS == 16) return select_shape<128, 16>(simt_heads, info);

@@ -11,8 +11,8 @@ namespace pkv {
 
 // Parameters of one decode launch (device pointers; sizes as in pkv_dims).
 struct DecodeParams {
-  const void* q;               // [B, Hq, D] bf16
-  void* out;                   // [B, Hq, D] bf16
+  const void* q;               // [B, q_len, Hq, D] bf16
+  void* out;                   // [B, q_len, Hq, D] bf16
   const float* k_scale;        // [NB, Hkv, BS] fp32 (one-byte caches only)
   const float* v_scale;
   const int32_t* block_tables; // [B, MBS]
@@ -25,9 +25,10 @@ struct DecodeParams {
                                //       instead of the output (cascade); -1: normal
   int32_t* status;             // optional device status word
   int B, Hq, Hkv, MBS, NB;
+  int q_len;                   // new tokens per sequence (1: single-token decode)
   int g;                       // Hq / Hkv
-  int gs;                      // query heads handled per work unit
-  int nsg;                     // work units per KV head (g / gs)
+  int gs;                      // query rows (token, head) handled per work unit
+  int nsg;                     // work units per KV head (q_len * g / gs)
   int HU;                      // work units per sequence (Hkv * nsg)
   float scale_log2;            // softmax scale * log2(e)
   unsigned long long timeout_ns;
@@ -75,6 +76,7 @@ struct MergeParams {
   const int32_t* context_lens;
   int32_t* status;
   int B, Hq, D, MBS, NB, BS;
+  int q_len;                   // new tokens per sequence (rows map as in DecodeParams)
   int g, gs, nsg, HU;
   int W;                       // number of decode workers (warps)
 };
@@ -93,6 +95,8 @@ struct DecodeKernelInfo {
 
 // Kernel tables, one per translation unit. Return false if the shape is not built.
 bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info);
+// q_len > 1: the causal multi-query variant of the bf16 tensor-core path
+bool select_decode_bf16_multi(int D, int BS, DecodeKernelInfo* info);
 // One-byte KV code formats.
 enum : int { CODE_I8 = 0, CODE_E4M3 = 1, CODE_E5M2 = 2 };
 

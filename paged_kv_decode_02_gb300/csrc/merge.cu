@@ -32,9 +32,13 @@ __global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const
   const int n = p.prefix[s + 1] - p.prefix[s];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gs = p.gs, D = p.D, Q = D / 4, nout = gs * Q;
-  __nv_bfloat16* out =
-      reinterpret_cast<__nv_bfloat16*>(p.out) +
-      (size_t(s) * p.Hq + (u / p.nsg) * p.g + (u % p.nsg) * p.gs) * D;
+  // output row of unit row r: (s * q_len + i) * Hq + kvh * g + j for the unit's query
+  // row R = (u % nsg) * gs + r = i * g + j (with q_len = 1: head kvh * g + R)
+  __nv_bfloat16* out_base = reinterpret_cast<__nv_bfloat16*>(p.out);
+  auto out_row = [&](int r) -> __nv_bfloat16* {
+    const int R = (u % p.nsg) * gs + r;
+    return out_base + ((size_t(s) * p.q_len + R / p.g) * p.Hq + (u / p.nsg) * p.g + R % p.g) * D;
+  };
 
   bool zero = (n == 0);
   if (p.status != nullptr) {
@@ -43,7 +47,7 @@ __global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const
     __syncthreads();
     int flags = 0;
     const int L = p.context_lens[s];
-    if (tid == 0 && (L < 0 || L > p.MBS * p.BS)) flags |= 0x1;
+    if (tid == 0 && (L < 0 || L > p.MBS * p.BS || (L > 0 && L < p.q_len))) flags |= 0x1;
     for (int j = tid; j < n; j += blockDim.x) {
       const int id = p.block_tables[size_t(s) * p.MBS + j];
       if (id < 0 || id >= p.NB) flags |= 0x2;
@@ -57,7 +61,7 @@ __global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const
   }
   if (zero) {
     for (int o = tid; o < nout; o += blockDim.x)
-      *reinterpret_cast<uint2*>(out + size_t(o / Q) * D + 4 * (o % Q)) = make_uint2(0u, 0u);
+      *reinterpret_cast<uint2*>(out_row(o / Q) + 4 * (o % Q)) = make_uint2(0u, 0u);
     return;
   }
   const long long T = (long long)p.HU * p.prefix[p.B];
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const
   float L = 0.f;
   if (g < NG) {
     const int row = o / Q, dq = o % Q;
-    const float M = s_max[row];
+    const float M = s_max[row] == -INFINITY ? 0.f : s_max[row];  // no part saw a token
 #pragma unroll 4
     for (int i = g; i < nparts; i += NG) {
       const size_t slot = slot_of(i);
@@ -126,11 +130,11 @@ __global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const
       acc.w += a.w;
       L += s_l[k * span + (o - o0)];
     }
-    const float inv = 1.f / L;
+    const float inv = L > 0.f ? 1.f / L : 0.f;  // a row that saw nothing: zeros
     uint2 pk;
     pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
     pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2*>(out + size_t(o / Q) * D + 4 * (o % Q)) = pk;
+    *reinterpret_cast<uint2*>(out_row(o / Q) + 4 * (o % Q)) = pk;
   }
   __syncthreads();  // s_acc is reused by the next span
   }

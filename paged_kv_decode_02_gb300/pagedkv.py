@@ -79,6 +79,15 @@ EXPORTS = {
                                                                ctypes.c_void_p, ctypes.c_void_p,
                                                                ctypes.c_size_t, ctypes.c_void_p,
                                                                ctypes.c_void_p]),
+    "pkv_decode_multi_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
+                                                        ctypes.POINTER(ctypes.c_size_t)]),
+    "pkv_decode_multi_bf16": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int32,
+                                                                      ctypes.c_float,
+                                                                      ctypes.c_void_p,
+                                                                      ctypes.c_void_p,
+                                                                      ctypes.c_size_t,
+                                                                      ctypes.c_void_p,
+                                                                      ctypes.c_void_p]),
     "pkv_decode_cascade_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
                                                           ctypes.POINTER(ctypes.c_size_t)]),
     "pkv_decode_cascade_bf16": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int32,
@@ -346,6 +355,56 @@ def paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     scales ``k_scale``/``v_scale`` [NB, Hkv, bs]."""
     return _decode(_fp8_format(fmt), q, k_cache, v_cache, k_scale, v_scale, block_tables,
                    context_lens, scale, out, workspace, status)
+
+
+def multi_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, max_blocks_per_seq, q_len, device=None):
+    dims = Dims(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq)
+    out = ctypes.c_size_t(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = _lib().pkv_decode_multi_workspace_bytes(ctypes.byref(dims), int(q_len),
+                                                     ctypes.byref(out))
+    _check(st, "pkv_decode_multi_workspace_bytes")
+    return int(out.value)
+
+
+def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                 out=None, workspace=None, status=None):
+    """Attention for q_len new tokens per sequence in one call (speculative
+    verification, q_len = k + 1): q [B, q_len, Hq, D] bf16; the q_len newest tokens of
+    every sequence are already in the bf16 caches and counted by ``context_lens``; new
+    token i attends causally to positions 0 .. context_lens - q_len + i. Returns out
+    [B, q_len, Hq, D] bf16."""
+    dev = q.device
+    _require(q, "q", torch.bfloat16, 4, dev)
+    _require(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _require(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    B, n, Hq, D = q.shape
+    if k_cache.shape != v_cache.shape or k_cache.shape[3] != D:
+        raise ValueError("cache shapes disagree with q")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    dims = _dims(B, Hq, k_cache, block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _require(out, "out", torch.bfloat16, 4, dev)
+    with _OnDevice(dev):
+        need = ctypes.c_size_t(0)
+        _check(_lib().pkv_decode_multi_workspace_bytes(ctypes.byref(dims), n,
+                                                       ctypes.byref(need)),
+               "pkv_decode_multi_workspace_bytes")
+        if workspace is None or workspace.numel() < need.value:
+            workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=dev)
+        st = _lib().pkv_decode_multi_bf16(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(block_tables), _ptr(context_lens), n,
+                                          float(scale), ctypes.byref(dims), _ptr(workspace),
+                                          workspace.numel(), _ptr(status), _stream(dev))
+    _check(st, "pkv_decode_multi_bf16")
+    return out
 
 
 def cascade_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,

@@ -36,8 +36,13 @@ Workload recipes (names are the shapes they model):
   the format by PyTorch's float8 cast (FP8_MAX = 57344 or 448), scales uniformly from
   [2.5, 3.5] / FP8_MAX -- again the shape absmax scaling of N(0, 1) rows produces.
 
-The token appended in the step is the last one of each request: ``new_k``/``new_v``
-hold it and ``slot_mapping`` points at its slot (``-1`` for an empty request).
+* ``spec-70b``: the ``70b-gqa`` shape and lengths with q_len = 6 new tokens per
+  request (k = 5 drafted tokens plus the next position, the number of speculative
+  tokens in the vLLM example of "推测解码", chenk.top page), for multi-query decode.
+
+The tokens appended in the step are the last q_len (1 unless stated) of each
+request: ``new_k``/``new_v`` hold them ([B * q_len, Hkv, D], request-major) and
+``slot_mapping`` points at their slots (``-1`` for an empty request).
 """
 
 from __future__ import annotations
@@ -137,18 +142,19 @@ class Workload:
     max_blocks_per_seq: int
     kv_dtype: str                      # "bf16", "int8", "fp8_e4m3" or "fp8_e5m2"
     scale: float
-    q: torch.Tensor                    # [B, Hq, D] bf16
+    q: torch.Tensor                    # [B, Hq, D] bf16 ([B, q_len, Hq, D] when q_len > 1)
     k_cache: torch.Tensor              # [NB, Hkv, bs, D] bf16, int8 or uint8 (FP8 codes)
     v_cache: torch.Tensor
     block_tables: torch.Tensor         # [B, MBS] int32 (entries past a request's blocks are poison)
     context_lens: torch.Tensor         # [B] int32
-    new_k: torch.Tensor                # [B, Hkv, D] bf16: the token appended this step
+    new_k: torch.Tensor                # [B * q_len, Hkv, D] bf16: tokens appended this step
     new_v: torch.Tensor
-    slot_mapping: torch.Tensor         # [B] int64
+    slot_mapping: torch.Tensor         # [B * q_len] int64
     k_scale: Optional[torch.Tensor] = None   # [NB, Hkv, bs] fp32 (one-byte caches only)
     v_scale: Optional[torch.Tensor] = None
     refcount: Optional[np.ndarray] = None
     extra: dict = field(default_factory=dict)
+    q_len: int = 1                     # new tokens per request (multi-query decode)
 
     @property
     def group(self) -> int:
@@ -172,6 +178,7 @@ SPECS = {
     "int8-bs16": dict(B=128, Hq=32, Hkv=8,  D=128, bs=16, seed=4),
     "fp8-e5m2":  dict(B=128, Hq=32, Hkv=8,  D=128, bs=32, seed=4),
     "fp8-e4m3":  dict(B=128, Hq=32, Hkv=8,  D=128, bs=32, seed=4),
+    "spec-70b":  dict(B=64,  Hq=64, Hkv=8,  D=128, bs=16, seed=2, q_len=6),
 }
 
 FP8_KV = {"fp8_e4m3": (torch.float8_e4m3fn, 448.0), "fp8_e5m2": (torch.float8_e5m2, 57344.0)}
@@ -182,7 +189,7 @@ def _draw_lengths(name, rng, B):
         return rng.integers(1, 65, size=B).astype(np.int64)
     if name == "7b":
         return np.full(B, 2048, dtype=np.int64)
-    if name == "70b-gqa":
+    if name in ("70b-gqa", "spec-70b"):
         return _lognormal_lengths(rng, B, 1024, 1.0, 128, 32768)
     if name == "prefix":
         return 2048 + rng.integers(16, 513, size=B).astype(np.int64)
@@ -242,13 +249,16 @@ def _randn_bf16(shape, gen, device):
 def make_workload(name: str, device="cpu", seed: Optional[int] = None,
                   lengths=None, num_seqs=None, num_q_heads=None, num_kv_heads=None,
                   head_dim=None, block_size=None, num_blocks=None,
-                  poison_unused=False, kv_dtype=None, prefix_tokens=None) -> Workload:
+                  poison_unused=False, kv_dtype=None, prefix_tokens=None,
+                  q_len=None) -> Workload:
     """Build a named workload (optionally overriding its sizes) on ``device``.
 
     ``poison_unused`` fills every cache row that no request's context covers with NaN
     (bf16) or, for INT8, NaN scales, so that a kernel reading one shows up.
     ``prefix_tokens`` (a multiple of the block size) puts that many leading tokens of
     every request in one set of shared, refcounted blocks (2048 for ``prefix``).
+    ``q_len`` > 1 gives every request that many new tokens (q [B, q_len, Hq, D]); a
+    request's length must then be 0 or at least q_len.
     """
     spec = dict(SPECS[name])
     seed = spec["seed"] if seed is None else seed
@@ -257,6 +267,7 @@ def make_workload(name: str, device="cpu", seed: Optional[int] = None,
     Hkv = num_kv_heads or spec["Hkv"]
     D = head_dim or spec["D"]
     bs = block_size or spec["bs"]
+    n_new = int(q_len if q_len is not None else spec.get("q_len", 1))
     kvt = kv_dtype or ("int8" if name.startswith("int8") else
                        "fp8_" + name[4:] if name.startswith("fp8-") else "bf16")
     rng = np.random.default_rng(seed)
@@ -272,9 +283,18 @@ def make_workload(name: str, device="cpu", seed: Optional[int] = None,
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
     gen.manual_seed(int(seed))
-    q = _randn_bf16((B, Hq, D), gen, dev)
-    new_k = _randn_bf16((B, Hkv, D), gen, dev)
-    new_v = _randn_bf16((B, Hkv, D), gen, dev)
+    q = _randn_bf16((B, Hq, D) if n_new == 1 else (B, n_new, Hq, D), gen, dev)
+    new_k = _randn_bf16((B * n_new, Hkv, D), gen, dev)
+    new_v = _randn_bf16((B * n_new, Hkv, D), gen, dev)
+    if n_new > 1:
+        if np.any((lengths > 0) & (lengths < n_new)):
+            raise ValueError("a request holds fewer tokens than its new tokens")
+        last_slots = np.full(B * n_new, -1, dtype=np.int64)
+        for s in range(B):
+            L = int(lengths[s])
+            for i in range(n_new if L else 0):
+                t = L - n_new + i
+                last_slots[s * n_new + i] = int(tables[s, t // bs]) * bs + t % bs
     k_scale = v_scale = None
     if kvt == "bf16":
         k_cache = _randn_bf16((NB, Hkv, bs, D), gen, dev)
@@ -319,4 +339,4 @@ def make_workload(name: str, device="cpu", seed: Optional[int] = None,
         context_lens=torch.from_numpy(lengths.astype(np.int32)).to(dev),
         new_k=new_k, new_v=new_v, slot_mapping=torch.from_numpy(last_slots).to(dev),
         k_scale=k_scale, v_scale=v_scale, refcount=alloc.refcount.copy(),
-        extra={"prefix_tokens": prefix})
+        extra={"prefix_tokens": prefix}, q_len=n_new)

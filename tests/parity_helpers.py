@@ -87,3 +87,39 @@ def sample_pairs(w, n, seed=0):
     while len(picks) < n:
         picks.add((int(rng.integers(B)), int(rng.integers(Hq))))
     return sorted(picks)
+
+
+def oracle_outputs_multi(w, triples=None):
+    """Oracle outputs [B, q_len, Hq, D] (NaN where not computed) of multi-query decode
+    for the (s, i, h) triples given (all when None): each sequence's own blocks are
+    copied to the host and re-indexed; whole sequences go through
+    oracle.decode_attention_multi, single triples through the same causal window."""
+    B, n, Hq, D = w.q.shape
+    g = w.group
+    out = np.full((B, n, Hq, D), np.nan)
+    q = to_f64(w.q)
+    if triples is None:
+        for s in range(B):
+            L, blocks = sequence_blocks(w, s)
+            if L == 0:
+                out[s] = 0.0
+                continue
+            kc, vc = to_f64(w.k_cache[blocks]), to_f64(w.v_cache[blocks])
+            out[s] = oracle.decode_attention_multi(q[s:s + 1], kc, vc,
+                                                   np.arange(len(blocks))[None, :], [L],
+                                                   w.scale, w.block_size)[0]
+        return out
+    for (s, i, h) in triples:
+        L, blocks = sequence_blocks(w, s)
+        if L == 0:
+            out[s, i, h] = 0.0
+            continue
+        kvh = h // g
+        table = np.arange(len(blocks))
+        K = oracle.gather_sequence(to_f64(w.k_cache[blocks][:, kvh:kvh + 1]), table, L, 0,
+                                   w.block_size)
+        V = oracle.gather_sequence(to_f64(w.v_cache[blocks][:, kvh:kvh + 1]), table, L, 0,
+                                   w.block_size)
+        visible = L - n + i + 1
+        out[s, i, h], _ = oracle.attend_one_head(q[s, i, h], K[:visible], V[:visible], w.scale)
+    return out

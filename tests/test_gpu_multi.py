@@ -1,0 +1,125 @@
+"""GPU parity of multi-query paged decode (q_len new tokens per sequence, causal; the
+verification pass of speculative decoding) against the fp64 oracle: whole outputs
+at small sizes covering every group size, ragged lengths, contexts made only of the
+new tokens and long contexts cut between many workers; sampled outputs at the full
+spec-70b size after appending the step's tokens; status flags."""
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_decode_02_gb300.workloads import make_workload
+from parity_helpers import DECODE_ATOL, oracle_outputs_multi, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_decode_02_gb300 import build_lib
+    build_lib.build()
+    import paged_kv_decode_02_gb300 as pk
+    pk.load_library()
+    return pk
+
+
+def _run(pk, w, **kw):
+    return pk.paged_decode_attention_multi(w.q, w.k_cache, w.v_cache, w.block_tables,
+                                           w.context_lens, w.scale, **kw)
+
+
+def _err(out, ref, triples=None):
+    got = to_f64(out)
+    if triples is None:
+        assert np.all(np.isfinite(got))
+        return float(np.max(np.abs(got - ref)))
+    return float(max(np.max(np.abs(got[s, i, h] - ref[s, i, h])) for (s, i, h) in triples))
+
+
+SHAPES = [
+    # (id, Hq, Hkv, D, bs, q_len, lengths)
+    ("mha-q2", 4, 4, 128, 16, 2, [2, 17, 100, 0, 33]),
+    ("mha-q6-d64-bs32", 4, 4, 64, 32, 6, [6, 7, 64, 65, 300]),
+    ("g2-q3", 8, 4, 128, 16, 3, [3, 16, 19, 250]),
+    ("g4-q4", 16, 4, 128, 16, 4, [4, 5, 31, 200, 513]),
+    ("g8-q6", 16, 2, 128, 16, 6, [6, 40, 700, 12, 0, 64]),
+    ("g8-q16-bs32", 16, 2, 128, 32, 16, [16, 17, 300, 1000]),
+    ("g16-q2-d64", 32, 2, 64, 16, 2, [90, 17, 2]),
+    ("g5-q5", 10, 2, 128, 32, 5, [100, 5, 37]),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])
+def test_multi_small_shapes(pk, shape):
+    _, Hq, Hkv, D, bs, n, lengths = shape
+    w = make_workload("spec-70b", device=DEV, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                      block_size=bs, lengths=lengths, q_len=n, seed=13, poison_unused=True)
+    out = _run(pk, w)
+    torch.cuda.synchronize()
+    assert _err(out, oracle_outputs_multi(w)) <= DECODE_ATOL
+
+
+@pytest.mark.parametrize("Hq,Hkv,n", [(8, 1, 4), (1, 1, 8)])
+def test_multi_long_context_split_many_ways(pk, Hq, Hkv, n):
+    """One long context over every worker: the segments holding only the last block
+    leave fully masked rows for the early query tokens, which the merge must skip."""
+    w = make_workload("spec-70b", device=DEV, lengths=[20000], num_q_heads=Hq,
+                      num_kv_heads=Hkv, q_len=n, seed=14)
+    out = _run(pk, w)
+    torch.cuda.synchronize()
+    assert _err(out, oracle_outputs_multi(w)) <= DECODE_ATOL
+
+
+def test_multi_single_token_matches_decode(pk):
+    w = make_workload("70b-gqa", device=DEV, num_seqs=6, seed=15)
+    a = pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                                  w.scale)
+    b = pk.paged_decode_attention_multi(w.q[:, None], w.k_cache, w.v_cache, w.block_tables,
+                                        w.context_lens, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b[:, 0])
+
+
+def test_multi_full_size_after_append(pk):
+    """The spec-70b step: append the 6 new tokens of every request, then verify."""
+    w = make_workload("spec-70b", device=DEV)
+    pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
+    out = _run(pk, w)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    L = w.context_lens.cpu().numpy()
+    triples = {(int(np.argmax(L)), 0, 0), (int(np.argmax(L)), w.q_len - 1, w.num_q_heads - 1),
+               (int(np.argmin(L)), 0, 5)}
+    while len(triples) < 24:
+        triples.add((int(rng.integers(w.num_seqs)), int(rng.integers(w.q_len)),
+                     int(rng.integers(w.num_q_heads))))
+    triples = sorted(triples)
+    got = to_f64(out)
+    assert np.all(np.isfinite(got))
+    assert _err(out, oracle_outputs_multi(w, triples), triples) <= DECODE_ATOL
+
+
+def test_multi_flags_context_shorter_than_queries(pk):
+    w = make_workload("spec-70b", device=DEV, num_q_heads=16, num_kv_heads=2,
+                      lengths=[40, 9, 0], q_len=4, seed=16)
+    lens = w.context_lens.clone()
+    lens[1] = 2                               # 0 < L < q_len
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = pk.paged_decode_attention_multi(w.q, w.k_cache, w.v_cache, w.block_tables, lens,
+                                          w.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x1
+    got = to_f64(out)
+    assert np.all(got[1] == 0) and np.all(got[2] == 0)
+    ref = oracle_outputs_multi(w)
+    assert float(np.max(np.abs(got[0] - ref[0]))) <= DECODE_ATOL
+
+
+def test_multi_rejects_bad_query_length(pk):
+    w = make_workload("spec-70b", device=DEV, num_seqs=2, q_len=2, lengths=[5, 9])
+    q = torch.zeros((2, 17, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(pk.PagedKVError):
+        pk.paged_decode_attention_multi(q, w.k_cache, w.v_cache, w.block_tables,
+                                        w.context_lens, w.scale)

@@ -12,14 +12,19 @@ Sources (the pages the method is taken from):
   "两个特性截然不同的阶段" (decode reads the whole KV cache every step),
   "分页注意力" (fixed 16-token blocks, per-request block table, the 47/200-token
   worked example, at most 15 tokens wasted, prefix sharing), "块管理器：分页如何运作"
-  (free list, refcounted copy-on-write blocks), "INT8 仅权重量化" (``w_q = round(w/s)``)
-  and "KV 缓存量化" (per-token-per-head scales).
+  (free list, refcounted copy-on-write blocks, eviction of a request's blocks to
+  pinned host memory and back), "INT8 仅权重量化" (``w_q = round(w/s)``), "FP8（及
+  H100/H200 硬件路径）" (E4M3 and E5M2, E5M2 for KV caches), "KV 缓存量化"
+  (per-token-per-head scales) and "推测解码" (the target model scores k drafted
+  tokens plus one in a single pass: multi-query decode).
 * The gsyq.cn inference-optimisation page, section 2.1 (the KV-cache size formula and
   its 7B example), 2.2 (block sizes 16 or 32, shared blocks) and 2.3 (per-token or
   per-channel KV scales, softmax stability after quantisation).
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` against the pages'
-worked examples, closed forms, invariants and brute force; none is marked
+Every function here is pinned against the pages' worked examples, closed forms,
+invariants, independent implementations and brute force -- ``tests/test_oracle_pins.py``
+(paging, decode, INT8), ``tests/test_oracle_fp8_pins.py``, ``tests/test_oracle_multi_pins.py``
+and ``tests/test_oracle_block_pins.py`` (copy-on-write and swap); none is marked
 "parity unpinned".
 """
 
@@ -44,4 +49,7 @@ from .paged_attention import (  # noqa: F401
     append_scatter_fp8,
     gather_sequence_fp8,
     decode_attention_fp8,
+    copy_blocks,
+    swap_out_blocks,
+    swap_in_blocks,
 )

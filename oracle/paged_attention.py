@@ -394,3 +394,43 @@ def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, co
                 if _kv_head_of(h, g) == kvh:
                     out[s, h], _ = attend_one_head(q[s, h], K, V, scale)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Block moves -- "块管理器：分页如何运作" of the chenk.top page: a block shared under
+# copy-on-write is copied to a fresh block before a request writes into it; under
+# memory pressure a victim request's blocks are copied to pinned host memory and
+# freed, and copied back into (new) blocks later.
+# ---------------------------------------------------------------------------
+
+def copy_blocks(cache, src_ids, dst_ids):
+    """cache[dst_ids[i]] = cache[src_ids[i]] for every pair, all reads before any write.
+    The pairs must not chain: no destination may also be a source or repeat."""
+    src = [int(x) for x in src_ids]
+    dst = [int(x) for x in dst_ids]
+    if len(src) != len(dst):
+        raise ValueError("src_ids and dst_ids differ in length")
+    if len(set(dst)) != len(dst) or set(dst) & set(src):
+        raise ValueError("copy pairs chain or repeat a destination")
+    out = np.array(cache, copy=True)
+    saved = [np.array(cache[b], copy=True) for b in src]
+    for d, blk in zip(dst, saved):
+        out[d] = blk
+    return out
+
+
+def swap_out_blocks(cache, block_ids):
+    """The listed blocks stacked in list order: host[i] = cache[block_ids[i]]."""
+    return np.stack([np.array(cache[int(b)], copy=True) for b in block_ids]) if len(block_ids) \
+        else np.zeros((0,) + tuple(np.shape(cache)[1:]), dtype=np.asarray(cache).dtype)
+
+
+def swap_in_blocks(cache, host, block_ids):
+    """cache[block_ids[i]] = host[i]; the ids must be distinct. Returns a new array."""
+    ids = [int(b) for b in block_ids]
+    if len(set(ids)) != len(ids):
+        raise ValueError("swap-in ids repeat")
+    out = np.array(cache, copy=True)
+    for i, b in enumerate(ids):
+        out[b] = host[i]
+    return out

@@ -111,17 +111,49 @@ class SequenceBlocks:
         self.blocks = [self.alloc.fork(b) for b in other.blocks[:n]]
         self.num_tokens = num_tokens
 
-    def append_tokens(self, n: int) -> list[int]:
+    def fork_all(self, other: "SequenceBlocks") -> None:
+        """Share every block of ``other``, a partly filled last block included (a fork
+        for parallel sampling or beam search)."""
+        self.blocks = [self.alloc.fork(b) for b in other.blocks]
+        self.num_tokens = other.num_tokens
+
+    def append_tokens(self, n: int, copies: Optional[list] = None) -> list[int]:
         """Grow by ``n`` tokens, taking a fresh block whenever the last one is full.
+        Writing into a partly filled last block that another request still shares
+        first moves this request to a private copy (copy-on-write): a fresh block is
+        allocated, the pair (shared, fresh) is appended to ``copies`` for the device
+        block copy, and the shared block loses this request's reference.
         Returns each new token's slot (physical block * block_size + offset)."""
         slots = []
         for _ in range(n):
             off = self.num_tokens % self.block_size
             if off == 0:
                 self.blocks.append(self.alloc.allocate())
+            elif self.alloc.refcount[self.blocks[-1]] > 1:
+                if copies is None:
+                    raise ValueError("a write into a shared block needs a copy list")
+                fresh = self.alloc.allocate()
+                copies.append((self.blocks[-1], fresh))
+                self.alloc.free(self.blocks[-1])
+                self.blocks[-1] = fresh
             slots.append(self.blocks[-1] * self.block_size + off)
             self.num_tokens += 1
         return slots
+
+    def swap_out(self) -> list[int]:
+        """Evict: return the blocks to copy to host memory (in table order) and drop
+        this request's references to them."""
+        ids = list(self.blocks)
+        for b in ids:
+            self.alloc.free(b)
+        self.blocks = []
+        return ids
+
+    def swap_in(self, num_blocks: int) -> list[int]:
+        """Bring an evicted request back: allocate ``num_blocks`` fresh blocks (its new
+        table) for the copy from host memory."""
+        self.blocks = [self.alloc.allocate() for _ in range(num_blocks)]
+        return list(self.blocks)
 
     def release(self) -> None:
         for b in self.blocks:

@@ -45,6 +45,9 @@ WORKLOAD_TEXT = {
                 "block 32, per-token per-head fp32 scales",
     "fp8-e4m3": "FP8 E4M3 KV: batch 128, 32 q / 8 kv heads, head_dim 128, context 8192, "
                 "block 32, per-token per-head fp32 scales",
+    "blocks": "KV block moves on the 7B-like layer's cache (32 kv heads, head_dim 128, block 16, "
+              "bf16, 256 KiB per block with V): copy-on-write copy of half the pool, swap-out "
+              "of 8 requests (1024 blocks) to pinned host memory and swap-in back",
     "spec-70b": "speculative verification on the 70B-like GQA shape: batch 64, 64 q / 8 kv "
                 "heads, head_dim 128, block 16, context log-normal (median 1024, sigma 1) "
                 "clipped [128, 32768], q_len 6 new tokens per request (k = 5), causal",
@@ -462,6 +465,131 @@ def run_ours(args, rank, world):
     return result, w
 
 
+def run_blocks(args, rank, world):
+    """Block moves: the copy-on-write copy (HBM to HBM, read + write bytes against the
+    copy roofline) and eviction to / return from pinned host memory (GPU-driven over
+    NVLink-C2C), each timed with CUDA events over K back-to-back calls."""
+    import numpy as np
+    import torch
+
+    import paged_kv_decode_02_gb300 as pk
+    from paged_kv_decode_02_gb300 import build_lib
+    from paged_kv_decode_02_gb300.workloads import make_workload
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pk.load_library()
+    w = make_workload("7b", device=dev)
+    stream = torch.cuda.current_stream(dev)
+    blk_bytes = 2 * w.num_kv_heads * w.block_size * w.head_dim * 2       # K + V of a block
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(w.num_blocks)
+    n = w.num_blocks // 2
+    src = torch.tensor(perm[:n], dtype=torch.int32, device=dev)
+    dst = torch.tensor(perm[n:2 * n], dtype=torch.int32, device=dev)
+    L = w.context_lens.cpu().numpy()
+    victims = list(range(8))
+    ids_np = np.concatenate([w.block_tables[s, :-(-int(L[s]) // w.block_size)].cpu().numpy()
+                             for s in victims])
+    ids = torch.tensor(ids_np, dtype=torch.int32, device=dev)
+    host_k = torch.empty((len(ids_np),) + tuple(w.k_cache.shape[1:]),
+                         dtype=torch.bfloat16).pin_memory()
+    host_v = torch.empty_like(host_k).pin_memory()
+    K = max(1, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / K
+
+    clocks = ClockSampler(dev.index) if (rank == 0 and not args.no_clocks) else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    ms_copy = timed(lambda: pk.copy_blocks(w.k_cache, w.v_cache, src, dst))
+    ms_out = timed(lambda: pk.swap_out(w.k_cache, w.v_cache, ids, host_k, host_v))
+    ms_in = timed(lambda: pk.swap_in(w.k_cache, w.v_cache, ids, host_k, host_v))
+    # the two-step alternative: gather on the device, then one bulk copy to the host
+    staged = torch.empty((len(ids_np),) + tuple(w.k_cache.shape[1:]), dtype=torch.bfloat16,
+                         device=dev)
+    ids64 = ids.long()
+
+    def staged_out():
+        torch.index_select(w.k_cache, 0, ids64, out=staged)
+        host_k.copy_(staged, non_blocking=True)
+        torch.index_select(w.v_cache, 0, ids64, out=staged)
+        host_v.copy_(staged, non_blocking=True)
+    ms_staged = timed(staged_out)
+    clk = clocks.stop() if clocks else None
+    ms_copy_job = job_time_ms(ms_copy, world, dev)
+    copy_bytes = 2 * n * blk_bytes                     # every byte read once and written once
+    swap_bytes = len(ids_np) * blk_bytes
+    peak, peak_kind = measured_peak()
+    copy_gbs = job_throughput(copy_bytes, ms_copy_job, world)
+    return {
+        "metric": "KV block moves: copy-on-write block copy GB/s (read + write) against the "
+                  "HBM copy roofline; swap-out / swap-in GB/s to pinned host memory",
+        "value": round(copy_gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_copy_job, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD_TEXT["blocks"], "name": "blocks",
+                   "copy_pairs": n, "copy_bytes": copy_bytes, "swap_blocks": len(ids_np),
+                   "swap_bytes": swap_bytes,
+                   "l2": f"{copy_bytes / 1e6:.0f} MB moved per copy call vs "
+                         f"{L2_BYTES / 1e6:.0f} MB L2, no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(copy_bytes / (ms_copy * 1e-3) / 1e9, 2),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(copy_bytes / (ms_copy * 1e-3) / 1e9 / peak, 4),
+                     "traffic": None, "kernel": "paged_block_move_kernel (copy)",
+                     "bytes_per_launch": copy_bytes, "avg_launch_ms": round(ms_copy, 5),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
+        "swap": {"swap_out_gbs": round(swap_bytes / (ms_out * 1e-3) / 1e9, 2),
+                 "swap_in_gbs": round(swap_bytes / (ms_in * 1e-3) / 1e9, 2),
+                 "swap_out_ms": round(ms_out, 4), "swap_in_ms": round(ms_in, 4),
+                 "staged_swap_out_gbs": round(swap_bytes / (ms_staged * 1e-3) / 1e9, 2),
+                 "staged": "torch index_select into a device buffer + one copy to host, "
+                           "for comparison",
+                 "bound": "NVLink-C2C between the GPU and Grace memory"},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+    }
+
+
+def blocks_cpu_baseline(seconds):
+    """The oracle's block copy on host arrays of the same block shape (bounded)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(0)
+    cache = rng.integers(-2 ** 15, 2 ** 15, size=(64, 32, 16, 128),
+                         dtype=np.int16)                 # 2-byte elements, 128 KiB per block
+    src, dst = list(range(0, 32)), list(range(32, 64))
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.copy_blocks(cache, src, dst)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    moved = n * len(src) * cache[0].nbytes * 2
+    return {"value": round(moved / el / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} oracle copy_blocks calls of 32 blocks of 128 KiB (K only) on host "
+                      f"arrays, {el:.1f} s, numpy, one thread"}
+
+
 def job_time_ms(ms_local, world, device):
     """Whole-job time of the timed region: the maximum over ranks (replicas finish
     when the slowest does). With one rank, the local time."""
@@ -535,6 +663,18 @@ def run_reference(args, rank):
     from paged_kv_decode_02_gb300.workloads import make_workload
     if rank != 0:
         return None
+    if args.config == "blocks":
+        base = blocks_cpu_baseline(min(30.0, 2.0 + 0.05 * (args.steps + args.warmup)))
+        return {"impl": "reference",
+                "metric": "KV block moves: copy-on-write block copy GB/s (read + write) against "
+                          "the HBM copy roofline; swap-out / swap-in GB/s to pinned host memory",
+                "value": base["value"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+                "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+                "config": {"workload": WORKLOAD_TEXT["blocks"], "name": "blocks"},
+                "cpu_baseline": base,
+                "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
     w = make_workload(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
     units = _host_units(w, 16, seed=1)
     budget_s = 150.0
@@ -587,10 +727,15 @@ def main():
     if world > 1:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    res, w = run_ours(args, rank, world)
-    if rank == 0:
-        if not args.no_cpu_baseline:
+    if args.config == "blocks":
+        res = run_blocks(args, rank, world)
+        if rank == 0 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = blocks_cpu_baseline(min(args.cpu_seconds, 10.0))
+    else:
+        res, w = run_ours(args, rank, world)
+        if rank == 0 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.barrier()

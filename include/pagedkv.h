@@ -57,7 +57,8 @@ typedef enum pkv_status {
   PKV_ERR_UNSUPPORTED = -4,  /* head_dim / block_size / batch outside what is built */
   PKV_ERR_WORKSPACE = -5,    /* workspace NULL, too small or misaligned */
   PKV_ERR_CUDA = -6,         /* a CUDA runtime or driver call failed */
-  PKV_ERR_ALIGNMENT = -7     /* a device pointer is not 16-byte aligned */
+  PKV_ERR_ALIGNMENT = -7,    /* a device pointer is not 16-byte aligned */
+  PKV_ERR_HOST_MEMORY = -8   /* a host buffer is not pinned (page-locked) host memory */
 } pkv_status;
 
 typedef enum pkv_kv_dtype {
@@ -188,6 +189,49 @@ pkv_status pkv_decode_fp8(void* out, const void* q, const uint8_t* k_cache,
                           const int32_t* block_tables, const int32_t* context_lens, float scale,
                           pkv_kv_dtype fp8_format, const pkv_dims* dims, void* workspace,
                           size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
+
+/*
+ * Whole-block moves ("块管理器：分页如何运作", chenk.top page). One block of the cache
+ * holds the rows of every KV head: Hkv * block_size * head_dim elements of K (and of
+ * V), plus Hkv * block_size fp32 scales each for one-byte caches. kv_dtype selects
+ * the element size (PKV_KV_BF16: 2 bytes, no scales; INT8 / FP8: 1 byte + scales);
+ * the scale pointers are ignored (may be NULL) for bf16. Ids are device int32 arrays
+ * checked against [0, num_blocks): a pair with a bad id is skipped and, when
+ * `status` (optional device int32) is given, flagged PKV_DEV_BAD_BLOCK_ID. Moves are
+ * bit-exact. num_blocks_moved == 0 is a no-op.
+ *
+ * pkv_copy_blocks -- copy-on-write: block dst_ids[i] := block src_ids[i] for every
+ *   pair (K, V and scales). Before a request writes into a block that another request
+ *   still shares (refcount > 1 after a fork for parallel sampling, beam search or a
+ *   speculative rollback), the block manager moves it to a fresh block; this is that
+ *   copy, batched. The pairs must not chain: no destination may also be a source or
+ *   repeat (the copies run in parallel).
+ */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                           const int32_t* src_ids, const int32_t* dst_ids, int32_t num_pairs,
+                           pkv_kv_dtype kv_dtype, const pkv_dims* dims, int32_t* status,
+                           pkv_stream_t stream);
+
+/*
+ * pkv_swap_out -- eviction to host memory: host_k[i] := block block_ids[i] of k_cache
+ *   (likewise V and scales), i.e. the request's blocks packed densely in list order:
+ *   host_k [num_blocks_moved, Hkv, block_size, D], host_k_scale [num_blocks_moved,
+ *   Hkv, block_size]. The host buffers must be pinned host memory (cudaHostAlloc or
+ *   cudaHostRegister; else PKV_ERR_HOST_MEMORY): the GPU writes them directly.
+ * pkv_swap_in -- the reverse: block block_ids[i] := host_k[i] (block ids distinct).
+ * Both are asynchronous on `stream`; the host buffer must not be touched until the
+ * stream reaches the call.
+ */
+pkv_status pkv_swap_out(void* host_k, void* host_v, float* host_k_scale, float* host_v_scale,
+                        const void* k_cache, const void* v_cache, const float* k_scale,
+                        const float* v_scale, const int32_t* block_ids, int32_t num_blocks_moved,
+                        pkv_kv_dtype kv_dtype, const pkv_dims* dims, int32_t* status,
+                        pkv_stream_t stream);
+pkv_status pkv_swap_in(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                       const void* host_k, const void* host_v, const float* host_k_scale,
+                       const float* host_v_scale, const int32_t* block_ids,
+                       int32_t num_blocks_moved, pkv_kv_dtype kv_dtype, const pkv_dims* dims,
+                       int32_t* status, pkv_stream_t stream);
 
 /* Largest q_len of pkv_decode_multi_bf16. */
 #define PKV_MAX_QUERY_LEN 16

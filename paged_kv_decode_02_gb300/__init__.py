@@ -11,6 +11,7 @@ _API = (
     "paged_decode_attention", "paged_decode_attention_int8", "paged_decode_attention_fp8",
     "paged_decode_attention_cascade", "paged_decode_attention_multi",
     "cascade_workspace_bytes", "multi_workspace_bytes",
+    "copy_blocks", "swap_out", "swap_in",
     "decode_workspace_bytes", "library_path", "load_library", "PagedKVError",
     "Status", "Dims",
 )

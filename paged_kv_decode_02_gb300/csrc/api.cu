@@ -487,6 +487,82 @@ pkv_status check_append(const void* k, const void* v, const void* kc, const void
 
 using namespace pkv;
 
+namespace pkv {
+namespace {
+
+// Element sizes of a block move for a KV dtype: bytes per cache element, and whether
+// there are scale arrays.
+bool move_layout(int kvt, int* elt, bool* scales) {
+  switch (kvt) {
+    case PKV_KV_BF16: *elt = 2; *scales = false; return true;
+    case PKV_KV_INT8:
+    case PKV_KV_FP8_E4M3:
+    case PKV_KV_FP8_E5M2: *elt = 1; *scales = true; return true;
+    default: return false;
+  }
+}
+
+// The device address of a pinned host buffer (the same address under unified
+// addressing); false for pageable or unknown memory.
+bool host_device_ptr(const void* host, void** dev) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, host) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) return false;
+  *dev = attr.devicePointer;
+  return true;
+}
+
+enum MoveKind { kCopy, kSwapOut, kSwapIn };
+
+// cache arrays: k, v, ks, vs (device); other: host arrays in the same order (swap) or
+// unused (copy).
+pkv_status run_move(MoveKind kind, void* const cache[4], void* const other[4],
+                    const int32_t* src_ids, const int32_t* dst_ids, int32_t n, int kvt,
+                    const pkv_dims* d, int32_t* status, cudaStream_t stream) {
+  if (!d) return PKV_ERR_NULL;
+  if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 || d->block_size <= 0 ||
+      d->num_blocks <= 0 || n < 0)
+    return PKV_ERR_SHAPE;
+  int elt = 0;
+  bool scales = false;
+  if (!move_layout(kvt, &elt, &scales)) return PKV_ERR_DTYPE;
+  if (n == 0) return PKV_OK;
+  const int narrays = scales ? 4 : 2;
+  const long long rows = (long long)d->num_kv_heads * d->block_size;
+  const long long chunk[4] = {rows * d->head_dim * elt, rows * d->head_dim * elt, rows * 4,
+                              rows * 4};
+  for (int i = 0; i < narrays; ++i) {
+    if (chunk[i] % 16 != 0 || chunk[i] / 16 >= (1ll << 31)) return PKV_ERR_UNSUPPORTED;
+    if (!cache[i] || (kind != kCopy && !other[i])) return PKV_ERR_NULL;
+    if (!aligned16(cache[i]) || (kind != kCopy && !aligned16(other[i])))
+      return PKV_ERR_ALIGNMENT;
+  }
+  if ((kind != kSwapIn && !src_ids) || (kind != kSwapOut && !dst_ids)) return PKV_ERR_NULL;
+  MoveParams p{};
+  p.narrays = narrays;
+  p.n = n;
+  p.NB = d->num_blocks;
+  p.status = status;
+  p.src_ids = kind == kSwapIn ? nullptr : src_ids;
+  p.dst_ids = kind == kSwapOut ? nullptr : dst_ids;
+  for (int i = 0; i < narrays; ++i) {
+    void* host = nullptr;
+    if (kind != kCopy && !host_device_ptr(other[i], &host)) return PKV_ERR_HOST_MEMORY;
+    const void* src = kind == kSwapIn ? host : cache[i];
+    void* dst = kind == kSwapOut ? host : cache[i];
+    p.arrays[i].src = static_cast<const uint4*>(src);
+    p.arrays[i].dst = static_cast<uint4*>(dst);
+    p.arrays[i].chunk16 = int(chunk[i] / 16);
+  }
+  return launch_block_move(p, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pkv
+
 extern "C" {
 
 const char* pkv_status_string(pkv_status s) {
@@ -499,6 +575,7 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA call failed";
     case PKV_ERR_ALIGNMENT: return "PKV_ERR_ALIGNMENT: a device pointer is not 16-byte aligned";
+    case PKV_ERR_HOST_MEMORY: return "PKV_ERR_HOST_MEMORY: a host buffer is not pinned host memory";
   }
   return "unknown pkv_status";
 }
@@ -627,6 +704,40 @@ pkv_status pkv_decode_multi_bf16(void* out, const void* q, const void* k_cache,
   return run_decode(PKV_KV_BF16, out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
                     context_lens, scale, dims, workspace, workspace_bytes, status,
                     reinterpret_cast<cudaStream_t>(stream), q_len);
+}
+
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                           const int32_t* src_ids, const int32_t* dst_ids, int32_t num_pairs,
+                           pkv_kv_dtype kv_dtype, const pkv_dims* dims, int32_t* status,
+                           pkv_stream_t stream) {
+  void* cache[4] = {k_cache, v_cache, k_scale, v_scale};
+  void* none[4] = {nullptr, nullptr, nullptr, nullptr};
+  return run_move(kCopy, cache, none, src_ids, dst_ids, num_pairs, kv_dtype, dims, status,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_swap_out(void* host_k, void* host_v, float* host_k_scale, float* host_v_scale,
+                        const void* k_cache, const void* v_cache, const float* k_scale,
+                        const float* v_scale, const int32_t* block_ids, int32_t num_blocks_moved,
+                        pkv_kv_dtype kv_dtype, const pkv_dims* dims, int32_t* status,
+                        pkv_stream_t stream) {
+  void* cache[4] = {const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                    const_cast<float*>(k_scale), const_cast<float*>(v_scale)};
+  void* host[4] = {host_k, host_v, host_k_scale, host_v_scale};
+  return run_move(kSwapOut, cache, host, block_ids, nullptr, num_blocks_moved, kv_dtype, dims,
+                  status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_swap_in(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                       const void* host_k, const void* host_v, const float* host_k_scale,
+                       const float* host_v_scale, const int32_t* block_ids,
+                       int32_t num_blocks_moved, pkv_kv_dtype kv_dtype, const pkv_dims* dims,
+                       int32_t* status, pkv_stream_t stream) {
+  void* cache[4] = {k_cache, v_cache, k_scale, v_scale};
+  void* host[4] = {const_cast<void*>(host_k), const_cast<void*>(host_v),
+                   const_cast<float*>(host_k_scale), const_cast<float*>(host_v_scale)};
+  return run_move(kSwapIn, cache, host, nullptr, block_ids, num_blocks_moved, kv_dtype, dims,
+                  status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -83,6 +83,26 @@ struct MergeParams {
 
 void launch_merge(const MergeParams& p, cudaStream_t stream);
 
+// Whole-block moves (copy-on-write copy, swap-out, swap-in): pair i moves chunk
+// src_ids[i] (or i when src_ids is NULL: a dense host buffer) of every array to chunk
+// dst_ids[i] (or i). Ids are checked against [0, NB): a bad pair is skipped and
+// flagged PKV_DEV_BAD_BLOCK_ID.
+struct MoveArray {
+  const uint4* src;
+  uint4* dst;
+  int chunk16;                 // 16-byte words per block
+};
+struct MoveParams {
+  MoveArray arrays[4];
+  int narrays;
+  const int32_t* src_ids;
+  const int32_t* dst_ids;
+  int n, NB;
+  int32_t* status;
+};
+
+cudaError_t launch_block_move(const MoveParams& p, cudaStream_t stream);
+
 // A compiled decode kernel and its static shape.
 struct DecodeKernelInfo {
   const void* fn;

@@ -31,6 +31,7 @@ class Status(enum.IntEnum):
     ERR_WORKSPACE = -5
     ERR_CUDA = -6
     ERR_ALIGNMENT = -7
+    ERR_HOST_MEMORY = -8
 
 
 DEV_BAD_CONTEXT_LEN = 0x1
@@ -43,6 +44,10 @@ KV_INT8 = 1
 KV_FP8_E4M3 = 2
 KV_FP8_E5M2 = 3
 FP8_FORMATS = {"e4m3": KV_FP8_E4M3, "e5m2": KV_FP8_E5M2}
+
+
+_KV_OF_DTYPE = {torch.bfloat16: KV_BF16, torch.int8: KV_INT8, torch.uint8: None,
+                torch.float8_e4m3fn: KV_FP8_E4M3, torch.float8_e5m2: KV_FP8_E5M2}
 
 
 class PagedKVError(RuntimeError):
@@ -79,6 +84,15 @@ EXPORTS = {
                                                                ctypes.c_void_p, ctypes.c_void_p,
                                                                ctypes.c_size_t, ctypes.c_void_p,
                                                                ctypes.c_void_p]),
+    "pkv_copy_blocks": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int32, ctypes.c_int,
+                                                                ctypes.c_void_p, ctypes.c_void_p,
+                                                                ctypes.c_void_p]),
+    "pkv_swap_out": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int32, ctypes.c_int,
+                                                             ctypes.c_void_p, ctypes.c_void_p,
+                                                             ctypes.c_void_p]),
+    "pkv_swap_in": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int32, ctypes.c_int,
+                                                            ctypes.c_void_p, ctypes.c_void_p,
+                                                            ctypes.c_void_p]),
     "pkv_decode_multi_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
                                                         ctypes.POINTER(ctypes.c_size_t)]),
     "pkv_decode_multi_bf16": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int32,
@@ -355,6 +369,83 @@ def paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     scales ``k_scale``/``v_scale`` [NB, Hkv, bs]."""
     return _decode(_fp8_format(fmt), q, k_cache, v_cache, k_scale, v_scale, block_tables,
                    context_lens, scale, out, workspace, status)
+
+
+def _move_kv(k_cache, kv_dtype):
+    """KV dtype code of a block move: from the cache dtype, or ``kv_dtype`` (needed for
+    uint8 FP8 codes, where any one-byte code gives the same move)."""
+    kv = _KV_OF_DTYPE.get(k_cache.dtype, -1) if kv_dtype is None else kv_dtype
+    if kv is None:
+        kv = KV_FP8_E5M2                      # uint8 codes: one byte + scales
+    if kv == -1:
+        raise TypeError(f"unsupported cache dtype {k_cache.dtype}")
+    return kv
+
+
+def _move_dims(k_cache):
+    nb, hkv, bs, d = k_cache.shape
+    return Dims(0, hkv, hkv, d, bs, nb, 1)
+
+
+def copy_blocks(k_cache, v_cache, src_ids, dst_ids, k_scale=None, v_scale=None, status=None,
+                kv_dtype=None):
+    """Copy-on-write block copy: block dst_ids[i] := block src_ids[i] of the K/V caches
+    (and their scales, for one-byte caches). ``src_ids``/``dst_ids``: device int32.
+    In place, asynchronous on the current stream."""
+    dev = k_cache.device
+    kv = _move_kv(k_cache, kv_dtype)
+    for t, n in ((src_ids, "src_ids"), (dst_ids, "dst_ids")):
+        _require(t, n, torch.int32, 1, dev)
+    if src_ids.numel() != dst_ids.numel():
+        raise ValueError("src_ids and dst_ids differ in length")
+    dims = _move_dims(k_cache)
+    with _OnDevice(dev):
+        st = _lib().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                    _ptr(src_ids), _ptr(dst_ids), src_ids.numel(), kv,
+                                    ctypes.byref(dims), _ptr(status), _stream(dev))
+    _check(st, "pkv_copy_blocks")
+
+
+def _host(t, name):
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned host tensor")
+    return t
+
+
+def swap_out(k_cache, v_cache, block_ids, host_k, host_v, k_scale=None, v_scale=None,
+             host_k_scale=None, host_v_scale=None, status=None, kv_dtype=None):
+    """Evict blocks to pinned host memory: host_k[i] := block block_ids[i] (likewise V
+    and scales). Asynchronous on the current stream."""
+    dev = k_cache.device
+    kv = _move_kv(k_cache, kv_dtype)
+    _require(block_ids, "block_ids", torch.int32, 1, dev)
+    for t, n in ((host_k, "host_k"), (host_v, "host_v")):
+        _host(t, n)
+    dims = _move_dims(k_cache)
+    with _OnDevice(dev):
+        st = _lib().pkv_swap_out(_ptr(host_k), _ptr(host_v), _ptr(host_k_scale),
+                                 _ptr(host_v_scale), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                 _ptr(v_scale), _ptr(block_ids), block_ids.numel(), kv,
+                                 ctypes.byref(dims), _ptr(status), _stream(dev))
+    _check(st, "pkv_swap_out")
+
+
+def swap_in(k_cache, v_cache, block_ids, host_k, host_v, k_scale=None, v_scale=None,
+            host_k_scale=None, host_v_scale=None, status=None, kv_dtype=None):
+    """Bring evicted blocks back: block block_ids[i] := host_k[i] (likewise V and
+    scales). Asynchronous on the current stream."""
+    dev = k_cache.device
+    kv = _move_kv(k_cache, kv_dtype)
+    _require(block_ids, "block_ids", torch.int32, 1, dev)
+    for t, n in ((host_k, "host_k"), (host_v, "host_v")):
+        _host(t, n)
+    dims = _move_dims(k_cache)
+    with _OnDevice(dev):
+        st = _lib().pkv_swap_in(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                _ptr(host_k), _ptr(host_v), _ptr(host_k_scale),
+                                _ptr(host_v_scale), _ptr(block_ids), block_ids.numel(), kv,
+                                ctypes.byref(dims), _ptr(status), _stream(dev))
+    _check(st, "pkv_swap_in")
 
 
 def multi_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,

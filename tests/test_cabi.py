@@ -53,6 +53,7 @@ def test_binding_signatures_cover_the_header(lib_path):
     assert lib.pkv_status_string(0) == b"PKV_OK"
     assert b"NULL" in lib.pkv_status_string(-1)
     assert lib.pkv_status_string(12345) == b"unknown pkv_status"
+    assert b"pinned" in lib.pkv_status_string(-8)
 
 
 def test_host_validation_without_gpu(lib_path):
@@ -101,6 +102,24 @@ def test_host_validation_without_gpu(lib_path):
     st = lib.pkv_append_fp8(p, p, p, p, None, p, p, 3, pagedkv.KV_FP8_E4M3, ctypes.byref(good),
                             None)
     assert st == pagedkv.Status.ERR_NULL
+    # block moves: argument checks before any CUDA call
+    st = lib.pkv_copy_blocks(p, p, None, None, None, p, 4, pagedkv.KV_BF16, ctypes.byref(good),
+                             None, None)
+    assert st == pagedkv.Status.ERR_NULL
+    st = lib.pkv_copy_blocks(p, p, None, None, p, p, 4, 9, ctypes.byref(good), None, None)
+    assert st == pagedkv.Status.ERR_DTYPE
+    st = lib.pkv_copy_blocks(p, p, None, None, p, p, 0, pagedkv.KV_BF16, ctypes.byref(good),
+                             None, None)
+    assert st == pagedkv.Status.OK
+    st = lib.pkv_copy_blocks(p, p, None, None, p, p, 4, pagedkv.KV_INT8, ctypes.byref(good),
+                             None, None)
+    assert st == pagedkv.Status.ERR_NULL                  # one-byte caches need scales
+    st = lib.pkv_swap_out(None, p, p, p, p, p, p, p, p, 4, pagedkv.KV_INT8, ctypes.byref(good),
+                          None, None)
+    assert st == pagedkv.Status.ERR_NULL
+    st = lib.pkv_swap_in(p, mis, None, None, p, p, None, None, p, 4, pagedkv.KV_BF16,
+                         ctypes.byref(good), None, None)
+    assert st == pagedkv.Status.ERR_ALIGNMENT
     n = ctypes.c_size_t(0)
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 4, ctypes.byref(n)) == \
         pagedkv.Status.ERR_DTYPE

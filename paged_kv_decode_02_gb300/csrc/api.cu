@@ -314,7 +314,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   m.gs = P.gs;
   m.nsg = P.nsg;
   m.HU = P.HU;
-  m.W = P.W;
+  m.W = P.W / P.nsg;  // workers of nsg warps
   launch_merge(m, stream);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
@@ -464,6 +464,7 @@ pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void
   m.nsg = P.nsg;
   m.HU = P.HU;
   m.W = P.W;
+  m.Wg = P.W / P.nsg;
   m.R = C.R;
   m.nsplit = C.nsplit;
   launch_cascade_merge(m, stream);

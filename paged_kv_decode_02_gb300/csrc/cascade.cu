@@ -171,19 +171,22 @@ __global__ void __launch_bounds__(kCascadeThreads)
   }
 
   // the parts: nsplit prefix records, then the suffix parts
+  // suffix parts: the decode kernel's flat order is (sequence, KV head, block) over Wg
+  // workers of nsg warps; this unit's parts come from warp worker * nsg + sg
   const int n = p.prefix[s + 1] - p.prefix[s];
-  const long long T = (long long)p.HU * p.prefix[p.B];
+  const long long T = (long long)p.Hkv * p.prefix[p.B];
+  const int Wg = p.Wg;
   int nsuf = 0, w0 = 0;
   bool dense = true, first_cut = false, whole = false;
   long long A = 0;
   if (n > 0) {
-    A = (long long)p.HU * p.prefix[s] + (long long)u * n;
-    w0 = int(((A + 1) * p.W + T - 1) / T) - 1;
-    const int w1 = int(((A + n) * p.W + T - 1) / T) - 1;
+    A = (long long)p.Hkv * p.prefix[s] + (long long)h * n;
+    w0 = int(((A + 1) * Wg + T - 1) / T) - 1;
+    const int w1 = int(((A + n) * Wg + T - 1) / T) - 1;
     whole = (w0 == w1);
-    dense = T >= p.W;
+    dense = T >= Wg;
     nsuf = whole ? 1 : (dense ? (w1 - w0 + 1) : n);
-    first_cut = (T * w0 / p.W) != A;
+    first_cut = (T * w0 / Wg) != A;
   }
   const int nparts = p.nsplit + nsuf;
   const size_t prow = size_t(s) * p.g + size_t(sg) * gs;  // prefix record row of row 0
@@ -198,8 +201,8 @@ __global__ void __launch_bounds__(kCascadeThreads)
     const int k = i - p.nsplit;
     size_t slot;
     if (whole) slot = size_t(2 * p.W) + size_t(s) * p.HU + u;
-    else if (dense) slot = size_t(2 * (w0 + k) + ((k == 0 && first_cut) ? 1 : 0));
-    else slot = size_t(2 * (int(((A + k + 1) * p.W + T - 1) / T) - 1));
+    else if (dense) slot = size_t(2 * ((w0 + k) * p.nsg + sg) + ((k == 0 && first_cut) ? 1 : 0));
+    else slot = size_t(2 * ((int(((A + k + 1) * Wg + T - 1) / T) - 1) * p.nsg + sg));
     o = p.part_o + slot * gs * D;
     ml = reinterpret_cast<const float2*>(p.part_ml) + slot * gs;
   };

@@ -153,7 +153,7 @@ __device__ __forceinline__ int causal_hidden(const DecodeParams& p, int u, int r
 }
 
 // Where a warp leaves a cut unit: slot 2w for the unit its range starts in, 2w+1
-// for the unit its range ends in.
+// for the unit its range ends in (w = worker * nsg + row subgroup).
 __device__ __forceinline__ size_t partial_slot(int w, bool first_segment) {
   return size_t(2 * w + (first_segment ? 0 : 1));
 }
@@ -820,27 +820,27 @@ struct MmaPathInt8 {
 // Work cursor over the flat (sequence, unit, block) order.
 // ===========================================================================
 struct Cursor {
-  int s, u, j, n;
+  int s, u, j, n;  // sequence, unit of the sequence (U per sequence), block, blocks of s
 };
 
 __device__ __forceinline__ void cursor_locate(Cursor& c, long long f, const int* prefix, int B,
-                                              int HU) {
-  int lo = 0, hi = B;  // HU*prefix[lo] <= f < HU*prefix[hi]
+                                              int U) {
+  int lo = 0, hi = B;  // U*prefix[lo] <= f < U*prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if ((long long)HU * prefix[mid] <= f) lo = mid; else hi = mid;
+    if ((long long)U * prefix[mid] <= f) lo = mid; else hi = mid;
   }
   c.s = lo;
   c.n = prefix[lo + 1] - prefix[lo];
-  const long long rem = f - (long long)HU * prefix[lo];
+  const long long rem = f - (long long)U * prefix[lo];
   c.u = int(rem / c.n);
   c.j = int(rem % c.n);
 }
 
-__device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B, int HU) {
+__device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B, int U) {
   if (++c.j < c.n) return;
   c.j = 0;
-  if (++c.u < HU) return;
+  if (++c.u < U) return;
   c.u = 0;
   do { ++c.s; } while (c.s < B && prefix[c.s + 1] == prefix[c.s]);
   c.n = c.s < B ? prefix[c.s + 1] - prefix[c.s] : 0;
@@ -911,11 +911,16 @@ __global__ void __launch_bounds__(kWarps * 32)
       for (int i = tid; i <= B; i += nthr) p.prefix_out[i] = s_prefix[i];
   }
 
-  const int HU = p.HU;
-  const long long T = (long long)HU * s_prefix[B];
-  const int W = gridDim.x * kWarps;
+  // Flat order (sequence, KV head, block), cut into Wg equal ranges. A worker is nsg
+  // consecutive warps, one per row subgroup of the KV head: they stream the same blocks
+  // at the same time, so all but the first read of a block hit L2.
+  const int Hkv = p.Hkv, nsg = p.nsg;
+  const long long T = (long long)Hkv * s_prefix[B];
+  const int Wg = (gridDim.x * kWarps) / nsg;
   const int w = blockIdx.x * kWarps + warp;
-  const long long a = T * w / W, b = T * (w + 1) / W;
+  const int wk = w / nsg, sg = w % nsg;
+  if (wk >= Wg) return;
+  const long long a = T * wk / Wg, b = T * (wk + 1) / Wg;
   if (a >= b) return;
   const int nblk = int(b - a);
 
@@ -934,8 +939,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   __syncwarp();
 
-  Cursor pc, cc;
-  cursor_locate(pc, a, s_prefix, B, HU);
+  Cursor pc, cc;  // u: the KV head
+  cursor_locate(pc, a, s_prefix, B, Hkv);
   cc = pc;
 
   // lane 0 issues the copies of the block at the producer cursor into stage st
@@ -943,8 +948,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (lane == 0) {
       int phys = __ldg(p.block_tables + size_t(pc.s) * p.MBS + p.skip + pc.j);
       phys = (phys < 0 || phys >= p.NB) ? 0 : phys;  // never copy outside the pool
-      const int kvh = pc.u / p.nsg;
-      const int row = (phys * p.Hkv + kvh) * BS;
+      const int row = (phys * p.Hkv + pc.u) * BS;
       mbar_arrive_expect_tx(bar(st), K::kTxBytes);
 #pragma unroll
       for (int hf = 0; hf < Geo::kHalves; ++hf) {
@@ -962,12 +966,12 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int npro = min(kStages, nblk);
   for (int i = 0; i < npro; ++i) {
     issue(i);
-    cursor_next(pc, s_prefix, B, HU);
+    cursor_next(pc, s_prefix, B, Hkv);
   }
 
   Path path;
   path.init(lane);
-  path.begin(p, cc.s, cc.u);
+  path.begin(p, cc.s, cc.u * nsg + sg);
   int seg_j0 = cc.j;
   bool first_seg = true;
   int Lc = min(__ldg(p.context_lens + cc.s), p.MBS * BS);
@@ -989,22 +993,23 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (i + kStages < nblk) {
       fence_proxy_async_smem();
       issue(st);
-      cursor_next(pc, s_prefix, B, HU);
+      cursor_next(pc, s_prefix, B, Hkv);
     }
     const bool seg_end = (cc.j == cc.n - 1) || (i == nblk - 1);
     if (seg_end) {
       const bool complete = (seg_j0 == 0) && (cc.j == cc.n - 1);
       if (complete && p.unit_slot0 >= 0)  // cascade: the suffix result is one more part
-        path.finish(p, false, size_t(p.unit_slot0) + size_t(cc.s) * HU + cc.u);
+        path.finish(p, false,
+                    size_t(p.unit_slot0) + size_t(cc.s) * p.HU + size_t(cc.u) * nsg + sg);
       else
         path.finish(p, complete, partial_slot(w, first_seg));
       first_seg = false;
     }
-    cursor_next(cc, s_prefix, B, HU);
+    cursor_next(cc, s_prefix, B, Hkv);
     if (seg_end && i + 1 < nblk) {
       seg_j0 = cc.j;
       Lc = min(__ldg(p.context_lens + cc.s), p.MBS * BS);
-      path.begin(p, cc.s, cc.u);
+      path.begin(p, cc.s, cc.u * nsg + sg);
     }
   }
 }

@@ -60,7 +60,9 @@ struct CascadeMergeParams {
   const int32_t* context_lens;
   int32_t* status;
   int B, Hq, Hkv, D, MBS, NB, BS, P;
-  int g, gs, nsg, HU, W, R, nsplit;
+  int g, gs, nsg, HU, R, nsplit;
+  int W;                       // decode warps (whole-unit records start at slot 2W)
+  int Wg;                      // decode workers (groups of nsg warps)
 };
 
 bool select_prefix_kernel(int D, int BS, const void** fn, int* smem_bytes);
@@ -78,7 +80,7 @@ struct MergeParams {
   int B, Hq, D, MBS, NB, BS;
   int q_len;                   // new tokens per sequence (rows map as in DecodeParams)
   int g, gs, nsg, HU;
-  int W;                       // number of decode workers (warps)
+  int W;                       // decode workers (groups of nsg warps)
 };
 
 void launch_merge(const MergeParams& p, cudaStream_t stream);

@@ -64,8 +64,11 @@ __global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const
       *reinterpret_cast<uint2*>(out_row(o / Q) + 4 * (o % Q)) = make_uint2(0u, 0u);
     return;
   }
-  const long long T = (long long)p.HU * p.prefix[p.B];
-  const long long A = (long long)p.HU * p.prefix[s] + (long long)u * n;
+  // the decode kernel's flat order is (sequence, KV head, block) over W workers of nsg
+  // warps each; this unit's parts come from warp worker * nsg + sg of each worker
+  const int nsg = p.nsg, kvh = u / nsg, sg = u % nsg, Hkv = p.HU / nsg;
+  const long long T = (long long)Hkv * p.prefix[p.B];
+  const long long A = (long long)Hkv * p.prefix[s] + (long long)kvh * n;
   const int W = p.W;
   const int w0 = merge_worker_of(A, T, W), w1 = merge_worker_of(A + n - 1, T, W);
   if (w0 == w1) return;  // one worker covered the whole unit and wrote the output
@@ -75,8 +78,8 @@ __global__ void __launch_bounds__(kMergeThreads) paged_decode_merge_kernel(const
   const int nparts = dense ? (w1 - w0 + 1) : n;
   const bool first_cut = merge_worker_start(T, w0, W) != A;
   auto slot_of = [&](int i) -> size_t {
-    if (dense) return size_t(2 * (w0 + i) + ((i == 0 && first_cut) ? 1 : 0));
-    return size_t(2 * merge_worker_of(A + i, T, W));
+    if (dense) return size_t(2 * ((w0 + i) * nsg + sg) + ((i == 0 && first_cut) ? 1 : 0));
+    return size_t(2 * (merge_worker_of(A + i, T, W) * nsg + sg));
   };
 
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);

@@ -325,8 +325,8 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
 // ---------------------------------------------------------------------------
 struct CascadePlan {
   Plan dec;                    // suffix decode (its partial arrays get 2W + B*HU slots)
-  int R, nsplit, per_split, psmem;
-  const void* pfn;
+  int R, nsplit, per_split;
+  PrefixKernelInfo pk;
   size_t off_prefix, off_ml, off_o, off_pre_o, off_pre_ml, ws_bytes;
 };
 
@@ -334,17 +334,21 @@ pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* 
   pkv_status st = make_plan(d, PKV_KV_BF16, &cp->dec);
   if (st != PKV_OK) return st;
   if (prefix_blocks < 1 || prefix_blocks > d->max_blocks_per_seq) return PKV_ERR_SHAPE;
-  if (!select_prefix_kernel(d->head_dim, d->block_size, &cp->pfn, &cp->psmem))
-    return PKV_ERR_UNSUPPORTED;
+  if (!select_prefix_kernel(d->head_dim, d->block_size, &cp->pk)) return PKV_ERR_UNSUPPORTED;
   const Plan& P = cp->dec;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PKV_ERR_CUDA;
   cp->R = d->num_seqs * P.g;
-  const int ctas = ((cp->R + 63) / 64) * d->num_kv_heads;
-  int nsplit = std::max(1, std::min(prefix_blocks, (3 * sms + ctas - 1) / ctas));
-  cp->per_split = (prefix_blocks + nsplit - 1) / nsplit;
+  // one CTA per SM (TMEM and shared memory): split the prefix so that the
+  // (row tile, KV head, split) grid fills at most one wave, cutting at tile boundaries
+  const int ctas = ((cp->R + cp->pk.rows - 1) / cp->pk.rows) * d->num_kv_heads;
+  const int tiles = (prefix_blocks + cp->pk.tile_blocks - 1) / cp->pk.tile_blocks;
+  const int max_tiles = cp->pk.max_split_blocks / cp->pk.tile_blocks;
+  const int nsplit = std::max((tiles + max_tiles - 1) / max_tiles,
+                              std::max(1, std::min(tiles, sms / std::max(1, ctas))));
+  cp->per_split = ((tiles + nsplit - 1) / nsplit) * cp->pk.tile_blocks;
   cp->nsplit = (prefix_blocks + cp->per_split - 1) / cp->per_split;
   const size_t nslots = size_t(2) * P.W + size_t(d->num_seqs) * P.HU;
   cp->off_prefix = 0;
@@ -354,7 +358,7 @@ pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* 
   const size_t recs = size_t(cp->nsplit) * d->num_kv_heads * cp->R;
   cp->off_pre_ml = align_up(cp->off_pre_o + recs * d->head_dim * 4, 256);
   cp->ws_bytes = align_up(cp->off_pre_ml + recs * 8, 256);
-  if (cudaFuncSetAttribute(cp->pfn, cudaFuncAttributeMaxDynamicSharedMemorySize, cp->psmem) !=
+  if (cudaFuncSetAttribute(cp->pk.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, cp->pk.smem) !=
       cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;
@@ -405,8 +409,8 @@ pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void
   pp.status = status;
   {
     void* args[] = {&tmk, &tmv, &pp};
-    if (launch_pdl(C.pfn, dim3((C.R + 63) / 64, d->num_kv_heads, C.nsplit), dim3(160), args,
-                   C.psmem, stream) != cudaSuccess)
+    if (launch_pdl(C.pk.fn, dim3((C.R + C.pk.rows - 1) / C.pk.rows, d->num_kv_heads, C.nsplit),
+                   dim3(C.pk.threads), args, C.pk.smem, stream) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
   // 2. the private suffixes: the ordinary decode over the tables past the prefix; a

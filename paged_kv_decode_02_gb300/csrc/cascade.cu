@@ -6,123 +6,406 @@
 // block tables. Every query row of a KV head then attends the same prefix keys, so for
 // the prefix the B*g query rows of a KV head form a real dense contraction:
 //   S = Q_rows (B*g x D) . K_prefix^T (D x P*bs),  O = softmax-weighted V_prefix.
-// paged_prefix_kernel computes it once per KV head on the tensor cores (a producer warp
-// streams each prefix block into shared memory once per CTA for four consumer warps of
-// 16 query rows), leaving unnormalised partials per query row. The private suffixes go
+// paged_prefix_kernel computes it once per KV head on the fifth-generation tensor cores
+// (tcgen05 MMAs with operands in shared memory and accumulators in tensor memory, 128
+// query rows per CTA), leaving unnormalised partials per query row. The private suffixes go
 // through the ordinary decode kernel (skipping the prefix entries of the tables), and
 // paged_cascade_merge_kernel folds prefix and suffix partials with the online-softmax
 // rescaling. The result equals decode attention over the whole table.
 #include "decode.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
-template <int D, int BS, int kStages>
-struct PrefixKernel {
-  using Geo = TileGeom<false, D, BS>;
-  static constexpr int kTile = Geo::kTileBytes;
-  static constexpr int kConsumers = 4;                    // 16 query rows each
-  static constexpr int kRows = 16 * kConsumers;
-  static constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
-  static constexpr int kOffV = kStages * kTile;
-  static constexpr int kOffBar = 2 * kStages * kTile;     // full[kStages], empty[kStages]
-  static constexpr int kSmem = kOffBar + 2 * kStages * 8 + 1024;
+// ---------------------------------------------------------------------------
+// Prefix kernel on the fifth-generation tensor cores. One CTA takes 128 query rows
+// of one KV head and one split of the prefix, in tiles of 128 prefix tokens:
+//   S_j = Q K_j^T          (tcgen05 MMA, M 128 x N 128 x K D, fp32 in TMEM, two buffers)
+//   P_j = 2^(S_j*scale*log2e - m)   (softmax warps, one row per thread, bf16 to TMEM)
+//   O  += P_j V_j          (tcgen05 MMA, A = P from TMEM, M 128 x N D x K 128, fp32 in TMEM)
+// Roles: warps 0 and 6 issue the TMA copies of the K and the V tiles (128 tokens as
+// boxes of one block x 64 columns, 128-byte swizzled; lane b copies block b, so the
+// small copies of a tile leave in parallel and a score MMA never waits behind a V
+// tile); warp 1 allocates TMEM and one of its threads issues every MMA; warps 2..5
+// (TMEM lane quarters 2, 3, 0, 1) run the online softmax. The running reference max m of a row moves only when a tile's max
+// exceeds it by more than 8 (log2 units); O in TMEM is then rescaled by 2^(m_old -
+// m_new) before the next P.V accumulates, so weights stay below 2^8 and most tiles
+// skip the rescale. Each split leaves per row the unnormalised (o, m, l) record that
+// the cascade merge folds.
+// Shared memory (1024-byte aligned): Q [D/64 slabs][128 rows x 128 B], K and V
+// tiles x2 [D/64 slabs][128 tokens x 128 B], then the mbarriers, the TMEM address
+// word and the split's block ids. TMEM columns: S x2 [0, 256), O [256, 256 + D),
+// P (bf16 pairs) [384, 448).
+// ---------------------------------------------------------------------------
+template <int D, int BS>
+struct PrefixTc {
+  static constexpr int kM = 128;                      // query rows per CTA
+  static constexpr int kN = 128;                      // prefix tokens per tile
+  static constexpr int kBlocks = kN / BS;             // blocks per tile
+  static constexpr int kSlabs = D / 64;               // 128-byte column slabs of a row
+  static constexpr int kSlab = kN * 128;              // one slab of a K or V tile
+  static constexpr int kQSlab = kM * 128;
+  static constexpr int kTile = kSlabs * kSlab;        // a K or V tile
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kSlabs * kQSlab;
+  static constexpr int kOffV = kOffK + 2 * kTile;
+  static constexpr int kOffBar = kOffV + 2 * kTile;
+  // mbarriers: kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] pfull ofull mdone
+  static constexpr int kNumBars = 13;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kMaxIds = 2048;                // prefix blocks per split (planner cap)
+  static constexpr int kOffIds = kOffAbort + 4;
+  static constexpr int kSmem = kOffIds + 4 * kMaxIds + 1024;  // + slack for 1024-byte alignment
+  static constexpr int kThreads = 224;  // warps: 0 K copies, 1 MMA, 2..5 softmax, 6 V copies
+  static constexpr uint32_t kTmemCols = 512;          // power of two
+  static constexpr int kColS = 0, kColO = 2 * kN, kColP = 2 * kN + 128;
+  static_assert(kColP + kN / 2 <= int(kTmemCols) && kColO + D <= kColP, "TMEM columns");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert(kN % BS == 0 && D % 64 == 0, "tile shape");
+  static_assert(kQSlab == kSlab, "Q, K and P slabs share one stride");
+  static_assert(kMaxIds % kBlocks == 0, "split cap in whole tiles");
 };
 
-template <int D, int BS, int kStages>
-__global__ void __launch_bounds__(PrefixKernel<D, BS, kStages>::kThreads)
-    paged_prefix_kernel(const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmv, const PrefixParams pp) {
-  using K = PrefixKernel<D, BS, kStages>;
-  using Geo = typename K::Geo;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.y, z = blockIdx.z;
-  const int b0 = z * pp.per_split, b1 = min(pp.P, b0 + pp.per_split);
-  const int nb = max(0, b1 - b0);
-  auto sK = [&](int st) { return base + st * K::kTile; };
-  auto sV = [&](int st) { return base + K::kOffV + st * K::kTile; };
-  auto full = [&](int st) { return base + K::kOffBar + st * 8; };
-  auto empty = [&](int st) { return base + K::kOffBar + (kStages + st) * 8; };
-  pdl_wait_prior_grid();
-  if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) {
-      mbar_init(full(st), 1);
-      mbar_init(empty(st), K::kConsumers);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == K::kConsumers) {  // producer: one TMA stream per CTA
-    if (lane == 0) {
-      for (int i = 0; i < nb; ++i) {
-        const int st = i % kStages;
-        if (i >= kStages &&
-            !mbar_wait_bounded(empty(st), uint32_t(i / kStages - 1) & 1u, pp.timeout_ns)) {
-          if (pp.status) atomicOr(pp.status, 0x4);
-          break;
-        }
-        int phys = __ldg(pp.prefix_ids + b0 + i);
-        phys = (phys < 0 || phys >= pp.NB) ? 0 : phys;  // never copy outside the pool
-        const int row = (phys * pp.Hkv + h) * BS;
-        mbar_arrive_expect_tx(full(st), 2 * K::kTile);
-#pragma unroll
-        for (int hf = 0; hf < Geo::kHalves; ++hf) {
-          const int x = hf * (Geo::kSeg / Geo::kElt);
-          tma_load_2d(sK(st) + hf * BS * Geo::kSeg, &tmk, full(st), x, row);
-          tma_load_2d(sV(st) + hf * BS * Geo::kSeg, &tmv, full(st), x, row);
-        }
+// Bounded wait that also gives up once another thread of the CTA has given up.
+__device__ __forceinline__ bool prefix_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                            volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        return false;
       }
     }
-    return;
   }
+}
 
-  // consumer warp: query rows r0 = rbase + gid and r1 = r0 + 8 of KV head h
-  MmaPathBf16<D, BS> path;
-  path.init(lane);
-  const int gid = lane >> 2;
-  const int r0 = blockIdx.x * K::kRows + warp * 16 + gid, r1 = r0 + 8;
-  const bool v0 = r0 < pp.R, v1 = r1 < pp.R;
-  auto qrow = [&](int r) {
-    const int s = r / pp.g, i = r % pp.g;
-    return reinterpret_cast<const uint32_t*>(pp.q) + (size_t(s) * pp.Hq + h * pp.g + i) * (D / 2);
-  };
-  path.load_q(qrow(v0 ? r0 : 0), qrow(v1 ? r1 : 0), v0, v1);
-  DecodeParams dp{};
-  dp.scale_log2 = pp.scale_log2;
-  for (int i = 0; i < nb; ++i) {
-    const int st = i % kStages;
-    if (!__all_sync(0xffffffffu,
-                    mbar_wait_bounded(full(st), uint32_t(i / kStages) & 1u, pp.timeout_ns))) {
-      if (lane == 0 && pp.status) atomicOr(pp.status, 0x4);
-      return;
-    }
-    path.block(dp, sK(st), sV(st), 0u, 0u, BS);
-    __syncwarp();
-    if (lane == 0) {
-      fence_proxy_async_smem();  // this warp's reads of the stage before the refill
-      mbar_arrive(empty(st));
-    }
-  }
-  const size_t rec = size_t(z * pp.Hkv + h) * pp.R;
-  float2* ml = reinterpret_cast<float2*>(pp.pre_ml);
-  path.store_rows(pp.pre_o + (rec + (v0 ? r0 : 0)) * D, pp.pre_o + (rec + (v1 ? r1 : 0)) * D,
-                  ml + rec + (v0 ? r0 : 0), ml + rec + (v1 ? r1 : 0), v0, v1);
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
 template <int D, int BS>
-void prefix_info(const void** fn, int* smem) {
-  constexpr int kStages = 4;
-  *fn = reinterpret_cast<const void*>(&paged_prefix_kernel<D, BS, kStages>);
-  *smem = PrefixKernel<D, BS, kStages>::kSmem;
+__global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
+    paged_prefix_kernel(const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const PrefixParams pp) {
+  using K = PrefixTc<D, BS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(smem_raw + (base - raw) + K::kOffAbort);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y, z = blockIdx.z;
+  const int row0 = blockIdx.x * K::kM;
+  const int b0 = z * pp.per_split, b1 = min(pp.P, b0 + pp.per_split);
+  const int nb = max(0, b1 - b0);
+  const int ntiles = (nb + K::kBlocks - 1) / K::kBlocks;
+  auto bar = [&](int i) { return base + K::kOffBar + 8 * i; };
+  auto kfull = [&](int st) { return bar(st); };
+  auto kempty = [&](int st) { return bar(2 + st); };
+  auto vfull = [&](int st) { return bar(4 + st); };
+  auto vempty = [&](int st) { return bar(6 + st); };
+  auto sfull = [&](int st) { return bar(8 + st); };
+  const uint32_t pfull = bar(10), ofull = bar(11), mdone = bar(12);
+  const uint32_t tmem_slot = base + K::kOffTmemSlot;
+
+  pdl_wait_prior_grid();
+  if (tid == 0) {
+    for (int i = 0; i < 10; ++i) mbar_init(bar(i), 1);
+    mbar_init(pfull, 4 * 32);
+    mbar_init(ofull, 1);
+    mbar_init(mdone, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, K::kTmemCols);
+
+  // this split's physical block ids -> shared memory (the producer's copies then need
+  // no dependent global load)
+  int* s_ids = reinterpret_cast<int*>(smem_raw + (base - raw) + K::kOffIds);
+  for (int i = tid; i < min(nb, K::kMaxIds); i += K::kThreads)
+    s_ids[i] = __ldg(pp.prefix_ids + b0 + i);
+  // Q rows of this CTA -> shared memory as the K-major A operand (zero rows past R);
+  // every load is issued before the first store
+  {
+    const uint4* q = reinterpret_cast<const uint4*>(pp.q);
+    constexpr int kChunks = D / 8;  // 16-byte chunks per row
+    constexpr int kIters = (K::kM * kChunks + K::kThreads - 1) / K::kThreads;
+    uint4 v[kIters];
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+      const int c = tid + it * K::kThreads;
+      const int r = c / kChunks, cc = c % kChunks;
+      const int gr = row0 + r;
+      v[it] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < K::kM * kChunks && gr < pp.R) {
+        const int s = gr / pp.g, i = gr % pp.g;
+        v[it] = __ldg(q + (size_t(s) * pp.Hq + h * pp.g + i) * kChunks + cc);
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+      const int c = tid + it * K::kThreads;
+      const int r = c / kChunks, cc = c % kChunks;
+      if (c < K::kM * kChunks)
+        sts128(base + K::kOffQ + (cc >> 3) * K::kQSlab + r * 128 + (((cc & 7) ^ (r & 7)) << 4),
+               v[it]);
+    }
+  }
+  fence_proxy_async_smem();  // Q (generic-proxy writes) before the MMAs read it
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem_raw + (base - raw) +
+                                                             K::kOffTmemSlot);
+
+  if (warp == 0 || warp == 6) {
+    // ---------------- TMA producers: warp 0 streams K, warp 6 streams V ----------------
+    // lane b issues the copies of block b of a tile, so a tile's copies leave together
+    const bool is_k = warp == 0;
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    const uint32_t region = base + (is_k ? K::kOffK : K::kOffV);
+    const int rows_total = pp.NB * pp.Hkv * BS;  // a box at this row is all zero fill
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      const uint32_t fb = is_k ? kfull(st) : vfull(st);
+      if (j >= 2 &&
+          !__all_sync(0xffffffffu, prefix_wait(is_k ? kempty(st) : vempty(st),
+                                               uint32_t((j >> 1) - 1) & 1u, pp.timeout_ns,
+                                               abort_flag)))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(fb, K::kTile);
+      __syncwarp();
+      if (lane < K::kBlocks) {
+        const int i = j * K::kBlocks + lane;  // block of the split
+        int row = rows_total;
+        if (i < nb) {
+          int phys = s_ids[i];
+          phys = (phys < 0 || phys >= pp.NB) ? 0 : phys;  // never copy outside the pool
+          row = (phys * pp.Hkv + h) * BS;
+        }
+        const uint32_t dst = region + st * K::kTile + lane * BS * 128;
+#pragma unroll
+        for (int sl = 0; sl < K::kSlabs; ++sl)
+          tma_load_2d(dst + sl * K::kSlab, map, fb, sl * 64, row);
+      }
+      issued = j + 1;
+    }
+    // every copy issued must have landed before the CTA may exit
+    if (lane == 0)
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        mbar_wait_bounded(is_k ? kfull(j & 1) : vfull(j & 1), uint32_t(j >> 1) & 1u,
+                          pp.timeout_ns);
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t kIdS = tc::idesc_bf16<128, K::kN, false>();
+      constexpr uint32_t kIdO = tc::idesc_bf16<128, D, true>();
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!prefix_wait(kfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t kb = base + K::kOffK + st * K::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * K::kQSlab + (kk & 3) * 32;  // kQSlab == kSlab
+          tc::mma_bf16(tmem + K::kColS + st * K::kN,
+                       tc::sdesc_sw128(base + K::kOffQ + koff, 16, 1024),
+                       tc::sdesc_sw128(kb + koff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        }
+        tc::commit(sfull(st));
+        tc::commit(kempty(st));
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!prefix_wait(vfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag) ||
+            !prefix_wait(pfull, uint32_t(j) & 1u, pp.timeout_ns, abort_flag))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t vb = base + K::kOffV + st * K::kTile;
+#pragma unroll
+        for (int kk = 0; kk < K::kN / 16; ++kk) {
+          // A = P in TMEM (8 columns per 16 tokens), B = V (MN-major: D contiguous,
+          // tokens as rows)
+          tc::mma_bf16_tmem_a(tmem + K::kColO, tmem + K::kColP + kk * 8,
+                              tc::sdesc_sw128(vb + kk * 16 * 128, K::kSlab, 1024), kIdO,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::commit(vempty(st));
+        tc::commit(ofull);
+        return true;
+      };
+      bool ok = true;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        ok = issue_s(j);
+        if (ok && j >= 1) ok = issue_pv(j - 1);
+      }
+      if (ok && ntiles > 0) issue_pv(ntiles - 1);
+      // every MMA issued must have completed before TMEM is freed
+      tc::commit(mdone);
+      mbar_wait_bounded(mdone, 0u, pp.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax warps (2..5): one query row per thread ----------------
+    const int quarter = warp & 3;  // warps 2, 3, 4, 5 own TMEM lanes 64.., 96.., 0.., 32..
+    const int r = quarter * 32 + lane;
+    const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
+    const float sl = pp.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      if (!__all_sync(0xffffffffu,
+                      prefix_wait(sfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t s[K::kN];
+      tc::tmem_ld128(trow + K::kColS + st * K::kN, s);
+      // scores of masked columns (past the split, zero-filled K) never count; a
+      // negative scale is carried by flipping the scores' signs (warp-uniform branches,
+      // taken only on a split's last tile or with scale < 0)
+      const int valid = min(K::kBlocks, nb - j * K::kBlocks) * BS;
+      if (sl < 0.f) {
+#pragma unroll
+        for (int t = 0; t < K::kN; ++t) s[t] ^= 0x80000000u;
+      }
+      if (valid < K::kN) {
+#pragma unroll
+        for (int t = 0; t < K::kN; ++t)
+          if (t >= valid) s[t] = 0xff800000u;  // -inf
+      }
+      const float asl = fabsf(sl);
+      float mx[8];  // eight interleaved partial maxima: short dependency chains
+#pragma unroll
+      for (int t = 0; t < K::kN; ++t)
+        mx[t & 7] = (t < 8) ? __uint_as_float(s[t]) : fmaxf(mx[t & 7], __uint_as_float(s[t]));
+      const float mt = asl * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mt > m_ref + 8.f) {
+        alpha = fast_exp2(m_ref - mt);  // 0 on the first tile
+        m_ref = mt;
+        l *= alpha;
+        rescale = j > 0;
+      }
+      uint32_t pk[K::kN / 2];
+      float sm[4] = {0.f, 0.f, 0.f, 0.f};
+      const float nm = -m_ref;
+      if (valid == K::kN) {
+#pragma unroll
+        for (int t = 0; t < K::kN; t += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(s[t]), asl, nm));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(s[t + 1]), asl, nm));
+          sm[(t >> 1) & 3] += p0 + p1;
+          pk[t / 2] = pack_bf16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < K::kN; t += 2) {
+          const float p0 = t < valid ? fast_exp2(fmaf(__uint_as_float(s[t]), asl, nm)) : 0.f;
+          const float p1 =
+              t + 1 < valid ? fast_exp2(fmaf(__uint_as_float(s[t + 1]), asl, nm)) : 0.f;
+          sm[(t >> 1) & 3] += p0 + p1;
+          pk[t / 2] = pack_bf16x2(p0, p1);
+        }
+      }
+      l += (sm[0] + sm[1]) + (sm[2] + sm[3]);
+      // P.V of the previous tile must be complete before P is overwritten or O rescaled
+      if (j > 0 && !__all_sync(0xffffffffu, prefix_wait(ofull, uint32_t(j - 1) & 1u,
+                                                        pp.timeout_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tc::tmem_ld32(trow + K::kColO + c, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::tmem_st32(trow + K::kColO + c, o);
+        }
+      }
+      // P row -> TMEM (bf16 pairs of consecutive tokens), the A operand of P.V
+#pragma unroll
+      for (int c = 0; c < K::kN / 2; c += 32) {
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) w[e] = pk[c + e];
+        tc::tmem_st32(trow + K::kColP + c, w);
+      }
+      tc::fence_before_sync();
+      mbar_arrive(pfull);
+    }
+    if (ok && ntiles > 0 &&
+        !__all_sync(0xffffffffu, prefix_wait(ofull, uint32_t(ntiles - 1) & 1u, pp.timeout_ns,
+                                             abort_flag)))
+      ok = false;
+    tc::fence_after_sync();
+    const int gr = row0 + r;
+    const size_t rec = size_t(z * pp.Hkv + h) * pp.R + gr;
+    float4* dst = reinterpret_cast<float4*>(pp.pre_o + rec * D);
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      if (ok && ntiles > 0) {
+        tc::tmem_ld32(trow + K::kColO + c, o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+      if (gr < pp.R) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          dst[(c + e) / 4] = make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                         __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+      }
+    }
+    if (gr < pp.R)
+      reinterpret_cast<float2*>(pp.pre_ml)[rec] =
+          (ok && ntiles > 0) ? make_float2(m_ref, l) : make_float2(-INFINITY, 0.f);
+    tc::fence_before_sync();
+  }
+  __syncthreads();
+  if (*abort_flag && tid == 0 && pp.status) atomicOr(pp.status, 0x4);
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, K::kTmemCols);
+  }
 }
 
-bool select_prefix_kernel(int D, int BS, const void** fn, int* smem_bytes) {
-  if (D == 128 && BS == 16) prefix_info<128, 16>(fn, smem_bytes);
-  else if (D == 128 && BS == 32) prefix_info<128, 32>(fn, smem_bytes);
-  else if (D == 64 && BS == 16) prefix_info<64, 16>(fn, smem_bytes);
-  else if (D == 64 && BS == 32) prefix_info<64, 32>(fn, smem_bytes);
+template <int D, int BS>
+void prefix_info(PrefixKernelInfo* info) {
+  using K = PrefixTc<D, BS>;
+  info->fn = reinterpret_cast<const void*>(&paged_prefix_kernel<D, BS>);
+  info->smem = K::kSmem;
+  info->threads = K::kThreads;
+  info->rows = K::kM;
+  info->tile_blocks = K::kBlocks;
+  info->max_split_blocks = K::kMaxIds;
+}
+
+bool select_prefix_kernel(int D, int BS, PrefixKernelInfo* info) {
+  if (D == 128 && BS == 16) prefix_info<128, 16>(info);
+  else if (D == 128 && BS == 32) prefix_info<128, 32>(info);
+  else if (D == 64 && BS == 16) prefix_info<64, 16>(info);
+  else if (D == 64 && BS == 32) prefix_info<64, 32>(info);
   else return false;
   return true;
 }

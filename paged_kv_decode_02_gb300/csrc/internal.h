@@ -65,7 +65,16 @@ struct CascadeMergeParams {
   int Wg;                      // decode workers (groups of nsg warps)
 };
 
-bool select_prefix_kernel(int D, int BS, const void** fn, int* smem_bytes);
+// The compiled prefix kernel for a (head_dim, block_size) and its launch shape.
+struct PrefixKernelInfo {
+  const void* fn;
+  int smem;          // dynamic shared memory bytes
+  int threads;       // threads per CTA
+  int rows;          // query rows per CTA
+  int tile_blocks;   // prefix blocks per tile (splits are cut at tile boundaries)
+  int max_split_blocks;  // most prefix blocks one split may hold (a multiple of tile_blocks)
+};
+bool select_prefix_kernel(int D, int BS, PrefixKernelInfo* info);
 void launch_cascade_merge(const CascadeMergeParams& p, cudaStream_t stream);
 
 // Parameters of the split-KV merge launch (units cut between decode workers).

@@ -311,6 +311,64 @@ def test_cascade_small_shapes(pk, shape):
     assert float((out.float() - plain.float()).abs().max()) <= DECODE_ATOL
 
 
+def test_cascade_row_tiles_and_ragged_prefix_tail(pk):
+    # 70 sequences x 4 query heads per KV head = 280 query rows (two full 128-row tiles
+    # and a ragged one); a 21-block prefix ends 5 blocks into its third 128-token tile
+    rng = np.random.default_rng(5)
+    pre, bs = 21 * 16, 16
+    lengths = [pre + int(x) for x in rng.integers(0, 100, size=70)]
+    w = make_workload("prefix", device=DEV, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                      block_size=bs, lengths=lengths, prefix_tokens=pre, seed=21,
+                      poison_unused=True)
+    out = _cascade(pk, w, pre // bs)
+    torch.cuda.synchronize()
+    ref = oracle_outputs(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+
+
+def test_cascade_scores_growing_across_prefix_tiles(pk):
+    # Prefix keys scaled by 1, 5, 9, 13 in successive 128-token tiles: each tile's
+    # maximum score exceeds the previous tiles' by far more than 2^8, so the prefix
+    # kernel's accumulated output must be rescaled between tiles. 700 x 1 query rows
+    # per KV head keep the grid above one wave, hence one prefix split on any GPU.
+    # Such peaked weights make each output nearly one V row, so V is scaled by 1/4
+    # (exact in bf16) to keep outputs in the range the bf16 tolerance is set for.
+    pre, bs = 512, 16
+    rng = np.random.default_rng(6)
+    lengths = [pre + int(x) for x in rng.integers(0, 17, size=700)]
+    w = make_workload("prefix", device=DEV, num_q_heads=32, num_kv_heads=32, head_dim=128,
+                      block_size=bs, lengths=lengths, prefix_tokens=pre, seed=22)
+    kc = w.k_cache.clone()
+    for j in range(pre // bs):
+        phys = int(w.block_tables[0, j])
+        kc[phys] = (kc[phys].float() * (1 + 4 * (j * bs // 128))).to(torch.bfloat16)
+    w.k_cache = kc
+    w.v_cache = w.v_cache * 0.25
+    out = _cascade(pk, w, pre // bs)
+    torch.cuda.synchronize()
+    pairs = sample_pairs(w, 48, seed=3)
+    ref = oracle_outputs(w, pairs)
+    assert max_err(out, ref, pairs) <= DECODE_ATOL
+    plain = _decode(pk, w)
+    torch.cuda.synchronize()
+    assert float((out.float() - plain.float()).abs().max()) <= DECODE_ATOL
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.125], ids=["zero", "negative"])
+def test_cascade_zero_and_negative_scale(pk, scale):
+    # scale 0 weighs every position equally; a negative scale flips the ordering of
+    # the scores (the prefix ends 3 blocks into its second 128-token tile)
+    pre, bs = 11 * 16, 16
+    w = make_workload("prefix", device=DEV, num_q_heads=16, num_kv_heads=4, head_dim=64,
+                      block_size=bs, lengths=[pre + x for x in (0, 5, 40, 17, 90)],
+                      prefix_tokens=pre, seed=23, poison_unused=True)
+    w.scale = scale
+    out = _cascade(pk, w, pre // bs)
+    torch.cuda.synchronize()
+    ref = oracle_outputs(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+
+
 def test_cascade_full_prefix_workload(pk):
     w = make_workload("prefix", device=DEV)
     out = _cascade(pk, w, 2048 // w.block_size)

@@ -13,6 +13,7 @@
 // paged_cascade_merge_kernel folds prefix and suffix partials with the online-softmax
 // rescaling. The result equals decode attention over the whole table.
 #include "decode.cuh"
+#include "fold.cuh"
 #include "tcgen05.cuh"
 
 namespace pkv {
@@ -411,47 +412,52 @@ bool select_prefix_kernel(int D, int BS, PrefixKernelInfo* info) {
 }
 
 // ---------------------------------------------------------------------------
-// Cascade merge: one CTA per (sequence, unit) folds the nsplit prefix partials of its
-// query rows and the suffix parts (the unit's own record when one decode worker
-// covered the whole suffix, else the cut workers' slots). With a status word it first
-// validates the sequence: context length in [prefix, max_blocks*block_size], block ids
-// in the pool, and the table's head equal to the shared prefix (row 0); a sequence
-// that fails gets a zero output.
+// Cascade merge: one warp per (sequence, unit, group of query rows), one 16-byte
+// output quad per lane, folds the nsplit prefix partials of its rows and the suffix
+// parts (the unit's own record when one decode worker covered the whole suffix, else
+// the cut workers' slots). With a status word it first validates the sequence:
+// context length in [prefix, max_blocks*block_size], block ids in the pool, and the
+// table's head equal to the shared prefix (row 0); a sequence that fails gets a zero
+// output.
 // ---------------------------------------------------------------------------
-constexpr int kCascadeThreads = 256;
+constexpr int kCascadeWarps = 8;  // one (unit, row group) per warp
 
-__global__ void __launch_bounds__(kCascadeThreads)
+__global__ void __launch_bounds__(kCascadeWarps * 32, 4)
     paged_cascade_merge_kernel(const CascadeMergeParams p) {
   pdl_wait_prior_grid();
-  const int s = blockIdx.x / p.HU, u = blockIdx.x % p.HU;
+  const int lane = threadIdx.x & 31;
+  const int gs = p.gs, D = p.D, Q = D / 4;
+  const int rpw = 32 / Q;                 // rows per warp: one output quad per lane
+  const int ngrp = (gs + rpw - 1) / rpw;  // row groups per unit
+  const int item = blockIdx.x * kCascadeWarps + (threadIdx.x >> 5);
+  if (item >= p.B * p.HU * ngrp) return;
+  const int unit = item / ngrp, r0 = (item % ngrp) * rpw;
+  const int s = unit / p.HU, u = unit % p.HU;
   const int h = u / p.nsg, sg = u % p.nsg;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gs = p.gs, D = p.D, Q = D / 4, nout = gs * Q;
-  __nv_bfloat16* out =
-      reinterpret_cast<__nv_bfloat16*>(p.out) + (size_t(s) * p.Hq + h * p.g + sg * gs) * D;
+  const int row = r0 + lane / Q, dq = lane % Q;
+  const bool active = row < gs;
+  uint2* out = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                        (size_t(s) * p.Hq + h * p.g + sg * gs + row) * D) +
+               dq;
 
   if (p.status != nullptr) {
-    __shared__ int s_flags;
-    if (tid == 0) s_flags = 0;
-    __syncthreads();
     int flags = 0;
     const int L = p.context_lens[s];
-    if (tid == 0 && (L < p.P * p.BS || L > p.MBS * p.BS)) flags |= (L < p.P * p.BS) ? 0x8 : 0x1;
+    if (lane == 0 && (L < p.P * p.BS || L > p.MBS * p.BS)) flags |= (L < p.P * p.BS) ? 0x8 : 0x1;
     const int n = L <= 0 ? 0 : min((L + p.BS - 1) / p.BS, p.MBS);
-    for (int j = tid; j < n; j += blockDim.x) {
+    for (int j = lane; j < n; j += 32) {
       const int id = p.block_tables[size_t(s) * p.MBS + j];
       if (id < 0 || id >= p.NB) flags |= 0x2;
       if (j < p.P && id != p.block_tables[j]) flags |= 0x8;
     }
-    if (flags) atomicOr(&s_flags, flags);
-    __syncthreads();
-    if (s_flags) {
-      if (tid == 0 && u == 0) atomicOr(p.status, s_flags);
-      for (int o = tid; o < nout; o += blockDim.x)
-        *reinterpret_cast<uint2*>(out + size_t(o / Q) * D + 4 * (o % Q)) = make_uint2(0u, 0u);
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (flags) {
+      if (lane == 0 && u == 0 && r0 == 0) atomicOr(p.status, flags);
+      if (active) *out = make_uint2(0u, 0u);
       return;
     }
   }
+  if (!active) return;
 
   // the parts: nsplit prefix records, then the suffix parts
   // suffix parts: the decode kernel's flat order is (sequence, KV head, block) over Wg
@@ -472,13 +478,13 @@ __global__ void __launch_bounds__(kCascadeThreads)
     first_cut = (T * w0 / Wg) != A;
   }
   const int nparts = p.nsplit + nsuf;
-  const size_t prow = size_t(s) * p.g + size_t(sg) * gs;  // prefix record row of row 0
-  // row 0 of part i: (o, ml) base pointers
-  auto part = [&](int i, const float*& o, const float2*& ml) {
+  const size_t prow = size_t(s) * p.g + size_t(sg) * gs + row;  // prefix record row
+  Fold f = fold_empty();
+  fold_parts<4>(f, 0, 1, nparts, [&](int i, const float2*& pm, const float4*& po) {
     if (i < p.nsplit) {
       const size_t rec = size_t(i * p.Hkv + h) * p.R + prow;
-      o = p.pre_o + rec * D;
-      ml = reinterpret_cast<const float2*>(p.pre_ml) + rec;
+      pm = reinterpret_cast<const float2*>(p.pre_ml) + rec;
+      po = reinterpret_cast<const float4*>(p.pre_o + rec * D) + dq;
       return;
     }
     const int k = i - p.nsplit;
@@ -486,80 +492,21 @@ __global__ void __launch_bounds__(kCascadeThreads)
     if (whole) slot = size_t(2 * p.W) + size_t(s) * p.HU + u;
     else if (dense) slot = size_t(2 * ((w0 + k) * p.nsg + sg) + ((k == 0 && first_cut) ? 1 : 0));
     else slot = size_t(2 * ((int(((A + k + 1) * Wg + T - 1) / T) - 1) * p.nsg + sg));
-    o = p.part_o + slot * gs * D;
-    ml = reinterpret_cast<const float2*>(p.part_ml) + slot * gs;
-  };
-
-  constexpr int kWarps = kCascadeThreads / 32;
-  __shared__ float s_max[16];
-  __shared__ float4 s_acc[kCascadeThreads];
-  __shared__ float s_l[kCascadeThreads];
-  for (int r = warp; r < gs; r += kWarps) {
-    float mx = -INFINITY;
-    for (int i = lane; i < nparts; i += 32) {
-      const float* o;
-      const float2* ml;
-      part(i, o, ml);
-      mx = fmaxf(mx, ml[r].x);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) s_max[r] = mx;
-  }
-  __syncthreads();
-
-  for (int o0 = 0; o0 < nout; o0 += blockDim.x) {
-    const int span = min(nout - o0, int(blockDim.x));
-    const int NG = blockDim.x / span;
-    const int oi = o0 + tid % span, grp = tid / span;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
-    if (grp < NG) {
-      const int row = oi / Q, dq = oi % Q;
-      const float M = s_max[row];
-      for (int i = grp; i < nparts; i += NG) {
-        const float* o;
-        const float2* ml;
-        part(i, o, ml);
-        const float2 v = ml[row];
-        const float4 x = reinterpret_cast<const float4*>(o + size_t(row) * D)[dq];
-        const float f = fast_exp2(v.x - M);
-        L = fmaf(f, v.y, L);
-        acc.x = fmaf(f, x.x, acc.x);
-        acc.y = fmaf(f, x.y, acc.y);
-        acc.z = fmaf(f, x.z, acc.z);
-        acc.w = fmaf(f, x.w, acc.w);
-      }
-    }
-    s_acc[tid] = acc;
-    s_l[tid] = L;
-    __syncthreads();
-    if (grp == 0) {
-      for (int k = 1; k < NG; ++k) {
-        const float4 a = s_acc[k * span + (oi - o0)];
-        acc.x += a.x;
-        acc.y += a.y;
-        acc.z += a.z;
-        acc.w += a.w;
-        L += s_l[k * span + (oi - o0)];
-      }
-      const float inv = 1.f / L;
-      uint2 pk;
-      pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-      pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(out + size_t(oi / Q) * D + 4 * (oi % Q)) = pk;
-    }
-    __syncthreads();
-  }
+    pm = reinterpret_cast<const float2*>(p.part_ml) + slot * gs + row;
+    po = reinterpret_cast<const float4*>(p.part_o + (slot * gs + row) * D) + dq;
+  });
+  *out = fold_result(f);
 }
 
 void launch_cascade_merge(const CascadeMergeParams& p, cudaStream_t stream) {
-  const int grid = p.B * p.HU;
-  if (grid <= 0) return;
+  const int rpw = 32 / (p.D / 4);
+  const long long items = (long long)p.B * p.HU * ((p.gs + rpw - 1) / rpw);
+  if (items <= 0) return;
+  const int grid = int((items + kCascadeWarps - 1) / kCascadeWarps);
   CascadeMergeParams copy = p;
   void* args[] = {&copy};
   launch_pdl(reinterpret_cast<const void*>(&paged_cascade_merge_kernel), dim3(grid),
-             dim3(kCascadeThreads), args, 0, stream);
+             dim3(kCascadeWarps * 32), args, 0, stream);
 }
 
 }  // namespace pkv

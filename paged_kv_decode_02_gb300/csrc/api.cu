@@ -187,7 +187,7 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
   bool found = false;
   if (q_len > 1) {
     if (kvt != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
-    found = select_decode_bf16_multi(d->head_dim, d->block_size, &P.k);
+    found = select_decode_bf16_multi(d->head_dim, d->block_size, P.nsg, &P.k);
   } else {
     switch (kvt) {
       case PKV_KV_BF16: found = select_decode_bf16(d->head_dim, d->block_size, simt, &P.k); break;
@@ -202,7 +202,9 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
     }
   }
   if (!found) return PKV_ERR_UNSUPPORTED;
-  P.smem = size_t(P.k.warps) * P.k.warp_smem + 1024 + align_up(size_t(d->num_seqs + 1) * 4, 16);
+  // shared-memory rings per CTA: one per warp, or one per worker of nsg warps
+  const int rings = P.k.coop ? P.k.warps / P.nsg : P.k.warps;
+  P.smem = size_t(rings) * P.k.warp_smem + 1024 + align_up(size_t(d->num_seqs + 1) * 4, 16);
 
   int dev = 0, sms = 0, per_sm = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -223,7 +225,8 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
       per_sm <= 0)
     return PKV_ERR_CUDA;
   P.grid = sms * per_sm;
-  P.W = P.grid * P.k.warps;
+  // decode warps that own partial slots (warps left idle by a cooperative CTA own none)
+  P.W = P.k.coop ? P.grid * rings * P.nsg : P.grid * P.k.warps;
 
   // workspace: [prefix (B+1) int32][partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
   P.off_prefix = 0;

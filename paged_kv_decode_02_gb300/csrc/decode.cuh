@@ -849,33 +849,51 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B,
 // ===========================================================================
 // The kernel
 // ===========================================================================
-template <bool Q8, int D, int BS, class Path, int kWarps, int kStages>
+// kCoop = false: every warp is a worker with its own ring of stages, filled by its own
+// lane 0. kCoop = true (multi-query decode): a worker is nsg warps of one CTA, one per
+// row subgroup of a KV head; they share one ring, filled once per block by the first
+// warp of the worker (the leader) and released by all nsg warps through an "empty"
+// mbarrier per stage, so a block crosses from L2 into shared memory once per worker
+// rather than once per warp.
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false>
 struct DecodeKernel {
   using Geo = TileGeom<Q8, D, BS>;
   static constexpr int kTile = Geo::kTileBytes;
   static constexpr int kScaleBytes = Geo::kScaleBytes;
-  // per-warp shared memory: K tiles, V tiles, K/V scales, mbarriers
+  // per-ring shared memory: K tiles, V tiles, K/V scales, mbarriers (full[kStages],
+  // then empty[kStages] for a shared ring)
   static constexpr int kOffV = kStages * kTile;
   static constexpr int kOffScale = 2 * kStages * kTile;
   static constexpr int kOffBar = kOffScale + kStages * 2 * kScaleBytes;
-  static constexpr int kWarpBytes = ((kOffBar + kStages * 8) + 1023) / 1024 * 1024;
+  static constexpr int kWarpBytes =
+      ((kOffBar + (kCoop ? 2 : 1) * kStages * 8) + 1023) / 1024 * 1024;
   static constexpr uint32_t kTxBytes = 2 * kTile + 2 * kScaleBytes;
 };
 
-template <bool Q8, int D, int BS, class Path, int kWarps, int kStages>
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false>
 __global__ void __launch_bounds__(kWarps * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
-  using K = DecodeKernel<Q8, D, BS, Path, kWarps, kStages>;
+  using K = DecodeKernel<Q8, D, BS, Path, kWarps, kStages, kCoop>;
   using Geo = typename K::Geo;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
-  int* s_prefix = reinterpret_cast<int*>(smem_gen + kWarps * K::kWarpBytes);
+  const int nsg = p.nsg;
+  const int wpc = kCoop ? kWarps / nsg : kWarps;  // rings (workers or warps) per CTA
+  int* s_prefix = reinterpret_cast<int*>(smem_gen + wpc * K::kWarpBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.B;
   pdl_wait_prior_grid();
+  if constexpr (kCoop) {  // shared rings: barriers ready before the CTA-wide sync below
+    if (tid < wpc * kStages) {
+      const uint32_t rb = smem_base + (tid / kStages) * K::kWarpBytes + K::kOffBar;
+      mbar_init(rb + (tid % kStages) * 8, 1);
+      mbar_init(rb + (kStages + tid % kStages) * 8, uint32_t(nsg));
+    }
+    fence_mbar_init();
+  }
 
   // ---- blocks per sequence and their exclusive prefix (every CTA computes it) ----
   {
@@ -914,28 +932,45 @@ __global__ void __launch_bounds__(kWarps * 32)
   // Flat order (sequence, KV head, block), cut into Wg equal ranges. A worker is nsg
   // consecutive warps, one per row subgroup of the KV head: they stream the same blocks
   // at the same time, so all but the first read of a block hit L2.
-  const int Hkv = p.Hkv, nsg = p.nsg;
+  const int Hkv = p.Hkv;
   const long long T = (long long)Hkv * s_prefix[B];
-  const int Wg = (gridDim.x * kWarps) / nsg;
-  const int w = blockIdx.x * kWarps + warp;
-  const int wk = w / nsg, sg = w % nsg;
+  int Wg, wk, sg, ring;
+  if constexpr (kCoop) {
+    if (warp >= wpc * nsg) return;  // warps left over when nsg does not divide kWarps
+    Wg = gridDim.x * wpc;
+    wk = blockIdx.x * wpc + warp / nsg;
+    sg = warp % nsg;
+    ring = warp / nsg;
+  } else {
+    Wg = (gridDim.x * kWarps) / nsg;
+    wk = (blockIdx.x * kWarps + warp) / nsg;
+    sg = (blockIdx.x * kWarps + warp) % nsg;
+    ring = warp;
+  }
+  const int w = wk * nsg + sg;  // partial slots 2w, 2w + 1
   if (wk >= Wg) return;
   const long long a = T * wk / Wg, b = T * (wk + 1) / Wg;
   if (a >= b) return;
   const int nblk = int(b - a);
 
-  const uint32_t wbase = smem_base + warp * K::kWarpBytes;
+  const uint32_t wbase = smem_base + ring * K::kWarpBytes;
+  const bool leader = !kCoop || sg == 0;  // fills the ring
   auto sK = [&](int st) { return wbase + st * K::kTile; };
   auto sV = [&](int st) { return wbase + K::kOffV + st * K::kTile; };
   auto sKs = [&](int st) { return wbase + K::kOffScale + st * 2 * K::kScaleBytes; };
   auto sVs = [&](int st) { return sKs(st) + K::kScaleBytes; };
   auto bar = [&](int st) { return wbase + K::kOffBar + st * 8; };
+  auto empty_bar = [&](int st) { return wbase + K::kOffBar + (kStages + st) * 8; };
 
   if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(bar(st), 1);
-    fence_mbar_init();
-    tma_prefetch_desc(&tmk);
-    tma_prefetch_desc(&tmv);
+    if constexpr (!kCoop) {
+      for (int st = 0; st < kStages; ++st) mbar_init(bar(st), 1);
+      fence_mbar_init();
+    }
+    if (leader) {
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+    }
   }
   __syncwarp();
 
@@ -943,11 +978,17 @@ __global__ void __launch_bounds__(kWarps * 32)
   cursor_locate(pc, a, s_prefix, B, Hkv);
   cc = pc;
 
-  // lane 0 issues the copies of the block at the producer cursor into stage st
+  // lane 0 of the leader issues the copies of the block at the producer cursor into
+  // stage st. The block's physical id was loaded one refill earlier (fetch_id right
+  // after the cursor moved), so no table read sits on the warp's critical path.
+  int pid = 0;
+  auto fetch_id = [&]() {
+    if (lane == 0 && leader && pc.s < B)
+      pid = __ldg(p.block_tables + size_t(pc.s) * p.MBS + p.skip + pc.j);
+  };
   auto issue = [&](int st) {
-    if (lane == 0) {
-      int phys = __ldg(p.block_tables + size_t(pc.s) * p.MBS + p.skip + pc.j);
-      phys = (phys < 0 || phys >= p.NB) ? 0 : phys;  // never copy outside the pool
+    if (lane == 0 && leader) {
+      const int phys = (pid < 0 || pid >= p.NB) ? 0 : pid;  // never copy outside the pool
       const int row = (phys * p.Hkv + pc.u) * BS;
       mbar_arrive_expect_tx(bar(st), K::kTxBytes);
 #pragma unroll
@@ -964,9 +1005,11 @@ __global__ void __launch_bounds__(kWarps * 32)
   };
 
   const int npro = min(kStages, nblk);
+  fetch_id();
   for (int i = 0; i < npro; ++i) {
     issue(i);
     cursor_next(pc, s_prefix, B, Hkv);
+    fetch_id();
   }
 
   Path path;
@@ -983,17 +1026,33 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (!ok) {
       if (lane == 0 && p.status) atomicOr(p.status, 0x4);
       // let the copies already in flight land before the warp leaves
-      const int issued = min(nblk, i + kStages);
-      for (int k2 = i + 1; k2 < issued; ++k2)
-        mbar_wait_bounded(bar(k2 % kStages), uint32_t(k2 / kStages) & 1u, p.timeout_ns);
+      if (leader) {
+        const int issued = min(nblk, i + kStages);
+        for (int k2 = i + 1; k2 < issued; ++k2)
+          mbar_wait_bounded(bar(k2 % kStages), uint32_t(k2 / kStages) & 1u, p.timeout_ns);
+      }
       return;
     }
     path.block(p, sK(st), sV(st), sKs(st), sVs(st), Lc - (p.skip + cc.j) * BS);
     __syncwarp();
     if (i + kStages < nblk) {
-      fence_proxy_async_smem();
+      fence_proxy_async_smem();  // this warp's reads of the stage before its refill
+      if constexpr (kCoop) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(st));
+        // the leader refills once every warp of the worker has released the stage
+        if (leader &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(empty_bar(st), par, p.timeout_ns))) {
+          if (lane == 0 && p.status) atomicOr(p.status, 0x4);
+          const int issued = min(nblk, i + kStages);
+          for (int k2 = i + 1; k2 < issued; ++k2)
+            mbar_wait_bounded(bar(k2 % kStages), uint32_t(k2 / kStages) & 1u, p.timeout_ns);
+          return;
+        }
+      }
       issue(st);
       cursor_next(pc, s_prefix, B, Hkv);
+      fetch_id();
     }
     const bool seg_end = (cc.j == cc.n - 1) || (i == nblk - 1);
     if (seg_end) {
@@ -1014,21 +1073,17 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-// Shared-memory bytes of one CTA for a batch of B sequences.
-template <bool Q8, int D, int BS, class Path, int kWarps, int kStages>
-constexpr int decode_smem_bytes_fixed() {
-  return kWarps * DecodeKernel<Q8, D, BS, Path, kWarps, kStages>::kWarpBytes + 1024;
-}
-
-template <bool Q8, int D, int BS, class Path, int kWarps, int kStages>
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false>
 DecodeKernelInfo make_decode_info(int mma, int simt_heads) {
   DecodeKernelInfo info;
-  info.fn = reinterpret_cast<const void*>(&paged_decode_kernel<Q8, D, BS, Path, kWarps, kStages>);
+  info.fn = reinterpret_cast<const void*>(
+      &paged_decode_kernel<Q8, D, BS, Path, kWarps, kStages, kCoop>);
   info.warps = kWarps;
   info.stages = kStages;
-  info.warp_smem = DecodeKernel<Q8, D, BS, Path, kWarps, kStages>::kWarpBytes;
+  info.warp_smem = DecodeKernel<Q8, D, BS, Path, kWarps, kStages, kCoop>::kWarpBytes;
   info.mma = mma;
   info.simt_heads = simt_heads;
+  info.coop = kCoop ? 1 : 0;
   return info;
 }
 

@@ -40,18 +40,31 @@ bool select_shape(int simt_heads, DecodeKernelInfo* info) {
       return false;
   }
 }
+// Multi-query decode: workers of nsg warps share a ring of at least two stages (16 KiB
+// or more in flight per worker). CTAs of 6 or 8 warps, whichever leaves fewer warps
+// idle for the given nsg (at most one for nsg up to 8); on a tie the 6-warp CTA, two
+// of which fit an SM (12 warps) where only one 8-warp CTA does.
 template <int D, int BS>
-DecodeKernelInfo multi_shape() {
-  return make_decode_info<false, D, BS, MmaPathBf16<D, BS, true>, Bf16Warps<D, BS, true>::kWarps,
-                          Bf16Shape<D, BS>::kStages>(1, 0);
+struct MultiShape {
+  static constexpr int kStage = Bf16Shape<D, BS>::kStage;
+  static constexpr int kStages = kStage >= 8192 ? 2 : 16384 / kStage;
+};
+template <int D, int BS>
+DecodeKernelInfo multi_shape(int nsg) {
+  using Path = MmaPathBf16<D, BS, true>;
+  constexpr int kS = MultiShape<D, BS>::kStages;
+  const int idle6 = nsg <= 6 ? 6 % nsg : 6, idle8 = 8 % nsg;
+  if (idle6 <= idle8) return make_decode_info<false, D, BS, Path, 6, kS, true>(1, 0);
+  return make_decode_info<false, D, BS, Path, 8, kS, true>(1, 0);
 }
 }  // namespace
 
-bool select_decode_bf16_multi(int D, int BS, DecodeKernelInfo* info) {
-  if (D == 128 && BS == 16) *info = multi_shape<128, 16>();
-  else if (D == 128 && BS == 32) *info = multi_shape<128, 32>();
-  else if (D == 64 && BS == 16) *info = multi_shape<64, 16>();
-  else if (D == 64 && BS == 32) *info = multi_shape<64, 32>();
+bool select_decode_bf16_multi(int D, int BS, int nsg, DecodeKernelInfo* info) {
+  if (nsg < 1 || nsg > 8) return false;
+  if (D == 128 && BS == 16) *info = multi_shape<128, 16>(nsg);
+  else if (D == 128 && BS == 32) *info = multi_shape<128, 32>(nsg);
+  else if (D == 64 && BS == 16) *info = multi_shape<64, 16>(nsg);
+  else if (D == 64 && BS == 32) *info = multi_shape<64, 32>(nsg);
   else return false;
   return true;
 }

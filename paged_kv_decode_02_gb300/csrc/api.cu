@@ -16,6 +16,7 @@ namespace {
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per shared-memory copy wait
 constexpr int kMaxQueryLen = PKV_MAX_QUERY_LEN;
+constexpr int kTcMinRows = 64;  // multi-query rows per KV head from which tcgen05 wins
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -187,7 +188,20 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
   bool found = false;
   if (q_len > 1) {
     if (kvt != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
-    found = select_decode_bf16_multi(d->head_dim, d->block_size, P.nsg, &P.k);
+    // KV heads with 64..128 query rows go through the tcgen05 kernel, fewer rows through
+    // the mma.sync path: measured on GB300 with the spec-70b lengths, tcgen05 vs mma.sync
+    // per call: 16 rows 173.7 vs 93.8 us, 48 rows 183.9 vs 150.6, 64 rows 55.7 vs 73.0,
+    // 128 rows 204.3 vs 491.5 (an M = 128 MMA wastes what a small head leaves empty)
+    if (rows >= kTcMinRows && rows <= 128 &&
+        select_decode_tc(d->head_dim, d->block_size, &P.k)) {
+      // every row of a KV head in one tcgen05 MMA: one work unit per KV head
+      P.nsg = 1;
+      P.gs = rows;
+      P.HU = d->num_kv_heads;
+      found = true;
+    } else {
+      found = select_decode_bf16_multi(d->head_dim, d->block_size, P.nsg, &P.k);
+    }
   } else {
     switch (kvt) {
       case PKV_KV_BF16: found = select_decode_bf16(d->head_dim, d->block_size, simt, &P.k); break;
@@ -202,9 +216,12 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
     }
   }
   if (!found) return PKV_ERR_UNSUPPORTED;
-  // shared-memory rings per CTA: one per warp, or one per worker of nsg warps
+  // shared-memory rings per CTA: one per warp, or one per worker of nsg warps; the
+  // tcgen05 kernel: its fixed layout plus the tile prefix and lengths of the batch
   const int rings = P.k.coop ? P.k.warps / P.nsg : P.k.warps;
-  P.smem = size_t(rings) * P.k.warp_smem + 1024 + align_up(size_t(d->num_seqs + 1) * 4, 16);
+  P.smem = P.k.tc ? size_t(P.k.warp_smem) + size_t(8) * (d->num_seqs + 1)
+                  : size_t(rings) * P.k.warp_smem + 1024 +
+                        align_up(size_t(d->num_seqs + 1) * 4, 16);
 
   int dev = 0, sms = 0, per_sm = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -224,9 +241,11 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
           cudaSuccess ||
       per_sm <= 0)
     return PKV_ERR_CUDA;
+  if (P.k.tc) per_sm = 1;  // 512 TMEM columns per CTA: one CTA per SM
   P.grid = sms * per_sm;
-  // decode warps that own partial slots (warps left idle by a cooperative CTA own none)
-  P.W = P.k.coop ? P.grid * rings * P.nsg : P.grid * P.k.warps;
+  // owners of partial slots: decode warps (warps left idle by a cooperative CTA own
+  // none), or the CTAs of the tcgen05 kernel
+  P.W = P.k.tc ? P.grid : (P.k.coop ? P.grid * rings * P.nsg : P.grid * P.k.warps);
 
   // workspace: [prefix (B+1) int32][partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
   P.off_prefix = 0;

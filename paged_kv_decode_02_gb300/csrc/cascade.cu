@@ -68,29 +68,6 @@ struct PrefixTc {
   static_assert(kMaxIds % kBlocks == 0, "split cap in whole tiles");
 };
 
-// Bounded wait that also gives up once another thread of the CTA has given up.
-__device__ __forceinline__ bool prefix_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                            volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 template <int D, int BS>
 __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
     paged_prefix_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -155,7 +132,7 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
       const int c = tid + it * K::kThreads;
       const int r = c / kChunks, cc = c % kChunks;
       if (c < K::kM * kChunks)
-        sts128(base + K::kOffQ + (cc >> 3) * K::kQSlab + r * 128 + (((cc & 7) ^ (r & 7)) << 4),
+        tc::sts128(base + K::kOffQ + (cc >> 3) * K::kQSlab + r * 128 + (((cc & 7) ^ (r & 7)) << 4),
                v[it]);
     }
   }
@@ -178,7 +155,7 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
       const int st = j & 1;
       const uint32_t fb = is_k ? kfull(st) : vfull(st);
       if (j >= 2 &&
-          !__all_sync(0xffffffffu, prefix_wait(is_k ? kempty(st) : vempty(st),
+          !__all_sync(0xffffffffu, tc::wait_or_abort(is_k ? kempty(st) : vempty(st),
                                                uint32_t((j >> 1) - 1) & 1u, pp.timeout_ns,
                                                abort_flag)))
         break;
@@ -212,7 +189,7 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
       constexpr uint32_t kIdO = tc::idesc_bf16<128, D, true>();
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!prefix_wait(kfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag))
+        if (!tc::wait_or_abort(kfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag))
           return false;
         tc::fence_after_sync();
         const uint32_t kb = base + K::kOffK + st * K::kTile;
@@ -229,8 +206,8 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
       };
       auto issue_pv = [&](int j) -> bool {
         const int st = j & 1;
-        if (!prefix_wait(vfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag) ||
-            !prefix_wait(pfull, uint32_t(j) & 1u, pp.timeout_ns, abort_flag))
+        if (!tc::wait_or_abort(vfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag) ||
+            !tc::wait_or_abort(pfull, uint32_t(j) & 1u, pp.timeout_ns, abort_flag))
           return false;
         tc::fence_after_sync();
         const uint32_t vb = base + K::kOffV + st * K::kTile;
@@ -268,7 +245,7 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
       if (!__all_sync(0xffffffffu,
-                      prefix_wait(sfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag))) {
+                      tc::wait_or_abort(sfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag))) {
         ok = false;
         break;
       }
@@ -326,7 +303,7 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
       }
       l += (sm[0] + sm[1]) + (sm[2] + sm[3]);
       // P.V of the previous tile must be complete before P is overwritten or O rescaled
-      if (j > 0 && !__all_sync(0xffffffffu, prefix_wait(ofull, uint32_t(j - 1) & 1u,
+      if (j > 0 && !__all_sync(0xffffffffu, tc::wait_or_abort(ofull, uint32_t(j - 1) & 1u,
                                                         pp.timeout_ns, abort_flag))) {
         ok = false;
         break;
@@ -354,7 +331,7 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
       mbar_arrive(pfull);
     }
     if (ok && ntiles > 0 &&
-        !__all_sync(0xffffffffu, prefix_wait(ofull, uint32_t(ntiles - 1) & 1u, pp.timeout_ns,
+        !__all_sync(0xffffffffu, tc::wait_or_abort(ofull, uint32_t(ntiles - 1) & 1u, pp.timeout_ns,
                                              abort_flag)))
       ok = false;
     tc::fence_after_sync();

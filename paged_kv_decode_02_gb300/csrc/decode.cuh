@@ -1075,7 +1075,7 @@ __global__ void __launch_bounds__(kWarps * 32)
 
 template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false>
 DecodeKernelInfo make_decode_info(int mma, int simt_heads) {
-  DecodeKernelInfo info;
+  DecodeKernelInfo info{};
   info.fn = reinterpret_cast<const void*>(
       &paged_decode_kernel<Q8, D, BS, Path, kWarps, kStages, kCoop>);
   info.warps = kWarps;
@@ -1084,6 +1084,7 @@ DecodeKernelInfo make_decode_info(int mma, int simt_heads) {
   info.mma = mma;
   info.simt_heads = simt_heads;
   info.coop = kCoop ? 1 : 0;
+  info.tc = 0;
   return info;
 }
 

@@ -57,14 +57,23 @@ DecodeKernelInfo multi_shape(int nsg) {
   if (idle6 <= idle8) return make_decode_info<false, D, BS, Path, 6, kS, true>(1, 0);
   return make_decode_info<false, D, BS, Path, 8, kS, true>(1, 0);
 }
+
+// More than 8 row subgroups (over 128 rows per KV head): workers span CTAs, each warp
+// with its own ring (4 warps per CTA, one stage).
+template <int D, int BS>
+DecodeKernelInfo multi_shape_wide() {
+  return make_decode_info<false, D, BS, MmaPathBf16<D, BS, true>, Bf16Warps<D, BS, true>::kWarps,
+                          Bf16Shape<D, BS>::kStages>(1, 0);
+}
 }  // namespace
 
 bool select_decode_bf16_multi(int D, int BS, int nsg, DecodeKernelInfo* info) {
-  if (nsg < 1 || nsg > 8) return false;
-  if (D == 128 && BS == 16) *info = multi_shape<128, 16>(nsg);
-  else if (D == 128 && BS == 32) *info = multi_shape<128, 32>(nsg);
-  else if (D == 64 && BS == 16) *info = multi_shape<64, 16>(nsg);
-  else if (D == 64 && BS == 32) *info = multi_shape<64, 32>(nsg);
+  if (nsg < 1) return false;
+  const bool wide = nsg > 8;
+  if (D == 128 && BS == 16) *info = wide ? multi_shape_wide<128, 16>() : multi_shape<128, 16>(nsg);
+  else if (D == 128 && BS == 32) *info = wide ? multi_shape_wide<128, 32>() : multi_shape<128, 32>(nsg);
+  else if (D == 64 && BS == 16) *info = wide ? multi_shape_wide<64, 16>() : multi_shape<64, 16>(nsg);
+  else if (D == 64 && BS == 32) *info = wide ? multi_shape_wide<64, 32>() : multi_shape<64, 32>(nsg);
   else return false;
   return true;
 }

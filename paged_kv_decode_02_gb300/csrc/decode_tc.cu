@@ -1,0 +1,598 @@
+// decode_tc.cu -- paged decode attention on the fifth-generation tensor cores.
+//
+// What is computed is the decode attention of decode.cuh: for every sequence s, KV
+// head h and query row r of that head (q_len new tokens x g query heads; new token i
+// sees the first L - q_len + 1 + i cached tokens, the causal rule of speculative
+// verification in "推测解码" of "大模型工程（五）：推理优化核心技法", chenk.top),
+//   out[r] = softmax(scale * K q_r) V
+// over the tokens reached through the block table ("分页注意力", same page).
+//
+// All q_len * g rows of a KV head (at most 128) go through one M = 128 tcgen05 MMA, so
+// a KV block is multiplied once for every row of its head instead of once per 16-row
+// subgroup. Work: the flat order (sequence, KV head, tile of 128 tokens) is cut into
+// one contiguous range per CTA (one CTA per SM). Within a range the tiles of one KV
+// head form a segment; a segment covering the whole head writes the output, a cut
+// one (only a range's first and last can be) leaves an unnormalised (o, m, l) record
+// per row in the slots the split-KV merge kernel reads (slot 2c for the first segment
+// of CTA c, 2c + 1 for the last).
+// Roles per CTA (224 threads), as in the cascade prefix kernel:
+//   warp 0 / warp 6: TMA copies of the K / V tiles into two-stage rings (one box per
+//                    16- or 32-token block and 64-column slab, lane b copies block b;
+//                    block ids are read one tile ahead);
+//   warp 1:          TMEM allocation; one thread issues every MMA:
+//                    S_t = Q K_t^T (fp32, two TMEM buffers), O += P_t V_t (A = P in TMEM);
+//   warps 2..5:      one query row per thread: Q rows of each segment into shared
+//                    memory, softmax with the causal and context masks, P to TMEM,
+//                    the segment's epilogue from O in TMEM.
+// The softmax keeps a reference maximum per row that moves only when a tile's maximum
+// exceeds it by more than 8 (log2 units); O is then rescaled in TMEM before the next
+// P.V. Every wait is bounded: on a timeout the CTA sets a status bit, lets its copies
+// and MMAs complete, frees its TMEM and leaves.
+#include "decode.cuh"
+#include "tcgen05.cuh"
+
+namespace pkv {
+
+// 16-byte asynchronous copy global -> shared (zero fill when src_bytes is 0); the
+// copies of a thread complete at cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+template <int D, int BS>
+struct TcDecode {
+  static constexpr int kM = 128;               // query rows per MMA (rows of a KV head, padded)
+  static constexpr int kN = 128;               // tokens per tile
+  static constexpr int kBlocks = kN / BS;      // blocks per tile
+  static constexpr int kSlabs = D / 64;        // 128-byte column slabs of a row
+  static constexpr int kSlab = kN * 128;       // one slab of a tile (== kM * 128)
+  static constexpr int kTile = kSlabs * kSlab; // a Q, K or V tile
+  static constexpr int kOffQ = 0;              // Q x2 (segment parity)
+  static constexpr int kOffK = kOffQ + 2 * kTile;
+  static constexpr int kOffV = kOffK + 2 * kTile;
+  static constexpr int kOffBar = kOffV + 2 * kTile;
+  // mbarriers: kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] pfull ofull mdone qfull[2] ofree
+  static constexpr int kNumBars = 16;
+  static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kOffTables = kOffAbort + 12;  // [B+1] tile prefix, [B] clamped lengths
+  static constexpr int kFixedSmem = kOffTables + 1024;  // + 8 * (B + 1) at run time
+  static constexpr int kThreads = 224;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kColS = 0, kColO = 2 * kN, kColP = 2 * kN + 128;
+  static_assert(kColP + kN / 2 <= int(kTmemCols) && kColO + D <= kColP, "TMEM columns");
+  static_assert(kN % BS == 0 && D % 64 == 0 && kSlab == kM * 128, "tile shape");
+  static_assert(kOffTables % 16 == 0, "table alignment");
+};
+
+// Position in the flat (sequence, KV head, tile) order.
+struct TileCursor {
+  int s, h, j, n;  // sequence, KV head, tile of the head, tiles of the sequence
+};
+
+__device__ __forceinline__ void tile_locate(TileCursor& c, long long f, const int* prefix, int B,
+                                            int Hkv) {
+  int lo = 0, hi = B;  // Hkv*prefix[lo] <= f < Hkv*prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((long long)Hkv * prefix[mid] <= f) lo = mid; else hi = mid;
+  }
+  c.s = lo;
+  c.n = prefix[lo + 1] - prefix[lo];
+  const long long rem = f - (long long)Hkv * prefix[lo];
+  c.h = int(rem / c.n);
+  c.j = int(rem % c.n);
+}
+
+__device__ __forceinline__ void tile_next(TileCursor& c, const int* prefix, int B, int Hkv) {
+  if (++c.j < c.n) return;
+  c.j = 0;
+  if (++c.h < Hkv) return;
+  c.h = 0;
+  do { ++c.s; } while (c.s < B && prefix[c.s + 1] == prefix[c.s]);
+  c.n = c.s < B ? prefix[c.s + 1] - prefix[c.s] : 0;
+}
+
+template <int D, int BS>
+__global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
+    paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                           const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+  using K = TcDecode<D, BS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + K::kOffAbort);
+  int* s_prefix = reinterpret_cast<int*>(gbase + K::kOffTables);
+  const int B = p.B, Hkv = p.Hkv;
+  int* s_len = s_prefix + (B + 1);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto bar = [&](int i) { return base + K::kOffBar + 8 * i; };
+  auto kfull = [&](int st) { return bar(st); };
+  auto kempty = [&](int st) { return bar(2 + st); };
+  auto vfull = [&](int st) { return bar(4 + st); };
+  auto vempty = [&](int st) { return bar(6 + st); };
+  auto sfull = [&](int st) { return bar(8 + st); };
+  const uint32_t pfull = bar(10), ofull = bar(11), mdone = bar(12), ofree = bar(15);
+  auto qfull = [&](int b) { return bar(13 + b); };
+  const uint32_t tmem_slot = base + K::kOffTmemSlot;
+
+  pdl_wait_prior_grid();
+  if (tid == 0) {
+    for (int i = 0; i < 10; ++i) mbar_init(bar(i), 1);
+    mbar_init(pfull, 4 * 32);
+    mbar_init(ofull, 1);
+    mbar_init(mdone, 1);
+    mbar_init(qfull(0), 4 * 32);
+    mbar_init(qfull(1), 4 * 32);
+    mbar_init(ofree, 4 * 32);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, K::kTmemCols);
+
+  // ---- tiles per sequence, their exclusive prefix, clamped lengths (every CTA) ----
+  {
+    const int per = (B + K::kThreads - 1) / K::kThreads;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int sum = 0;
+    for (int i = b0; i < b1; ++i) {
+      const int L = min(max(__ldg(p.context_lens + i), 0), p.MBS * BS);
+      s_len[i] = L;
+      sum += (L + K::kN - 1) / K::kN;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    __shared__ int warp_tot[K::kThreads / 32];
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int run = incl - sum;
+    for (int w2 = 0; w2 < warp; ++w2) run += warp_tot[w2];
+    for (int i = b0; i < b1; ++i) {
+      run += (s_len[i] + K::kN - 1) / K::kN;
+      s_prefix[i + 1] = run;
+    }
+    if (tid == 0) s_prefix[0] = 0;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= B; i += K::kThreads) p.prefix_out[i] = s_prefix[i];
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + K::kOffTmemSlot);
+
+  // this CTA's range of the flat (sequence, KV head, tile) order
+  const long long T = (long long)Hkv * s_prefix[B];
+  const int C = gridDim.x, c = blockIdx.x;
+  const long long ra = T * c / C, rb = T * (c + 1) / C;
+  const int cnt = int(rb - ra);
+  const int R = p.gs;  // query rows per KV head (q_len * g)
+
+  if (cnt > 0 && (warp == 0 || warp == 6)) {
+    // ---------------- TMA producers: warp 0 streams K, warp 6 streams V ----------------
+    const bool is_k = warp == 0;
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    const uint32_t region = base + (is_k ? K::kOffK : K::kOffV);
+    const int rows_total = p.NB * Hkv * BS;  // a box at this row is all zero fill
+    TileCursor cur;
+    tile_locate(cur, ra, s_prefix, B, Hkv);
+    // lane b: physical block of block b of the tile at the cursor (rows_total: none)
+    auto block_row = [&](const TileCursor& t) -> int {
+      const int blk = t.j * K::kBlocks + lane;
+      if (lane >= K::kBlocks || t.s >= B || blk * BS >= s_len[t.s]) return rows_total;
+      int phys = __ldg(p.block_tables + size_t(t.s) * p.MBS + blk);
+      phys = (phys < 0 || phys >= p.NB) ? 0 : phys;  // never copy outside the pool
+      return (phys * Hkv + t.h) * BS;
+    };
+    int row = block_row(cur);
+    int issued = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const int st = i & 1;
+      const uint32_t fb = is_k ? kfull(st) : vfull(st);
+      if (i >= 2 &&
+          !__all_sync(0xffffffffu, tc::wait_or_abort(is_k ? kempty(st) : vempty(st),
+                                                     uint32_t((i >> 1) - 1) & 1u, p.timeout_ns,
+                                                     abort_flag)))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(fb, K::kTile);
+      __syncwarp();
+      if (lane < K::kBlocks) {
+        const uint32_t dst = region + st * K::kTile + lane * BS * 128;
+#pragma unroll
+        for (int sl = 0; sl < K::kSlabs; ++sl)
+          tma_load_2d(dst + sl * K::kSlab, map, fb, sl * 64, row);
+      }
+      issued = i + 1;
+      tile_next(cur, s_prefix, B, Hkv);
+      if (i + 1 < cnt) row = block_row(cur);  // next tile's ids, a tile ahead
+    }
+    if (lane == 0)  // every copy issued must have landed before the CTA may exit
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        mbar_wait_bounded(is_k ? kfull(j & 1) : vfull(j & 1), uint32_t(j >> 1) & 1u,
+                          p.timeout_ns);
+    __syncwarp();
+  } else if (cnt > 0 && warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t kIdS = tc::idesc_bf16<128, K::kN, false>();
+      constexpr uint32_t kIdO = tc::idesc_bf16<128, D, true>();
+      auto issue_s = [&](int i, int qb) -> bool {
+        const int st = i & 1;
+        if (!tc::wait_or_abort(kfull(st), uint32_t(i >> 1) & 1u, p.timeout_ns, abort_flag))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t qa = base + K::kOffQ + qb * K::kTile;
+        const uint32_t kb = base + K::kOffK + st * K::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * K::kSlab + (kk & 3) * 32;
+          tc::mma_bf16(tmem + K::kColS + st * K::kN, tc::sdesc_sw128(qa + koff, 16, 1024),
+                       tc::sdesc_sw128(kb + koff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        }
+        tc::commit(sfull(st));
+        tc::commit(kempty(st));
+        return true;
+      };
+      // P.V of tile i; the first P.V of segment seg overwrites O, once the previous
+      // segment's epilogue has read it
+      auto issue_pv = [&](int i, bool seg_first, int sgi) -> bool {
+        const int st = i & 1;
+        if (seg_first && sgi > 0 &&
+            !tc::wait_or_abort(ofree, uint32_t(sgi - 1) & 1u, p.timeout_ns, abort_flag))
+          return false;
+        if (!tc::wait_or_abort(vfull(st), uint32_t(i >> 1) & 1u, p.timeout_ns, abort_flag) ||
+            !tc::wait_or_abort(pfull, uint32_t(i) & 1u, p.timeout_ns, abort_flag))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t vb = base + K::kOffV + st * K::kTile;
+#pragma unroll
+        for (int kk = 0; kk < K::kN / 16; ++kk)
+          tc::mma_bf16_tmem_a(tmem + K::kColO, tmem + K::kColP + kk * 8,
+                              tc::sdesc_sw128(vb + kk * 16 * 128, K::kSlab, 1024), kIdO,
+                              (!seg_first || kk > 0) ? 1u : 0u);
+        tc::commit(vempty(st));
+        tc::commit(ofull);
+        return true;
+      };
+      TileCursor cur;
+      tile_locate(cur, ra, s_prefix, B, Hkv);
+      bool ok = true;
+      int seg = -1, pend = -1, pend_seg = 0;
+      bool pend_first = false;
+      for (int i = 0; i < cnt && ok; ++i) {
+        const bool first = i == 0 || cur.j == 0;
+        if (first) {
+          // a segment's last P.V goes before the next segment's scores: the softmax
+          // warps read O and load the next Q in between
+          if (pend >= 0) ok = issue_pv(pend, pend_first, pend_seg);
+          pend = -1;
+          ++seg;
+          if (ok) ok = tc::wait_or_abort(qfull(seg & 1), uint32_t(seg >> 1) & 1u, p.timeout_ns,
+                                         abort_flag);
+        }
+        if (ok) ok = issue_s(i, seg & 1);
+        if (ok && pend >= 0) ok = issue_pv(pend, pend_first, pend_seg);
+        pend = i;
+        pend_first = first;
+        pend_seg = seg;
+        tile_next(cur, s_prefix, B, Hkv);
+      }
+      if (ok && pend >= 0) issue_pv(pend, pend_first, pend_seg);
+      tc::commit(mdone);  // every MMA issued must have completed before TMEM is freed
+      mbar_wait_bounded(mdone, 0u, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (cnt > 0 && warp >= 2 && warp <= 5) {
+    // ---------------- softmax warps: one query row per thread ----------------
+    const int quarter = warp & 3;  // warps 2, 3, 4, 5 own TMEM lanes 64.., 96.., 0.., 32..
+    const int r = quarter * 32 + lane;
+    const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
+    const float sl = p.scale_log2, asl = fabsf(sl);
+    const bool row_ok = r < R;
+    // causal: new token i = r / g hides the last q_len - 1 - i positions of its head
+    const int hide = row_ok ? p.q_len - 1 - r / p.g : 0;
+    TileCursor cur;
+    tile_locate(cur, ra, s_prefix, B, Hkv);
+    // Q rows of the KV head at cursor t -> Q buffer qb (K-major, 128-byte swizzle), as
+    // asynchronous copies (padding rows zero-filled); q_ready completes and publishes them
+    auto prefetch_q = [&](const TileCursor& t, int qb) {
+      constexpr int kChunks = D / 8;
+      const uint4* q = reinterpret_cast<const uint4*>(p.q);
+      const size_t qrow = (size_t(t.s) * p.q_len + (row_ok ? r / p.g : 0)) * p.Hq + t.h * p.g +
+                          (row_ok ? r % p.g : 0);
+      const uint32_t qa = base + K::kOffQ + qb * K::kTile;
+#pragma unroll
+      for (int cc = 0; cc < kChunks; ++cc)
+        cp_async16(qa + (cc >> 3) * K::kSlab + r * 128 + (((cc & 7) ^ (r & 7)) << 4),
+                   q + qrow * kChunks + cc, row_ok ? 16u : 0u);
+      cp_async_commit();
+    };
+    auto q_ready = [&](int qb) {
+      cp_async_wait_all();
+      fence_proxy_async_smem();  // generic-proxy writes before the MMAs read them
+      mbar_arrive(qfull(qb));
+    };
+    // a warp whose 32 rows are all padding computes nothing: its P and O rows feed
+    // output rows that are never stored
+    const bool warp_idle = quarter * 32 >= R;
+    // rows of a head's last block past its context may hold anything (even NaN): the
+    // four softmax warps zero them in the V tile before P.V reads it (weights there are 0)
+    auto zero_v_tail = [&](int i, int L, int t0) -> bool {
+      const int zr0 = L - t0, zr1 = min(K::kN, ((L + BS - 1) / BS) * BS - t0);
+      if (zr0 >= zr1) return true;
+      if (!__all_sync(0xffffffffu, tc::wait_or_abort(vfull(i & 1), uint32_t(i >> 1) & 1u,
+                                                     p.timeout_ns, abort_flag)))
+        return false;
+      const uint32_t vb = base + K::kOffV + (i & 1) * K::kTile;
+      for (int idx = tid - 64; idx < (zr1 - zr0) * (D / 8); idx += 128) {
+        const int rr = zr0 + idx / (D / 8), cc = idx % (D / 8);
+        tc::sts128(vb + (cc >> 3) * K::kSlab + rr * 128 + (((cc & 7) ^ (rr & 7)) << 4),
+                   make_uint4(0u, 0u, 0u, 0u));
+      }
+      fence_proxy_async_smem();
+      return true;
+    };
+    float m_ref = -INFINITY, l = 0.f;
+    int seg = 0, seg_j0 = cur.j, seg_tile = 0;
+    bool ok = true;
+    prefetch_q(cur, 0);
+    q_ready(0);
+    for (int i = 0; i < cnt; ++i) {
+      const int st = i & 1;
+      const bool first = i == 0 || cur.j == 0;
+      const bool last = i == cnt - 1 || cur.j == cur.n - 1;
+      if (first && i > 0) {  // this Q was published before the previous epilogue
+        seg_j0 = cur.j;
+        seg_tile = 0;
+      }
+      if (last && i + 1 < cnt) {  // the next KV head's Q rows, while this tile runs
+        TileCursor nx = cur;
+        tile_next(nx, s_prefix, B, Hkv);
+        prefetch_q(nx, (seg + 1) & 1);
+      }
+      const int L = s_len[cur.s];
+      const int t0 = cur.j * K::kN;  // first token of the tile
+      if (!__all_sync(0xffffffffu, tc::wait_or_abort(sfull(st), uint32_t(i >> 1) & 1u,
+                                                     p.timeout_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      // columns this row may see in the tile (context end, causal limit); padding rows
+      // take the warp's largest count so that the warp runs one path
+      const int vis_row = row_ok ? min(K::kN, L - hide - t0) : -1;
+      const int vis_w = __reduce_max_sync(0xffffffffu, vis_row);
+      const int vis = row_ok ? vis_row : vis_w;
+      if (warp_idle) {  // no row of this warp is stored: only keep the barriers going
+        if (!zero_v_tail(i, L, t0)) {
+          ok = false;
+          break;
+        }
+        if (i > 0 && !__all_sync(0xffffffffu, tc::wait_or_abort(ofull, uint32_t(i - 1) & 1u,
+                                                                p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        mbar_arrive(pfull);
+        ++seg_tile;
+        if (last) {
+          if (i + 1 < cnt) q_ready((seg + 1) & 1);
+          if (!__all_sync(0xffffffffu, tc::wait_or_abort(ofull, uint32_t(i) & 1u,
+                                                         p.timeout_ns, abort_flag))) {
+            ok = false;
+            break;
+          }
+          mbar_arrive(ofree);
+          ++seg;
+        }
+        tile_next(cur, s_prefix, B, Hkv);
+        continue;
+      }
+      uint32_t s[K::kN];
+      tc::tmem_ld128(trow + K::kColS + st * K::kN, s);
+      if (sl < 0.f) {  // a negative scale is carried by the scores' signs
+#pragma unroll
+        for (int t = 0; t < K::kN; ++t) s[t] ^= 0x80000000u;
+      }
+      // warp-uniform: every row sees the whole tile (all tiles but a head's last, and
+      // the last ones of causal rows), else columns past each row's limit are masked
+      const bool full = __all_sync(0xffffffffu, vis >= K::kN);
+      if (!full) {
+#pragma unroll
+        for (int t = 0; t < K::kN; ++t)
+          if (t >= vis) s[t] = 0xff800000u;  // -inf
+      }
+      float mx[8];
+#pragma unroll
+      for (int t = 0; t < K::kN; ++t)
+        mx[t & 7] = (t < 8) ? __uint_as_float(s[t]) : fmaxf(mx[t & 7], __uint_as_float(s[t]));
+      const float mt = asl * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float alpha = 1.f;
+      bool rescale = false;
+      if (vis > 0 && mt > m_ref + 8.f) {
+        alpha = fast_exp2(m_ref - mt);  // 0 while the row has seen nothing
+        m_ref = mt;
+        l *= alpha;
+        rescale = seg_tile > 0;
+      }
+      uint32_t pk[K::kN / 2];
+      float sm[4] = {0.f, 0.f, 0.f, 0.f};
+      const float nm = -m_ref;
+      if (full) {
+#pragma unroll
+        for (int t = 0; t < K::kN; t += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(s[t]), asl, nm));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(s[t + 1]), asl, nm));
+          sm[(t >> 1) & 3] += p0 + p1;
+          pk[t / 2] = pack_bf16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < K::kN; t += 2) {
+          const float p0 = t < vis ? fast_exp2(fmaf(__uint_as_float(s[t]), asl, nm)) : 0.f;
+          const float p1 =
+              t + 1 < vis ? fast_exp2(fmaf(__uint_as_float(s[t + 1]), asl, nm)) : 0.f;
+          sm[(t >> 1) & 3] += p0 + p1;
+          pk[t / 2] = pack_bf16x2(p0, p1);
+        }
+      }
+      l += (sm[0] + sm[1]) + (sm[2] + sm[3]);
+      if (!zero_v_tail(i, L, t0)) {
+        ok = false;
+        break;
+      }
+      // P.V of the previous tile must be complete before P is overwritten or O rescaled
+      if (i > 0 && !__all_sync(0xffffffffu, tc::wait_or_abort(ofull, uint32_t(i - 1) & 1u,
+                                                              p.timeout_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int c2 = 0; c2 < D; c2 += 32) {
+          uint32_t o[32];
+          tc::tmem_ld32(trow + K::kColO + c2, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::tmem_st32(trow + K::kColO + c2, o);
+        }
+      }
+#pragma unroll
+      for (int c2 = 0; c2 < K::kN / 2; c2 += 32) {
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) w[e] = pk[c2 + e];
+        tc::tmem_st32(trow + K::kColP + c2, w);
+      }
+      tc::fence_before_sync();
+      mbar_arrive(pfull);
+      ++seg_tile;
+      if (last) {
+        // the next KV head's Q (prefetched during this tile) goes to the MMA thread
+        // first, so its scores are computed while this epilogue runs
+        if (i + 1 < cnt) q_ready((seg + 1) & 1);
+        // ---- segment epilogue: the output (whole head) or a partial record ----
+        if (!__all_sync(0xffffffffu, tc::wait_or_abort(ofull, uint32_t(i) & 1u, p.timeout_ns,
+                                                       abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const bool whole = seg_j0 == 0 && cur.j == cur.n - 1;
+        const size_t slot = size_t(2 * c + (seg == 0 ? 0 : 1));
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (whole) {
+          // the bf16 rows go through this segment's Q buffer (its MMAs are complete),
+          // each row in its own Q row's slots (16-byte chunk k in slab k / 8, position
+          // (k % 8) ^ (row % 8)): no other warp writes there, not even a faster warp
+          // already prefetching the next Q rows; then 16 lanes store one contiguous
+          // 2*D-byte output row
+          constexpr int kCh = D / 8;  // 16-byte chunks of an output row
+          const uint32_t qbuf = base + K::kOffQ + (seg & 1) * K::kTile;
+          auto slot_addr = [&](int row, int ch) {
+            return qbuf + (ch >> 3) * K::kSlab + row * 128 + (((ch & 7) ^ (row & 7)) << 4);
+          };
+          fence_proxy_async_smem();  // the MMAs' reads of the buffer before these writes
+#pragma unroll
+          for (int c2 = 0; c2 < D; c2 += 32) {
+            uint32_t o[32];
+            tc::tmem_ld32(trow + K::kColO + c2, o);
+#pragma unroll
+            for (int e = 0; e < 32; e += 8)
+              tc::sts128(slot_addr(r, (c2 + e) / 8),
+                         make_uint4(pack_bf16x2(__uint_as_float(o[e]) * inv,
+                                                __uint_as_float(o[e + 1]) * inv),
+                                    pack_bf16x2(__uint_as_float(o[e + 2]) * inv,
+                                                __uint_as_float(o[e + 3]) * inv),
+                                    pack_bf16x2(__uint_as_float(o[e + 4]) * inv,
+                                                __uint_as_float(o[e + 5]) * inv),
+                                    pack_bf16x2(__uint_as_float(o[e + 6]) * inv,
+                                                __uint_as_float(o[e + 7]) * inv)));
+          }
+          __syncwarp();
+          // lane l's own output row, handed to the lanes that store it
+          const long long my_row =
+              (long long)((size_t(cur.s) * p.q_len + (row_ok ? r / p.g : 0)) * p.Hq +
+                          cur.h * p.g + (row_ok ? r % p.g : 0));
+          const int nrows = min(32, R - quarter * 32);
+#pragma unroll 4
+          for (int k2 = 0; k2 < kCh; ++k2) {
+            const int idx = k2 * 32 + lane, rl = idx / kCh, ch = idx % kCh;
+            const long long orow2 = __shfl_sync(0xffffffffu, my_row, rl);
+            if (rl < nrows)
+              reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                       size_t(orow2) * D)[ch] = lds128(slot_addr(quarter * 32 + rl, ch));
+          }
+        } else {
+#pragma unroll
+          for (int c2 = 0; c2 < D; c2 += 32) {
+            uint32_t o[32];
+            tc::tmem_ld32(trow + K::kColO + c2, o);
+            if (!row_ok) continue;
+            float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * R + r) * D + c2);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              dst[e / 4] = make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                       __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+          }
+        }
+        if (row_ok && !whole)
+          reinterpret_cast<float2*>(p.part_ml)[slot * R + r] = make_float2(m_ref, l);
+        tc::fence_before_sync();
+        mbar_arrive(ofree);
+        ++seg;
+        m_ref = -INFINITY;
+        l = 0.f;
+      }
+      tile_next(cur, s_prefix, B, Hkv);
+    }
+    (void)ok;
+    tc::fence_before_sync();
+  }
+  __syncthreads();
+  if (*abort_flag && tid == 0 && p.status) atomicOr(p.status, 0x4);
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, K::kTmemCols);
+  }
+}
+
+template <int D, int BS>
+DecodeKernelInfo tc_info() {
+  DecodeKernelInfo info{};
+  info.fn = reinterpret_cast<const void*>(&paged_decode_tc_kernel<D, BS>);
+  info.warps = TcDecode<D, BS>::kThreads / 32;
+  info.stages = 2;
+  info.warp_smem = TcDecode<D, BS>::kFixedSmem;  // per CTA, plus 8 * (B + 1)
+  info.mma = 1;
+  info.simt_heads = 0;
+  info.coop = 0;
+  info.tc = 1;
+  return info;
+}
+
+bool select_decode_tc(int D, int BS, DecodeKernelInfo* info) {
+  if (D == 128 && BS == 16) *info = tc_info<128, 16>();
+  else if (D == 128 && BS == 32) *info = tc_info<128, 32>();
+  else if (D == 64 && BS == 16) *info = tc_info<64, 16>();
+  else if (D == 64 && BS == 32) *info = tc_info<64, 32>();
+  else return false;
+  return true;
+}
+
+}  // namespace pkv

@@ -123,6 +123,8 @@ struct DecodeKernelInfo {
   int mma;           // 1 = tensor-core path (groups >= 4), 0 = CUDA-core path
   int simt_heads;    // query heads per unit on the CUDA-core path
   int coop;          // 1: a worker is nsg warps sharing one ring (warp_smem per worker)
+  int tc;            // 1: the tcgen05 kernel (decode_tc.cu): one CTA per SM, all rows of a
+                     //    KV head per MMA, warp_smem = fixed shared memory per CTA
 };
 
 // Kernel tables, one per translation unit. Return false if the shape is not built.
@@ -130,6 +132,8 @@ bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info);
 // q_len > 1: the causal multi-query variant of the bf16 tensor-core path, with
 // workers of nsg warps sharing their shared-memory ring (CTA shape chosen for nsg)
 bool select_decode_bf16_multi(int D, int BS, int nsg, DecodeKernelInfo* info);
+// The tcgen05 decode kernel (bf16 caches, q_len * g <= 128 rows per KV head).
+bool select_decode_tc(int D, int BS, DecodeKernelInfo* info);
 // One-byte KV code formats.
 enum : int { CODE_I8 = 0, CODE_E4M3 = 1, CODE_E5M2 = 2 };
 

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 3) paged_decode_merge_kernel
   const int s = unit / p.HU, u = unit % p.HU;
   const int row = r0 + lane / Q, dq = lane % Q;
   const bool active = row < gs;
+  // work items (blocks, or 128-token tiles for the tcgen05 kernel) of the sequence
   const int n = p.prefix[s + 1] - p.prefix[s];
   // output row of unit row r: (s * q_len + i) * Hq + kvh * g + j for the unit's query
   // row R = (u % nsg) * gs + r = i * g + j (with q_len = 1: head kvh * g + R)
@@ -52,7 +53,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 3) paged_decode_merge_kernel
     int flags = 0;
     const int L = p.context_lens[s];
     if (lane == 0 && (L < 0 || L > p.MBS * p.BS || (L > 0 && L < p.q_len))) flags |= 0x1;
-    for (int j = lane; j < n; j += 32) {
+    const int nblk = L <= 0 ? 0 : min((L + p.BS - 1) / p.BS, p.MBS);
+    for (int j = lane; j < nblk; j += 32) {
       const int id = p.block_tables[size_t(s) * p.MBS + j];
       if (id < 0 || id >= p.NB) flags |= 0x2;
     }

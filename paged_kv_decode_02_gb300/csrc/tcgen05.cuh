@@ -14,6 +14,31 @@
 namespace pkv {
 namespace tc {
 
+// Bounded mbarrier wait for the warp-specialised tcgen05 kernels: gives up after
+// `limit_ns` (raising the CTA's abort flag) or as soon as another thread of the CTA
+// has raised it, so that one stuck role never leaves the others spinning.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // Whole warp: allocate `ncols` columns (a power of two, 32..512); the base address
 // is written to shared memory at `dst`. The permit is given back at once so that
 // other CTAs on the SM may allocate.

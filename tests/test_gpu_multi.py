@@ -48,6 +48,11 @@ SHAPES = [
     ("g8-q16-bs32", 16, 2, 128, 32, 16, [16, 17, 300, 1000]),
     ("g16-q2-d64", 32, 2, 64, 16, 2, [90, 17, 2]),
     ("g5-q5", 10, 2, 128, 32, 5, [100, 5, 37]),
+    # 64..128 rows per KV head take the tcgen05 kernel, more than 128 the wide mma.sync one
+    ("g16-q4-d64", 32, 2, 64, 16, 4, [4, 5, 129, 300, 0, 77]),
+    ("g8-q8-bs32", 16, 2, 128, 32, 8, [8, 9, 130, 600]),
+    ("g16-q8", 32, 2, 128, 16, 8, [8, 200, 1500, 127, 129]),
+    ("g16-q12-d64", 32, 2, 64, 16, 12, [12, 40, 150]),
 ]
 
 
@@ -92,6 +97,24 @@ def test_multi_full_size_after_append(pk):
     L = w.context_lens.cpu().numpy()
     triples = {(int(np.argmax(L)), 0, 0), (int(np.argmax(L)), w.q_len - 1, w.num_q_heads - 1),
                (int(np.argmin(L)), 0, 5)}
+    while len(triples) < 24:
+        triples.add((int(rng.integers(w.num_seqs)), int(rng.integers(w.q_len)),
+                     int(rng.integers(w.num_q_heads))))
+    triples = sorted(triples)
+    got = to_f64(out)
+    assert np.all(np.isfinite(got))
+    assert _err(out, oracle_outputs_multi(w, triples), triples) <= DECODE_ATOL
+
+
+def test_multi_full_size_128_rows(pk):
+    """spec-70b lengths with 16 new tokens per request: 128 query rows per KV head."""
+    w = make_workload("spec-70b", device=DEV, q_len=16)
+    out = _run(pk, w)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    L = w.context_lens.cpu().numpy()
+    triples = {(int(np.argmax(L)), 0, 0), (int(np.argmax(L)), 15, w.num_q_heads - 1),
+               (int(np.argmin(L)), 15, 7)}
     while len(triples) < 24:
         triples.add((int(rng.integers(w.num_seqs)), int(rng.integers(w.q_len)),
                      int(rng.integers(w.num_q_heads))))

@@ -51,6 +51,10 @@ WORKLOAD_TEXT = {
     "spec-70b": "speculative verification on the 70B-like GQA shape: batch 64, 64 q / 8 kv "
                 "heads, head_dim 128, block 16, context log-normal (median 1024, sigma 1) "
                 "clipped [128, 32768], q_len 6 new tokens per request (k = 5), causal",
+    "spec-70b-q16": "speculative verification on the 70B-like GQA shape with 15 drafted "
+                    "tokens: batch 64, 64 q / 8 kv heads, head_dim 128, block 16, context "
+                    "log-normal (median 1024, sigma 1) clipped [128, 32768], q_len 16 new "
+                    "tokens per request (128 query rows per KV head), causal",
 }
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0

@@ -211,6 +211,7 @@ SPECS = {
     "fp8-e5m2":  dict(B=128, Hq=32, Hkv=8,  D=128, bs=32, seed=4),
     "fp8-e4m3":  dict(B=128, Hq=32, Hkv=8,  D=128, bs=32, seed=4),
     "spec-70b":  dict(B=64,  Hq=64, Hkv=8,  D=128, bs=16, seed=2, q_len=6),
+    "spec-70b-q16": dict(B=64, Hq=64, Hkv=8, D=128, bs=16, seed=2, q_len=16),
 }
 
 FP8_KV = {"fp8_e4m3": (torch.float8_e4m3fn, 448.0), "fp8_e5m2": (torch.float8_e5m2, 57344.0)}
@@ -221,7 +222,7 @@ def _draw_lengths(name, rng, B):
         return rng.integers(1, 65, size=B).astype(np.int64)
     if name == "7b":
         return np.full(B, 2048, dtype=np.int64)
-    if name in ("70b-gqa", "spec-70b"):
+    if name in ("70b-gqa", "spec-70b", "spec-70b-q16"):
         return _lognormal_lengths(rng, B, 1024, 1.0, 128, 32768)
     if name == "prefix":
         return 2048 + rng.integers(16, 513, size=B).astype(np.int64)

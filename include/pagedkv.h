@@ -260,7 +260,7 @@ pkv_status pkv_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len,
  *              also flagged PKV_DEV_BAD_CONTEXT_LEN (and zeroed). Without status,
  *              query tokens that see no position get zeros.
  * Rows are (token, head) pairs on the tensor cores for every group size: a KV head
- * with 64 to 128 rows (q_len * g) runs all its rows in one M = 128 tcgen05 MMA per
+ * with 48 to 128 rows (q_len * g) runs all its rows in one M = 128 tcgen05 MMA per
  * 128-token tile, once per block; fewer rows run as 16-row mma.sync subgroups sharing
  * each block through shared memory; more than 128 rows as subgroups that each read the
  * block (ceil(q_len * g / 16) reads per KV head).

@@ -16,7 +16,11 @@ namespace {
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per shared-memory copy wait
 constexpr int kMaxQueryLen = PKV_MAX_QUERY_LEN;
-constexpr int kTcMinRows = 64;  // multi-query rows per KV head from which tcgen05 wins
+constexpr int kTcMinRows = 48;  // multi-query rows per KV head from which tcgen05 wins
+// tcgen05 kernel: the cost of ending a KV head (epilogue, next head's first scores) in
+// tiles, from per-CTA timings on GB300 (~4.7 us per head boundary against ~1.3 us per
+// 128-token tile); ranges are balanced on tiles plus this much per head
+constexpr int kTcHeadCost = 4;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -188,10 +192,10 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
   bool found = false;
   if (q_len > 1) {
     if (kvt != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
-    // KV heads with 64..128 query rows go through the tcgen05 kernel, fewer rows through
+    // KV heads with 48..128 query rows go through the tcgen05 kernel, fewer rows through
     // the mma.sync path: measured on GB300 with the spec-70b lengths, tcgen05 vs mma.sync
-    // per call: 16 rows 173.7 vs 93.8 us, 48 rows 183.9 vs 150.6, 64 rows 55.7 vs 73.0,
-    // 128 rows 204.3 vs 491.5 (an M = 128 MMA wastes what a small head leaves empty)
+    // per call: 16 rows 136.6 vs 93.4 us, 48 rows 146.4 vs 150.8, 64 rows 49.8 vs 72.8,
+    // 128 rows 152.4 vs 490.6 (an M = 128 MMA wastes what a small head leaves empty)
     if (rows >= kTcMinRows && rows <= 128 &&
         select_decode_tc(d->head_dim, d->block_size, &P.k)) {
       // every row of a KV head in one tcgen05 MMA: one work unit per KV head
@@ -219,7 +223,7 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
   // shared-memory rings per CTA: one per warp, or one per worker of nsg warps; the
   // tcgen05 kernel: its fixed layout plus the tile prefix and lengths of the batch
   const int rings = P.k.coop ? P.k.warps / P.nsg : P.k.warps;
-  P.smem = P.k.tc ? size_t(P.k.warp_smem) + size_t(8) * (d->num_seqs + 1)
+  P.smem = P.k.tc ? size_t(P.k.warp_smem) + size_t(12) * (d->num_seqs + 1)
                   : size_t(rings) * P.k.warp_smem + 1024 +
                         align_up(size_t(d->num_seqs + 1) * 4, 16);
 
@@ -248,8 +252,8 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
   P.W = P.k.tc ? P.grid : (P.k.coop ? P.grid * rings * P.nsg : P.grid * P.k.warps);
 
   // workspace: [prefix (B+1) int32][partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
-  P.off_prefix = 0;
-  P.off_ml = align_up(size_t(d->num_seqs + 1) * 4, 256);
+  P.off_prefix = 0;  // [B+1] work prefix, then [B+1] weighted prefix (tcgen05 kernel)
+  P.off_ml = align_up(size_t(d->num_seqs + 1) * 8, 256);
   P.off_o = align_up(P.off_ml + size_t(2) * P.W * P.gs * 8, 256);
   P.ws_bytes = align_up(P.off_o + size_t(2) * P.W * P.gs * d->head_dim * 4, 256);
   *pl = P;
@@ -311,6 +315,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   p.skip = 0;
   p.unit_slot0 = -1;
   p.q_len = q_len;
+  p.beta = P.k.tc ? kTcHeadCost : 0;
 
   void* args[] = {&tmk, &tmv, &p};
   if (launch_pdl(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), args, P.smem, stream) !=
@@ -337,6 +342,8 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   m.nsg = P.nsg;
   m.HU = P.HU;
   m.W = P.W / P.nsg;  // workers of nsg warps
+  m.beta = p.beta;
+  m.wprefix = p.prefix_out + (d->num_seqs + 1);
   launch_merge(m, stream);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;

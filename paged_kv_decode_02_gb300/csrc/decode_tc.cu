@@ -63,8 +63,10 @@ struct TcDecode {
   static constexpr int kNumBars = 16;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
-  static constexpr int kOffTables = kOffAbort + 12;  // [B+1] tile prefix, [B] clamped lengths
-  static constexpr int kFixedSmem = kOffTables + 1024;  // + 8 * (B + 1) at run time
+  // [B+1] tile prefix, [B+1] weighted prefix (tiles + beta per non-empty sequence),
+  // [B] clamped lengths
+  static constexpr int kOffTables = kOffAbort + 12;
+  static constexpr int kFixedSmem = kOffTables + 1024;  // + 12 * (B + 1) at run time
   static constexpr int kThreads = 224;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kColS = 0, kColO = 2 * kN, kColP = 2 * kN + 128;
@@ -112,8 +114,9 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + K::kOffAbort);
   int* s_prefix = reinterpret_cast<int*>(gbase + K::kOffTables);
-  const int B = p.B, Hkv = p.Hkv;
-  int* s_len = s_prefix + (B + 1);
+  const int B = p.B, Hkv = p.Hkv, beta = p.beta;
+  int* s_wpre = s_prefix + (B + 1);
+  int* s_len = s_wpre + (B + 1);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   auto bar = [&](int i) { return base + K::kOffBar + 8 * i; };
   auto kfull = [&](int st) { return bar(st); };
@@ -139,44 +142,78 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, K::kTmemCols);
 
-  // ---- tiles per sequence, their exclusive prefix, clamped lengths (every CTA) ----
+  // ---- tiles per sequence, their exclusive prefix, the weighted prefix (tiles plus
+  //      beta per non-empty sequence), clamped lengths (every CTA) ----
   {
     const int per = (B + K::kThreads - 1) / K::kThreads;
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
-    int sum = 0;
+    int sum = 0, wsum = 0;
     for (int i = b0; i < b1; ++i) {
       const int L = min(max(__ldg(p.context_lens + i), 0), p.MBS * BS);
       s_len[i] = L;
-      sum += (L + K::kN - 1) / K::kN;
+      const int n = (L + K::kN - 1) / K::kN;
+      sum += n;
+      wsum += n + (n > 0 ? beta : 0);
     }
-    int incl = sum;
+    int incl = sum, wincl = wsum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
+      const int wy = __shfl_up_sync(0xffffffffu, wincl, off);
+      if (lane >= off) {
+        incl += y;
+        wincl += wy;
+      }
     }
-    __shared__ int warp_tot[K::kThreads / 32];
-    if (lane == 31) warp_tot[warp] = incl;
+    __shared__ int warp_tot[K::kThreads / 32], warp_wtot[K::kThreads / 32];
+    if (lane == 31) {
+      warp_tot[warp] = incl;
+      warp_wtot[warp] = wincl;
+    }
     __syncthreads();
-    int run = incl - sum;
-    for (int w2 = 0; w2 < warp; ++w2) run += warp_tot[w2];
-    for (int i = b0; i < b1; ++i) {
-      run += (s_len[i] + K::kN - 1) / K::kN;
-      s_prefix[i + 1] = run;
+    int run = incl - sum, wrun = wincl - wsum;
+    for (int w2 = 0; w2 < warp; ++w2) {
+      run += warp_tot[w2];
+      wrun += warp_wtot[w2];
     }
-    if (tid == 0) s_prefix[0] = 0;
+    for (int i = b0; i < b1; ++i) {
+      const int n = (s_len[i] + K::kN - 1) / K::kN;
+      run += n;
+      wrun += n + (n > 0 ? beta : 0);
+      s_prefix[i + 1] = run;
+      s_wpre[i + 1] = wrun;
+    }
+    if (tid == 0) s_prefix[0] = s_wpre[0] = 0;
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (blockIdx.x == 0)
-    for (int i = tid; i <= B; i += K::kThreads) p.prefix_out[i] = s_prefix[i];
+    for (int i = tid; i <= B; i += K::kThreads) {
+      p.prefix_out[i] = s_prefix[i];
+      p.prefix_out[B + 1 + i] = s_wpre[i];
+    }
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + K::kOffTmemSlot);
 
-  // this CTA's range of the flat (sequence, KV head, tile) order
-  const long long T = (long long)Hkv * s_prefix[B];
+  // This CTA's tiles. Ranges are equal cuts of the weighted order, in which KV head
+  // (s, h) takes tiles_s + beta positions (its tiles, then beta for the cost of ending
+  // a head); a range covers the tiles whose positions fall in it. Tiles before
+  // weighted position x:
+  auto tiles_before = [&](long long x) -> long long {
+    if (x >= (long long)Hkv * s_wpre[B]) return (long long)Hkv * s_prefix[B];
+    int lo = 0, hi = B;  // Hkv*s_wpre[lo] <= x < Hkv*s_wpre[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((long long)Hkv * s_wpre[mid] <= x) lo = mid; else hi = mid;
+    }
+    const int n = s_prefix[lo + 1] - s_prefix[lo];
+    const long long rem = x - (long long)Hkv * s_wpre[lo];
+    const long long h = rem / (n + beta), o = rem % (n + beta);
+    return (long long)Hkv * s_prefix[lo] + h * n + min(o, (long long)n);
+  };
+  const long long TW = (long long)Hkv * s_wpre[B];
   const int C = gridDim.x, c = blockIdx.x;
-  const long long ra = T * c / C, rb = T * (c + 1) / C;
+  const long long ra = tiles_before(TW * c / C), rb = tiles_before(TW * (c + 1) / C);
   const int cnt = int(rb - ra);
   const int R = p.gs;  // query rows per KV head (q_len * g)
 
@@ -578,7 +615,7 @@ DecodeKernelInfo tc_info() {
   info.fn = reinterpret_cast<const void*>(&paged_decode_tc_kernel<D, BS>);
   info.warps = TcDecode<D, BS>::kThreads / 32;
   info.stages = 2;
-  info.warp_smem = TcDecode<D, BS>::kFixedSmem;  // per CTA, plus 8 * (B + 1)
+  info.warp_smem = TcDecode<D, BS>::kFixedSmem;  // per CTA, plus 12 * (B + 1)
   info.mma = 1;
   info.simt_heads = 0;
   info.coop = 0;

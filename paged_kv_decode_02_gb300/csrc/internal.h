@@ -26,6 +26,8 @@ struct DecodeParams {
   int32_t* status;             // optional device status word
   int B, Hq, Hkv, MBS, NB;
   int q_len;                   // new tokens per sequence (1: single-token decode)
+  int beta;                    // tcgen05 kernel: ranges are cut in an order where every
+                               //   non-empty KV head adds beta units after its tiles
   int g;                       // Hq / Hkv
   int gs;                      // query rows (token, head) handled per work unit
   int nsg;                     // work units per KV head (q_len * g / gs)
@@ -89,7 +91,9 @@ struct MergeParams {
   int B, Hq, D, MBS, NB, BS;
   int q_len;                   // new tokens per sequence (rows map as in DecodeParams)
   int g, gs, nsg, HU;
-  int W;                       // decode workers (groups of nsg warps)
+  int W;                       // decode workers (groups of nsg warps, or tcgen05 CTAs)
+  const int32_t* wprefix;      // beta > 0: per-sequence prefix of tiles + beta * [tiles > 0]
+  int beta;                    // as in DecodeParams (0: workers cut the plain order)
 };
 
 void launch_merge(const MergeParams& p, cudaStream_t stream);

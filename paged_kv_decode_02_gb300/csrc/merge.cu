@@ -70,17 +70,24 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 3) paged_decode_merge_kernel
   }
   // the decode kernel's flat order is (sequence, KV head, block) over W workers of nsg
   // warps each; this unit's parts come from warp worker * nsg + sg of each worker
+  // Workers cut the flat order (sequence, unit, item) into W equal ranges; with beta >
+  // 0 (tcgen05 kernel) the order is weighted: every unit of a non-empty sequence takes
+  // n + beta positions, its n items (tiles) first, then beta that hold none.
   const int nsg = p.nsg, kvh = u / nsg, sg = u % nsg, Hkv = p.HU / nsg;
-  const long long T = (long long)Hkv * p.prefix[p.B];
-  const long long A = (long long)Hkv * p.prefix[s] + (long long)kvh * n;
+  const int beta = p.beta;
+  const int* pre = beta > 0 ? p.wprefix : p.prefix;
+  const long long T = (long long)Hkv * pre[p.B];
+  const long long A = (long long)Hkv * pre[s] + (long long)kvh * (n + beta);
   const int W = p.W;
   const int w0 = merge_worker_of(A, T, W), w1 = merge_worker_of(A + n - 1, T, W);
   if (w0 == w1 || !active) return;  // one worker covered the whole unit: output written
   // T >= W: every worker range is non-empty and the parts are workers w0..w1;
-  // otherwise ranges hold one block at most and part i is the worker of block A + i
+  // otherwise ranges hold one position at most and part i is the worker of item A + i
   const bool dense = T >= W;
   const int nparts = dense ? (w1 - w0 + 1) : n;
-  const bool first_cut = merge_worker_start(T, w0, W) != A;
+  // the unit is not worker w0's first segment when w0 processed an item before it (the
+  // previous unit's items end beta positions before A)
+  const bool first_cut = A > 0 && merge_worker_start(T, w0, W) < A - beta;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
   Fold f = fold_empty();
   fold_parts<8>(f, 0, 1, nparts, [&](int i, const float2*& pm, const float4*& po) {

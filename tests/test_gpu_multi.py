@@ -48,7 +48,7 @@ SHAPES = [
     ("g8-q16-bs32", 16, 2, 128, 32, 16, [16, 17, 300, 1000]),
     ("g16-q2-d64", 32, 2, 64, 16, 2, [90, 17, 2]),
     ("g5-q5", 10, 2, 128, 32, 5, [100, 5, 37]),
-    # 64..128 rows per KV head take the tcgen05 kernel, more than 128 the wide mma.sync one
+    # 48..128 rows per KV head take the tcgen05 kernel, more than 128 the wide mma.sync one
     ("g16-q4-d64", 32, 2, 64, 16, 4, [4, 5, 129, 300, 0, 77]),
     ("g8-q8-bs32", 16, 2, 128, 32, 8, [8, 9, 130, 600]),
     ("g16-q8", 32, 2, 128, 16, 8, [8, 200, 1500, 127, 129]),

@@ -317,9 +317,18 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   p.q_len = q_len;
   p.beta = P.k.tc ? kTcHeadCost : 0;
 
-  void* args[] = {&tmk, &tmv, &p};
-  if (launch_pdl(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), args, P.smem, stream) !=
-      cudaSuccess)
+  // tcgen05 kernel: whole KV heads leave through TMA tensor stores of g-row boxes when
+  // g is 8, 16 or 32 (each box then starts on a 1024-byte swizzle atom of the staged rows)
+  CUtensorMap tmo;
+  std::memset(&tmo, 0, sizeof(tmo));
+  if (P.k.tc && (P.g == 8 || P.g == 16 || P.g == 32) &&
+      cache_map(&tmo, out, false, d->head_dim,
+                (long long)d->num_seqs * q_len * d->num_q_heads, P.g))
+    p.tma_out = 1;
+  void* args3[] = {&tmk, &tmv, &p};
+  void* args4[] = {&tmk, &tmv, &tmo, &p};
+  if (launch_pdl(P.k.fn, dim3(P.grid), dim3(P.k.warps * 32), P.k.tc ? args4 : args3, P.smem,
+                 stream) != cudaSuccess)
     return PKV_ERR_CUDA;
 
   MergeParams m{};
@@ -344,7 +353,26 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   m.W = P.W / P.nsg;  // workers of nsg warps
   m.beta = p.beta;
   m.wprefix = p.prefix_out + (d->num_seqs + 1);
-  launch_merge(m, stream);
+  if (P.k.tc && status == nullptr && P.grid <= 1024) {
+    // at most one cut head per CTA boundary: merge those and zero empty sequences
+    TcMergeParams t{};
+    t.out = out;
+    t.part_o = p.part_o;
+    t.part_ml = p.part_ml;
+    t.prefix = p.prefix_out;
+    t.wprefix = m.wprefix;
+    t.B = p.B;
+    t.Hq = p.Hq;
+    t.Hkv = p.Hkv;
+    t.D = d->head_dim;
+    t.q_len = q_len;
+    t.g = P.g;
+    t.R = P.gs;
+    t.beta = p.beta;
+    launch_tc_merge(t, P.grid, stream);
+  } else {
+    launch_merge(m, stream);
+  }
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
 }

@@ -29,6 +29,7 @@
 // P.V. Every wait is bounded: on a timeout the CTA sets a status bit, lets its copies
 // and MMAs complete, frees its TMEM and leaves.
 #include "decode.cuh"
+#include "fold.cuh"
 #include "tcgen05.cuh"
 
 namespace pkv {
@@ -106,7 +107,8 @@ __device__ __forceinline__ void tile_next(TileCursor& c, const int* prefix, int 
 template <int D, int BS>
 __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
-                           const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
+                           const __grid_constant__ CUtensorMap tmv,
+                           const __grid_constant__ CUtensorMap tmo, const DecodeParams p) {
   using K = TcDecode<D, BS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -346,6 +348,10 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
     // asynchronous copies (padding rows zero-filled); q_ready completes and publishes them
     auto prefetch_q = [&](const TileCursor& t, int qb) {
       constexpr int kChunks = D / 8;
+      if (p.tma_out) {  // this warp's earlier output boxes have left these rows
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
       const uint4* q = reinterpret_cast<const uint4*>(p.q);
       const size_t qrow = (size_t(t.s) * p.q_len + (row_ok ? r / p.g : 0)) * p.Hq + t.h * p.g +
                           (row_ok ? r % p.g : 0);
@@ -560,19 +566,36 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
                                     pack_bf16x2(__uint_as_float(o[e + 6]) * inv,
                                                 __uint_as_float(o[e + 7]) * inv)));
           }
-          __syncwarp();
-          // lane l's own output row, handed to the lanes that store it
-          const long long my_row =
-              (long long)((size_t(cur.s) * p.q_len + (row_ok ? r / p.g : 0)) * p.Hq +
-                          cur.h * p.g + (row_ok ? r % p.g : 0));
-          const int nrows = min(32, R - quarter * 32);
+          if (p.tma_out) {
+            // one TMA box per new token (its g rows) and 64-column slab; g divides 32,
+            // so a token's rows belong to this warp and its box starts on an atom
+            fence_proxy_async_smem();  // the staged rows, for the async proxy
+            __syncwarp();
+            if (lane == 0) {
+              const int i0 = quarter * 32 / p.g, i1 = min(p.q_len, (quarter * 32 + 32) / p.g);
+              for (int i = i0; i < i1; ++i)
+#pragma unroll
+                for (int sl = 0; sl < K::kSlabs; ++sl)
+                  tma_store_2d(&tmo, qbuf + sl * K::kSlab + (i * p.g) * 128, sl * 64,
+                               (cur.s * p.q_len + i) * p.Hq + cur.h * p.g);
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
+            // lane l's own output row, handed to the lanes that store it
+            const long long my_row =
+                (long long)((size_t(cur.s) * p.q_len + (row_ok ? r / p.g : 0)) * p.Hq +
+                            cur.h * p.g + (row_ok ? r % p.g : 0));
+            const int nrows = min(32, R - quarter * 32);
 #pragma unroll 4
-          for (int k2 = 0; k2 < kCh; ++k2) {
-            const int idx = k2 * 32 + lane, rl = idx / kCh, ch = idx % kCh;
-            const long long orow2 = __shfl_sync(0xffffffffu, my_row, rl);
-            if (rl < nrows)
-              reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                       size_t(orow2) * D)[ch] = lds128(slot_addr(quarter * 32 + rl, ch));
+            for (int k2 = 0; k2 < kCh; ++k2) {
+              const int idx = k2 * 32 + lane, rl = idx / kCh, ch = idx % kCh;
+              const long long orow2 = __shfl_sync(0xffffffffu, my_row, rl);
+              if (rl < nrows)
+                reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                         size_t(orow2) * D)[ch] =
+                    lds128(slot_addr(quarter * 32 + rl, ch));
+            }
           }
         } else {
 #pragma unroll
@@ -598,6 +621,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
       tile_next(cur, s_prefix, B, Hkv);
     }
     (void)ok;
+    if (p.tma_out && lane == 0) bulk_wait_all();  // output boxes complete before exit
     tc::fence_before_sync();
   }
   __syncthreads();
@@ -621,6 +645,97 @@ DecodeKernelInfo tc_info() {
   info.coop = 0;
   info.tc = 1;
   return info;
+}
+
+// ---------------------------------------------------------------------------
+// Merge for the tcgen05 kernel without a status word: a head is cut only where one
+// CTA's range ends inside it, so merge CTA c takes the head that contains the first
+// tile of range c when that head began inside range c - 1 (each cut head once), and
+// folds its parts from CTAs c - 1 .. (the CTA of its last tile) with the
+// online-softmax rescaling. It also zero-fills the sequences c, c + C, ... that have
+// no tile. One wave of C CTAs instead of one warp per (head, row).
+// ---------------------------------------------------------------------------
+constexpr int kTcMergeThreads = 512;
+
+__global__ void __launch_bounds__(kTcMergeThreads) paged_tc_merge_kernel(const TcMergeParams p) {
+  pdl_wait_prior_grid();
+  const int c = blockIdx.x, C = gridDim.x, tid = threadIdx.x;
+  const int B = p.B, Hkv = p.Hkv, beta = p.beta, D = p.D, Q = D / 4, R = p.R;
+  const int* tpre = p.prefix;   // tiles per sequence, exclusive prefix
+  const int* wpre = p.wprefix;  // tiles + beta per non-empty sequence, exclusive prefix
+  __nv_bfloat16* outb = reinterpret_cast<__nv_bfloat16*>(p.out);
+  // sequences without a tile get zeros
+  for (int s = c; s < B; s += C) {
+    if (tpre[s + 1] != tpre[s]) continue;
+    const size_t row0 = size_t(s) * p.q_len * p.Hq;
+    for (int k = tid; k < p.q_len * p.Hq * Q; k += blockDim.x)
+      reinterpret_cast<uint2*>(outb + (row0 + k / Q) * D)[k % Q] = make_uint2(0u, 0u);
+  }
+  if (c == 0) return;
+  const long long TW = (long long)Hkv * wpre[B], TT = (long long)Hkv * tpre[B];
+  // first tile of range w (as in the decode kernel)
+  auto range_start = [&](int w) -> long long {
+    const long long x = TW * w / C;
+    if (x >= TW) return TT;
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((long long)Hkv * wpre[mid] <= x) lo = mid; else hi = mid;
+    }
+    const int n = tpre[lo + 1] - tpre[lo];
+    const long long rem = x - (long long)Hkv * wpre[lo];
+    const long long h = rem / (n + beta), o = rem % (n + beta);
+    return (long long)Hkv * tpre[lo] + h * n + min(o, (long long)n);
+  };
+  const long long t = range_start(c);
+  if (t >= TT) return;
+  // the head holding tile t
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((long long)Hkv * tpre[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int s = lo, n = tpre[s + 1] - tpre[s];
+  const long long rem = t - (long long)Hkv * tpre[s];
+  const int h = int(rem / n);
+  const long long u0 = (long long)Hkv * tpre[s] + (long long)h * n;  // its first tile
+  const long long prev = range_start(c - 1);
+  if (u0 == t || u0 < prev) return;  // not cut here, or cut first at an earlier boundary
+  // parts: CTA c-1 (its first segment only if its range starts at the head), then
+  // CTAs c, c+1, ... whose ranges start inside the head (their first segment)
+  constexpr int kMaxParts = 1024;  // a head has at most one part per CTA (grid <= 1024)
+  __shared__ int s_slot[kMaxParts];
+  __shared__ int s_np;
+  if (tid == 0) {
+    int np = 0;
+    s_slot[np++] = 2 * (c - 1) + (prev < u0 ? 1 : 0);
+    for (int w = c; w < C && np < kMaxParts; ++w) {
+      if (range_start(w) >= u0 + n) break;
+      if (range_start(w + 1) > range_start(w)) s_slot[np++] = 2 * w;
+    }
+    s_np = np;
+  }
+  __syncthreads();
+  const int np = s_np;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  for (int k = tid; k < R * Q; k += blockDim.x) {
+    const int r = k / Q, dq = k % Q;
+    Fold f = fold_empty();
+    fold_parts<4>(f, 0, 1, np, [&](int i, const float2*& pm, const float4*& po) {
+      const size_t slot = size_t(s_slot[i]);
+      pm = ml + slot * R + r;
+      po = reinterpret_cast<const float4*>(p.part_o + (slot * R + r) * D) + dq;
+    });
+    const size_t orow = (size_t(s) * p.q_len + r / p.g) * p.Hq + size_t(h) * p.g + r % p.g;
+    reinterpret_cast<uint2*>(outb + orow * D)[dq] = fold_result(f);
+  }
+}
+
+void launch_tc_merge(const TcMergeParams& p, int grid, cudaStream_t stream) {
+  TcMergeParams copy = p;
+  void* args[] = {&copy};
+  launch_pdl(reinterpret_cast<const void*>(&paged_tc_merge_kernel), dim3(grid),
+             dim3(kTcMergeThreads), args, 0, stream);
 }
 
 bool select_decode_tc(int D, int BS, DecodeKernelInfo* info) {

@@ -28,6 +28,8 @@ struct DecodeParams {
   int q_len;                   // new tokens per sequence (1: single-token decode)
   int beta;                    // tcgen05 kernel: ranges are cut in an order where every
                                //   non-empty KV head adds beta units after its tiles
+  int tma_out;                 // tcgen05 kernel: whole heads leave through TMA tensor stores
+                               //   (boxes of g rows x 64 columns; needs g in {8, 16, 32})
   int g;                       // Hq / Hkv
   int gs;                      // query rows (token, head) handled per work unit
   int nsg;                     // work units per KV head (q_len * g / gs)
@@ -97,6 +99,18 @@ struct MergeParams {
 };
 
 void launch_merge(const MergeParams& p, cudaStream_t stream);
+
+// Merge of the tcgen05 decode kernel's cut heads when no status word is given (grid:
+// the decode kernel's CTA count).
+struct TcMergeParams {
+  void* out;
+  const float* part_o;         // [2C, R, D]
+  const float* part_ml;        // [2C, R] (running max in log2 units, sum)
+  const int32_t* prefix;       // [B+1] tiles per sequence, exclusive prefix
+  const int32_t* wprefix;      // [B+1] tiles + beta per non-empty sequence
+  int B, Hq, Hkv, D, q_len, g, R, beta;
+};
+void launch_tc_merge(const TcMergeParams& p, int grid, cudaStream_t stream);
 
 // Whole-block moves (copy-on-write copy, swap-out, swap-in): pair i moves chunk
 // src_ids[i] (or i when src_ids is NULL: a dense host buffer) of every array to chunk

@@ -53,6 +53,9 @@ SHAPES = [
     ("g8-q8-bs32", 16, 2, 128, 32, 8, [8, 9, 130, 600]),
     ("g16-q8", 32, 2, 128, 16, 8, [8, 200, 1500, 127, 129]),
     ("g16-q12-d64", 32, 2, 64, 16, 12, [12, 40, 150]),
+    # tcgen05 with groups whose rows do not form whole 8-row atoms (plain row stores)
+    ("g12-q4", 24, 2, 128, 16, 4, [4, 60, 300, 129]),
+    ("g4-q16-d64-bs32", 8, 2, 64, 32, 16, [16, 40, 500]),
 ]
 
 

@@ -130,10 +130,10 @@ pkv_status check_dims(const pkv_dims* d) {
 // sets a kernel attribute, which costs tens of microseconds, so recent plans are kept.
 struct PlanKey {
   pkv_dims d;
-  int kvt, q_len, device;
+  int kvt, q_len, device, pair;
   bool operator==(const PlanKey& o) const {
     return std::memcmp(&d, &o.d, sizeof(d)) == 0 && kvt == o.kvt && q_len == o.q_len &&
-           device == o.device;
+           device == o.device && pair == o.pair;
   }
 };
 constexpr int kPlanCache = 16;
@@ -142,10 +142,12 @@ PlanKey g_plan_keys[kPlanCache];
 Plan g_plans[kPlanCache];
 int g_plan_count = 0, g_plan_next = 0;
 
-pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl);
+pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, Plan* pl);
 
-// q_len > 1: the causal multi-query decode (bf16 caches).
-pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1) {
+// q_len > 1: the causal multi-query decode (bf16 caches). pair: 16-token blocks go in
+// pairs on the tensor-core path (the cascade's suffix decode, which skips a prefix of
+// single blocks, asks for single blocks).
+pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1, bool pair = true) {
   pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
   int dev = 0;
@@ -156,13 +158,14 @@ pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1) {
   key.kvt = kvt;
   key.q_len = q_len;
   key.device = dev;
+  key.pair = pair ? 1 : 0;
   std::lock_guard<std::mutex> lock(g_plan_mu);
   for (int i = 0; i < g_plan_count; ++i)
     if (g_plan_keys[i] == key) {
       *pl = g_plans[i];
       return PKV_OK;
     }
-  st = make_plan_uncached(d, kvt, q_len, pl);
+  st = make_plan_uncached(d, kvt, q_len, pair, pl);
   if (st != PKV_OK) return st;
   g_plan_keys[g_plan_next] = key;
   g_plans[g_plan_next] = *pl;
@@ -171,7 +174,7 @@ pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1) {
   return PKV_OK;
 }
 
-pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
+pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, Plan* pl) {
   Plan P{};
   P.g = d->num_q_heads / d->num_kv_heads;
   // query rows per KV head: (new token, group member) pairs, split into work units of
@@ -208,13 +211,17 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, Plan* pl) {
     }
   } else {
     switch (kvt) {
-      case PKV_KV_BF16: found = select_decode_bf16(d->head_dim, d->block_size, simt, &P.k); break;
-      case PKV_KV_INT8: found = select_decode_int8(d->head_dim, d->block_size, simt, &P.k); break;
+      case PKV_KV_BF16:
+        found = select_decode_bf16(d->head_dim, d->block_size, simt, &P.k, pair);
+        break;
+      case PKV_KV_INT8:
+        found = select_decode_int8(d->head_dim, d->block_size, simt, &P.k, pair);
+        break;
       case PKV_KV_FP8_E4M3:
-        found = select_decode_e4m3(d->head_dim, d->block_size, simt, &P.k);
+        found = select_decode_e4m3(d->head_dim, d->block_size, simt, &P.k, pair);
         break;
       case PKV_KV_FP8_E5M2:
-        found = select_decode_e5m2(d->head_dim, d->block_size, simt, &P.k);
+        found = select_decode_e5m2(d->head_dim, d->block_size, simt, &P.k, pair);
         break;
       default: return PKV_ERR_DTYPE;
     }
@@ -388,7 +395,7 @@ struct CascadePlan {
 };
 
 pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* cp) {
-  pkv_status st = make_plan(d, PKV_KV_BF16, &cp->dec);
+  pkv_status st = make_plan(d, PKV_KV_BF16, &cp->dec, 1, false);
   if (st != PKV_OK) return st;
   if (prefix_blocks < 1 || prefix_blocks > d->max_blocks_per_seq) return PKV_ERR_SHAPE;
   if (!select_prefix_kernel(d->head_dim, d->block_size, &cp->pk)) return PKV_ERR_UNSUPPORTED;

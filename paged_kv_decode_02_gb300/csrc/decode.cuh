@@ -855,9 +855,14 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const int* prefix, int B,
 // warp of the worker (the leader) and released by all nsg warps through an "empty"
 // mbarrier per stage, so a block crosses from L2 into shared memory once per worker
 // rather than once per warp.
-template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false>
+// kBlk = 2 (16-token caches, tensor-core paths): a work item is two consecutive blocks
+// of one KV head, landed by two boxes into one 32-token stage and processed as one
+// tile, so per-item costs (waits, fragment set-up, row maxima, rescaling) are paid
+// once per 32 tokens.
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false,
+          int kBlk = 1>
 struct DecodeKernel {
-  using Geo = TileGeom<Q8, D, BS>;
+  using Geo = TileGeom<Q8, D, BS * kBlk>;
   static constexpr int kTile = Geo::kTileBytes;
   static constexpr int kScaleBytes = Geo::kScaleBytes;
   // per-ring shared memory: K tiles, V tiles, K/V scales, mbarriers (full[kStages],
@@ -870,11 +875,13 @@ struct DecodeKernel {
   static constexpr uint32_t kTxBytes = 2 * kTile + 2 * kScaleBytes;
 };
 
-template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false>
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false,
+          int kBlk = 1>
 __global__ void __launch_bounds__(kWarps * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
-  using K = DecodeKernel<Q8, D, BS, Path, kWarps, kStages, kCoop>;
+  using K = DecodeKernel<Q8, D, BS, Path, kWarps, kStages, kCoop, kBlk>;
+  constexpr int BSI = BS * kBlk;  // tokens per work item
   using Geo = typename K::Geo;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -903,7 +910,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     int sum = 0;
     for (int i = b0; i < b1; ++i) {
       const int L = __ldg(p.context_lens + i);
-      sum += max(0, (L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS)) - p.skip);
+      sum += (max(0, (L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS)) - p.skip) + kBlk - 1) / kBlk;
     }
     // inclusive warp scan, then across warps
     int incl = sum;
@@ -920,7 +927,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     int run = base + incl - sum;
     for (int i = b0; i < b1; ++i) {
       const int L = __ldg(p.context_lens + i);
-      run += max(0, (L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS)) - p.skip);
+      run += (max(0, (L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS)) - p.skip) + kBlk - 1) / kBlk;
       s_prefix[i + 1] = run;
     }
     if (tid == 0) s_prefix[0] = 0;
@@ -978,28 +985,55 @@ __global__ void __launch_bounds__(kWarps * 32)
   cursor_locate(pc, a, s_prefix, B, Hkv);
   cc = pc;
 
-  // lane 0 of the leader issues the copies of the block at the producer cursor into
-  // stage st. The block's physical id was loaded one refill earlier (fetch_id right
-  // after the cursor moved), so no table read sits on the warp's critical path.
-  int pid = 0;
+  // lane 0 of the leader issues the copies of the item at the producer cursor into
+  // stage st. The item's physical block ids were loaded one refill earlier (fetch_id
+  // right after the cursor moved), so no table read sits on the warp's critical path.
+  // A pair's second block past its sequence is an all-zero box (and, for one-byte
+  // caches, takes the first block's scales: its weights are 0 but must stay finite).
+  int pid[kBlk];
+  int pc_s = -1, pc_nb = 0;  // sequence at the producer cursor and its blocks (pairs)
   auto fetch_id = [&]() {
-    if (lane == 0 && leader && pc.s < B)
-      pid = __ldg(p.block_tables + size_t(pc.s) * p.MBS + p.skip + pc.j);
+    if (lane == 0 && leader && pc.s < B) {
+      if constexpr (kBlk > 1) {
+        if (pc.s != pc_s) {
+          pc_s = pc.s;
+          const int L = __ldg(p.context_lens + pc.s);
+          pc_nb = (L <= 0 ? 0 : min((L + BS - 1) / BS, p.MBS)) - p.skip;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBlk; ++b) {
+        const int blk = pc.j * kBlk + b;
+        pid[b] = (kBlk == 1 || blk < pc_nb)
+                     ? __ldg(p.block_tables + size_t(pc.s) * p.MBS + p.skip + blk)
+                     : -1;
+      }
+    }
   };
+  const int rows_total = p.NB * p.Hkv * BS;  // a box at this row is all zero fill
   auto issue = [&](int st) {
     if (lane == 0 && leader) {
-      const int phys = (pid < 0 || pid >= p.NB) ? 0 : pid;  // never copy outside the pool
-      const int row = (phys * p.Hkv + pc.u) * BS;
       mbar_arrive_expect_tx(bar(st), K::kTxBytes);
+      int row0 = 0;
 #pragma unroll
-      for (int hf = 0; hf < Geo::kHalves; ++hf) {
-        const int x = hf * (Geo::kSeg / Geo::kElt);
-        tma_load_2d(sK(st) + hf * BS * Geo::kSeg, &tmk, bar(st), x, row);
-        tma_load_2d(sV(st) + hf * BS * Geo::kSeg, &tmv, bar(st), x, row);
-      }
-      if constexpr (Q8) {
-        bulk_load(sKs(st), p.k_scale + size_t(row), K::kScaleBytes, bar(st));
-        bulk_load(sVs(st), p.v_scale + size_t(row), K::kScaleBytes, bar(st));
+      for (int b = 0; b < kBlk; ++b) {
+        int row = rows_total;
+        if (b == 0 || pid[b] >= 0) {
+          const int phys = (pid[b] < 0 || pid[b] >= p.NB) ? 0 : pid[b];  // stay in the pool
+          row = (phys * p.Hkv + pc.u) * BS;
+        }
+        if (b == 0) row0 = row;
+#pragma unroll
+        for (int hf = 0; hf < Geo::kHalves; ++hf) {
+          const int x = hf * (Geo::kSeg / Geo::kElt);
+          tma_load_2d(sK(st) + (hf * BSI + b * BS) * Geo::kSeg, &tmk, bar(st), x, row);
+          tma_load_2d(sV(st) + (hf * BSI + b * BS) * Geo::kSeg, &tmv, bar(st), x, row);
+        }
+        if constexpr (Q8) {
+          const int srow = row == rows_total ? row0 : row;
+          bulk_load(sKs(st) + b * BS * 4, p.k_scale + size_t(srow), BS * 4, bar(st));
+          bulk_load(sVs(st) + b * BS * 4, p.v_scale + size_t(srow), BS * 4, bar(st));
+        }
       }
     }
   };
@@ -1019,7 +1053,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   bool first_seg = true;
   int Lc = min(__ldg(p.context_lens + cc.s), p.MBS * BS);
 
-  for (int i = 0; i < nblk; ++i) {
+  for (int i = 0; i < nblk; ++i) {  // nblk: work items (blocks, or pairs of blocks)
     const int st = i % kStages;
     const uint32_t par = uint32_t(i / kStages) & 1u;
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(st), par, p.timeout_ns));
@@ -1033,7 +1067,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
       return;
     }
-    path.block(p, sK(st), sV(st), sKs(st), sVs(st), Lc - (p.skip + cc.j) * BS);
+    path.block(p, sK(st), sV(st), sKs(st), sVs(st), Lc - (p.skip + cc.j * kBlk) * BS);
     __syncwarp();
     if (i + kStages < nblk) {
       fence_proxy_async_smem();  // this warp's reads of the stage before its refill
@@ -1073,14 +1107,16 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false>
+template <bool Q8, int D, int BS, class Path, int kWarps, int kStages, bool kCoop = false,
+          int kBlk = 1>
 DecodeKernelInfo make_decode_info(int mma, int simt_heads) {
   DecodeKernelInfo info{};
   info.fn = reinterpret_cast<const void*>(
-      &paged_decode_kernel<Q8, D, BS, Path, kWarps, kStages, kCoop>);
+      &paged_decode_kernel<Q8, D, BS, Path, kWarps, kStages, kCoop, kBlk>);
   info.warps = kWarps;
   info.stages = kStages;
-  info.warp_smem = DecodeKernel<Q8, D, BS, Path, kWarps, kStages, kCoop>::kWarpBytes;
+  info.warp_smem = DecodeKernel<Q8, D, BS, Path, kWarps, kStages, kCoop, kBlk>::kWarpBytes;
+  info.blk = kBlk;
   info.mma = mma;
   info.simt_heads = simt_heads;
   info.coop = kCoop ? 1 : 0;

@@ -20,11 +20,18 @@ struct Bf16Warps {
 };
 
 template <int D, int BS>
-bool select_shape(int simt_heads, DecodeKernelInfo* info) {
+bool select_shape(int simt_heads, DecodeKernelInfo* info, bool pair) {
   constexpr int kS = Bf16Shape<D, BS>::kStages;
   constexpr int kWm = Bf16Warps<D, BS, true>::kWarps, kWs = Bf16Warps<D, BS, false>::kWarps;
   switch (simt_heads) {
     case 0:
+      if constexpr (BS == 16) {
+        if (pair) {  // 32-token items: two 16-token blocks per stage
+          *info = make_decode_info<false, D, 16, MmaPathBf16<D, 32>, kWm,
+                                   Bf16Shape<D, 32>::kStages, false, 2>(1, 0);
+          return true;
+        }
+      }
       *info = make_decode_info<false, D, BS, MmaPathBf16<D, BS>, kWm, kS>(1, 0);
       return true;
     case 1:
@@ -78,11 +85,11 @@ bool select_decode_bf16_multi(int D, int BS, int nsg, DecodeKernelInfo* info) {
   return true;
 }
 
-bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info) {
-  if (D == 128 && BS == 16) return select_shape<128, 16>(simt_heads, info);
-  if (D == 128 && BS == 32) return select_shape<128, 32>(simt_heads, info);
-  if (D == 64 && BS == 16) return select_shape<64, 16>(simt_heads, info);
-  if (D == 64 && BS == 32) return select_shape<64, 32>(simt_heads, info);
+bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info, bool pair) {
+  if (D == 128 && BS == 16) return select_shape<128, 16>(simt_heads, info, pair);
+  if (D == 128 && BS == 32) return select_shape<128, 32>(simt_heads, info, pair);
+  if (D == 64 && BS == 16) return select_shape<64, 16>(simt_heads, info, pair);
+  if (D == 64 && BS == 32) return select_shape<64, 32>(simt_heads, info, pair);
   return false;
 }
 

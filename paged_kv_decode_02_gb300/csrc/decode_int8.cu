@@ -3,8 +3,8 @@
 
 namespace pkv {
 
-bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info) {
-  return select_q8<CODE_I8>(D, BS, simt_heads, info);
+bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info, bool pair) {
+  return select_q8<CODE_I8>(D, BS, simt_heads, info, pair);
 }
 
 }  // namespace pkv

@@ -17,10 +17,17 @@ struct Q8Shape {
 };
 
 template <int CODE, int D, int BS>
-bool select_q8_shape(int simt_heads, DecodeKernelInfo* info) {
+bool select_q8_shape(int simt_heads, DecodeKernelInfo* info, bool pair) {
   using S = Q8Shape<D, BS>;
   switch (simt_heads) {
     case 0:
+      if constexpr (BS == 16) {
+        if (pair) {  // 32-token items: two 16-token blocks per stage
+          *info = make_decode_info<true, D, 16, MmaPathInt8<D, 32, CODE>, 1,
+                                   Q8Shape<D, 32>::kMmaStages, false, 2>(1, 0);
+          return true;
+        }
+      }
       *info = make_decode_info<true, D, BS, MmaPathInt8<D, BS, CODE>, 1, S::kMmaStages>(1, 0);
       return true;
     case 1:
@@ -41,11 +48,11 @@ bool select_q8_shape(int simt_heads, DecodeKernelInfo* info) {
 }
 
 template <int CODE>
-bool select_q8(int D, int BS, int simt_heads, DecodeKernelInfo* info) {
-  if (D == 128 && BS == 16) return select_q8_shape<CODE, 128, 16>(simt_heads, info);
-  if (D == 128 && BS == 32) return select_q8_shape<CODE, 128, 32>(simt_heads, info);
-  if (D == 64 && BS == 16) return select_q8_shape<CODE, 64, 16>(simt_heads, info);
-  if (D == 64 && BS == 32) return select_q8_shape<CODE, 64, 32>(simt_heads, info);
+bool select_q8(int D, int BS, int simt_heads, DecodeKernelInfo* info, bool pair) {
+  if (D == 128 && BS == 16) return select_q8_shape<CODE, 128, 16>(simt_heads, info, pair);
+  if (D == 128 && BS == 32) return select_q8_shape<CODE, 128, 32>(simt_heads, info, pair);
+  if (D == 64 && BS == 16) return select_q8_shape<CODE, 64, 16>(simt_heads, info, pair);
+  if (D == 64 && BS == 32) return select_q8_shape<CODE, 64, 32>(simt_heads, info, pair);
   return false;
 }
 

@@ -643,6 +643,7 @@ DecodeKernelInfo tc_info() {
   info.mma = 1;
   info.simt_heads = 0;
   info.coop = 0;
+  info.blk = 1;
   info.tc = 1;
   return info;
 }

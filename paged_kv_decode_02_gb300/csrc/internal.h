@@ -141,12 +141,15 @@ struct DecodeKernelInfo {
   int mma;           // 1 = tensor-core path (groups >= 4), 0 = CUDA-core path
   int simt_heads;    // query heads per unit on the CUDA-core path
   int coop;          // 1: a worker is nsg warps sharing one ring (warp_smem per worker)
+  int blk;           // physical blocks per work item (2: pairs of 16-token blocks)
   int tc;            // 1: the tcgen05 kernel (decode_tc.cu): one CTA per SM, all rows of a
                      //    KV head per MMA, warp_smem = fixed shared memory per CTA
 };
 
 // Kernel tables, one per translation unit. Return false if the shape is not built.
-bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info);
+// pair: 16-token blocks in pairs on the tensor-core path (not with a skipped prefix)
+bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info,
+                        bool pair = false);
 // q_len > 1: the causal multi-query variant of the bf16 tensor-core path, with
 // workers of nsg warps sharing their shared-memory ring (CTA shape chosen for nsg)
 bool select_decode_bf16_multi(int D, int BS, int nsg, DecodeKernelInfo* info);
@@ -155,9 +158,12 @@ bool select_decode_tc(int D, int BS, DecodeKernelInfo* info);
 // One-byte KV code formats.
 enum : int { CODE_I8 = 0, CODE_E4M3 = 1, CODE_E5M2 = 2 };
 
-bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info);
-bool select_decode_e4m3(int D, int BS, int simt_heads, DecodeKernelInfo* info);
-bool select_decode_e5m2(int D, int BS, int simt_heads, DecodeKernelInfo* info);
+bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info,
+                        bool pair = false);
+bool select_decode_e4m3(int D, int BS, int simt_heads, DecodeKernelInfo* info,
+                        bool pair = false);
+bool select_decode_e5m2(int D, int BS, int simt_heads, DecodeKernelInfo* info,
+                        bool pair = false);
 
 // Launches with programmatic stream serialisation: the kernel may be scheduled while
 // the previous kernel on the stream drains; every kernel of this library waits for its

@@ -145,8 +145,7 @@ int g_plan_count = 0, g_plan_next = 0;
 pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, Plan* pl);
 
 // q_len > 1: the causal multi-query decode (bf16 caches). pair: 16-token blocks go in
-// pairs on the tensor-core path (the cascade's suffix decode, which skips a prefix of
-// single blocks, asks for single blocks).
+// pairs on the tensor-core paths (pairs start after a skipped prefix).
 pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1, bool pair = true) {
   pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
@@ -395,7 +394,7 @@ struct CascadePlan {
 };
 
 pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* cp) {
-  pkv_status st = make_plan(d, PKV_KV_BF16, &cp->dec, 1, false);
+  pkv_status st = make_plan(d, PKV_KV_BF16, &cp->dec);
   if (st != PKV_OK) return st;
   if (prefix_blocks < 1 || prefix_blocks > d->max_blocks_per_seq) return PKV_ERR_SHAPE;
   if (!select_prefix_kernel(d->head_dim, d->block_size, &cp->pk)) return PKV_ERR_UNSUPPORTED;

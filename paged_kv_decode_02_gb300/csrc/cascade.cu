@@ -28,10 +28,10 @@ namespace pkv {
 // boxes of one block x 64 columns, 128-byte swizzled; lane b copies block b, so the
 // small copies of a tile leave in parallel and a score MMA never waits behind a V
 // tile); warp 1 allocates TMEM and one of its threads issues every MMA; warps 2..5
-// (TMEM lane quarters 2, 3, 0, 1) run the online softmax. The running reference max m of a row moves only when a tile's max
-// exceeds it by more than 8 (log2 units); O in TMEM is then rescaled by 2^(m_old -
-// m_new) before the next P.V accumulates, so weights stay below 2^8 and most tiles
-// skip the rescale. Each split leaves per row the unnormalised (o, m, l) record that
+// (TMEM lane quarters 2, 3, 0, 1) run the online softmax. The running reference max m
+// of a row moves only when a tile's max exceeds it by more than 8 (log2 units); O in
+// TMEM is then rescaled by 2^(m_old - m_new) before the next P.V accumulates, so
+// weights stay below 2^8 and most tiles skip the rescale. Each split leaves per row the unnormalised (o, m, l) record that
 // the cascade merge folds.
 // Shared memory (1024-byte aligned): Q [D/64 slabs][128 rows x 128 B], K and V
 // tiles x2 [D/64 slabs][128 tokens x 128 B], then the mbarriers, the TMEM address
@@ -245,7 +245,8 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
       if (!__all_sync(0xffffffffu,
-                      tc::wait_or_abort(sfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag))) {
+                      tc::wait_or_abort(sfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns,
+                                        abort_flag))) {
         ok = false;
         break;
       }
@@ -389,33 +390,33 @@ bool select_prefix_kernel(int D, int BS, PrefixKernelInfo* info) {
 }
 
 // ---------------------------------------------------------------------------
-// Cascade merge: one warp per (sequence, unit, group of query rows), one 16-byte
-// output quad per lane, folds the nsplit prefix partials of its rows and the suffix
-// parts (the unit's own record when one decode worker covered the whole suffix, else
-// the cut workers' slots). With a status word it first validates the sequence:
+// Cascade merge: one warp per (sequence, unit), one 16-byte output quad per lane and
+// row, folds the nsplit prefix partials of the unit's rows and the suffix parts (the
+// unit's own record when one decode worker covered the whole suffix, else the cut
+// workers' slots). With a status word it first validates the sequence:
 // context length in [prefix, max_blocks*block_size], block ids in the pool, and the
 // table's head equal to the shared prefix (row 0); a sequence that fails gets a zero
 // output.
 // ---------------------------------------------------------------------------
-constexpr int kCascadeWarps = 8;  // one (unit, row group) per warp
+constexpr int kCascadeWarps = 8;  // one (sequence, unit) per warp
 
-__global__ void __launch_bounds__(kCascadeWarps * 32, 4)
+__global__ void __launch_bounds__(kCascadeWarps * 32)
     paged_cascade_merge_kernel(const CascadeMergeParams p) {
   pdl_wait_prior_grid();
   const int lane = threadIdx.x & 31;
   const int gs = p.gs, D = p.D, Q = D / 4;
-  const int rpw = 32 / Q;                 // rows per warp: one output quad per lane
-  const int ngrp = (gs + rpw - 1) / rpw;  // row groups per unit
-  const int item = blockIdx.x * kCascadeWarps + (threadIdx.x >> 5);
-  if (item >= p.B * p.HU * ngrp) return;
-  const int unit = item / ngrp, r0 = (item % ngrp) * rpw;
+  const int rpw = 32 / Q;                    // rows per warp step: one quad per lane
+  const int nsteps = (gs + rpw - 1) / rpw;   // steps over the unit's rows
+  const int unit = blockIdx.x * kCascadeWarps + (threadIdx.x >> 5);
+  if (unit >= p.B * p.HU) return;
   const int s = unit / p.HU, u = unit % p.HU;
   const int h = u / p.nsg, sg = u % p.nsg;
-  const int row = r0 + lane / Q, dq = lane % Q;
-  const bool active = row < gs;
-  uint2* out = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
-                                        (size_t(s) * p.Hq + h * p.g + sg * gs + row) * D) +
-               dq;
+  const int dq = lane % Q;
+  auto out_quad = [&](int row) {
+    return reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                    (size_t(s) * p.Hq + h * p.g + sg * gs + row) * D) +
+           dq;
+  };
 
   if (p.status != nullptr) {
     int flags = 0;
@@ -429,12 +430,14 @@ __global__ void __launch_bounds__(kCascadeWarps * 32, 4)
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
     if (flags) {
-      if (lane == 0 && u == 0 && r0 == 0) atomicOr(p.status, flags);
-      if (active) *out = make_uint2(0u, 0u);
+      if (lane == 0 && u == 0) atomicOr(p.status, flags);
+      for (int k = 0; k < nsteps; ++k) {
+        const int row = k * rpw + lane / Q;
+        if (row < gs) *out_quad(row) = make_uint2(0u, 0u);
+      }
       return;
     }
   }
-  if (!active) return;
 
   // the parts: nsplit prefix records, then the suffix parts
   // suffix parts: the decode kernel's flat order is (sequence, KV head, block) over Wg
@@ -455,31 +458,44 @@ __global__ void __launch_bounds__(kCascadeWarps * 32, 4)
     first_cut = (T * w0 / Wg) != A;
   }
   const int nparts = p.nsplit + nsuf;
-  const size_t prow = size_t(s) * p.g + size_t(sg) * gs + row;  // prefix record row
-  Fold f = fold_empty();
-  fold_parts<4>(f, 0, 1, nparts, [&](int i, const float2*& pm, const float4*& po) {
-    if (i < p.nsplit) {
-      const size_t rec = size_t(i * p.Hkv + h) * p.R + prow;
-      pm = reinterpret_cast<const float2*>(p.pre_ml) + rec;
-      po = reinterpret_cast<const float4*>(p.pre_o + rec * D) + dq;
-      return;
+  const float2* pre_ml = reinterpret_cast<const float2*>(p.pre_ml);
+  const float2* part_ml = reinterpret_cast<const float2*>(p.part_ml);
+  // up to four row steps at a time, every load of a chunk in flight together
+  constexpr int kRows = 4;
+  for (int k0 = 0; k0 < nsteps; k0 += kRows) {
+    const int kn = min(kRows, nsteps - k0);
+    Fold f[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) f[k] = fold_empty();
+    fold_rows<kRows, 2>(f, kn, nparts, [&](int i, int k, const float2*& pm, const float4*& po) {
+      const int row = min((k0 + k) * rpw + lane / Q, gs - 1);  // rows past gs: not stored
+      if (i < p.nsplit) {
+        const size_t rec = size_t(i * p.Hkv + h) * p.R + size_t(s) * p.g + size_t(sg) * gs + row;
+        pm = pre_ml + rec;
+        po = reinterpret_cast<const float4*>(p.pre_o + rec * D) + dq;
+        return;
+      }
+      const int kk = i - p.nsplit;
+      size_t slot;
+      if (whole) slot = size_t(2 * p.W) + size_t(s) * p.HU + u;
+      else if (dense)
+        slot = size_t(2 * ((w0 + kk) * p.nsg + sg) + ((kk == 0 && first_cut) ? 1 : 0));
+      else slot = size_t(2 * ((int(((A + kk + 1) * Wg + T - 1) / T) - 1) * p.nsg + sg));
+      pm = part_ml + slot * gs + row;
+      po = reinterpret_cast<const float4*>(p.part_o + (slot * gs + row) * D) + dq;
+    });
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      const int row = (k0 + k) * rpw + lane / Q;
+      if (k < kn && row < gs) *out_quad(row) = fold_result(f[k]);
     }
-    const int k = i - p.nsplit;
-    size_t slot;
-    if (whole) slot = size_t(2 * p.W) + size_t(s) * p.HU + u;
-    else if (dense) slot = size_t(2 * ((w0 + k) * p.nsg + sg) + ((k == 0 && first_cut) ? 1 : 0));
-    else slot = size_t(2 * ((int(((A + k + 1) * Wg + T - 1) / T) - 1) * p.nsg + sg));
-    pm = reinterpret_cast<const float2*>(p.part_ml) + slot * gs + row;
-    po = reinterpret_cast<const float4*>(p.part_o + (slot * gs + row) * D) + dq;
-  });
-  *out = fold_result(f);
+  }
 }
 
 void launch_cascade_merge(const CascadeMergeParams& p, cudaStream_t stream) {
-  const int rpw = 32 / (p.D / 4);
-  const long long items = (long long)p.B * p.HU * ((p.gs + rpw - 1) / rpw);
-  if (items <= 0) return;
-  const int grid = int((items + kCascadeWarps - 1) / kCascadeWarps);
+  const long long units = (long long)p.B * p.HU;
+  if (units <= 0) return;
+  const int grid = int((units + kCascadeWarps - 1) / kCascadeWarps);
   CascadeMergeParams copy = p;
   void* args[] = {&copy};
   launch_pdl(reinterpret_cast<const void*>(&paged_cascade_merge_kernel), dim3(grid),

@@ -70,6 +70,52 @@ __device__ __forceinline__ void fold_parts(Fold& f, int first, int stride, int n
   }
 }
 
+// fold_parts for up to kRows rows at once (nrows of them live): the chunk's loads of
+// every row are issued before any is used. part(i, k) returns part i of row k.
+template <int kRows, int kChunk, class PartFn>
+__device__ __forceinline__ void fold_rows(Fold (&f)[kRows], int nrows, int nparts,
+                                          PartFn part) {
+  for (int i0 = 0; i0 < nparts; i0 += kChunk) {
+    float2 v[kRows][kChunk];
+    float4 x[kRows][kChunk];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) {
+        const int i = i0 + c;
+        v[k][c] = make_float2(-INFINITY, 0.f);
+        x[k][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < nrows && i < nparts) {
+          const float2* ml;
+          const float4* o;
+          part(i, k, ml, o);
+          v[k][c] = *ml;
+          x[k][c] = *o;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      float cm = v[k][0].x;
+#pragma unroll
+      for (int c = 1; c < kChunk; ++c) cm = fmaxf(cm, v[k][c].x);
+      if (cm > f[k].m) {
+        fold_scale(f[k], fast_exp2(f[k].m - cm));
+        f[k].m = cm;
+      }
+#pragma unroll
+      for (int c = 0; c < kChunk; ++c) {
+        const float e = v[k][c].x > -INFINITY ? fast_exp2(v[k][c].x - f[k].m) : 0.f;
+        f[k].l = fmaf(e, v[k][c].y, f[k].l);
+        f[k].o.x = fmaf(e, x[k][c].x, f[k].o.x);
+        f[k].o.y = fmaf(e, x[k][c].y, f[k].o.y);
+        f[k].o.z = fmaf(e, x[k][c].z, f[k].o.z);
+        f[k].o.w = fmaf(e, x[k][c].w, f[k].o.w);
+      }
+    }
+  }
+}
+
 // Adds another running fold.
 __device__ __forceinline__ void fold_merge(Fold& f, const Fold& g) {
   if (!(g.m > -INFINITY)) return;

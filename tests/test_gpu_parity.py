@@ -369,6 +369,23 @@ def test_cascade_zero_and_negative_scale(pk, scale):
     assert max_err(out, ref) <= DECODE_ATOL
 
 
+@pytest.mark.parametrize("B,bs", [(128, 16), (256, 32)], ids=["4x16", "8x32"])
+def test_cascade_four_and_eight_row_tiles(pk, B, bs):
+    # 4 query heads per KV head: 128 sequences make 4 row tiles of 128 query rows per KV
+    # head, 256 sequences 8 row tiles over blocks of 32 (4 blocks per 128-token tile)
+    pre = 160 if bs == 16 else 192
+    rng = np.random.default_rng(B + bs)
+    lengths = [pre + int(x) for x in rng.integers(0, 41, size=B)]
+    w = make_workload("prefix", device=DEV, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                      block_size=bs, lengths=lengths, prefix_tokens=pre, seed=24,
+                      poison_unused=True)
+    out = _cascade(pk, w, pre // bs)
+    torch.cuda.synchronize()
+    pairs = sample_pairs(w, 40, seed=5)
+    ref = oracle_outputs(w, pairs)
+    assert max_err(out, ref, pairs) <= DECODE_ATOL
+
+
 def test_cascade_full_prefix_workload(pk):
     w = make_workload("prefix", device=DEV)
     out = _cascade(pk, w, 2048 // w.block_size)

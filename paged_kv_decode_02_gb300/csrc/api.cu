@@ -109,7 +109,7 @@ struct Plan {
   int g, gs, nsg, HU;
   int grid, W;
   size_t smem;
-  size_t off_prefix, off_ml, off_o, ws_bytes;
+  size_t off_prefix, off_rng, off_ml, off_o, ws_bytes;
 };
 
 pkv_status check_dims(const pkv_dims* d) {
@@ -259,7 +259,8 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
 
   // workspace: [prefix (B+1) int32][partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
   P.off_prefix = 0;  // [B+1] work prefix, then [B+1] weighted prefix (tcgen05 kernel)
-  P.off_ml = align_up(size_t(d->num_seqs + 1) * 8, 256);
+  P.off_rng = align_up(size_t(d->num_seqs + 1) * 8, 256);  // tcgen05: [grid] range starts
+  P.off_ml = align_up(P.off_rng + (P.k.tc ? size_t(P.grid) * sizeof(TcRange) : 0), 256);
   P.off_o = align_up(P.off_ml + size_t(2) * P.W * P.gs * 8, 256);
   P.ws_bytes = align_up(P.off_o + size_t(2) * P.W * P.gs * d->head_dim * 4, 256);
   *pl = P;
@@ -306,6 +307,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   p.part_o = reinterpret_cast<float*>(ws + P.off_o);
   p.part_ml = reinterpret_cast<float*>(ws + P.off_ml);
   p.prefix_out = reinterpret_cast<int32_t*>(ws + P.off_prefix);
+  p.range_out = P.k.tc ? reinterpret_cast<TcRange*>(ws + P.off_rng) : nullptr;
   p.status = status;
   p.B = d->num_seqs;
   p.Hq = d->num_q_heads;
@@ -366,7 +368,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
     t.part_o = p.part_o;
     t.part_ml = p.part_ml;
     t.prefix = p.prefix_out;
-    t.wprefix = m.wprefix;
+    t.ranges = p.range_out;
     t.B = p.B;
     t.Hq = p.Hq;
     t.Hkv = p.Hkv;
@@ -374,7 +376,6 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
     t.q_len = q_len;
     t.g = P.g;
     t.R = P.gs;
-    t.beta = p.beta;
     launch_tc_merge(t, P.grid, stream);
   } else {
     launch_merge(m, stream);

@@ -17,10 +17,11 @@ namespace {
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per shared-memory copy wait
 constexpr int kMaxQueryLen = PKV_MAX_QUERY_LEN;
 constexpr int kTcMinRows = 48;  // multi-query rows per KV head from which tcgen05 wins
-// tcgen05 kernel: the cost of ending a KV head (epilogue, next head's first scores) in
-// tiles, from per-CTA timings on GB300 (~4.7 us per head boundary against ~1.3 us per
-// 128-token tile); ranges are balanced on tiles plus this much per head
-constexpr int kTcHeadCost = 4;
+// tcgen05 kernel: the cost of ending a KV head (its partly filled last tile, the
+// epilogue, the next head's first scores) in tiles; ranges are balanced on tiles plus
+// this much per head. A sweep of whole calls on GB300 (48, 64 and 128 query rows per
+// KV head) put the best at 3 for all three shapes (2 and 4: 4-8 % slower)
+constexpr int kTcHeadCost = 3;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

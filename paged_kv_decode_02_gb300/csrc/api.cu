@@ -22,6 +22,8 @@ constexpr int kTcMinRows = 48;  // multi-query rows per KV head from which tcgen
 // this much per head. A sweep of whole calls on GB300 (48, 64 and 128 query rows per
 // KV head) put the best at 3 for all three shapes (2 and 4: 4-8 % slower)
 constexpr int kTcHeadCost = 3;
+// cascade decode: the prefix kernel runs on about 1/kCascadePrefixShare of the SMs
+constexpr int kCascadePrefixShare = 3;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -131,10 +133,10 @@ pkv_status check_dims(const pkv_dims* d) {
 // sets a kernel attribute, which costs tens of microseconds, so recent plans are kept.
 struct PlanKey {
   pkv_dims d;
-  int kvt, q_len, device, pair;
+  int kvt, q_len, device, pair, sm_cap;
   bool operator==(const PlanKey& o) const {
     return std::memcmp(&d, &o.d, sizeof(d)) == 0 && kvt == o.kvt && q_len == o.q_len &&
-           device == o.device && pair == o.pair;
+           device == o.device && pair == o.pair && sm_cap == o.sm_cap;
   }
 };
 constexpr int kPlanCache = 16;
@@ -143,11 +145,14 @@ PlanKey g_plan_keys[kPlanCache];
 Plan g_plans[kPlanCache];
 int g_plan_count = 0, g_plan_next = 0;
 
-pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, Plan* pl);
+pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, int sm_cap,
+                              Plan* pl);
 
 // q_len > 1: the causal multi-query decode (bf16 caches). pair: 16-token blocks go in
-// pairs on the tensor-core paths (pairs start after a skipped prefix).
-pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1, bool pair = true) {
+// pairs on the tensor-core paths (pairs start after a skipped prefix). sm_cap > 0: size
+// the grid for that many SMs (the rest run another kernel at the same time).
+pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1, bool pair = true,
+                     int sm_cap = 0) {
   pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
   int dev = 0;
@@ -159,13 +164,14 @@ pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1, bool p
   key.q_len = q_len;
   key.device = dev;
   key.pair = pair ? 1 : 0;
+  key.sm_cap = sm_cap;
   std::lock_guard<std::mutex> lock(g_plan_mu);
   for (int i = 0; i < g_plan_count; ++i)
     if (g_plan_keys[i] == key) {
       *pl = g_plans[i];
       return PKV_OK;
     }
-  st = make_plan_uncached(d, kvt, q_len, pair, pl);
+  st = make_plan_uncached(d, kvt, q_len, pair, sm_cap, pl);
   if (st != PKV_OK) return st;
   g_plan_keys[g_plan_next] = key;
   g_plans[g_plan_next] = *pl;
@@ -174,7 +180,8 @@ pkv_status make_plan(const pkv_dims* d, int kvt, Plan* pl, int q_len = 1, bool p
   return PKV_OK;
 }
 
-pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, Plan* pl) {
+pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, int sm_cap,
+                              Plan* pl) {
   Plan P{};
   P.g = d->num_q_heads / d->num_kv_heads;
   // query rows per KV head: (new token, group member) pairs, split into work units of
@@ -253,7 +260,7 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
       per_sm <= 0)
     return PKV_ERR_CUDA;
   if (P.k.tc) per_sm = 1;  // 512 TMEM columns per CTA: one CTA per SM
-  P.grid = sms * per_sm;
+  P.grid = (sm_cap > 0 ? std::min(sm_cap, sms) : sms) * per_sm;
   // owners of partial slots: decode warps (warps left idle by a cooperative CTA own
   // none), or the CTAs of the tcgen05 kernel
   P.W = P.k.tc ? P.grid : (P.k.coop ? P.grid * rings * P.nsg : P.grid * P.k.warps);
@@ -390,31 +397,41 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
 // ---------------------------------------------------------------------------
 struct CascadePlan {
   Plan dec;                    // suffix decode (its partial arrays get 2W + B*HU slots)
-  int R, nsplit, per_split;
+  int R, nsplit, per_split, overlap;
   PrefixKernelInfo pk;
   size_t off_prefix, off_ml, off_o, off_pre_o, off_pre_ml, ws_bytes;
 };
 
 pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* cp) {
-  pkv_status st = make_plan(d, PKV_KV_BF16, &cp->dec);
+  pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
   if (prefix_blocks < 1 || prefix_blocks > d->max_blocks_per_seq) return PKV_ERR_SHAPE;
   if (!select_prefix_kernel(d->head_dim, d->block_size, &cp->pk)) return PKV_ERR_UNSUPPORTED;
-  const Plan& P = cp->dec;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return PKV_ERR_CUDA;
-  cp->R = d->num_seqs * P.g;
-  // one CTA per SM (TMEM and shared memory): split the prefix so that the
-  // (row tile, KV head, split) grid fills at most one wave, cutting at tile boundaries
+  cp->R = d->num_seqs * (d->num_q_heads / d->num_kv_heads);
+  // One prefix CTA per SM (TMEM and shared memory), grid (row tile, KV head, split),
+  // cut at tile boundaries. The prefix kernel and the suffix decode are independent:
+  // the prefix takes about a third of the SMs (at least one CTA per row tile and KV
+  // head, at most half) and the suffix decode, sized for the other SMs, runs beside it.
+  // When the row tiles alone need more than half the SMs, the two run one after the
+  // other and the prefix splits to fill one wave.
   const int ctas = ((cp->R + cp->pk.rows - 1) / cp->pk.rows) * d->num_kv_heads;
   const int tiles = (prefix_blocks + cp->pk.tile_blocks - 1) / cp->pk.tile_blocks;
   const int max_tiles = cp->pk.max_split_blocks / cp->pk.tile_blocks;
-  const int nsplit = std::max((tiles + max_tiles - 1) / max_tiles,
-                              std::max(1, std::min(tiles, sms / std::max(1, ctas))));
+  const int min_split = (tiles + max_tiles - 1) / max_tiles;
+  cp->overlap = ctas * min_split <= sms / 2 ? 1 : 0;
+  const int budget = cp->overlap ? std::max(ctas * min_split, sms / kCascadePrefixShare) : sms;
+  const int nsplit =
+      std::max(min_split, std::max(1, std::min(tiles, budget / std::max(1, ctas))));
   cp->per_split = ((tiles + nsplit - 1) / nsplit) * cp->pk.tile_blocks;
   cp->nsplit = (prefix_blocks + cp->per_split - 1) / cp->per_split;
+  st = make_plan(d, PKV_KV_BF16, &cp->dec, 1, true,
+                 cp->overlap ? sms - ctas * cp->nsplit : 0);
+  if (st != PKV_OK) return st;
+  const Plan& P = cp->dec;
   const size_t nslots = size_t(2) * P.W + size_t(d->num_seqs) * P.HU;
   cp->off_prefix = 0;
   cp->off_ml = align_up(size_t(d->num_seqs + 1) * 4, 256);
@@ -468,6 +485,7 @@ pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void
   pp.R = C.R;
   pp.NB = d->num_blocks;
   pp.nsplit = C.nsplit;
+  pp.overlap = C.overlap;
   pp.per_split = C.per_split;
   pp.scale_log2 = scale_log2;
   pp.timeout_ns = kTimeoutNs;
@@ -502,6 +520,7 @@ pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void
   p.timeout_ns = kTimeoutNs;
   p.skip = prefix_blocks;
   p.unit_slot0 = 2 * P.W;
+  p.late_wait = C.overlap;
   p.q_len = 1;
   {
     void* args[] = {&tmk, &tmv, &p};

@@ -94,6 +94,9 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
   const uint32_t tmem_slot = base + K::kOffTmemSlot;
 
   pdl_wait_prior_grid();
+  // the suffix decode reads nothing this kernel writes: with its late wait it may start
+  // now, on the SMs this grid leaves free
+  if (pp.overlap) pdl_allow_next_grid();
   if (tid == 0) {
     for (int i = 0; i < 10; ++i) mbar_init(bar(i), 1);
     mbar_init(pfull, 4 * 32);

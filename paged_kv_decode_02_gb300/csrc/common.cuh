@@ -25,6 +25,13 @@ __device__ __forceinline__ void pdl_wait_prior_grid() {
 __device__ __forceinline__ void pdl_allow_next_grid() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Waits for the previous grid when the enclosing scope is left (every return path).
+struct PdlWaitOnExit {
+  bool on;
+  __device__ __forceinline__ ~PdlWaitOnExit() {
+    if (on) pdl_wait_prior_grid();
+  }
+};
 
 // ---------------------------------------------------------------------------
 // mbarrier

@@ -892,7 +892,11 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.B;
-  pdl_wait_prior_grid();
+  // late_wait: the previous grid (the cascade prefix kernel, which waited for its own
+  // predecessor before letting this grid start) writes nothing read here; this grid
+  // only must not complete before it, so every thread waits on the way out
+  const PdlWaitOnExit wait_on_exit{p.late_wait != 0};
+  if (!p.late_wait) pdl_wait_prior_grid();
   if constexpr (kCoop) {  // shared rings: barriers ready before the CTA-wide sync below
     if (tid < wpc * kStages) {
       const uint32_t rb = smem_base + (tid / kStages) * K::kWarpBytes + K::kOffBar;

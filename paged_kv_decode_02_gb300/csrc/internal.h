@@ -37,6 +37,8 @@ struct DecodeParams {
   int q_len;                   // new tokens per sequence (1: single-token decode)
   int beta;                    // tcgen05 kernel: ranges are cut in an order where every
                                //   non-empty KV head adds beta units after its tiles
+  int late_wait;               // wait for the previous grid only before exiting (cascade
+                               //   suffix running beside the prefix kernel)
   int tma_out;                 // tcgen05 kernel: whole heads leave through TMA tensor stores
                                //   (boxes of g rows x 64 columns; needs g in {8, 16, 32})
   int g;                       // Hq / Hkv
@@ -56,6 +58,7 @@ struct PrefixParams {
   float* pre_ml;               // [nsplit, Hkv, R, 2] (running max in log2 units, sum)
   int P, B, Hq, Hkv, g, R, NB;  // R = B * g query rows per KV head
   int nsplit, per_split;       // prefix blocks [z*per_split, min(P, (z+1)*per_split)) for split z
+  int overlap;                 // let the next grid (the suffix decode, late_wait) start at once
   float scale_log2;
   unsigned long long timeout_ns;
   int32_t* status;

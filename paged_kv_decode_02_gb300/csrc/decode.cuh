@@ -34,6 +34,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "fold.cuh"
 #include "internal.h"
 
 namespace pkv {
@@ -158,6 +159,84 @@ __device__ __forceinline__ size_t partial_slot(int w, bool first_segment) {
   return size_t(2 * w + (first_segment ? 0 : 1));
 }
 
+// Launch number of this grid within the context (differs between launches, graph
+// replays included).
+__device__ __forceinline__ unsigned long long grid_launch_id() {
+  unsigned long long g;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(g));
+  return g;
+}
+
+// Stream-K fixup inside the decode kernel (single-token decode, one warp per unit row
+// group, no status word): a warp that left a partial record for a cut unit adds the
+// unit items it covered to the unit's counter; the warp whose addition completes the
+// unit's n items folds every part (the same parts and slots the split-KV merge kernel
+// would take) and writes the output. A counter word holds a launch tag (low 40 bits of
+// the grid's launch number) over a 24-bit item count: a word with another tag counts
+// as zero, so the workspace needs no clearing, and the completing warp resets it.
+// Writers fence their records before the counter update, the completing warp fences
+// after it and reads the records through L2.
+template <int D>
+__device__ __forceinline__ void fixup_cut_unit(const DecodeParams& p, const int* s_prefix,
+                                               int s, int kvh, int n, int mine,
+                                               long long T, int W, int lane) {
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) {
+    const unsigned long long tag = grid_launch_id() & ((1ull << 40) - 1ull);
+    unsigned long long* ctr = p.fix_ctr + size_t(s) * p.Hkv + kvh;
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    for (;;) {
+      const unsigned long long base = (cur >> 24) == tag ? (cur & 0xffffffull) : 0ull;
+      const unsigned long long want = (tag << 24) | (base + unsigned(mine));
+      const unsigned long long seen = atomicCAS(ctr, cur, want);
+      if (seen == cur) {
+        last = int(base) + mine == n;
+        break;
+      }
+      cur = seen;
+    }
+    if (last) atomicExch(ctr, 0ull);
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
+  // the unit's parts, as in the split-KV merge kernel
+  const long long A = (long long)p.Hkv * s_prefix[s] + (long long)kvh * n;
+  auto worker_of = [&](long long x) { return int(((x + 1) * W + T - 1) / T) - 1; };
+  const int w0 = worker_of(A), w1 = worker_of(A + n - 1);
+  const bool dense = T >= W;
+  const int nparts = dense ? (w1 - w0 + 1) : n;
+  const bool first_cut = A > 0 && (T * w0 / W) < A;
+  constexpr int Q = D / 4;
+  const int gs = p.gs, items = gs * Q;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  constexpr int kRows = 1;  // one item per lane at a time: few registers beside the main loop
+  for (int k0 = lane; k0 < items; k0 += 32 * kRows) {
+    const int live = min(kRows, (items - k0 + 31) / 32);
+    Fold f[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) f[j] = fold_empty();
+    fold_rows<kRows, 2, true>(f, live, nparts, [&](int i, int j, const float2*& pm,
+                                                   const float4*& po) {
+      const int k = k0 + 32 * j, r = k / Q, dq = k % Q;
+      const size_t slot =
+          dense ? size_t(2 * (w0 + i) + ((i == 0 && first_cut) ? 1 : 0))
+                : size_t(2 * worker_of(A + i));
+      pm = ml + slot * gs + r;
+      po = reinterpret_cast<const float4*>(p.part_o + (slot * gs + r) * D) + dq;
+    });
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      if (j >= live) break;
+      const int k = k0 + 32 * j, r = k / Q, dq = k % Q;
+      reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                               (size_t(s) * p.Hq + size_t(kvh) * p.g + r) * D)[dq] =
+          fold_result(f[j]);
+    }
+  }
+}
+
 // ===========================================================================
 // CUDA-core path (groups of 1..3 query heads per KV head)
 //
@@ -169,6 +248,9 @@ __device__ __forceinline__ size_t partial_slot(int w, bool first_segment) {
 // ===========================================================================
 template <bool Q8, int D, int BS, int G, int CODE = CODE_I8>
 struct SimtPath {
+  // cut units are folded in the decode kernel (fixup_cut_unit) where that leaves the
+  // kernel's occupancy as it was: bf16 caches, head_dim 128, one query head per KV head
+  static constexpr bool kFixup = !Q8 && D == 128 && G == 1;
   using Geo = TileGeom<Q8, D, BS>;
   using Codec = Code8<CODE>;
   static constexpr int kChunks = Geo::kChunksPerRow;          // 16-byte chunks per row
@@ -361,6 +443,7 @@ struct SimtPath {
 // ===========================================================================
 template <int D, int BS, bool kCausal = false>
 struct MmaPathBf16 {
+  static constexpr bool kFixup = false;  // cut units go to the merge kernel
   using Geo = TileGeom<false, D, BS>;
   static constexpr int kKS = D / 16;  // k-steps of q.K^T
   static constexpr int kNT = BS / 8;  // token n-tiles
@@ -575,6 +658,7 @@ struct MmaPathBf16 {
 // ===========================================================================
 template <int D, int BS, int CODE = CODE_I8>
 struct MmaPathInt8 {
+  static constexpr bool kFixup = false;  // cut units go to the merge kernel
   using Geo = TileGeom<true, D, BS>;
   using Codec = Code8<CODE>;
   static constexpr float kVUp = CODE == CODE_E5M2 ? 32768.f : CODE == CODE_E4M3 ? 256.f : 1.f;
@@ -939,6 +1023,15 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (blockIdx.x == 0)
       for (int i = tid; i <= B; i += nthr) p.prefix_out[i] = s_prefix[i];
   }
+  if (Path::kFixup && p.fixup) {  // no merge kernel follows: empty sequences get zeros here
+    constexpr int Q = D / 4;
+    for (int s = blockIdx.x; s < B; s += gridDim.x) {
+      if (s_prefix[s + 1] != s_prefix[s]) continue;
+      uint2* row = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                            size_t(s) * p.Hq * D);
+      for (int k = tid; k < p.Hq * Q; k += kWarps * 32) row[k] = make_uint2(0u, 0u);
+    }
+  }
 
   // Flat order (sequence, KV head, block), cut into Wg equal ranges. A worker is nsg
   // consecutive warps, one per row subgroup of the KV head: they stream the same blocks
@@ -1098,8 +1191,13 @@ __global__ void __launch_bounds__(kWarps * 32)
       if (complete && p.unit_slot0 >= 0)  // cascade: the suffix result is one more part
         path.finish(p, false,
                     size_t(p.unit_slot0) + size_t(cc.s) * p.HU + size_t(cc.u) * nsg + sg);
-      else
+      else {
         path.finish(p, complete, partial_slot(w, first_seg));
+        if constexpr (Path::kFixup) {
+          if (!complete && p.fixup)
+            fixup_cut_unit<D>(p, s_prefix, cc.s, cc.u, cc.n, cc.j - seg_j0 + 1, T, Wg, lane);
+        }
+      }
       first_seg = false;
     }
     cursor_next(cc, s_prefix, B, Hkv);
@@ -1125,6 +1223,7 @@ DecodeKernelInfo make_decode_info(int mma, int simt_heads) {
   info.simt_heads = simt_heads;
   info.coop = kCoop ? 1 : 0;
   info.tc = 0;
+  info.fixup = Path::kFixup ? 1 : 0;
   return info;
 }
 

@@ -72,7 +72,8 @@ __device__ __forceinline__ void fold_parts(Fold& f, int first, int stride, int n
 
 // fold_parts for up to kRows rows at once (nrows of them live): the chunk's loads of
 // every row are issued before any is used. part(i, k) returns part i of row k.
-template <int kRows, int kChunk, class PartFn>
+// kL2: load through L2 only (parts other CTAs wrote during the same launch).
+template <int kRows, int kChunk, bool kL2 = false, class PartFn>
 __device__ __forceinline__ void fold_rows(Fold (&f)[kRows], int nrows, int nparts,
                                           PartFn part) {
   for (int i0 = 0; i0 < nparts; i0 += kChunk) {
@@ -89,8 +90,8 @@ __device__ __forceinline__ void fold_rows(Fold (&f)[kRows], int nrows, int npart
           const float2* ml;
           const float4* o;
           part(i, k, ml, o);
-          v[k][c] = *ml;
-          x[k][c] = *o;
+          v[k][c] = kL2 ? __ldcg(ml) : *ml;
+          x[k][c] = kL2 ? __ldcg(o) : *o;
         }
       }
     }

@@ -37,6 +37,8 @@ struct DecodeParams {
   int q_len;                   // new tokens per sequence (1: single-token decode)
   int beta;                    // tcgen05 kernel: ranges are cut in an order where every
                                //   non-empty KV head adds beta units after its tiles
+  unsigned long long* fix_ctr; // [B, Hkv] counters of the in-kernel stream-K fixup
+  int fixup;                   // fold cut units in the decode kernel (no merge kernel)
   int late_wait;               // wait for the previous grid only before exiting (cascade
                                //   suffix running beside the prefix kernel)
   int tma_out;                 // tcgen05 kernel: whole heads leave through TMA tensor stores
@@ -156,6 +158,7 @@ struct DecodeKernelInfo {
   int blk;           // physical blocks per work item (2: pairs of 16-token blocks)
   int tc;            // 1: the tcgen05 kernel (decode_tc.cu): one CTA per SM, all rows of a
                      //    KV head per MMA, warp_smem = fixed shared memory per CTA
+  int fixup;         // 1: can fold cut units itself (DecodeParams::fixup)
 };
 
 // Kernel tables, one per translation unit. Return false if the shape is not built.

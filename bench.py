@@ -386,7 +386,10 @@ def run_ours(args, rank, world):
     # No events sit between the kernels: append, decode and merge chain with
     # programmatic dependent launch exactly as in a user's stream.
     K = args.steps
+    lib = pk.pagedkv.load_library()
+    launches0 = lib.pkv_kernel_launch_count()
     step_graph = capture(K, lambda: (append(), decode()), dev)
+    step_launches = lib.pkv_kernel_launch_count() - launches0   # kernels in the K steps
     step_graph.replay()                 # upload + warm replay (untimed)
     torch.cuda.synchronize(dev)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -403,7 +406,9 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize(dev)
     # roofline of the dominant call: K back-to-back decode calls (decode + merge
     # kernels) in a second timed region, CUDA events on the launching stream
+    launches0 = lib.pkv_kernel_launch_count()
     dec_graph = capture(K, decode, dev)
+    dec_launches = (lib.pkv_kernel_launch_count() - launches0) // K
     dec_graph.replay()
     torch.cuda.synchronize(dev)
     d_start, d_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -456,17 +461,32 @@ def run_ours(args, rank, world):
                      "traffic": measured_traffic(args.config),
                      "traffic_source": "profiles/decode_traffic.txt (ncu dram bytes read+write, "
                                        "decode + merge kernels, one call)",
-                     "kernel": "paged_decode_kernel + paged_decode_merge_kernel (one decode call)",
+                     "kernel": decode_kernels(w, cascade_blocks, dec_launches),
+                     "launches_per_call": dec_launches,
                      "bytes_per_launch": db["total"], "avg_launch_ms": round(dec_ms, 5),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "timing": dec_how},
-        "gpu_launches": (4 if cascade_blocks else 3) * K,
+        "gpu_launches": step_launches,
         "clocks": clk,
     }
     if e2e is not None:
         result["e2e"] = e2e
     return result, w
+
+
+def decode_kernels(w, cascade_blocks, launches):
+    """Names of the kernels one decode call launches (for the roofline record)."""
+    if cascade_blocks:
+        return "paged_prefix_kernel + paged_decode_kernel + paged_cascade_merge_kernel"
+    rows = w.q_len * w.num_q_heads // w.num_kv_heads        # query rows per KV head
+    main = "paged_decode_tc_kernel" if (w.q_len > 1 and 48 <= rows <= 128) else \
+        "paged_decode_kernel"
+    if launches == 1:
+        return main + " (split-KV parts folded inside the kernel, one launch per call)"
+    merge = "paged_tc_merge_kernel" if main == "paged_decode_tc_kernel" else \
+        "paged_decode_merge_kernel"
+    return f"{main} + {merge} (one decode call)"
 
 
 def run_blocks(args, rank, world):

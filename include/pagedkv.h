@@ -90,6 +90,14 @@ const char* pkv_status_string(pkv_status status);
 /* Library version as major*10000 + minor*100 + patch. */
 int pkv_version(void);
 
+/* Number of kernels this library has launched (or recorded into a CUDA graph being
+ * captured) in this process since it was loaded, all devices and threads together.
+ * Read it before and after a call to learn how many kernels the call launched. A
+ * launch that fails is not counted. Host-side counter only: it never touches a
+ * device. No counterpart on the pages; it exists to count the kernels of a timed
+ * region. */
+uint64_t pkv_kernel_launch_count(void);
+
 /*
  * pkv_append_bf16 -- write each new token's K and V rows into its cache slot.
  * Block manager of the chenk.top page ("块管理器：分页如何运作"): a growing request

@@ -12,6 +12,8 @@
 #include "pagedkv.h"
 
 namespace pkv {
+
+std::atomic<unsigned long long> g_kernel_launches{0};
 namespace {
 
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per shared-memory copy wait
@@ -676,6 +678,10 @@ const char* pkv_status_string(pkv_status s) {
 }
 
 int pkv_version(void) { return 100; }
+
+uint64_t pkv_kernel_launch_count(void) {
+  return g_kernel_launches.load(std::memory_order_relaxed);
+}
 
 pkv_status pkv_append_bf16(const void* k, const void* v, void* k_cache, void* v_cache,
                            const int64_t* slot_mapping, int32_t num_tokens,

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <atomic>
 
 #include "pagedkv.h"
 
@@ -184,6 +185,10 @@ bool select_decode_e5m2(int D, int BS, int simt_heads, DecodeKernelInfo* info,
 // the previous kernel on the stream drains; every kernel of this library waits for its
 // predecessor (griddepcontrol.wait) before touching global memory, so results are
 // the same as with plain stream ordering.
+// Kernels this library has launched in this process (launch_pdl is the only launch
+// site); read through pkv_kernel_launch_count.
+extern std::atomic<unsigned long long> g_kernel_launches;
+
 inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, size_t smem,
                               cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -196,7 +201,9 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelExC(&cfg, fn, args);
+  cudaError_t err = cudaLaunchKernelExC(&cfg, fn, args);
+  if (err == cudaSuccess) g_kernel_launches.fetch_add(1, std::memory_order_relaxed);
+  return err;
 }
 
 cudaError_t launch_append_bf16(const void* k, const void* v, void* k_cache, void* v_cache,

@@ -66,6 +66,7 @@ class Dims(ctypes.Structure):
 EXPORTS = {
     "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_version": (ctypes.c_int, []),
+    "pkv_kernel_launch_count": (ctypes.c_uint64, []),
     "pkv_append_bf16": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int32, ctypes.c_void_p,
                                                                 ctypes.c_void_p]),
     "pkv_append_int8": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int32, ctypes.c_void_p,

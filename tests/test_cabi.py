@@ -60,6 +60,7 @@ def test_host_validation_without_gpu(lib_path):
     """Each failing check returns before any CUDA call, so these run on a CPU machine."""
     from paged_kv_decode_02_gb300 import pagedkv
     lib = pagedkv.load_library(lib_path)
+    launches_before = lib.pkv_kernel_launch_count()
     good = pagedkv.Dims(4, 8, 8, 64, 16, 64, 4)
     p = ctypes.c_void_p(0x1000)
     st = lib.pkv_decode_bf16(None, p, p, p, p, p, 0.1, ctypes.byref(good), p, 1 << 20, None, None)
@@ -126,3 +127,5 @@ def test_host_validation_without_gpu(lib_path):
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 7, ctypes.byref(n)) == \
         pagedkv.Status.ERR_DTYPE
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 0, None) == pagedkv.Status.ERR_NULL
+    # nothing above reached a launch
+    assert lib.pkv_kernel_launch_count() == launches_before

@@ -250,6 +250,8 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
     return PKV_ERR_CUDA;
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, P.k.fn) != cudaSuccess) return PKV_ERR_CUDA;
+  // tcgen05 kernel: every CTA's range start, [grid + 1] (grid <= SMs)
+  if (P.k.tc) P.smem += size_t(8) * (sms + 1);
   const size_t max_dyn = size_t(optin) - fa.sharedSizeBytes;
   if (P.smem > max_dyn) return PKV_ERR_UNSUPPORTED;  // batch too large for one CTA's table
   // the attribute is an upper bound only: set it to the most any batch size may need,
@@ -323,7 +325,11 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   p.fix_ctr = reinterpret_cast<unsigned long long*>(ws + P.off_ctr);
   // single-token decode without a status word folds its cut units in the decode
   // kernel (the last warp to finish a unit); otherwise the merge kernel does
-  p.fixup = (P.k.fixup && q_len == 1 && P.nsg == 1 && status == nullptr) ? 1 : 0;
+  // (the tcgen05 kernel: every call without a status word whose fold weights, one per
+  // part and row with at most one part per CTA, fit its six idle tile buffers)
+  const bool tc_fold = P.k.tc && P.grid <= 1024 && size_t(8192) + size_t(4) * P.grid * P.gs <=
+                                     size_t(6) * (d->head_dim / 64) * 128 * 128;
+  p.fixup = ((P.k.fixup && q_len == 1 && P.nsg == 1) || tc_fold) && status == nullptr ? 1 : 0;
   p.status = status;
   p.B = d->num_seqs;
   p.Hq = d->num_q_heads;
@@ -377,25 +383,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   m.W = P.W / P.nsg;  // workers of nsg warps
   m.beta = p.beta;
   m.wprefix = p.prefix_out + (d->num_seqs + 1);
-  if (P.k.tc && status == nullptr && P.grid <= 1024) {
-    // at most one cut head per CTA boundary: merge those and zero empty sequences
-    TcMergeParams t{};
-    t.out = out;
-    t.part_o = p.part_o;
-    t.part_ml = p.part_ml;
-    t.prefix = p.prefix_out;
-    t.ranges = p.range_out;
-    t.B = p.B;
-    t.Hq = p.Hq;
-    t.Hkv = p.Hkv;
-    t.D = d->head_dim;
-    t.q_len = q_len;
-    t.g = P.g;
-    t.R = P.gs;
-    launch_tc_merge(t, P.grid, stream);
-  } else if (!p.fixup) {
-    launch_merge(m, stream);
-  }
+  if (!p.fixup) launch_merge(m, stream);  // else cut units were folded in the kernel
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   return PKV_OK;
 }

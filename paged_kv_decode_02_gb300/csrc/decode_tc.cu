@@ -59,21 +59,28 @@ struct TcDecode {
   static constexpr int kOffQ = 0;              // Q x2 (segment parity)
   static constexpr int kOffK = kOffQ + 2 * kTile;
   static constexpr int kOffV = kOffK + 2 * kTile;
-  static constexpr int kOffBar = kOffV + 2 * kTile;
+  // all-ones B operand (16 x 128 tokens, K-major) of the MMA that sums the rows of P
+  static constexpr int kOffOnes = kOffV + 2 * kTile;
+  static constexpr int kOffBar = kOffOnes + 4096;
   // mbarriers: kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] pfull ofull mdone qfull[2] ofree
   static constexpr int kNumBars = 16;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
+  // [2] cut segments of this CTA (first, last) for the tail fixup: s, h, n, tiles, state
+  static constexpr int kOffCut = kOffAbort + 12;
   // [B+1] tile prefix, [B+1] weighted prefix (tiles + beta per non-empty sequence),
   // [B] clamped lengths
-  static constexpr int kOffTables = kOffAbort + 12;
-  static constexpr int kFixedSmem = kOffTables + 1024;  // + 12 * (B + 1) at run time
+  static constexpr int kOffTables = kOffCut + 48;
+  // + 8 * (grid + 1) + 12 * (B + 1) at run time
+  static constexpr int kFixedSmem = kOffTables + 1024;
   static constexpr int kThreads = 224;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kColS = 0, kColO = 2 * kN, kColP = 2 * kN + 128;
-  static_assert(kColP + kN / 2 <= int(kTmemCols) && kColO + D <= kColP, "TMEM columns");
+  // S x2, O, P (bf16 pairs), l (row sums of P, fp32; 16 columns written by its MMA)
+  static constexpr int kColS = 0, kColO = 2 * kN, kColP = 2 * kN + 128, kColL = kColP + kN / 2;
+  static_assert(kColL + 16 <= int(kTmemCols) && kColO + D <= kColP, "TMEM columns");
+  static_assert(kOffOnes % 1024 == 0, "swizzle atom alignment");
   static_assert(kN % BS == 0 && D % 64 == 0 && kSlab == kM * 128, "tile shape");
-  static_assert(kOffTables % 16 == 0, "table alignment");
+  static_assert(kOffTables % 16 == 0 && kOffCut % 16 == 0, "table alignment");
 };
 
 // Position in the flat (sequence, KV head, tile) order.
@@ -104,6 +111,171 @@ __device__ __forceinline__ void tile_next(TileCursor& c, const int* prefix, int 
   c.n = c.s < B ? prefix[c.s + 1] - prefix[c.s] : 0;
 }
 
+// Tiles of the flat (sequence, KV head, tile) order before weighted position x. Ranges
+// are equal cuts of a weighted order in which KV head (s, h) takes tiles_s + beta
+// positions (its tiles, then beta for the cost of ending a head); a range covers the
+// tiles whose positions fall in it. prefix / wprefix: exclusive prefixes of the tiles
+// and of the weights per sequence.
+__device__ __forceinline__ long long tc_tiles_before(long long x, const int* prefix,
+                                                     const int* wprefix, int B, int Hkv,
+                                                     int beta) {
+  if (x >= (long long)Hkv * wprefix[B]) return (long long)Hkv * prefix[B];
+  int lo = 0, hi = B;  // Hkv*wprefix[lo] <= x < Hkv*wprefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((long long)Hkv * wprefix[mid] <= x) lo = mid; else hi = mid;
+  }
+  const int n = prefix[lo + 1] - prefix[lo];
+  const long long rem = x - (long long)Hkv * wprefix[lo];
+  const long long h = rem / (n + beta), o = rem % (n + beta);
+  return (long long)Hkv * prefix[lo] + h * n + min(o, (long long)n);
+}
+
+// Stream-K fixup at the end of a CTA (no merge kernel follows). A KV head is cut only
+// where a range ends inside it, so a CTA holds at most two cut segments (its first and
+// its last), whose unnormalised (o, m, l) records are in slots 2c and 2c + 1. After its
+// last tile the CTA fences its records and adds the tiles of each cut segment to the
+// head's counter; the CTA whose addition completes the head's n tiles folds every part
+// of it with the online-softmax rescaling, all threads together: first per row the
+// largest m, l = sum 2^(m_i - m) l_i and each part's weight 2^(m_i - m) / l (in the
+// idle Q, K and V tile buffers: 8 KiB + 4 * parts * rows bytes), then per 16-byte
+// output quad the weighted sum of the parts' o.
+// The parts are the segments of the CTAs whose ranges hold the head's tiles: the first
+// one's last segment (its first when its range starts at the head), then the first
+// segments of the CTAs whose non-empty ranges start inside the head. A counter word
+// holds a launch tag (low 40 bits of the grid's launch number) over a 24-bit tile
+// count: a word with another tag counts as zero, so the workspace needs no clearing,
+// and the completing CTA resets it. Writers fence their records before the counter
+// update, the completing CTA fences after it and reads the records through L2.
+template <int D>
+__device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* s_prefix,
+                                              const long long* s_rs, volatile int* cut,
+                                              uint8_t* scratch, int nthreads) {
+  const int tid = threadIdx.x, C = gridDim.x, R = p.gs, Hkv = p.Hkv;
+  if (!(cut[4] | cut[9])) return;  // no cut segment (uniform: shared memory after a barrier)
+  __threadfence();                 // this thread's records, device-wide
+  __syncthreads();
+  if (tid < 2 && cut[5 * tid + 4]) {
+    volatile int* e = cut + 5 * tid;
+    const int s = e[0], h = e[1], n = e[2], mine = e[3];
+    const unsigned long long tag = grid_launch_id() & ((1ull << 40) - 1ull);
+    unsigned long long* ctr = p.fix_ctr + size_t(s) * Hkv + h;
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    int last = 0;
+    for (;;) {
+      const unsigned long long base = (cur >> 24) == tag ? (cur & 0xffffffull) : 0ull;
+      const unsigned long long want = (tag << 24) | (base + unsigned(mine));
+      const unsigned long long seen = atomicCAS(ctr, cur, want);
+      if (seen == cur) {
+        last = int(base) + mine == n;
+        break;
+      }
+      cur = seen;
+    }
+    if (last) atomicExch(ctr, 0ull);
+    e[4] = last ? 2 : 0;
+  }
+  __syncthreads();
+  int* parts = reinterpret_cast<int*>(scratch);          // [C] part slots
+  volatile int* s_np = parts + 1024;                      // part count
+  float* wts = reinterpret_cast<float*>(scratch + 8192);  // [parts][R] weights
+  constexpr int Q = D / 4;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  const float4* po = reinterpret_cast<const float4*>(p.part_o);
+  __nv_bfloat16* outb = reinterpret_cast<__nv_bfloat16*>(p.out);
+  for (int ei = 0; ei < 2; ++ei) {
+    if (cut[5 * ei + 4] != 2) continue;
+    __threadfence();
+    const int s = cut[5 * ei], h = cut[5 * ei + 1], n = cut[5 * ei + 2];
+    if (tid == 0) {  // the parts: slots of the CTAs whose ranges hold tiles [u0, u1)
+      const long long u0 = (long long)Hkv * s_prefix[s] + (long long)h * n, u1 = u0 + n;
+      int lo = 0, hi = C;  // s_rs[lo] <= u0 < s_rs[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_rs[mid] <= u0) lo = mid; else hi = mid;
+      }
+      int np = 0;
+      parts[np++] = 2 * lo + (s_rs[lo] < u0 ? 1 : 0);
+      for (int c2 = lo + 1; c2 < C && s_rs[c2] < u1; ++c2)
+        if (s_rs[c2 + 1] > s_rs[c2]) parts[np++] = 2 * c2;
+      *s_np = np;
+    }
+    __syncthreads();
+    const int np = *s_np;
+    // per row: the largest m, l and every part's weight
+    for (int r = tid; r < R; r += nthreads) {
+      float M = -INFINITY, L = 0.f;
+      for (int i0 = 0; i0 < np; i0 += 8) {
+        float2 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          v[k] = i0 + k < np ? __ldcg(ml + size_t(parts[i0 + k]) * R + r)
+                             : make_float2(-INFINITY, 0.f);
+        float cm = v[0].x;
+#pragma unroll
+        for (int k = 1; k < 8; ++k) cm = fmaxf(cm, v[k].x);
+        if (cm > M) {
+          L *= fast_exp2(M - cm);  // 0 while nothing was folded in
+          M = cm;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (i0 + k < np) wts[(i0 + k) * R + r] = v[k].x;
+          if (v[k].x > -INFINITY) L = fmaf(fast_exp2(v[k].x - M), v[k].y, L);
+        }
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int i = 0; i < np; ++i) {
+        const float m = wts[i * R + r];
+        wts[i * R + r] = m > -INFINITY ? fast_exp2(m - M) * inv : 0.f;
+      }
+    }
+    __syncthreads();
+    // per output quad: the weighted sum of the parts, 8 quads per thread at a time with
+    // the loads of two parts in flight together
+    const int items = R * Q;
+    for (int k0 = tid; k0 < items; k0 += 8 * nthreads) {
+      float4 acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i0 = 0; i0 < np; i0 += 2) {
+        float4 x[8][2];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int k = k0 + j * nthreads, r = k / Q, dq = k % Q;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2)
+            x[j][c2] = (k < items && i0 + c2 < np)
+                           ? __ldcg(po + (size_t(parts[i0 + c2]) * R + r) * Q + dq)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int k = k0 + j * nthreads, r = min(k / Q, R - 1);
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const float w = i0 + c2 < np ? wts[(i0 + c2) * R + r] : 0.f;
+            acc[j].x = fmaf(w, x[j][c2].x, acc[j].x);
+            acc[j].y = fmaf(w, x[j][c2].y, acc[j].y);
+            acc[j].z = fmaf(w, x[j][c2].z, acc[j].z);
+            acc[j].w = fmaf(w, x[j][c2].w, acc[j].w);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int k = k0 + j * nthreads;
+        if (k >= items) break;
+        const int r = k / Q, dq = k % Q;
+        const size_t orow = (size_t(s) * p.q_len + r / p.g) * p.Hq + size_t(h) * p.g + r % p.g;
+        reinterpret_cast<uint2*>(outb + orow * D)[dq] =
+            make_uint2(pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j].z, acc[j].w));
+      }
+    }
+    __syncthreads();  // the scratch of the next entry
+  }
+}
+
 template <int D, int BS>
 __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
@@ -115,7 +287,10 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + K::kOffAbort);
-  int* s_prefix = reinterpret_cast<int*>(gbase + K::kOffTables);
+  // [grid + 1] first tile of every CTA's range, then the per-sequence tables
+  long long* s_rs = reinterpret_cast<long long*>(gbase + K::kOffTables);
+  int* s_prefix = reinterpret_cast<int*>(s_rs + gridDim.x + 1);
+  volatile int* s_cut = reinterpret_cast<volatile int*>(gbase + K::kOffCut);
   const int B = p.B, Hkv = p.Hkv, beta = p.beta;
   int* s_wpre = s_prefix + (B + 1);
   int* s_len = s_wpre + (B + 1);
@@ -140,9 +315,14 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
     mbar_init(qfull(1), 4 * 32);
     mbar_init(ofree, 4 * 32);
     *abort_flag = 0;
+    s_cut[4] = s_cut[9] = 0;
     fence_mbar_init();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, K::kTmemCols);
+  for (int k = tid; k < 4096 / 16; k += K::kThreads)  // bf16 1.0 everywhere
+    tc::sts128(base + K::kOffOnes + 16 * k,
+               make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u));
+  fence_proxy_async_smem();  // for the MMAs that read it
 
   // ---- tiles per sequence, their exclusive prefix, the weighted prefix (tiles plus
   //      beta per non-empty sequence), clamped lengths (every CTA) ----
@@ -195,27 +375,26 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
       p.prefix_out[i] = s_prefix[i];
       p.prefix_out[B + 1 + i] = s_wpre[i];
     }
+  if (p.fixup)  // no merge kernel follows: sequences without a tile get zeros here
+    for (int s2 = blockIdx.x; s2 < B; s2 += gridDim.x) {
+      if (s_prefix[s2 + 1] != s_prefix[s2]) continue;
+      const int chunks = p.q_len * p.Hq * (D / 8);
+      uint4* o = reinterpret_cast<uint4*>(p.out) + size_t(s2) * chunks;
+      for (int k = tid; k < chunks; k += K::kThreads) o[k] = make_uint4(0u, 0u, 0u, 0u);
+    }
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + K::kOffTmemSlot);
 
   // This CTA's tiles. Ranges are equal cuts of the weighted order, in which KV head
   // (s, h) takes tiles_s + beta positions (its tiles, then beta for the cost of ending
   // a head); a range covers the tiles whose positions fall in it. Tiles before
   // weighted position x:
-  auto tiles_before = [&](long long x) -> long long {
-    if (x >= (long long)Hkv * s_wpre[B]) return (long long)Hkv * s_prefix[B];
-    int lo = 0, hi = B;  // Hkv*s_wpre[lo] <= x < Hkv*s_wpre[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if ((long long)Hkv * s_wpre[mid] <= x) lo = mid; else hi = mid;
-    }
-    const int n = s_prefix[lo + 1] - s_prefix[lo];
-    const long long rem = x - (long long)Hkv * s_wpre[lo];
-    const long long h = rem / (n + beta), o = rem % (n + beta);
-    return (long long)Hkv * s_prefix[lo] + h * n + min(o, (long long)n);
-  };
+  // every CTA's range start (equal cuts of the weighted order), all threads at once
   const long long TW = (long long)Hkv * s_wpre[B];
   const int C = gridDim.x, c = blockIdx.x;
-  const long long ra = tiles_before(TW * c / C), rb = tiles_before(TW * (c + 1) / C);
+  for (int c2 = tid; c2 <= C; c2 += K::kThreads)
+    s_rs[c2] = tc_tiles_before(TW * c2 / C, s_prefix, s_wpre, B, Hkv, beta);
+  __syncthreads();
+  const long long ra = s_rs[c], rb = s_rs[c + 1];
   const int cnt = int(rb - ra);
   const int R = p.gs;  // query rows per KV head (q_len * g)
   if (tid == 0 && p.range_out) {  // for the merge: where this range starts
@@ -279,6 +458,8 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_bf16<128, K::kN, false>();
       constexpr uint32_t kIdO = tc::idesc_bf16<128, D, true>();
+      constexpr uint32_t kIdL = tc::idesc_bf16<128, 16, false>();
+      const uint32_t ones = base + K::kOffOnes;
       auto issue_s = [&](int i, int qb) -> bool {
         const int st = i & 1;
         if (!tc::wait_or_abort(kfull(st), uint32_t(i >> 1) & 1u, p.timeout_ns, abort_flag))
@@ -309,10 +490,15 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
         tc::fence_after_sync();
         const uint32_t vb = base + K::kOffV + st * K::kTile;
 #pragma unroll
-        for (int kk = 0; kk < K::kN / 16; ++kk)
+        for (int kk = 0; kk < K::kN / 16; ++kk) {
           tc::mma_bf16_tmem_a(tmem + K::kColO, tmem + K::kColP + kk * 8,
                               tc::sdesc_sw128(vb + kk * 16 * 128, K::kSlab, 1024), kIdO,
                               (!seg_first || kk > 0) ? 1u : 0u);
+          // the row sums of the bf16 weights this P.V used, next to O (same rescaling)
+          tc::mma_bf16_tmem_a(tmem + K::kColL, tmem + K::kColP + kk * 8,
+                              tc::sdesc_sw128(ones + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024),
+                              kIdL, (!seg_first || kk > 0) ? 1u : 0u);
+        }
         tc::commit(vempty(st));
         tc::commit(ofull);
         return true;
@@ -399,7 +585,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
       fence_proxy_async_smem();
       return true;
     };
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY;
     int seg = 0, seg_j0 = cur.j, seg_tile = 0;
     bool ok = true;
     prefetch_q(cur, 0);
@@ -469,42 +655,41 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
         for (int t = 0; t < K::kN; ++t)
           if (t >= vis) s[t] = 0xff800000u;  // -inf
       }
+      // tile maximum: three-input max over eight independent chains
       float mx[8];
 #pragma unroll
-      for (int t = 0; t < K::kN; ++t)
-        mx[t & 7] = (t < 8) ? __uint_as_float(s[t]) : fmaxf(mx[t & 7], __uint_as_float(s[t]));
-      const float mt = asl * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int j = 0; j < 8; ++j) mx[j] = __uint_as_float(s[j]);
+#pragma unroll
+      for (int u = 0; u < (K::kN - 8) / 2; ++u)
+        mx[u & 7] = fmax3(mx[u & 7], __uint_as_float(s[8 + 2 * u]), __uint_as_float(s[9 + 2 * u]));
+      const float mt = asl * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                   fmaxf(mx[6], mx[7]));
       float alpha = 1.f;
       bool rescale = false;
       if (vis > 0 && mt > m_ref + 8.f) {
         alpha = fast_exp2(m_ref - mt);  // 0 while the row has seen nothing
         m_ref = mt;
-        l *= alpha;
         rescale = seg_tile > 0;
       }
+      // weights 2^(scale * s - m) (packed fp32x2 FMAs), bf16 pairs; their row sums come
+      // from the tensor cores (P times a ones tile, beside P.V)
       uint32_t pk[K::kN / 2];
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
-      const float nm = -m_ref;
+      const float2 asl2 = make_float2(asl, asl), nm2 = make_float2(-m_ref, -m_ref);
       if (full) {
 #pragma unroll
         for (int t = 0; t < K::kN; t += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(s[t]), asl, nm));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(s[t + 1]), asl, nm));
-          sm[(t >> 1) & 3] += p0 + p1;
-          pk[t / 2] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
+                                      asl2, nm2);
+          pk[t / 2] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
         }
       } else {
 #pragma unroll
         for (int t = 0; t < K::kN; t += 2) {
-          const float p0 = t < vis ? fast_exp2(fmaf(__uint_as_float(s[t]), asl, nm)) : 0.f;
-          const float p1 =
-              t + 1 < vis ? fast_exp2(fmaf(__uint_as_float(s[t + 1]), asl, nm)) : 0.f;
-          sm[(t >> 1) & 3] += p0 + p1;
-          pk[t / 2] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
+                                      asl2, nm2);
+          pk[t / 2] = pack_bf16x2(t < vis ? fast_exp2(x.x) : 0.f, t + 1 < vis ? fast_exp2(x.y) : 0.f);
         }
       }
-      l += (sm[0] + sm[1]) + (sm[2] + sm[3]);
       if (!zero_v_tail(i, L, t0)) {
         ok = false;
         break;
@@ -525,6 +710,8 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tc::tmem_st32(trow + K::kColO + c2, o);
         }
+        tc::tmem_st1(trow + K::kColL,
+                     __float_as_uint(__uint_as_float(tc::tmem_ld1(trow + K::kColL)) * alpha));
       }
 #pragma unroll
       for (int c2 = 0; c2 < K::kN / 2; c2 += 32) {
@@ -549,6 +736,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
         tc::fence_after_sync();
         const bool whole = seg_j0 == 0 && cur.j == cur.n - 1;
         const size_t slot = size_t(2 * c + (seg == 0 ? 0 : 1));
+        const float l = __uint_as_float(tc::tmem_ld1(trow + K::kColL));  // sum of the weights
         const float inv = l > 0.f ? 1.f / l : 0.f;
         if (whole) {
           // the bf16 rows go through this segment's Q buffer (its MMAs are complete),
@@ -624,11 +812,18 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
         }
         if (row_ok && !whole)
           reinterpret_cast<float2*>(p.part_ml)[slot * R + r] = make_float2(m_ref, l);
+        if (!whole && p.fixup && quarter == 0 && lane == 0) {  // for the tail fixup
+          volatile int* e = s_cut + 5 * int(slot & 1);
+          e[0] = cur.s;
+          e[1] = cur.h;
+          e[2] = cur.n;
+          e[3] = cur.j - seg_j0 + 1;
+          e[4] = 1;
+        }
         tc::fence_before_sync();
         mbar_arrive(ofree);
         ++seg;
         m_ref = -INFINITY;
-        l = 0.f;
       }
       tile_next(cur, s_prefix, B, Hkv);
     }
@@ -643,6 +838,10 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, K::kTmemCols);
   }
+  // cut heads this CTA completes (the tile buffers are idle: every copy has landed,
+  // every MMA and output store has completed)
+  if (p.fixup && !*abort_flag) tc_tail_fixup<D>(p, s_prefix, s_rs, s_cut, gbase + K::kOffQ,
+                                                K::kThreads);
 }
 
 template <int D, int BS>

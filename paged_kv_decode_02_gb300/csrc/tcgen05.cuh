@@ -151,6 +151,27 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
       : "memory");
 }
 
+// 1 x tcgen05.ld 32x32b.x1 (column col of this warp's 32 lanes), waited for.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r)
+      : "r"(taddr)
+      : "memory");
+  return r;
+}
+
+// tcgen05.st 32x32b.x1 (column col of this warp's 32 lanes), then tcgen05.wait::st.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(v)
+      : "memory");
+}
+
 // tcgen05.st 32x32b.x32: columns col .. col+31 of this warp's 32 lanes, then
 // tcgen05.wait::st.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {

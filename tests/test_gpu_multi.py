@@ -149,3 +149,67 @@ def test_multi_rejects_bad_query_length(pk):
     with pytest.raises(pk.PagedKVError):
         pk.paged_decode_attention_multi(q, w.k_cache, w.v_cache, w.block_tables,
                                         w.context_lens, w.scale)
+
+
+# tcgen05 kernel (q_len * g query rows per KV head in 48..128): a head of 157 tiles cut
+# over most CTAs, an empty sequence, fewer tiles than CTAs; two-token windows (new
+# token 0 of a 9-token context) where the bf16 weights must be normalised by their own
+# sum to stay inside the tolerance
+TC_CASES = {
+    "tc-64rows-long": dict(num_q_heads=16, num_kv_heads=2, q_len=8, lengths=[20000, 9, 300]),
+    "tc-128rows-empty": dict(num_q_heads=16, num_kv_heads=2, q_len=16,
+                             lengths=[3000, 0, 16, 1200]),
+    "tc-48rows-sparse": dict(num_q_heads=16, num_kv_heads=2, q_len=6, lengths=[600, 6, 130]),
+}
+
+
+def _tc_workspace(pk, w, fill):
+    n = pk.multi_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                 w.block_size, w.num_blocks, w.block_tables.shape[1], w.q_len)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=DEV)
+    if fill == "ones":
+        ws.fill_(0xFF)
+    else:
+        gen = torch.Generator(device=DEV).manual_seed(12)
+        ws.copy_(torch.randint(0, 256, ws.shape, generator=gen, device=DEV, dtype=torch.int32)
+                 .to(torch.uint8))
+    return ws
+
+
+@pytest.mark.parametrize("case", sorted(TC_CASES))
+@pytest.mark.parametrize("fill", ["ones", "random"])
+def test_tc_garbage_workspace_and_repeats(pk, case, fill):
+    w = make_workload("spec-70b", device=DEV, seed=21, poison_unused=True, **TC_CASES[case])
+    ref = oracle_outputs_multi(w)
+    ws = _tc_workspace(pk, w, fill)
+    out = torch.empty_like(w.q)
+    for _ in range(3):  # one workspace for every call, never cleared
+        out.fill_(float("nan"))
+        _run(pk, w, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        assert _err(out, ref) <= DECODE_ATOL
+
+
+def test_tc_graph_replays(pk):
+    w = make_workload("spec-70b", device=DEV, seed=22, **TC_CASES["tc-64rows-long"])
+    ws = _tc_workspace(pk, w, "random")
+    out = torch.empty_like(w.q)
+    q = w.q.clone()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):  # warm-up outside the capture
+        pk.paged_decode_attention_multi(q, w.k_cache, w.v_cache, w.block_tables,
+                                        w.context_lens, w.scale, out=out, workspace=ws)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        pk.paged_decode_attention_multi(q, w.k_cache, w.v_cache, w.block_tables,
+                                        w.context_lens, w.scale, out=out, workspace=ws)
+    gen = torch.Generator(device=DEV).manual_seed(6)
+    for _ in range(3):
+        q.copy_(torch.randn(q.shape, generator=gen, device=DEV).to(q.dtype))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        w.q = q.clone()
+        assert _err(out, oracle_outputs_multi(w)) <= DECODE_ATOL

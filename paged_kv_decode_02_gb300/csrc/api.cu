@@ -114,7 +114,7 @@ struct Plan {
   int g, gs, nsg, HU;
   int grid, W;
   size_t smem;
-  size_t off_prefix, off_rng, off_ctr, off_ml, off_o, ws_bytes;
+  size_t off_prefix, off_ctr, off_ml, off_o, ws_bytes;
 };
 
 pkv_status check_dims(const pkv_dims* d) {
@@ -271,9 +271,9 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
 
   // workspace: [prefix (B+1) int32][partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
   P.off_prefix = 0;  // [B+1] work prefix, then [B+1] weighted prefix (tcgen05 kernel)
-  P.off_rng = align_up(size_t(d->num_seqs + 1) * 8, 256);  // tcgen05: [grid] range starts
-  // [B, Hkv] counters of the in-kernel stream-K fixup (single-token decode)
-  P.off_ctr = align_up(P.off_rng + (P.k.tc ? size_t(P.grid) * sizeof(TcRange) : 0), 256);
+  // [B, Hkv] counters of the in-kernel stream-K fixups (single-token decode; the
+  // tcgen05 kernel, one per KV head)
+  P.off_ctr = align_up(size_t(d->num_seqs + 1) * 8, 256);
   P.off_ml = align_up(P.off_ctr + size_t(d->num_seqs) * d->num_kv_heads * 8, 256);
   P.off_o = align_up(P.off_ml + size_t(2) * P.W * P.gs * 8, 256);
   P.ws_bytes = align_up(P.off_o + size_t(2) * P.W * P.gs * d->head_dim * 4, 256);
@@ -321,7 +321,6 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   p.part_o = reinterpret_cast<float*>(ws + P.off_o);
   p.part_ml = reinterpret_cast<float*>(ws + P.off_ml);
   p.prefix_out = reinterpret_cast<int32_t*>(ws + P.off_prefix);
-  p.range_out = P.k.tc ? reinterpret_cast<TcRange*>(ws + P.off_rng) : nullptr;
   p.fix_ctr = reinterpret_cast<unsigned long long*>(ws + P.off_ctr);
   // single-token decode without a status word folds its cut units in the decode
   // kernel (the last warp to finish a unit); otherwise the merge kernel does

@@ -13,21 +13,25 @@
 // one contiguous range per CTA (one CTA per SM). Within a range the tiles of one KV
 // head form a segment; a segment covering the whole head writes the output, a cut
 // one (only a range's first and last can be) leaves an unnormalised (o, m, l) record
-// per row in the slots the split-KV merge kernel reads (slot 2c for the first segment
-// of CTA c, 2c + 1 for the last).
+// per row in slot 2c (the first segment of CTA c) or 2c + 1 (the last). Without a
+// status word the CTA that completes a cut head folds its records at its end
+// (tc_tail_fixup); with one, the split-KV merge kernel validates and folds.
 // Roles per CTA (224 threads), as in the cascade prefix kernel:
 //   warp 0 / warp 6: TMA copies of the K / V tiles into two-stage rings (one box per
 //                    16- or 32-token block and 64-column slab, lane b copies block b;
 //                    block ids are read one tile ahead);
 //   warp 1:          TMEM allocation; one thread issues every MMA:
-//                    S_t = Q K_t^T (fp32, two TMEM buffers), O += P_t V_t (A = P in TMEM);
+//                    S_t = Q K_t^T (fp32, two TMEM buffers), O += P_t V_t (A = P in TMEM)
+//                    and l += P_t 1 (the row sums of the bf16 weights, P times a ones
+//                    tile in shared memory), so the normalisation uses exactly the
+//                    weights P.V used and the softmax warps add nothing up;
 //   warps 2..5:      one query row per thread: Q rows of each segment into shared
 //                    memory, softmax with the causal and context masks, P to TMEM,
-//                    the segment's epilogue from O in TMEM.
+//                    the segment's epilogue from O and l in TMEM.
 // The softmax keeps a reference maximum per row that moves only when a tile's maximum
-// exceeds it by more than 8 (log2 units); O is then rescaled in TMEM before the next
-// P.V. Every wait is bounded: on a timeout the CTA sets a status bit, lets its copies
-// and MMAs complete, frees its TMEM and leaves.
+// exceeds it by more than 8 (log2 units); O and l are then rescaled in TMEM before the
+// next P.V. Every wait is bounded: on a timeout the CTA sets a status bit, lets its
+// copies and MMAs complete, frees its TMEM and leaves.
 #include "decode.cuh"
 #include "fold.cuh"
 #include "tcgen05.cuh"
@@ -397,18 +401,6 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
   const long long ra = s_rs[c], rb = s_rs[c + 1];
   const int cnt = int(rb - ra);
   const int R = p.gs;  // query rows per KV head (q_len * g)
-  if (tid == 0 && p.range_out) {  // for the merge: where this range starts
-    TcRange rr{ra, -1, 0, 0, 0};
-    if (ra < (long long)Hkv * s_prefix[B]) {
-      TileCursor t0;
-      tile_locate(t0, ra, s_prefix, B, Hkv);
-      rr.s = t0.s;
-      rr.h = t0.h;
-      rr.j = t0.j;
-      rr.n = t0.n;
-    }
-    p.range_out[c] = rr;
-  }
 
   if (cnt > 0 && (warp == 0 || warp == 6)) {
     // ---------------- TMA producers: warp 0 streams K, warp 6 streams V ----------------
@@ -857,119 +849,6 @@ DecodeKernelInfo tc_info() {
   info.blk = 1;
   info.tc = 1;
   return info;
-}
-
-// ---------------------------------------------------------------------------
-// Merge for the tcgen05 kernel without a status word: a head is cut only where one
-// CTA's range ends inside it, so merge CTAs (c, y) take the head that contains the
-// first tile of range c when that head began inside range c - 1 (each cut head once),
-// and fold rows y, y + Y, ... of its parts from CTAs c - 1 .. (the CTA of its last
-// tile) with the online-softmax rescaling. The ranges come from the decode kernel's
-// per-CTA records; CTAs (c, 0) also zero-fill the sequences c, c + C, ... that have no
-// tile. Every thread's loads of a step are in flight together: the merge is a few
-// memory round trips long.
-// ---------------------------------------------------------------------------
-constexpr int kTcMergeThreads = 256;
-constexpr int kTcMergeSplit = 4;  // CTAs per cut head (row-interleaved)
-constexpr int kTcMergeItems = 4;  // (row, 4-column group) items per thread, loads in flight together
-
-__global__ void __launch_bounds__(kTcMergeThreads) paged_tc_merge_kernel(const TcMergeParams p) {
-  pdl_wait_prior_grid();
-  const int c = blockIdx.x, C = gridDim.x, y = blockIdx.y, Y = gridDim.y;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int B = p.B, D = p.D, Q = D / 4, R = p.R;
-  const int* tpre = p.prefix;  // tiles per sequence, exclusive prefix
-  __nv_bfloat16* outb = reinterpret_cast<__nv_bfloat16*>(p.out);
-  // sequences without a tile get zeros
-  if (y == 0)
-    for (int s = c; s < B; s += C) {
-      if (tpre[s + 1] != tpre[s]) continue;
-      const size_t row0 = size_t(s) * p.q_len * p.Hq;
-      for (int k = tid; k < p.q_len * p.Hq * Q; k += blockDim.x)
-        reinterpret_cast<uint2*>(outb + (row0 + k / Q) * D)[k % Q] = make_uint2(0u, 0u);
-    }
-  if (c == 0) return;
-  // warp 0: records of ranges c - 1 .. c + 31 in one step (lane l holds range c - 1 + l,
-  // and the first tile past the end stands for range C), then the head holding the
-  // first tile of range c; it is cut here when that tile is not the head's first and
-  // the head began inside range c - 1 (else it was merged where it was first cut).
-  // Parts: CTA c-1 (its first segment only if its range starts at the head), then the
-  // CTAs c, c+1, ... whose non-empty ranges start inside the head (their first segment).
-  constexpr int kMaxParts = 1024;  // a head has at most one part per CTA (grid <= 1024)
-  __shared__ int s_slot[kMaxParts];
-  __shared__ int s_np, s_s, s_h;
-  if (tid < 32) {
-    const long long TT = (long long)p.Hkv * tpre[B];
-    auto load = [&](int w, TcRange& r) {
-      if (w < C) r = p.ranges[w];
-      else r = TcRange{TT, -1, 0, 0, 0};
-    };
-    TcRange mine, nxt;
-    load(c - 1 + lane, mine);
-    load(c + lane, nxt);
-    const long long ra_c = __shfl_sync(0xffffffffu, mine.ra, 1);
-    const long long ra_p = __shfl_sync(0xffffffffu, mine.ra, 0);
-    const int hs = __shfl_sync(0xffffffffu, mine.s, 1), hh = __shfl_sync(0xffffffffu, mine.h, 1);
-    const int hj = __shfl_sync(0xffffffffu, mine.j, 1), hn = __shfl_sync(0xffffffffu, mine.n, 1);
-    const long long u0 = ra_c - hj, u1 = u0 + hn;  // the head's tiles [u0, u1)
-    int np = 0;
-    if (hs >= 0 && hj > 0 && u0 >= ra_p) {
-      np = 1;
-      if (lane == 0) s_slot[0] = 2 * (c - 1) + (ra_p < u0 ? 1 : 0);
-      // lane l >= 1 judges range w = c - 1 + l from its own start and the next one's
-      for (int w0 = c - 1;; w0 += 31) {
-        const int w = w0 + lane;
-        const bool inside = lane >= 1 && w < C && mine.ra < u1;
-        const bool part = inside && nxt.ra > mine.ra;
-        const unsigned pm = __ballot_sync(0xffffffffu, part);
-        if (part && np + __popc(pm & ((1u << lane) - 1u)) < kMaxParts)
-          s_slot[np + __popc(pm & ((1u << lane) - 1u))] = 2 * w;
-        np = min(kMaxParts, np + __popc(pm));
-        // continue while every judged range lies inside the head
-        if ((__ballot_sync(0xffffffffu, inside) | 1u) != 0xffffffffu || np >= kMaxParts) break;
-        load(w0 + 31 + lane, mine);
-        load(w0 + 32 + lane, nxt);
-      }
-    }
-    if (lane == 0) {
-      s_np = np;
-      s_s = hs;
-      s_h = hh;
-    }
-  }
-  __syncthreads();
-  const int np = s_np, s = s_s, h = s_h;
-  if (np == 0) return;
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  // this CTA's items: rows y, y + Y, ... (Q items each), kTcMergeItems per thread at once
-  const int rows = (R - y + Y - 1) / Y, items = rows * Q;
-  for (int k0 = tid; k0 < items; k0 += kTcMergeItems * kTcMergeThreads) {
-    const int live = min(kTcMergeItems, (items - k0 + kTcMergeThreads - 1) / kTcMergeThreads);
-    Fold f[kTcMergeItems];
-#pragma unroll
-    for (int j = 0; j < kTcMergeItems; ++j) f[j] = fold_empty();
-    fold_rows<kTcMergeItems, 2>(f, live, np, [&](int i, int j, const float2*& pm,
-                                                 const float4*& po) {
-      const int k = k0 + j * kTcMergeThreads, r = y + (k / Q) * Y, dq = k % Q;
-      const size_t slot = size_t(s_slot[i]);
-      pm = ml + slot * R + r;
-      po = reinterpret_cast<const float4*>(p.part_o + (slot * R + r) * D) + dq;
-    });
-#pragma unroll
-    for (int j = 0; j < kTcMergeItems; ++j) {
-      if (j >= live) break;
-      const int k = k0 + j * kTcMergeThreads, r = y + (k / Q) * Y, dq = k % Q;
-      const size_t orow = (size_t(s) * p.q_len + r / p.g) * p.Hq + size_t(h) * p.g + r % p.g;
-      reinterpret_cast<uint2*>(outb + orow * D)[dq] = fold_result(f[j]);
-    }
-  }
-}
-
-void launch_tc_merge(const TcMergeParams& p, int grid, cudaStream_t stream) {
-  TcMergeParams copy = p;
-  void* args[] = {&copy};
-  launch_pdl(reinterpret_cast<const void*>(&paged_tc_merge_kernel), dim3(grid, kTcMergeSplit),
-             dim3(kTcMergeThreads), args, 0, stream);
 }
 
 bool select_decode_tc(int D, int BS, DecodeKernelInfo* info) {

@@ -10,14 +10,6 @@
 
 namespace pkv {
 
-// First tile of a tcgen05 CTA's range in the flat (sequence, KV head, tile) order, and
-// the head holding it: sequence s, KV head h, tile j of the head's n tiles (s = -1 when
-// the range is empty and starts past the last tile).
-struct TcRange {
-  long long ra;
-  int s, h, j, n;
-};
-
 // Parameters of one decode launch (device pointers; sizes as in pkv_dims).
 struct DecodeParams {
   const void* q;               // [B, q_len, Hq, D] bf16
@@ -29,7 +21,6 @@ struct DecodeParams {
   float* part_o;               // [2W, GS, D] fp32 partial outputs (unnormalised)
   float* part_ml;              // [2W, GS, 2] fp32 (running max in log2 units, sum)
   int32_t* prefix_out;         // [B+1] blocks-per-sequence exclusive prefix (CTA 0 writes)
-  TcRange* range_out;          // tcgen05 kernel: [grid] first tile of each CTA's range (or null)
   int skip;                    // table entries skipped at the head of every sequence (cascade)
   int unit_slot0;              // >= 0: complete units write a partial to slot unit_slot0 + s*HU + u
                                //       instead of the output (cascade); -1: normal
@@ -114,18 +105,6 @@ struct MergeParams {
 };
 
 void launch_merge(const MergeParams& p, cudaStream_t stream);
-
-// Merge of the tcgen05 decode kernel's cut heads when no status word is given (grid:
-// the decode kernel's CTA count).
-struct TcMergeParams {
-  void* out;
-  const float* part_o;         // [2C, R, D]
-  const float* part_ml;        // [2C, R] (running max in log2 units, sum)
-  const int32_t* prefix;       // [B+1] tiles per sequence, exclusive prefix
-  const TcRange* ranges;       // [C] first tile of every CTA's range (decode kernel writes)
-  int B, Hq, Hkv, D, q_len, g, R;
-};
-void launch_tc_merge(const TcMergeParams& p, int grid, cudaStream_t stream);
 
 // Whole-block moves (copy-on-write copy, swap-out, swap-in): pair i moves chunk
 // src_ids[i] (or i when src_ids is NULL: a dense host buffer) of every array to chunk

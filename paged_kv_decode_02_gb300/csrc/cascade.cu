@@ -33,10 +33,13 @@ namespace pkv {
 // TMEM is then rescaled by 2^(m_old - m_new) before the next P.V accumulates, so
 // weights stay below 2^8 and most tiles skip the rescale. Each split leaves per row the unnormalised (o, m, l) record that
 // the cascade merge folds.
+// The row sums l of the bf16 weights come from the tensor cores too (P times a tile
+// of ones, issued beside P.V and rescaled with O), so the normalisation uses exactly
+// the weights P.V used and the softmax warps add nothing up.
 // Shared memory (1024-byte aligned): Q [D/64 slabs][128 rows x 128 B], K and V
-// tiles x2 [D/64 slabs][128 tokens x 128 B], then the mbarriers, the TMEM address
-// word and the split's block ids. TMEM columns: S x2 [0, 256), O [256, 256 + D),
-// P (bf16 pairs) [384, 448).
+// tiles x2 [D/64 slabs][128 tokens x 128 B], the ones tile (4 KiB), then the
+// mbarriers, the TMEM address word and the split's block ids. TMEM columns: S x2
+// [0, 256), O [256, 256 + D), P (bf16 pairs) [384, 448), l [448, 464).
 // ---------------------------------------------------------------------------
 template <int D, int BS>
 struct PrefixTc {
@@ -50,7 +53,9 @@ struct PrefixTc {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kSlabs * kQSlab;
   static constexpr int kOffV = kOffK + 2 * kTile;
-  static constexpr int kOffBar = kOffV + 2 * kTile;
+  // all-ones B operand (16 x 128 tokens, K-major) of the MMA that sums the rows of P
+  static constexpr int kOffOnes = kOffV + 2 * kTile;
+  static constexpr int kOffBar = kOffOnes + 4096;
   // mbarriers: kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] pfull ofull mdone
   static constexpr int kNumBars = 13;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
@@ -60,8 +65,10 @@ struct PrefixTc {
   static constexpr int kSmem = kOffIds + 4 * kMaxIds + 1024;  // + slack for 1024-byte alignment
   static constexpr int kThreads = 224;  // warps: 0 K copies, 1 MMA, 2..5 softmax, 6 V copies
   static constexpr uint32_t kTmemCols = 512;          // power of two
-  static constexpr int kColS = 0, kColO = 2 * kN, kColP = 2 * kN + 128;
-  static_assert(kColP + kN / 2 <= int(kTmemCols) && kColO + D <= kColP, "TMEM columns");
+  // S x2, O, P (bf16 pairs), l (row sums of P, fp32; 16 columns written by its MMA)
+  static constexpr int kColS = 0, kColO = 2 * kN, kColP = 2 * kN + 128, kColL = kColP + kN / 2;
+  static_assert(kColL + 16 <= int(kTmemCols) && kColO + D <= kColP, "TMEM columns");
+  static_assert(kOffOnes % 1024 == 0, "swizzle atom alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory");
   static_assert(kN % BS == 0 && D % 64 == 0, "tile shape");
   static_assert(kQSlab == kSlab, "Q, K and P slabs share one stride");
@@ -106,6 +113,9 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, K::kTmemCols);
+  for (int k = tid; k < 4096 / 16; k += K::kThreads)  // bf16 1.0 everywhere
+    tc::sts128(base + K::kOffOnes + 16 * k,
+               make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u));
 
   // this split's physical block ids -> shared memory (the producer's copies then need
   // no dependent global load)
@@ -190,6 +200,8 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_bf16<128, K::kN, false>();
       constexpr uint32_t kIdO = tc::idesc_bf16<128, D, true>();
+      constexpr uint32_t kIdL = tc::idesc_bf16<128, 16, false>();
+      const uint32_t ones = base + K::kOffOnes;
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
         if (!tc::wait_or_abort(kfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag))
@@ -221,6 +233,10 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
           tc::mma_bf16_tmem_a(tmem + K::kColO, tmem + K::kColP + kk * 8,
                               tc::sdesc_sw128(vb + kk * 16 * 128, K::kSlab, 1024), kIdO,
                               (j > 0 || kk > 0) ? 1u : 0u);
+          // the row sums of the bf16 weights this P.V used (P times the ones tile)
+          tc::mma_bf16_tmem_a(tmem + K::kColL, tmem + K::kColP + kk * 8,
+                              tc::sdesc_sw128(ones + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024),
+                              kIdL, (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc::commit(vempty(st));
         tc::commit(ofull);
@@ -243,7 +259,7 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
     const float sl = pp.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref = -INFINITY;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
@@ -270,42 +286,42 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
           if (t >= valid) s[t] = 0xff800000u;  // -inf
       }
       const float asl = fabsf(sl);
-      float mx[8];  // eight interleaved partial maxima: short dependency chains
+      // tile maximum: three-input max over eight independent chains
+      float mx[8];
 #pragma unroll
-      for (int t = 0; t < K::kN; ++t)
-        mx[t & 7] = (t < 8) ? __uint_as_float(s[t]) : fmaxf(mx[t & 7], __uint_as_float(s[t]));
-      const float mt = asl * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(s[e]);
+#pragma unroll
+      for (int u = 0; u < (K::kN - 8) / 2; ++u)
+        mx[u & 7] = fmax3(mx[u & 7], __uint_as_float(s[8 + 2 * u]), __uint_as_float(s[9 + 2 * u]));
+      const float mt = asl * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                   fmaxf(mx[6], mx[7]));
       float alpha = 1.f;
       bool rescale = false;
       if (mt > m_ref + 8.f) {
         alpha = fast_exp2(m_ref - mt);  // 0 on the first tile
         m_ref = mt;
-        l *= alpha;
         rescale = j > 0;
       }
+      // weights 2^(scale * s - m) (packed fp32x2 FMAs), bf16 pairs; their row sums come
+      // from the tensor cores (P times the ones tile, beside P.V)
       uint32_t pk[K::kN / 2];
-      float sm[4] = {0.f, 0.f, 0.f, 0.f};
-      const float nm = -m_ref;
+      const float2 asl2 = make_float2(asl, asl), nm2 = make_float2(-m_ref, -m_ref);
       if (valid == K::kN) {
 #pragma unroll
         for (int t = 0; t < K::kN; t += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(s[t]), asl, nm));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(s[t + 1]), asl, nm));
-          sm[(t >> 1) & 3] += p0 + p1;
-          pk[t / 2] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
+                                      asl2, nm2);
+          pk[t / 2] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
         }
       } else {
 #pragma unroll
         for (int t = 0; t < K::kN; t += 2) {
-          const float p0 = t < valid ? fast_exp2(fmaf(__uint_as_float(s[t]), asl, nm)) : 0.f;
-          const float p1 =
-              t + 1 < valid ? fast_exp2(fmaf(__uint_as_float(s[t + 1]), asl, nm)) : 0.f;
-          sm[(t >> 1) & 3] += p0 + p1;
-          pk[t / 2] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
+                                      asl2, nm2);
+          pk[t / 2] =
+              pack_bf16x2(t < valid ? fast_exp2(x.x) : 0.f, t + 1 < valid ? fast_exp2(x.y) : 0.f);
         }
       }
-      l += (sm[0] + sm[1]) + (sm[2] + sm[3]);
       // P.V of the previous tile must be complete before P is overwritten or O rescaled
       if (j > 0 && !__all_sync(0xffffffffu, tc::wait_or_abort(ofull, uint32_t(j - 1) & 1u,
                                                         pp.timeout_ns, abort_flag))) {
@@ -322,6 +338,8 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tc::tmem_st32(trow + K::kColO + c, o);
         }
+        tc::tmem_st1(trow + K::kColL,
+                     __float_as_uint(__uint_as_float(tc::tmem_ld1(trow + K::kColL)) * alpha));
       }
       // P row -> TMEM (bf16 pairs of consecutive tokens), the A operand of P.V
 #pragma unroll
@@ -358,6 +376,7 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
                                          __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
       }
     }
+    const float l = (ok && ntiles > 0) ? __uint_as_float(tc::tmem_ld1(trow + K::kColL)) : 0.f;
     if (gr < pp.R)
       reinterpret_cast<float2*>(pp.pre_ml)[rec] =
           (ok && ntiles > 0) ? make_float2(m_ref, l) : make_float2(-INFINITY, 0.f);

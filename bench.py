@@ -460,7 +460,7 @@ def run_ours(args, rank, world):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": measured_traffic(args.config),
                      "traffic_source": "profiles/decode_traffic.txt (ncu dram bytes read+write, "
-                                       "decode + merge kernels, one call)",
+                                       "every kernel of one decode call)",
                      "kernel": decode_kernels(w, cascade_blocks, dec_launches),
                      "launches_per_call": dec_launches,
                      "bytes_per_launch": db["total"], "avg_launch_ms": round(dec_ms, 5),

@@ -252,6 +252,39 @@ def test_decode_reuses_caller_workspace_and_output(pk):
     assert torch.equal(r1, r3)
 
 
+def test_kernel_launch_counts_per_call(pk):
+    """The library's launch counter (what bench.py reports as gpu_launches) against the
+    kernels each call is documented to launch."""
+    lib = pk.pagedkv.load_library()
+
+    def launches(fn):
+        torch.cuda.synchronize()
+        n0 = lib.pkv_kernel_launch_count()
+        fn()
+        torch.cuda.synchronize()
+        return lib.pkv_kernel_launch_count() - n0
+
+    mha = make_workload("7b", device=DEV, lengths=[700, 30, 2048], seed=7)
+    gqa = make_workload("70b-gqa", device=DEV, num_seqs=6, seed=8)
+    spec = make_workload("spec-70b", device=DEV, num_q_heads=16, num_kv_heads=2, q_len=6,
+                         lengths=[600, 6, 130], seed=9)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert launches(lambda: pk.paged_kv_append(mha.new_k, mha.new_v, mha.k_cache, mha.v_cache,
+                                               mha.slot_mapping)) == 1
+    # MHA, head_dim 128, bf16, no status word: cut units folded inside the decode kernel
+    assert launches(lambda: _decode(pk, mha)) == 1
+    assert launches(lambda: _decode(pk, mha, status=status)) == 2      # + validating merge
+    assert launches(lambda: _decode(pk, gqa)) == 2                     # decode + merge
+    # tcgen05 multi-query kernel: cut heads folded at the CTA tail
+    assert launches(lambda: pk.paged_decode_attention_multi(
+        spec.q, spec.k_cache, spec.v_cache, spec.block_tables, spec.context_lens,
+        spec.scale)) == 1
+    assert launches(lambda: pk.paged_decode_attention_multi(
+        spec.q, spec.k_cache, spec.v_cache, spec.block_tables, spec.context_lens, spec.scale,
+        status=status)) == 2
+    assert int(status.item()) == 0
+
+
 # ---------------------------------------------------------------------------
 # decode at the full workload sizes, sampled outputs
 # ---------------------------------------------------------------------------

@@ -484,9 +484,7 @@ def decode_kernels(w, cascade_blocks, launches):
         "paged_decode_kernel"
     if launches == 1:
         return main + " (split-KV parts folded inside the kernel, one launch per call)"
-    merge = "paged_tc_merge_kernel" if main == "paged_decode_tc_kernel" else \
-        "paged_decode_merge_kernel"
-    return f"{main} + {merge} (one decode call)"
+    return f"{main} + paged_decode_merge_kernel (one decode call)"
 
 
 def run_blocks(args, rank, world):

@@ -21,9 +21,10 @@ constexpr int kMaxQueryLen = PKV_MAX_QUERY_LEN;
 constexpr int kTcMinRows = 48;  // multi-query rows per KV head from which tcgen05 wins
 // tcgen05 kernel: the cost of ending a KV head (its partly filled last tile, the
 // epilogue, the next head's first scores) in tiles; ranges are balanced on tiles plus
-// this much per head. A sweep of whole calls on GB300 (48, 64 and 128 query rows per
-// KV head) put the best at 3 for all three shapes (2 and 4: 4-8 % slower)
-constexpr int kTcHeadCost = 3;
+// this much per head. A sweep of whole calls on GB300 (48 and 128 query rows per KV
+// head, with the softmax row sums on the tensor cores) put the best at 2 (1: 8-15 %
+// slower, 3: 1-3 %, 4 and 5: 3-5 %)
+constexpr int kTcHeadCost = 2;
 // cascade decode: the prefix kernel runs on about 1/kCascadePrefixShare of the SMs
 constexpr int kCascadePrefixShare = 3;
 

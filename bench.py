@@ -644,27 +644,44 @@ def capture(K, fn, dev):
 
 def run_e2e(args, w, pk, dev, append_dev, out, ws, step_bytes, world, cascade_blocks=0):
     """Same step through the public API from pinned HOST buffers: per step, copy the
-    step's inputs host->device, append + decode, copy the output device->host."""
+    step's inputs host->device (one copy of a packed buffer), append + decode, copy the
+    output device->host."""
     import torch
     stream = torch.cuda.current_stream(dev)
-    host_in = {n: getattr(w, n).cpu().pin_memory()
-               for n in ("q", "new_k", "new_v", "slot_mapping", "block_tables", "context_lens")}
-    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+    # the step's inputs packed into one pinned host buffer (256-byte aligned regions) and
+    # moved by one copy per step into views of one device buffer
+    names = ("q", "new_k", "new_v", "slot_mapping", "block_tables", "context_lens")
+    srcs = {n: getattr(w, n).contiguous() for n in names}
+    offs, total = {}, 0
+    for n in names:
+        offs[n] = total
+        total += (srcs[n].numel() * srcs[n].element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+    dev_in = {}
+    for n in names:
+        t = srcs[n]
+        nb = t.numel() * t.element_size()
+        host_buf[offs[n]:offs[n] + nb].view(t.dtype).copy_(t.reshape(-1).cpu())
+        dev_in[n] = dev_buf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = total
     d2h = host_out.numel() * host_out.element_size()
 
     def step():
-        for n, t in host_in.items():
-            dev_in[n].copy_(t, non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         api_append(pk, w, dev_in["new_k"], dev_in["new_v"], dev_in["slot_mapping"])
         api_decode(pk, w, dev_in["q"], dev_in["block_tables"], dev_in["context_lens"], out, ws,
                    cascade_blocks)
         host_out.copy_(out, non_blocking=True)
 
+    ref = out.clone()
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
+    # the packed inputs are the device-resident step's inputs: the same result
+    if not torch.equal(host_out, ref.cpu()):
+        raise RuntimeError("end-to-end step disagrees with the device-resident step")
     K = max(1, min(args.steps, 500))
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)

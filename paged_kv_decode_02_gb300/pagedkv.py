@@ -290,9 +290,38 @@ def _require_any(t, name, dtypes, ndim, device):
     _require(t, name, dtypes[0], ndim, device)
 
 
+def _status_word(status, device):
+    """The optional device status word: None, or an int32 CUDA tensor on ``device``."""
+    if status is None:
+        return None
+    if not isinstance(status, torch.Tensor) or not status.is_cuda or status.device != device:
+        raise ValueError(f"status must be an int32 CUDA tensor on {device}")
+    if status.dtype != torch.int32 or status.numel() < 1 or not status.is_contiguous():
+        raise TypeError("status must be a contiguous int32 tensor of at least one element")
+    return status
+
+
+def _workspace(workspace, need, device):
+    """(tensor, size in bytes) of the decode workspace: the caller's, checked to be a
+    contiguous CUDA tensor on ``device``, when it holds ``need`` bytes; else a fresh
+    uint8 buffer from torch's allocator."""
+    if workspace is not None:
+        if (not isinstance(workspace, torch.Tensor) or not workspace.is_cuda
+                or workspace.device != device):
+            raise ValueError(f"workspace must be a CUDA tensor on {device}")
+        if not workspace.is_contiguous():
+            raise ValueError("workspace must be contiguous")
+        nbytes = workspace.numel() * workspace.element_size()
+        if nbytes >= need:
+            return workspace, nbytes
+    ws = torch.empty(max(int(need), 256), dtype=torch.uint8, device=device)
+    return ws, ws.numel()
+
+
 def _decode(kv, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
             out, workspace, status):
     dev = q.device
+    status = _status_word(status, dev)
     _require(q, "q", torch.bfloat16, 3, dev)
     _require_any(k_cache, "k_cache", _code_dtypes(kv), 4, dev)
     _require_any(v_cache, "v_cache", _code_dtypes(kv), 4, dev)
@@ -315,27 +344,26 @@ def _decode(kv, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_len
         need = ctypes.c_size_t(0)
         _check(_lib().pkv_decode_workspace_bytes(ctypes.byref(dims), kv, ctypes.byref(need)),
                "pkv_decode_workspace_bytes")
-        if workspace is None or workspace.numel() < need.value:
-            workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=dev)
+        workspace, ws_bytes = _workspace(workspace, need.value, dev)
         if kv == KV_INT8:
             name = "pkv_decode_int8"
             st = _lib().pkv_decode_int8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                         _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
                                         _ptr(context_lens), float(scale), ctypes.byref(dims),
-                                        _ptr(workspace), workspace.numel(), _ptr(status),
+                                        _ptr(workspace), ws_bytes, _ptr(status),
                                         _stream(dev))
         elif kv == KV_BF16:
             name = "pkv_decode_bf16"
             st = _lib().pkv_decode_bf16(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                         _ptr(block_tables), _ptr(context_lens), float(scale),
-                                        ctypes.byref(dims), _ptr(workspace), workspace.numel(),
+                                        ctypes.byref(dims), _ptr(workspace), ws_bytes,
                                         _ptr(status), _stream(dev))
         else:
             name = "pkv_decode_fp8"
             st = _lib().pkv_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                        _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
                                        _ptr(context_lens), float(scale), kv, ctypes.byref(dims),
-                                       _ptr(workspace), workspace.numel(), _ptr(status),
+                                       _ptr(workspace), ws_bytes, _ptr(status),
                                        _stream(dev))
     _check(st, name)
     return out
@@ -375,6 +403,8 @@ def paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tabl
 def _move_kv(k_cache, kv_dtype):
     """KV dtype code of a block move: from the cache dtype, or ``kv_dtype`` (needed for
     uint8 FP8 codes, where any one-byte code gives the same move)."""
+    if not isinstance(k_cache, torch.Tensor):
+        raise TypeError("k_cache must be a torch.Tensor")
     kv = _KV_OF_DTYPE.get(k_cache.dtype, -1) if kv_dtype is None else kv_dtype
     if kv is None:
         kv = KV_FP8_E5M2                      # uint8 codes: one byte + scales
@@ -388,13 +418,49 @@ def _move_dims(k_cache):
     return Dims(0, hkv, hkv, d, bs, nb, 1)
 
 
+def _move_caches(kv, k_cache, v_cache, k_scale, v_scale):
+    """Checks the device side of a block move; returns (device, bytes of one block of
+    one cache, bytes of one block's scales or 0)."""
+    dev = k_cache.device
+    _require(k_cache, "k_cache", k_cache.dtype, 4, dev)
+    _require(v_cache, "v_cache", k_cache.dtype, 4, dev)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache differ in shape")
+    nb, hkv, bs, d = k_cache.shape
+    block = hkv * bs * d * k_cache.element_size()
+    if kv == KV_BF16:
+        return dev, block, 0
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _require(t, n, torch.float32, 3, dev)
+        if tuple(t.shape) != (nb, hkv, bs):
+            raise ValueError(f"{n} must be [num_blocks, num_kv_heads, block_size]")
+    return dev, block, hkv * bs * 4
+
+
+def _host_buffers(kv, n, block, scale_block, host_k, host_v, host_k_scale, host_v_scale):
+    """Checks that the pinned host buffers of a swap hold ``n`` packed blocks (the GPU
+    reads or writes them directly, so a short buffer would be overrun)."""
+    bufs = [(host_k, "host_k", block), (host_v, "host_v", block)]
+    if kv != KV_BF16:
+        bufs += [(host_k_scale, "host_k_scale", scale_block),
+                 (host_v_scale, "host_v_scale", scale_block)]
+    for t, name, per_block in bufs:
+        _host(t, name)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.numel() * t.element_size() < n * per_block:
+            raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, "
+                             f"{n} blocks need {n * per_block}")
+
+
 def copy_blocks(k_cache, v_cache, src_ids, dst_ids, k_scale=None, v_scale=None, status=None,
                 kv_dtype=None):
     """Copy-on-write block copy: block dst_ids[i] := block src_ids[i] of the K/V caches
     (and their scales, for one-byte caches). ``src_ids``/``dst_ids``: device int32.
     In place, asynchronous on the current stream."""
-    dev = k_cache.device
     kv = _move_kv(k_cache, kv_dtype)
+    dev, _, _ = _move_caches(kv, k_cache, v_cache, k_scale, v_scale)
+    status = _status_word(status, dev)
     for t, n in ((src_ids, "src_ids"), (dst_ids, "dst_ids")):
         _require(t, n, torch.int32, 1, dev)
     if src_ids.numel() != dst_ids.numel():
@@ -417,11 +483,12 @@ def swap_out(k_cache, v_cache, block_ids, host_k, host_v, k_scale=None, v_scale=
              host_k_scale=None, host_v_scale=None, status=None, kv_dtype=None):
     """Evict blocks to pinned host memory: host_k[i] := block block_ids[i] (likewise V
     and scales). Asynchronous on the current stream."""
-    dev = k_cache.device
     kv = _move_kv(k_cache, kv_dtype)
+    dev, block, scale_block = _move_caches(kv, k_cache, v_cache, k_scale, v_scale)
+    status = _status_word(status, dev)
     _require(block_ids, "block_ids", torch.int32, 1, dev)
-    for t, n in ((host_k, "host_k"), (host_v, "host_v")):
-        _host(t, n)
+    _host_buffers(kv, block_ids.numel(), block, scale_block, host_k, host_v, host_k_scale,
+                  host_v_scale)
     dims = _move_dims(k_cache)
     with _OnDevice(dev):
         st = _lib().pkv_swap_out(_ptr(host_k), _ptr(host_v), _ptr(host_k_scale),
@@ -435,11 +502,12 @@ def swap_in(k_cache, v_cache, block_ids, host_k, host_v, k_scale=None, v_scale=N
             host_k_scale=None, host_v_scale=None, status=None, kv_dtype=None):
     """Bring evicted blocks back: block block_ids[i] := host_k[i] (likewise V and
     scales). Asynchronous on the current stream."""
-    dev = k_cache.device
     kv = _move_kv(k_cache, kv_dtype)
+    dev, block, scale_block = _move_caches(kv, k_cache, v_cache, k_scale, v_scale)
+    status = _status_word(status, dev)
     _require(block_ids, "block_ids", torch.int32, 1, dev)
-    for t, n in ((host_k, "host_k"), (host_v, "host_v")):
-        _host(t, n)
+    _host_buffers(kv, block_ids.numel(), block, scale_block, host_k, host_v, host_k_scale,
+                  host_v_scale)
     dims = _move_dims(k_cache)
     with _OnDevice(dev):
         st = _lib().pkv_swap_in(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
@@ -469,6 +537,7 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
     token i attends causally to positions 0 .. context_lens - q_len + i. Returns out
     [B, q_len, Hq, D] bf16."""
     dev = q.device
+    status = _status_word(status, dev)
     _require(q, "q", torch.bfloat16, 4, dev)
     _require(k_cache, "k_cache", torch.bfloat16, 4, dev)
     _require(v_cache, "v_cache", torch.bfloat16, 4, dev)
@@ -489,12 +558,11 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
         _check(_lib().pkv_decode_multi_workspace_bytes(ctypes.byref(dims), n,
                                                        ctypes.byref(need)),
                "pkv_decode_multi_workspace_bytes")
-        if workspace is None or workspace.numel() < need.value:
-            workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=dev)
+        workspace, ws_bytes = _workspace(workspace, need.value, dev)
         st = _lib().pkv_decode_multi_bf16(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                           _ptr(block_tables), _ptr(context_lens), n,
                                           float(scale), ctypes.byref(dims), _ptr(workspace),
-                                          workspace.numel(), _ptr(status), _stream(dev))
+                                          ws_bytes, _ptr(status), _stream(dev))
     _check(st, "pkv_decode_multi_bf16")
     return out
 
@@ -518,6 +586,7 @@ def paged_decode_attention_cascade(q, k_cache, v_cache, block_tables, context_le
     per KV head for every query row as a dense tensor-core contraction, the suffixes by
     the ordinary decode. Same result as :func:`paged_decode_attention` (bf16 caches)."""
     dev = q.device
+    status = _status_word(status, dev)
     _require(q, "q", torch.bfloat16, 3, dev)
     _require(k_cache, "k_cache", torch.bfloat16, 4, dev)
     _require(v_cache, "v_cache", torch.bfloat16, 4, dev)
@@ -538,12 +607,11 @@ def paged_decode_attention_cascade(q, k_cache, v_cache, block_tables, context_le
         _check(_lib().pkv_decode_cascade_workspace_bytes(ctypes.byref(dims), int(prefix_blocks),
                                                          ctypes.byref(need)),
                "pkv_decode_cascade_workspace_bytes")
-        if workspace is None or workspace.numel() < need.value:
-            workspace = torch.empty(max(int(need.value), 256), dtype=torch.uint8, device=dev)
+        workspace, ws_bytes = _workspace(workspace, need.value, dev)
         st = _lib().pkv_decode_cascade_bf16(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                             _ptr(block_tables), _ptr(context_lens),
                                             int(prefix_blocks), float(scale), ctypes.byref(dims),
-                                            _ptr(workspace), workspace.numel(), _ptr(status),
+                                            _ptr(workspace), ws_bytes, _ptr(status),
                                             _stream(dev))
     _check(st, "pkv_decode_cascade_bf16")
     return out

@@ -95,6 +95,32 @@ def test_swap_out_and_in_bit_exact(pk, name, kv):
         assert np.array_equal(_np(got), oracle.swap_in_blocks(old, _np(h), in_ids))
 
 
+def test_moves_check_buffers_before_launch(pk):
+    """Host buffers too short for the listed blocks, caches that disagree and one-byte
+    caches without their scales are refused by the binding; nothing launches."""
+    lib = pk.pagedkv.load_library()
+    w = make_workload("tiny", device=DEV)
+    i8 = make_workload("tiny", device=DEV, kv_dtype="int8")
+    ids = torch.tensor([1, 5, 9], dtype=torch.int32, device=DEV)
+    short = torch.empty((2,) + tuple(w.k_cache.shape[1:]), dtype=torch.bfloat16).pin_memory()
+    full = torch.empty((3,) + tuple(w.k_cache.shape[1:]), dtype=torch.bfloat16).pin_memory()
+    n0 = lib.pkv_kernel_launch_count()
+    with pytest.raises(ValueError):
+        pk.swap_out(w.k_cache, w.v_cache, ids, short, full)
+    with pytest.raises(ValueError):
+        pk.swap_in(w.k_cache, w.v_cache, ids, full, short)
+    with pytest.raises(ValueError):
+        pk.copy_blocks(w.k_cache, w.v_cache[:-1], ids, ids + 1)
+    with pytest.raises(TypeError):
+        pk.copy_blocks(i8.k_cache, i8.v_cache, ids, ids + 1)                    # no scales
+    hk = torch.empty((3,) + tuple(i8.k_cache.shape[1:]), dtype=torch.int8).pin_memory()
+    hs = torch.empty((2,) + tuple(i8.k_scale.shape[1:]), dtype=torch.float32).pin_memory()
+    with pytest.raises(ValueError):
+        pk.swap_out(i8.k_cache, i8.v_cache, ids, hk, hk.clone().pin_memory(), i8.k_scale,
+                    i8.v_scale, hs, hs.clone().pin_memory())                   # short scales
+    assert lib.pkv_kernel_launch_count() == n0
+
+
 def test_swap_refuses_pageable_host_memory(pk):
     from paged_kv_decode_02_gb300 import pagedkv
     w = make_workload("tiny", device=DEV)

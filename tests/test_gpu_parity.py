@@ -252,6 +252,31 @@ def test_decode_reuses_caller_workspace_and_output(pk):
     assert torch.equal(r1, r3)
 
 
+def test_binding_checks_caller_workspace_and_status(pk):
+    """The binding refuses a workspace or status word the kernels could not use (host
+    memory, wrong dtype) before anything launches, and counts a caller workspace of any
+    dtype in bytes."""
+    lib = pk.pagedkv.load_library()
+    w = make_workload("70b-gqa", device=DEV, num_seqs=4, seed=8)
+    need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                     w.block_size, w.num_blocks, w.max_blocks_per_seq)
+    ref = _decode(pk, w)
+    torch.cuda.synchronize()
+    n0 = lib.pkv_kernel_launch_count()
+    with pytest.raises(ValueError):
+        _decode(pk, w, workspace=torch.zeros(need, dtype=torch.uint8))           # host memory
+    with pytest.raises(TypeError):
+        _decode(pk, w, status=torch.zeros(1, dtype=torch.int64, device=DEV))
+    with pytest.raises(ValueError):
+        _decode(pk, w, status=torch.zeros(1, dtype=torch.int32))                 # host memory
+    assert lib.pkv_kernel_launch_count() == n0
+    # a float32 workspace holding the bytes is used as it is (its size counted in bytes)
+    ws = torch.zeros(-(-need // 4) + 64, dtype=torch.float32, device=DEV)
+    out = _decode(pk, w, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
 def test_kernel_launch_counts_per_call(pk):
     """The library's launch counter (what bench.py reports as gpu_launches) against the
     kernels each call is documented to launch."""

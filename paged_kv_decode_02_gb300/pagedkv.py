@@ -200,6 +200,29 @@ def _dims(num_seqs, num_q_heads, k_cache, max_blocks_per_seq):
     return Dims(num_seqs, num_q_heads, hkv, d, bs, nb, max_blocks_per_seq)
 
 
+def _same_shape(t, name, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _cache_shapes(k_cache, v_cache, k_scale=None, v_scale=None):
+    """V cache and scales against the K cache [NB, Hkv, bs, D]: the kernels address all
+    of them through the K cache's sizes."""
+    _same_shape(v_cache, "v_cache", k_cache.shape)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t is not None:
+            _same_shape(t, n, k_cache.shape[:3])
+
+
+def _append_shapes(k, v, k_cache, v_cache, slot_mapping, k_scale=None, v_scale=None):
+    """New rows [T, Hkv, D] and T slots, against the caches."""
+    _cache_shapes(k_cache, v_cache, k_scale, v_scale)
+    row = (k.shape[0], k_cache.shape[1], k_cache.shape[3])
+    _same_shape(k, "k", row)
+    _same_shape(v, "v", row)
+    _same_shape(slot_mapping, "slot_mapping", (k.shape[0],))
+
+
 def paged_kv_append(k, v, k_cache, v_cache, slot_mapping):
     """Write new tokens' K/V rows ([T, Hkv, D] bf16) into the bf16 paged caches
     ([NB, Hkv, bs, D]) at ``slot_mapping`` ([T] int64, -1 = skip). In place."""
@@ -209,6 +232,7 @@ def paged_kv_append(k, v, k_cache, v_cache, slot_mapping):
                          (v_cache, "v_cache", torch.bfloat16, 4),
                          (slot_mapping, "slot_mapping", torch.int64, 1)):
         _require(t, n, dt, nd, dev)
+    _append_shapes(k, v, k_cache, v_cache, slot_mapping)
     dims = _dims(0, k_cache.shape[1], k_cache, 1)
     with _OnDevice(dev):
         st = _lib().pkv_append_bf16(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
@@ -228,6 +252,7 @@ def paged_kv_append_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping)
                          (v_scale, "v_scale", torch.float32, 3),
                          (slot_mapping, "slot_mapping", torch.int64, 1)):
         _require(t, n, dt, nd, dev)
+    _append_shapes(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale)
     dims = _dims(0, k_cache.shape[1], k_cache, 1)
     with _OnDevice(dev):
         st = _lib().pkv_append_int8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
@@ -250,6 +275,7 @@ def paged_kv_append_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, 
         _require(t, n, dt, nd, dev)
     _require_any(k_cache, "k_cache", _code_dtypes(kv), 4, dev)
     _require_any(v_cache, "v_cache", _code_dtypes(kv), 4, dev)
+    _append_shapes(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale)
     dims = _dims(0, k_cache.shape[1], k_cache, 1)
     with _OnDevice(dev):
         st = _lib().pkv_append_fp8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
@@ -335,11 +361,14 @@ def _decode(kv, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_len
         raise ValueError("cache shapes disagree with q")
     if block_tables.shape[0] != B or context_lens.shape[0] != B:
         raise ValueError("block_tables / context_lens must have num_seqs rows")
+    _cache_shapes(k_cache, v_cache, k_scale if kv != KV_BF16 else None,
+                  v_scale if kv != KV_BF16 else None)
     dims = _dims(B, Hq, k_cache, block_tables.shape[1])
     if out is None:
         out = torch.empty_like(q)
     else:
         _require(out, "out", torch.bfloat16, 3, dev)
+        _same_shape(out, "out", q.shape)
     with _OnDevice(dev):
         need = ctypes.c_size_t(0)
         _check(_lib().pkv_decode_workspace_bytes(ctypes.byref(dims), kv, ctypes.byref(need)),
@@ -553,6 +582,7 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
         out = torch.empty_like(q)
     else:
         _require(out, "out", torch.bfloat16, 4, dev)
+        _same_shape(out, "out", q.shape)
     with _OnDevice(dev):
         need = ctypes.c_size_t(0)
         _check(_lib().pkv_decode_multi_workspace_bytes(ctypes.byref(dims), n,
@@ -602,6 +632,7 @@ def paged_decode_attention_cascade(q, k_cache, v_cache, block_tables, context_le
         out = torch.empty_like(q)
     else:
         _require(out, "out", torch.bfloat16, 3, dev)
+        _same_shape(out, "out", q.shape)
     with _OnDevice(dev):
         need = ctypes.c_size_t(0)
         _check(_lib().pkv_decode_cascade_workspace_bytes(ctypes.byref(dims), int(prefix_blocks),

@@ -252,10 +252,11 @@ def test_decode_reuses_caller_workspace_and_output(pk):
     assert torch.equal(r1, r3)
 
 
-def test_binding_checks_caller_workspace_and_status(pk):
-    """The binding refuses a workspace or status word the kernels could not use (host
-    memory, wrong dtype) before anything launches, and counts a caller workspace of any
-    dtype in bytes."""
+def test_binding_checks_buffers_before_launch(pk):
+    """The binding refuses, before anything launches, a workspace or status word the
+    kernels could not use (host memory, wrong dtype) and tensors whose shapes disagree
+    with the caches (output, new rows, slots, scales); it counts a caller workspace of
+    any dtype in bytes."""
     lib = pk.pagedkv.load_library()
     w = make_workload("70b-gqa", device=DEV, num_seqs=4, seed=8)
     need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
@@ -269,6 +270,21 @@ def test_binding_checks_caller_workspace_and_status(pk):
         _decode(pk, w, status=torch.zeros(1, dtype=torch.int64, device=DEV))
     with pytest.raises(ValueError):
         _decode(pk, w, status=torch.zeros(1, dtype=torch.int32))                 # host memory
+    # shapes the kernels would address past a buffer's end
+    with pytest.raises(ValueError):
+        _decode(pk, w, out=torch.empty_like(w.q)[:-1])                          # short out
+    with pytest.raises(ValueError):
+        pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping[:-1])
+    with pytest.raises(ValueError):
+        pk.paged_kv_append(w.new_k[..., :64].contiguous(), w.new_v, w.k_cache, w.v_cache,
+                           w.slot_mapping)                                     # wrong head_dim
+    i8 = make_workload("int8", device=DEV, num_seqs=2, lengths=[40, 9], block_size=16)
+    with pytest.raises(ValueError):
+        pk.paged_decode_attention_int8(i8.q, i8.k_cache, i8.v_cache, i8.k_scale[:-1],
+                                       i8.v_scale, i8.block_tables, i8.context_lens, i8.scale)
+    with pytest.raises(ValueError):
+        pk.paged_kv_append_int8(i8.new_k, i8.new_v, i8.k_cache, i8.v_cache, i8.k_scale,
+                                i8.v_scale[:-1], i8.slot_mapping)
     assert lib.pkv_kernel_launch_count() == n0
     # a float32 workspace holding the bytes is used as it is (its size counted in bytes)
     ws = torch.zeros(-(-need // 4) + 64, dtype=torch.float32, device=DEV)

@@ -129,3 +129,34 @@ def test_host_validation_without_gpu(lib_path):
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 0, None) == pagedkv.Status.ERR_NULL
     # nothing above reached a launch
     assert lib.pkv_kernel_launch_count() == launches_before
+
+
+def test_binding_host_checks_without_gpu():
+    """The binding's own checks (the C ABI cannot see buffer sizes) refuse
+    disagreeing shapes, unusable workspaces and status words, and host buffers too
+    short for a swap, before any library call."""
+    import torch
+    from paged_kv_decode_02_gb300 import pagedkv as P
+    kc = torch.zeros(6, 2, 16, 64, dtype=torch.bfloat16)
+    row = torch.zeros(3, 2, 64, dtype=torch.bfloat16)
+    slots = torch.zeros(3, dtype=torch.int64)
+    P._append_shapes(row, row, kc, kc.clone(), slots)                   # consistent: passes
+    for args in ((row[:2], row, kc, kc, slots),                          # k rows vs slots
+                 (row, row, kc, kc, slots[:2]),                          # short slot_mapping
+                 (row[..., :32], row[..., :32], kc, kc, slots),          # head_dim
+                 (row, row, kc, kc[:5], slots)):                         # v_cache pool
+        with pytest.raises(ValueError):
+            P._append_shapes(*args)
+    sc = torch.zeros(6, 2, 16)
+    P._cache_shapes(kc, kc, sc, sc)
+    with pytest.raises(ValueError):
+        P._cache_shapes(kc, kc, sc, sc[:, :, :8])                       # scales per block
+    dev = torch.device("cuda", 0)
+    with pytest.raises(ValueError):
+        P._workspace(torch.zeros(1 << 10, dtype=torch.uint8), 256, dev)   # host memory
+    with pytest.raises(ValueError):
+        P._status_word(torch.zeros(1, dtype=torch.int32), dev)          # host memory
+    assert P._status_word(None, dev) is None
+    with pytest.raises(ValueError):                                       # not pinned
+        P._host_buffers(P.KV_BF16, 3, 4096, 0, torch.zeros(3, 4096, dtype=torch.uint8),
+                        torch.zeros(3, 4096, dtype=torch.uint8), None, None)

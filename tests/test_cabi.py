@@ -127,6 +127,28 @@ def test_host_validation_without_gpu(lib_path):
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 7, ctypes.byref(n)) == \
         pagedkv.Status.ERR_DTYPE
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 0, None) == pagedkv.Status.ERR_NULL
+    # multi-query decode: 1 <= q_len <= PKV_MAX_QUERY_LEN (16)
+    for q_len in (0, 17):
+        assert lib.pkv_decode_multi_workspace_bytes(ctypes.byref(good), q_len,
+                                                    ctypes.byref(n)) == pagedkv.Status.ERR_SHAPE
+        st = lib.pkv_decode_multi_bf16(p, p, p, p, p, p, q_len, 0.1, ctypes.byref(good), p,
+                                       1 << 20, None, None)
+        assert st == pagedkv.Status.ERR_SHAPE
+    assert lib.pkv_decode_multi_workspace_bytes(ctypes.byref(good), 2, None) == \
+        pagedkv.Status.ERR_NULL
+    st = lib.pkv_decode_multi_bf16(p, p, p, None, p, p, 2, 0.1, ctypes.byref(good), p, 1 << 20,
+                                   None, None)
+    assert st == pagedkv.Status.ERR_NULL
+    # cascade: the shared prefix is 1 .. max_blocks_per_seq blocks
+    for blocks in (0, 5):
+        assert lib.pkv_decode_cascade_workspace_bytes(ctypes.byref(good), blocks,
+                                                      ctypes.byref(n)) == pagedkv.Status.ERR_SHAPE
+    st = lib.pkv_decode_cascade_bf16(p, mis, p, p, p, p, 2, 0.1, ctypes.byref(good), p, 1 << 20,
+                                     None, None)
+    assert st == pagedkv.Status.ERR_ALIGNMENT
+    st = lib.pkv_decode_cascade_bf16(p, p, p, p, p, p, 2, 0.1, ctypes.byref(bad_bs), p, 1 << 20,
+                                     None, None)
+    assert st == pagedkv.Status.ERR_UNSUPPORTED
     # nothing above reached a launch
     assert lib.pkv_kernel_launch_count() == launches_before
 

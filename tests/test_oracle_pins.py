@@ -462,6 +462,59 @@ def test_int8_append_then_decode_matches_dequantised_bf16_path():
     assert np.array_equal(a, b)
 
 
+def test_int8_append_places_codes_and_scales_at_each_slot():
+    """Read-back through the block tables (block manager of the chenk.top page, "块管理器：
+    分页如何运作"; slot = block * block_size + offset): token t of sequence s is found in
+    block tables[s, t // bs] at offset t % bs, its K codes and K scale in the K arrays
+    and its V codes and V scale in the V arrays, and each row dequantises to within half
+    a step (s / 2) of the row that was appended. A token with slot -1 writes nothing, and
+    every slot no token was given keeps the canary it held before."""
+    rng = np.random.default_rng(17)
+    bs, Hkv, D = 16, 2, 8
+    lengths = np.array([5, 16, 17, 40])
+    tables, _, NB, _ = build_tables(lengths, bs, rng)
+    NB += 1                                # block NB - 1 (index -1) is never in a table
+    canary_code, canary_scale = 99, np.float32(-7.0)
+    kc = np.full((NB, Hkv, bs, D), canary_code, dtype=np.int8)
+    vc = np.full((NB, Hkv, bs, D), -canary_code, dtype=np.int8)
+    ksc = np.full((NB, Hkv, bs), canary_scale, dtype=np.float32)
+    vsc = np.full((NB, Hkv, bs), canary_scale, dtype=np.float32)
+    written = np.zeros((NB, bs), dtype=bool)
+    rows = {}
+    for s, L in enumerate(lengths):
+        slots = [int(tables[s, t // bs]) * bs + t % bs for t in range(L)] + [-1]
+        # K and V of different magnitudes, so that a K/V mix-up shows in the read-back
+        kk = _bf16_exact(rng.standard_normal((L + 1, Hkv, D)) * 5.0).astype(np.float32)
+        vv = _bf16_exact(rng.standard_normal((L + 1, Hkv, D)) * 0.25).astype(np.float32)
+        kk[L] = 1000.0                     # the skipped token: a row no slot may receive
+        vv[L] = -1000.0
+        kc, vc, ksc, vsc = oracle.append_scatter_int8(kk, vv, kc, vc, ksc, vsc, slots, bs)
+        for t in range(L):
+            rows[(s, t)] = (kk[t], vv[t])
+            written[tables[s, t // bs], t % bs] = True
+    for (s, t), (k_row, v_row) in rows.items():
+        blk, off = int(tables[s, t // bs]), t % bs
+        for h in range(Hkv):
+            for codes, scales, x in ((kc, ksc, k_row[h]), (vc, vsc, v_row[h])):
+                sc = float(scales[blk, h, off])
+                amax = float(np.max(np.abs(x)))
+                # the scale belongs to this row: absmax / 127 within fp32 rounding
+                assert abs(sc * 127.0 - amax) <= amax * 1e-6
+                back = codes[blk, h, off].astype(np.float64) * sc
+                # half a step, plus the fp32 rounding of x / s (a ratio up to 127)
+                assert np.all(np.abs(back - x) <= sc * (0.5 + 1e-5))
+                assert np.max(np.abs(codes[blk, h, off].astype(np.int64))) == 127
+    # untouched slots keep their canaries (nothing of the skipped token landed anywhere)
+    for blk in range(NB):
+        for off in range(bs):
+            if written[blk, off]:
+                continue
+            assert np.all(kc[blk, :, off] == canary_code)
+            assert np.all(vc[blk, :, off] == -canary_code)
+            assert np.all(ksc[blk, :, off] == canary_scale)
+            assert np.all(vsc[blk, :, off] == canary_scale)
+
+
 # ---------------------------------------------------------------------------
 # Planted mistakes: every one must be caught by a pin above
 # ---------------------------------------------------------------------------
@@ -534,3 +587,39 @@ def test_pins_catch_round_half_away_from_zero(monkeypatch):
         return np.sign(x) * np.floor(np.abs(x) + 0.5)
     monkeypatch.setattr(np, "rint", away)
     assert _fails(test_quantizer_unit_scale_rounds_half_to_even)
+
+
+def _planted_int8_scatter(swap_kv=False, shift=0):
+    """append_scatter_int8 with a mistake in where rows land: K and V swapped, or the
+    offset inside the block moved by `shift`."""
+    def scatter(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, block_size):
+        kq, ks = pa.quantize_rows_int8(k)
+        vq, vs = pa.quantize_rows_int8(v)
+        kc, vc, ksc, vsc = [np.array(a, copy=True) for a in (k_cache, v_cache, k_scale, v_scale)]
+        if swap_kv:
+            kq, vq, ks, vs = vq, kq, vs, ks
+        for t in range(len(slot_mapping)):
+            slot = int(slot_mapping[t])
+            if slot < 0:
+                continue
+            blk, off = slot // block_size, (slot + shift) % block_size
+            kc[blk, :, off], vc[blk, :, off] = kq[t], vq[t]
+            ksc[blk, :, off], vsc[blk, :, off] = ks[t], vs[t]
+        return kc, vc, ksc, vsc
+    return scatter
+
+
+def test_pins_catch_int8_scatter_misplacement(monkeypatch):
+    _plant(monkeypatch, "append_scatter_int8", _planted_int8_scatter(swap_kv=True))
+    assert _fails(test_int8_append_places_codes_and_scales_at_each_slot)
+    _plant(monkeypatch, "append_scatter_int8", _planted_int8_scatter(shift=1))
+    assert _fails(test_int8_append_places_codes_and_scales_at_each_slot)
+    # a scatter that writes the skipped token (slot -1 read as the last slot of the pool)
+    orig = pa.append_scatter_int8
+
+    def no_skip(k, v, kc, vc, ks, vs, slots, bs):
+        nb = np.shape(kc)[0]
+        slots = [int(x) if int(x) >= 0 else nb * bs - 1 for x in slots]
+        return orig(k, v, kc, vc, ks, vs, slots, bs)
+    _plant(monkeypatch, "append_scatter_int8", no_skip)
+    assert _fails(test_int8_append_places_codes_and_scales_at_each_slot)

@@ -312,16 +312,21 @@ pkv_status pkv_decode_cascade_bf16(void* out, const void* q, const void* k_cache
  *   fixed scratch array of PKV_NOALLOC_SCRATCH_BYTES that the library keeps in device
  *   memory on every GPU that loads it, until the process exits. It allocates nothing
  *   (no cudaMalloc, no cudaFree, no allocating library routine).
- *   Returns PKV_ERR_WORKSPACE, launching nothing, when these dims need more scratch
- *   than PKV_NOALLOC_SCRATCH_BYTES (see pkv_decode_workspace_bytes with PKV_KV_BF16).
- *   The first call on a device looks up the scratch's device address with
- *   cudaGetSymbolAddress (once per device, with that device current); make that first
- *   call before any stream capture.
+ *   Limits: the first PKV_NOALLOC_MAX_SEQ_HEADS * 8 bytes of the array hold the
+ *   counters of the split-KV fold, so num_seqs * num_kv_heads may be at most
+ *   PKV_NOALLOC_MAX_SEQ_HEADS, and the workspace these dims need (see
+ *   pkv_decode_workspace_bytes with PKV_KV_BF16) at most the rest of the array. A call
+ *   beyond either limit returns PKV_ERR_WORKSPACE and launches nothing.
+ *   The array's device address is looked up with cudaGetSymbolAddress the first time a
+ *   call runs under a CUDA context (once per device, and again after a device reset or
+ *   under another context made current on that device); make that first call before
+ *   any stream capture.
  *   Every call on a device shares the one scratch array, which keeps the last call's
  *   contents (nothing in it needs to start at zero). Calls whose executions overlap
  *   on the GPU (different streams, or other threads) race on it: serialise them.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define PKV_NOALLOC_MAX_SEQ_HEADS 65536
 
 pkv_status pkv_decode_bf16_noalloc(void* out, const void* q, const void* k_cache,
                                    const void* v_cache, const int32_t* block_tables,

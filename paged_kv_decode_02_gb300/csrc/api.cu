@@ -282,11 +282,14 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
   return PKV_OK;
 }
 
+// counters (optional): where the in-kernel fixup keeps its [B, Hkv] counter words,
+// counter_words of them, instead of its region of the workspace.
 pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
                       const void* v_cache, const float* k_scale, const float* v_scale,
                       const int32_t* block_tables, const int32_t* context_lens, float scale,
                       const pkv_dims* d, void* workspace, size_t workspace_bytes,
-                      int32_t* status, cudaStream_t stream, int q_len = 1) {
+                      int32_t* status, cudaStream_t stream, int q_len = 1,
+                      unsigned long long* counters = nullptr, size_t counter_words = 0) {
   pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
   if (q_len < 1 || q_len > kMaxQueryLen) return PKV_ERR_SHAPE;
@@ -303,6 +306,9 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   if (st != PKV_OK) return st;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < P.ws_bytes)
+    return PKV_ERR_WORKSPACE;
+  if (counters && ((reinterpret_cast<uintptr_t>(counters) & 7u) != 0 ||
+                   size_t(d->num_seqs) * d->num_kv_heads > counter_words))
     return PKV_ERR_WORKSPACE;
 
   const long long rows = (long long)d->num_blocks * d->num_kv_heads * d->block_size;
@@ -322,7 +328,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   p.part_o = reinterpret_cast<float*>(ws + P.off_o);
   p.part_ml = reinterpret_cast<float*>(ws + P.off_ml);
   p.prefix_out = reinterpret_cast<int32_t*>(ws + P.off_prefix);
-  p.fix_ctr = reinterpret_cast<unsigned long long*>(ws + P.off_ctr);
+  p.fix_ctr = counters ? counters : reinterpret_cast<unsigned long long*>(ws + P.off_ctr);
   // single-token decode without a status word folds its cut units in the decode
   // kernel (the last warp to finish a unit); otherwise the merge kernel does
   // (the tcgen05 kernel: every call without a status word whose fold weights, one per
@@ -568,6 +574,20 @@ pkv_status check_append(const void* k, const void* v, const void* kc, const void
 }
 
 }  // namespace
+
+pkv_status decode_bf16_fixed_counters(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, float scale,
+                                      const pkv_dims* dims, void* workspace,
+                                      size_t workspace_bytes, unsigned long long* counters,
+                                      size_t counter_words, int32_t* status,
+                                      cudaStream_t stream) {
+  if (!counters) return PKV_ERR_NULL;
+  return run_decode(PKV_KV_BF16, out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
+                    context_lens, scale, dims, workspace, workspace_bytes, status, stream, 1,
+                    counters, counter_words);
+}
+
 }  // namespace pkv
 
 using namespace pkv;

@@ -167,13 +167,24 @@ __device__ __forceinline__ unsigned long long grid_launch_id() {
   return g;
 }
 
+// 40-bit tag of this launch for the fixup counters: the launch number spread over all
+// 40 bits by a multiplicative (Fibonacci) hash, never 0. Launch numbers are small
+// integers, so unhashed tags would sit in the low bits, where stale data of another
+// use of the workspace (floats such as +0.0 or small integers) often does; spread
+// tags meet such a word by chance only (one in 2^40 per word).
+__device__ __forceinline__ unsigned long long launch_tag() {
+  const unsigned long long t = ((grid_launch_id() + 1ull) * 0x9E3779B97F4A7C15ull) >> 24;
+  return t == 0ull ? 1ull : t;
+}
+
 // Stream-K fixup inside the decode kernel (single-token decode, one warp per unit row
 // group, no status word): a warp that left a partial record for a cut unit adds the
 // unit items it covered to the unit's counter; the warp whose addition completes the
 // unit's n items folds every part (the same parts and slots the split-KV merge kernel
-// would take) and writes the output. A counter word holds a launch tag (low 40 bits of
-// the grid's launch number) over a 24-bit item count: a word with another tag counts
-// as zero, so the workspace needs no clearing, and the completing warp resets it.
+// would take) and writes the output. A counter word holds a launch tag (launch_tag: a
+// 40-bit hash of the grid's launch number) over a 24-bit item count: a word with
+// another tag counts as zero, so the workspace needs no clearing, and the completing
+// warp resets it.
 // Writers fence their records before the counter update, the completing warp fences
 // after it and reads the records through L2.
 template <int D>
@@ -184,7 +195,7 @@ __device__ __forceinline__ void fixup_cut_unit(const DecodeParams& p, const int*
   __syncwarp();
   int last = 0;
   if (lane == 0) {
-    const unsigned long long tag = grid_launch_id() & ((1ull << 40) - 1ull);
+    const unsigned long long tag = launch_tag();
     unsigned long long* ctr = p.fix_ctr + size_t(s) * p.Hkv + kvh;
     unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
     for (;;) {
@@ -1156,10 +1167,12 @@ __global__ void __launch_bounds__(kWarps * 32)
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(st), par, p.timeout_ns));
     if (!ok) {
       if (lane == 0 && p.status) atomicOr(p.status, 0x4);
-      // let the copies already in flight land before the warp leaves
+      // let every copy in flight land before the warp leaves its shared memory: the
+      // stage that timed out (it is still owed its bytes) and the ones issued after it,
+      // each with a wait of its own, also bounded
       if (leader) {
         const int issued = min(nblk, i + kStages);
-        for (int k2 = i + 1; k2 < issued; ++k2)
+        for (int k2 = i; k2 < issued; ++k2)
           mbar_wait_bounded(bar(k2 % kStages), uint32_t(k2 / kStages) & 1u, p.timeout_ns);
       }
       return;

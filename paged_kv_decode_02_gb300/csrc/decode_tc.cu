@@ -147,8 +147,8 @@ __device__ __forceinline__ long long tc_tiles_before(long long x, const int* pre
 // The parts are the segments of the CTAs whose ranges hold the head's tiles: the first
 // one's last segment (its first when its range starts at the head), then the first
 // segments of the CTAs whose non-empty ranges start inside the head. A counter word
-// holds a launch tag (low 40 bits of the grid's launch number) over a 24-bit tile
-// count: a word with another tag counts as zero, so the workspace needs no clearing,
+// holds a launch tag (launch_tag: a 40-bit hash of the grid's launch number) over a
+// 24-bit tile count: a word with another tag counts as zero, so the workspace needs no clearing,
 // and the completing CTA resets it. Writers fence their records before the counter
 // update, the completing CTA fences after it and reads the records through L2.
 template <int D>
@@ -162,7 +162,7 @@ __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* 
   if (tid < 2 && cut[5 * tid + 4]) {
     volatile int* e = cut + 5 * tid;
     const int s = e[0], h = e[1], n = e[2], mine = e[3];
-    const unsigned long long tag = grid_launch_id() & ((1ull << 40) - 1ull);
+    const unsigned long long tag = launch_tag();
     unsigned long long* ctr = p.fix_ctr + size_t(s) * Hkv + h;
     unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
     int last = 0;

@@ -185,6 +185,17 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args
   return err;
 }
 
+// pkv_decode_bf16 whose in-kernel fixup keeps its [B, Hkv] counter words at
+// `counters` (at least B * Hkv 8-byte words, holding nothing but these counters)
+// rather than in its region of the workspace.
+pkv_status decode_bf16_fixed_counters(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, float scale,
+                                      const pkv_dims* dims, void* workspace,
+                                      size_t workspace_bytes, unsigned long long* counters,
+                                      size_t counter_words, int32_t* status,
+                                      cudaStream_t stream);
+
 cudaError_t launch_append_bf16(const void* k, const void* v, void* k_cache, void* v_cache,
                                const int64_t* slots, int T, int Hkv, int D, int BS, int NB,
                                cudaStream_t stream);

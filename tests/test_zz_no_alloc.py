@@ -7,8 +7,10 @@ serves them from a fixed scratch array kept in the library's device image. This 
 calls it through the C ABI, twice in a row on different shapes (so the second call
 finds the first call's leftovers in the shared scratch), and checks each result
 against the ordinary entry point given a freshly allocated workspace, within the
-tolerance the other decode tests use. It also checks that a shape needing more
-scratch than the fixed maximum is refused without a launch.
+tolerance the other decode tests use. A third call passes a device status word, which
+sends the split-KV parts through the merge kernel (it reads the partials the decode
+left in the shared scratch): the status must stay 0 and the result must match too. It
+also checks that shapes beyond the fixed limits are refused without a launch.
 
 The file name sorts last so that a run stopping at the first failure has already run
 every other test; it builds and loads the library itself so that it also passes alone.
@@ -23,7 +25,10 @@ import torch
 pytestmark = pytest.mark.gpu
 
 DECODE_ATOL = 1e-2
-NOALLOC_MAX_BYTES = 16 << 20      # PKV_NOALLOC_SCRATCH_BYTES in include/pagedkv.h
+NOALLOC_SCRATCH_BYTES = 16 << 20  # PKV_NOALLOC_SCRATCH_BYTES in include/pagedkv.h
+NOALLOC_MAX_SEQ_HEADS = 65536     # PKV_NOALLOC_MAX_SEQ_HEADS in include/pagedkv.h
+# the first PKV_NOALLOC_MAX_SEQ_HEADS 8-byte words of the scratch hold counters only
+NOALLOC_MAX_BYTES = NOALLOC_SCRATCH_BYTES - 8 * NOALLOC_MAX_SEQ_HEADS
 
 
 def _lib():
@@ -62,16 +67,22 @@ def test_noalloc_decode_matches_allocating_entry_point():
         make_workload("70b-gqa", device="cuda", num_seqs=12, seed=21),           # g = 8
         make_workload("7b", device="cuda", lengths=[3, 2048, 700, 1, 64], seed=22),  # MHA
     ]
-    for w in cases:
+    # (workload, pass a status word): the third call repeats the MHA shape, whose
+    # 2048-token sequence is split over several workers, with a status word
+    for w, with_status in ((cases[0], False), (cases[1], False), (cases[1], True)):
         ref, need = _reference(lib, pagedkv, w, stream)
         assert need <= NOALLOC_MAX_BYTES
         dims, p = _args(w, pagedkv)
         out = torch.full_like(w.q, float("nan"))
+        status = torch.zeros(1, dtype=torch.int32, device="cuda") if with_status else None
         st = lib.pkv_decode_bf16_noalloc(p(out), p(w.q), p(w.k_cache), p(w.v_cache),
                                          p(w.block_tables), p(w.context_lens), w.scale,
-                                         ctypes.byref(dims), None, stream)
+                                         ctypes.byref(dims),
+                                         p(status) if with_status else None, stream)
         assert st == 0, lib.pkv_status_string(st)
         torch.cuda.synchronize()
+        if with_status:
+            assert int(status.item()) == 0
         got = out.double().cpu().numpy()
         assert np.all(np.isfinite(got))
         assert float(np.max(np.abs(got - ref.double().cpu().numpy()))) <= DECODE_ATOL
@@ -86,6 +97,22 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(dims), pagedkv.KV_BF16,
                                           ctypes.byref(need)) == 0
     assert need.value > NOALLOC_MAX_BYTES
+    p = ctypes.c_void_p(256)
+    st = lib.pkv_decode_bf16_noalloc(p, p, p, p, p, p, 0.1, ctypes.byref(dims), None, None)
+    assert st == pagedkv.Status.ERR_WORKSPACE
+
+
+def test_noalloc_refuses_more_sequence_heads_than_its_counters():
+    pagedkv, lib = _lib()
+    torch.cuda.set_device(0)
+    # 2100 sequences x 32 KV heads = 67200 (sequence, KV head) counters, over the limit,
+    # on a shape whose workspace alone would fit
+    dims = pagedkv.Dims(2100, 32, 32, 64, 16, 4096, 4)
+    need = ctypes.c_size_t(0)
+    assert lib.pkv_decode_workspace_bytes(ctypes.byref(dims), pagedkv.KV_BF16,
+                                          ctypes.byref(need)) == 0
+    assert need.value <= NOALLOC_MAX_BYTES
+    assert 2100 * 32 > NOALLOC_MAX_SEQ_HEADS
     p = ctypes.c_void_p(256)
     st = lib.pkv_decode_bf16_noalloc(p, p, p, p, p, p, 0.1, ctypes.byref(dims), None, None)
     assert st == pagedkv.Status.ERR_WORKSPACE

@@ -3,13 +3,19 @@
 (paged_kv_append) and attend over the whole paged cache (paged_decode_attention,
 split-KV merge included), on seeded synthetic inputs shaped like the pages' workloads.
 
-Prints ONE JSON line (rank 0). ``value`` is achieved HBM throughput in GB/s of
-algorithmic bytes (valid KV rows + scales + q + out + used table entries + context
-lengths + the appended rows) over the measured step time, summed over ranks; the line
-also carries KV tokens/s, the roofline of the decode kernel, an end-to-end figure with
-host buffers, clocks, and the CPU oracle timed on a bounded sample.
+Prints ONE JSON line (rank 0). The headline is the largest workload, ``prefix`` (batch
+256, a 2048-token prefix shared by every request plus private suffixes), decoded
+through the shared-prefix (cascade) entry point. ``value`` is achieved HBM throughput
+in GB/s of algorithmic bytes that must cross HBM at least once per step: the distinct
+physical KV rows (shared prefix blocks counted once) + scales + q + out + used table
+entries + context lengths + the appended rows, over the measured step time, summed
+over ranks; the logical-byte figure (every request's whole context, the prefix once
+per request) is reported beside it as ``effective``. The line also carries KV
+tokens/s, the roofline of the decode call, one record per other workload
+(``per_config``), an end-to-end figure with host buffers, clocks, and the CPU oracle
+timed on all host cores over a bounded sample.
 
-    python bench.py [--config 7b] [--steps K] [--warmup W] [--gpus N]
+    python bench.py [--config prefix] [--plain] [--steps K] [--warmup W] [--gpus N]
     python bench.py --impl reference ...     # the CPU oracle as the reference arm
 """
 
@@ -56,24 +62,44 @@ WORKLOAD_TEXT = {
                     "log-normal (median 1024, sigma 1) clipped [128, 32768], q_len 16 new "
                     "tokens per request (128 query rows per KV head), causal",
 }
+# the workloads recorded beside the headline, each as (config, cascade)
+PER_CONFIG = [("tiny", False), ("7b", False), ("70b-gqa", False), ("prefix", False),
+              ("int8", False), ("int8-bs16", False), ("fp8-e5m2", False), ("fp8-e4m3", False),
+              ("spec-70b", False), ("spec-70b-q16", False)]
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="7b", choices=sorted(WORKLOAD_TEXT))
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--config", default="prefix", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--plain", action="store_true",
+                    help="prefix workload: decode through the ordinary entry point instead of "
+                         "the shared-prefix (cascade) one")
+    ap.add_argument("--cascade", action="store_true",
+                    help="(the default for the prefix workload) decode through the "
+                         "shared-prefix entry point")
+    ap.add_argument("--min-seconds", type=float, default=0.5,
+                    help="device time of graph replays per timed series of the headline")
+    ap.add_argument("--per-config-seconds", type=float, default=0.25,
+                    help="device time of graph replays per timed series of a per_config record")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="wall time of the CPU oracle baseline on all host cores")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="reference arm: wall time of the oracle over all steps and warm-up")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--cascade", action="store_true",
-                    help="prefix workload: decode through the shared-prefix (cascade) entry point")
-    return ap.parse_args()
+    ap.add_argument("--no-per-config", action="store_true")
+    args = ap.parse_args(argv)
+    if args.cascade and args.config != "prefix":
+        ap.error("--cascade needs the prefix workload (a prefix shared by every request)")
+    args.use_cascade = args.config == "prefix" and not args.plain
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -85,17 +111,43 @@ def _one_byte(w):
     return w.kv_dtype != "bf16"
 
 
-def decode_bytes(w):
+def _row_bytes(w):
+    """Bytes of one token's K and V rows of every KV head (+ their scales)."""
+    elt = 1 if _one_byte(w) else 2
+    return 2 * w.num_kv_heads * w.head_dim * elt + (2 * w.num_kv_heads * 4 if _one_byte(w) else 0)
+
+
+def unique_kv_tokens(w):
+    """Distinct physical KV token rows one decode call must read (a block shared by
+    several tables counted once, each block to its furthest filled slot)."""
     import numpy as np
     L = w.context_lens.cpu().numpy().astype(np.int64)
-    elt = 1 if _one_byte(w) else 2
+    bt = w.block_tables.cpu().numpy()
+    fill = {}
+    for s, Ls in enumerate(L):
+        n = -(-int(Ls) // w.block_size)
+        for j in range(n):
+            f = min(w.block_size, int(Ls) - j * w.block_size)
+            b = int(bt[s, j])
+            if f > fill.get(b, 0):
+                fill[b] = f
+    return int(sum(fill.values()))
+
+
+def decode_bytes(w):
+    """Algorithmic bytes of one decode call: ``total`` counts distinct physical KV rows
+    (what must cross HBM), ``logical`` every request's whole context (a shared prefix
+    once per request); q, out, used table entries and context lengths in both."""
+    import numpy as np
+    L = w.context_lens.cpu().numpy().astype(np.int64)
     tokens = int(L.sum())
-    kv = tokens * 2 * w.num_kv_heads * w.head_dim * elt
-    scales = tokens * 2 * w.num_kv_heads * 4 if _one_byte(w) else 0
+    uniq = unique_kv_tokens(w)
+    rb = _row_bytes(w)
     qo = 2 * w.num_seqs * w.q_len * w.num_q_heads * w.head_dim * 2
-    tables = int(sum(-(-int(x) // w.block_size) for x in L)) * 4
-    return {"kv": kv, "scales": scales, "q_out": qo, "tables": tables + 4 * w.num_seqs,
-            "total": kv + scales + qo + tables + 4 * w.num_seqs, "tokens": tokens}
+    tables = int(sum(-(-int(x) // w.block_size) for x in L)) * 4 + 4 * w.num_seqs
+    return {"kv": uniq * rb, "kv_logical": tokens * rb, "q_out": qo, "tables": tables,
+            "total": uniq * rb + qo + tables, "logical": tokens * rb + qo + tables,
+            "tokens": tokens, "unique_tokens": uniq}
 
 
 def append_bytes(w):
@@ -104,21 +156,6 @@ def append_bytes(w):
     rows = T * 2 * w.num_kv_heads * w.head_dim
     scales = T * 2 * w.num_kv_heads * 4 if _one_byte(w) else 0
     return rows * 2 + rows * elt + scales + 8 * w.slot_mapping.numel()
-
-
-def unique_kv_bytes(w):
-    """Bytes of distinct physical KV rows the step touches (prefix blocks counted once)."""
-    import numpy as np
-    L = w.context_lens.cpu().numpy()
-    bt = w.block_tables.cpu().numpy()
-    seen = {}
-    for s, Ls in enumerate(L):
-        n = -(-int(Ls) // w.block_size)
-        for j in range(n):
-            fill = min(w.block_size, int(Ls) - j * w.block_size)
-            seen[int(bt[s, j])] = max(seen.get(int(bt[s, j]), 0), fill)
-    elt = 1 if _one_byte(w) else 2
-    return sum(seen.values()) * 2 * w.num_kv_heads * w.head_dim * elt
 
 
 def source_digest():
@@ -134,7 +171,7 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
-def measured_traffic(config):
+def measured_traffic(key):
     """DRAM bytes per decode call from the committed ncu summary, or None when the
     library sources changed since the capture (or the workload was not captured)."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
@@ -149,7 +186,7 @@ def measured_traffic(config):
                     table[parts[1]] = int(parts[2])
         if digest != source_digest():
             return None
-        return table.get(config)
+        return table.get(key)
     except OSError:
         return None
 
@@ -163,12 +200,36 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def config_key(name, cascade):
+    return name + ("+cascade" if cascade else "")
+
+
+def config_record(name, cascade, w, world):
+    """The ``config`` object of a JSON line (shared by both arms)."""
+    db = decode_bytes(w)
+    return {"workload": WORKLOAD_TEXT[name] + (" (shared-prefix cascade decode)" if cascade
+                                               else ""),
+            "name": config_key(name, cascade),
+            "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "num_blocks": w.num_blocks, "q_len": w.q_len,
+            "kv_dtype": w.kv_dtype, "kv_tokens": db["tokens"],
+            "unique_kv_tokens": db["unique_tokens"],
+            "step_bytes": db["total"] + append_bytes(w),
+            "step_bytes_logical": db["logical"] + append_bytes(w),
+            "l2": f"inputs larger than L2: {db['kv'] / 1e6:.0f} MB of distinct KV per step vs "
+                  f"{L2_BYTES / 1e6:.0f} MB L2, no flush" if db["kv"] > L2_BYTES else
+                  f"{db['kv'] / 1e6:.1f} MB of distinct KV per step fits the {L2_BYTES / 1e6:.0f} "
+                  f"MB L2 (no flush: a per_config record, not the headline)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 # ---------------------------------------------------------------------------
-# Clocks sampled during the timed region
+# Clocks sampled during the timed regions
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -199,102 +260,77 @@ class ClockSampler:
         self.file.seek(0)
         rows = [r.strip().split(", ") for r in self.file.read().strip().splitlines() if r.strip()]
         os.unlink(self.file.name)
-        sm, mx, reasons = [], [], set()
+        sm, mx, load_sm, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             if len(r) < 9:
                 continue
             try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
+                mhz, top = float(r[1]), float(r[2])
             except ValueError:
                 continue
-            for n, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
+            sm.append(mhz)
+            mx.append(top)
+            try:
+                busy = float(r[4]) >= 50.0
+            except ValueError:
+                busy = False
+            if busy:
+                load_sm.append(mhz)
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+        use = load_sm or sm
+        return {"sm_mhz": statistics.median(use) if use else None,
                 "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "samples_under_load": len(load_sm),
+                "sm_mhz_median_under_load": statistics.median(load_sm) if load_sm else None,
+                "under_load": "nvidia-smi utilization.gpu >= 50 %, sampled every 100 ms",
                 "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle on a bounded sample (the reported baseline and the reference arm)
+# CPU oracle on all host cores over a bounded sample (the reported baseline and the
+# reference arm)
 # ---------------------------------------------------------------------------
 
-def _host_units(w, count, seed=0):
-    """Copy `count` (sequence, KV head) units of the workload to host arrays."""
+def oracle_sample(w, count, seed=0):
+    """Host copies of ``count`` randomly drawn (sequence, KV head) units."""
     import numpy as np
-    import torch
+    from paged_kv_decode_02_gb300.workloads import host_units
     rng = np.random.default_rng(seed)
-    units = []
-    g = w.num_q_heads // w.num_kv_heads
-    for _ in range(count):
-        s = int(rng.integers(w.num_seqs))
-        kvh = int(rng.integers(w.num_kv_heads))
-        L = int(w.context_lens[s].item())
-        n = -(-L // w.block_size)
-        blocks = w.block_tables[s, :n].to(torch.int64)
-        qs = w.q[s] if w.q_len > 1 else w.q[s][None]        # [q_len, Hq, D]
-        unit = {"L": L, "q": qs[:, kvh * g:(kvh + 1) * g].double().cpu().numpy(),
-                "table": np.arange(n)}
-        if _one_byte(w):
-            unit["k"] = w.k_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
-            unit["v"] = w.v_cache[blocks][:, kvh:kvh + 1].cpu().numpy()
-            unit["ks"] = w.k_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
-            unit["vs"] = w.v_scale[blocks][:, kvh:kvh + 1].cpu().numpy()
-        else:
-            unit["k"] = w.k_cache[blocks][:, kvh:kvh + 1].double().cpu().numpy()
-            unit["v"] = w.v_cache[blocks][:, kvh:kvh + 1].double().cpu().numpy()
-        units.append(unit)
-    return units
+    pairs = [(int(rng.integers(w.num_seqs)), int(rng.integers(w.num_kv_heads)))
+             for _ in range(count)]
+    return host_units(w, pairs)
 
 
-def _oracle_unit(w, u):
-    import oracle
-    if w.kv_dtype == "int8":
-        K = oracle.gather_sequence_int8(u["k"], u["ks"], u["table"], u["L"], 0, w.block_size)
-        V = oracle.gather_sequence_int8(u["v"], u["vs"], u["table"], u["L"], 0, w.block_size)
-    elif w.kv_dtype.startswith("fp8_"):
-        f = w.kv_dtype[4:]
-        K = oracle.gather_sequence_fp8(u["k"], u["ks"], u["table"], u["L"], 0, w.block_size, f)
-        V = oracle.gather_sequence_fp8(u["v"], u["vs"], u["table"], u["L"], 0, w.block_size, f)
-    else:
-        K = oracle.gather_sequence(u["k"], u["table"], u["L"], 0, w.block_size)
-        V = oracle.gather_sequence(u["v"], u["table"], u["L"], 0, w.block_size)
-    n = u["q"].shape[0]
-    for i in range(n):                       # causal window of new token i
-        visible = max(u["L"] - n + i + 1, 0)
-        for qh in u["q"][i]:
-            oracle.attend_one_head(qh, K[:visible], V[:visible], w.scale)
+def cpu_rate(pool, units, seconds):
+    """Oracle throughput of the host cores on the sample: (KV tokens/s, logical
+    GB/s of the units, units done, elapsed s)."""
+    b, t, c, el = pool.run(units, seconds)
+    return t / el, b / el / 1e9, c, el
 
 
-def _unit_bytes(w, u):
-    elt = 1 if _one_byte(w) else 2
-    g = w.num_q_heads // w.num_kv_heads
-    b = (u["L"] * 2 * w.head_dim * elt + 2 * w.q_len * g * w.head_dim * 2 +
-         4 * len(u["table"]))
-    if _one_byte(w):
-        b += u["L"] * 2 * 4
-    return b
-
-
-def cpu_baseline(w, seconds):
-    units = _host_units(w, 64)
-    t0 = time.perf_counter()
-    done_bytes = done_tokens = n = 0
-    while True:
-        u = units[n % len(units)]
-        _oracle_unit(w, u)
-        done_bytes += _unit_bytes(w, u)
-        done_tokens += u["L"]
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return {"value": done_bytes / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "kv_tokens_per_s": done_tokens / el,
-            "sample": f"{n} (sequence, kv-head) units of the {w.name} workload "
-                      f"({done_tokens} KV tokens, {el:.1f} s, fp64 numpy, one thread)"}
+def cpu_record(w, cascade, seconds, world):
+    """The oracle as it stands, timed on every host core for ``seconds`` over a sample
+    of the workload's (sequence, KV head) units, expressed in the GPU line's metric:
+    the time the host would need for one whole step at the measured KV tokens/s, and
+    the step's bytes (distinct physical KV, as in ``value``) over that time."""
+    from oracle import parallel
+    units = oracle_sample(w, max(4 * parallel.host_cores(), 32))
+    with parallel.TimedPool() as pool:
+        tok_s, logical_gbs, n, el = cpu_rate(pool, units, seconds)
+        cores = pool.processes
+    db = decode_bytes(w)
+    step_s = db["tokens"] / tok_s
+    value = (db["total"] + append_bytes(w)) / step_s / 1e9
+    return {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "kv_tokens_per_s": tok_s, "logical_gbs": logical_gbs, "step_s": step_s,
+            "sample": f"{n} (sequence, kv-head) units of the {config_key(w.name, cascade)} "
+                      f"workload drawn from {len(units)} ({int(tok_s * el)} KV tokens in "
+                      f"{el:.1f} s), fp64 numpy oracle, one spawned process per host core "
+                      f"({cores}); value = the step's bytes over the time one whole step "
+                      f"({db['tokens']} KV tokens) takes at that rate"}
 
 
 # ---------------------------------------------------------------------------
@@ -336,24 +372,8 @@ def api_decode(pk, w, q, tables, lens, out, ws, cascade_blocks=0):
                                   workspace=ws)
 
 
-def run_ours(args, rank, world):
+def workspace_for(pk, w, cascade_blocks, dev):
     import torch
-
-    import paged_kv_decode_02_gb300 as pk
-    from paged_kv_decode_02_gb300 import build_lib
-    from paged_kv_decode_02_gb300.workloads import make_workload
-
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    if rank == 0 or not os.path.exists(build_lib.LIB):
-        build_lib.build()
-    if world > 1:
-        torch.distributed.barrier()
-    pk.load_library()
-    w = make_workload(args.config, device=dev)
-    cascade_blocks = w.extra.get("prefix_tokens", 0) // w.block_size if args.cascade else 0
-    if args.cascade and (_one_byte(w) or cascade_blocks == 0):
-        raise SystemExit("--cascade needs a bf16 workload with a shared prefix (prefix)")
     if cascade_blocks:
         need = pk.cascade_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                           w.block_size, w.num_blocks, w.max_blocks_per_seq,
@@ -366,9 +386,44 @@ def run_ours(args, rank, world):
         need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                          w.block_size, w.num_blocks, w.max_blocks_per_seq,
                                          _kv_code(pk, w))
-    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    return torch.zeros(need, dtype=torch.uint8, device=dev)
+
+
+def replay_series(graph, stream, min_seconds, max_replays=4000):
+    """Replay a captured graph back to back until at least ``min_seconds`` of device
+    time, with CUDA events on the launching stream between replays (issued in batches
+    so the device never waits for the host); returns the per-replay times in ms."""
+    import torch
+    graph.replay()                       # one untimed replay sizes the series
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    graph.replay()
+    b.record(stream)
+    b.synchronize()
+    one = max(a.elapsed_time(b), 1e-3)
+    n = int(min(max_replays, max(3, math.ceil(min_seconds * 1e3 / one))))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    ev[0].record(stream)
+    for i in range(n):
+        graph.replay()
+        ev[i + 1].record(stream)
+    ev[n].synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+
+
+def measure_workload(pk, name, cascade, args, dev, world, min_seconds, with_e2e=False):
+    """Time one workload: R replays of a graph of K steps (append + decode call) and R'
+    replays of a graph of K decode calls; medians per step / per call."""
+    import torch
+    from paged_kv_decode_02_gb300.workloads import make_workload
+    w = make_workload(name, device=dev)
+    cascade_blocks = w.extra.get("prefix_tokens", 0) // w.block_size if cascade else 0
+    if cascade and (_one_byte(w) or cascade_blocks == 0):
+        raise SystemExit("cascade decode needs a bf16 workload with a shared prefix (prefix)")
+    ws = workspace_for(pk, w, cascade_blocks, dev)
     out = torch.empty_like(w.q)
     stream = torch.cuda.current_stream(dev)
+    lib = pk.pagedkv.load_library()
 
     def append():
         api_append(pk, w, w.new_k, w.new_v, w.slot_mapping)
@@ -380,98 +435,131 @@ def run_ours(args, rank, world):
         append()
         decode()
     torch.cuda.synchronize(dev)
-
-    # The K timed steps are captured once into a CUDA graph (as a serving loop replays
-    # its decode step), so the device time is not bounded by Python launch overhead.
-    # No events sit between the kernels: append, decode and merge chain with
+    K = max(1, args.steps)
+    # The K steps are captured once into a CUDA graph (as a serving loop replays its
+    # decode step), so the device time is not bounded by Python launch overhead. No
+    # events sit between the kernels of a replay: append, decode and merge chain with
     # programmatic dependent launch exactly as in a user's stream.
-    K = args.steps
-    lib = pk.pagedkv.load_library()
     launches0 = lib.pkv_kernel_launch_count()
     step_graph = capture(K, lambda: (append(), decode()), dev)
-    step_launches = lib.pkv_kernel_launch_count() - launches0   # kernels in the K steps
-    step_graph.replay()                 # upload + warm replay (untimed)
-    torch.cuda.synchronize(dev)
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev.index) if (rank == 0 and not args.no_clocks) else None
+    step_launches = lib.pkv_kernel_launch_count() - launches0        # kernels in K steps
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    if clocks:
-        clocks.start()
-        time.sleep(0.3)  # let the sampler start before the timed region
-    t_start.record(stream)
-    step_graph.replay()
-    t_end.record(stream)
+    step_ms = replay_series(step_graph, stream, min_seconds)
     torch.cuda.synchronize(dev)
-    # roofline of the dominant call: K back-to-back decode calls (decode + merge
-    # kernels) in a second timed region, CUDA events on the launching stream
     launches0 = lib.pkv_kernel_launch_count()
     dec_graph = capture(K, decode, dev)
     dec_launches = (lib.pkv_kernel_launch_count() - launches0) // K
-    dec_graph.replay()
+    dec_ms = replay_series(dec_graph, stream, min_seconds)
     torch.cuda.synchronize(dev)
-    d_start, d_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d_start.record(stream)
-    dec_graph.replay()
-    d_end.record(stream)
-    torch.cuda.synchronize(dev)
-    clk = clocks.stop() if clocks else None
     if world > 1:
         torch.distributed.barrier()
-    ms_total = t_start.elapsed_time(t_end)
-    dec_ms = d_start.elapsed_time(d_end) / K
-    dec_how = ("CUDA events around K back-to-back decode calls (decode + merge kernels, "
-               "graph replay) after the K timed steps")
-    ms_total = job_time_ms(ms_total, world, dev)
-    ms_step = ms_total / K
-
+    ms_step = job_time_ms(statistics.median(step_ms) / K, world, dev)
+    ms_dec = statistics.median(dec_ms) / K
     db = decode_bytes(w)
     step_bytes = db["total"] + append_bytes(w)
-    value = job_throughput(step_bytes, ms_step, world)
-    tokens_per_s = world * db["tokens"] / (ms_step * 1e-3)
     peak, peak_kind = measured_peak()
-    achieved = db["total"] / (dec_ms * 1e-3) / 1e9
+    achieved = db["total"] / (ms_dec * 1e-3) / 1e9
+    rec = {"w": w, "ws": ws, "out": out, "cascade_blocks": cascade_blocks, "db": db,
+           "step_bytes": step_bytes, "ms_step": ms_step, "ms_dec": ms_dec,
+           "replays": len(step_ms), "dec_replays": len(dec_ms),
+           "step_launches": step_launches, "dec_launches": dec_launches,
+           "value": job_throughput(step_bytes, ms_step, world),
+           "effective": job_throughput(db["logical"] + append_bytes(w), ms_step, world),
+           "tokens_per_s": world * db["tokens"] / (ms_step * 1e-3),
+           "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                        "unit": "GB/s", "frac": round(achieved / peak, 4),
+                        "traffic": measured_traffic(config_key(name, cascade)),
+                        "traffic_source": "profiles/decode_traffic.txt (ncu dram bytes "
+                                          "read+write, every kernel of one decode call)",
+                        "kernel": decode_kernels(w, cascade_blocks, dec_launches),
+                        "launches_per_call": dec_launches,
+                        "bytes_per_launch": db["total"],
+                        "bytes_counted": "distinct physical KV rows + q + out + used table "
+                                         "entries + context lengths",
+                        "effective_gbs": round(db["logical"] / (ms_dec * 1e-3) / 1e9, 2),
+                        "effective_bytes_per_launch": db["logical"],
+                        "avg_launch_ms": round(ms_dec, 5),
+                        "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy "
+                                       f"bandwidth)" if peak_kind == "measured"
+                                       else "fallback 6.8 TB/s",
+                        "timing": f"median over {len(dec_ms)} replays of a CUDA graph of K "
+                                  f"back-to-back decode calls (decode + merge kernels), CUDA "
+                                  f"events on the launching stream"}}
+    if with_e2e and not args.no_e2e:
+        rec["e2e"] = run_e2e(args, w, pk, dev, out, ws, step_bytes, world, cascade_blocks)
+    return rec
 
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, w, pk, dev, append, out, ws, step_bytes, world, cascade_blocks)
 
+def per_config_line(name, cascade, r):
+    rf = r["roofline"]
+    return {"name": config_key(name, cascade), "workload": WORKLOAD_TEXT[name],
+            "kv_dtype": r["w"].kv_dtype, "ms_per_step": round(r["ms_step"], 5),
+            "step_gbs": round(r["value"], 2), "decode_call_ms": rf["avg_launch_ms"],
+            "algorithmic_bytes": rf["bytes_per_launch"], "achieved_gbs": rf["achieved"],
+            "frac": rf["frac"], "effective_gbs": rf["effective_gbs"],
+            "traffic": rf["traffic"], "kernel": rf["kernel"],
+            "launches_per_call": rf["launches_per_call"],
+            "kv_tokens_per_s": round(r["tokens_per_s"], 1), "replays": r["replays"]}
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import paged_kv_decode_02_gb300 as pk
+    from paged_kv_decode_02_gb300 import build_lib
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pk.load_library()
+    clocks = ClockSampler(dev.index) if (rank == 0 and not args.no_clocks) else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)  # let the sampler start before the timed regions
+    r = measure_workload(pk, args.config, args.use_cascade, args, dev, world, args.min_seconds,
+                         with_e2e=True)
+    w = r["w"]
+    per_config = []
+    if not args.no_per_config and args.config == "prefix" and args.use_cascade:
+        for name, casc in PER_CONFIG:
+            rr = measure_workload(pk, name, casc, args, dev, world, args.per_config_seconds)
+            per_config.append(per_config_line(name, casc, rr))
+            del rr
+            torch.cuda.empty_cache()
+    clk = clocks.stop() if clocks else None
+    peak, _ = measured_peak()
+    K = max(1, args.steps)
     result = {
         "metric": "paged decode attention: achieved HBM GB/s (% of GB300 peak) and KV tokens/s",
-        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+        "value": round(r["value"], 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(r["ms_step"], 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype,
         "data": "synthetic (seeded)",
-        "kv_tokens_per_s": round(tokens_per_s, 1),
-        "pct_of_peak": round(100.0 * value / world / peak, 2),
-        "config": {"workload": WORKLOAD_TEXT[args.config] + (" (cascade decode)" if cascade_blocks
-                                                             else ""),
-                   "name": args.config + ("+cascade" if cascade_blocks else ""),
-                   "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "block_size": w.block_size, "num_blocks": w.num_blocks,
-                   "kv_tokens": db["tokens"], "step_bytes": step_bytes,
-                   "unique_kv_bytes": unique_kv_bytes(w) if args.config == "prefix" else None,
-                   "l2": f"inputs larger than L2: {db['kv'] / 1e6:.0f} MB of KV per step vs "
-                         f"{L2_BYTES / 1e6:.0f} MB L2, no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": measured_traffic(args.config),
-                     "traffic_source": "profiles/decode_traffic.txt (ncu dram bytes read+write, "
-                                       "every kernel of one decode call)",
-                     "kernel": decode_kernels(w, cascade_blocks, dec_launches),
-                     "launches_per_call": dec_launches,
-                     "bytes_per_launch": db["total"], "avg_launch_ms": round(dec_ms, 5),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "timing": dec_how},
-        "gpu_launches": step_launches,
+        "timing": f"median over {r['replays']} back-to-back replays of a CUDA graph of the K "
+                  f"steps (CUDA events on the launching stream between replays), per step; "
+                  f"max over ranks",
+        "replays": r["replays"],
+        "kv_tokens_per_s": round(r["tokens_per_s"], 1),
+        "effective_gbs": round(r["effective"], 2),
+        "effective": "the same steps over logical bytes (every request's whole context, a "
+                     "shared prefix once per request): what a decode reading each request's "
+                     "blocks from HBM would have to move",
+        "pct_of_peak": round(100.0 * r["value"] / world / peak, 2),
+        "config": config_record(args.config, args.use_cascade, w, world),
+        "roofline": r["roofline"],
+        "gpu_launches": r["step_launches"] * r["replays"],
+        "gpu_launches_per_step": r["step_launches"] / K,
         "clocks": clk,
     }
-    if e2e is not None:
-        result["e2e"] = e2e
+    if per_config:
+        result["per_config"] = per_config
+    if "e2e" in r:
+        result["e2e"] = r["e2e"]
     return result, w
 
 
@@ -642,7 +730,7 @@ def capture(K, fn, dev):
     return g
 
 
-def run_e2e(args, w, pk, dev, append_dev, out, ws, step_bytes, world, cascade_blocks=0):
+def run_e2e(args, w, pk, dev, out, ws, step_bytes, world, cascade_blocks=0):
     """Same step through the public API from pinned HOST buffers: per step, copy the
     step's inputs host->device (one copy of a packed buffer), append + decode, copy the
     output device->host."""
@@ -682,23 +770,32 @@ def run_e2e(args, w, pk, dev, append_dev, out, ws, step_bytes, world, cascade_bl
     # the packed inputs are the device-resident step's inputs: the same result
     if not torch.equal(host_out, ref.cpu()):
         raise RuntimeError("end-to-end step disagrees with the device-resident step")
-    K = max(1, min(args.steps, 500))
+    K = max(1, args.steps)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(K):
         step()
     b.record(stream)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / K
+    est = a.elapsed_time(b) / K
+    n = int(min(5000, max(K, math.ceil(300.0 / max(est, 1e-3)))))   # >= 0.3 s of steps
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = job_time_ms(a.elapsed_time(b) / n, world, dev)
     return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "ms_per_step": round(ms, 5), "steps": K,
+            "ms_per_step": round(ms, 5), "steps": n,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
 def run_reference(args, rank):
-    """The CPU oracle as the reference arm: each step runs it, as it stands, on a
-    bounded sample of the same workload on the host cores."""
+    """The CPU oracle as the reference arm: each step runs it, as it stands, on all host
+    cores over a bounded sample of the same workload, expressed in the same metric and
+    config as our arm (the time a whole step would take at the measured KV tokens/s)."""
     import torch
+    from oracle import parallel
     from paged_kv_decode_02_gb300.workloads import make_workload
     if rank != 0:
         return None
@@ -715,39 +812,40 @@ def run_reference(args, rank):
                 "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
     w = make_workload(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
-    units = _host_units(w, 16, seed=1)
-    budget_s = 150.0
-    per_step = max(1e-3, budget_s / max(1, args.steps + args.warmup))
-    done_bytes = 0
-    done_tokens = 0
-    for _ in range(args.warmup):
-        _oracle_unit(w, units[0])
-    t0 = time.perf_counter()
-    n = 0
-    for _ in range(args.steps):
-        ts = time.perf_counter()
-        while True:
-            u = units[n % len(units)]
-            _oracle_unit(w, u)
-            done_bytes += _unit_bytes(w, u)
-            done_tokens += u["L"]
-            n += 1
-            if time.perf_counter() - ts >= per_step:
-                break
-    el = time.perf_counter() - t0
-    value = done_bytes / el / 1e9
-    sample = (f"{n} (sequence, kv-head) units of the {args.config} workload per run "
-              f"({done_tokens} KV tokens), fp64 numpy oracle, one thread")
+    units = oracle_sample(w, max(4 * parallel.host_cores(), 32), seed=1)
+    db = decode_bytes(w)
+    step_bytes = db["total"] + append_bytes(w)
+    per_step = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
+    done_tok = 0.0
+    el_tot = 0.0
+    n_units = 0
+    with parallel.TimedPool() as pool:
+        cores = pool.processes
+        for _ in range(args.warmup):
+            pool.run(units, per_step)
+        for _ in range(args.steps):
+            _, t, c, el = pool.run(units, per_step)
+            done_tok += t
+            el_tot += el
+            n_units += c
+    tok_s = done_tok / el_tot
+    step_s = db["tokens"] / tok_s
+    value = step_bytes / step_s / 1e9
+    sample = (f"{n_units} (sequence, kv-head) units of the "
+              f"{config_key(args.config, args.use_cascade)} workload drawn from {len(units)}, "
+              f"{per_step:.2f} s of wall time per step on {cores} spawned processes (one per "
+              f"host core), fp64 numpy oracle; ms_per_step = the time one whole step "
+              f"({db['tokens']} KV tokens) takes at the measured rate")
     return {
         "impl": "reference",
         "metric": "paged decode attention: achieved HBM GB/s (% of GB300 peak) and KV tokens/s",
         "value": round(value, 6), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(1e3 * el / max(1, args.steps), 3),
+        "warmup": args.warmup, "ms_per_step": round(1e3 * step_s, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "kv_tokens_per_s": round(done_tokens / el, 1),
-        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config},
-        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "data": "synthetic (seeded)", "kv_tokens_per_s": round(tok_s, 1),
+        "config": config_record(args.config, args.use_cascade, w, 1),
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -773,7 +871,7 @@ def main():
     else:
         res, w = run_ours(args, rank, world)
         if rank == 0 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+            res["cpu_baseline"] = cpu_record(w, args.use_cascade, args.cpu_seconds, world)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -373,3 +373,48 @@ def make_workload(name: str, device="cpu", seed: Optional[int] = None,
         new_k=new_k, new_v=new_v, slot_mapping=torch.from_numpy(last_slots).to(dev),
         k_scale=k_scale, v_scale=v_scale, refcount=alloc.refcount.copy(),
         extra={"prefix_tokens": prefix}, q_len=n_new)
+
+
+def host_units(w: Workload, pairs) -> list:
+    """Host copies of (sequence, KV head) units of a workload, in the form the CPU
+    oracle's process pool takes: each unit holds its sequence's blocks of that KV head
+    re-indexed 0..n-1 (bf16 rows as their 16-bit patterns, one-byte codes and their
+    scales as stored), the KV head's q rows as float64 [q_len, g, D], the context
+    length, and its byte and token counts for throughput accounting (valid KV rows,
+    scales, q and out rows, table entries). Only copies: no arithmetic of the method."""
+    g = w.group
+    bs = w.block_size
+    one_byte = w.kv_dtype != "bf16"
+    elt = 1 if one_byte else 2
+    L_all = w.context_lens.cpu().numpy()
+    q = w.q if w.q_len > 1 else w.q[:, None]          # [B, q_len, Hq, D]
+    by_seq: dict = {}
+    for s, kvh in pairs:
+        by_seq.setdefault(int(s), []).append(int(kvh))
+    units = {}
+    for s, kvhs in by_seq.items():
+        L = int(L_all[s])
+        n = -(-L // bs)
+        blocks = w.block_tables[s, :n].to(torch.int64)
+        kc, vc = w.k_cache[blocks], w.v_cache[blocks]
+        if not one_byte:
+            kc, vc = kc.view(torch.int16), vc.view(torch.int16)
+        kc, vc = kc.cpu().numpy(), vc.cpu().numpy()
+        if not one_byte:
+            kc, vc = kc.view(np.uint16), vc.view(np.uint16)
+        if one_byte:
+            ks, vs = w.k_scale[blocks].cpu().numpy(), w.v_scale[blocks].cpu().numpy()
+        qs = q[s].to(torch.float64).cpu().numpy()    # [q_len, Hq, D]
+        for kvh in kvhs:
+            u = {"kind": w.kv_dtype, "bs": bs, "L": L, "table": np.arange(n),
+                 "k": np.ascontiguousarray(kc[:, kvh:kvh + 1]),
+                 "v": np.ascontiguousarray(vc[:, kvh:kvh + 1]),
+                 "q": np.ascontiguousarray(qs[:, kvh * g:(kvh + 1) * g]),
+                 "scale": float(w.scale), "tokens": L,
+                 "bytes": (L * 2 * w.head_dim * elt + (L * 2 * 4 if one_byte else 0) +
+                           2 * w.q_len * g * w.head_dim * 2 + 4 * n)}
+            if one_byte:
+                u["ks"] = np.ascontiguousarray(ks[:, kvh:kvh + 1])
+                u["vs"] = np.ascontiguousarray(vs[:, kvh:kvh + 1])
+            units[(s, kvh)] = u
+    return [units[(int(s), int(kvh))] for s, kvh in pairs]

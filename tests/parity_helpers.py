@@ -7,6 +7,8 @@ import numpy as np
 import torch
 
 import oracle
+from oracle import parallel
+from paged_kv_decode_02_gb300.workloads import host_units
 
 # Bound on |GPU - oracle| for bf16 outputs of decode attention (bf16, INT8 and FP8
 # caches).
@@ -123,3 +125,16 @@ def oracle_outputs_multi(w, triples=None):
         visible = L - n + i + 1
         out[s, i, h], _ = oracle.attend_one_head(q[s, i, h], K[:visible], V[:visible], w.scale)
     return out
+
+
+def oracle_outputs_all(w):
+    """The oracle's whole output of a workload, [B, Hq, D] (or [B, q_len, Hq, D] for
+    multi-query decode), computed unit by unit -- every (sequence, KV head) -- in a
+    process pool over all host cores (oracle.parallel, the oracle's own functions)."""
+    B, Hkv, g = w.num_seqs, w.num_kv_heads, w.group
+    pairs = [(s, h) for s in range(B) for h in range(Hkv)]
+    res = parallel.map_units(host_units(w, pairs))
+    out = np.zeros((B, w.q_len, w.num_q_heads, w.head_dim))
+    for (s, h), r in zip(pairs, res):
+        out[s, :, h * g:(h + 1) * g] = r
+    return out if w.q_len > 1 else out[:, 0]

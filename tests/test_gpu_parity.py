@@ -13,7 +13,8 @@ import torch
 
 import oracle
 from paged_kv_decode_02_gb300.workloads import make_workload
-from parity_helpers import DECODE_ATOL, max_err, oracle_outputs, sample_pairs, to_f64
+from parity_helpers import (DECODE_ATOL, max_err, oracle_outputs, oracle_outputs_all,
+                            sample_pairs, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -350,6 +351,19 @@ def test_decode_full_size_sampled(pk, name):
     assert max_err(out, ref, pairs) <= DECODE_ATOL
 
 
+@pytest.mark.parametrize("name", ["70b-gqa", "7b"])
+def test_decode_full_size_whole_output(pk, name):
+    """Every output row of a full-size workload against the oracle (run on all host
+    cores): 70b-gqa has cut units everywhere (470 of its 512 (sequence, KV head) units
+    are split over several workers and merged), 7b folds its parts inside the kernel."""
+    w = make_workload(name, device=DEV)
+    pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
+    out = _decode(pk, w)
+    torch.cuda.synchronize()
+    ref = oracle_outputs_all(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+
+
 # ---------------------------------------------------------------------------
 # cascade decode for a prefix shared by the whole batch
 # ---------------------------------------------------------------------------
@@ -461,12 +475,14 @@ def test_cascade_four_and_eight_row_tiles(pk, B, bs):
 
 
 def test_cascade_full_prefix_workload(pk):
+    """The benchmark's headline step (append, then the cascade decode of the full prefix
+    workload), every output row against the oracle run on all host cores."""
     w = make_workload("prefix", device=DEV)
+    pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
     out = _cascade(pk, w, 2048 // w.block_size)
     torch.cuda.synchronize()
-    pairs = sample_pairs(w, 24)
-    ref = oracle_outputs(w, pairs)
-    assert max_err(out, ref, pairs) <= DECODE_ATOL
+    ref = oracle_outputs_all(w)
+    assert max_err(out, ref) <= DECODE_ATOL
 
 
 def test_cascade_flags_a_table_without_the_prefix(pk):

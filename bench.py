@@ -61,11 +61,15 @@ WORKLOAD_TEXT = {
                     "tokens: batch 64, 64 q / 8 kv heads, head_dim 128, block 16, context "
                     "log-normal (median 1024, sigma 1) clipped [128, 32768], q_len 16 new "
                     "tokens per request (128 query rows per KV head), causal",
+    "chunk-70b": "chunked prefill on the 70B-like GQA shape: 16 requests, 64 q / 8 kv heads, "
+                 "head_dim 128, block 16, a 256-token prefill chunk per request (2048 query "
+                 "rows per KV head) at the end of a context log-normal (median 1024, sigma 1) "
+                 "clipped [256, 32768], causal",
 }
 # the workloads recorded beside the headline, each as (config, cascade)
 PER_CONFIG = [("tiny", False), ("7b", False), ("70b-gqa", False), ("prefix", False),
               ("int8", False), ("int8-bs16", False), ("fp8-e5m2", False), ("fp8-e4m3", False),
-              ("spec-70b", False), ("spec-70b-q16", False)]
+              ("spec-70b", False), ("spec-70b-q16", False), ("chunk-70b", False)]
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 
@@ -148,6 +152,29 @@ def decode_bytes(w):
     return {"kv": uniq * rb, "kv_logical": tokens * rb, "q_out": qo, "tables": tables,
             "total": uniq * rb + qo + tables, "logical": tokens * rb + qo + tables,
             "tokens": tokens, "unique_tokens": uniq}
+
+
+def decode_flops(w):
+    """Algorithmic FLOPs of one decode call: 4 * D per (query row, visible token) (q.k
+    and p.v, a multiply and an add each); new token i of a request of length L sees
+    L - q_len + 1 + i tokens."""
+    import numpy as np
+    L = w.context_lens.cpu().numpy().astype(np.int64)
+    n = w.q_len
+    vis = 0
+    for Ls in L:
+        if Ls > 0:
+            vis += int(sum(Ls - n + 1 + i for i in range(n)))
+    return 4 * w.head_dim * w.num_q_heads * vis
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured sustained"
+    except Exception:
+        return 1700.0, "fallback sustained"
 
 
 def append_bytes(w):
@@ -487,6 +514,12 @@ def measure_workload(pk, name, cascade, args, dev, world, min_seconds, with_e2e=
                         "timing": f"median over {len(dec_ms)} replays of a CUDA graph of K "
                                   f"back-to-back decode calls (decode + merge kernels), CUDA "
                                   f"events on the launching stream"}}
+    if w.q_len > 1:  # multi-query and prefill chunks: the tensor-core side of the roofline
+        fl = decode_flops(w)
+        tpk, tkind = measured_tensor_peak()
+        rec["tensor"] = {"flops_per_call": fl, "tflops": round(fl / (ms_dec * 1e-3) / 1e12, 2),
+                         "peak_tflops": tpk, "frac": round(fl / (ms_dec * 1e-3) / 1e12 / tpk, 4),
+                         "peak_source": f"{tkind} bf16 (MEASURED_PEAKS.json)"}
     if with_e2e and not args.no_e2e:
         rec["e2e"] = run_e2e(args, w, pk, dev, out, ws, step_bytes, world, cascade_blocks)
     return rec
@@ -501,7 +534,8 @@ def per_config_line(name, cascade, r):
             "frac": rf["frac"], "effective_gbs": rf["effective_gbs"],
             "traffic": rf["traffic"], "kernel": rf["kernel"],
             "launches_per_call": rf["launches_per_call"],
-            "kv_tokens_per_s": round(r["tokens_per_s"], 1), "replays": r["replays"]}
+            "kv_tokens_per_s": round(r["tokens_per_s"], 1), "replays": r["replays"],
+            **({"tensor": r["tensor"]} if "tensor" in r else {})}
 
 
 def run_ours(args, rank, world):

@@ -242,7 +242,7 @@ pkv_status pkv_swap_in(void* k_cache, void* v_cache, float* k_scale, float* v_sc
                        int32_t* status, pkv_stream_t stream);
 
 /* Largest q_len of pkv_decode_multi_bf16. */
-#define PKV_MAX_QUERY_LEN 16
+#define PKV_MAX_QUERY_LEN 256
 
 /*
  * pkv_decode_multi_workspace_bytes -- workspace that pkv_decode_multi_bf16 needs for
@@ -255,8 +255,8 @@ pkv_status pkv_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len,
  * pkv_decode_multi_bf16 -- paged attention for q_len new tokens per sequence in one
  * call: the verification pass of speculative decoding ("推测解码", chenk.top page: the
  * target model scores the k drafted tokens and the next position, q_len = k + 1, in
- * one forward pass); also a short chunk of chunked prefill ("Orca 的迭代级调度", same
- * page). Every sequence's q_len newest tokens are already in the cache (appended
+ * one forward pass); also a chunk of chunked prefill ("Orca 的迭代级调度", same page:
+ * a prompt's prefill split into chunks that run beside the decode steps). Every sequence's q_len newest tokens are already in the cache (appended
  * with pkv_append_bf16), so context_lens[s] counts them; new token i of sequence s
  * sits at position context_lens[s] - q_len + i and attends causally:
  *   out[s, i, h, :] = softmax(scale * K q[s, i, h]) V over positions 0 .. that position.
@@ -268,10 +268,11 @@ pkv_status pkv_decode_multi_workspace_bytes(const pkv_dims* dims, int32_t q_len,
  *              also flagged PKV_DEV_BAD_CONTEXT_LEN (and zeroed). Without status,
  *              query tokens that see no position get zeros.
  * Rows are (token, head) pairs on the tensor cores for every group size: a KV head
- * with 48 to 128 rows (q_len * g) runs all its rows in one M = 128 tcgen05 MMA per
- * 128-token tile, once per block; fewer rows run as 16-row mma.sync subgroups sharing
- * each block through shared memory; more than 128 rows as subgroups that each read the
- * block (ceil(q_len * g / 16) reads per KV head).
+ * with 48 or more rows (q_len * g) runs them as ceil(rows / 128) equal row tiles, each
+ * in one M = 128 tcgen05 MMA per 128-token tile (the row tiles of a head run one after
+ * the other, so their re-reads of its blocks come from L2); fewer rows run as 16-row
+ * mma.sync subgroups sharing each block through shared memory. Every row tile reads
+ * the head's whole context (positions a row may not see are masked, not skipped).
  */
 pkv_status pkv_decode_multi_bf16(void* out, const void* q, const void* k_cache,
                                  const void* v_cache, const int32_t* block_tables,

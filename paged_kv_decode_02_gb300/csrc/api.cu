@@ -19,6 +19,7 @@ namespace {
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per shared-memory copy wait
 constexpr int kMaxQueryLen = PKV_MAX_QUERY_LEN;
 constexpr int kTcMinRows = 48;  // multi-query rows per KV head from which tcgen05 wins
+constexpr int kTcTileRows = 128;  // rows of one tcgen05 MMA (M): a KV head's row tile
 // tcgen05 kernel: the cost of ending a KV head (its partly filled last tile, the
 // epilogue, the next head's first scores) in tiles; ranges are balanced on tiles plus
 // this much per head. A sweep of whole calls on GB300 (48 and 128 query rows per KV
@@ -205,16 +206,16 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
   bool found = false;
   if (q_len > 1) {
     if (kvt != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
-    // KV heads with 48..128 query rows go through the tcgen05 kernel, fewer rows through
-    // the mma.sync path: measured on GB300 with the spec-70b lengths, tcgen05 vs mma.sync
-    // per call: 16 rows 136.6 vs 93.4 us, 48 rows 146.4 vs 150.8, 64 rows 49.8 vs 72.8,
-    // 128 rows 152.4 vs 490.6 (an M = 128 MMA wastes what a small head leaves empty)
-    if (rows >= kTcMinRows && rows <= 128 &&
-        select_decode_tc(d->head_dim, d->block_size, &P.k)) {
-      // every row of a KV head in one tcgen05 MMA: one work unit per KV head
-      P.nsg = 1;
-      P.gs = rows;
-      P.HU = d->num_kv_heads;
+    // KV heads with 48 or more query rows go through the tcgen05 kernel, fewer rows
+    // through the mma.sync path: measured on GB300 with the spec-70b lengths, tcgen05 vs
+    // mma.sync per call: 16 rows 136.6 vs 93.4 us, 48 rows 146.4 vs 150.8, 64 rows 49.8
+    // vs 72.8, 128 rows 152.4 vs 490.6 (an M = 128 MMA wastes what a small head leaves
+    // empty). A head's rows are cut into nsg equal row tiles of at most 128 (the last one
+    // padded when they do not divide), one tcgen05 work unit each.
+    if (rows >= kTcMinRows && select_decode_tc(d->head_dim, d->block_size, &P.k)) {
+      P.nsg = (rows + kTcTileRows - 1) / kTcTileRows;
+      P.gs = (rows + P.nsg - 1) / P.nsg;
+      P.HU = d->num_kv_heads * P.nsg;
       found = true;
     } else {
       found = select_decode_bf16_multi(d->head_dim, d->block_size, P.nsg, &P.k);
@@ -272,10 +273,10 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
 
   // workspace: [prefix (B+1) int32][partial (m, l) 2W*gs float2][partial o 2W*gs*D float]
   P.off_prefix = 0;  // [B+1] work prefix, then [B+1] weighted prefix (tcgen05 kernel)
-  // [B, Hkv] counters of the in-kernel stream-K fixups (single-token decode; the
-  // tcgen05 kernel, one per KV head)
+  // [B, HU] counters of the in-kernel stream-K fixups (single-token decode: one per KV
+  // head; the tcgen05 kernel: one per unit)
   P.off_ctr = align_up(size_t(d->num_seqs + 1) * 8, 256);
-  P.off_ml = align_up(P.off_ctr + size_t(d->num_seqs) * d->num_kv_heads * 8, 256);
+  P.off_ml = align_up(P.off_ctr + size_t(d->num_seqs) * P.HU * 8, 256);
   P.off_o = align_up(P.off_ml + size_t(2) * P.W * P.gs * 8, 256);
   P.ws_bytes = align_up(P.off_o + size_t(2) * P.W * P.gs * d->head_dim * 4, 256);
   *pl = P;
@@ -353,11 +354,12 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   p.q_len = q_len;
   p.beta = P.k.tc ? kTcHeadCost : 0;
 
-  // tcgen05 kernel: whole KV heads leave through TMA tensor stores of g-row boxes when
-  // g is 8, 16 or 32 (each box then starts on a 1024-byte swizzle atom of the staged rows)
+  // tcgen05 kernel: whole units leave through TMA tensor stores of g-row boxes when g is
+  // 8, 16 or 32 and the row tiles start on tokens (each box then starts on a 1024-byte
+  // swizzle atom of the staged rows)
   CUtensorMap tmo;
   std::memset(&tmo, 0, sizeof(tmo));
-  if (P.k.tc && (P.g == 8 || P.g == 16 || P.g == 32) &&
+  if (P.k.tc && (P.g == 8 || P.g == 16 || P.g == 32) && P.gs % P.g == 0 &&
       cache_map(&tmo, out, false, d->head_dim,
                 (long long)d->num_seqs * q_len * d->num_q_heads, P.g))
     p.tma_out = 1;
@@ -386,7 +388,7 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   m.gs = P.gs;
   m.nsg = P.nsg;
   m.HU = P.HU;
-  m.W = P.W / P.nsg;  // workers of nsg warps
+  m.W = P.k.tc ? P.W : P.W / P.nsg;  // CTAs, or workers of nsg warps
   m.beta = p.beta;
   m.wprefix = p.prefix_out + (d->num_seqs + 1);
   if (!p.fixup) launch_merge(m, stream);  // else cut units were folded in the kernel

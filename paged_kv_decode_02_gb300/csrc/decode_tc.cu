@@ -7,15 +7,20 @@
 //   out[r] = softmax(scale * K q_r) V
 // over the tokens reached through the block table ("分页注意力", same page).
 //
-// All q_len * g rows of a KV head (at most 128) go through one M = 128 tcgen05 MMA, so
-// a KV block is multiplied once for every row of its head instead of once per 16-row
-// subgroup. Work: the flat order (sequence, KV head, tile of 128 tokens) is cut into
-// one contiguous range per CTA (one CTA per SM). Within a range the tiles of one KV
-// head form a segment; a segment covering the whole head writes the output, a cut
-// one (only a range's first and last can be) leaves an unnormalised (o, m, l) record
-// per row in slot 2c (the first segment of CTA c) or 2c + 1 (the last). Without a
-// status word the CTA that completes a cut head folds its records at its end
-// (tc_tail_fixup); with one, the split-KV merge kernel validates and folds.
+// The q_len * g rows of a KV head are cut into nsg equal row tiles of gs <= 128 rows
+// (one tile up to 128 rows; a chunk of chunked prefill, q_len up to 256, takes
+// several), and each row tile goes through one M = 128 tcgen05 MMA per KV tile, so a
+// KV block is multiplied once for every 128 rows instead of once per 16-row subgroup.
+// A work unit is (KV head, row tile): unit u of a sequence is KV head u / nsg, rows
+// (u % nsg) * gs .. + gs - 1. The row tiles of one head are consecutive units, so
+// their re-reads of the head's blocks come from L2. Work: the flat order (sequence,
+// unit, tile of 128 tokens) is cut into one contiguous range per CTA (one CTA per SM).
+// Within a range the tiles of one unit form a segment; a segment covering the whole
+// unit writes the output, a cut one (only a range's first and last can be) leaves an
+// unnormalised (o, m, l) record per row in slot 2c (the first segment of CTA c) or
+// 2c + 1 (the last). Without a status word the CTA that completes a cut unit folds its
+// records at its end (tc_tail_fixup); with one, the split-KV merge kernel validates
+// and folds.
 // Roles per CTA (224 threads), as in the cascade prefix kernel:
 //   warp 0 / warp 6: TMA copies of the K / V tiles into two-stage rings (one box per
 //                    16- or 32-token block and 64-column slab, lane b copies block b;
@@ -87,52 +92,52 @@ struct TcDecode {
   static_assert(kOffTables % 16 == 0 && kOffCut % 16 == 0, "table alignment");
 };
 
-// Position in the flat (sequence, KV head, tile) order.
+// Position in the flat (sequence, unit, tile) order; a unit is (KV head, row tile).
 struct TileCursor {
-  int s, h, j, n;  // sequence, KV head, tile of the head, tiles of the sequence
+  int s, h, j, n;  // sequence, unit, tile of the unit, tiles per unit of the sequence
 };
 
 __device__ __forceinline__ void tile_locate(TileCursor& c, long long f, const int* prefix, int B,
-                                            int Hkv) {
-  int lo = 0, hi = B;  // Hkv*prefix[lo] <= f < Hkv*prefix[hi]
+                                            int U) {
+  int lo = 0, hi = B;  // U*prefix[lo] <= f < U*prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if ((long long)Hkv * prefix[mid] <= f) lo = mid; else hi = mid;
+    if ((long long)U * prefix[mid] <= f) lo = mid; else hi = mid;
   }
   c.s = lo;
   c.n = prefix[lo + 1] - prefix[lo];
-  const long long rem = f - (long long)Hkv * prefix[lo];
+  const long long rem = f - (long long)U * prefix[lo];
   c.h = int(rem / c.n);
   c.j = int(rem % c.n);
 }
 
-__device__ __forceinline__ void tile_next(TileCursor& c, const int* prefix, int B, int Hkv) {
+__device__ __forceinline__ void tile_next(TileCursor& c, const int* prefix, int B, int U) {
   if (++c.j < c.n) return;
   c.j = 0;
-  if (++c.h < Hkv) return;
+  if (++c.h < U) return;
   c.h = 0;
   do { ++c.s; } while (c.s < B && prefix[c.s + 1] == prefix[c.s]);
   c.n = c.s < B ? prefix[c.s + 1] - prefix[c.s] : 0;
 }
 
-// Tiles of the flat (sequence, KV head, tile) order before weighted position x. Ranges
-// are equal cuts of a weighted order in which KV head (s, h) takes tiles_s + beta
-// positions (its tiles, then beta for the cost of ending a head); a range covers the
-// tiles whose positions fall in it. prefix / wprefix: exclusive prefixes of the tiles
-// and of the weights per sequence.
+// Tiles of the flat (sequence, unit, tile) order before weighted position x (U units
+// per sequence). Ranges are equal cuts of a weighted order in which unit (s, h)
+// takes tiles_s + beta positions (its tiles, then beta for the cost of ending a unit);
+// a range covers the tiles whose positions fall in it. prefix / wprefix: exclusive
+// prefixes of the tiles and of the weights per sequence.
 __device__ __forceinline__ long long tc_tiles_before(long long x, const int* prefix,
-                                                     const int* wprefix, int B, int Hkv,
+                                                     const int* wprefix, int B, int U,
                                                      int beta) {
-  if (x >= (long long)Hkv * wprefix[B]) return (long long)Hkv * prefix[B];
-  int lo = 0, hi = B;  // Hkv*wprefix[lo] <= x < Hkv*wprefix[hi]
+  if (x >= (long long)U * wprefix[B]) return (long long)U * prefix[B];
+  int lo = 0, hi = B;  // U*wprefix[lo] <= x < U*wprefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if ((long long)Hkv * wprefix[mid] <= x) lo = mid; else hi = mid;
+    if ((long long)U * wprefix[mid] <= x) lo = mid; else hi = mid;
   }
   const int n = prefix[lo + 1] - prefix[lo];
-  const long long rem = x - (long long)Hkv * wprefix[lo];
+  const long long rem = x - (long long)U * wprefix[lo];
   const long long h = rem / (n + beta), o = rem % (n + beta);
-  return (long long)Hkv * prefix[lo] + h * n + min(o, (long long)n);
+  return (long long)U * prefix[lo] + h * n + min(o, (long long)n);
 }
 
 // Stream-K fixup at the end of a CTA (no merge kernel follows). A KV head is cut only
@@ -155,7 +160,7 @@ template <int D>
 __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* s_prefix,
                                               const long long* s_rs, volatile int* cut,
                                               uint8_t* scratch, int nthreads) {
-  const int tid = threadIdx.x, C = gridDim.x, R = p.gs, Hkv = p.Hkv;
+  const int tid = threadIdx.x, C = gridDim.x, R = p.gs, U = p.HU;
   if (!(cut[4] | cut[9])) return;  // no cut segment (uniform: shared memory after a barrier)
   __threadfence();                 // this thread's records, device-wide
   __syncthreads();
@@ -163,7 +168,7 @@ __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* 
     volatile int* e = cut + 5 * tid;
     const int s = e[0], h = e[1], n = e[2], mine = e[3];
     const unsigned long long tag = launch_tag();
-    unsigned long long* ctr = p.fix_ctr + size_t(s) * Hkv + h;
+    unsigned long long* ctr = p.fix_ctr + size_t(s) * U + h;
     unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
     int last = 0;
     for (;;) {
@@ -192,7 +197,7 @@ __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* 
     __threadfence();
     const int s = cut[5 * ei], h = cut[5 * ei + 1], n = cut[5 * ei + 2];
     if (tid == 0) {  // the parts: slots of the CTAs whose ranges hold tiles [u0, u1)
-      const long long u0 = (long long)Hkv * s_prefix[s] + (long long)h * n, u1 = u0 + n;
+      const long long u0 = (long long)U * s_prefix[s] + (long long)h * n, u1 = u0 + n;
       int lo = 0, hi = C;  // s_rs[lo] <= u0 < s_rs[hi]
       while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -271,7 +276,11 @@ __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* 
         const int k = k0 + j * nthreads;
         if (k >= items) break;
         const int r = k / Q, dq = k % Q;
-        const size_t orow = (size_t(s) * p.q_len + r / p.g) * p.Hq + size_t(h) * p.g + r % p.g;
+        // unit h: KV head h / nsg, rows from (h % nsg) * R
+        const int Rg = (h % p.nsg) * R + r;
+        if (Rg >= p.q_len * p.g) continue;  // past the last row of a partial row tile
+        const size_t orow =
+            (size_t(s) * p.q_len + Rg / p.g) * p.Hq + size_t(h / p.nsg) * p.g + Rg % p.g;
         reinterpret_cast<uint2*>(outb + orow * D)[dq] =
             make_uint2(pack_bf16x2(acc[j].x, acc[j].y), pack_bf16x2(acc[j].z, acc[j].w));
       }
@@ -295,7 +304,9 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
   long long* s_rs = reinterpret_cast<long long*>(gbase + K::kOffTables);
   int* s_prefix = reinterpret_cast<int*>(s_rs + gridDim.x + 1);
   volatile int* s_cut = reinterpret_cast<volatile int*>(gbase + K::kOffCut);
-  const int B = p.B, Hkv = p.Hkv, beta = p.beta;
+  // U units per sequence: KV head u / nsg, row tile u % nsg of gs rows (rows = q_len * g)
+  const int B = p.B, Hkv = p.Hkv, beta = p.beta, U = p.HU, nsg = p.nsg;
+  const int rows = p.q_len * p.g;
   int* s_wpre = s_prefix + (B + 1);
   int* s_len = s_wpre + (B + 1);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -393,14 +404,14 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
   // a head); a range covers the tiles whose positions fall in it. Tiles before
   // weighted position x:
   // every CTA's range start (equal cuts of the weighted order), all threads at once
-  const long long TW = (long long)Hkv * s_wpre[B];
+  const long long TW = (long long)U * s_wpre[B];
   const int C = gridDim.x, c = blockIdx.x;
   for (int c2 = tid; c2 <= C; c2 += K::kThreads)
-    s_rs[c2] = tc_tiles_before(TW * c2 / C, s_prefix, s_wpre, B, Hkv, beta);
+    s_rs[c2] = tc_tiles_before(TW * c2 / C, s_prefix, s_wpre, B, U, beta);
   __syncthreads();
   const long long ra = s_rs[c], rb = s_rs[c + 1];
   const int cnt = int(rb - ra);
-  const int R = p.gs;  // query rows per KV head (q_len * g)
+  const int R = p.gs;  // query rows per unit (a row tile of the KV head's q_len * g rows)
 
   if (cnt > 0 && (warp == 0 || warp == 6)) {
     // ---------------- TMA producers: warp 0 streams K, warp 6 streams V ----------------
@@ -409,14 +420,14 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
     const uint32_t region = base + (is_k ? K::kOffK : K::kOffV);
     const int rows_total = p.NB * Hkv * BS;  // a box at this row is all zero fill
     TileCursor cur;
-    tile_locate(cur, ra, s_prefix, B, Hkv);
+    tile_locate(cur, ra, s_prefix, B, U);
     // lane b: physical block of block b of the tile at the cursor (rows_total: none)
     auto block_row = [&](const TileCursor& t) -> int {
       const int blk = t.j * K::kBlocks + lane;
       if (lane >= K::kBlocks || t.s >= B || blk * BS >= s_len[t.s]) return rows_total;
       int phys = __ldg(p.block_tables + size_t(t.s) * p.MBS + blk);
       phys = (phys < 0 || phys >= p.NB) ? 0 : phys;  // never copy outside the pool
-      return (phys * Hkv + t.h) * BS;
+      return (phys * Hkv + t.h / nsg) * BS;
     };
     int row = block_row(cur);
     int issued = 0;
@@ -437,7 +448,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
           tma_load_2d(dst + sl * K::kSlab, map, fb, sl * 64, row);
       }
       issued = i + 1;
-      tile_next(cur, s_prefix, B, Hkv);
+      tile_next(cur, s_prefix, B, U);
       if (i + 1 < cnt) row = block_row(cur);  // next tile's ids, a tile ahead
     }
     if (lane == 0)  // every copy issued must have landed before the CTA may exit
@@ -496,7 +507,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
         return true;
       };
       TileCursor cur;
-      tile_locate(cur, ra, s_prefix, B, Hkv);
+      tile_locate(cur, ra, s_prefix, B, U);
       bool ok = true;
       int seg = -1, pend = -1, pend_seg = 0;
       bool pend_first = false;
@@ -516,7 +527,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
         pend = i;
         pend_first = first;
         pend_seg = seg;
-        tile_next(cur, s_prefix, B, Hkv);
+        tile_next(cur, s_prefix, B, U);
       }
       if (ok && pend >= 0) issue_pv(pend, pend_first, pend_seg);
       tc::commit(mdone);  // every MMA issued must have completed before TMEM is freed
@@ -529,11 +540,15 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
     const float sl = p.scale_log2, asl = fabsf(sl);
-    const bool row_ok = r < R;
-    // causal: new token i = r / g hides the last q_len - 1 - i positions of its head
-    const int hide = row_ok ? p.q_len - 1 - r / p.g : 0;
+    // this thread's query row of unit u: row (u % nsg) * R + r of its KV head (new
+    // token Rg / g, query head Rg % g of the group), if it exists
+    auto row_of = [&](int u) { return (u % nsg) * R + r; };
+    auto row_exists = [&](int u) { return r < R && row_of(u) < rows; };
     TileCursor cur;
-    tile_locate(cur, ra, s_prefix, B, Hkv);
+    tile_locate(cur, ra, s_prefix, B, U);
+    bool row_ok = row_exists(cur.h);
+    // causal: new token i = Rg / g hides the last q_len - 1 - i positions of its head
+    int hide = row_ok ? p.q_len - 1 - row_of(cur.h) / p.g : 0;
     // Q rows of the KV head at cursor t -> Q buffer qb (K-major, 128-byte swizzle), as
     // asynchronous copies (padding rows zero-filled); q_ready completes and publishes them
     auto prefetch_q = [&](const TileCursor& t, int qb) {
@@ -543,13 +558,15 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
         __syncwarp();
       }
       const uint4* q = reinterpret_cast<const uint4*>(p.q);
-      const size_t qrow = (size_t(t.s) * p.q_len + (row_ok ? r / p.g : 0)) * p.Hq + t.h * p.g +
-                          (row_ok ? r % p.g : 0);
+      const bool ex = row_exists(t.h);
+      const int Rg = ex ? row_of(t.h) : 0;
+      const size_t qrow =
+          (size_t(t.s) * p.q_len + Rg / p.g) * p.Hq + (t.h / nsg) * p.g + Rg % p.g;
       const uint32_t qa = base + K::kOffQ + qb * K::kTile;
 #pragma unroll
       for (int cc = 0; cc < kChunks; ++cc)
         cp_async16(qa + (cc >> 3) * K::kSlab + r * 128 + (((cc & 7) ^ (r & 7)) << 4),
-                   q + qrow * kChunks + cc, row_ok ? 16u : 0u);
+                   q + qrow * kChunks + cc, ex ? 16u : 0u);
       cp_async_commit();
     };
     auto q_ready = [&](int qb) {
@@ -589,10 +606,12 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
       if (first && i > 0) {  // this Q was published before the previous epilogue
         seg_j0 = cur.j;
         seg_tile = 0;
+        row_ok = row_exists(cur.h);
+        hide = row_ok ? p.q_len - 1 - row_of(cur.h) / p.g : 0;
       }
-      if (last && i + 1 < cnt) {  // the next KV head's Q rows, while this tile runs
+      if (last && i + 1 < cnt) {  // the next unit's Q rows, while this tile runs
         TileCursor nx = cur;
-        tile_next(nx, s_prefix, B, Hkv);
+        tile_next(nx, s_prefix, B, U);
         prefetch_q(nx, (seg + 1) & 1);
       }
       const int L = s_len[cur.s];
@@ -630,7 +649,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
           mbar_arrive(ofree);
           ++seg;
         }
-        tile_next(cur, s_prefix, B, Hkv);
+        tile_next(cur, s_prefix, B, U);
         continue;
       }
       uint32_t s[K::kN];
@@ -759,26 +778,30 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
                                                 __uint_as_float(o[e + 7]) * inv)));
           }
           if (p.tma_out) {
-            // one TMA box per new token (its g rows) and 64-column slab; g divides 32,
-            // so a token's rows belong to this warp and its box starts on an atom
+            // one TMA box per new token (its g rows) and 64-column slab; g divides 32
+            // and the row tile (gs) starts on a token, so a token's rows belong to this
+            // warp and its box starts on an atom
             fence_proxy_async_smem();  // the staged rows, for the async proxy
             __syncwarp();
             if (lane == 0) {
-              const int i0 = quarter * 32 / p.g, i1 = min(p.q_len, (quarter * 32 + 32) / p.g);
+              const int rt0 = (cur.h % nsg) * R;  // first row of the tile in the head
+              const int nloc = min(R, rows - rt0);  // rows of the tile that exist
+              const int i0 = quarter * 32 / p.g, i1 = min(nloc, quarter * 32 + 32) / p.g;
               for (int i = i0; i < i1; ++i)
 #pragma unroll
                 for (int sl = 0; sl < K::kSlabs; ++sl)
                   tma_store_2d(&tmo, qbuf + sl * K::kSlab + (i * p.g) * 128, sl * 64,
-                               (cur.s * p.q_len + i) * p.Hq + cur.h * p.g);
+                               (cur.s * p.q_len + rt0 / p.g + i) * p.Hq + (cur.h / nsg) * p.g);
               bulk_commit();
             }
           } else {
             __syncwarp();
             // lane l's own output row, handed to the lanes that store it
-            const long long my_row =
-                (long long)((size_t(cur.s) * p.q_len + (row_ok ? r / p.g : 0)) * p.Hq +
-                            cur.h * p.g + (row_ok ? r % p.g : 0));
-            const int nrows = min(32, R - quarter * 32);
+            const int Rg = row_ok ? row_of(cur.h) : 0;
+            const long long my_row = (long long)((size_t(cur.s) * p.q_len + Rg / p.g) * p.Hq +
+                                                 (cur.h / nsg) * p.g + Rg % p.g);
+            // rows of this warp that exist (a partial last row tile ends early)
+            const int nrows = min(32, min(R, rows - (cur.h % nsg) * R) - quarter * 32);
 #pragma unroll 4
             for (int k2 = 0; k2 < kCh; ++k2) {
               const int idx = k2 * 32 + lane, rl = idx / kCh, ch = idx % kCh;
@@ -817,7 +840,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS>::kThreads, 1)
         ++seg;
         m_ref = -INFINITY;
       }
-      tile_next(cur, s_prefix, B, Hkv);
+      tile_next(cur, s_prefix, B, U);
     }
     (void)ok;
     if (p.tma_out && lane == 0) bulk_wait_all();  // output boxes complete before exit

@@ -38,12 +38,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 3) paged_decode_merge_kernel
   const int unit = item / ngrp, r0 = (item % ngrp) * rpw;
   const int s = unit / p.HU, u = unit % p.HU;
   const int row = r0 + lane / Q, dq = lane % Q;
-  const bool active = row < gs;
   // work items (blocks, or 128-token tiles for the tcgen05 kernel) of the sequence
   const int n = p.prefix[s + 1] - p.prefix[s];
   // output row of unit row r: (s * q_len + i) * Hq + kvh * g + j for the unit's query
   // row R = (u % nsg) * gs + r = i * g + j (with q_len = 1: head kvh * g + R)
   const int R = (u % p.nsg) * gs + row;
+  // rows past q_len * g: the padding of a partial last row tile (tcgen05 kernel)
+  const bool active = row < gs && R < p.q_len * p.g;
   uint2* out = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
                                         ((size_t(s) * p.q_len + R / p.g) * p.Hq +
                                          (u / p.nsg) * p.g + R % p.g) * D) + dq;
@@ -68,16 +69,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 3) paged_decode_merge_kernel
     if (active) *out = make_uint2(0u, 0u);
     return;
   }
-  // the decode kernel's flat order is (sequence, KV head, block) over W workers of nsg
-  // warps each; this unit's parts come from warp worker * nsg + sg of each worker
-  // Workers cut the flat order (sequence, unit, item) into W equal ranges; with beta >
-  // 0 (tcgen05 kernel) the order is weighted: every unit of a non-empty sequence takes
-  // n + beta positions, its n items (tiles) first, then beta that hold none.
-  const int nsg = p.nsg, kvh = u / nsg, sg = u % nsg, Hkv = p.HU / nsg;
+  // The mma.sync kernels' flat order is (sequence, KV head, block) over W workers of nsg
+  // warps each; this unit's parts come from warp worker * nsg + sg of each worker. The
+  // tcgen05 kernel (beta > 0) orders (sequence, unit, tile) over W CTAs, every unit (a
+  // row tile of a KV head) its own position in the order, and its parts are the CTAs'
+  // slots; that order is weighted: every unit of a non-empty sequence takes n + beta
+  // positions, its n tiles first, then beta that hold none.
   const int beta = p.beta;
-  const int* pre = beta > 0 ? p.wprefix : p.prefix;
+  const bool tc = beta > 0;
+  const int nsg = tc ? 1 : p.nsg, sg = tc ? 0 : u % p.nsg;
+  const int ord = tc ? u : u / p.nsg;            // the unit's place within its sequence
+  const int Hkv = tc ? p.HU : p.HU / p.nsg;      // places per sequence
+  const int* pre = tc ? p.wprefix : p.prefix;
   const long long T = (long long)Hkv * pre[p.B];
-  const long long A = (long long)Hkv * pre[s] + (long long)kvh * (n + beta);
+  const long long A = (long long)Hkv * pre[s] + (long long)ord * (n + beta);
   const int W = p.W;
   const int w0 = merge_worker_of(A, T, W), w1 = merge_worker_of(A + n - 1, T, W);
   if (w0 == w1 || !active) return;  // one worker covered the whole unit: output written

@@ -561,7 +561,8 @@ def multi_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_s
 def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens, scale,
                                  out=None, workspace=None, status=None):
     """Attention for q_len new tokens per sequence in one call (speculative
-    verification, q_len = k + 1): q [B, q_len, Hq, D] bf16; the q_len newest tokens of
+    verification, q_len = k + 1, or a chunk of chunked prefill, q_len up to 256):
+    q [B, q_len, Hq, D] bf16; the q_len newest tokens of
     every sequence are already in the bf16 caches and counted by ``context_lens``; new
     token i attends causally to positions 0 .. context_lens - q_len + i. Returns out
     [B, q_len, Hq, D] bf16."""

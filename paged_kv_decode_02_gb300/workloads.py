@@ -39,6 +39,11 @@ Workload recipes (names are the shapes they model):
 * ``spec-70b``: the ``70b-gqa`` shape and lengths with q_len = 6 new tokens per
   request (k = 5 drafted tokens plus the next position, the number of speculative
   tokens in the vLLM example of "推测解码", chenk.top page), for multi-query decode.
+  ``spec-70b-q16``: the same with q_len = 16 (128 query rows per KV head).
+* ``chunk-70b``: a chunk of chunked prefill ("Orca 的迭代级调度", chenk.top page) on the
+  ``70b-gqa`` shape: 16 requests whose last 256 tokens are the chunk being prefilled
+  (q_len = 256, 2048 query rows per KV head), lengths log-normal (median 1024, sigma 1)
+  rounded and clipped to [256, 32768], seed 5.
 
 The tokens appended in the step are the last q_len (1 unless stated) of each
 request: ``new_k``/``new_v`` hold them ([B * q_len, Hkv, D], request-major) and
@@ -212,6 +217,7 @@ SPECS = {
     "fp8-e4m3":  dict(B=128, Hq=32, Hkv=8,  D=128, bs=32, seed=4),
     "spec-70b":  dict(B=64,  Hq=64, Hkv=8,  D=128, bs=16, seed=2, q_len=6),
     "spec-70b-q16": dict(B=64, Hq=64, Hkv=8, D=128, bs=16, seed=2, q_len=16),
+    "chunk-70b": dict(B=16, Hq=64, Hkv=8, D=128, bs=16, seed=5, q_len=256),
 }
 
 FP8_KV = {"fp8_e4m3": (torch.float8_e4m3fn, 448.0), "fp8_e5m2": (torch.float8_e5m2, 57344.0)}
@@ -224,6 +230,8 @@ def _draw_lengths(name, rng, B):
         return np.full(B, 2048, dtype=np.int64)
     if name in ("70b-gqa", "spec-70b", "spec-70b-q16"):
         return _lognormal_lengths(rng, B, 1024, 1.0, 128, 32768)
+    if name == "chunk-70b":
+        return _lognormal_lengths(rng, B, 1024, 1.0, 256, 32768)
     if name == "prefix":
         return 2048 + rng.integers(16, 513, size=B).astype(np.int64)
     if name.startswith("int8") or name.startswith("fp8"):

@@ -127,8 +127,8 @@ def test_host_validation_without_gpu(lib_path):
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 7, ctypes.byref(n)) == \
         pagedkv.Status.ERR_DTYPE
     assert lib.pkv_decode_workspace_bytes(ctypes.byref(good), 0, None) == pagedkv.Status.ERR_NULL
-    # multi-query decode: 1 <= q_len <= PKV_MAX_QUERY_LEN (16)
-    for q_len in (0, 17):
+    # multi-query decode: 1 <= q_len <= PKV_MAX_QUERY_LEN (256)
+    for q_len in (0, 257):
         assert lib.pkv_decode_multi_workspace_bytes(ctypes.byref(good), q_len,
                                                     ctypes.byref(n)) == pagedkv.Status.ERR_SHAPE
         st = lib.pkv_decode_multi_bf16(p, p, p, p, p, p, q_len, 0.1, ctypes.byref(good), p,

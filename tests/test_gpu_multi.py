@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from paged_kv_decode_02_gb300.workloads import make_workload
-from parity_helpers import DECODE_ATOL, oracle_outputs_multi, to_f64
+from parity_helpers import DECODE_ATOL, oracle_outputs_all, oracle_outputs_multi, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -57,6 +57,45 @@ SHAPES = [
     ("g12-q4", 24, 2, 128, 16, 4, [4, 60, 300, 129]),
     ("g4-q16-d64-bs32", 8, 2, 64, 32, 16, [16, 40, 500]),
 ]
+
+# chunks of chunked prefill: more than 128 rows per KV head, run as equal tcgen05 row
+# tiles (the last one padded when the tiles do not divide the rows), with ragged causal
+# tails and contexts that hold only the chunk
+CHUNKS = [
+    # (id, Hq, Hkv, D, bs, q_len, lengths)
+    ("g8-q64", 16, 2, 128, 16, 64, [64, 65, 300, 1000, 0, 127]),
+    ("g8-q256", 16, 2, 128, 16, 256, [256, 300, 1300]),
+    ("g4-q256-d64-bs32", 8, 2, 64, 32, 256, [256, 513, 900]),
+    ("g6-q100", 12, 2, 128, 16, 100, [100, 101, 450]),       # g 6: plain row stores
+    ("g1-q131-bs32", 2, 2, 128, 32, 131, [131, 200, 0]),     # 2 tiles of 66, the last padded
+    ("g8-q17", 16, 2, 64, 16, 17, [17, 50, 333]),            # 2 tiles of 68 rows
+]
+
+
+@pytest.mark.parametrize("shape", CHUNKS, ids=[s[0] for s in CHUNKS])
+def test_multi_prefill_chunks(pk, shape):
+    _, Hq, Hkv, D, bs, n, lengths = shape
+    w = make_workload("spec-70b", device=DEV, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                      block_size=bs, lengths=lengths, q_len=n, seed=31, poison_unused=True)
+    out = _run(pk, w)
+    torch.cuda.synchronize()
+    assert _err(out, oracle_outputs_all(w)) <= DECODE_ATOL
+    # the same call with a status word (the split-KV merge kernel folds the cut units)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out2 = _run(pk, w, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert _err(out2, oracle_outputs_all(w)) <= DECODE_ATOL
+
+
+def test_multi_prefill_chunk_full_size(pk):
+    """A 256-token chunk for each of 16 requests with the 70b-gqa length mix (2048 query
+    rows per KV head, 16 row tiles), after appending the chunk: every output row."""
+    w = make_workload("chunk-70b", device=DEV)
+    pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
+    out = _run(pk, w)
+    torch.cuda.synchronize()
+    assert _err(out, oracle_outputs_all(w)) <= DECODE_ATOL
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[s[0] for s in SHAPES])

@@ -184,7 +184,8 @@ def test_multi_flags_context_shorter_than_queries(pk):
 
 def test_multi_rejects_bad_query_length(pk):
     w = make_workload("spec-70b", device=DEV, num_seqs=2, q_len=2, lengths=[5, 9])
-    q = torch.zeros((2, 17, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=DEV)
+    # one more new token than PKV_MAX_QUERY_LEN (256)
+    q = torch.zeros((2, 257, w.num_q_heads, w.head_dim), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(pk.PagedKVError):
         pk.paged_decode_attention_multi(q, w.k_cache, w.v_cache, w.block_tables,
                                         w.context_lens, w.scale)

@@ -212,7 +212,8 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
     // vs 72.8, 128 rows 152.4 vs 490.6 (an M = 128 MMA wastes what a small head leaves
     // empty). A head's rows are cut into nsg equal row tiles of at most 128 (the last one
     // padded when they do not divide), one tcgen05 work unit each.
-    if (rows >= kTcMinRows && select_decode_tc(d->head_dim, d->block_size, &P.k)) {
+    if (rows >= kTcMinRows &&
+        select_decode_tc(d->head_dim, d->block_size, rows > kTcTileRows, &P.k)) {
       P.nsg = (rows + kTcTileRows - 1) / kTcTileRows;
       P.gs = (rows + P.nsg - 1) / P.nsg;
       P.HU = d->num_kv_heads * P.nsg;

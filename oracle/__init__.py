@@ -41,6 +41,7 @@ from .paged_attention import (  # noqa: F401
     decode_attention,
     decode_attention_int8,
     decode_attention_multi,
+    decode_attention_multi_quantized,
     FP8_MAX,
     fp8_decode,
     fp8_round,

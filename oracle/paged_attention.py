@@ -396,6 +396,44 @@ def decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, co
     return out
 
 
+def decode_attention_multi_quantized(q, k_codes, v_codes, k_scale, v_scale, block_tables,
+                                     context_lens, scale, fmt, block_size=None):
+    """Multi-query paged attention (the causal rule of :func:`decode_attention_multi`)
+    over a one-byte cache: ``fmt`` "int8", "e4m3" or "e5m2"; the cached K/V values are
+    the codes (decoded exactly) times their fp32 per-(token, head) scales, the
+    quantised caches of "KV 缓存量化" on the chenk.top page. float64, returns
+    [B, q_len, Hq, D]."""
+    q = np.asarray(q)
+    B, n, Hq, D = q.shape
+    Hkv = k_codes.shape[1]
+    bs = int(block_size) if block_size is not None else k_codes.shape[2]
+    if Hq % Hkv != 0:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    g = Hq // Hkv
+    out = np.zeros((B, n, Hq, D), dtype=np.float64)
+    for s in range(B):
+        L = int(context_lens[s])
+        if L == 0:
+            continue
+        if L < n:
+            raise ValueError("a sequence holds fewer tokens than its queries")
+        for kvh in range(Hkv):
+            if fmt == "int8":
+                K = gather_sequence_int8(k_codes, k_scale, block_tables[s], L, kvh, bs)
+                V = gather_sequence_int8(v_codes, v_scale, block_tables[s], L, kvh, bs)
+            else:
+                K = gather_sequence_fp8(k_codes, k_scale, block_tables[s], L, kvh, bs, fmt)
+                V = gather_sequence_fp8(v_codes, v_scale, block_tables[s], L, kvh, bs, fmt)
+            for i in range(n):
+                visible = L - n + i + 1            # positions 0 .. L - n + i
+                for h in range(Hq):
+                    if _kv_head_of(h, g) != kvh:
+                        continue
+                    out[s, i, h], _ = attend_one_head(q[s, i, h], K[:visible], V[:visible],
+                                                      scale)
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Block moves -- "块管理器：分页如何运作" of the chenk.top page: a block shared under
 # copy-on-write is copied to a fresh block before a request writes into it; under

@@ -141,6 +141,67 @@ def test_block_placement_is_invisible():
     assert np.array_equal(a, b)
 
 
+def _quantized_case(seed, fmt, n=3, B=3, Hq=4, Hkv=2, D=8, bs=4, max_len=13):
+    """Random codes and scales of a one-byte cache, with the dequantised real values."""
+    rng = np.random.default_rng(seed)
+    lengths = rng.integers(n, max_len + 1, size=B)
+    lengths[-1] = 0
+    tables, _, NB, _ = build_tables(lengths, bs, rng)
+    if fmt == "int8":
+        kc = rng.integers(-127, 128, size=(NB, Hkv, bs, D)).astype(np.int8)
+        vc = rng.integers(-127, 128, size=(NB, Hkv, bs, D)).astype(np.int8)
+        deq = lambda c, sc: oracle.dequantize_rows_int8(c, sc)  # noqa: E731
+    else:
+        finite = np.flatnonzero(np.isfinite(oracle.fp8_decode(np.arange(256), fmt)))
+        kc = rng.choice(finite, size=(NB, Hkv, bs, D)).astype(np.uint8)
+        vc = rng.choice(finite, size=(NB, Hkv, bs, D)).astype(np.uint8)
+        deq = lambda c, sc: oracle.dequantize_rows_fp8(c, sc, fmt)  # noqa: E731
+    ks = rng.uniform(0.005, 0.03, size=(NB, Hkv, bs)).astype(np.float32)
+    vs = rng.uniform(0.005, 0.03, size=(NB, Hkv, bs)).astype(np.float32)
+    q = rng.standard_normal((B, n, Hq, D))
+    return q, kc, vc, ks, vs, deq(kc, ks), deq(vc, vs), tables, lengths
+
+
+@pytest.mark.parametrize("fmt", ["int8", "e4m3", "e5m2"])
+def test_quantized_equals_multi_on_dequantised_values(fmt):
+    """Over a one-byte cache the multi-query oracle is the (pinned) multi-query oracle
+    on the dequantised values: code x scale, decoded exactly."""
+    q, kc, vc, ks, vs, kr, vr, tables, lengths = _quantized_case(20, fmt)
+    a = oracle.decode_attention_multi_quantized(q, kc, vc, ks, vs, tables, lengths, 0.3, fmt)
+    b = oracle.decode_attention_multi(q, kr, vr, tables, lengths, 0.3)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("fmt", ["int8", "e4m3"])
+def test_quantized_single_query_is_single_token_decode(fmt):
+    """q_len = 1 over a one-byte cache is the (pinned) single-token INT8 / FP8 oracle."""
+    q, kc, vc, ks, vs, _, _, tables, lengths = _quantized_case(21, fmt, n=1)
+    a = oracle.decode_attention_multi_quantized(q, kc, vc, ks, vs, tables, lengths, 0.4, fmt)
+    if fmt == "int8":
+        b = oracle.decode_attention_int8(q[:, 0], kc, vc, ks, vs, tables, lengths, 0.4)
+    else:
+        b = oracle.decode_attention_fp8(q[:, 0], kc, vc, ks, vs, tables, lengths, 0.4, fmt)
+    assert np.array_equal(a[:, 0], b)
+
+
+def test_quantized_closed_form_running_means():
+    """Scale 0, context = the q_len new tokens: query i averages code x scale of V rows
+    0..i (the scales multiply the V codes, the K codes do not matter)."""
+    n, D, bs = 4, 3, 4
+    rng = np.random.default_rng(22)
+    tables, _, NB, _ = build_tables([n], bs, rng)
+    vc = rng.integers(-127, 128, size=(NB, 1, bs, D)).astype(np.int8)
+    kc = rng.integers(-127, 128, size=(NB, 1, bs, D)).astype(np.int8)
+    vs = rng.uniform(0.01, 0.02, size=(NB, 1, bs)).astype(np.float32)
+    ks = rng.uniform(0.01, 0.02, size=(NB, 1, bs)).astype(np.float32)
+    out = oracle.decode_attention_multi_quantized(rng.standard_normal((1, n, 1, D)), kc, vc,
+                                                  ks, vs, tables, [n], 0.0, "int8")
+    vals = [vc[tables[0, t // bs], 0, t % bs].astype(np.float64) *
+            float(vs[tables[0, t // bs], 0, t % bs]) for t in range(n)]
+    for i in range(n):
+        assert np.allclose(out[0, i, 0], np.mean(vals[:i + 1], axis=0), rtol=0, atol=1e-15)
+
+
 def test_too_short_context_is_refused():
     q = np.zeros((1, 3, 1, 2))
     with pytest.raises(ValueError):
@@ -200,3 +261,44 @@ def test_pins_catch_missing_causal_mask(monkeypatch):
 def test_pins_catch_reversed_query_order(monkeypatch):
     _plant_visible(monkeypatch, lambda L, n, i: L - i)
     assert _fails(test_scale_zero_gives_running_means)
+
+
+def _plant_quantized(monkeypatch, swap_scales=False, visible_of=None):
+    """Replace the one-byte multi-query oracle by one with a mistake: K and V scales
+    exchanged, or another causal window visible_of(L, n, i)."""
+    def bad(q, k_codes, v_codes, k_scale, v_scale, block_tables, context_lens, scale, fmt,
+            block_size=None):
+        q = np.asarray(q)
+        B, n, Hq, D = q.shape
+        Hkv = k_codes.shape[1]
+        bs = block_size or k_codes.shape[2]
+        g = Hq // Hkv
+        ks, vs = (v_scale, k_scale) if swap_scales else (k_scale, v_scale)
+        out = np.zeros((B, n, Hq, D))
+        for s in range(B):
+            L = int(context_lens[s])
+            if L == 0:
+                continue
+            for kvh in range(Hkv):
+                K = pa.gather_sequence_int8(k_codes, ks, block_tables[s], L, kvh, bs)
+                V = pa.gather_sequence_int8(v_codes, vs, block_tables[s], L, kvh, bs)
+                for i in range(n):
+                    m = L - n + i + 1 if visible_of is None else visible_of(L, n, i)
+                    m = max(0, min(L, m))
+                    for h in range(kvh * g, (kvh + 1) * g):
+                        out[s, i, h], _ = pa.attend_one_head(q[s, i, h], K[:m], V[:m], scale)
+        return out
+    monkeypatch.setattr(pa, "decode_attention_multi_quantized", bad)
+    monkeypatch.setattr(oracle, "decode_attention_multi_quantized", bad)
+
+
+def test_pins_catch_quantized_scales_swapped(monkeypatch):
+    _plant_quantized(monkeypatch, swap_scales=True)
+    assert _fails(test_quantized_closed_form_running_means)
+    assert _fails(test_quantized_equals_multi_on_dequantised_values, "int8")
+
+
+def test_pins_catch_quantized_missing_causal_window(monkeypatch):
+    _plant_quantized(monkeypatch, visible_of=lambda L, n, i: L)
+    assert _fails(test_quantized_equals_multi_on_dequantised_values, "int8")
+    assert _fails(test_quantized_closed_form_running_means)

@@ -281,6 +281,30 @@ pkv_status pkv_decode_multi_bf16(void* out, const void* q, const void* k_cache,
                                  int32_t* status, pkv_stream_t stream);
 
 /*
+ * pkv_decode_multi_q8 -- pkv_decode_multi_bf16 over a one-byte cache: INT8, FP8 E4M3 or
+ * FP8 E5M2 codes with one fp32 scale per (token, KV head) for K and for V, as written
+ * by pkv_append_int8 / pkv_append_fp8 (the quantised KV caches of "KV 缓存量化",
+ * chenk.top page), for speculative verification or a prefill chunk over such a cache.
+ * The cached value of a row element is decode(code) * scale; codes are widened exactly
+ * and each K and V value is rounded once to bf16 (code x scale) before the same
+ * tensor-core contraction as the bf16 path, for every row count (q_len * g).
+ *   kv_dtype   PKV_KV_INT8, PKV_KV_FP8_E4M3 or PKV_KV_FP8_E5M2 (else PKV_ERR_DTYPE).
+ *   k_cache, v_cache  one-byte codes [num_blocks, Hkv, block_size, D];
+ *   k_scale, v_scale  fp32 [num_blocks, Hkv, block_size].
+ *   workspace  at least pkv_decode_multi_q8_workspace_bytes(dims, q_len, kv_dtype).
+ * Other arguments, layouts and the causal rule as for pkv_decode_multi_bf16; q_len 1 is
+ * pkv_decode_int8 / pkv_decode_fp8.
+ */
+pkv_status pkv_decode_multi_q8_workspace_bytes(const pkv_dims* dims, int32_t q_len,
+                                               pkv_kv_dtype kv_dtype, size_t* bytes);
+pkv_status pkv_decode_multi_q8(void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               int32_t q_len, float scale, pkv_kv_dtype kv_dtype,
+                               const pkv_dims* dims, void* workspace, size_t workspace_bytes,
+                               int32_t* status, pkv_stream_t stream);
+
+/*
  * pkv_decode_cascade_bf16 -- pkv_decode_bf16 for a batch whose sequences all start
  * with the same `prefix_blocks` physical blocks (a shared system prompt or few-shot
  * prefix: the shared blocks of "分页注意力", chenk.top, and section 2.2 of the gsyq.cn

@@ -23,7 +23,8 @@ LIB = os.path.join(PKG, "libpagedkv.so")
 
 SOURCES = ["api.cu", "append.cu", "merge.cu", "decode_bf16.cu", "decode_int8.cu",
            "decode_e4m3.cu", "decode_e5m2.cu", "noalloc.cu",
-           "cascade.cu", "blocks.cu", "decode_tc.cu"]
+           "cascade.cu", "blocks.cu", "decode_tc.cu", "decode_tc_int8.cu", "decode_tc_e4m3.cu",
+           "decode_tc_e5m2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

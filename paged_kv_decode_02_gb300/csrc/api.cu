@@ -205,20 +205,22 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
   const int simt = mma ? 0 : P.g;
   bool found = false;
   if (q_len > 1) {
-    if (kvt != PKV_KV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (kvt < PKV_KV_BF16 || kvt > PKV_KV_FP8_E5M2) return PKV_ERR_DTYPE;
     // KV heads with 48 or more query rows go through the tcgen05 kernel, fewer rows
     // through the mma.sync path: measured on GB300 with the spec-70b lengths, tcgen05 vs
     // mma.sync per call: 16 rows 136.6 vs 93.4 us, 48 rows 146.4 vs 150.8, 64 rows 49.8
     // vs 72.8, 128 rows 152.4 vs 490.6 (an M = 128 MMA wastes what a small head leaves
     // empty). A head's rows are cut into nsg equal row tiles of at most 128 (the last one
-    // padded when they do not divide), one tcgen05 work unit each.
-    if (rows >= kTcMinRows &&
-        select_decode_tc(d->head_dim, d->block_size, rows > kTcTileRows, &P.k)) {
+    // padded when they do not divide), one tcgen05 work unit each. One-byte caches take
+    // the tcgen05 kernel for every row count (it widens the codes to bf16 in shared
+    // memory; the mma.sync multi-query path reads bf16 caches only).
+    if ((rows >= kTcMinRows || kvt != PKV_KV_BF16) &&
+        select_decode_tc(d->head_dim, d->block_size, rows > kTcTileRows, kvt, &P.k)) {
       P.nsg = (rows + kTcTileRows - 1) / kTcTileRows;
       P.gs = (rows + P.nsg - 1) / P.nsg;
       P.HU = d->num_kv_heads * P.nsg;
       found = true;
-    } else {
+    } else if (kvt == PKV_KV_BF16) {
       found = select_decode_bf16_multi(d->head_dim, d->block_size, P.nsg, &P.k);
     }
   } else {
@@ -814,6 +816,32 @@ pkv_status pkv_decode_multi_bf16(void* out, const void* q, const void* k_cache,
                                  const pkv_dims* dims, void* workspace, size_t workspace_bytes,
                                  int32_t* status, pkv_stream_t stream) {
   return run_decode(PKV_KV_BF16, out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
+                    context_lens, scale, dims, workspace, workspace_bytes, status,
+                    reinterpret_cast<cudaStream_t>(stream), q_len);
+}
+
+pkv_status pkv_decode_multi_q8_workspace_bytes(const pkv_dims* dims, int32_t q_len,
+                                               pkv_kv_dtype kv_dtype, size_t* bytes) {
+  if (!bytes) return PKV_ERR_NULL;
+  if (kv_dtype != PKV_KV_INT8 && kv_dtype != PKV_KV_FP8_E4M3 && kv_dtype != PKV_KV_FP8_E5M2)
+    return PKV_ERR_DTYPE;
+  if (q_len < 1 || q_len > kMaxQueryLen) return PKV_ERR_SHAPE;
+  Plan P;
+  pkv_status st = make_plan(dims, kv_dtype, &P, q_len);
+  if (st != PKV_OK) return st;
+  *bytes = P.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_multi_q8(void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const float* k_scale, const float* v_scale,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               int32_t q_len, float scale, pkv_kv_dtype kv_dtype,
+                               const pkv_dims* dims, void* workspace, size_t workspace_bytes,
+                               int32_t* status, pkv_stream_t stream) {
+  if (kv_dtype != PKV_KV_INT8 && kv_dtype != PKV_KV_FP8_E4M3 && kv_dtype != PKV_KV_FP8_E5M2)
+    return PKV_ERR_DTYPE;
+  return run_decode(kv_dtype, out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
                     context_lens, scale, dims, workspace, workspace_bytes, status,
                     reinterpret_cast<cudaStream_t>(stream), q_len);
 }

@@ -1,0 +1,11 @@
+// decode_tc_int8.cu -- INT8-cache instantiations of the tcgen05 decode kernel
+// (decode_tc.cuh), in a unit of their own so that the kernels compile in parallel.
+#include "decode_tc.cuh"
+
+namespace pkv {
+
+bool select_decode_tc_int8(int D, int BS, bool row_tiles, DecodeKernelInfo* info) {
+  return select_tc_code<CODE_I8>(D, BS, row_tiles, info);
+}
+
+}  // namespace pkv

@@ -148,11 +148,15 @@ bool select_decode_bf16(int D, int BS, int simt_heads, DecodeKernelInfo* info,
 // q_len > 1: the causal multi-query variant of the bf16 tensor-core path, with
 // workers of nsg warps sharing their shared-memory ring (CTA shape chosen for nsg)
 bool select_decode_bf16_multi(int D, int BS, int nsg, DecodeKernelInfo* info);
-// The tcgen05 decode kernel (bf16 caches); row_tiles: the rows of a KV head run as
-// several row tiles (more than 128 rows).
-bool select_decode_tc(int D, int BS, bool row_tiles, DecodeKernelInfo* info);
 // One-byte KV code formats.
 enum : int { CODE_I8 = 0, CODE_E4M3 = 1, CODE_E5M2 = 2 };
+// The tcgen05 decode kernel for a KV dtype (pkv_kv_dtype); row_tiles: the rows of a KV
+// head run as several row tiles (more than 128 rows). The per-code tables live in
+// decode_tc_int8.cu, decode_tc_e4m3.cu and decode_tc_e5m2.cu.
+bool select_decode_tc(int D, int BS, bool row_tiles, int kvt, DecodeKernelInfo* info);
+bool select_decode_tc_int8(int D, int BS, bool row_tiles, DecodeKernelInfo* info);
+bool select_decode_tc_e4m3(int D, int BS, bool row_tiles, DecodeKernelInfo* info);
+bool select_decode_tc_e5m2(int D, int BS, bool row_tiles, DecodeKernelInfo* info);
 
 bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info,
                         bool pair = false);

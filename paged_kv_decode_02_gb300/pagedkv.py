@@ -103,6 +103,16 @@ EXPORTS = {
                                                                       ctypes.c_size_t,
                                                                       ctypes.c_void_p,
                                                                       ctypes.c_void_p]),
+    "pkv_decode_multi_q8_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
+                                                           ctypes.c_int,
+                                                           ctypes.POINTER(ctypes.c_size_t)]),
+    "pkv_decode_multi_q8": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int32,
+                                                                   ctypes.c_float, ctypes.c_int,
+                                                                   ctypes.c_void_p,
+                                                                   ctypes.c_void_p,
+                                                                   ctypes.c_size_t,
+                                                                   ctypes.c_void_p,
+                                                                   ctypes.c_void_p]),
     "pkv_decode_cascade_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
                                                           ctypes.POINTER(ctypes.c_size_t)]),
     "pkv_decode_cascade_bf16": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int32,
@@ -595,6 +605,77 @@ def paged_decode_attention_multi(q, k_cache, v_cache, block_tables, context_lens
                                           float(scale), ctypes.byref(dims), _ptr(workspace),
                                           ws_bytes, _ptr(status), _stream(dev))
     _check(st, "pkv_decode_multi_bf16")
+    return out
+
+
+def multi_q8_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             num_blocks, max_blocks_per_seq, q_len, kv_dtype, device=None):
+    """Workspace of :func:`paged_decode_attention_multi_q8` (kv_dtype KV_INT8,
+    KV_FP8_E4M3 or KV_FP8_E5M2)."""
+    dims = Dims(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq)
+    out = ctypes.c_size_t(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = _lib().pkv_decode_multi_q8_workspace_bytes(ctypes.byref(dims), int(q_len),
+                                                        int(kv_dtype), ctypes.byref(out))
+    _check(st, "pkv_decode_multi_q8_workspace_bytes")
+    return int(out.value)
+
+
+def _q8_kind(k_cache, fmt):
+    """KV dtype code of a one-byte cache: int8 codes, or FP8 codes (uint8 with ``fmt``,
+    or a torch float8 dtype)."""
+    if k_cache.dtype == torch.int8:
+        return KV_INT8
+    if k_cache.dtype == torch.float8_e4m3fn:
+        return KV_FP8_E4M3
+    if k_cache.dtype == torch.float8_e5m2:
+        return KV_FP8_E5M2
+    if k_cache.dtype == torch.uint8:
+        return _fp8_format(fmt)
+    raise TypeError(f"a one-byte cache holds int8, uint8 or float8 codes, not {k_cache.dtype}")
+
+
+def paged_decode_attention_multi_q8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                    context_lens, scale, fmt="e5m2", out=None, workspace=None,
+                                    status=None):
+    """:func:`paged_decode_attention_multi` over a one-byte cache: int8 codes (INT8), or
+    FP8 codes (uint8 with ``fmt`` "e4m3" / "e5m2", or the matching torch float8 dtype),
+    with per-(token, KV head) fp32 scales ``k_scale``/``v_scale`` [NB, Hkv, bs]."""
+    dev = q.device
+    status = _status_word(status, dev)
+    kv = _q8_kind(k_cache, fmt)
+    _require(q, "q", torch.bfloat16, 4, dev)
+    _require_any(k_cache, "k_cache", _code_dtypes(kv), 4, dev)
+    _require_any(v_cache, "v_cache", _code_dtypes(kv), 4, dev)
+    _require(k_scale, "k_scale", torch.float32, 3, dev)
+    _require(v_scale, "v_scale", torch.float32, 3, dev)
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    B, n, Hq, D = q.shape
+    if k_cache.shape != v_cache.shape or k_cache.shape[3] != D:
+        raise ValueError("cache shapes disagree with q")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    _cache_shapes(k_cache, v_cache, k_scale, v_scale)
+    dims = _dims(B, Hq, k_cache, block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _require(out, "out", torch.bfloat16, 4, dev)
+        _same_shape(out, "out", q.shape)
+    with _OnDevice(dev):
+        need = ctypes.c_size_t(0)
+        _check(_lib().pkv_decode_multi_q8_workspace_bytes(ctypes.byref(dims), n, kv,
+                                                          ctypes.byref(need)),
+               "pkv_decode_multi_q8_workspace_bytes")
+        workspace, ws_bytes = _workspace(workspace, need.value, dev)
+        st = _lib().pkv_decode_multi_q8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                                        _ptr(context_lens), n, float(scale), kv,
+                                        ctypes.byref(dims), _ptr(workspace), ws_bytes,
+                                        _ptr(status), _stream(dev))
+    _check(st, "pkv_decode_multi_q8")
     return out
 
 

@@ -138,3 +138,23 @@ def oracle_outputs_all(w):
     for (s, h), r in zip(pairs, res):
         out[s, :, h * g:(h + 1) * g] = r
     return out if w.q_len > 1 else out[:, 0]
+
+
+def oracle_outputs_multi_q8(w):
+    """Whole output [B, q_len, Hq, D] of multi-query decode over a one-byte cache from
+    oracle.decode_attention_multi_quantized, each sequence's own blocks copied to the
+    host and re-indexed."""
+    B, n, Hq, D = w.q.shape
+    fmt = "int8" if w.kv_dtype == "int8" else w.kv_dtype[4:]
+    out = np.zeros((B, n, Hq, D))
+    q = to_f64(w.q)
+    for s in range(B):
+        L, blocks = sequence_blocks(w, s)
+        if L == 0:
+            continue
+        kc, vc = w.k_cache[blocks].cpu().numpy(), w.v_cache[blocks].cpu().numpy()
+        ks, vs = w.k_scale[blocks].cpu().numpy(), w.v_scale[blocks].cpu().numpy()
+        out[s] = oracle.decode_attention_multi_quantized(
+            q[s:s + 1], kc, vc, ks, vs, np.arange(len(blocks))[None, :], [L], w.scale, fmt,
+            w.block_size)[0]
+    return out

@@ -9,7 +9,8 @@ import pytest
 import torch
 
 from paged_kv_decode_02_gb300.workloads import make_workload
-from parity_helpers import DECODE_ATOL, oracle_outputs_all, oracle_outputs_multi, to_f64
+from parity_helpers import (DECODE_ATOL, oracle_outputs_all, oracle_outputs_multi,
+                            oracle_outputs_multi_q8, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -253,3 +254,67 @@ def test_tc_graph_replays(pk):
         torch.cuda.synchronize()
         w.q = q.clone()
         assert _err(out, oracle_outputs_multi(w)) <= DECODE_ATOL
+
+
+# ---------------------------------------------------------------------------
+# one-byte caches (INT8, FP8 E4M3 / E5M2 codes with per-(token, KV head) scales)
+# ---------------------------------------------------------------------------
+
+def _run_q8(pk, w, **kw):
+    return pk.paged_decode_attention_multi_q8(w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                              w.block_tables, w.context_lens, w.scale,
+                                              fmt=w.kv_dtype[4:] if w.kv_dtype != "int8"
+                                              else "e5m2", **kw)
+
+
+Q8_SHAPES = [
+    # (id, Hq, Hkv, D, bs, q_len, lengths): 16, 48, 128 and several row tiles of rows
+    ("g8-q2", 16, 2, 128, 16, 2, [2, 17, 300, 0, 129]),
+    ("g8-q6-bs32", 16, 2, 128, 32, 6, [6, 40, 700, 33]),
+    ("g8-q16-d64", 16, 2, 64, 16, 16, [16, 100, 1000]),
+    ("g4-q64", 8, 2, 128, 16, 64, [64, 65, 500]),
+    ("g1-q3-mha", 4, 4, 128, 32, 3, [3, 90, 257]),
+]
+
+
+@pytest.mark.parametrize("kvt", ["int8", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("shape", Q8_SHAPES, ids=[s[0] for s in Q8_SHAPES])
+def test_multi_q8_small_shapes(pk, shape, kvt):
+    _, Hq, Hkv, D, bs, n, lengths = shape
+    w = make_workload("spec-70b", device=DEV, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                      block_size=bs, lengths=lengths, q_len=n, seed=33, kv_dtype=kvt,
+                      poison_unused=True)
+    out = _run_q8(pk, w)
+    torch.cuda.synchronize()
+    assert _err(out, oracle_outputs_multi_q8(w)) <= DECODE_ATOL
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out2 = _run_q8(pk, w, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert _err(out2, oracle_outputs_multi_q8(w)) <= DECODE_ATOL
+
+
+@pytest.mark.parametrize("kvt", ["int8", "fp8_e5m2"])
+def test_multi_q8_full_size_after_append(pk, kvt):
+    """The spec-70b step over a one-byte cache: quantise and append the 6 new tokens of
+    every request, then verify; every output row against the oracle."""
+    w = make_workload("spec-70b", device=DEV, kv_dtype=kvt)
+    if kvt == "int8":
+        pk.paged_kv_append_int8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                w.slot_mapping)
+    else:
+        pk.paged_kv_append_fp8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                               w.slot_mapping, fmt=kvt[4:])
+    out = _run_q8(pk, w)
+    torch.cuda.synchronize()
+    assert _err(out, oracle_outputs_all(w)) <= DECODE_ATOL
+
+
+def test_multi_q8_single_token_is_decode(pk):
+    w = make_workload("int8", device=DEV, num_seqs=4, lengths=[5, 300, 1000, 0], seed=34)
+    a = pk.paged_decode_attention_int8(w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                       w.block_tables, w.context_lens, w.scale)
+    b = pk.paged_decode_attention_multi_q8(w.q[:, None], w.k_cache, w.v_cache, w.k_scale,
+                                           w.v_scale, w.block_tables, w.context_lens, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b[:, 0])

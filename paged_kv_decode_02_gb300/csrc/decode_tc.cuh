@@ -330,15 +330,15 @@ __device__ __forceinline__ bool converters_all(bool v) {
   return r != 0;
 }
 
-// One-byte codes of a 128-token tile -> bf16 values (code x scale, one rounding) in the
-// MMA layout of the tile's buffer (K-major, 128-byte swizzled 64-column slabs). The
-// codes sit in the buffer's last kCodeTile bytes as the TMA wrote them (D-byte rows,
-// 128- or 64-byte swizzle); every thread first loads all its chunks and scales, the
-// converters meet, then write (the writes cover the codes). Rows from `valid` on
-// become zeros (their scales may hold anything). ct: 0..127.
-template <int D, int CODE>
-__device__ __forceinline__ void convert_codes_to_bf16(uint32_t tile, uint32_t scales, int valid,
-                                                      int ct) {
+// One-byte codes of a 128-token tile -> 16-bit values (code x scale, one rounding; bf16,
+// or fp16 when kF16) in the MMA layout of the tile's buffer (K-major, 128-byte swizzled
+// 64-column slabs). The codes sit in the buffer's last kCodeTile bytes as the TMA wrote
+// them (D-byte rows, 128- or 64-byte swizzle); every thread first loads all its chunks
+// and scales, the converters meet, then write (the writes cover the codes). Rows from
+// `valid` on become zeros (their scales may hold anything). ct: 0..127.
+template <int D, int CODE, bool kF16>
+__device__ __forceinline__ void convert_codes(uint32_t tile, uint32_t scales, int valid,
+                                              int ct) {
   using Codec = Code8<CODE>;
   constexpr int kN = 128, kSlab = kN * 128;
   constexpr int kCh = D / 16;                  // 16-code chunks per row
@@ -364,8 +364,13 @@ __device__ __forceinline__ void convert_codes_to_bf16(uint32_t tile, uint32_t sc
     for (int e = 0; e < 4; ++e) {
       const uint32_t b = Codec::pre(wd[e]);
       const float2 f01 = unpack_f16x2(Codec::lo(b)), f23 = unpack_f16x2(Codec::hi(b));
-      o[2 * e] = live ? pack_bf16x2(f01.x * sc[m], f01.y * sc[m]) : 0u;
-      o[2 * e + 1] = live ? pack_bf16x2(f23.x * sc[m], f23.y * sc[m]) : 0u;
+      if constexpr (kF16) {
+        o[2 * e] = live ? pack_f16x2(f01.x * sc[m], f01.y * sc[m]) : 0u;
+        o[2 * e + 1] = live ? pack_f16x2(f23.x * sc[m], f23.y * sc[m]) : 0u;
+      } else {
+        o[2 * e] = live ? pack_bf16x2(f01.x * sc[m], f01.y * sc[m]) : 0u;
+        o[2 * e + 1] = live ? pack_bf16x2(f23.x * sc[m], f23.y * sc[m]) : 0u;
+      }
     }
     // columns 16c .. 16c + 15: slab 16c / 64, 16-byte chunks 2 (c % 4) and + 1 of it
     const int slab = (16 * c) >> 6, ch0 = ((16 * c) & 63) >> 3;
@@ -434,9 +439,10 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, K::kTmemCols);
-  for (int k = tid; k < 4096 / 16; k += K::kThreads)  // bf16 1.0 everywhere
+  for (int k = tid; k < 4096 / 16; k += K::kThreads)  // 1.0 everywhere (bf16, or fp16)
     tc::sts128(base + K::kOffOnes + 16 * k,
-               make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u));
+               kQ8 ? make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u)   // fp16 1.0
+                   : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u)); // bf16
   fence_proxy_async_smem();  // for the MMAs that read it
 
   // ---- tiles per sequence, their exclusive prefix, the weighted prefix (tiles plus
@@ -578,8 +584,11 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_bf16<128, K::kN, false>();
-      constexpr uint32_t kIdO = tc::idesc_bf16<128, D, true>();
-      constexpr uint32_t kIdL = tc::idesc_bf16<128, 16, false>();
+      // P.V and the row sums run on fp16 weights and values for one-byte caches
+      constexpr uint32_t kIdO =
+          kQ8 ? tc::idesc_f16<128, D, true>() : tc::idesc_bf16<128, D, true>();
+      constexpr uint32_t kIdL =
+          kQ8 ? tc::idesc_f16<128, 16, false>() : tc::idesc_bf16<128, 16, false>();
       const uint32_t ones = base + K::kOffOnes;
       auto issue_s = [&](int i, int qb) -> bool {
         const int st = i & 1;
@@ -816,8 +825,9 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         m_ref = mt;
         rescale = seg_tile > 0;
       }
-      // weights 2^(scale * s - m) (packed fp32x2 FMAs), bf16 pairs; their row sums come
-      // from the tensor cores (P times a ones tile, beside P.V)
+      // weights 2^(scale * s - m) (packed fp32x2 FMAs), bf16 pairs (fp16 over one-byte
+      // caches); their row sums come from the tensor cores (P times a ones tile, beside
+      // P.V)
       uint32_t pk[K::kN / 2];
       const float2 asl2 = make_float2(asl, asl), nm2 = make_float2(-m_ref, -m_ref);
       if (full) {
@@ -825,14 +835,16 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         for (int t = 0; t < K::kN; t += 2) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
                                       asl2, nm2);
-          pk[t / 2] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
+          pk[t / 2] = kQ8 ? pack_f16x2(fast_exp2(x.x), fast_exp2(x.y))
+                          : pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
         }
       } else {
 #pragma unroll
         for (int t = 0; t < K::kN; t += 2) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
                                       asl2, nm2);
-          pk[t / 2] = pack_bf16x2(t < vis ? fast_exp2(x.x) : 0.f, t + 1 < vis ? fast_exp2(x.y) : 0.f);
+          const float w0 = t < vis ? fast_exp2(x.x) : 0.f, w1 = t + 1 < vis ? fast_exp2(x.y) : 0.f;
+          pk[t / 2] = kQ8 ? pack_f16x2(w0, w1) : pack_bf16x2(w0, w1);
         }
       }
       if (!zero_v_tail(i, L, t0)) {
@@ -1015,10 +1027,16 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
           ok = false;
           break;
         }
-        if constexpr (kQ8)
-          convert_codes_to_bf16<D, (kQ8 ? CODE : 0)>(
-              base + (kv == 0 ? K::kOffK : K::kOffV) + st * K::kTile, scale_area(kv == 0, st),
-              valid, ct);
+        // K as bf16 (the score MMA's other operand is the bf16 q); V as fp16, whose
+        // 11-bit significand keeps code x scale within 2^-12 of its value (P.V then
+        // runs on fp16 weights)
+        if constexpr (kQ8) {
+          const uint32_t tile = base + (kv == 0 ? K::kOffK : K::kOffV) + st * K::kTile;
+          if (kv == 0)
+            convert_codes<D, (kQ8 ? CODE : 0), false>(tile, scale_area(true, st), valid, ct);
+          else
+            convert_codes<D, (kQ8 ? CODE : 0), true>(tile, scale_area(false, st), valid, ct);
+        }
         fence_proxy_async_smem();  // the bf16 values, for the MMAs (async proxy)
         converters_sync();
         if (ct == 0) mbar_arrive(kv == 0 ? kfull(st) : vfull(st));

@@ -92,6 +92,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16() {
          (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// The same with fp16 A and B (format code 0 in bits 7..9 and 10..12).
+template <int M, int N, bool kBMnMajor>
+__host__ __device__ constexpr uint32_t idesc_f16() {
+  static_assert(M == 64 || M == 128, "one-CTA MMA: M is 64 or 128");
+  static_assert(N % 16 == 0 && N >= 16 && N <= 256, "N: multiple of 16 up to 256");
+  return (1u << 4) | (kBMnMajor ? (1u << 16) : 0u) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
+}
+
 // One thread: D[tmem] (+)= A[smem] * B[smem]^T (K = 16 for bf16). `accumulate` = 0
 // overwrites D.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,

@@ -82,16 +82,19 @@ struct TcDecode {
   static constexpr int kOffV = kOffK + 2 * kTile;
   // all-ones B operand (16 x 128 tokens, K-major) of the MMA that sums the rows of P
   static constexpr int kOffOnes = kOffV + 2 * kTile;
-  // one-byte caches: a tile's codes land in the last kCodeTile bytes of its bf16 buffer;
-  // its scales in [K stage 0, K stage 1, V stage 0, V stage 1] x kN fp32
+  // one-byte caches: a tile's codes land in the last kCodeTile bytes of its 16-bit
+  // buffer; its scales in kN fp32 slots: K scales in four (tile i in slot i % 4: the
+  // softmax of tile i reads them, and tile i + 4's copy only starts once it has), then V
+  // scales in two (the stage's, read by the converters only)
   static constexpr int kCodeTile = kN * D;
   static constexpr int kCodeOff = kTile - kCodeTile;
   static constexpr int kScaleBytes = kN * 4;
   static constexpr int kOffScales = kOffOnes + 4096;
-  static constexpr int kOffBar = kOffScales + (Q8 ? 4 * kScaleBytes : 0);
+  static constexpr int kOffBar = kOffScales + (Q8 ? 6 * kScaleBytes : 0);
   // mbarriers: kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] pfull ofull mdone qfull[2] ofree
-  // (+ one-byte caches: kstage[2] vstage[2], the copies of the codes)
-  static constexpr int kNumBars = Q8 ? 20 : 16;
+  // (+ one-byte caches: kstage[2] vstage[2], the copies of the codes; kscale[4], the K
+  // scales of slot i % 4 ready for the softmax)
+  static constexpr int kNumBars = Q8 ? 24 : 16;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   // [2] cut segments of this CTA (first, last) for the tail fixup: s, h, n, tiles, state
@@ -336,7 +339,7 @@ __device__ __forceinline__ bool converters_all(bool v) {
 // them (D-byte rows, 128- or 64-byte swizzle); every thread first loads all its chunks
 // and scales, the converters meet, then write (the writes cover the codes). Rows from
 // `valid` on become zeros (their scales may hold anything). ct: 0..127.
-template <int D, int CODE, bool kF16>
+template <int D, int CODE, bool kF16, bool kScale>
 __device__ __forceinline__ void convert_codes(uint32_t tile, uint32_t scales, int valid,
                                               int ct) {
   using Codec = Code8<CODE>;
@@ -351,7 +354,7 @@ __device__ __forceinline__ void convert_codes(uint32_t tile, uint32_t scales, in
   for (int m = 0; m < kItems; ++m) {
     const int item = ct + 128 * m, t = item / kCh, c = item % kCh;
     raw[m] = lds128(stg + swz<kSeg>(uint32_t(t * D + c * 16)));
-    sc[m] = lds_f32(scales + 4 * t);
+    sc[m] = kScale ? lds_f32(scales + 4 * t) : 1.f;
   }
   converters_sync();  // every read of the codes before any write over them
 #pragma unroll
@@ -418,9 +421,11 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
   // complete when the converters have written the bf16 values
   auto kstage = [&](int st) { return bar(16 + st); };
   auto vstage = [&](int st) { return bar(18 + st); };
-  auto scale_area = [&](bool is_k, int st) {
-    return base + K::kOffScales + uint32_t((is_k ? 0 : 2) + st) * K::kScaleBytes;
+  // K scales of tile i: slot i % 4; V scales of tile i: slot 4 + i % 2
+  auto scale_area = [&](bool is_k, int i) {
+    return base + K::kOffScales + uint32_t(is_k ? (i & 3) : 4 + (i & 1)) * K::kScaleBytes;
   };
+  auto kscale = [&](int i) { return bar(20 + (i & 3)); };
   const uint32_t tmem_slot = base + K::kOffTmemSlot;
 
   pdl_wait_prior_grid();
@@ -433,7 +438,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     mbar_init(qfull(1), 4 * 32);
     mbar_init(ofree, 4 * 32);
     if constexpr (kQ8)
-      for (int i = 16; i < 20; ++i) mbar_init(bar(i), 1);
+      for (int i = 16; i < 24; ++i) mbar_init(bar(i), 1);
     *abort_flag = 0;
     s_cut[4] = s_cut[9] = 0;
     fence_mbar_init();
@@ -559,7 +564,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         if (lane < K::kBlocks) {
           tma_load_2d(region + st * K::kTile + K::kCodeOff + lane * BS * D, map, fb, 0, row);
           const float* sc = is_k ? p.k_scale : p.v_scale;
-          bulk_load(scale_area(is_k, st) + lane * BS * 4,
+          bulk_load(scale_area(is_k, i) + lane * BS * 4,
                     sc + size_t(row == rows_total ? row0 : row), BS * 4, fb);
         }
       } else {
@@ -797,6 +802,22 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
       }
       uint32_t s[K::kN];
       tc::tmem_ld128(trow + K::kColS + st * K::kN, s);
+      if constexpr (kQ8) {  // one-byte caches: each column times its K scale
+        if (!__all_sync(0xffffffffu, tc::wait_or_abort(kscale(i), uint32_t(i >> 2) & 1u,
+                                                       p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const uint32_t ks = scale_area(true, i);
+#pragma unroll
+        for (int t = 0; t < K::kN; t += 4) {
+          const uint4 k4 = lds128(ks + 4 * t);  // the same address in every lane
+          s[t] = __float_as_uint(__uint_as_float(s[t]) * __uint_as_float(k4.x));
+          s[t + 1] = __float_as_uint(__uint_as_float(s[t + 1]) * __uint_as_float(k4.y));
+          s[t + 2] = __float_as_uint(__uint_as_float(s[t + 2]) * __uint_as_float(k4.z));
+          s[t + 3] = __float_as_uint(__uint_as_float(s[t + 3]) * __uint_as_float(k4.w));
+        }
+      }
       if (sl < 0.f) {  // a negative scale is carried by the scores' signs
 #pragma unroll
         for (int t = 0; t < K::kN; ++t) s[t] ^= 0x80000000u;
@@ -1027,19 +1048,28 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
           ok = false;
           break;
         }
-        // K as bf16 (the score MMA's other operand is the bf16 q); V as fp16, whose
-        // 11-bit significand keeps code x scale within 2^-12 of its value (P.V then
-        // runs on fp16 weights)
+        // K: the codes themselves as bf16 (exact), the score MMA's other operand being
+        // the bf16 q, and the softmax multiplies each score column by its K scale (fp32);
+        // V: code x scale as fp16, whose 11-bit significand keeps it within 2^-12 of its
+        // value (P.V then runs on fp16 weights)
         if constexpr (kQ8) {
           const uint32_t tile = base + (kv == 0 ? K::kOffK : K::kOffV) + st * K::kTile;
-          if (kv == 0)
-            convert_codes<D, (kQ8 ? CODE : 0), false>(tile, scale_area(true, st), valid, ct);
-          else
-            convert_codes<D, (kQ8 ? CODE : 0), true>(tile, scale_area(false, st), valid, ct);
+          if (kv == 0) {
+            convert_codes<D, (kQ8 ? CODE : 0), false, false>(tile, scale_area(true, i), valid,
+                                                             ct);
+            // scales of rows past the context may hold anything: zero for the softmax
+            if (ct >= valid) tc::sts32(scale_area(true, i) + 4 * ct, 0u);
+          } else {
+            convert_codes<D, (kQ8 ? CODE : 0), true, true>(tile, scale_area(false, i), valid,
+                                                           ct);
+          }
         }
-        fence_proxy_async_smem();  // the bf16 values, for the MMAs (async proxy)
+        fence_proxy_async_smem();  // the 16-bit values, for the MMAs (async proxy)
         converters_sync();
-        if (ct == 0) mbar_arrive(kv == 0 ? kfull(st) : vfull(st));
+        if (ct == 0) {
+          mbar_arrive(kv == 0 ? kfull(st) : vfull(st));
+          if (kv == 0) mbar_arrive(kscale(i));
+        }
       }
       tile_next(cur, s_prefix, B, U);
     }

@@ -61,6 +61,18 @@ WORKLOAD_TEXT = {
                     "tokens: batch 64, 64 q / 8 kv heads, head_dim 128, block 16, context "
                     "log-normal (median 1024, sigma 1) clipped [128, 32768], q_len 16 new "
                     "tokens per request (128 query rows per KV head), causal",
+    "prefix-int8": "prefix sharing over an INT8 KV cache: batch 256, 32 q / 8 kv heads, "
+                   "head_dim 128, block 16, shared 2048-token prefix + suffix U[16,512], "
+                   "per-token per-head fp32 scales",
+    "prefix-e5m2": "prefix sharing over an FP8 E5M2 KV cache: batch 256, 32 q / 8 kv heads, "
+                   "head_dim 128, block 16, shared 2048-token prefix + suffix U[16,512], "
+                   "per-token per-head fp32 scales",
+    "spec-70b-int8": "speculative verification over an INT8 KV cache: the spec-70b shape "
+                     "(batch 64, 64 q / 8 kv heads, head_dim 128, block 16, q_len 6), "
+                     "per-token per-head fp32 scales",
+    "spec-70b-e4m3": "speculative verification over an FP8 E4M3 KV cache: the spec-70b shape "
+                     "(batch 64, 64 q / 8 kv heads, head_dim 128, block 16, q_len 6), "
+                     "per-token per-head fp32 scales",
     "chunk-70b": "chunked prefill on the 70B-like GQA shape: 16 requests, 64 q / 8 kv heads, "
                  "head_dim 128, block 16, a 256-token prefill chunk per request (2048 query "
                  "rows per KV head) at the end of a context log-normal (median 1024, sigma 1) "
@@ -69,7 +81,9 @@ WORKLOAD_TEXT = {
 # the workloads recorded beside the headline, each as (config, cascade)
 PER_CONFIG = [("tiny", False), ("7b", False), ("70b-gqa", False), ("prefix", False),
               ("int8", False), ("int8-bs16", False), ("fp8-e5m2", False), ("fp8-e4m3", False),
-              ("spec-70b", False), ("spec-70b-q16", False), ("chunk-70b", False)]
+              ("spec-70b", False), ("spec-70b-q16", False), ("chunk-70b", False),
+              ("prefix-int8", True), ("prefix-e5m2", True), ("spec-70b-int8", False),
+              ("spec-70b-e4m3", False)]
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 
@@ -100,9 +114,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
     args = ap.parse_args(argv)
-    if args.cascade and args.config != "prefix":
+    if args.cascade and not args.config.startswith("prefix"):
         ap.error("--cascade needs the prefix workload (a prefix shared by every request)")
-    args.use_cascade = args.config == "prefix" and not args.plain
+    args.use_cascade = args.config.startswith("prefix") and not args.plain
     return args
 
 
@@ -382,18 +396,29 @@ def api_append(pk, w, k, v, slots):
 
 def api_decode(pk, w, q, tables, lens, out, ws, cascade_blocks=0):
     """The decode call for the workload's cache dtype (cascade when asked)."""
-    if w.kv_dtype == "int8":
+    fmt = w.kv_dtype[4:] if w.kv_dtype.startswith("fp8_") else "e5m2"
+    if cascade_blocks:
+        if _one_byte(w):
+            pk.paged_decode_attention_cascade_q8(q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                                 tables, lens, cascade_blocks, w.scale, fmt=fmt,
+                                                 out=out, workspace=ws)
+        else:
+            pk.paged_decode_attention_cascade(q, w.k_cache, w.v_cache, tables, lens,
+                                              cascade_blocks, w.scale, out=out, workspace=ws)
+    elif w.q_len > 1:
+        if _one_byte(w):
+            pk.paged_decode_attention_multi_q8(q, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                               tables, lens, w.scale, fmt=fmt, out=out,
+                                               workspace=ws)
+        else:
+            pk.paged_decode_attention_multi(q, w.k_cache, w.v_cache, tables, lens, w.scale,
+                                            out=out, workspace=ws)
+    elif w.kv_dtype == "int8":
         pk.paged_decode_attention_int8(q, w.k_cache, w.v_cache, w.k_scale, w.v_scale, tables,
                                        lens, w.scale, out=out, workspace=ws)
     elif w.kv_dtype.startswith("fp8_"):
         pk.paged_decode_attention_fp8(q, w.k_cache, w.v_cache, w.k_scale, w.v_scale, tables,
-                                      lens, w.scale, fmt=w.kv_dtype[4:], out=out, workspace=ws)
-    elif cascade_blocks:
-        pk.paged_decode_attention_cascade(q, w.k_cache, w.v_cache, tables, lens, cascade_blocks,
-                                          w.scale, out=out, workspace=ws)
-    elif w.q_len > 1:
-        pk.paged_decode_attention_multi(q, w.k_cache, w.v_cache, tables, lens, w.scale, out=out,
-                                        workspace=ws)
+                                      lens, w.scale, fmt=fmt, out=out, workspace=ws)
     else:
         pk.paged_decode_attention(q, w.k_cache, w.v_cache, tables, lens, w.scale, out=out,
                                   workspace=ws)
@@ -401,18 +426,16 @@ def api_decode(pk, w, q, tables, lens, out, ws, cascade_blocks=0):
 
 def workspace_for(pk, w, cascade_blocks, dev):
     import torch
+    dims = (w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.num_blocks,
+            w.max_blocks_per_seq)
     if cascade_blocks:
-        need = pk.cascade_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                          w.block_size, w.num_blocks, w.max_blocks_per_seq,
-                                          cascade_blocks)
+        need = pk.cascade_q8_workspace_bytes(*dims, cascade_blocks, _kv_code(pk, w)) \
+            if _one_byte(w) else pk.cascade_workspace_bytes(*dims, cascade_blocks)
     elif w.q_len > 1:
-        need = pk.multi_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                        w.block_size, w.num_blocks, w.max_blocks_per_seq,
-                                        w.q_len)
+        need = pk.multi_q8_workspace_bytes(*dims, w.q_len, _kv_code(pk, w)) \
+            if _one_byte(w) else pk.multi_workspace_bytes(*dims, w.q_len)
     else:
-        need = pk.decode_workspace_bytes(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                         w.block_size, w.num_blocks, w.max_blocks_per_seq,
-                                         _kv_code(pk, w))
+        need = pk.decode_workspace_bytes(*dims, _kv_code(pk, w))
     return torch.zeros(need, dtype=torch.uint8, device=dev)
 
 
@@ -445,8 +468,8 @@ def measure_workload(pk, name, cascade, args, dev, world, min_seconds, with_e2e=
     from paged_kv_decode_02_gb300.workloads import make_workload
     w = make_workload(name, device=dev)
     cascade_blocks = w.extra.get("prefix_tokens", 0) // w.block_size if cascade else 0
-    if cascade and (_one_byte(w) or cascade_blocks == 0):
-        raise SystemExit("cascade decode needs a bf16 workload with a shared prefix (prefix)")
+    if cascade and cascade_blocks == 0:
+        raise SystemExit("cascade decode needs a workload with a shared prefix (prefix*)")
     ws = workspace_for(pk, w, cascade_blocks, dev)
     out = torch.empty_like(w.q)
     stream = torch.cuda.current_stream(dev)
@@ -602,7 +625,7 @@ def decode_kernels(w, cascade_blocks, launches):
     if cascade_blocks:
         return "paged_prefix_kernel + paged_decode_kernel + paged_cascade_merge_kernel"
     rows = w.q_len * w.num_q_heads // w.num_kv_heads        # query rows per KV head
-    main = "paged_decode_tc_kernel" if (w.q_len > 1 and 48 <= rows <= 128) else \
+    main = "paged_decode_tc_kernel" if (w.q_len > 1 and (rows >= 48 or _one_byte(w))) else \
         "paged_decode_kernel"
     if launches == 1:
         return main + " (split-KV parts folded inside the kernel, one launch per call)"

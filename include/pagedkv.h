@@ -329,6 +329,27 @@ pkv_status pkv_decode_cascade_bf16(void* out, const void* q, const void* k_cache
                                    size_t workspace_bytes, int32_t* status, pkv_stream_t stream);
 
 /*
+ * pkv_decode_cascade_q8 -- pkv_decode_cascade_bf16 over a one-byte cache (INT8, FP8 E4M3
+ * or E5M2 codes with one fp32 scale per (token, KV head) for K and for V): a shared
+ * system prompt over the quantised caches of "KV 缓存量化" (chenk.top page). The
+ * shared prefix runs on the tensor cores with the codes widened in shared memory (K
+ * codes exactly, each score column times its K scale; V as fp16 code x scale), the
+ * suffixes through the one-byte decode of pkv_decode_int8 / pkv_decode_fp8.
+ *   kv_dtype   PKV_KV_INT8, PKV_KV_FP8_E4M3 or PKV_KV_FP8_E5M2 (else PKV_ERR_DTYPE).
+ *   workspace  at least pkv_decode_cascade_q8_workspace_bytes(dims, prefix_blocks,
+ *              kv_dtype) bytes.
+ * Everything else as for pkv_decode_cascade_bf16.
+ */
+pkv_status pkv_decode_cascade_q8_workspace_bytes(const pkv_dims* dims, int32_t prefix_blocks,
+                                                 pkv_kv_dtype kv_dtype, size_t* bytes);
+pkv_status pkv_decode_cascade_q8(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const float* k_scale, const float* v_scale,
+                                 const int32_t* block_tables, const int32_t* context_lens,
+                                 int32_t prefix_blocks, float scale, pkv_kv_dtype kv_dtype,
+                                 const pkv_dims* dims, void* workspace, size_t workspace_bytes,
+                                 int32_t* status, pkv_stream_t stream);
+
+/*
  * pkv_decode_bf16_noalloc -- pkv_decode_bf16 for callers that cannot allocate device
  * memory (code running inside another runtime's memory pool, plugins not allowed to
  * call cudaMalloc, or latency-critical paths where no allocation may happen). The pages

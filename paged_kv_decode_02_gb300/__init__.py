@@ -10,7 +10,8 @@ _API = (
     "paged_kv_append", "paged_kv_append_int8", "paged_kv_append_fp8",
     "paged_decode_attention", "paged_decode_attention_int8", "paged_decode_attention_fp8",
     "paged_decode_attention_cascade", "paged_decode_attention_multi",
-    "paged_decode_attention_multi_q8",
+    "paged_decode_attention_multi_q8", "paged_decode_attention_cascade_q8",
+    "cascade_q8_workspace_bytes",
     "cascade_workspace_bytes", "multi_workspace_bytes", "multi_q8_workspace_bytes",
     "copy_blocks", "swap_out", "swap_in",
     "decode_workspace_bytes", "library_path", "load_library", "PagedKVError",

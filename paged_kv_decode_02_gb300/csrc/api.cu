@@ -409,11 +409,14 @@ struct CascadePlan {
   size_t off_prefix, off_ml, off_o, off_pre_o, off_pre_ml, ws_bytes;
 };
 
-pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* cp) {
+pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* cp,
+                             int kvt = PKV_KV_BF16) {
   pkv_status st = check_dims(d);
   if (st != PKV_OK) return st;
+  if (kvt < PKV_KV_BF16 || kvt > PKV_KV_FP8_E5M2) return PKV_ERR_DTYPE;
   if (prefix_blocks < 1 || prefix_blocks > d->max_blocks_per_seq) return PKV_ERR_SHAPE;
-  if (!select_prefix_kernel(d->head_dim, d->block_size, &cp->pk)) return PKV_ERR_UNSUPPORTED;
+  if (!select_prefix_kernel(d->head_dim, d->block_size, kvt, &cp->pk))
+    return PKV_ERR_UNSUPPORTED;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -435,8 +438,7 @@ pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* 
       std::max(min_split, std::max(1, std::min(tiles, budget / std::max(1, ctas))));
   cp->per_split = ((tiles + nsplit - 1) / nsplit) * cp->pk.tile_blocks;
   cp->nsplit = (prefix_blocks + cp->per_split - 1) / cp->per_split;
-  st = make_plan(d, PKV_KV_BF16, &cp->dec, 1, true,
-                 cp->overlap ? sms - ctas * cp->nsplit : 0);
+  st = make_plan(d, kvt, &cp->dec, 1, true, cp->overlap ? sms - ctas * cp->nsplit : 0);
   if (st != PKV_OK) return st;
   const Plan& P = cp->dec;
   const size_t nslots = size_t(2) * P.W + size_t(d->num_seqs) * P.HU;
@@ -453,7 +455,8 @@ pkv_status make_cascade_plan(const pkv_dims* d, int prefix_blocks, CascadePlan* 
   return PKV_OK;
 }
 
-pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
+pkv_status run_cascade(int kvt, void* out, const void* q, const void* k_cache,
+                       const void* v_cache, const float* k_scale, const float* v_scale,
                        const int32_t* block_tables, const int32_t* context_lens,
                        int prefix_blocks, float scale, const pkv_dims* d, void* workspace,
                        size_t workspace_bytes, int32_t* status, cudaStream_t stream) {
@@ -461,10 +464,13 @@ pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void
   if (st != PKV_OK) return st;
   if (d->num_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_NULL;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+  const bool q8 = kvt != PKV_KV_BF16;
+  if (q8 && (!k_scale || !v_scale)) return PKV_ERR_NULL;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (q8 && (!aligned16(k_scale) || !aligned16(v_scale))))
     return PKV_ERR_ALIGNMENT;
   CascadePlan C;
-  st = make_cascade_plan(d, prefix_blocks, &C);
+  st = make_cascade_plan(d, prefix_blocks, &C, kvt);
   if (st != PKV_OK) return st;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < C.ws_bytes)
@@ -472,8 +478,8 @@ pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void
   const Plan& P = C.dec;
   const long long rows = (long long)d->num_blocks * d->num_kv_heads * d->block_size;
   CUtensorMap tmk, tmv;
-  if (!cache_map(&tmk, k_cache, false, d->head_dim, rows, d->block_size) ||
-      !cache_map(&tmv, v_cache, false, d->head_dim, rows, d->block_size))
+  if (!cache_map(&tmk, k_cache, q8, d->head_dim, rows, d->block_size) ||
+      !cache_map(&tmv, v_cache, q8, d->head_dim, rows, d->block_size))
     return PKV_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const float scale_log2 = scale * 1.4426950408889634f;
@@ -481,6 +487,8 @@ pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void
   // 1. the shared prefix, once per KV head for all B*g query rows
   PrefixParams pp{};
   pp.q = q;
+  pp.k_scale = k_scale;
+  pp.v_scale = v_scale;
   pp.prefix_ids = block_tables;  // row 0 holds the shared prefix
   pp.pre_o = reinterpret_cast<float*>(ws + C.off_pre_o);
   pp.pre_ml = reinterpret_cast<float*>(ws + C.off_pre_ml);
@@ -508,6 +516,8 @@ pkv_status run_cascade(void* out, const void* q, const void* k_cache, const void
   DecodeParams p{};
   p.q = q;
   p.out = out;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.part_o = reinterpret_cast<float*>(ws + C.off_o);
@@ -756,8 +766,33 @@ pkv_status pkv_decode_cascade_bf16(void* out, const void* q, const void* k_cache
                                    const int32_t* context_lens, int32_t prefix_blocks,
                                    float scale, const pkv_dims* dims, void* workspace,
                                    size_t workspace_bytes, int32_t* status, pkv_stream_t stream) {
-  return run_cascade(out, q, k_cache, v_cache, block_tables, context_lens, prefix_blocks, scale,
-                     dims, workspace, workspace_bytes, status,
+  return run_cascade(PKV_KV_BF16, out, q, k_cache, v_cache, nullptr, nullptr, block_tables,
+                     context_lens, prefix_blocks, scale, dims, workspace, workspace_bytes, status,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_decode_cascade_q8_workspace_bytes(const pkv_dims* dims, int32_t prefix_blocks,
+                                                 pkv_kv_dtype kv_dtype, size_t* bytes) {
+  if (!bytes) return PKV_ERR_NULL;
+  if (kv_dtype != PKV_KV_INT8 && kv_dtype != PKV_KV_FP8_E4M3 && kv_dtype != PKV_KV_FP8_E5M2)
+    return PKV_ERR_DTYPE;
+  CascadePlan C;
+  pkv_status st = make_cascade_plan(dims, prefix_blocks, &C, kv_dtype);
+  if (st != PKV_OK) return st;
+  *bytes = C.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_cascade_q8(void* out, const void* q, const void* k_cache,
+                                 const void* v_cache, const float* k_scale, const float* v_scale,
+                                 const int32_t* block_tables, const int32_t* context_lens,
+                                 int32_t prefix_blocks, float scale, pkv_kv_dtype kv_dtype,
+                                 const pkv_dims* dims, void* workspace, size_t workspace_bytes,
+                                 int32_t* status, pkv_stream_t stream) {
+  if (kv_dtype != PKV_KV_INT8 && kv_dtype != PKV_KV_FP8_E4M3 && kv_dtype != PKV_KV_FP8_E5M2)
+    return PKV_ERR_DTYPE;
+  return run_cascade(kv_dtype, out, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                     context_lens, prefix_blocks, scale, dims, workspace, workspace_bytes, status,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -12,6 +12,7 @@
 // through the ordinary decode kernel (skipping the prefix entries of the tables), and
 // paged_cascade_merge_kernel folds prefix and suffix partials with the online-softmax
 // rescaling. The result equals decode attention over the whole table.
+#include "convert.cuh"
 #include "decode.cuh"
 #include "fold.cuh"
 #include "tcgen05.cuh"
@@ -40,8 +41,12 @@ namespace pkv {
 // tiles x2 [D/64 slabs][128 tokens x 128 B], the ones tile (4 KiB), then the
 // mbarriers, the TMEM address word and the split's block ids. TMEM columns: S x2
 // [0, 256), O [256, 256 + D), P (bf16 pairs) [384, 448), l [448, 464).
+// One-byte caches (INT8 / FP8 codes with per-(token, KV head) scales): as in the
+// tcgen05 decode kernel, the producers land codes and scales, four converter warps
+// (7..10) widen K codes exactly to bf16 and V to fp16 code x scale (convert.cuh), the
+// softmax multiplies each score column by its K scale, and P.V runs on fp16 weights.
 // ---------------------------------------------------------------------------
-template <int D, int BS>
+template <int D, int BS, bool Q8 = false>
 struct PrefixTc {
   static constexpr int kM = 128;                      // query rows per CTA
   static constexpr int kN = 128;                      // prefix tokens per tile
@@ -55,15 +60,23 @@ struct PrefixTc {
   static constexpr int kOffV = kOffK + 2 * kTile;
   // all-ones B operand (16 x 128 tokens, K-major) of the MMA that sums the rows of P
   static constexpr int kOffOnes = kOffV + 2 * kTile;
-  static constexpr int kOffBar = kOffOnes + 4096;
+  // one-byte caches: codes in the last kCodeTile bytes of a tile's buffer; scales in kN
+  // fp32 slots, K scales of tile j in slot j % 4, V scales in slot 4 + j % 2
+  static constexpr int kCodeTile = kN * D;
+  static constexpr int kCodeOff = kTile - kCodeTile;
+  static constexpr int kScaleBytes = kN * 4;
+  static constexpr int kOffScales = kOffOnes + 4096;
+  static constexpr int kOffBar = kOffScales + (Q8 ? 6 * kScaleBytes : 0);
   // mbarriers: kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] pfull ofull mdone
-  static constexpr int kNumBars = 13;
+  // (+ one-byte caches: kstage[2] vstage[2] kscale[4])
+  static constexpr int kNumBars = Q8 ? 21 : 13;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kMaxIds = 2048;                // prefix blocks per split (planner cap)
   static constexpr int kOffIds = kOffAbort + 4;
   static constexpr int kSmem = kOffIds + 4 * kMaxIds + 1024;  // + slack for 1024-byte alignment
-  static constexpr int kThreads = 224;  // warps: 0 K copies, 1 MMA, 2..5 softmax, 6 V copies
+  // warps: 0 K copies, 1 MMA, 2..5 softmax, 6 V copies (+ 7..10 converters)
+  static constexpr int kThreads = Q8 ? 352 : 224;
   static constexpr uint32_t kTmemCols = 512;          // power of two
   // S x2, O, P (bf16 pairs), l (row sums of P, fp32; 16 columns written by its MMA)
   static constexpr int kColS = 0, kColO = 2 * kN, kColP = 2 * kN + 128, kColL = kColP + kN / 2;
@@ -75,11 +88,13 @@ struct PrefixTc {
   static_assert(kMaxIds % kBlocks == 0, "split cap in whole tiles");
 };
 
-template <int D, int BS>
-__global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
+// CODE: -1 for bf16 caches, else the one-byte code format.
+template <int D, int BS, int CODE = -1>
+__global__ void __launch_bounds__(PrefixTc<D, BS, (CODE >= 0)>::kThreads, 1)
     paged_prefix_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const PrefixParams pp) {
-  using K = PrefixTc<D, BS>;
+  constexpr bool kQ8 = CODE >= 0;
+  using K = PrefixTc<D, BS, kQ8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -98,6 +113,12 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
   auto vempty = [&](int st) { return bar(6 + st); };
   auto sfull = [&](int st) { return bar(8 + st); };
   const uint32_t pfull = bar(10), ofull = bar(11), mdone = bar(12);
+  auto kstage = [&](int st) { return bar(13 + st); };
+  auto vstage = [&](int st) { return bar(15 + st); };
+  auto kscale = [&](int j) { return bar(17 + (j & 3)); };
+  auto scale_area = [&](bool is_k, int j) {
+    return base + K::kOffScales + uint32_t(is_k ? (j & 3) : 4 + (j & 1)) * K::kScaleBytes;
+  };
   const uint32_t tmem_slot = base + K::kOffTmemSlot;
 
   pdl_wait_prior_grid();
@@ -109,13 +130,16 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
     mbar_init(pfull, 4 * 32);
     mbar_init(ofull, 1);
     mbar_init(mdone, 1);
+    if constexpr (kQ8)
+      for (int i = 13; i < 21; ++i) mbar_init(bar(i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, K::kTmemCols);
-  for (int k = tid; k < 4096 / 16; k += K::kThreads)  // bf16 1.0 everywhere
+  for (int k = tid; k < 4096 / 16; k += K::kThreads)  // 1.0 everywhere (bf16, or fp16)
     tc::sts128(base + K::kOffOnes + 16 * k,
-               make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u));
+               kQ8 ? make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u)
+                   : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u));
 
   // this split's physical block ids -> shared memory (the producer's copies then need
   // no dependent global load)
@@ -164,24 +188,40 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
     const uint32_t region = base + (is_k ? K::kOffK : K::kOffV);
     const int rows_total = pp.NB * pp.Hkv * BS;  // a box at this row is all zero fill
     int issued = 0;
+    // the barrier a tile's copies complete on: the tile itself (bf16), or the staged
+    // codes and scales the converters wait for (one-byte caches)
+    auto copy_bar = [&](int st) {
+      return kQ8 ? (is_k ? kstage(st) : vstage(st)) : (is_k ? kfull(st) : vfull(st));
+    };
     for (int j = 0; j < ntiles; ++j) {
       const int st = j & 1;
-      const uint32_t fb = is_k ? kfull(st) : vfull(st);
+      const uint32_t fb = copy_bar(st);
       if (j >= 2 &&
           !__all_sync(0xffffffffu, tc::wait_or_abort(is_k ? kempty(st) : vempty(st),
                                                uint32_t((j >> 1) - 1) & 1u, pp.timeout_ns,
                                                abort_flag)))
         break;
-      if (lane == 0) mbar_arrive_expect_tx(fb, K::kTile);
+      if (lane == 0) mbar_arrive_expect_tx(fb, kQ8 ? K::kCodeTile + K::kScaleBytes : K::kTile);
       __syncwarp();
+      int row = rows_total;
       if (lane < K::kBlocks) {
         const int i = j * K::kBlocks + lane;  // block of the split
-        int row = rows_total;
         if (i < nb) {
           int phys = s_ids[i];
           phys = (phys < 0 || phys >= pp.NB) ? 0 : phys;  // never copy outside the pool
           row = (phys * pp.Hkv + h) * BS;
         }
+      }
+      if constexpr (kQ8) {
+        // a block past the split copies zero-filled codes and block 0's scales
+        const int row0 = __shfl_sync(0xffffffffu, row, 0);
+        if (lane < K::kBlocks) {
+          tma_load_2d(region + st * K::kTile + K::kCodeOff + lane * BS * D, map, fb, 0, row);
+          bulk_load(scale_area(is_k, j) + lane * BS * 4,
+                    (is_k ? pp.k_scale : pp.v_scale) + size_t(row == rows_total ? row0 : row),
+                    BS * 4, fb);
+        }
+      } else if (lane < K::kBlocks) {
         const uint32_t dst = region + st * K::kTile + lane * BS * 128;
 #pragma unroll
         for (int sl = 0; sl < K::kSlabs; ++sl)
@@ -192,15 +232,17 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
     // every copy issued must have landed before the CTA may exit
     if (lane == 0)
       for (int j = max(0, issued - 2); j < issued; ++j)
-        mbar_wait_bounded(is_k ? kfull(j & 1) : vfull(j & 1), uint32_t(j >> 1) & 1u,
-                          pp.timeout_ns);
+        mbar_wait_bounded(copy_bar(j & 1), uint32_t(j >> 1) & 1u, pp.timeout_ns);
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_bf16<128, K::kN, false>();
-      constexpr uint32_t kIdO = tc::idesc_bf16<128, D, true>();
-      constexpr uint32_t kIdL = tc::idesc_bf16<128, 16, false>();
+      // P.V and the row sums run on fp16 weights and values for one-byte caches
+      constexpr uint32_t kIdO =
+          kQ8 ? tc::idesc_f16<128, D, true>() : tc::idesc_bf16<128, D, true>();
+      constexpr uint32_t kIdL =
+          kQ8 ? tc::idesc_f16<128, 16, false>() : tc::idesc_bf16<128, 16, false>();
       const uint32_t ones = base + K::kOffOnes;
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
@@ -253,7 +295,7 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
       mbar_wait_bounded(mdone, 0u, pp.timeout_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ---------------- softmax warps (2..5): one query row per thread ----------------
     const int quarter = warp & 3;  // warps 2, 3, 4, 5 own TMEM lanes 64.., 96.., 0.., 32..
     const int r = quarter * 32 + lane;
@@ -272,6 +314,22 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
       tc::fence_after_sync();
       uint32_t s[K::kN];
       tc::tmem_ld128(trow + K::kColS + st * K::kN, s);
+      if constexpr (kQ8) {  // one-byte caches: each column times its K scale
+        if (!__all_sync(0xffffffffu, tc::wait_or_abort(kscale(j), uint32_t(j >> 2) & 1u,
+                                                       pp.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const uint32_t ks = scale_area(true, j);
+#pragma unroll
+        for (int t = 0; t < K::kN; t += 4) {
+          const uint4 k4 = lds128(ks + 4 * t);  // the same address in every lane
+          s[t] = __float_as_uint(__uint_as_float(s[t]) * __uint_as_float(k4.x));
+          s[t + 1] = __float_as_uint(__uint_as_float(s[t + 1]) * __uint_as_float(k4.y));
+          s[t + 2] = __float_as_uint(__uint_as_float(s[t + 2]) * __uint_as_float(k4.z));
+          s[t + 3] = __float_as_uint(__uint_as_float(s[t + 3]) * __uint_as_float(k4.w));
+        }
+      }
       // scores of masked columns (past the split, zero-filled K) never count; a
       // negative scale is carried by flipping the scores' signs (warp-uniform branches,
       // taken only on a split's last tile or with scale < 0)
@@ -311,15 +369,17 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
         for (int t = 0; t < K::kN; t += 2) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
                                       asl2, nm2);
-          pk[t / 2] = pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
+          pk[t / 2] = kQ8 ? pack_f16x2(fast_exp2(x.x), fast_exp2(x.y))
+                          : pack_bf16x2(fast_exp2(x.x), fast_exp2(x.y));
         }
       } else {
 #pragma unroll
         for (int t = 0; t < K::kN; t += 2) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
                                       asl2, nm2);
-          pk[t / 2] =
-              pack_bf16x2(t < valid ? fast_exp2(x.x) : 0.f, t + 1 < valid ? fast_exp2(x.y) : 0.f);
+          const float w0 = t < valid ? fast_exp2(x.x) : 0.f;
+          const float w1 = t + 1 < valid ? fast_exp2(x.y) : 0.f;
+          pk[t / 2] = kQ8 ? pack_f16x2(w0, w1) : pack_bf16x2(w0, w1);
         }
       }
       // P.V of the previous tile must be complete before P is overwritten or O rescaled
@@ -381,6 +441,45 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
       reinterpret_cast<float2*>(pp.pre_ml)[rec] =
           (ok && ntiles > 0) ? make_float2(m_ref, l) : make_float2(-INFINITY, 0.f);
     tc::fence_before_sync();
+  } else if (kQ8) {
+    // ---------------- converters (7..10): one-byte codes -> 16-bit values ----------------
+    const int ct = tid - 7 * 32;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j & 1;
+      const uint32_t par = uint32_t(j >> 1) & 1u;
+      const int valid = min(K::kBlocks, nb - j * K::kBlocks) * BS;  // tokens of the split
+      bool go = true;
+      for (int kv = 0; kv < 2; ++kv) {
+        // every converter takes part in every barrier: they agree on going on first
+        const bool landed = __all_sync(
+            0xffffffffu,
+            tc::wait_or_abort(kv == 0 ? kstage(st) : vstage(st), par, pp.timeout_ns, abort_flag));
+        if (!converters_all(landed)) {
+          go = false;
+          break;
+        }
+        // K: the codes themselves as bf16 (exact; the softmax applies the K scales);
+        // V: code x scale as fp16
+        if constexpr (kQ8) {
+          const uint32_t tile = base + (kv == 0 ? K::kOffK : K::kOffV) + st * K::kTile;
+          if (kv == 0) {
+            convert_codes<D, (kQ8 ? CODE : 0), false, false>(tile, scale_area(true, j), valid,
+                                                             ct);
+            if (ct >= valid) tc::sts32(scale_area(true, j) + 4 * ct, 0u);
+          } else {
+            convert_codes<D, (kQ8 ? CODE : 0), true, true>(tile, scale_area(false, j), valid,
+                                                           ct);
+          }
+        }
+        fence_proxy_async_smem();  // the 16-bit values, for the MMAs (async proxy)
+        converters_sync();
+        if (ct == 0) {
+          mbar_arrive(kv == 0 ? kfull(st) : vfull(st));
+          if (kv == 0) mbar_arrive(kscale(j));
+        }
+      }
+      if (!go) break;
+    }
   }
   __syncthreads();
   if (*abort_flag && tid == 0 && pp.status) atomicOr(pp.status, 0x4);
@@ -391,10 +490,10 @@ __global__ void __launch_bounds__(PrefixTc<D, BS>::kThreads, 1)
   }
 }
 
-template <int D, int BS>
+template <int D, int BS, int CODE>
 void prefix_info(PrefixKernelInfo* info) {
-  using K = PrefixTc<D, BS>;
-  info->fn = reinterpret_cast<const void*>(&paged_prefix_kernel<D, BS>);
+  using K = PrefixTc<D, BS, (CODE >= 0)>;
+  info->fn = reinterpret_cast<const void*>(&paged_prefix_kernel<D, BS, CODE>);
   info->smem = K::kSmem;
   info->threads = K::kThreads;
   info->rows = K::kM;
@@ -402,13 +501,24 @@ void prefix_info(PrefixKernelInfo* info) {
   info->max_split_blocks = K::kMaxIds;
 }
 
-bool select_prefix_kernel(int D, int BS, PrefixKernelInfo* info) {
-  if (D == 128 && BS == 16) prefix_info<128, 16>(info);
-  else if (D == 128 && BS == 32) prefix_info<128, 32>(info);
-  else if (D == 64 && BS == 16) prefix_info<64, 16>(info);
-  else if (D == 64 && BS == 32) prefix_info<64, 32>(info);
+template <int CODE>
+bool select_prefix_code(int D, int BS, PrefixKernelInfo* info) {
+  if (D == 128 && BS == 16) prefix_info<128, 16, CODE>(info);
+  else if (D == 128 && BS == 32) prefix_info<128, 32, CODE>(info);
+  else if (D == 64 && BS == 16) prefix_info<64, 16, CODE>(info);
+  else if (D == 64 && BS == 32) prefix_info<64, 32, CODE>(info);
   else return false;
   return true;
+}
+
+bool select_prefix_kernel(int D, int BS, int kvt, PrefixKernelInfo* info) {
+  switch (kvt) {
+    case PKV_KV_BF16: return select_prefix_code<-1>(D, BS, info);
+    case PKV_KV_INT8: return select_prefix_code<CODE_I8>(D, BS, info);
+    case PKV_KV_FP8_E4M3: return select_prefix_code<CODE_E4M3>(D, BS, info);
+    case PKV_KV_FP8_E5M2: return select_prefix_code<CODE_E5M2>(D, BS, info);
+    default: return false;
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -47,6 +47,8 @@ struct DecodeParams {
 // (sequence s, group member i) attend the prefix blocks block_tables[0, 0..P-1].
 struct PrefixParams {
   const void* q;               // [B, Hq, D] bf16
+  const float* k_scale;        // [NB, Hkv, BS] fp32 (one-byte caches only)
+  const float* v_scale;
   const int32_t* prefix_ids;   // [P] physical ids of the shared prefix (row 0 of the tables)
   float* pre_o;                // [nsplit, Hkv, R, D] unnormalised partial outputs
   float* pre_ml;               // [nsplit, Hkv, R, 2] (running max in log2 units, sum)
@@ -84,7 +86,7 @@ struct PrefixKernelInfo {
   int tile_blocks;   // prefix blocks per tile (splits are cut at tile boundaries)
   int max_split_blocks;  // most prefix blocks one split may hold (a multiple of tile_blocks)
 };
-bool select_prefix_kernel(int D, int BS, PrefixKernelInfo* info);
+bool select_prefix_kernel(int D, int BS, int kvt, PrefixKernelInfo* info);
 void launch_cascade_merge(const CascadeMergeParams& p, cudaStream_t stream);
 
 // Parameters of the split-KV merge launch (units cut between decode workers).

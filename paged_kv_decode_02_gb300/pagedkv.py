@@ -113,6 +113,16 @@ EXPORTS = {
                                                                    ctypes.c_size_t,
                                                                    ctypes.c_void_p,
                                                                    ctypes.c_void_p]),
+    "pkv_decode_cascade_q8_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
+                                                             ctypes.c_int,
+                                                             ctypes.POINTER(ctypes.c_size_t)]),
+    "pkv_decode_cascade_q8": (ctypes.c_int, [ctypes.c_void_p] * 8 + [ctypes.c_int32,
+                                                                     ctypes.c_float, ctypes.c_int,
+                                                                     ctypes.c_void_p,
+                                                                     ctypes.c_void_p,
+                                                                     ctypes.c_size_t,
+                                                                     ctypes.c_void_p,
+                                                                     ctypes.c_void_p]),
     "pkv_decode_cascade_workspace_bytes": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32,
                                                           ctypes.POINTER(ctypes.c_size_t)]),
     "pkv_decode_cascade_bf16": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int32,
@@ -490,6 +500,66 @@ def _host_buffers(kv, n, block, scale_block, host_k, host_v, host_k_scale, host_
         if t.numel() * t.element_size() < n * per_block:
             raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, "
                              f"{n} blocks need {n * per_block}")
+
+
+def cascade_q8_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                               num_blocks, max_blocks_per_seq, prefix_blocks, kv_dtype,
+                               device=None):
+    """Workspace of :func:`paged_decode_attention_cascade_q8` (kv_dtype KV_INT8,
+    KV_FP8_E4M3 or KV_FP8_E5M2)."""
+    dims = Dims(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                max_blocks_per_seq)
+    out = ctypes.c_size_t(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = _lib().pkv_decode_cascade_q8_workspace_bytes(ctypes.byref(dims), int(prefix_blocks),
+                                                          int(kv_dtype), ctypes.byref(out))
+    _check(st, "pkv_decode_cascade_q8_workspace_bytes")
+    return int(out.value)
+
+
+def paged_decode_attention_cascade_q8(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                      context_lens, prefix_blocks, scale, fmt="e5m2", out=None,
+                                      workspace=None, status=None):
+    """:func:`paged_decode_attention_cascade` over a one-byte cache: int8 codes (INT8),
+    or FP8 codes (uint8 with ``fmt`` "e4m3" / "e5m2", or the matching torch float8
+    dtype), with per-(token, KV head) fp32 scales ``k_scale``/``v_scale`` [NB, Hkv, bs].
+    Same result as :func:`paged_decode_attention_int8` / :func:`paged_decode_attention_fp8`."""
+    dev = q.device
+    status = _status_word(status, dev)
+    kv = _q8_kind(k_cache, fmt)
+    _require(q, "q", torch.bfloat16, 3, dev)
+    _require_any(k_cache, "k_cache", _code_dtypes(kv), 4, dev)
+    _require_any(v_cache, "v_cache", _code_dtypes(kv), 4, dev)
+    _require(k_scale, "k_scale", torch.float32, 3, dev)
+    _require(v_scale, "v_scale", torch.float32, 3, dev)
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    B, Hq, D = q.shape
+    if k_cache.shape != v_cache.shape or k_cache.shape[3] != D:
+        raise ValueError("cache shapes disagree with q")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    _cache_shapes(k_cache, v_cache, k_scale, v_scale)
+    dims = _dims(B, Hq, k_cache, block_tables.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _require(out, "out", torch.bfloat16, 3, dev)
+        _same_shape(out, "out", q.shape)
+    with _OnDevice(dev):
+        need = ctypes.c_size_t(0)
+        _check(_lib().pkv_decode_cascade_q8_workspace_bytes(ctypes.byref(dims),
+                                                            int(prefix_blocks), kv,
+                                                            ctypes.byref(need)),
+               "pkv_decode_cascade_q8_workspace_bytes")
+        workspace, ws_bytes = _workspace(workspace, need.value, dev)
+        st = _lib().pkv_decode_cascade_q8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(k_scale), _ptr(v_scale), _ptr(block_tables),
+                                          _ptr(context_lens), int(prefix_blocks), float(scale),
+                                          kv, ctypes.byref(dims), _ptr(workspace), ws_bytes,
+                                          _ptr(status), _stream(dev))
+    _check(st, "pkv_decode_cascade_q8")
+    return out
 
 
 def copy_blocks(k_cache, v_cache, src_ids, dst_ids, k_scale=None, v_scale=None, status=None,

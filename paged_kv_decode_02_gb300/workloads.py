@@ -40,6 +40,9 @@ Workload recipes (names are the shapes they model):
   request (k = 5 drafted tokens plus the next position, the number of speculative
   tokens in the vLLM example of "推测解码", chenk.top page), for multi-query decode.
   ``spec-70b-q16``: the same with q_len = 16 (128 query rows per KV head).
+* ``prefix-int8`` / ``prefix-e5m2`` and ``spec-70b-int8`` / ``spec-70b-e4m3``: the
+  ``prefix`` and ``spec-70b`` shapes and lengths over one-byte caches, codes and scales
+  drawn as for ``int8`` / ``fp8-*``.
 * ``chunk-70b``: a chunk of chunked prefill ("Orca 的迭代级调度", chenk.top page) on the
   ``70b-gqa`` shape: 16 requests whose last 256 tokens are the chunk being prefilled
   (q_len = 256, 2048 query rows per KV head), lengths log-normal (median 1024, sigma 1)
@@ -218,6 +221,11 @@ SPECS = {
     "spec-70b":  dict(B=64,  Hq=64, Hkv=8,  D=128, bs=16, seed=2, q_len=6),
     "spec-70b-q16": dict(B=64, Hq=64, Hkv=8, D=128, bs=16, seed=2, q_len=16),
     "chunk-70b": dict(B=16, Hq=64, Hkv=8, D=128, bs=16, seed=5, q_len=256),
+    # one-byte caches under the same shapes (codes and scales drawn as for int8 / fp8-*)
+    "prefix-int8": dict(B=256, Hq=32, Hkv=8, D=128, bs=16, seed=3),
+    "prefix-e5m2": dict(B=256, Hq=32, Hkv=8, D=128, bs=16, seed=3),
+    "spec-70b-int8": dict(B=64, Hq=64, Hkv=8, D=128, bs=16, seed=2, q_len=6),
+    "spec-70b-e4m3": dict(B=64, Hq=64, Hkv=8, D=128, bs=16, seed=2, q_len=6),
 }
 
 FP8_KV = {"fp8_e4m3": (torch.float8_e4m3fn, 448.0), "fp8_e5m2": (torch.float8_e5m2, 57344.0)}
@@ -228,11 +236,11 @@ def _draw_lengths(name, rng, B):
         return rng.integers(1, 65, size=B).astype(np.int64)
     if name == "7b":
         return np.full(B, 2048, dtype=np.int64)
-    if name in ("70b-gqa", "spec-70b", "spec-70b-q16"):
+    if name in ("70b-gqa", "spec-70b", "spec-70b-q16", "spec-70b-int8", "spec-70b-e4m3"):
         return _lognormal_lengths(rng, B, 1024, 1.0, 128, 32768)
     if name == "chunk-70b":
         return _lognormal_lengths(rng, B, 1024, 1.0, 256, 32768)
-    if name == "prefix":
+    if name in ("prefix", "prefix-int8", "prefix-e5m2"):
         return 2048 + rng.integers(16, 513, size=B).astype(np.int64)
     if name.startswith("int8") or name.startswith("fp8"):
         return np.full(B, 8192, dtype=np.int64)
@@ -309,8 +317,9 @@ def make_workload(name: str, device="cpu", seed: Optional[int] = None,
     D = head_dim or spec["D"]
     bs = block_size or spec["bs"]
     n_new = int(q_len if q_len is not None else spec.get("q_len", 1))
-    kvt = kv_dtype or ("int8" if name.startswith("int8") else
-                       "fp8_" + name[4:] if name.startswith("fp8-") else "bf16")
+    kvt = kv_dtype or ("int8" if name.startswith("int8") or name.endswith("-int8") else
+                       "fp8_" + name[4:] if name.startswith("fp8-") else
+                       "fp8_" + name[-4:] if name.endswith(("-e4m3", "-e5m2")) else "bf16")
     rng = np.random.default_rng(seed)
     if lengths is None:
         lengths = _draw_lengths(name, rng, B)
@@ -318,7 +327,8 @@ def make_workload(name: str, device="cpu", seed: Optional[int] = None,
     B = len(lengths)
     if name == "tiny" and num_blocks is None:
         num_blocks = 64
-    prefix = (2048 if name == "prefix" else 0) if prefix_tokens is None else int(prefix_tokens)
+    prefix = (2048 if name.startswith("prefix") else 0) if prefix_tokens is None \
+        else int(prefix_tokens)
     tables, last_slots, NB, alloc = build_tables(lengths, bs, rng, num_blocks=num_blocks,
                                                  shared_prefix_tokens=prefix)
     dev = torch.device(device)

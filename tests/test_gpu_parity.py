@@ -485,6 +485,57 @@ def test_cascade_full_prefix_workload(pk):
     assert max_err(out, ref) <= DECODE_ATOL
 
 
+def _cascade_q8(pk, w, prefix_blocks, **kw):
+    return pk.paged_decode_attention_cascade_q8(
+        w.q, w.k_cache, w.v_cache, w.k_scale, w.v_scale, w.block_tables, w.context_lens,
+        prefix_blocks, w.scale, fmt=w.kv_dtype[4:] if w.kv_dtype != "int8" else "e5m2", **kw)
+
+
+CASCADE_Q8 = [
+    # (id, B, Hq, Hkv, D, bs, prefix tokens, suffix lengths)
+    ("g4-bs16", 6, 16, 4, 128, 16, 256, [0, 5, 16, 17, 100, 300]),
+    ("g8-bs32-d64", 5, 16, 2, 64, 32, 320, [1, 31, 64, 200, 0]),
+    ("g1-bs16", 4, 4, 4, 128, 16, 144, [7, 0, 60, 129]),
+]
+
+
+@pytest.mark.parametrize("kvt", ["int8", "fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("case", CASCADE_Q8, ids=[c[0] for c in CASCADE_Q8])
+def test_cascade_q8_small_shapes(pk, case, kvt):
+    """Shared-prefix decode over one-byte caches: whole outputs against the oracle, with
+    and without a status word (the latter validates the tables)."""
+    _, B, Hq, Hkv, D, bs, pre, suf = case
+    w = make_workload("prefix", device=DEV, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                      block_size=bs, lengths=[pre + x for x in suf], prefix_tokens=pre,
+                      kv_dtype=kvt, seed=41, poison_unused=True)
+    out = _cascade_q8(pk, w, pre // bs)
+    torch.cuda.synchronize()
+    ref = oracle_outputs(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out2 = _cascade_q8(pk, w, pre // bs, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert max_err(out2, ref) <= DECODE_ATOL
+
+
+@pytest.mark.parametrize("kvt", ["int8", "fp8_e5m2"])
+def test_cascade_q8_full_prefix_workload(pk, kvt):
+    """The prefix workload over a one-byte cache: quantise-append the step's tokens, then
+    the cascade decode; every output row against the oracle (all host cores)."""
+    w = make_workload("prefix", device=DEV, kv_dtype=kvt)
+    if kvt == "int8":
+        pk.paged_kv_append_int8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                w.slot_mapping)
+    else:
+        pk.paged_kv_append_fp8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                               w.slot_mapping, fmt=kvt[4:])
+    out = _cascade_q8(pk, w, 2048 // w.block_size)
+    torch.cuda.synchronize()
+    ref = oracle_outputs_all(w)
+    assert max_err(out, ref) <= DECODE_ATOL
+
+
 def test_cascade_flags_a_table_without_the_prefix(pk):
     pre, bs = 64, 16
     w = make_workload("prefix", device=DEV, num_q_heads=16, num_kv_heads=4, head_dim=128,

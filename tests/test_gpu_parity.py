@@ -351,13 +351,23 @@ def test_decode_full_size_sampled(pk, name):
     assert max_err(out, ref, pairs) <= DECODE_ATOL
 
 
-@pytest.mark.parametrize("name", ["70b-gqa", "7b"])
+@pytest.mark.parametrize("name", ["70b-gqa", "7b", "prefix", "int8", "int8-bs16", "fp8-e5m2",
+                                  "fp8-e4m3"])
 def test_decode_full_size_whole_output(pk, name):
-    """Every output row of a full-size workload against the oracle (run on all host
-    cores): 70b-gqa has cut units everywhere (470 of its 512 (sequence, KV head) units
-    are split over several workers and merged), 7b folds its parts inside the kernel."""
+    """Every output row of a full-size workload, after the step's append, against the
+    oracle (run on all host cores): 70b-gqa has cut units everywhere (470 of its 512
+    (sequence, KV head) units are split over several workers and merged), 7b folds its
+    parts inside the kernel, prefix reads its shared blocks from every table, the one-byte
+    workloads quantise their new tokens on append."""
     w = make_workload(name, device=DEV)
-    pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
+    if w.kv_dtype == "bf16":
+        pk.paged_kv_append(w.new_k, w.new_v, w.k_cache, w.v_cache, w.slot_mapping)
+    elif w.kv_dtype.startswith("fp8_"):
+        pk.paged_kv_append_fp8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                               w.slot_mapping, fmt=w.kv_dtype[4:])
+    else:
+        pk.paged_kv_append_int8(w.new_k, w.new_v, w.k_cache, w.v_cache, w.k_scale, w.v_scale,
+                                w.slot_mapping)
     out = _decode(pk, w)
     torch.cuda.synchronize()
     ref = oracle_outputs_all(w)

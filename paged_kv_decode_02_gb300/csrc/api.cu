@@ -20,6 +20,9 @@ constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per shared-memo
 constexpr int kMaxQueryLen = PKV_MAX_QUERY_LEN;
 constexpr int kTcMinRows = 48;  // multi-query rows per KV head from which tcgen05 wins
 constexpr int kTcTileRows = 128;  // rows of one tcgen05 MMA (M): a KV head's row tile
+// at most this many rows per KV head: two softmax threads per row (each lane quarter holds
+// 16 rows twice), so that the exponentials of a tile spread over all four SM sub-partitions
+constexpr int kTcSplitRows = 64;
 // tcgen05 kernel: the cost of ending a KV head (its partly filled last tile, the
 // epilogue, the next head's first scores) in tiles; ranges are balanced on tiles plus
 // this much per head. A sweep of whole calls on GB300 (48 and 128 query rows per KV
@@ -215,7 +218,8 @@ pkv_status make_plan_uncached(const pkv_dims* d, int kvt, int q_len, bool pair, 
     // the tcgen05 kernel for every row count (it widens the codes to bf16 in shared
     // memory; the mma.sync multi-query path reads bf16 caches only).
     if ((rows >= kTcMinRows || kvt != PKV_KV_BF16) &&
-        select_decode_tc(d->head_dim, d->block_size, rows > kTcTileRows, kvt, &P.k)) {
+        select_decode_tc(d->head_dim, d->block_size, rows > kTcTileRows, rows <= kTcSplitRows,
+                         kvt, &P.k)) {
       P.nsg = (rows + kTcTileRows - 1) / kTcTileRows;
       P.gs = (rows + P.nsg - 1) / P.nsg;
       P.HU = d->num_kv_heads * P.nsg;
@@ -362,7 +366,9 @@ pkv_status run_decode(int kvt, void* out, const void* q, const void* k_cache,
   // swizzle atom of the staged rows)
   CUtensorMap tmo;
   std::memset(&tmo, 0, sizeof(tmo));
-  if (P.k.tc && (P.g == 8 || P.g == 16 || P.g == 32) && P.gs % P.g == 0 &&
+  // (a split tile stages 16 rows per lane quarter: g up to 16)
+  if (P.k.tc && (P.g == 8 || P.g == 16 || (P.g == 32 && P.gs > kTcSplitRows)) &&
+      P.gs % P.g == 0 &&
       cache_map(&tmo, out, false, d->head_dim,
                 (long long)d->num_seqs * q_len * d->num_q_heads, P.g))
     p.tma_out = 1;

@@ -34,7 +34,11 @@
 //                    weights P.V used and the softmax warps add nothing up;
 //   warps 2..5:      one query row per thread: Q rows of each segment into shared
 //                    memory, softmax with the causal and context masks, P to TMEM,
-//                    the segment's epilogue from O and l in TMEM.
+//                    the segment's epilogue from O and l in TMEM. A unit of at most 64
+//                    rows runs split (CS = 2): each lane quarter holds 16 rows twice and
+//                    the two threads of a row take half of each tile's columns, so the
+//                    exponentials spread over all four SM sub-partitions (measured on
+//                    GB300, spec-70b with 48 rows per head: 103.2 -> 97.2 us per call).
 // The softmax keeps a reference maximum per row that moves only when a tile's maximum
 // exceeds it by more than 8 (log2 units); O and l are then rescaled in TMEM before the
 // next P.V. Every wait is bounded: on a timeout the CTA sets a status bit, lets its
@@ -321,7 +325,7 @@ __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* 
 // instantiation keeps its own index arithmetic: measured on GB300, the general form
 // made the one-tile calls 17 % slower (spec-70b 102.4 -> 120.1 us) although it computes
 // the same values. CODE: -1 for bf16 caches, else the one-byte code format.
-template <int D, int BS, bool kTiles, int CODE = -1>
+template <int D, int BS, bool kTiles, int CODE = -1, int CS = 1>
 __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                            const __grid_constant__ CUtensorMap tmv,
@@ -601,9 +605,19 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     }
     __syncwarp();
   } else if (cnt > 0 && warp >= 2 && warp <= 5) {
-    // ---------------- softmax warps: one query row per thread ----------------
+    // ---------------- softmax warps: one query row per CS threads ----------------
+    // A warp reaches only its own quarter of the TMEM lanes, and the exponentials of a
+    // lane quarter run on one SM sub-partition. With CS = 2 (at most 64 rows) each
+    // quarter holds 16 rows, each twice (A rows 32q + j and 32q + 16 + j carry the same
+    // Q row): the two threads of a row take half of the tile's columns each, their P rows
+    // are zero outside their half and their O and l rows add up to the row's.
+    static_assert(CS == 1 || (CS == 2 && !kTiles), "split rows: one row tile only");
+    constexpr int kRpq = 32 / CS;       // query rows per lane quarter
+    constexpr int kNc = K::kN / CS;     // tile columns per thread
     const int quarter = warp & 3;  // warps 2, 3, 4, 5 own TMEM lanes 64.., 96.., 0.., 32..
-    const int r = quarter * 32 + lane;
+    const int part = CS == 1 ? 0 : lane / kRpq;  // which kNc columns of the row it takes
+    const int r = quarter * kRpq + lane % kRpq;  // query row of the unit
+    const int ar = quarter * 32 + lane;          // A row / TMEM lane of this thread
     const uint32_t trow = tmem + (uint32_t(quarter * 32) << 16);
     const float sl = p.scale_log2, asl = fabsf(sl);
     // this thread's query row of unit u: row (u % nsg) * R + r of its KV head (new
@@ -645,7 +659,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
       const uint32_t qa = base + K::kOffQ + qb * K::kTile;
 #pragma unroll
       for (int cc = 0; cc < kChunks; ++cc)
-        cp_async16(qa + (cc >> 3) * K::kSlab + r * 128 + (((cc & 7) ^ (r & 7)) << 4),
+        cp_async16(qa + (cc >> 3) * K::kSlab + ar * 128 + (((cc & 7) ^ (ar & 7)) << 4),
                    q + qrow * kChunks + cc, ex ? 16u : 0u);
       cp_async_commit();
     };
@@ -656,7 +670,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     };
     // a warp whose 32 rows are all padding computes nothing: its P and O rows feed
     // output rows that are never stored
-    const bool warp_idle = quarter * 32 >= R;
+    const bool warp_idle = quarter * kRpq >= R;
     // rows of a head's last block past its context may hold anything (even NaN): the
     // four softmax warps zero them in the V tile before P.V reads it (weights there are 0)
     auto zero_v_tail = [&](int i, int L, int t0) -> bool {
@@ -734,18 +748,27 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         tile_next(cur, s_prefix, B, U);
         continue;
       }
-      uint32_t s[K::kN];
-      tc::tmem_ld128(trow + K::kColS + st * K::kN, s);
+      // this thread's columns c0 .. c0 + kNc - 1 of the tile's scores
+      const int c0 = part * kNc;
+      uint32_t s[kNc];
+      if constexpr (CS == 1) {
+        tc::tmem_ld128(trow + K::kColS + st * K::kN, s);
+      } else {
+        uint32_t sa[K::kN];
+        tc::tmem_ld128(trow + K::kColS + st * K::kN, sa);
+#pragma unroll
+        for (int t = 0; t < kNc; ++t) s[t] = part == 0 ? sa[t] : sa[t + kNc];
+      }
       if constexpr (kQ8) {  // one-byte caches: each column times its K scale
         if (!__all_sync(0xffffffffu, tc::wait_or_abort(kscale(i), uint32_t(i >> 2) & 1u,
                                                        p.timeout_ns, abort_flag))) {
           ok = false;
           break;
         }
-        const uint32_t ks = scale_area(true, i);
+        const uint32_t ks = scale_area(true, i) + 4 * c0;
 #pragma unroll
-        for (int t = 0; t < K::kN; t += 4) {
-          const uint4 k4 = lds128(ks + 4 * t);  // the same address in every lane
+        for (int t = 0; t < kNc; t += 4) {
+          const uint4 k4 = lds128(ks + 4 * t);  // the same address in the lanes of a part
           s[t] = __float_as_uint(__uint_as_float(s[t]) * __uint_as_float(k4.x));
           s[t + 1] = __float_as_uint(__uint_as_float(s[t + 1]) * __uint_as_float(k4.y));
           s[t + 2] = __float_as_uint(__uint_as_float(s[t + 2]) * __uint_as_float(k4.z));
@@ -754,25 +777,27 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
       }
       if (sl < 0.f) {  // a negative scale is carried by the scores' signs
 #pragma unroll
-        for (int t = 0; t < K::kN; ++t) s[t] ^= 0x80000000u;
+        for (int t = 0; t < kNc; ++t) s[t] ^= 0x80000000u;
       }
       // warp-uniform: every row sees the whole tile (all tiles but a head's last, and
       // the last ones of causal rows), else columns past each row's limit are masked
       const bool full = __all_sync(0xffffffffu, vis >= K::kN);
       if (!full) {
 #pragma unroll
-        for (int t = 0; t < K::kN; ++t)
-          if (t >= vis) s[t] = 0xff800000u;  // -inf
+        for (int t = 0; t < kNc; ++t)
+          if (c0 + t >= vis) s[t] = 0xff800000u;  // -inf
       }
-      // tile maximum: three-input max over eight independent chains
+      // tile maximum: three-input max over eight independent chains (then over the
+      // row's CS threads)
       float mx[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) mx[j] = __uint_as_float(s[j]);
 #pragma unroll
-      for (int u = 0; u < (K::kN - 8) / 2; ++u)
+      for (int u = 0; u < (kNc - 8) / 2; ++u)
         mx[u & 7] = fmax3(mx[u & 7], __uint_as_float(s[8 + 2 * u]), __uint_as_float(s[9 + 2 * u]));
-      const float mt = asl * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                   fmaxf(mx[6], mx[7]));
+      float mt = asl * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7]));
+      if constexpr (CS == 2) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, kRpq));
       float alpha = 1.f;
       bool rescale = false;
       if (vis > 0 && mt > m_ref + 8.f) {
@@ -783,11 +808,11 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
       // weights 2^(scale * s - m) (packed fp32x2 FMAs), bf16 pairs (fp16 over one-byte
       // caches); their row sums come from the tensor cores (P times a ones tile, beside
       // P.V)
-      uint32_t pk[K::kN / 2];
+      uint32_t pk[kNc / 2];
       const float2 asl2 = make_float2(asl, asl), nm2 = make_float2(-m_ref, -m_ref);
       if (full) {
 #pragma unroll
-        for (int t = 0; t < K::kN; t += 2) {
+        for (int t = 0; t < kNc; t += 2) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
                                       asl2, nm2);
           pk[t / 2] = kQ8 ? pack_f16x2(fast_exp2(x.x), fast_exp2(x.y))
@@ -795,10 +820,11 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         }
       } else {
 #pragma unroll
-        for (int t = 0; t < K::kN; t += 2) {
+        for (int t = 0; t < kNc; t += 2) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
                                       asl2, nm2);
-          const float w0 = t < vis ? fast_exp2(x.x) : 0.f, w1 = t + 1 < vis ? fast_exp2(x.y) : 0.f;
+          const float w0 = c0 + t < vis ? fast_exp2(x.x) : 0.f,
+                      w1 = c0 + t + 1 < vis ? fast_exp2(x.y) : 0.f;
           pk[t / 2] = kQ8 ? pack_f16x2(w0, w1) : pack_bf16x2(w0, w1);
         }
       }
@@ -825,11 +851,14 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         tc::tmem_st1(trow + K::kColL,
                      __float_as_uint(__uint_as_float(tc::tmem_ld1(trow + K::kColL)) * alpha));
       }
+      // P (column pairs); with CS = 2 each thread writes its half and zeros in the other
 #pragma unroll
       for (int c2 = 0; c2 < K::kN / 2; c2 += 32) {
         uint32_t w[32];
+        constexpr int kHalf = kNc / 2;  // column pairs per thread
 #pragma unroll
-        for (int e = 0; e < 32; ++e) w[e] = pk[c2 + e];
+        for (int e = 0; e < 32; ++e)
+          w[e] = (CS == 1 || part == c2 / kHalf) ? pk[c2 % kHalf + e] : 0u;
         tc::tmem_st32(trow + K::kColP + c2, w);
       }
       tc::fence_before_sync();
@@ -848,7 +877,9 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         tc::fence_after_sync();
         const bool whole = seg_j0 == 0 && cur.j == cur.n - 1;
         const size_t slot = size_t(2 * c + (seg == 0 ? 0 : 1));
-        const float l = __uint_as_float(tc::tmem_ld1(trow + K::kColL));  // sum of the weights
+        // the sum of the weights (over the row's CS threads)
+        const float l1 = __uint_as_float(tc::tmem_ld1(trow + K::kColL));
+        const float l = CS == 1 ? l1 : l1 + __shfl_xor_sync(0xffffffffu, l1, kRpq);
         const float inv = l > 0.f ? 1.f / l : 0.f;
         if (whole) {
           // the bf16 rows go through this segment's Q buffer (its MMAs are complete),
@@ -866,22 +897,31 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
           for (int c2 = 0; c2 < D; c2 += 32) {
             uint32_t o[32];
             tc::tmem_ld32(trow + K::kColO + c2, o);
+            if constexpr (CS == 2) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8)
-              tc::sts128(slot_addr(r, (c2 + e) / 8),
-                         make_uint4(pack_bf16x2(__uint_as_float(o[e]) * inv,
-                                                __uint_as_float(o[e + 1]) * inv),
-                                    pack_bf16x2(__uint_as_float(o[e + 2]) * inv,
-                                                __uint_as_float(o[e + 3]) * inv),
-                                    pack_bf16x2(__uint_as_float(o[e + 4]) * inv,
-                                                __uint_as_float(o[e + 5]) * inv),
-                                    pack_bf16x2(__uint_as_float(o[e + 6]) * inv,
-                                                __uint_as_float(o[e + 7]) * inv)));
+              for (int e = 0; e < 32; ++e)
+                o[e] = __float_as_uint(__uint_as_float(o[e]) +
+                                       __uint_as_float(__shfl_xor_sync(0xffffffffu, o[e], kRpq)));
+            }
+            if (part == 0) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 8)
+                tc::sts128(slot_addr(ar, (c2 + e) / 8),
+                           make_uint4(pack_bf16x2(__uint_as_float(o[e]) * inv,
+                                                  __uint_as_float(o[e + 1]) * inv),
+                                      pack_bf16x2(__uint_as_float(o[e + 2]) * inv,
+                                                  __uint_as_float(o[e + 3]) * inv),
+                                      pack_bf16x2(__uint_as_float(o[e + 4]) * inv,
+                                                  __uint_as_float(o[e + 5]) * inv),
+                                      pack_bf16x2(__uint_as_float(o[e + 6]) * inv,
+                                                  __uint_as_float(o[e + 7]) * inv)));
+            }
           }
           if (p.tma_out) {
-            // one TMA box per new token (its g rows) and 64-column slab; g divides 32
-            // and the row tile (gs) starts on a token, so a token's rows belong to this
-            // warp and its box starts on an atom
+            // one TMA box per new token (its g rows) and 64-column slab; g divides the
+            // warp's kRpq rows (32, or 16 in a split tile) and the row tile (gs) starts
+            // on a token, so a token's rows belong to this warp and its box starts on an
+            // atom
             fence_proxy_async_smem();  // the staged rows, for the async proxy
             __syncwarp();
             if (lane == 0) {
@@ -895,12 +935,16 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
                     tma_store_2d(&tmo, qbuf + sl * K::kSlab + (i * p.g) * 128, sl * 64,
                                  (cur.s * p.q_len + rt0 / p.g + i) * p.Hq + (cur.h / nsg) * p.g);
               } else {
-                const int i0 = quarter * 32 / p.g, i1 = min(p.q_len, (quarter * 32 + 32) / p.g);
+                // rows quarter * kRpq .. + kRpq - 1, staged from A row quarter * 32 on
+                const int i0 = quarter * kRpq / p.g,
+                          i1 = min(p.q_len, (quarter * kRpq + kRpq) / p.g);
                 for (int i = i0; i < i1; ++i)
 #pragma unroll
                   for (int sl = 0; sl < K::kSlabs; ++sl)
-                    tma_store_2d(&tmo, qbuf + sl * K::kSlab + (i * p.g) * 128, sl * 64,
-                                 (cur.s * p.q_len + i) * p.Hq + cur.h * p.g);
+                    tma_store_2d(&tmo,
+                                 qbuf + sl * K::kSlab +
+                                     (quarter * (32 - kRpq) + i * p.g) * 128,
+                                 sl * 64, (cur.s * p.q_len + i) * p.Hq + cur.h * p.g);
               }
               bulk_commit();
             }
@@ -918,7 +962,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
             } else {
               my_row = (long long)((size_t(cur.s) * p.q_len + (row_ok ? r / p.g : 0)) * p.Hq +
                                    cur.h * p.g + (row_ok ? r % p.g : 0));
-              nrows = min(32, R - quarter * 32);
+              nrows = min(kRpq, R - quarter * kRpq);
             }
 #pragma unroll 4
             for (int k2 = 0; k2 < kCh; ++k2) {
@@ -935,15 +979,22 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
           for (int c2 = 0; c2 < D; c2 += 32) {
             uint32_t o[32];
             tc::tmem_ld32(trow + K::kColO + c2, o);
-            if (!row_ok) continue;
-            float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * R + r) * D + c2);
+            if constexpr (CS == 2) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              dst[e / 4] = make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                       __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+              for (int e = 0; e < 32; ++e)
+                o[e] = __float_as_uint(__uint_as_float(o[e]) +
+                                       __uint_as_float(__shfl_xor_sync(0xffffffffu, o[e], kRpq)));
+            }
+            if (row_ok && part == 0) {
+              float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * R + r) * D + c2);
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                dst[e / 4] = make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                         __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+            }
           }
         }
-        if (row_ok && !whole)
+        if (row_ok && !whole && part == 0)
           reinterpret_cast<float2*>(p.part_ml)[slot * R + r] = make_float2(m_ref, l);
         if (!whole && p.fixup && quarter == 0 && lane == 0) {  // for the tail fixup
           volatile int* e = s_cut + 5 * int(slot & 1);
@@ -1021,11 +1072,11 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     tc_tail_fixup<D, kTiles>(p, s_prefix, s_rs, s_cut, gbase + K::kOffQ, K::kThreads);
 }
 
-template <int D, int BS, bool kTiles, int CODE>
+template <int D, int BS, bool kTiles, int CODE, int CS = 1>
 DecodeKernelInfo tc_info() {
   using K = TcDecode<D, BS, (CODE >= 0)>;
   DecodeKernelInfo info{};
-  info.fn = reinterpret_cast<const void*>(&paged_decode_tc_kernel<D, BS, kTiles, CODE>);
+  info.fn = reinterpret_cast<const void*>(&paged_decode_tc_kernel<D, BS, kTiles, CODE, CS>);
   info.warps = K::kThreads / 32;
   info.stages = 2;
   info.warp_smem = K::kFixedSmem;  // per CTA, plus 12 * (B + 1)
@@ -1037,13 +1088,21 @@ DecodeKernelInfo tc_info() {
   return info;
 }
 
+// row_tiles: several row tiles per KV head; split (one tile of at most 64 rows): two
+// threads per query row, each with half of a tile's columns.
 template <int CODE>
-bool select_tc_code(int D, int BS, bool row_tiles, DecodeKernelInfo* info) {
+bool select_tc_code(int D, int BS, bool row_tiles, bool split, DecodeKernelInfo* info) {
   if (row_tiles) {
     if (D == 128 && BS == 16) *info = tc_info<128, 16, true, CODE>();
     else if (D == 128 && BS == 32) *info = tc_info<128, 32, true, CODE>();
     else if (D == 64 && BS == 16) *info = tc_info<64, 16, true, CODE>();
     else if (D == 64 && BS == 32) *info = tc_info<64, 32, true, CODE>();
+    else return false;
+  } else if (split) {
+    if (D == 128 && BS == 16) *info = tc_info<128, 16, false, CODE, 2>();
+    else if (D == 128 && BS == 32) *info = tc_info<128, 32, false, CODE, 2>();
+    else if (D == 64 && BS == 16) *info = tc_info<64, 16, false, CODE, 2>();
+    else if (D == 64 && BS == 32) *info = tc_info<64, 32, false, CODE, 2>();
     else return false;
   } else {
     if (D == 128 && BS == 16) *info = tc_info<128, 16, false, CODE>();

@@ -4,8 +4,9 @@
 
 namespace pkv {
 
-bool select_decode_tc_e4m3(int D, int BS, bool row_tiles, DecodeKernelInfo* info) {
-  return select_tc_code<CODE_E4M3>(D, BS, row_tiles, info);
+bool select_decode_tc_e4m3(int D, int BS, bool row_tiles, bool split,
+                           DecodeKernelInfo* info) {
+  return select_tc_code<CODE_E4M3>(D, BS, row_tiles, split, info);
 }
 
 }  // namespace pkv

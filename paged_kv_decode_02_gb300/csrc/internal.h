@@ -153,12 +153,14 @@ bool select_decode_bf16_multi(int D, int BS, int nsg, DecodeKernelInfo* info);
 // One-byte KV code formats.
 enum : int { CODE_I8 = 0, CODE_E4M3 = 1, CODE_E5M2 = 2 };
 // The tcgen05 decode kernel for a KV dtype (pkv_kv_dtype); row_tiles: the rows of a KV
-// head run as several row tiles (more than 128 rows). The per-code tables live in
-// decode_tc_int8.cu, decode_tc_e4m3.cu and decode_tc_e5m2.cu.
-bool select_decode_tc(int D, int BS, bool row_tiles, int kvt, DecodeKernelInfo* info);
-bool select_decode_tc_int8(int D, int BS, bool row_tiles, DecodeKernelInfo* info);
-bool select_decode_tc_e4m3(int D, int BS, bool row_tiles, DecodeKernelInfo* info);
-bool select_decode_tc_e5m2(int D, int BS, bool row_tiles, DecodeKernelInfo* info);
+// head run as several row tiles (more than 128 rows); split: a single tile of at most
+// 64 rows, two softmax threads per row. The per-code tables live in decode_tc_int8.cu,
+// decode_tc_e4m3.cu and decode_tc_e5m2.cu.
+bool select_decode_tc(int D, int BS, bool row_tiles, bool split, int kvt,
+                      DecodeKernelInfo* info);
+bool select_decode_tc_int8(int D, int BS, bool row_tiles, bool split, DecodeKernelInfo* info);
+bool select_decode_tc_e4m3(int D, int BS, bool row_tiles, bool split, DecodeKernelInfo* info);
+bool select_decode_tc_e5m2(int D, int BS, bool row_tiles, bool split, DecodeKernelInfo* info);
 
 bool select_decode_int8(int D, int BS, int simt_heads, DecodeKernelInfo* info,
                         bool pair = false);

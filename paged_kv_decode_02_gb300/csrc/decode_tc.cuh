@@ -533,10 +533,9 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
       constexpr uint32_t kIdL =
           kQ8 ? tc::idesc_f16<128, 16, false>() : tc::idesc_bf16<128, 16, false>();
       const uint32_t ones = base + K::kOffOnes;
-      auto issue_s = [&](int i, int qb) -> bool {
+      // S_i = Q K_i^T into score buffer i & 1 (its inputs known to be ready)
+      auto mma_s = [&](int i, int qb) {
         const int st = i & 1;
-        if (!tc::wait_or_abort(kfull(st), uint32_t(i >> 1) & 1u, p.timeout_ns, abort_flag))
-          return false;
         tc::fence_after_sync();
         const uint32_t qa = base + K::kOffQ + qb * K::kTile;
         const uint32_t kb = base + K::kOffK + st * K::kTile;
@@ -548,18 +547,10 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         }
         tc::commit(sfull(st));
         tc::commit(kempty(st));
-        return true;
       };
-      // P.V of tile i; the first P.V of segment seg overwrites O, once the previous
-      // segment's epilogue has read it
-      auto issue_pv = [&](int i, bool seg_first, int sgi) -> bool {
+      // P.V of tile i; the first P.V of a segment overwrites O
+      auto mma_pv = [&](int i, bool seg_first) {
         const int st = i & 1;
-        if (seg_first && sgi > 0 &&
-            !tc::wait_or_abort(ofree, uint32_t(sgi - 1) & 1u, p.timeout_ns, abort_flag))
-          return false;
-        if (!tc::wait_or_abort(vfull(st), uint32_t(i >> 1) & 1u, p.timeout_ns, abort_flag) ||
-            !tc::wait_or_abort(pfull, uint32_t(i) & 1u, p.timeout_ns, abort_flag))
-          return false;
         tc::fence_after_sync();
         const uint32_t vb = base + K::kOffV + st * K::kTile;
 #pragma unroll
@@ -574,32 +565,67 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         }
         tc::commit(vempty(st));
         tc::commit(ofull);
-        return true;
       };
-      TileCursor cur;
-      tile_locate(cur, ra, s_prefix, B, U);
-      bool ok = true;
-      int seg = -1, pend = -1, pend_seg = 0;
-      bool pend_first = false;
-      for (int i = 0; i < cnt && ok; ++i) {
-        const bool first = i == 0 || cur.j == 0;
-        if (first) {
-          // a segment's last P.V goes before the next segment's scores: the softmax
-          // warps read O and load the next Q in between
-          if (pend >= 0) ok = issue_pv(pend, pend_first, pend_seg);
-          pend = -1;
-          ++seg;
-          if (ok) ok = tc::wait_or_abort(qfull(seg & 1), uint32_t(seg >> 1) & 1u, p.timeout_ns,
-                                         abort_flag);
+      // MMAs go out in the order their inputs become ready, not strictly tile by tile,
+      // so that scores never wait behind a P.V whose V tile is still in flight
+      // (measured on GB300: in strict order the softmax warps spent a third of their
+      // time waiting for scores, most of it behind late V tiles). With pdone softmax
+      // passes observed (pfull), np P.V and ns score MMAs issued:
+      //   S_ns  once K_ns has landed, its score buffer is free (pass ns - 2 observed:
+      //         pdone >= ns - 1) and, first in a segment, that segment's Q is ready;
+      //   PV_np once pass np is observed, V_np has landed and, first in a segment, the
+      //         previous segment's epilogue has read O (ofree).
+      // A pass i + 1 cannot complete before PV_i, hence before pass i is observed, and
+      // ns <= pdone + 1 <= np + 2, so no barrier can run two phases past the one polled.
+      TileCursor sc, pc;  // tiles of the next S and the next P.V
+      tile_locate(sc, ra, s_prefix, B, U);
+      pc = sc;
+      int ns = 0, np = 0, pdone = 0, sseg = -1, pseg = -1;
+      uint32_t idle = 0;
+      uint64_t t_idle = 0;
+      while (np < cnt) {
+        bool prog = false;
+        if (pdone < ns && mbar_test_wait(pfull, uint32_t(pdone) & 1u)) {
+          ++pdone;
+          prog = true;
         }
-        if (ok) ok = issue_s(i, seg & 1);
-        if (ok && pend >= 0) ok = issue_pv(pend, pend_first, pend_seg);
-        pend = i;
-        pend_first = first;
-        pend_seg = seg;
-        tile_next(cur, s_prefix, B, U);
+        if (np < pdone) {
+          const bool first = np == 0 || pc.j == 0;
+          const int sg = pseg + (first ? 1 : 0);
+          if ((!first || sg == 0 || mbar_test_wait(ofree, uint32_t(sg - 1) & 1u)) &&
+              mbar_test_wait(vfull(np & 1), uint32_t(np >> 1) & 1u)) {
+            mma_pv(np, first);
+            pseg = sg;
+            ++np;
+            tile_next(pc, s_prefix, B, U);
+            prog = true;
+          }
+        }
+        if (ns < cnt && pdone + 1 >= ns) {
+          const bool first = ns == 0 || sc.j == 0;
+          const int sg = sseg + (first ? 1 : 0);
+          if ((!first || mbar_test_wait(qfull(sg & 1), uint32_t(sg >> 1) & 1u)) &&
+              mbar_test_wait(kfull(ns & 1), uint32_t(ns >> 1) & 1u)) {
+            mma_s(ns, sg & 1);
+            sseg = sg;
+            ++ns;
+            tile_next(sc, s_prefix, B, U);
+            prog = true;
+          }
+        }
+        if (prog) {
+          idle = 0;
+        } else {  // bounded like every other wait: give up on a timeout or another abort
+          if (idle == 0) t_idle = global_timer_ns();
+          if ((++idle & 63u) == 0u) {
+            if (*abort_flag) break;
+            if (global_timer_ns() - t_idle > p.timeout_ns) {
+              *abort_flag = 1;
+              break;
+            }
+          }
+        }
       }
-      if (ok && pend >= 0) issue_pv(pend, pend_first, pend_seg);
       tc::commit(mdone);  // every MMA issued must have completed before TMEM is freed
       mbar_wait_bounded(mdone, 0u, p.timeout_ns);
     }

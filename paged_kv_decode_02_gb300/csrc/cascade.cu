@@ -244,10 +244,8 @@ __global__ void __launch_bounds__(PrefixTc<D, BS, (CODE >= 0)>::kThreads, 1)
       constexpr uint32_t kIdL =
           kQ8 ? tc::idesc_f16<128, 16, false>() : tc::idesc_bf16<128, 16, false>();
       const uint32_t ones = base + K::kOffOnes;
-      auto issue_s = [&](int j) -> bool {
+      auto mma_s = [&](int j) {
         const int st = j & 1;
-        if (!tc::wait_or_abort(kfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag))
-          return false;
         tc::fence_after_sync();
         const uint32_t kb = base + K::kOffK + st * K::kTile;
 #pragma unroll
@@ -259,13 +257,9 @@ __global__ void __launch_bounds__(PrefixTc<D, BS, (CODE >= 0)>::kThreads, 1)
         }
         tc::commit(sfull(st));
         tc::commit(kempty(st));
-        return true;
       };
-      auto issue_pv = [&](int j) -> bool {
+      auto mma_pv = [&](int j) {
         const int st = j & 1;
-        if (!tc::wait_or_abort(vfull(st), uint32_t(j >> 1) & 1u, pp.timeout_ns, abort_flag) ||
-            !tc::wait_or_abort(pfull, uint32_t(j) & 1u, pp.timeout_ns, abort_flag))
-          return false;
         tc::fence_after_sync();
         const uint32_t vb = base + K::kOffV + st * K::kTile;
 #pragma unroll
@@ -282,14 +276,44 @@ __global__ void __launch_bounds__(PrefixTc<D, BS, (CODE >= 0)>::kThreads, 1)
         }
         tc::commit(vempty(st));
         tc::commit(ofull);
-        return true;
       };
-      bool ok = true;
-      for (int j = 0; j < ntiles && ok; ++j) {
-        ok = issue_s(j);
-        if (ok && j >= 1) ok = issue_pv(j - 1);
+      // MMAs go out in the order their inputs become ready (as in the tcgen05 decode
+      // kernel): S_ns once K_ns has landed and softmax pass ns - 2 is observed (its score
+      // buffer free), PV_np once pass np is observed and V_np has landed. Pass i + 1
+      // cannot complete before PV_i, so no barrier runs two phases past the one polled.
+      int ns = 0, np = 0, pdone = 0;
+      uint32_t idle = 0;
+      uint64_t t_idle = 0;
+      while (np < ntiles) {
+        bool prog = false;
+        if (pdone < ns && mbar_test_wait(pfull, uint32_t(pdone) & 1u)) {
+          ++pdone;
+          prog = true;
+        }
+        if (np < pdone && mbar_test_wait(vfull(np & 1), uint32_t(np >> 1) & 1u)) {
+          mma_pv(np);
+          ++np;
+          prog = true;
+        }
+        if (ns < ntiles && pdone + 1 >= ns &&
+            mbar_test_wait(kfull(ns & 1), uint32_t(ns >> 1) & 1u)) {
+          mma_s(ns);
+          ++ns;
+          prog = true;
+        }
+        if (prog) {
+          idle = 0;
+        } else {  // bounded like every other wait: give up on a timeout or another abort
+          if (idle == 0) t_idle = global_timer_ns();
+          if ((++idle & 63u) == 0u) {
+            if (*abort_flag) break;
+            if (global_timer_ns() - t_idle > pp.timeout_ns) {
+              *abort_flag = 1;
+              break;
+            }
+          }
+        }
       }
-      if (ok && ntiles > 0) issue_pv(ntiles - 1);
       // every MMA issued must have completed before TMEM is freed
       tc::commit(mdone);
       mbar_wait_bounded(mdone, 0u, pp.timeout_ns);

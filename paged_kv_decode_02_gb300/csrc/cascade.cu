@@ -243,17 +243,21 @@ __global__ void __launch_bounds__(PrefixTc<D, BS, (CODE >= 0)>::kThreads, 1)
           kQ8 ? tc::idesc_f16<128, D, true>() : tc::idesc_bf16<128, D, true>();
       constexpr uint32_t kIdL =
           kQ8 ? tc::idesc_f16<128, 16, false>() : tc::idesc_bf16<128, 16, false>();
-      const uint32_t ones = base + K::kOffOnes;
+      // shared-memory descriptors built once and advanced by offset / 16 (the start
+      // address field, as in the tcgen05 decode kernel)
+      constexpr uint32_t kTileDesc = K::kTile >> 4, kSlabDesc = K::kSlab >> 4;
+      const uint64_t desc_q = tc::sdesc_sw128(base + K::kOffQ, 16, 1024);
+      const uint64_t desc_k = tc::sdesc_sw128(base + K::kOffK, 16, 1024);
+      const uint64_t desc_v = tc::sdesc_sw128(base + K::kOffV, K::kSlab, 1024);
+      const uint64_t desc_ones = tc::sdesc_sw128(base + K::kOffOnes, 16, 1024);
       auto mma_s = [&](int j) {
         const int st = j & 1;
         tc::fence_after_sync();
-        const uint32_t kb = base + K::kOffK + st * K::kTile;
+        const uint64_t kd = desc_k + st * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * K::kQSlab + (kk & 3) * 32;  // kQSlab == kSlab
-          tc::mma_bf16(tmem + K::kColS + st * K::kN,
-                       tc::sdesc_sw128(base + K::kOffQ + koff, 16, 1024),
-                       tc::sdesc_sw128(kb + koff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          const uint32_t ko = (kk >> 2) * kSlabDesc + (kk & 3) * 2;  // kQSlab == kSlab
+          tc::mma_bf16(tmem + K::kColS + st * K::kN, desc_q + ko, kd + ko, kIdS, kk > 0 ? 1u : 0u);
         }
         tc::commit(sfull(st));
         tc::commit(kempty(st));
@@ -261,18 +265,17 @@ __global__ void __launch_bounds__(PrefixTc<D, BS, (CODE >= 0)>::kThreads, 1)
       auto mma_pv = [&](int j) {
         const int st = j & 1;
         tc::fence_after_sync();
-        const uint32_t vb = base + K::kOffV + st * K::kTile;
+        const uint64_t vd = desc_v + st * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < K::kN / 16; ++kk) {
           // A = P in TMEM (8 columns per 16 tokens), B = V (MN-major: D contiguous,
           // tokens as rows)
-          tc::mma_bf16_tmem_a(tmem + K::kColO, tmem + K::kColP + kk * 8,
-                              tc::sdesc_sw128(vb + kk * 16 * 128, K::kSlab, 1024), kIdO,
+          tc::mma_bf16_tmem_a(tmem + K::kColO, tmem + K::kColP + kk * 8, vd + kk * 128, kIdO,
                               (j > 0 || kk > 0) ? 1u : 0u);
           // the row sums of the bf16 weights this P.V used (P times the ones tile)
           tc::mma_bf16_tmem_a(tmem + K::kColL, tmem + K::kColP + kk * 8,
-                              tc::sdesc_sw128(ones + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024),
-                              kIdL, (j > 0 || kk > 0) ? 1u : 0u);
+                              desc_ones + (kk >> 2) * 128 + (kk & 3) * 2, kIdL,
+                              (j > 0 || kk > 0) ? 1u : 0u);
         }
         tc::commit(vempty(st));
         tc::commit(ofull);

@@ -532,18 +532,26 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
           kQ8 ? tc::idesc_f16<128, D, true>() : tc::idesc_bf16<128, D, true>();
       constexpr uint32_t kIdL =
           kQ8 ? tc::idesc_f16<128, 16, false>() : tc::idesc_bf16<128, 16, false>();
-      const uint32_t ones = base + K::kOffOnes;
+      // Shared-memory descriptors, built once: the start address sits in the low 14 bits
+      // (address >> 4, every operand below 256 KiB), so the descriptor of base + off is
+      // the base's descriptor + off / 16. Measured on GB300, a thread that builds the
+      // descriptors before each MMA issues one every ~125-165 cycles, while the tensor
+      // cores finish an M = 128, N = 128, K = 16 step every 64 cycles.
+      constexpr uint32_t kTileDesc = K::kTile >> 4;
+      const uint64_t desc_q = tc::sdesc_sw128(base + K::kOffQ, 16, 1024);
+      const uint64_t desc_k = tc::sdesc_sw128(base + K::kOffK, 16, 1024);
+      const uint64_t desc_v = tc::sdesc_sw128(base + K::kOffV, K::kSlab, 1024);
+      const uint64_t desc_ones = tc::sdesc_sw128(base + K::kOffOnes, 16, 1024);
       // S_i = Q K_i^T into score buffer i & 1 (its inputs known to be ready)
       auto mma_s = [&](int i, int qb) {
         const int st = i & 1;
         tc::fence_after_sync();
-        const uint32_t qa = base + K::kOffQ + qb * K::kTile;
-        const uint32_t kb = base + K::kOffK + st * K::kTile;
+        const uint64_t qd = desc_q + qb * kTileDesc, kd = desc_k + st * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * K::kSlab + (kk & 3) * 32;
-          tc::mma_bf16(tmem + K::kColS + st * K::kN, tc::sdesc_sw128(qa + koff, 16, 1024),
-                       tc::sdesc_sw128(kb + koff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+          constexpr uint32_t kSlabDesc = K::kSlab >> 4;
+          const uint32_t ko = (kk >> 2) * kSlabDesc + (kk & 3) * 2;  // (koff) / 16
+          tc::mma_bf16(tmem + K::kColS + st * K::kN, qd + ko, kd + ko, kIdS, kk > 0 ? 1u : 0u);
         }
         tc::commit(sfull(st));
         tc::commit(kempty(st));
@@ -552,16 +560,15 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
       auto mma_pv = [&](int i, bool seg_first) {
         const int st = i & 1;
         tc::fence_after_sync();
-        const uint32_t vb = base + K::kOffV + st * K::kTile;
+        const uint64_t vd = desc_v + st * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < K::kN / 16; ++kk) {
-          tc::mma_bf16_tmem_a(tmem + K::kColO, tmem + K::kColP + kk * 8,
-                              tc::sdesc_sw128(vb + kk * 16 * 128, K::kSlab, 1024), kIdO,
+          tc::mma_bf16_tmem_a(tmem + K::kColO, tmem + K::kColP + kk * 8, vd + kk * 128, kIdO,
                               (!seg_first || kk > 0) ? 1u : 0u);
           // the row sums of the bf16 weights this P.V used, next to O (same rescaling)
           tc::mma_bf16_tmem_a(tmem + K::kColL, tmem + K::kColP + kk * 8,
-                              tc::sdesc_sw128(ones + (kk >> 2) * 2048 + (kk & 3) * 32, 16, 1024),
-                              kIdL, (!seg_first || kk > 0) ? 1u : 0u);
+                              desc_ones + (kk >> 2) * 128 + (kk & 3) * 2, kIdL,
+                              (!seg_first || kk > 0) ? 1u : 0u);
         }
         tc::commit(vempty(st));
         tc::commit(ofull);

@@ -120,6 +120,31 @@ def test_multi_long_context_split_many_ways(pk, Hq, Hkv, n):
     assert _err(out, oracle_outputs_multi(w)) <= DECODE_ATOL
 
 
+@pytest.mark.parametrize("Hq,Hkv,n", [(16, 2, 6), (16, 2, 16), (32, 2, 4)],
+                         ids=["48rows-split", "128rows", "64rows-split"])
+def test_tc_scores_growing_across_tiles(pk, Hq, Hkv, n):
+    """Keys scaled by 1, 5, 9, ... in successive 128-token tiles of every sequence: each
+    tile's maximum score exceeds the previous tiles' by far more than 2^8, so the tcgen05
+    kernel rescales O and the row sums between tiles (with split rows when a KV head has
+    at most 64 rows, and across the MMAs it issues as their inputs become ready). V is
+    scaled by 1/4 (exact in bf16) to keep the peaked outputs in the range the bf16
+    tolerance is set for."""
+    lengths = [700, 1000, 390, 129]
+    w = make_workload("spec-70b", device=DEV, num_q_heads=Hq, num_kv_heads=Hkv, q_len=n,
+                      lengths=lengths, seed=41)
+    kc = w.k_cache.clone()
+    bs = w.block_size
+    for s_, L in enumerate(lengths):
+        for j in range((L + bs - 1) // bs):
+            phys = int(w.block_tables[s_, j])
+            kc[phys] = (kc[phys].float() * (1 + 4 * (j * bs // 128))).to(torch.bfloat16)
+    w.k_cache = kc
+    w.v_cache = w.v_cache * 0.25
+    out = _run(pk, w)
+    torch.cuda.synchronize()
+    assert _err(out, oracle_outputs_multi(w)) <= DECODE_ATOL
+
+
 def test_multi_single_token_matches_decode(pk):
     w = make_workload("70b-gqa", device=DEV, num_seqs=6, seed=15)
     a = pk.paged_decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,

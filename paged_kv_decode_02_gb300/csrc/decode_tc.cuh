@@ -74,7 +74,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-template <int D, int BS, bool Q8 = false>
+template <int D, int BS, bool Q8 = false, bool PAIR = false>
 struct TcDecode {
   static constexpr int kM = 128;               // query rows per MMA (rows of a KV head, padded)
   static constexpr int kN = 128;               // tokens per tile
@@ -95,11 +95,15 @@ struct TcDecode {
   static constexpr int kCodeOff = kTile - kCodeTile;
   static constexpr int kScaleBytes = kN * 4;
   static constexpr int kOffScales = kOffOnes + 4096;
-  static constexpr int kOffBar = kOffScales + (Q8 ? 6 * kScaleBytes : 0);
+  // paired softmax warps (bf16 caches, so no scales): the halves of each row's tile
+  // maximum, [2 tiles][2 halves][128 rows] fp32
+  static constexpr int kOffXmax = kOffScales;
+  static constexpr int kOffBar = kOffScales + (Q8 ? 6 * kScaleBytes : PAIR ? 2048 : 0);
   // mbarriers: kfull[2] kempty[2] vfull[2] vempty[2] sfull[2] pfull ofull mdone qfull[2] ofree
   // (+ one-byte caches: kstage[2] vstage[2], the copies of the codes; kscale[4], the K
-  // scales of slot i % 4 ready for the softmax)
-  static constexpr int kNumBars = Q8 ? 24 : 16;
+  // scales of slot i % 4 ready for the softmax; paired softmax warps: xmax[4], both
+  // halves of a lane quarter's tile maxima written)
+  static constexpr int kNumBars = Q8 ? 24 : PAIR ? 20 : 16;
   static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   // [2] cut segments of this CTA (first, last) for the tail fixup: s, h, n, tiles, state
@@ -109,8 +113,10 @@ struct TcDecode {
   static constexpr int kOffTables = kOffCut + 48;
   // + 8 * (grid + 1) + 12 * (B + 1) at run time
   static constexpr int kFixedSmem = kOffTables + 1024;
-  // warps: 0 K copies, 1 MMA, 2..5 softmax, 6 V copies (+ 7..10 converters)
-  static constexpr int kThreads = Q8 ? 352 : 224;
+  // warps: 0 K copies, 1 MMA, 2..5 softmax, 6 V copies (+ 7..10 converters, or the
+  // second softmax warp of each lane quarter)
+  static constexpr int kThreads = (Q8 || PAIR) ? 352 : 224;
+  static constexpr int kSoftThreads = PAIR ? 256 : 128;
   static constexpr uint32_t kTmemCols = 512;
   // S x2, O, P (bf16 pairs), l (row sums of P, fp32; 16 columns written by its MMA)
   static constexpr int kColS = 0, kColO = 2 * kN, kColP = 2 * kN + 128, kColL = kColP + kN / 2;
@@ -118,6 +124,7 @@ struct TcDecode {
   static_assert(kOffOnes % 1024 == 0, "swizzle atom alignment");
   static_assert(kN % BS == 0 && D % 64 == 0 && kSlab == kM * 128, "tile shape");
   static_assert(kOffTables % 16 == 0 && kOffCut % 16 == 0, "table alignment");
+  static_assert(!(Q8 && PAIR) && (!PAIR || D == 128), "paired softmax: bf16, D = 128");
 };
 
 // Position in the flat (sequence, unit, tile) order; a unit is (KV head, row tile).
@@ -182,22 +189,27 @@ __device__ __forceinline__ long long tc_tiles_before(long long x, const int* pre
 // segments of the CTAs whose non-empty ranges start inside the head. A counter word
 // holds a launch tag (launch_tag: a 40-bit hash of the grid's launch number) over a
 // 24-bit tile count: a word with another tag counts as zero, so the workspace needs no clearing,
-// and the completing CTA resets it. Writers fence their records before the counter
-// update, the completing CTA fences after it and reads the records through L2.
+// and the completing CTA resets it. Writers order their records before the counter
+// update (a barrier, then a fence by the counting thread), the completing thread fences
+// after it and, past a barrier, every thread reads the records through L2.
 template <int D, bool kTiles>
 __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* s_prefix,
                                               const long long* s_rs, volatile int* cut,
                                               uint8_t* scratch, int nthreads) {
   const int tid = threadIdx.x, C = gridDim.x, R = p.gs, U = p.HU;
   if (!(cut[4] | cut[9])) return;  // no cut segment (uniform: shared memory after a barrier)
-  __threadfence();                 // this thread's records, device-wide
-  __syncthreads();
+  __syncthreads();                 // every thread's records are written
   if (tid < 2 && cut[5 * tid + 4]) {
+    // release: the fence of the counting thread orders the records the barrier ordered
+    // before it ahead of its counter update (one thread waits, not every thread)
+    __threadfence();
     volatile int* e = cut + 5 * tid;
     const int s = e[0], h = e[1], n = e[2], mine = e[3];
     const unsigned long long tag = launch_tag();
     unsigned long long* ctr = p.fix_ctr + size_t(s) * U + h;
-    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    // first guess: every other part already counted, the usual state for the CTA that
+    // completes the head (a wrong guess costs one more round, as reading it would)
+    unsigned long long cur = (tag << 24) | unsigned(n - mine);
     int last = 0;
     for (;;) {
       const unsigned long long base = (cur >> 24) == tag ? (cur & 0xffffffull) : 0ull;
@@ -209,7 +221,10 @@ __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* 
       }
       cur = seen;
     }
-    if (last) atomicExch(ctr, 0ull);
+    if (last) {
+      __threadfence();  // acquire: the other parts' records, for every thread after the barrier
+      atomicExch(ctr, 0ull);
+    }
     e[4] = last ? 2 : 0;
   }
   __syncthreads();
@@ -222,7 +237,6 @@ __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* 
   __nv_bfloat16* outb = reinterpret_cast<__nv_bfloat16*>(p.out);
   for (int ei = 0; ei < 2; ++ei) {
     if (cut[5 * ei + 4] != 2) continue;
-    __threadfence();
     const int s = cut[5 * ei], h = cut[5 * ei + 1], n = cut[5 * ei + 2];
     if (tid == 0) {  // the parts: slots of the CTAs whose ranges hold tiles [u0, u1)
       const long long u0 = (long long)U * s_prefix[s] + (long long)h * n, u1 = u0 + n;
@@ -325,13 +339,13 @@ __device__ __forceinline__ void tc_tail_fixup(const DecodeParams& p, const int* 
 // instantiation keeps its own index arithmetic: measured on GB300, the general form
 // made the one-tile calls 17 % slower (spec-70b 102.4 -> 120.1 us) although it computes
 // the same values. CODE: -1 for bf16 caches, else the one-byte code format.
-template <int D, int BS, bool kTiles, int CODE = -1, int CS = 1>
-__global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
+template <int D, int BS, bool kTiles, int CODE = -1, int CS = 1, bool PAIR = false>
+__global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0), PAIR>::kThreads, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                            const __grid_constant__ CUtensorMap tmv,
                            const __grid_constant__ CUtensorMap tmo, const DecodeParams p) {
   constexpr bool kQ8 = CODE >= 0;
-  using K = TcDecode<D, BS, kQ8>;
+  using K = TcDecode<D, BS, kQ8, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -364,19 +378,23 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     return base + K::kOffScales + uint32_t(is_k ? (i & 3) : 4 + (i & 1)) * K::kScaleBytes;
   };
   auto kscale = [&](int i) { return bar(20 + (i & 3)); };
+  // paired softmax: both warps of lane quarter q have written their tile maxima
+  auto xmax = [&](int q) { return bar(16 + q); };
   const uint32_t tmem_slot = base + K::kOffTmemSlot;
 
   pdl_wait_prior_grid();
   if (tid == 0) {
     for (int i = 0; i < 10; ++i) mbar_init(bar(i), 1);
-    mbar_init(pfull, 4 * 32);
+    mbar_init(pfull, K::kSoftThreads);
     mbar_init(ofull, 1);
     mbar_init(mdone, 1);
-    mbar_init(qfull(0), 4 * 32);
-    mbar_init(qfull(1), 4 * 32);
-    mbar_init(ofree, 4 * 32);
+    mbar_init(qfull(0), K::kSoftThreads);
+    mbar_init(qfull(1), K::kSoftThreads);
+    mbar_init(ofree, K::kSoftThreads);
     if constexpr (kQ8)
       for (int i = 16; i < 24; ++i) mbar_init(bar(i), 1);
+    if constexpr (PAIR)
+      for (int q = 0; q < 4; ++q) mbar_init(xmax(q), 64);
     *abort_flag = 0;
     s_cut[4] = s_cut[9] = 0;
     fence_mbar_init();
@@ -637,17 +655,27 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
       mbar_wait_bounded(mdone, 0u, p.timeout_ns);
     }
     __syncwarp();
-  } else if (cnt > 0 && warp >= 2 && warp <= 5) {
+  } else if (cnt > 0 && ((warp >= 2 && warp <= 5) || (PAIR && warp >= 7))) {
     // ---------------- softmax warps: one query row per CS threads ----------------
     // A warp reaches only its own quarter of the TMEM lanes, and the exponentials of a
     // lane quarter run on one SM sub-partition. With CS = 2 (at most 64 rows) each
     // quarter holds 16 rows, each twice (A rows 32q + j and 32q + 16 + j carry the same
     // Q row): the two threads of a row take half of the tile's columns each, their P rows
     // are zero outside their half and their O and l rows add up to the row's.
+    // Paired (PAIR, bf16 caches, D = 128): warps 7..10 reach the same lane quarters as
+    // 2..5, and the two warps of a quarter take half of each row's columns, half of its
+    // O columns and half of its Q and output chunks; they share the row maximum of each
+    // tile through shared memory (one mbarrier per quarter), so both weight their half
+    // against the same reference.
     static_assert(CS == 1 || (CS == 2 && !kTiles), "split rows: one row tile only");
-    constexpr int kRpq = 32 / CS;       // query rows per lane quarter
-    constexpr int kNc = K::kN / CS;     // tile columns per thread
+    static_assert(!PAIR || CS == 1, "paired warps: one thread per row");
+    constexpr int kRpq = 32 / CS;                      // query rows per lane quarter
+    constexpr int kNc = K::kN / CS / (PAIR ? 2 : 1);   // tile columns per thread
+    constexpr int kOc = PAIR ? D / 2 : D;              // O columns of the row per thread
     const int quarter = warp & 3;  // warps 2, 3, 4, 5 own TMEM lanes 64.., 96.., 0.., 32..
+                                   // (warps 7, 8, 9, 10: 96.., 0.., 32.., 64..)
+    const int hp = PAIR && warp >= 7 ? 1 : 0;  // which half of the row (paired warps)
+    const int sidx = warp >= 7 ? 128 + (warp - 7) * 32 + lane : tid - 64;  // 0.. softmax threads
     const int part = CS == 1 ? 0 : lane / kRpq;  // which kNc columns of the row it takes
     const int r = quarter * kRpq + lane % kRpq;  // query row of the unit
     const int ar = quarter * 32 + lane;          // A row / TMEM lane of this thread
@@ -690,10 +718,13 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
                (ex ? r % p.g : 0);
       }
       const uint32_t qa = base + K::kOffQ + qb * K::kTile;
+      constexpr int kQc = PAIR ? kChunks / 2 : kChunks;  // chunks of the row it copies
 #pragma unroll
-      for (int cc = 0; cc < kChunks; ++cc)
+      for (int c1 = 0; c1 < kQc; ++c1) {
+        const int cc = hp * kQc + c1;
         cp_async16(qa + (cc >> 3) * K::kSlab + ar * 128 + (((cc & 7) ^ (ar & 7)) << 4),
                    q + qrow * kChunks + cc, ex ? 16u : 0u);
+      }
       cp_async_commit();
     };
     auto q_ready = [&](int qb) {
@@ -705,7 +736,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     // output rows that are never stored
     const bool warp_idle = quarter * kRpq >= R;
     // rows of a head's last block past its context may hold anything (even NaN): the
-    // four softmax warps zero them in the V tile before P.V reads it (weights there are 0)
+    // softmax warps zero them in the V tile before P.V reads it (weights there are 0)
     auto zero_v_tail = [&](int i, int L, int t0) -> bool {
       const int zr0 = L - t0, zr1 = min(K::kN, ((L + BS - 1) / BS) * BS - t0);
       if (zr0 >= zr1) return true;
@@ -713,7 +744,7 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
                                                      p.timeout_ns, abort_flag)))
         return false;
       const uint32_t vb = base + K::kOffV + (i & 1) * K::kTile;
-      for (int idx = tid - 64; idx < (zr1 - zr0) * (D / 8); idx += 128) {
+      for (int idx = sidx; idx < (zr1 - zr0) * (D / 8); idx += K::kSoftThreads) {
         const int rr = zr0 + idx / (D / 8), cc = idx % (D / 8);
         tc::sts128(vb + (cc >> 3) * K::kSlab + rr * 128 + (((cc & 7) ^ (rr & 7)) << 4),
                    make_uint4(0u, 0u, 0u, 0u));
@@ -782,9 +813,11 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
         continue;
       }
       // this thread's columns c0 .. c0 + kNc - 1 of the tile's scores
-      const int c0 = part * kNc;
+      const int c0 = (PAIR ? hp : part) * kNc;
       uint32_t s[kNc];
-      if constexpr (CS == 1) {
+      if constexpr (PAIR) {
+        tc::tmem_ld64(trow + K::kColS + st * K::kN + c0, s);
+      } else if constexpr (CS == 1) {
         tc::tmem_ld128(trow + K::kColS + st * K::kN, s);
       } else {
         uint32_t sa[K::kN];
@@ -831,6 +864,17 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
       float mt = asl * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
                              fmaxf(mx[6], mx[7]));
       if constexpr (CS == 2) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, kRpq));
+      if constexpr (PAIR) {  // the partner warp's half: [tile % 2][half][row] fp32
+        const uint32_t xa = base + K::kOffXmax + uint32_t(i & 1) * 1024 + uint32_t(ar) * 4;
+        tc::sts32(xa + hp * 512, __float_as_uint(mt));
+        mbar_arrive(xmax(quarter));
+        if (!__all_sync(0xffffffffu, tc::wait_or_abort(xmax(quarter), uint32_t(i) & 1u,
+                                                       p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        mt = fmaxf(mt, __uint_as_float(lds32(xa + (hp ^ 1) * 512)));
+      }
       float alpha = 1.f;
       bool rescale = false;
       if (vis > 0 && mt > m_ref + 8.f) {
@@ -874,25 +918,32 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
       tc::fence_after_sync();
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int c2 = 0; c2 < D; c2 += 32) {
+        for (int c1 = 0; c1 < kOc; c1 += 32) {
+          const int c2 = hp * kOc + c1;
           uint32_t o[32];
           tc::tmem_ld32(trow + K::kColO + c2, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tc::tmem_st32(trow + K::kColO + c2, o);
         }
-        tc::tmem_st1(trow + K::kColL,
-                     __float_as_uint(__uint_as_float(tc::tmem_ld1(trow + K::kColL)) * alpha));
+        if (hp == 0)
+          tc::tmem_st1(trow + K::kColL,
+                       __float_as_uint(__uint_as_float(tc::tmem_ld1(trow + K::kColL)) * alpha));
       }
-      // P (column pairs); with CS = 2 each thread writes its half and zeros in the other
+      // P (column pairs); with CS = 2 each thread writes its half and zeros in the other,
+      // a paired warp only its half
+      if constexpr (PAIR) {
+        tc::tmem_st32(trow + K::kColP + hp * (kNc / 2), pk);
+      } else {
 #pragma unroll
-      for (int c2 = 0; c2 < K::kN / 2; c2 += 32) {
-        uint32_t w[32];
-        constexpr int kHalf = kNc / 2;  // column pairs per thread
+        for (int c2 = 0; c2 < K::kN / 2; c2 += 32) {
+          uint32_t w[32];
+          constexpr int kHalf = kNc / 2;  // column pairs per thread
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          w[e] = (CS == 1 || part == c2 / kHalf) ? pk[c2 % kHalf + e] : 0u;
-        tc::tmem_st32(trow + K::kColP + c2, w);
+          for (int e = 0; e < 32; ++e)
+            w[e] = (CS == 1 || part == c2 / kHalf) ? pk[c2 % kHalf + e] : 0u;
+          tc::tmem_st32(trow + K::kColP + c2, w);
+        }
       }
       tc::fence_before_sync();
       mbar_arrive(pfull);
@@ -927,7 +978,8 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
           };
           fence_proxy_async_smem();  // the MMAs' reads of the buffer before these writes
 #pragma unroll
-          for (int c2 = 0; c2 < D; c2 += 32) {
+          for (int c1 = 0; c1 < kOc; c1 += 32) {
+            const int c2 = hp * kOc + c1;
             uint32_t o[32];
             tc::tmem_ld32(trow + K::kColO + c2, o);
             if constexpr (CS == 2) {
@@ -951,10 +1003,10 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
             }
           }
           if (p.tma_out) {
-            // one TMA box per new token (its g rows) and 64-column slab; g divides the
-            // warp's kRpq rows (32, or 16 in a split tile) and the row tile (gs) starts
-            // on a token, so a token's rows belong to this warp and its box starts on an
-            // atom
+            // one TMA box per new token (its g rows) and 64-column slab (a paired warp:
+            // its half's slab); g divides the warp's kRpq rows (32, or 16 in a split tile)
+            // and the row tile (gs) starts on a token, so a token's rows belong to this
+            // warp and its box starts on an atom
             fence_proxy_async_smem();  // the staged rows, for the async proxy
             __syncwarp();
             if (lane == 0) {
@@ -964,20 +1016,24 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
                 const int i0 = quarter * 32 / p.g, i1 = min(nloc, quarter * 32 + 32) / p.g;
                 for (int i = i0; i < i1; ++i)
 #pragma unroll
-                  for (int sl = 0; sl < K::kSlabs; ++sl)
+                  for (int s1 = 0; s1 < (PAIR ? 1 : K::kSlabs); ++s1) {
+                    const int sl = PAIR ? hp : s1;
                     tma_store_2d(&tmo, qbuf + sl * K::kSlab + (i * p.g) * 128, sl * 64,
                                  (cur.s * p.q_len + rt0 / p.g + i) * p.Hq + (cur.h / nsg) * p.g);
+                  }
               } else {
                 // rows quarter * kRpq .. + kRpq - 1, staged from A row quarter * 32 on
                 const int i0 = quarter * kRpq / p.g,
                           i1 = min(p.q_len, (quarter * kRpq + kRpq) / p.g);
                 for (int i = i0; i < i1; ++i)
 #pragma unroll
-                  for (int sl = 0; sl < K::kSlabs; ++sl)
+                  for (int s1 = 0; s1 < (PAIR ? 1 : K::kSlabs); ++s1) {
+                    const int sl = PAIR ? hp : s1;
                     tma_store_2d(&tmo,
                                  qbuf + sl * K::kSlab +
                                      (quarter * (32 - kRpq) + i * p.g) * 128,
                                  sl * 64, (cur.s * p.q_len + i) * p.Hq + cur.h * p.g);
+                  }
               }
               bulk_commit();
             }
@@ -997,9 +1053,10 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
                                    cur.h * p.g + (row_ok ? r % p.g : 0));
               nrows = min(kRpq, R - quarter * kRpq);
             }
+            constexpr int kChw = PAIR ? kCh / 2 : kCh;  // chunks of a row this warp stores
 #pragma unroll 4
-            for (int k2 = 0; k2 < kCh; ++k2) {
-              const int idx = k2 * 32 + lane, rl = idx / kCh, ch = idx % kCh;
+            for (int k2 = 0; k2 < kChw; ++k2) {
+              const int idx = k2 * 32 + lane, rl = idx / kChw, ch = hp * kChw + idx % kChw;
               const long long orow2 = __shfl_sync(0xffffffffu, my_row, rl);
               if (rl < nrows)
                 reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
@@ -1009,7 +1066,8 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
           }
         } else {
 #pragma unroll
-          for (int c2 = 0; c2 < D; c2 += 32) {
+          for (int c1 = 0; c1 < kOc; c1 += 32) {
+            const int c2 = hp * kOc + c1;
             uint32_t o[32];
             tc::tmem_ld32(trow + K::kColO + c2, o);
             if constexpr (CS == 2) {
@@ -1027,9 +1085,9 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
             }
           }
         }
-        if (row_ok && !whole && part == 0)
+        if (row_ok && !whole && part == 0 && hp == 0)
           reinterpret_cast<float2*>(p.part_ml)[slot * R + r] = make_float2(m_ref, l);
-        if (!whole && p.fixup && quarter == 0 && lane == 0) {  // for the tail fixup
+        if (!whole && p.fixup && quarter == 0 && lane == 0 && hp == 0) {  // tail fixup
           volatile int* e = s_cut + 5 * int(slot & 1);
           e[0] = cur.s;
           e[1] = cur.h;
@@ -1105,11 +1163,12 @@ __global__ void __launch_bounds__(TcDecode<D, BS, (CODE >= 0)>::kThreads, 1)
     tc_tail_fixup<D, kTiles>(p, s_prefix, s_rs, s_cut, gbase + K::kOffQ, K::kThreads);
 }
 
-template <int D, int BS, bool kTiles, int CODE, int CS = 1>
+template <int D, int BS, bool kTiles, int CODE, int CS = 1, bool PAIR = false>
 DecodeKernelInfo tc_info() {
-  using K = TcDecode<D, BS, (CODE >= 0)>;
+  using K = TcDecode<D, BS, (CODE >= 0), PAIR>;
   DecodeKernelInfo info{};
-  info.fn = reinterpret_cast<const void*>(&paged_decode_tc_kernel<D, BS, kTiles, CODE, CS>);
+  info.fn =
+      reinterpret_cast<const void*>(&paged_decode_tc_kernel<D, BS, kTiles, CODE, CS, PAIR>);
   info.warps = K::kThreads / 32;
   info.stages = 2;
   info.warp_smem = K::kFixedSmem;  // per CTA, plus 12 * (B + 1)
@@ -1122,12 +1181,14 @@ DecodeKernelInfo tc_info() {
 }
 
 // row_tiles: several row tiles per KV head; split (one tile of at most 64 rows): two
-// threads per query row, each with half of a tile's columns.
+// threads per query row, each with half of a tile's columns. Units of more than 64 rows
+// over bf16 caches with D = 128 take two softmax warps per lane quarter (paired).
 template <int CODE>
 bool select_tc_code(int D, int BS, bool row_tiles, bool split, DecodeKernelInfo* info) {
+  constexpr bool kPair = CODE < 0;
   if (row_tiles) {
-    if (D == 128 && BS == 16) *info = tc_info<128, 16, true, CODE>();
-    else if (D == 128 && BS == 32) *info = tc_info<128, 32, true, CODE>();
+    if (D == 128 && BS == 16) *info = tc_info<128, 16, true, CODE, 1, kPair>();
+    else if (D == 128 && BS == 32) *info = tc_info<128, 32, true, CODE, 1, kPair>();
     else if (D == 64 && BS == 16) *info = tc_info<64, 16, true, CODE>();
     else if (D == 64 && BS == 32) *info = tc_info<64, 32, true, CODE>();
     else return false;
@@ -1138,8 +1199,8 @@ bool select_tc_code(int D, int BS, bool row_tiles, bool split, DecodeKernelInfo*
     else if (D == 64 && BS == 32) *info = tc_info<64, 32, false, CODE, 2>();
     else return false;
   } else {
-    if (D == 128 && BS == 16) *info = tc_info<128, 16, false, CODE>();
-    else if (D == 128 && BS == 32) *info = tc_info<128, 32, false, CODE>();
+    if (D == 128 && BS == 16) *info = tc_info<128, 16, false, CODE, 1, kPair>();
+    else if (D == 128 && BS == 32) *info = tc_info<128, 32, false, CODE, 1, kPair>();
     else if (D == 64 && BS == 16) *info = tc_info<64, 16, false, CODE>();
     else if (D == 64 && BS == 32) *info = tc_info<64, 32, false, CODE>();
     else return false;

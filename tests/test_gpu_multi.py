@@ -57,6 +57,10 @@ SHAPES = [
     # tcgen05 with groups whose rows do not form whole 8-row atoms (plain row stores)
     ("g12-q4", 24, 2, 128, 16, 4, [4, 60, 300, 129]),
     ("g4-q16-d64-bs32", 8, 2, 64, 32, 16, [16, 40, 500]),
+    # more than 64 rows over bf16 with D 128: two softmax warps per lane quarter, each
+    # storing its half of a row (plain row stores for g 6, TMA boxes of 32 rows for g 32)
+    ("g6-q16-pair", 12, 2, 128, 16, 16, [16, 40, 700, 129, 0]),
+    ("g32-q3-pair", 64, 2, 128, 16, 3, [3, 50, 400]),
 ]
 
 # chunks of chunked prefill: more than 128 rows per KV head, run as equal tcgen05 row

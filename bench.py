@@ -790,11 +790,16 @@ def capture(K, fn, dev):
 def run_e2e(args, w, pk, dev, out, ws, step_bytes, world, cascade_blocks=0):
     """Same step through the public API from pinned HOST buffers: per step, copy the
     step's inputs host->device (one copy of a packed buffer), append + decode, copy the
-    output device->host."""
+    output device->host. As a serving loop runs it: inputs and outputs double-buffered,
+    the host->device copy of step k + 1 and the device->host copy of step k - 1 on two
+    copy streams while step k computes; every step's own copies stay inside the timed
+    region (the last output's copy included)."""
     import torch
     stream = torch.cuda.current_stream(dev)
+    h2d_stream = torch.cuda.Stream(dev)
+    d2h_stream = torch.cuda.Stream(dev)
     # the step's inputs packed into one pinned host buffer (256-byte aligned regions) and
-    # moved by one copy per step into views of one device buffer
+    # moved by one copy per step into views of one of two device buffers
     names = ("q", "new_k", "new_v", "slot_mapping", "block_tables", "context_lens")
     srcs = {n: getattr(w, n).contiguous() for n in names}
     offs, total = {}, 0
@@ -802,49 +807,103 @@ def run_e2e(args, w, pk, dev, out, ws, step_bytes, world, cascade_blocks=0):
         offs[n] = total
         total += (srcs[n].numel() * srcs[n].element_size() + 255) // 256 * 256
     host_buf = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
-    dev_in = {}
+    dev_bufs = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dev_in = [{}, {}]
     for n in names:
         t = srcs[n]
         nb = t.numel() * t.element_size()
         host_buf[offs[n]:offs[n] + nb].view(t.dtype).copy_(t.reshape(-1).cpu())
-        dev_in[n] = dev_buf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
-    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        for b in range(2):
+            dev_in[b][n] = dev_bufs[b][offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+    outs = [out, torch.empty_like(out)]
+    host_outs = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
     h2d = total
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_outs[0].numel() * host_outs[0].element_size()
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in_ready", "in_free",
+                                                               "out_ready", "out_free")}
+    started = torch.cuda.Event()
 
-    def step():
-        dev_buf.copy_(host_buf, non_blocking=True)
-        api_append(pk, w, dev_in["new_k"], dev_in["new_v"], dev_in["slot_mapping"])
-        api_decode(pk, w, dev_in["q"], dev_in["block_tables"], dev_in["context_lens"], out, ws,
-                   cascade_blocks)
-        host_out.copy_(out, non_blocking=True)
+    def step(k, main):
+        b = k & 1
+        # inputs of step k into buffer b, once step k - 2 has read it
+        h2d_stream.wait_event(ev["in_free"][b])
+        with torch.cuda.stream(h2d_stream):
+            dev_bufs[b].copy_(host_buf, non_blocking=True)
+        ev["in_ready"][b].record(h2d_stream)
+        main.wait_event(ev["in_ready"][b])
+        main.wait_event(ev["out_free"][b])  # step k - 2's output has left buffer b
+        api_append(pk, w, dev_in[b]["new_k"], dev_in[b]["new_v"], dev_in[b]["slot_mapping"])
+        api_decode(pk, w, dev_in[b]["q"], dev_in[b]["block_tables"],
+                   dev_in[b]["context_lens"], outs[b], ws, cascade_blocks)
+        ev["in_free"][b].record(main)
+        ev["out_ready"][b].record(main)
+        # step k's output to the host while step k + 1 computes
+        d2h_stream.wait_event(ev["out_ready"][b])
+        with torch.cuda.stream(d2h_stream):
+            host_outs[b].copy_(outs[b], non_blocking=True)
+        ev["out_free"][b].record(d2h_stream)
+
+    def run(n):
+        """n steps on the current stream: no copy starts before the work queued ahead of
+        them, and the last output is on the host before anything queued after them"""
+        main = torch.cuda.current_stream(dev)
+        for b in range(2):  # nothing in flight at the start
+            ev["in_free"][b].record(main)
+            ev["out_free"][b].record(main)
+        started.record(main)
+        h2d_stream.wait_event(started)
+        d2h_stream.wait_event(started)
+        for k in range(n):
+            step(k, main)
+        for b in range(2):
+            main.wait_event(ev["out_free"][b])
 
     ref = out.clone()
-    for _ in range(3):
-        step()
+    run(3)
     torch.cuda.synchronize(dev)
     # the packed inputs are the device-resident step's inputs: the same result
-    if not torch.equal(host_out, ref.cpu()):
-        raise RuntimeError("end-to-end step disagrees with the device-resident step")
-    K = max(1, args.steps)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(K):
-        step()
-    b.record(stream)
+    for b in range(2):
+        if not torch.equal(host_outs[b], ref.cpu()):
+            raise RuntimeError("end-to-end step disagrees with the device-resident step")
+    # the steps replayed as one CUDA graph of S steps (the host issues one launch per S
+    # steps, as the device-timed line does); each replay still copies every step's
+    # inputs in and its output out
+    S = 16
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap):
+        run(S)
+    stream.wait_stream(cap)
+    host_outs[0].zero_()
+    host_outs[1].zero_()
+    graph.replay()
     torch.cuda.synchronize(dev)
-    est = a.elapsed_time(b) / K
-    n = int(min(5000, max(K, math.ceil(300.0 / max(est, 1e-3)))))   # >= 0.3 s of steps
+    for b in range(2):
+        if not torch.equal(host_outs[b], ref.cpu()):
+            raise RuntimeError("replayed end-to-end step disagrees with the device-resident step")
+    R = max(1, -(-max(1, args.steps) // S))
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(n):
-        step()
-    b.record(stream)
+    for _ in range(R):
+        graph.replay()
+    e.record(stream)
     torch.cuda.synchronize(dev)
-    ms = job_time_ms(a.elapsed_time(b) / n, world, dev)
+    est = a.elapsed_time(e) / (R * S)
+    R = int(min(5000, max(R, math.ceil(300.0 / max(est * S, 1e-3)))))   # >= 0.3 s of steps
+    a.record(stream)
+    for _ in range(R):
+        graph.replay()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = job_time_ms(a.elapsed_time(e) / (R * S), world, dev)
     return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-            "ms_per_step": round(ms, 5), "steps": n,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(ms, 5), "steps": R * S,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": f"inputs and outputs double-buffered: the host->device copy of step "
+                       f"k + 1 and the device->host copy of step k - 1 run on two copy "
+                       f"streams beside step k; replayed as CUDA graphs of {S} steps "
+                       f"({R} replays)"}
 
 
 def run_reference(args, rank):

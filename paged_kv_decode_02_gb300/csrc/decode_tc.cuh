@@ -23,7 +23,8 @@
 // 2c + 1 (the last). Without a status word the CTA that completes a cut unit folds its
 // records at its end (tc_tail_fixup); with one, the split-KV merge kernel validates
 // and folds.
-// Roles per CTA (224 threads), as in the cascade prefix kernel:
+// Roles per CTA (224 threads; 352 with the warps 7..10 below), as in the cascade
+// prefix kernel:
 //   warp 0 / warp 6: TMA copies of the K / V tiles into two-stage rings (one box per
 //                    16- or 32-token block and 64-column slab, lane b copies block b;
 //                    block ids are read one tile ahead);
@@ -39,6 +40,11 @@
 //                    the two threads of a row take half of each tile's columns, so the
 //                    exponentials spread over all four SM sub-partitions (measured on
 //                    GB300, spec-70b with 48 rows per head: 103.2 -> 97.2 us per call).
+//   warps 7..10:     bf16 caches, D = 128, more than 64 rows (PAIR): the second softmax
+//                    warp of each lane quarter, the two of a quarter taking half of each
+//                    row's columns and sharing its tile maximum (measured on GB300:
+//                    chunk-70b 341.5 -> 321.8 us, spec-70b-q16 105.5 -> 104.2 us per
+//                    call); one-byte caches: the converters below.
 // The softmax keeps a reference maximum per row that moves only when a tile's maximum
 // exceeds it by more than 8 (log2 units); O and l are then rescaled in TMEM before the
 // next P.V. Every wait is bounded: on a timeout the CTA sets a status bit, lets its
